@@ -1,0 +1,179 @@
+"""CPU oracle for block-sparse attention with a mean-pooled top-k selector.
+
+TEST INFRASTRUCTURE ONLY: imported by the tests, by the package smoke check
+and by the benchmark's CPU-baseline leg. The product path never imports it.
+
+The arithmetic lives in ``bsa_oracle.c`` (plain C, double precision for the
+attention, the fp32 rules of the selector spelled out there). This module
+compiles it with gcc and wraps it with ctypes and numpy.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import subprocess
+from typing import Optional, Sequence, Tuple
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "bsa_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "liboracle.so")
+_lib = None
+
+OK = 0
+ERR_ARG = 1
+ERR_NONFINITE = 5
+
+
+def build(force: bool = False) -> str:
+    """Compile liboracle.so (gcc, -O2, OpenMP, no FP contraction)."""
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp", "-ffp-contract=off",
+           "-fno-fast-math", "-o", tmp, _SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    if _lib is not None:
+        return _lib
+    lib = ctypes.CDLL(build())
+    P = ctypes.c_void_p
+    i64, i32, f32, f64 = ctypes.c_int64, ctypes.c_int, ctypes.c_float, ctypes.c_double
+    lib.bsa_oracle_block_mean.argtypes = [P, i64, i64, i32, i32, P]
+    lib.bsa_oracle_block_scores.argtypes = [P, P, i64, i32, i32, i32, P]
+    lib.bsa_oracle_topk_count.argtypes = [f32, i32]
+    lib.bsa_oracle_topk.argtypes = [P, i64, i32, i32, P]
+    lib.bsa_oracle_band_mask.argtypes = [i32, i32, i32, P, i32, P]
+    lib.bsa_oracle_cuboid_mask.argtypes = [i32, i32, i32, i32, P]
+    lib.bsa_oracle_mask_to_index.argtypes = [P, i64, i32, P, P, P]
+    lib.bsa_oracle_mask_to_index.restype = i64
+    lib.bsa_oracle_attention.argtypes = [P, P, P, i64, i64, i32, i32, P, f64, P, i64, P, P]
+    _lib = lib
+    return lib
+
+
+def _ptr(a: Optional[np.ndarray]):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+class OracleError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        super().__init__(f"{what}: oracle status {code}")
+        self.code = code
+
+
+def _check(code: int, what: str):
+    if code != OK:
+        raise OracleError(code, what)
+
+
+def block_mean(x: np.ndarray, bs: int) -> np.ndarray:
+    """Mean-pooled block representation: x [..., N, d] fp32 -> [..., N/bs, d] fp32."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    *lead, N, d = x.shape
+    heads = int(np.prod(lead)) if lead else 1
+    out = np.empty((*lead, N // bs, d), np.float32)
+    _check(_load().bsa_oracle_block_mean(_ptr(x), heads, N, d, bs, _ptr(out)), "block_mean")
+    return out
+
+
+def block_scores(qbar: np.ndarray, kbar: np.ndarray) -> np.ndarray:
+    """Scores [..., nQB, nKB] of pooled blocks (fmaf chain over channels)."""
+    qbar = np.ascontiguousarray(qbar, dtype=np.float32)
+    kbar = np.ascontiguousarray(kbar, dtype=np.float32)
+    *lead, nQB, d = qbar.shape
+    nKB = kbar.shape[-2]
+    heads = int(np.prod(lead)) if lead else 1
+    out = np.empty((*lead, nQB, nKB), np.float32)
+    _check(_load().bsa_oracle_block_scores(_ptr(qbar), _ptr(kbar), heads, nQB, nKB, d, _ptr(out)),
+           "block_scores")
+    return out
+
+
+def topk_count(density: float, nKB: int) -> int:
+    return int(_load().bsa_oracle_topk_count(float(density), int(nKB)))
+
+
+def topk_mask(scores: np.ndarray, k: int) -> np.ndarray:
+    """uint8 mask [..., nQB, nKB] of the k best blocks per row (ties -> lower index)."""
+    scores = np.ascontiguousarray(scores, dtype=np.float32)
+    *lead, nKB = scores.shape
+    rows = int(np.prod(lead)) if lead else 1
+    out = np.empty(scores.shape, np.uint8)
+    _check(_load().bsa_oracle_topk(_ptr(scores), rows, nKB, int(k), _ptr(out)), "topk")
+    return out
+
+
+def band_mask(nB: int, n_text: int, band: int, anchors: Sequence[int]) -> np.ndarray:
+    a = np.ascontiguousarray(np.array(list(anchors) or [0], dtype=np.int32))
+    out = np.empty((nB, nB), np.uint8)
+    _check(_load().bsa_oracle_band_mask(nB, n_text, band, _ptr(a), len(anchors), _ptr(out)),
+           "band_mask")
+    return out
+
+
+def cuboid_mask(n_text: int, grid: Tuple[int, int, int]) -> np.ndarray:
+    gt, gh, gw = grid
+    nB = n_text + gt * gh * gw
+    out = np.empty((nB, nB), np.uint8)
+    _check(_load().bsa_oracle_cuboid_mask(n_text, gt, gh, gw, _ptr(out)), "cuboid_mask")
+    return out
+
+
+def mask_to_index(mask: np.ndarray):
+    """(row_ptr int32 [R+1], col_idx int32 [nnz], bitmap uint32 [R, ceil(nKB/32)])."""
+    mask = np.ascontiguousarray(mask, dtype=np.uint8)
+    nKB = mask.shape[-1]
+    R = mask.size // nKB
+    W = (nKB + 31) // 32
+    row_ptr = np.empty(R + 1, np.int32)
+    col_idx = np.empty(max(int(mask.sum()), 1), np.int32)
+    bitmap = np.empty((R, W), np.uint32)
+    nnz = _load().bsa_oracle_mask_to_index(_ptr(mask), R, nKB, _ptr(row_ptr), _ptr(col_idx),
+                                           _ptr(bitmap))
+    if nnz < 0:
+        raise OracleError(ERR_ARG, "mask_to_index")
+    return row_ptr, col_idx[:nnz].copy(), bitmap
+
+
+def attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, mask: np.ndarray, bs: int,
+              scale: Optional[float] = None, rows: Optional[np.ndarray] = None):
+    """Masked attention in double for selected rows.
+
+    q, k, v: fp32 [..., N, d]; mask: uint8 [..., nQB, nKB] (same leading dims);
+    rows: int64 global row ids (flattened head * N + r); default all rows.
+    Returns (O float64 [n_rows, d], LSE float64 [n_rows]).
+    """
+    q = np.ascontiguousarray(q, dtype=np.float32)
+    k = np.ascontiguousarray(k, dtype=np.float32)
+    v = np.ascontiguousarray(v, dtype=np.float32)
+    mask = np.ascontiguousarray(mask, dtype=np.uint8)
+    *lead, N, d = q.shape
+    heads = int(np.prod(lead)) if lead else 1
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if rows is None:
+        rows = np.arange(heads * N, dtype=np.int64)
+    rows = np.ascontiguousarray(rows, dtype=np.int64)
+    O = np.empty((rows.size, d), np.float64)
+    L = np.empty(rows.size, np.float64)
+    _check(_load().bsa_oracle_attention(_ptr(q), _ptr(k), _ptr(v), heads, N, d, bs, _ptr(mask),
+                                        float(scale), _ptr(rows), rows.size, _ptr(O), _ptr(L)),
+           "attention")
+    return O, L
+
+
+def select_mask(q: np.ndarray, k: np.ndarray, bs: int, density: float) -> np.ndarray:
+    """Naive BSA selector end to end: pool, score, top-k -> uint8 mask [..., nQB, nKB]."""
+    qbar = block_mean(q, bs)
+    kbar = block_mean(k, bs)
+    s = block_scores(qbar, kbar)
+    return topk_mask(s, topk_count(density, s.shape[-1]))

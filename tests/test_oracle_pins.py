@@ -1,0 +1,350 @@
+"""Pins of the CPU oracle to things other than itself.
+
+Each oracle function is tied to closed forms, library routines, brute force on
+tiny inputs or hand-derived fixtures under tests/golden/, chosen so that a
+plausible slip (a dropped term, a wrong sign or index, a transposed operand, a
+different summation order, a lost tie-break) fails at least one test.
+"""
+import itertools
+import math
+
+import numpy as np
+import pytest
+import scipy.special
+
+import oracle
+from tests.conftest import read_golden
+
+RNG = np.random.default_rng(12345)
+
+
+def _rand(*shape):
+    return RNG.standard_normal(shape).astype(np.float32)
+
+
+# ---------------------------------------------------------------- attention
+
+
+def _dense_library(q, k, v, scale, allowed):
+    """softmax/logsumexp from scipy over an explicit token-level allow matrix."""
+    s = (q.astype(np.float64) @ k.astype(np.float64).T) * scale
+    s = np.where(allowed, s, -np.inf)
+    lse = scipy.special.logsumexp(s, axis=-1)
+    p = scipy.special.softmax(s, axis=-1)
+    return p @ v.astype(np.float64), lse
+
+
+def test_all_ones_mask_equals_dense_attention():
+    H, N, d, bs = 2, 96, 16, 32
+    q, k, v = _rand(H, N, d), _rand(H, N, d), _rand(H, N, d)
+    mask = np.ones((H, N // bs, N // bs), np.uint8)
+    O, L = oracle.attention(q, k, v, mask, bs)
+    for h in range(H):
+        Od, Ld = _dense_library(q[h], k[h], v[h], 1.0 / math.sqrt(d), np.ones((N, N), bool))
+        np.testing.assert_allclose(O[h * N:(h + 1) * N], Od, rtol=1e-11, atol=1e-12)
+        np.testing.assert_allclose(L[h * N:(h + 1) * N], Ld, rtol=1e-12, atol=1e-12)
+
+
+def test_random_mask_equals_library_on_token_mask():
+    H, N, d, bs = 3, 64, 8, 16
+    q, k, v = _rand(H, N, d), _rand(H, N, d), _rand(H, N, d)
+    nB = N // bs
+    mask = (RNG.random((H, nB, nB)) < 0.5).astype(np.uint8)
+    mask[:, np.arange(nB), np.arange(nB)] = 1
+    O, L = oracle.attention(q, k, v, mask, bs, scale=0.3)
+    for h in range(H):
+        tok = np.kron(mask[h], np.ones((bs, bs), np.uint8)).astype(bool)
+        Od, Ld = _dense_library(q[h], k[h], v[h], 0.3, tok)
+        np.testing.assert_allclose(O[h * N:(h + 1) * N], Od, rtol=1e-11, atol=1e-12)
+        np.testing.assert_allclose(L[h * N:(h + 1) * N], Ld, rtol=1e-12, atol=1e-12)
+
+
+def test_block_diagonal_mask_is_independent_block_attention():
+    N, d, bs = 64, 8, 16
+    q, k, v = _rand(1, N, d), _rand(1, N, d), _rand(1, N, d)
+    mask = np.eye(N // bs, dtype=np.uint8)[None]
+    O, L = oracle.attention(q, k, v, mask, bs)
+    for i in range(N // bs):
+        sl = slice(i * bs, (i + 1) * bs)
+        Ob, Lb = _dense_library(q[0, sl], k[0, sl], v[0, sl], 1 / math.sqrt(d),
+                                np.ones((bs, bs), bool))
+        np.testing.assert_allclose(O[sl], Ob, rtol=1e-11, atol=1e-12)
+        np.testing.assert_allclose(L[sl], Lb, rtol=1e-12)
+
+
+def test_single_active_block_brute_force():
+    N, d, bs = 16, 3, 4
+    q, k, v = _rand(1, N, d), _rand(1, N, d), _rand(1, N, d)
+    nB = N // bs
+    mask = np.zeros((1, nB, nB), np.uint8)
+    pick = [2, 0, 3, 1]
+    for i, j in enumerate(pick):
+        mask[0, i, j] = 1
+    O, L = oracle.attention(q, k, v, mask, bs, scale=0.7)
+    for r in range(N):
+        j = pick[r // bs]
+        ss = []
+        for c in range(j * bs, (j + 1) * bs):
+            ss.append(0.7 * sum(float(q[0, r, e]) * float(k[0, c, e]) for e in range(d)))
+        mx = max(ss)
+        w = [math.exp(s - mx) for s in ss]
+        tot = sum(w)
+        for e in range(d):
+            ref = sum(w[t] * float(v[0, j * bs + t, e]) for t in range(bs)) / tot
+            assert abs(O[r, e] - ref) < 1e-12
+        assert abs(L[r] - (mx + math.log(tot))) < 1e-12
+
+
+def test_zero_keys_closed_form():
+    """K = 0: every active score is 0, so LSE = ln(#active keys), O = mean of active values."""
+    N, d, bs = 64, 8, 16
+    q, v = _rand(1, N, d), _rand(1, N, d)
+    k = np.zeros((1, N, d), np.float32)
+    nB = N // bs
+    mask = (RNG.random((1, nB, nB)) < 0.5).astype(np.uint8)
+    mask[0, :, 0] = 1
+    O, L = oracle.attention(q, k, v, mask, bs)
+    for r in range(N):
+        act = np.nonzero(mask[0, r // bs])[0]
+        keys = np.concatenate([np.arange(j * bs, (j + 1) * bs) for j in act])
+        assert L[r] == pytest.approx(math.log(len(keys)), abs=1e-13)
+        np.testing.assert_allclose(O[r], v[0, keys].astype(np.float64).mean(0), atol=1e-13)
+
+
+def test_constant_values_and_unit_row_mass():
+    N, d, bs = 64, 4, 16
+    q, k = _rand(2, N, d) * 3, _rand(2, N, d) * 3
+    nB = N // bs
+    mask = (RNG.random((2, nB, nB)) < 0.6).astype(np.uint8)
+    mask[:, :, 1] = 1
+    v = np.full((2, N, d), 1.0, np.float32)
+    O, _ = oracle.attention(q, k, v, mask, bs)
+    np.testing.assert_allclose(O, 1.0, atol=1e-13)  # sum_c p_c = 1 per row
+    v2 = np.broadcast_to(np.array([2.5, -1.0, 0.0, 7.0], np.float32), (2, N, d)).copy()
+    O2, _ = oracle.attention(q, k, v2, mask, bs)
+    np.testing.assert_allclose(O2, np.broadcast_to(v2[0, 0], O2.shape), atol=1e-12)
+
+
+def test_key_permutation_inside_blocks_is_invariant():
+    N, d, bs = 64, 8, 16
+    q, k, v = _rand(1, N, d), _rand(1, N, d), _rand(1, N, d)
+    nB = N // bs
+    mask = (RNG.random((1, nB, nB)) < 0.5).astype(np.uint8)
+    mask[0, np.arange(nB), np.arange(nB)] = 1
+    perm = np.concatenate([RNG.permutation(bs) + j * bs for j in range(nB)])
+    O1, L1 = oracle.attention(q, k, v, mask, bs)
+    O2, L2 = oracle.attention(q, k[:, perm], v[:, perm], mask, bs)
+    np.testing.assert_allclose(O1, O2, atol=1e-12)
+    np.testing.assert_allclose(L1, L2, atol=1e-12)
+
+
+def test_masked_keys_do_not_matter():
+    """Changing K/V inside skipped blocks leaves the result bit-identical (they are -inf)."""
+    N, d, bs = 64, 8, 16
+    q, k, v = _rand(1, N, d), _rand(1, N, d), _rand(1, N, d)
+    mask = np.zeros((1, 4, 4), np.uint8)
+    mask[0, :, 1] = 1
+    mask[0, 2, 3] = 1
+    O1, L1 = oracle.attention(q, k, v, mask, bs)
+    k2, v2 = k.copy(), v.copy()
+    k2[0, 0:16] *= 100
+    v2[0, 0:16] = 1e6
+    O2, L2 = oracle.attention(q, k2, v2, mask, bs)
+    assert np.array_equal(O1, O2) and np.array_equal(L1, L2)
+
+
+def test_empty_row_convention():
+    N, d, bs = 32, 4, 16
+    q, k, v = _rand(1, N, d), _rand(1, N, d), _rand(1, N, d)
+    mask = np.array([[[0, 0], [1, 1]]], np.uint8)
+    O, L = oracle.attention(q, k, v, mask, bs)
+    assert np.all(O[:16] == 0.0) and np.all(np.isneginf(L[:16]))
+    assert np.all(np.isfinite(L[16:]))
+
+
+def test_default_scale_is_inverse_sqrt_d():
+    N, d, bs = 32, 16, 16
+    q, k, v = _rand(1, N, d), _rand(1, N, d), _rand(1, N, d)
+    mask = np.ones((1, 2, 2), np.uint8)
+    O1, L1 = oracle.attention(q, k, v, mask, bs)
+    O2, L2 = oracle.attention(q, k, v, mask, bs, scale=0.25)
+    np.testing.assert_array_equal(O1, O2)
+    np.testing.assert_array_equal(L1, L2)
+
+
+def test_attention_golden_two_keys():
+    q = np.array([[[1.0], [0.0]]], np.float32)
+    k = np.array([[[0.0], [1.0]]], np.float32)
+    v = np.array([[[0.0], [1.0]]], np.float32)
+    for bits, o_ref, l_ref in read_golden("attention_two_keys.txt"):
+        mask = np.zeros((1, 2, 2), np.uint8)
+        mask[0, 0] = [int(c) for c in bits]
+        mask[0, 1] = 1
+        O, L = oracle.attention(q, k, v, mask, 1, scale=1.0, rows=np.array([0]))
+        assert O[0, 0] == pytest.approx(float(o_ref), abs=1e-15)
+        if l_ref == "-inf":
+            assert np.isneginf(L[0])
+        else:
+            assert L[0] == pytest.approx(float(l_ref), abs=1e-15)
+
+
+def test_row_subset_matches_full():
+    N, d, bs = 64, 8, 16
+    q, k, v = _rand(2, N, d), _rand(2, N, d), _rand(2, N, d)
+    mask = (RNG.random((2, 4, 4)) < 0.5).astype(np.uint8)
+    mask[:, :, 2] = 1
+    O, L = oracle.attention(q, k, v, mask, bs)
+    rows = np.array([5, 70, 127, 0])
+    Os, Ls = oracle.attention(q, k, v, mask, bs, rows=rows)
+    np.testing.assert_array_equal(Os, O[rows])
+    np.testing.assert_array_equal(Ls, L[rows])
+
+
+# ---------------------------------------------------------------- selector
+
+
+def test_block_mean_golden_order():
+    for bs, toks, ref in read_golden("block_mean_order.txt"):
+        bs = int(bs)
+        x = np.array([float(t) for t in toks.split()], np.float32).reshape(1, bs, 1)
+        out = oracle.block_mean(x, bs)
+        assert out.shape == (1, 1, 1)
+        assert float(out[0, 0, 0]) == float(ref)
+
+
+def test_block_mean_exact_integers_and_layout():
+    H, N, d, bs = 3, 64, 5, 16
+    x = RNG.integers(-50, 50, size=(H, N, d)).astype(np.float32)
+    out = oracle.block_mean(x, bs)
+    ref = x.astype(np.float64).reshape(H, N // bs, bs, d).mean(axis=2)
+    assert np.array_equal(out.astype(np.float64), ref)  # sums of small ints are exact
+
+
+def test_block_scores_golden_fma():
+    for qs, ks, ref in read_golden("score_fma.txt"):
+        qb = np.array([float(t) for t in qs.split()], np.float32).reshape(1, 1, -1)
+        kb = np.array([float(t) for t in ks.split()], np.float32).reshape(1, 1, -1)
+        assert float(oracle.block_scores(qb, kb)[0, 0, 0]) == float(ref)
+
+
+def test_block_scores_exact_small_integers_and_orientation():
+    qb = RNG.integers(-8, 8, size=(2, 5, 7)).astype(np.float32)
+    kb = RNG.integers(-8, 8, size=(2, 3, 7)).astype(np.float32)
+    s = oracle.block_scores(qb, kb)
+    assert s.shape == (2, 5, 3)
+    ref = np.einsum("hic,hjc->hij", qb.astype(np.int64), kb.astype(np.int64))
+    assert np.array_equal(s.astype(np.int64), ref)
+
+
+def test_topk_golden_ties_and_signed_zero():
+    for scores, k, kept in read_golden("topk_ties.txt"):
+        s = np.array([float(t) for t in scores.split()], np.float32).reshape(1, -1)
+        m = oracle.topk_mask(s, int(k))
+        assert list(np.nonzero(m[0])[0]) == [int(t) for t in kept.split()]
+
+
+def test_topk_brute_force_with_ties():
+    nKB = 40
+    for trial in range(30):
+        s = RNG.integers(-4, 4, size=(3, nKB)).astype(np.float32)  # many exact ties
+        if trial % 3 == 0:
+            s[s == 0] = -0.0
+        k = int(RNG.integers(1, nKB + 1))
+        m = oracle.topk_mask(s, k)
+        for r in range(3):
+            order = sorted(range(nKB), key=lambda j: (-float(s[r, j]), j))
+            ref = np.zeros(nKB, np.uint8)
+            ref[order[:k]] = 1
+            assert np.array_equal(m[r], ref)
+            assert int(m[r].sum()) == k
+
+
+def test_topk_rejects_nan():
+    s = np.array([[0.0, np.nan, 1.0]], np.float32)
+    with pytest.raises(oracle.OracleError) as e:
+        oracle.topk_mask(s, 1)
+    assert e.value.code == oracle.ERR_NONFINITE
+
+
+@pytest.mark.parametrize("density,nKB,k", [(0.15, 128, 19), (0.05, 512, 25), (0.05, 256, 12),
+                                           (0.001, 64, 1), (1.0, 66, 66), (0.5, 8, 4),
+                                           (0.25, 128, 32)])
+def test_topk_count(density, nKB, k):
+    assert oracle.topk_count(density, nKB) == k
+
+
+def test_select_mask_is_pool_score_topk():
+    """End to end on clustered blocks: blocks built from one centroid rank first."""
+    bs, d = 16, 8
+    cent = np.zeros((4, d), np.float32)
+    cent[np.arange(4), np.arange(4)] = 4.0
+    order = [0, 1, 2, 3, 0, 1, 2, 3]
+    x = np.concatenate([np.repeat(cent[c][None], bs, 0) for c in order])[None]
+    m = oracle.select_mask(x, x, bs, 0.25)
+    for i, c in enumerate(order):
+        assert list(np.nonzero(m[0, i])[0]) == [j for j, cc in enumerate(order) if cc == c]
+
+
+# ---------------------------------------------------------------- static masks
+
+
+def _golden_bits(name):
+    return np.array([[int(c) for c in row[0]] for row in read_golden(name)], np.uint8)
+
+
+def test_band_mask_golden_small():
+    assert np.array_equal(oracle.band_mask(6, 1, 1, [3]), _golden_bits("band_mask_small.txt"))
+
+
+def test_band_mask_t2i_count():
+    """66 blocks: 2 text + 64 image rows, band 2, anchors {0, 32}.
+
+    Text rows 2*66 = 132, text columns of image rows 64*2 = 128. Image-image:
+    band 64*5 - 2*(1+2) = 314; anchor rows/cols 2*64 + 2*64 - 4 = 252; band
+    cells on anchor rows/cols: row0 3 + row32 5 + col0 3 + col32 5 - 2 = 14;
+    total 314 + 252 - 14 = 552. Sum 812.
+    """
+    m = oracle.band_mask(66, 2, 2, [0, 32])
+    assert int(m.sum()) == 812
+    assert np.array_equal(m, m.T)
+
+
+def test_cuboid_mask_golden_small():
+    assert np.array_equal(oracle.cuboid_mask(1, (1, 2, 2)), _golden_bits("cuboid_mask_small.txt"))
+
+
+def test_cuboid_mask_video_count():
+    """4 text + 4x8x8 cuboids: self 256; face pairs t 2*3*64 = 384, h 2*4*7*8 = 448,
+    w 2*4*8*7 = 448 -> 1536; text rows 4*260 = 1040; text cols 256*4 = 1024. Sum 3600."""
+    m = oracle.cuboid_mask(4, (4, 8, 8))
+    assert m.shape == (260, 260)
+    assert int(m.sum()) == 3600
+    assert np.array_equal(m, m.T)
+    assert np.all(m[np.arange(260), np.arange(260)] == 1)
+
+
+def test_cuboid_mask_degree_brute_force():
+    grid = (3, 2, 4)
+    m = oracle.cuboid_mask(2, grid)
+    cells = list(itertools.product(range(3), range(2), range(4)))
+    for a, ca in enumerate(cells):
+        for b, cb in enumerate(cells):
+            want = sum(abs(x - y) for x, y in zip(ca, cb)) <= 1
+            assert m[2 + a, 2 + b] == want
+
+
+# ---------------------------------------------------------------- index forms
+
+
+def test_mask_to_index_brute_force():
+    for nKB in (1, 8, 31, 32, 33, 70):
+        mask = (RNG.random((5, nKB)) < 0.4).astype(np.uint8)
+        mask[2] = 0
+        row_ptr, col_idx, bitmap = oracle.mask_to_index(mask)
+        assert row_ptr[0] == 0 and row_ptr[-1] == mask.sum()
+        for r in range(5):
+            js = [j for j in range(nKB) if mask[r, j]]
+            assert list(col_idx[row_ptr[r]:row_ptr[r + 1]]) == js
+            for j in range(nKB):
+                assert ((int(bitmap[r, j // 32]) >> (j % 32)) & 1) == mask[r, j]
+            assert sum(bin(int(w)).count("1") for w in bitmap[r]) == len(js)
