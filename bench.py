@@ -1,0 +1,462 @@
+#!/usr/bin/env python
+"""Benchmark of the block-sparse attention forward hot path on GB300.
+
+A step is one pass of the whole path over one batch: bsa_build_mask (static
+spec evaluation or mean-pooled top-k selection, CSR + bitmap emit) followed by
+bsa_forward (tile ordering + the tcgen05 block-sparse FlashAttention kernel).
+
+Reported metric: effective TFLOP/s, counting only active block pairs
+(4 * block^2 * d FLOPs per active pair per head), plus ms per forward call and
+its fraction of the measured dense bf16 tensor peak.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+Timing: W warm-up steps, a short clock-settling phase, then exactly K timed
+steps, each replayed from CUDA graphs and bracketed by CUDA events on the
+launching stream; L2 is flushed (256 MB write) before every timed step.
+--impl reference times the CPU oracle (test infrastructure, double precision)
+on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+from block_sparse_attention_mean_gb300 import workloads as wl  # noqa: E402
+
+DEFAULT_WORKLOAD = "t2i_static"
+FLUSH_BYTES = 256 << 20
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "fwd_tc_traffic.txt")
+FWD_SOURCE = os.path.join(ROOT, "block_sparse_attention_mean_gb300", "csrc", "fwd_tc.cu")
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(wl.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def mask_nnz_oracle_free(w) -> int:
+    """Active block pairs of the workload, from the library's host count."""
+    from block_sparse_attention_mean_gb300 import binding as bb
+    spec = None
+    if w.mask == wl.BAND:
+        spec = bb.band_spec(w.n_text_blocks, w.band, list(w.anchors))
+    elif w.mask == wl.CUBOID:
+        spec = bb.cuboid_spec(w.n_text_blocks, w.grid)
+    return bb.bsa_mask_nnz(w.B, w.H, w.N, w.block, w.density, spec)
+
+
+def effective_flops(w, nnz: int) -> float:
+    return float(nnz) * 4.0 * w.block * w.block * w.d
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f), "measured"
+    except (OSError, ValueError):
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+def traffic_from_profile():
+    """dram bytes per forward launch from the committed ncu summary, or None when the
+    kernel source changed after that capture."""
+    try:
+        fields = {}
+        with open(PROFILE_TRAFFIC) as f:
+            for line in f:
+                if ":" in line and not line.startswith("#"):
+                    k, v = line.split(":", 1)
+                    fields[k.strip()] = v.strip()
+        sha = hashlib.sha256(open(FWD_SOURCE, "rb").read()).hexdigest()
+        if fields.get("fwd_tc.cu sha256") != sha:
+            return None
+        return float(fields["dram_bytes_per_launch_scaled"])
+    except (OSError, KeyError, ValueError):
+        return None
+
+
+# ---------------------------------------------------------------- clocks
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.tmp = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100",
+                 "-i", str(self.gpu)], stdout=self.tmp, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.tmp.flush()
+        rows = []
+        with open(self.tmp.name) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) == 9:
+                    rows.append(parts)
+        os.unlink(self.tmp.name)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "", 1).isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "", 1).isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def gpu_index_for(local_rank: int) -> int:
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+    ids = [v for v in vis.split(",") if v.strip()]
+    if local_rank < len(ids) and ids[local_rank].strip().isdigit():
+        return int(ids[local_rank])
+    return local_rank
+
+
+# ---------------------------------------------------------------- CPU oracle timing
+
+
+def time_oracle(w, inp, budget_s: float, seed: int = 0):
+    """Time the oracle on a bounded sample of the workload and extrapolate.
+
+    The mask step (the oracle's selector or static evaluator) runs on every head;
+    the attention runs on a seeded sample of query rows across all heads sized to
+    about `budget_s` seconds, and its time is scaled linearly to all rows.
+    Returns (seconds for the full workload, sample description, cores)."""
+    import oracle
+    oracle.build()
+    rng = np.random.default_rng(seed)
+    BH = w.B * w.H
+    total_rows = BH * w.N
+    q = inp["q"].reshape(BH, w.N, w.d)
+    k = inp["k"].reshape(BH, w.N, w.d)
+    v = inp["v"].reshape(BH, w.N, w.d)
+    t0 = time.perf_counter()
+    if w.mask == wl.TOPK:
+        mask = oracle.select_mask(q, k, w.block, w.density)
+    elif w.mask == wl.BAND:
+        mask = np.broadcast_to(oracle.band_mask(w.nQB, w.n_text_blocks, w.band, w.anchors),
+                               (BH, w.nQB, w.nKB)).copy()
+    elif w.mask == wl.CUBOID:
+        mask = np.broadcast_to(oracle.cuboid_mask(w.n_text_blocks, w.grid), (BH, w.nQB, w.nKB)).copy()
+    else:
+        mask = inp["mask"].reshape(BH, w.nQB, w.nKB)
+    t_mask = time.perf_counter() - t0
+    probe = np.sort(rng.choice(total_rows, size=min(512, total_rows), replace=False))
+    t0 = time.perf_counter()
+    oracle.attention(q, k, v, mask, w.block, rows=probe)
+    per_row = (time.perf_counter() - t0) / probe.size
+    n = int(min(total_rows, max(probe.size, budget_s / max(per_row, 1e-9))))
+    rows = np.sort(rng.choice(total_rows, size=n, replace=False)) if n < total_rows else \
+        np.arange(total_rows, dtype=np.int64)
+    t0 = time.perf_counter()
+    oracle.attention(q, k, v, mask, w.block, rows=rows)
+    t_rows = time.perf_counter() - t0
+    full = t_mask + t_rows * total_rows / n
+    cores = os.cpu_count() or 1
+    sample = (f"mask for all {BH} heads; attention on {n} of {total_rows} query rows (seeded, all heads), "
+              f"scaled linearly to all rows; OpenMP over rows on {cores} cores")
+    return full, sample, cores
+
+
+# ---------------------------------------------------------------- our arm
+
+
+def run_ours(args, world, rank, local):
+    import torch
+    import torch.distributed as dist
+
+    from block_sparse_attention_mean_gb300 import binding as bb
+    from block_sparse_attention_mean_gb300 import build as bbuild
+
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    bbuild.build()
+    bb.load()
+    w = wl.WORKLOADS[args.workload]
+    inp = wl.make_inputs(w)
+    dev = torch.device("cuda", local)
+
+    def upload(name):
+        if w.dtype == "bf16":
+            return torch.from_numpy(inp[name + "_bits"].view(np.int16)).to(dev).view(torch.bfloat16)
+        return torch.from_numpy(inp[name]).to(dev)
+
+    q, k, v = upload("q"), upload("k"), upload("v")
+    dt = bb.BF16 if w.dtype == "bf16" else bb.FP32
+    B, H, N, d, bs = w.B, w.H, w.N, w.d, w.block
+    nB = N // bs
+    W = (nB + 31) // 32
+    spec = None
+    mask_dev = None
+    if w.mask == wl.BAND:
+        spec = bb.band_spec(w.n_text_blocks, w.band, list(w.anchors))
+    elif w.mask == wl.CUBOID:
+        spec = bb.cuboid_spec(w.n_text_blocks, w.grid)
+    elif w.mask == wl.EXPLICIT:
+        mask_dev = torch.from_numpy(wl.pack_bitmap_words(inp["mask"]).reshape(-1)).to(dev)
+        spec = bb.explicit_spec(mask_dev)
+    cap = bb.bsa_mask_nnz(B, H, N, bs, w.density, spec)
+    row_ptr = torch.empty(B * H * nB + 1, dtype=torch.int32, device=dev)
+    col_idx = torch.empty(cap, dtype=torch.int32, device=dev)
+    bitmap = torch.empty(B * H * nB * W, dtype=torch.int32, device=dev)
+    ws_m = bb.workspace(0, B, H, N, d, bs, dev)
+    ws_f = bb.workspace(1, B, H, N, d, bs, dev)
+    O = torch.empty_like(q)
+    LSE = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    qk_in = (None, None) if spec is not None else (q, k)
+
+    def build_call(s):
+        bb.bsa_build_mask(qk_in[0], qk_in[1], dt, B, H, N, d, bs, w.density, spec, row_ptr, col_idx, cap,
+                          bitmap, ws_m, ws_m.numel(), s)
+
+    def fwd_call(s):
+        bb.bsa_forward(q, k, v, dt, B, H, N, d, bs, row_ptr, col_idx, bitmap, w.index_mode, 0.0, O, LSE, ws_f,
+                       ws_f.numel(), s)
+
+    launches_per_step = (3 if spec is not None else 2) + (2 if dt == bb.BF16 else 1)
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(args.warmup, 3)):
+            build_call(stream)
+            fwd_call(stream)
+    for ws in (ws_m, ws_f):
+        code = bb.bsa_check_device_error(ws, stream)
+        if code != 0:
+            raise bb.BsaError(code, "warm-up")
+    nnz = int(row_ptr[-1].item())
+    if not torch.isfinite(LSE[LSE > -float("inf")]).all():
+        raise RuntimeError("non-finite LSE after warm-up")
+
+    # CUDA graphs of the two calls (falls back to eager launches if capture fails)
+    graphs = None
+    try:
+        g_build, g_fwd = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_build, stream=stream):
+            build_call(torch.cuda.current_stream())
+        with torch.cuda.graph(g_fwd, stream=stream):
+            fwd_call(torch.cuda.current_stream())
+        graphs = (g_build, g_fwd)
+    except Exception as exc:  # noqa: BLE001
+        print(f"# graph capture failed ({exc}); timing eager launches", file=sys.stderr)
+
+    def step():
+        if graphs:
+            graphs[0].replay()
+            graphs[1].replay()
+        else:
+            build_call(stream)
+            fwd_call(stream)
+
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    sampler = ClockSampler(gpu_index_for(local))
+    sampler.start()
+    with torch.cuda.stream(stream):
+        t_end = time.perf_counter() + 1.5  # let clocks settle under load
+        while time.perf_counter() < t_end:
+            for _ in range(20):
+                flush.zero_()
+                step()
+            stream.synchronize()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+               torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        wall0 = time.perf_counter()
+        for i in range(args.steps):
+            flush.zero_()
+            ev[i][0].record(stream)
+            if graphs:
+                graphs[0].replay()
+                ev[i][1].record(stream)
+                graphs[1].replay()
+            else:
+                build_call(stream)
+                ev[i][1].record(stream)
+                fwd_call(stream)
+            ev[i][2].record(stream)
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - wall0
+        if world > 1:
+            dist.barrier()
+    clocks = sampler.stop()
+    code = bb.bsa_check_device_error(ws_f, stream) or bb.bsa_check_device_error(ws_m, stream)
+    if code != 0:
+        raise bb.BsaError(code, "timed steps")
+    step_ms = [e[0].elapsed_time(e[2]) for e in ev]
+    fwd_ms = [e[1].elapsed_time(e[2]) for e in ev]
+    build_ms = [e[0].elapsed_time(e[1]) for e in ev]
+    total_ms = sum(step_ms)
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    flops = effective_flops(w, nnz)
+    ms_per_step = total_ms / args.steps
+    value = flops * world * args.steps / (total_ms * 1e-3) / 1e12
+
+    # end to end through the C ABI from pinned host buffers
+    e2e = None
+    if args.e2e_steps > 0:
+        hq, hk, hv = (t.cpu().pin_memory() for t in (q, k, v))
+        hO = torch.empty(O.shape, dtype=O.dtype).pin_memory()
+        hL = torch.empty(LSE.shape, dtype=LSE.dtype).pin_memory()
+        e2e_ms = []
+        with torch.cuda.stream(stream):
+            for i in range(args.e2e_steps + 2):
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                q.copy_(hq, non_blocking=True)
+                k.copy_(hk, non_blocking=True)
+                v.copy_(hv, non_blocking=True)
+                build_call(stream)
+                fwd_call(stream)
+                hO.copy_(O, non_blocking=True)
+                hL.copy_(LSE, non_blocking=True)
+                e1.record(stream)
+                e1.synchronize()
+                if i >= 2:
+                    e2e_ms.append(e0.elapsed_time(e1))
+        h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
+        d2h = hO.numel() * hO.element_size() + hL.numel() * hL.element_size()
+        e2e_mean = sum(e2e_ms) / len(e2e_ms)
+        if world > 1:
+            t = torch.tensor([e2e_mean], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_mean = float(t.item())
+        e2e = {"value": round(flops * world / (e2e_mean * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
+               "ms_per_step": round(e2e_mean, 4), "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+    peaks, peak_kind = measured_peaks()
+    fwd_mean = sum(fwd_ms) / len(fwd_ms)
+    achieved = flops / (fwd_mean * 1e-3) / 1e12
+    peak = float(peaks["bf16_tflops"])
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        full_s, sample, cores = time_oracle(w, inp, budget_s=10.0)
+        cpu = {"value": round(flops / full_s / 1e12, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+               "sample": sample, "ms_per_call_extrapolated": round(full_s * 1e3, 1)}
+    line = {
+        "metric": "block-sparse attn fwd effective TFLOP/s (active blocks only, 4*bs^2*d per pair)",
+        "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if w.dtype == "bf16" else "f32",
+        "data": "synthetic (seeded generator; no dataset or weights)",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "block": w.block,
+                   "mask": w.mask, "density": w.density if w.mask == wl.TOPK else None,
+                   "active_block_pairs": nnz, "block_density": round(nnz / (w.B * w.H * nB * nB), 5),
+                   "index_mode": "bitmap" if w.index_mode else "csr",
+                   "l2": "flushed (256 MB write) before every timed step", "cuda_graphs": bool(graphs),
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "fwd_ms_per_call": round(fwd_mean, 5), "build_mask_ms": round(sum(build_ms) / len(build_ms), 5),
+        "fwd_tflops": round(achieved, 2), "pct_of_bf16_peak": round(100 * achieved / peak, 2),
+        "wall_s_timed_loop": round(wall, 4),
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
+                     "frac": round(achieved / peak, 4), "traffic": traffic_from_profile(),
+                     "kernel": "fwd_tc_kernel (+ tile_order_kernel in the same bracket)",
+                     "peak_source": f"{peak_kind} bf16_tflops (burst)"},
+        "e2e": e2e, "gpu_launches": launches_per_step * args.steps, "clocks": clocks, "cpu_baseline": cpu,
+    }
+    print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+
+
+# ---------------------------------------------------------------- reference arm (CPU oracle)
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    w = wl.WORKLOADS[args.workload]
+    inp = wl.make_inputs(w)
+    from block_sparse_attention_mean_gb300 import binding as bb  # host count only, no GPU call
+    from block_sparse_attention_mean_gb300 import build as bbuild
+    bbuild.build()
+    nnz = int(inp["mask"].sum()) if w.mask == wl.EXPLICIT else mask_nnz_oracle_free(w)
+    flops = effective_flops(w, nnz)
+    for i in range(max(args.warmup, 0)):
+        time_oracle(w, inp, budget_s=0.5, seed=i)
+    totals = []
+    sample = cores = None
+    for i in range(args.steps):
+        full_s, sample, cores = time_oracle(w, inp, budget_s=1.0, seed=100 + i)
+        totals.append(full_s)
+    ms = 1e3 * sum(totals) / len(totals)
+    value = flops / (ms * 1e-3) / 1e12
+    line = {"impl": "reference",
+            "metric": "block-sparse attn fwd effective TFLOP/s (active blocks only, 4*bs^2*d per pair)",
+            "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded generator)",
+            "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "block": w.block},
+            "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    del bb
+
+
+def main():
+    args = parse_args()
+    world, rank, local = dist_env()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_ours(args, world, rank, local)
+
+
+if __name__ == "__main__":
+    main()

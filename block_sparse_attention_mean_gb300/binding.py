@@ -1,0 +1,267 @@
+"""ctypes binding of libbsa.so: the C ABI of include/bsa.h, one Python function per
+entry point with the same name (argument marshalling only), plus small helpers
+that allocate outputs and workspaces with torch.
+
+There is no fallback: if libbsa.so cannot be loaded every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+from typing import Optional, Sequence, Tuple
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libbsa.so")
+
+OK = 0
+ERR_INVALID_ARG = 1
+ERR_SHAPE = 2
+ERR_DTYPE = 3
+ERR_CAPACITY = 4
+ERR_NONFINITE = 5
+ERR_TIMEOUT = 6
+ERR_CUDA = 7
+ERR_UNSUPPORTED = 8
+ERR_WORKSPACE = 9
+
+BF16 = 0
+FP32 = 1
+
+STATIC_EXPLICIT = 0
+STATIC_MODALITY_BAND = 1
+STATIC_CUBOID = 2
+MAX_ANCHORS = 8
+
+# every symbol declared in include/bsa.h
+EXPORTS = ("bsa_build_mask", "bsa_forward", "bsa_mask_nnz", "bsa_workspace_size",
+           "bsa_check_device_error", "bsa_validate_index", "bsa_debug_config",
+           "bsa_status_string")
+
+
+class StaticSpec(ctypes.Structure):
+    """Mirror of bsa_static_spec."""
+    _fields_ = [("kind", ctypes.c_int), ("bitmap", ctypes.c_void_p), ("broadcast_bh", ctypes.c_int),
+                ("n_text_blocks", ctypes.c_int), ("band", ctypes.c_int), ("n_anchors", ctypes.c_int),
+                ("anchors", ctypes.c_int * MAX_ANCHORS), ("grid_t", ctypes.c_int),
+                ("grid_h", ctypes.c_int), ("grid_w", ctypes.c_int)]
+
+
+class BsaError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        super().__init__(f"{where}: {status_string(code)} (status {code})")
+        self.code = code
+
+
+_lib = None
+
+
+def load():
+    """Load libbsa.so (raises OSError if it was not built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise OSError(f"libbsa.so not built at {LIB_PATH}; run block_sparse_attention_mean_gb300.build.build()")
+    lib = ctypes.CDLL(LIB_PATH)
+    P, I, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    I64, SZ, U32, U64 = ctypes.c_int64, ctypes.c_size_t, ctypes.c_uint32, ctypes.c_uint64
+    lib.bsa_build_mask.argtypes = [P, P, I, I, I, I, I, I, F, ctypes.POINTER(StaticSpec), P, P, I64, P, P,
+                                   SZ, P]
+    lib.bsa_forward.argtypes = [P, P, P, I, I, I, I, I, I, P, P, P, I, F, P, P, P, SZ, P]
+    lib.bsa_mask_nnz.argtypes = [I, I, I, I, F, ctypes.POINTER(StaticSpec), ctypes.POINTER(I64)]
+    lib.bsa_workspace_size.argtypes = [I, I, I, I, I, I, ctypes.POINTER(SZ)]
+    lib.bsa_check_device_error.argtypes = [P, P]
+    lib.bsa_validate_index.argtypes = [I, I, I, I, P, P, P, P, SZ, P]
+    lib.bsa_debug_config.argtypes = [U32, U64]
+    lib.bsa_status_string.argtypes = [I]
+    lib.bsa_status_string.restype = ctypes.c_char_p
+    for name in EXPORTS:
+        if name != "bsa_status_string":
+            getattr(lib, name).restype = I
+    _lib = lib
+    return lib
+
+
+def _ptr(t) -> Optional[int]:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(code: int, where: str):
+    if code != OK:
+        raise BsaError(code, where)
+
+
+def status_string(code: int) -> str:
+    return load().bsa_status_string(int(code)).decode()
+
+
+# ------------------------------------------------------------------ C ABI mirror
+
+
+def bsa_build_mask(Q, K, dt: int, B: int, H: int, N: int, d: int, block: int, density: float,
+                   spec: Optional[StaticSpec], row_ptr, col_idx, col_capacity: int, bitmap, workspace,
+                   workspace_bytes: int, stream=None) -> None:
+    code = load().bsa_build_mask(_ptr(Q), _ptr(K), dt, B, H, N, d, block, float(density),
+                                 ctypes.byref(spec) if spec is not None else None, _ptr(row_ptr),
+                                 _ptr(col_idx), int(col_capacity), _ptr(bitmap), _ptr(workspace),
+                                 int(workspace_bytes), _stream(stream))
+    _check(code, "bsa_build_mask")
+
+
+def bsa_forward(Q, K, V, dt: int, B: int, H: int, N: int, d: int, block: int, row_ptr, col_idx, bitmap,
+                index_mode: int, scale: float, O, LSE, workspace, workspace_bytes: int, stream=None) -> None:
+    code = load().bsa_forward(_ptr(Q), _ptr(K), _ptr(V), dt, B, H, N, d, block, _ptr(row_ptr), _ptr(col_idx),
+                              _ptr(bitmap), int(index_mode), float(scale), _ptr(O), _ptr(LSE),
+                              _ptr(workspace), int(workspace_bytes), _stream(stream))
+    _check(code, "bsa_forward")
+
+
+def bsa_mask_nnz(B: int, H: int, N: int, block: int, density: float, spec: Optional[StaticSpec]) -> int:
+    out = ctypes.c_int64(0)
+    code = load().bsa_mask_nnz(B, H, N, block, float(density),
+                               ctypes.byref(spec) if spec is not None else None, ctypes.byref(out))
+    _check(code, "bsa_mask_nnz")
+    return out.value
+
+
+def bsa_workspace_size(which: int, B: int, H: int, N: int, d: int, block: int) -> int:
+    out = ctypes.c_size_t(0)
+    _check(load().bsa_workspace_size(which, B, H, N, d, block, ctypes.byref(out)), "bsa_workspace_size")
+    return out.value
+
+
+def bsa_check_device_error(workspace, stream=None) -> int:
+    """Status recorded on the device (0 = none); synchronises the stream and clears it."""
+    return int(load().bsa_check_device_error(_ptr(workspace), _stream(stream)))
+
+
+def bsa_validate_index(B: int, H: int, N: int, block: int, row_ptr, col_idx, bitmap, workspace,
+                       workspace_bytes: int, stream=None) -> None:
+    _check(load().bsa_validate_index(B, H, N, block, _ptr(row_ptr), _ptr(col_idx), _ptr(bitmap),
+                                     _ptr(workspace), int(workspace_bytes), _stream(stream)),
+           "bsa_validate_index")
+
+
+def bsa_debug_config(flags: int, wait_limit_ns: int = 0) -> None:
+    _check(load().bsa_debug_config(int(flags), int(wait_limit_ns)), "bsa_debug_config")
+
+
+def bsa_status_string(code: int) -> str:
+    return status_string(code)
+
+
+# ------------------------------------------------------------------ helpers
+
+
+def band_spec(n_text_blocks: int, band: int, anchors: Sequence[int]) -> StaticSpec:
+    s = StaticSpec()
+    s.kind = STATIC_MODALITY_BAND
+    s.n_text_blocks = n_text_blocks
+    s.band = band
+    s.n_anchors = len(anchors)
+    for i, a in enumerate(anchors):
+        s.anchors[i] = a
+    return s
+
+
+def cuboid_spec(n_text_blocks: int, grid: Tuple[int, int, int]) -> StaticSpec:
+    s = StaticSpec()
+    s.kind = STATIC_CUBOID
+    s.n_text_blocks = n_text_blocks
+    s.grid_t, s.grid_h, s.grid_w = grid
+    return s
+
+
+def explicit_spec(bitmap: torch.Tensor, broadcast_bh: bool = False) -> StaticSpec:
+    s = StaticSpec()
+    s.kind = STATIC_EXPLICIT
+    s.bitmap = bitmap.data_ptr()
+    s.broadcast_bh = 1 if broadcast_bh else 0
+    s._keep = bitmap  # keep the device buffer alive with the spec
+    return s
+
+
+def _dtype_code(t: Optional[torch.Tensor], default: int = BF16) -> int:
+    if t is None:
+        return default
+    if t.dtype == torch.bfloat16:
+        return BF16
+    if t.dtype == torch.float32:
+        return FP32
+    raise BsaError(ERR_DTYPE, f"tensor dtype {t.dtype}")
+
+
+def workspace(which: int, B: int, H: int, N: int, d: int, block: int, device="cuda") -> torch.Tensor:
+    """Zero-initialised device workspace (the device error word starts cleared)."""
+    return torch.zeros(bsa_workspace_size(which, B, H, N, d, block), dtype=torch.uint8, device=device)
+
+
+class Index:
+    """Device CSR + bitmap index of a block mask."""
+
+    def __init__(self, row_ptr, col_idx, bitmap, nnz, block):
+        self.row_ptr, self.col_idx, self.bitmap, self.nnz, self.block = row_ptr, col_idx, bitmap, nnz, block
+
+
+def build_mask(q: Optional[torch.Tensor], k: Optional[torch.Tensor], block: int, density: float = 0.0,
+               spec: Optional[StaticSpec] = None, shape: Optional[Tuple[int, int, int, int]] = None,
+               ws: Optional[torch.Tensor] = None, stream=None, check: bool = True) -> Index:
+    """Allocate the index and run bsa_build_mask. `shape` = (B, H, N, d) when q is None."""
+    if q is not None:
+        B, H, N, d = q.shape
+        device = q.device
+    else:
+        B, H, N, d = shape
+        device = torch.device("cuda")
+    nB = N // block
+    nnz = bsa_mask_nnz(B, H, N, block, density, spec)
+    W = (nB + 31) // 32
+    row_ptr = torch.empty(B * H * nB + 1, dtype=torch.int32, device=device)
+    col_idx = torch.empty(max(nnz, 1), dtype=torch.int32, device=device)
+    bitmap = torch.empty(B * H * nB * W, dtype=torch.int32, device=device)
+    if ws is None:
+        ws = workspace(0, B, H, N, d, block, device)
+    bsa_build_mask(q, k, _dtype_code(q), B, H, N, d, block, density, spec, row_ptr, col_idx, nnz, bitmap,
+                   ws, ws.numel(), stream)
+    if check:
+        _check(bsa_check_device_error(ws, stream), "bsa_build_mask (device)")
+    if spec is not None and spec.kind == STATIC_EXPLICIT and check:
+        nnz = int(row_ptr[-1].item())
+    return Index(row_ptr, col_idx, bitmap, nnz, block)
+
+
+def forward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, index: Index, index_mode: int = 0,
+            scale: float = 0.0, ws: Optional[torch.Tensor] = None, out: Optional[torch.Tensor] = None,
+            lse: Optional[torch.Tensor] = None, stream=None, check: bool = True):
+    """Run bsa_forward; returns (O, LSE)."""
+    B, H, N, d = q.shape
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    if ws is None:
+        ws = workspace(1, B, H, N, d, index.block, q.device)
+    bsa_forward(q, k, v, _dtype_code(q), B, H, N, d, index.block, index.row_ptr, index.col_idx, index.bitmap,
+                index_mode, scale, out, lse, ws, ws.numel(), stream)
+    if check:
+        _check(bsa_check_device_error(ws, stream), "bsa_forward (device)")
+    return out, lse
+
+
+def default_scale(d: int) -> float:
+    return 1.0 / math.sqrt(d)

@@ -1,0 +1,264 @@
+// api.cu -- the C ABI of libbsa.so: argument validation, workspace layout and
+// dispatch to the kernels. Every check runs on the host before any launch.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstdlib>
+
+#include "internal.h"
+
+namespace {
+
+uint32_t g_dbg_flags = 0;
+uint64_t g_wait_limit_ns = bsa::kDefaultWaitNs;
+
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+bsa_status check_shape(int B, int H, int N, int d, int block)
+{
+    if (B <= 0 || H <= 0 || N <= 0) return BSA_ERR_SHAPE;
+    if (d != 64 && d != 128) return BSA_ERR_SHAPE;
+    if (block != 64 && block != 128) return BSA_ERR_SHAPE;
+    if (N % block != 0) return BSA_ERR_SHAPE;
+    const int64_t rows = static_cast<int64_t>(B) * H * N;
+    if (rows > INT32_MAX) return BSA_ERR_SHAPE;  // TMA row coordinates are int32
+    return BSA_OK;
+}
+
+// Blocks kept per Q block: max(1, floor(density * nKB)), density as given (fp32).
+int topk_keep(float density, int nKB)
+{
+    int k = static_cast<int>(std::floor(static_cast<double>(density) * static_cast<double>(nKB)));
+    if (k < 1) k = 1;
+    if (k > nKB) k = nKB;
+    return k;
+}
+
+bool valid_density(float density) { return std::isfinite(density) && density > 0.0f && density <= 1.0f; }
+
+// Static spec: structural checks; `count` gets the per-(b, h) active block count
+// (band and cuboid only).
+bsa_status check_spec(const bsa_static_spec *s, int nB, int64_t *count)
+{
+    *count = -1;
+    if (s->kind == BSA_STATIC_EXPLICIT) {
+        if (!s->bitmap || !aligned(s->bitmap, 4)) return BSA_ERR_INVALID_ARG;
+        return BSA_OK;
+    }
+    if (s->n_text_blocks < 0 || s->n_text_blocks > nB) return BSA_ERR_INVALID_ARG;
+    const int nt = s->n_text_blocks;
+    int64_t c = 0;
+    if (s->kind == BSA_STATIC_MODALITY_BAND) {
+        if (s->band < 0 || s->n_anchors < 0 || s->n_anchors > BSA_MAX_ANCHORS) return BSA_ERR_INVALID_ARG;
+        for (int a = 0; a < s->n_anchors; ++a)
+            if (s->anchors[a] < 0 || s->anchors[a] >= nB - nt) return BSA_ERR_INVALID_ARG;
+        for (int i = 0; i < nB; ++i)
+            for (int j = 0; j < nB; ++j) {
+                bool on = i < nt || j < nt;
+                if (!on) {
+                    const int r = i - nt, cc = j - nt;
+                    on = std::abs(r - cc) <= s->band;
+                    for (int a = 0; a < s->n_anchors && !on; ++a) on = r == s->anchors[a] || cc == s->anchors[a];
+                }
+                c += on;
+            }
+    } else if (s->kind == BSA_STATIC_CUBOID) {
+        if (s->grid_t <= 0 || s->grid_h <= 0 || s->grid_w <= 0) return BSA_ERR_INVALID_ARG;
+        const int64_t cells = static_cast<int64_t>(s->grid_t) * s->grid_h * s->grid_w;
+        if (nt + cells != nB) return BSA_ERR_SHAPE;
+        // text rows and columns, then each cuboid's own cell plus its in-grid faces
+        c = static_cast<int64_t>(nt) * nB + cells * nt;
+        for (int t = 0; t < s->grid_t; ++t)
+            for (int h = 0; h < s->grid_h; ++h)
+                for (int w = 0; w < s->grid_w; ++w)
+                    c += 1 + (t > 0) + (t + 1 < s->grid_t) + (h > 0) + (h + 1 < s->grid_h) + (w > 0) +
+                         (w + 1 < s->grid_w);
+    } else {
+        return BSA_ERR_INVALID_ARG;
+    }
+    *count = c;
+    return BSA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *bsa_status_string(int status)
+{
+    switch (status) {
+    case BSA_OK: return "ok";
+    case BSA_ERR_INVALID_ARG: return "invalid argument";
+    case BSA_ERR_SHAPE: return "unsupported shape";
+    case BSA_ERR_DTYPE: return "unsupported dtype";
+    case BSA_ERR_CAPACITY: return "col_idx capacity too small";
+    case BSA_ERR_NONFINITE: return "non-finite block score";
+    case BSA_ERR_TIMEOUT: return "device wait timed out";
+    case BSA_ERR_CUDA: return "CUDA runtime error";
+    case BSA_ERR_UNSUPPORTED: return "unsupported request";
+    case BSA_ERR_WORKSPACE: return "workspace missing or too small";
+    default: return "unknown status";
+    }
+}
+
+bsa_status bsa_workspace_size(int which, int B, int H, int N, int d, int block, size_t *bytes)
+{
+    if (!bytes) return BSA_ERR_INVALID_ARG;
+    const bsa_status s = check_shape(B, H, N, d, block);
+    if (s != BSA_OK) return s;
+    if (which == 0) *bytes = bsa::mask_workspace_bytes(B, H, N, d, block);
+    else if (which == 1) *bytes = bsa::fwd_workspace_bytes(B, H, N, d, block);
+    else return BSA_ERR_INVALID_ARG;
+    return BSA_OK;
+}
+
+bsa_status bsa_mask_nnz(int B, int H, int N, int block, float density, const bsa_static_spec *spec, int64_t *nnz)
+{
+    if (!nnz) return BSA_ERR_INVALID_ARG;
+    if (B <= 0 || H <= 0 || N <= 0 || (block != 64 && block != 128) || N % block != 0) return BSA_ERR_SHAPE;
+    const int nB = N / block;
+    const int64_t BH = static_cast<int64_t>(B) * H;
+    if (!spec) {
+        if (!valid_density(density)) return BSA_ERR_INVALID_ARG;
+        *nnz = BH * nB * topk_keep(density, nB);
+        return BSA_OK;
+    }
+    int64_t c = 0;
+    const bsa_status s = check_spec(spec, nB, &c);
+    if (s != BSA_OK) return s;
+    *nnz = spec->kind == BSA_STATIC_EXPLICIT ? BH * nB * nB : BH * c;
+    return BSA_OK;
+}
+
+bsa_status bsa_build_mask(const void *Q, const void *K, int dt, int B, int H, int N, int d, int block, float density,
+                          const bsa_static_spec *spec, int32_t *row_ptr, int32_t *col_idx, int64_t col_capacity,
+                          uint32_t *bitmap, void *workspace, size_t workspace_bytes, void *stream)
+{
+    bsa_status s = check_shape(B, H, N, d, block);
+    if (s != BSA_OK) return s;
+    if (dt != BSA_BF16 && dt != BSA_FP32) return BSA_ERR_DTYPE;
+    if (!row_ptr || !col_idx || !bitmap || col_capacity < 0) return BSA_ERR_INVALID_ARG;
+    if (!aligned(row_ptr, 4) || !aligned(col_idx, 4) || !aligned(bitmap, 4)) return BSA_ERR_INVALID_ARG;
+    if (!workspace || !aligned(workspace, 256) || workspace_bytes < bsa::mask_workspace_bytes(B, H, N, d, block))
+        return BSA_ERR_WORKSPACE;
+    const int nB = N / block;
+    const int64_t R = static_cast<int64_t>(B) * H * nB;
+    bsa::MaskArgs a{};
+    a.Q = Q;
+    a.K = K;
+    a.dt = dt;
+    a.B = B;
+    a.H = H;
+    a.N = N;
+    a.d = d;
+    a.block = block;
+    a.nQB = nB;
+    a.nKB = nB;
+    a.W = (nB + 31) / 32;
+    a.spec = spec;
+    a.row_ptr = row_ptr;
+    a.col_idx = col_idx;
+    a.col_capacity = col_capacity;
+    a.bitmap = bitmap;
+    a.ws = static_cast<char *>(workspace);
+    int64_t nnz;
+    if (!spec) {
+        if (!Q || !K || !aligned(Q, 16) || !aligned(K, 16)) return BSA_ERR_INVALID_ARG;
+        if (!valid_density(density)) return BSA_ERR_INVALID_ARG;
+        if (nB > bsa::kMaxKvBlocks) return BSA_ERR_UNSUPPORTED;
+        a.k = topk_keep(density, nB);
+        nnz = R * a.k;
+    } else {
+        int64_t c = 0;
+        s = check_spec(spec, nB, &c);
+        if (s != BSA_OK) return s;
+        nnz = spec->kind == BSA_STATIC_EXPLICIT ? -1 : R / nB * c;
+    }
+    if (nnz > col_capacity) return BSA_ERR_CAPACITY;
+    if (R * nB > INT32_MAX && (nnz < 0 || nnz > INT32_MAX)) return BSA_ERR_UNSUPPORTED;  // row_ptr is int32
+    return bsa::launch_build_mask(a, static_cast<cudaStream_t>(stream));
+}
+
+bsa_status bsa_forward(const void *Q, const void *K, const void *V, int dt, int B, int H, int N, int d, int block,
+                       const int32_t *row_ptr, const int32_t *col_idx, const uint32_t *bitmap, int index_mode,
+                       float scale, void *O, float *LSE, void *workspace, size_t workspace_bytes, void *stream)
+{
+    bsa_status s = check_shape(B, H, N, d, block);
+    if (s != BSA_OK) return s;
+    if (dt != BSA_BF16 && dt != BSA_FP32) return BSA_ERR_DTYPE;
+    if (!Q || !K || !V || !O || !LSE) return BSA_ERR_INVALID_ARG;
+    if (!aligned(Q, 16) || !aligned(K, 16) || !aligned(V, 16) || !aligned(O, 16) || !aligned(LSE, 4))
+        return BSA_ERR_INVALID_ARG;
+    if (index_mode == 0) {
+        if (!row_ptr || !col_idx) return BSA_ERR_INVALID_ARG;
+    } else if (index_mode == 1) {
+        if (!bitmap) return BSA_ERR_INVALID_ARG;
+    } else {
+        return BSA_ERR_INVALID_ARG;
+    }
+    if (std::isnan(scale) || std::isinf(scale)) return BSA_ERR_INVALID_ARG;
+    if (!workspace || !aligned(workspace, 256) || workspace_bytes < bsa::fwd_workspace_bytes(B, H, N, d, block))
+        return BSA_ERR_WORKSPACE;
+    bsa::FwdArgs a{};
+    a.Q = Q;
+    a.K = K;
+    a.V = V;
+    a.dt = dt;
+    a.B = B;
+    a.H = H;
+    a.N = N;
+    a.d = d;
+    a.block = block;
+    a.nQB = N / block;
+    a.nKB = N / block;
+    a.W = (a.nKB + 31) / 32;
+    a.row_ptr = row_ptr;
+    a.col_idx = col_idx;
+    a.bitmap = bitmap;
+    a.index_mode = index_mode;
+    a.scale = scale > 0.0f ? scale : static_cast<float>(1.0 / std::sqrt(static_cast<double>(d)));
+    a.O = O;
+    a.LSE = LSE;
+    a.ws = static_cast<char *>(workspace);
+    a.dbg_flags = g_dbg_flags;
+    a.wait_limit_ns = g_wait_limit_ns;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    return dt == BSA_BF16 ? bsa::launch_forward_tc(a, st) : bsa::launch_forward_simt(a, st);
+}
+
+bsa_status bsa_check_device_error(void *workspace, void *stream)
+{
+    if (!workspace) return BSA_ERR_INVALID_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    uint32_t err = 0;
+    if (cudaMemcpyAsync(&err, workspace, sizeof(err), cudaMemcpyDeviceToHost, st) != cudaSuccess)
+        return BSA_ERR_CUDA;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return BSA_ERR_CUDA;
+    if (err != 0) {
+        if (cudaMemsetAsync(workspace, 0, sizeof(err), st) != cudaSuccess) return BSA_ERR_CUDA;
+        if (cudaStreamSynchronize(st) != cudaSuccess) return BSA_ERR_CUDA;
+    }
+    return static_cast<bsa_status>(err);
+}
+
+bsa_status bsa_validate_index(int B, int H, int N, int block, const int32_t *row_ptr, const int32_t *col_idx,
+                              const uint32_t *bitmap, void *workspace, size_t workspace_bytes, void *stream)
+{
+    if (B <= 0 || H <= 0 || N <= 0 || (block != 64 && block != 128) || N % block != 0) return BSA_ERR_SHAPE;
+    if (!row_ptr || !col_idx) return BSA_ERR_INVALID_ARG;
+    if (!workspace || !aligned(workspace, 256) || workspace_bytes < bsa::kWsHeader) return BSA_ERR_WORKSPACE;
+    const int64_t R = static_cast<int64_t>(B) * H * (N / block);
+    if (R > INT32_MAX) return BSA_ERR_SHAPE;
+    return bsa::launch_validate_index(static_cast<int>(R), N / block, row_ptr, col_idx, bitmap,
+                                      static_cast<char *>(workspace), static_cast<cudaStream_t>(stream));
+}
+
+bsa_status bsa_debug_config(uint32_t flags, uint64_t wait_limit_ns)
+{
+    g_dbg_flags = flags;
+    g_wait_limit_ns = wait_limit_ns ? wait_limit_ns : bsa::kDefaultWaitNs;
+    return BSA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,663 @@
+// fwd_tc.cu -- bf16 block-sparse FlashAttention forward on sm_103a tensor cores.
+//
+// Method: "多模态DiT中的块稀疏注意力：从原理到工程落地" §4.1 (FlashAttention tile loop
+// whose inner loop walks only active_kv_blocks[i], read from a CSR or bitmap
+// index in device memory) and §4.3 (skipped blocks count as -inf: they are never
+// visited, and the output is divided by the true sum over the active blocks).
+//
+// Design (GB300-first, not the pages' Triton/xFormers recipes):
+//   * Persistent CTAs pull 128-row query tiles from a longest-first list with an
+//     atomic counter (balances rows with very different active counts, §5.3).
+//   * Warp roles: warps 0-3 softmax + epilogue (thread = query row = TMEM lane),
+//     warp 4 TMA producer, warp 5 tcgen05 MMA issuer (one thread).
+//   * Q tile and K/V blocks arrive by TMA (128-byte swizzle), K/V fetched by
+//     block index into an NS-stage shared-memory ring.
+//   * S = Q K^T and O += P V run on tcgen05 with fp32 accumulators in TMEM.
+//     S is double-buffered so the QK^T of block n+1 overlaps the softmax of
+//     block n; P (bf16) overwrites S in TMEM and feeds the PV MMA directly.
+//   * Online softmax in the log2 domain with one FFMA + one ex2 per score;
+//     the running max is only raised (and O rescaled in TMEM) when it grows by
+//     more than 2^8, which keeps the result exact while skipping most rescales.
+//   * At block size 64 a tile holds Q blocks 2t and 2t+1 and walks the union of
+//     their lists; rows of a Q block that does not have the current KV block
+//     get P = 0 and leave their running max and sum untouched.
+//   * Every wait is bounded (BSA_ERR_TIMEOUT in the workspace, clean exit).
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <math_constants.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+#include "walk.cuh"
+
+namespace bsa {
+namespace {
+
+constexpr int kThreads = 192;
+constexpr int kTileM = 128;
+constexpr float kRescaleLog2 = 8.0f;
+constexpr uint32_t kDbgStall = 1u;
+
+struct TcParams {
+    int N, nQB, nKB, W, tiles_per_bh, n_tiles;
+    const int32_t *row_ptr;
+    const int32_t *col_idx;
+    const uint32_t *bitmap;
+    int index_mode;
+    float scale_log2;
+    __nv_bfloat16 *O;
+    float *LSE;
+    const int32_t *tile_list;
+    uint32_t *tile_counter;
+    uint32_t *err;
+    unsigned long long wait_limit_ns;
+    uint32_t dbg;
+};
+
+template <int D, int BS, int NS>
+struct Cfg {
+    static constexpr int kQBytes = kTileM * D * 2;
+    static constexpr int kKVBytes = BS * D * 2;
+    static constexpr int kQChunk = kTileM * 128;  // bytes of one 64-column swizzled slab
+    static constexpr int kKVChunk = BS * 128;
+    static constexpr int Q_OFF = 0;
+    static constexpr int K_OFF = Q_OFF + kQBytes;
+    static constexpr int V_OFF = K_OFF + NS * kKVBytes;
+    static constexpr int BAR_OFF = V_OFF + NS * kKVBytes;
+    // barrier indices
+    static constexpr int B_QFULL = 0, B_QEMPTY = 1;
+    static constexpr int B_KFULL = 2, B_VFULL = 2 + NS, B_KVEMPTY = 2 + 2 * NS;
+    static constexpr int B_SFULL = 2 + 3 * NS, B_PFULL = B_SFULL + 2, B_PVDONE = B_SFULL + 4;
+    static constexpr int B_OEMPTY = B_SFULL + 6, B_TFULL = B_OEMPTY + 1, B_TEMPTY = B_TFULL + 2;
+    static constexpr int B_DRAIN = B_TEMPTY + 2;
+    static constexpr int NBAR = B_DRAIN + 1;
+    static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
+    static constexpr int SMEM = MISC_OFF + 32;
+    static constexpr int SMEM_ALLOC = SMEM + 1024;  // manual 1024-byte alignment
+    static constexpr int TCOLS_USED = 2 * BS + D;
+    static constexpr int TCOLS = TCOLS_USED <= 256 ? 256 : 512;
+    static constexpr uint32_t IDESC_QK = idesc_bf16_f32(kTileM, BS, 0, 0);
+    static constexpr uint32_t IDESC_PV = idesc_bf16_f32(kTileM, D, 0, 1);
+};
+
+struct Ctl {
+    volatile uint32_t *abort_flag;
+    uint32_t *err;
+    unsigned long long limit;
+};
+
+// Bounded wait on an mbarrier phase. Gives up (and raises the abort flag and
+// BSA_ERR_TIMEOUT) after `limit` ns, or early when another role aborted.
+__device__ __noinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Ctl &c)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t n = 1;; ++n) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((n & 15u) == 0u) {
+            if (*c.abort_flag) return false;
+            if (globaltimer_ns() - t0 > c.limit) {
+                *c.abort_flag = 1u;
+                raise_error(c.err, BSA_ERR_TIMEOUT);
+                return false;
+            }
+        }
+    }
+}
+
+// Bounded wait used while draining in-flight async work on the way out; it
+// ignores the abort flag.
+__device__ __noinline__ bool wait_bar_drain(uint32_t bar, uint32_t parity, unsigned long long limit)
+{
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(bar, parity))
+        if (globaltimer_ns() - t0 > limit) return false;
+    return true;
+}
+
+// Warp-uniform wait: lane 0 waits, the verdict is broadcast.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const Ctl &c, int lane)
+{
+    int ok = 0;
+    if (lane == 0) ok = wait_bar(bar, parity, c) ? 1 : 0;
+    return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
+__device__ __forceinline__ void tile_coords(const TcParams &p, int tile, int64_t &bh, int &qt)
+{
+    bh = tile / p.tiles_per_bh;
+    qt = tile % p.tiles_per_bh;
+}
+
+template <int BS>
+__device__ __forceinline__ void walk_init(TileWalk &w, const TcParams &p, int64_t bh, int qt)
+{
+    if (BS == 128) {
+        w.init(p.index_mode, p.row_ptr, p.col_idx, p.bitmap, p.W, bh * p.nQB + qt, -1, 3u);
+    } else {
+        const int i0 = 2 * qt, i1 = 2 * qt + 1;
+        w.init(p.index_mode, p.row_ptr, p.col_idx, p.bitmap, p.W, bh * p.nQB + i0,
+               i1 < p.nQB ? bh * p.nQB + i1 : -1, 0u);
+    }
+}
+
+template <int D, int BS, int NS, int MINB>
+__global__ void __launch_bounds__(kThreads, MINB)
+    fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                  const __grid_constant__ CUtensorMap tmV, const TcParams p)
+{
+    using C = Cfg<D, BS, NS>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = smem_u32(smem);
+    auto bar = [&](int idx) -> uint32_t { return sbase + C::BAR_OFF + 8u * idx; };
+    uint32_t *misc = reinterpret_cast<uint32_t *>(smem + C::MISC_OFF);
+    // misc[0]: TMEM base, misc[1]: abort flag, misc[2..3]: tile ids of the scheduler ring
+    volatile int32_t *tile_ids = reinterpret_cast<volatile int32_t *>(misc + 2);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        mbar_init(bar(C::B_QFULL), 1);
+        mbar_init(bar(C::B_QEMPTY), 1);
+        for (int s = 0; s < NS; ++s) {
+            mbar_init(bar(C::B_KFULL + s), 1);
+            mbar_init(bar(C::B_VFULL + s), 1);
+            mbar_init(bar(C::B_KVEMPTY + s), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(bar(C::B_SFULL + b), 1);
+            mbar_init(bar(C::B_PFULL + b), 4);
+            mbar_init(bar(C::B_PVDONE + b), 1);
+            mbar_init(bar(C::B_TFULL + b), 1);
+            mbar_init(bar(C::B_TEMPTY + b), 5);
+        }
+        mbar_init(bar(C::B_OEMPTY), 4);
+        mbar_init(bar(C::B_DRAIN), 1);
+        misc[1] = 0u;
+        fence_mbar_init();
+    }
+    if (warp == 5) {
+        tmem_alloc(smem_u32(misc), C::TCOLS);
+        tmem_relinquish();
+    }
+    if (warp == 4 && lane == 0) {
+        tma_prefetch_map(&tmQ);
+        tma_prefetch_map(&tmK);
+        tma_prefetch_map(&tmV);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = misc[0];
+    const Ctl ctl{reinterpret_cast<volatile uint32_t *>(misc + 1), p.err, p.wait_limit_ns};
+    const bool stall = (p.dbg & kDbgStall) != 0u;
+
+    if (warp == 4) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            int G = 0, e = 0, tcount = 0;
+            int last_issue[NS];
+            for (int s = 0; s < NS; ++s) last_issue[s] = -1;
+            int q_issued = -1;
+            bool ok = true;
+            while (ok) {
+                const int slot = tcount & 1;
+                if (tcount >= 2 && !wait_bar(bar(C::B_TEMPTY + slot), ((tcount >> 1) - 1) & 1, ctl)) break;
+                const uint32_t id = atomicAdd(p.tile_counter, 1u);
+                const int tile = id < static_cast<uint32_t>(p.n_tiles) ? p.tile_list[id] : -1;
+                tile_ids[slot] = tile;
+                mbar_arrive(bar(C::B_TFULL + slot));
+                ++tcount;
+                if (tile < 0) break;
+                if (stall) continue;
+                int64_t bh;
+                int qt;
+                tile_coords(p, tile, bh, qt);
+                TileWalk walk;
+                walk_init<BS>(walk, p, bh, qt);
+                int j;
+                uint32_t m;
+                if (!walk.next(j, m)) continue;  // empty tile: nothing to load
+                if (e >= 1 && !wait_bar(bar(C::B_QEMPTY), (e - 1) & 1, ctl)) break;
+                mbar_arrive_expect_tx(bar(C::B_QFULL), C::kQBytes);
+                const int qrow = static_cast<int>(bh * p.N) + qt * kTileM;
+#pragma unroll
+                for (int c = 0; c < D / 64; ++c)
+                    tma_load_2d(sbase + C::Q_OFF + c * C::kQChunk, &tmQ, c * 64, qrow, bar(C::B_QFULL));
+                q_issued = e;
+                do {
+                    const int s = G % NS;
+                    if (G >= NS && !wait_bar(bar(C::B_KVEMPTY + s), ((G / NS) - 1) & 1, ctl)) {
+                        ok = false;
+                        break;
+                    }
+                    const int krow = static_cast<int>(bh * p.N) + j * BS;
+                    mbar_arrive_expect_tx(bar(C::B_KFULL + s), C::kKVBytes);
+#pragma unroll
+                    for (int c = 0; c < D / 64; ++c)
+                        tma_load_2d(sbase + C::K_OFF + s * C::kKVBytes + c * C::kKVChunk, &tmK, c * 64, krow,
+                                    bar(C::B_KFULL + s));
+                    mbar_arrive_expect_tx(bar(C::B_VFULL + s), C::kKVBytes);
+#pragma unroll
+                    for (int c = 0; c < D / 64; ++c)
+                        tma_load_2d(sbase + C::V_OFF + s * C::kKVBytes + c * C::kKVChunk, &tmV, c * 64, krow,
+                                    bar(C::B_VFULL + s));
+                    last_issue[s] = G;
+                    ++G;
+                } while (walk.next(j, m));
+                ++e;
+            }
+            if (*ctl.abort_flag) {
+                // never leave while our copies may still land in shared memory
+                for (int s = 0; s < NS; ++s)
+                    if (last_issue[s] >= 0) {
+                        wait_bar_drain(bar(C::B_KFULL + s), (last_issue[s] / NS) & 1, p.wait_limit_ns);
+                        wait_bar_drain(bar(C::B_VFULL + s), (last_issue[s] / NS) & 1, p.wait_limit_ns);
+                    }
+                if (q_issued >= 0) wait_bar_drain(bar(C::B_QFULL), q_issued & 1, p.wait_limit_ns);
+            }
+        }
+    } else if (warp == 5) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0 && !stall) {
+            const uint32_t tS = tmem;             // two S/P buffers of BS columns
+            const uint32_t tO = tmem + 2 * BS;    // O accumulator, D columns
+            int G = 0, e = 0, tcount = 0;
+            bool ok = true;
+            auto issue_pv = [&](int t, bool first) -> bool {
+                const int b = t & 1, s = t % NS;
+                if (!wait_bar(bar(C::B_PFULL + b), (t >> 1) & 1, ctl)) return false;
+                if (!wait_bar(bar(C::B_VFULL + s), (t / NS) & 1, ctl)) return false;
+                if (first && e >= 1 && !wait_bar(bar(C::B_OEMPTY), (e - 1) & 1, ctl)) return false;
+                tc_fence_after();
+                const uint32_t vbase = sbase + C::V_OFF + s * C::kKVBytes;
+#pragma unroll
+                for (int kk = 0; kk < BS / 16; ++kk) {
+                    const uint64_t bdesc = sdesc_sw128(vbase + kk * 16 * 128, C::kKVChunk, 1024);
+                    mma_ts(tO, tS + b * BS + kk * 8, bdesc, C::IDESC_PV, (first && kk == 0) ? 0u : 1u);
+                }
+                tc_commit(bar(C::B_PVDONE + b));
+                tc_commit(bar(C::B_KVEMPTY + s));
+                return true;
+            };
+            while (ok) {
+                const int slot = tcount & 1;
+                if (!wait_bar(bar(C::B_TFULL + slot), (tcount >> 1) & 1, ctl)) break;
+                const int tile = tile_ids[slot];
+                mbar_arrive(bar(C::B_TEMPTY + slot));
+                ++tcount;
+                if (tile < 0) break;
+                int64_t bh;
+                int qt;
+                tile_coords(p, tile, bh, qt);
+                TileWalk walk;
+                walk_init<BS>(walk, p, bh, qt);
+                int j;
+                uint32_t m;
+                if (!walk.next(j, m)) continue;
+                if (!wait_bar(bar(C::B_QFULL), e & 1, ctl)) break;
+                tc_fence_after();
+                const int G0 = G;
+                do {
+                    const int s = G % NS, b = G & 1;
+                    if (!wait_bar(bar(C::B_KFULL + s), (G / NS) & 1, ctl)) { ok = false; break; }
+                    if (G >= 2 && !wait_bar(bar(C::B_PVDONE + b), ((G - 2) >> 1) & 1, ctl)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t kbase = sbase + C::K_OFF + s * C::kKVBytes;
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const int c = kk >> 2, off = (kk & 3) * 32;
+                        const uint64_t adesc = sdesc_sw128(sbase + C::Q_OFF + c * C::kQChunk + off, 16, 1024);
+                        const uint64_t bdesc = sdesc_sw128(kbase + c * C::kKVChunk + off, 16, 1024);
+                        mma_ss(tS + b * BS, adesc, bdesc, C::IDESC_QK, kk > 0 ? 1u : 0u);
+                    }
+                    tc_commit(bar(C::B_SFULL + b));
+                    if (G > G0 && !issue_pv(G - 1, G - 1 == G0)) { ok = false; break; }
+                    ++G;
+                } while (walk.next(j, m));
+                if (!ok) break;
+                tc_commit(bar(C::B_QEMPTY));
+                if (!issue_pv(G - 1, G - 1 == G0)) break;
+                ++e;
+            }
+            // all MMAs issued by this thread have completed before TMEM is freed
+            tc_commit(bar(C::B_DRAIN));
+            wait_bar_drain(bar(C::B_DRAIN), 0, p.wait_limit_ns);
+        }
+    } else {
+        // ------------------------------------------------------------ softmax + epilogue (warps 0-3)
+        const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+        const uint32_t tS = tmem + lane_base;
+        const uint32_t tO = tmem + lane_base + 2 * BS;
+        const uint32_t half = BS == 128 ? 0u : static_cast<uint32_t>(warp >> 1);
+        int G = 0, e = 0, tcount = 0;
+        bool ok = true;
+        while (ok) {
+            const int slot = tcount & 1;
+            if (!warp_wait(bar(C::B_TFULL + slot), (tcount >> 1) & 1, ctl, lane)) break;
+            int tile = 0;
+            if (lane == 0) {
+                tile = tile_ids[slot];
+                mbar_arrive(bar(C::B_TEMPTY + slot));
+            }
+            tile = __shfl_sync(0xffffffffu, tile, 0);
+            ++tcount;
+            if (tile < 0) break;
+            int64_t bh;
+            int qt;
+            tile_coords(p, tile, bh, qt);
+            const int row = qt * kTileM + warp * 32 + lane;
+            const bool row_valid = row < p.N;
+            const int64_t grow = bh * p.N + row;
+            TileWalk walk;
+            walk_init<BS>(walk, p, bh, qt);
+            int j;
+            uint32_t m;
+            if (!walk.next(j, m)) {
+                // no active block anywhere in the tile: O = 0, LSE = -inf
+                if (row_valid) {
+                    uint4 z = make_uint4(0u, 0u, 0u, 0u);
+                    uint4 *dst = reinterpret_cast<uint4 *>(p.O + grow * D);
+#pragma unroll
+                    for (int c = 0; c < D / 8; ++c) dst[c] = z;
+                    p.LSE[grow] = -CUDART_INF_F;
+                }
+                continue;
+            }
+            // l_run: sum of the fp32 probabilities (for LSE); lp_run: sum of the bf16
+            // probabilities the PV MMA consumes (normaliser of O, so rounding of P
+            // cancels between numerator and denominator)
+            float m_run = -CUDART_INF_F, l_run = 0.0f, lp_run = 0.0f;
+            do {
+                const int b = G & 1;
+                if (!warp_wait(bar(C::B_SFULL + b), (G >> 1) & 1, ctl, lane)) { ok = false; break; }
+                tc_fence_after();
+                const bool active = ((m >> half) & 1u) != 0u;
+                bool resc = false;
+                float alpha = 1.0f;
+                if (active) {
+                    uint32_t sv[BS / 32][32];
+#pragma unroll
+                    for (int c = 0; c < BS / 32; ++c) tmem_ld32(tS + b * BS + c * 32, sv[c]);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int c = 0; c < BS / 32; ++c) reg_fence32(sv[c]);
+                    float mx = -CUDART_INF_F;
+#pragma unroll
+                    for (int c = 0; c < BS / 32; ++c)
+#pragma unroll
+                        for (int t = 0; t < 32; ++t) mx = fmaxf(mx, __uint_as_float(sv[c][t]));
+                    const float m_tile = mx * p.scale_log2;
+                    if (m_run == -CUDART_INF_F) {
+                        m_run = m_tile;
+                    } else if (m_tile > m_run + kRescaleLog2) {
+                        alpha = ex2_approx(m_run - m_tile);
+                        l_run *= alpha;
+                        lp_run *= alpha;
+                        m_run = m_tile;
+                        resc = true;
+                    }
+                    const float neg_m = -m_run;
+                    float sum = 0.0f, sum_p = 0.0f;
+#pragma unroll
+                    for (int c2 = 0; c2 < BS / 64; ++c2) {
+                        uint32_t pk[32];
+#pragma unroll
+                        for (int q = 0; q < 32; ++q) {
+                            const int k0 = c2 * 64 + 2 * q;
+                            const float p0 =
+                                ex2_approx(fmaf(__uint_as_float(sv[k0 >> 5][k0 & 31]), p.scale_log2, neg_m));
+                            const float p1 = ex2_approx(
+                                fmaf(__uint_as_float(sv[(k0 + 1) >> 5][(k0 + 1) & 31]), p.scale_log2, neg_m));
+                            sum += p0 + p1;
+                            pk[q] = pack_bf16x2(p0, p1);
+                            sum_p += __uint_as_float(pk[q] << 16) + __uint_as_float(pk[q] & 0xFFFF0000u);
+                        }
+                        tmem_st32(tS + b * BS + c2 * 32, pk);
+                    }
+                    l_run += sum;
+                    lp_run += sum_p;
+                } else {
+                    uint32_t z[32];
+#pragma unroll
+                    for (int q = 0; q < 32; ++q) z[q] = 0u;
+#pragma unroll
+                    for (int c2 = 0; c2 < BS / 64; ++c2) tmem_st32(tS + b * BS + c2 * 32, z);
+                }
+                if (__any_sync(0xffffffffu, resc)) {
+                    // O holds the previous blocks' sum: rescale it once the last PV landed
+                    const int t = G - 1;
+                    if (!warp_wait(bar(C::B_PVDONE + (t & 1)), (t >> 1) & 1, ctl, lane)) { ok = false; break; }
+                    tc_fence_after();
+#pragma unroll
+                    for (int c = 0; c < D / 32; ++c) {
+                        uint32_t ov[32];
+                        tmem_ld32(tO + c * 32, ov);
+                        tmem_wait_ld();
+                        reg_fence32(ov);
+#pragma unroll
+                        for (int q = 0; q < 32; ++q) ov[q] = __float_as_uint(__uint_as_float(ov[q]) * alpha);
+                        tmem_st32(tO + c * 32, ov);
+                    }
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(C::B_PFULL + b));
+                ++G;
+            } while (walk.next(j, m));
+            if (!ok) break;
+            // ---------------- epilogue: O / l, LSE = ln2 * (m + log2 l)
+            const int t = G - 1;
+            if (!warp_wait(bar(C::B_PVDONE + (t & 1)), (t >> 1) & 1, ctl, lane)) break;
+            tc_fence_after();
+            const float inv_l = lp_run > 0.0f ? 1.0f / lp_run : 0.0f;
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t ov[32];
+                tmem_ld32(tO + c * 32, ov);
+                tmem_wait_ld();
+                reg_fence32(ov);
+                if (row_valid) {
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int q = 0; q < 16; ++q)
+                        pk[q] = pack_bf16x2(__uint_as_float(ov[2 * q]) * inv_l, __uint_as_float(ov[2 * q + 1]) * inv_l);
+                    uint4 *dst = reinterpret_cast<uint4 *>(p.O + grow * D + c * 32);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) dst[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(C::B_OEMPTY));
+            if (row_valid)
+                p.LSE[grow] = l_run > 0.0f ? (m_run + log2f(l_run)) * 0.69314718055994530942f : -CUDART_INF_F;
+            ++e;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 5) {
+        tc_fence_after();
+        tmem_dealloc(tmem, C::TCOLS);
+    }
+}
+
+// ---------------------------------------------------------------- tile order
+
+constexpr int kBuckets = 1024;
+
+__device__ __forceinline__ int tile_length(const TcParams &p, int tile, int BS)
+{
+    const int64_t bh = tile / p.tiles_per_bh;
+    const int qt = tile % p.tiles_per_bh;
+    const int nrows = BS == 128 ? 1 : 2;
+    int len = 0;
+    for (int h = 0; h < nrows; ++h) {
+        const int i = BS == 128 ? qt : 2 * qt + h;
+        if (i >= p.nQB) break;
+        const int64_t r = bh * p.nQB + i;
+        if (p.index_mode == 0) {
+            len += p.row_ptr[r + 1] - p.row_ptr[r];
+        } else {
+            for (int w = 0; w < p.W; ++w) len += __popc(p.bitmap[r * p.W + w]);
+        }
+    }
+    return len;
+}
+
+// Longest-first tile list (counting sort by active-block count, clamped) and
+// reset of the scheduler counter. One CTA.
+__global__ void __launch_bounds__(1024) tile_order_kernel(TcParams p, int BS, int32_t *tile_list)
+{
+    __shared__ int hist[kBuckets];
+    __shared__ int wsum[32];
+    const int t = threadIdx.x;
+    for (int b = t; b < kBuckets; b += 1024) hist[b] = 0;
+    __syncthreads();
+    for (int tile = t; tile < p.n_tiles; tile += 1024) {
+        const int len = min(tile_length(p, tile, BS), kBuckets - 1);
+        atomicAdd(&hist[kBuckets - 1 - len], 1);
+    }
+    __syncthreads();
+    // exclusive scan of hist (one bucket per thread)
+    const int v = hist[t];
+    int x = v;
+    const int lane = t & 31, warp = t >> 5;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) wsum[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        int s = wsum[lane];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, s, o);
+            if (lane >= o) s += y;
+        }
+        wsum[lane] = s;
+    }
+    __syncthreads();
+    const int excl = x - v + (warp > 0 ? wsum[warp - 1] : 0);
+    __syncthreads();
+    hist[t] = excl;
+    __syncthreads();
+    for (int tile = t; tile < p.n_tiles; tile += 1024) {
+        const int len = min(tile_length(p, tile, BS), kBuckets - 1);
+        const int pos = atomicAdd(&hist[kBuckets - 1 - len], 1);
+        tile_list[pos] = tile;
+    }
+    if (t == 0) *p.tile_counter = 0u;
+}
+
+// ---------------------------------------------------------------- host side
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn()
+{
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    }
+    return fn;
+}
+
+// 2-D view [rows][d] of a bf16 tensor, 64-column x box_rows boxes, 128-byte swizzle.
+bool make_map(CUtensorMap *m, const void *base, uint64_t rows, int d, int box_rows)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(d) * 2};
+    const cuuint32_t box[2] = {64u, static_cast<cuuint32_t>(box_rows)};
+    const cuuint32_t es[2] = {1u, 1u};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int D, int BS, int NS, int MINB>
+bsa_status launch_tc(const FwdArgs &a, cudaStream_t st)
+{
+    using C = Cfg<D, BS, NS>;
+    static_assert(C::SMEM_ALLOC <= 227 * 1024, "shared memory budget");
+    auto kern = fwd_tc_kernel<D, BS, NS, MINB>;
+    static int grid_cap = 0;
+    if (grid_cap == 0) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC) != cudaSuccess)
+            return BSA_ERR_CUDA;
+        int dev = 0, sms = 0, occ = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess) return BSA_ERR_CUDA;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return BSA_ERR_CUDA;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kThreads, C::SMEM_ALLOC) != cudaSuccess)
+            return BSA_ERR_CUDA;
+        if (occ < 1) return BSA_ERR_UNSUPPORTED;
+        const int by_tmem = 512 / C::TCOLS;  // CTAs whose TMEM allocations fit one SM
+        grid_cap = sms * (occ < by_tmem ? occ : by_tmem);
+    }
+    const int64_t BH = static_cast<int64_t>(a.B) * a.H;
+    const uint64_t rows = static_cast<uint64_t>(BH) * a.N;
+    CUtensorMap mq, mk, mv;
+    if (!make_map(&mq, a.Q, rows, D, kTileM) || !make_map(&mk, a.K, rows, D, BS) || !make_map(&mv, a.V, rows, D, BS))
+        return BSA_ERR_CUDA;
+    WsHeader *hdr = reinterpret_cast<WsHeader *>(a.ws);
+    TcParams p{};
+    p.N = a.N;
+    p.nQB = a.nQB;
+    p.nKB = a.nKB;
+    p.W = a.W;
+    p.tiles_per_bh = (a.N + kTileM - 1) / kTileM;
+    p.n_tiles = static_cast<int>(BH * p.tiles_per_bh);
+    p.row_ptr = a.row_ptr;
+    p.col_idx = a.col_idx;
+    p.bitmap = a.bitmap;
+    p.index_mode = a.index_mode;
+    p.scale_log2 = a.scale * 1.4426950408889634f;
+    p.O = static_cast<__nv_bfloat16 *>(a.O);
+    p.LSE = a.LSE;
+    p.tile_list = reinterpret_cast<const int32_t *>(a.ws + kWsHeader);
+    p.tile_counter = &hdr->tile_counter;
+    p.err = &hdr->err;
+    p.wait_limit_ns = a.wait_limit_ns;
+    p.dbg = a.dbg_flags;
+    tile_order_kernel<<<1, 1024, 0, st>>>(p, BS, reinterpret_cast<int32_t *>(a.ws + kWsHeader));
+    const int grid = static_cast<int>(p.n_tiles < grid_cap ? p.n_tiles : grid_cap);
+    kern<<<grid, kThreads, C::SMEM_ALLOC, st>>>(mq, mk, mv, p);
+    return cudaGetLastError() == cudaSuccess ? BSA_OK : BSA_ERR_CUDA;
+}
+
+}  // namespace
+
+size_t fwd_workspace_bytes(int B, int H, int N, int d, int block)
+{
+    (void)d;
+    (void)block;
+    const size_t tiles = static_cast<size_t>(B) * H * ((N + kTileM - 1) / kTileM);
+    return kWsHeader + align_up(tiles * sizeof(int32_t), 256);
+}
+
+bsa_status launch_forward_tc(const FwdArgs &a, cudaStream_t st)
+{
+    if (a.d == 64 && a.block == 64) return launch_tc<64, 64, 4, 2>(a, st);
+    if (a.d == 128 && a.block == 64) return launch_tc<128, 64, 2, 2>(a, st);
+    if (a.d == 64 && a.block == 128) return launch_tc<64, 128, 3, 1>(a, st);
+    if (a.d == 128 && a.block == 128) return launch_tc<128, 128, 2, 1>(a, st);
+    return BSA_ERR_SHAPE;
+}
+
+}  // namespace bsa

@@ -1,0 +1,71 @@
+// internal.h -- declarations shared by the host API (api.cu) and the kernel
+// translation units. Not part of the public C ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cstddef>
+#include <cstdint>
+
+#include "../../include/bsa.h"
+
+namespace bsa {
+
+// Workspace header (first 256 bytes of every workspace).
+struct WsHeader {
+    uint32_t err;          // first device-raised bsa_status (0 = none)
+    uint32_t tile_counter; // forward: dynamic tile scheduler counter
+    uint32_t pad[62];
+};
+static_assert(sizeof(WsHeader) == 256, "workspace header is 256 bytes");
+
+constexpr size_t kWsHeader = 256;
+constexpr int kMaxKvBlocks = 4096;     // nKB limit of the selector (scores row in smem)
+constexpr uint64_t kDefaultWaitNs = 2000000000ull;  // bounded device waits: 2 s
+
+// Records `code` as the workspace's device error unless one is already set.
+__device__ __forceinline__ void raise_error(uint32_t *err, uint32_t code)
+{
+    atomicCAS(err, 0u, code);
+}
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// ------------------------------------------------------------ mask builder
+struct MaskArgs {
+    const void *Q, *K;
+    int dt, B, H, N, d, block;
+    int nQB, nKB, W;       // blocks per row/column, bitmap words per row
+    int k;                 // dynamic: blocks kept per row
+    const bsa_static_spec *spec;  // host copy (NULL -> dynamic)
+    int32_t *row_ptr, *col_idx;
+    int64_t col_capacity;
+    uint32_t *bitmap;
+    char *ws;              // workspace base (device)
+};
+
+size_t mask_workspace_bytes(int B, int H, int N, int d, int block);
+bsa_status launch_build_mask(const MaskArgs &a, cudaStream_t st);
+bsa_status launch_validate_index(int R, int nKB, const int32_t *row_ptr, const int32_t *col_idx,
+                                 const uint32_t *bitmap, char *ws, cudaStream_t st);
+
+// ------------------------------------------------------------ forward
+struct FwdArgs {
+    const void *Q, *K, *V;
+    int dt, B, H, N, d, block;
+    int nQB, nKB, W;
+    const int32_t *row_ptr, *col_idx;
+    const uint32_t *bitmap;
+    int index_mode;
+    float scale;           // > 0
+    void *O;
+    float *LSE;
+    char *ws;
+    uint32_t dbg_flags;
+    uint64_t wait_limit_ns;
+};
+
+size_t fwd_workspace_bytes(int B, int H, int N, int d, int block);
+bsa_status launch_forward_tc(const FwdArgs &a, cudaStream_t st);    // bf16, tcgen05
+bsa_status launch_forward_simt(const FwdArgs &a, cudaStream_t st);  // fp32, CUDA cores
+
+}  // namespace bsa

@@ -247,3 +247,17 @@ def make_inputs(w: Workload) -> dict:
     out["mask"] = explicit_block_mask(w)
     return out
 
+
+
+def pack_bitmap_words(mask: np.ndarray) -> np.ndarray:
+    """Explicit block mask -> the bitmap input format of the static explicit spec.
+
+    uint8 [..., nKB] -> int32 words [..., ceil(nKB/32)]; bit j % 32 of word j / 32
+    is block j.
+    """
+    nKB = mask.shape[-1]
+    W = (nKB + 31) // 32
+    pad = np.zeros((*mask.shape[:-1], W * 32), np.uint64)
+    pad[..., :nKB] = mask
+    words = (pad.reshape(*mask.shape[:-1], W, 32) << np.arange(32, dtype=np.uint64)).sum(-1)
+    return words.astype(np.uint32).view(np.int32)

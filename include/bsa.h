@@ -1,0 +1,182 @@
+/*
+ * bsa.h -- C ABI of the GB300 block-sparse attention forward library (libbsa.so).
+ *
+ * The library computes, on one GPU (sm_103a), the hot path described in
+ *   [P1] "多模态DiT中的块稀疏注意力：从原理到工程落地"
+ *   [P3] "Can sparse attention close the quality gap in diffusion transformers"
+ * in two calls:
+ *   bsa_build_mask  -- block mask -> per-Q-block active KV block lists (CSR) + bitmap
+ *   bsa_forward     -- block-sparse FlashAttention forward over those lists -> O, LSE
+ *
+ * Conventions shared by every call
+ *   - Q, K, V, O are row-major [B][H][N][d], contiguous, in device memory.
+ *     dtype BSA_BF16 (bf16 inputs, bf16 O) or BSA_FP32 (fp32 inputs, fp32 O).
+ *     LSE is fp32 [B][H][N], natural logarithm.
+ *   - block (bs) in {64, 128}; d in {64, 128}; N % block == 0; nQB = nKB = N / block.
+ *   - Index: rows r = (b*H + h)*nQB + i.
+ *       row_ptr  int32 [B*H*nQB + 1], exclusive prefix sums of row lengths;
+ *       col_idx  int32 [nnz], the active KV block ids of each row, strictly ascending;
+ *       bitmap   uint32 [B*H*nQB][W], W = ceil(nKB / 32); bit (j % 32) of word j / 32
+ *                is set iff KV block j is active for the row.
+ *   - Ownership: the caller allocates and owns every buffer (device memory for
+ *     tensors, index and workspace). No call allocates, frees or synchronises
+ *     except bsa_check_device_error, which synchronises `stream`.
+ *   - Streams: device work is enqueued on `stream` (a cudaStream_t; NULL = legacy
+ *     default stream) and runs asynchronously.
+ *   - Errors: argument checks run on the host before any launch; a failed check
+ *     returns its status and enqueues nothing. Conditions only the device can see
+ *     (a NaN block score, a capacity overflow of an explicit bitmap, a bounded wait
+ *     that gave up) are recorded in the first bytes of the call's workspace and are
+ *     returned by bsa_check_device_error on that workspace.
+ *   - Workspaces are caller-provided device buffers of at least the size
+ *     bsa_workspace_size reports; they must be 256-byte aligned.
+ *   - Calls that share a workspace, or write the same outputs, must not overlap
+ *     on the GPU (put them on one stream or order them with events).
+ */
+#ifndef BSA_H_
+#define BSA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    BSA_OK = 0,
+    BSA_ERR_INVALID_ARG = 1, /* null pointer, bad enum, density out of (0, 1], misaligned buffer */
+    BSA_ERR_SHAPE = 2,       /* unsupported B, H, N, d or block, or N % block != 0 */
+    BSA_ERR_DTYPE = 3,       /* dtype not supported for this call */
+    BSA_ERR_CAPACITY = 4,    /* col_capacity smaller than the mask's nnz */
+    BSA_ERR_NONFINITE = 5,   /* a block score was NaN (device-raised) */
+    BSA_ERR_TIMEOUT = 6,     /* a bounded device wait gave up (device-raised) */
+    BSA_ERR_CUDA = 7,        /* a CUDA runtime call failed */
+    BSA_ERR_UNSUPPORTED = 8, /* valid request this build does not implement */
+    BSA_ERR_WORKSPACE = 9    /* workspace null or smaller than bsa_workspace_size */
+} bsa_status;
+
+typedef enum { BSA_BF16 = 0, BSA_FP32 = 1 } bsa_dtype;
+
+typedef enum {
+    BSA_STATIC_EXPLICIT = 0,      /* a caller-given block bitmap */
+    BSA_STATIC_MODALITY_BAND = 1, /* [P1] §3.1-§3.2: text dense + image band + anchors */
+    BSA_STATIC_CUBOID = 2         /* [P1] §3.2: video cuboids + face neighbours + text */
+} bsa_static_kind;
+
+#define BSA_MAX_ANCHORS 8
+
+/* A static block mask ([P1] §2.3: fixed before the run, from the task's structure).
+ * Leading `n_text_blocks` blocks are text: their rows and columns are dense
+ * ([P1] §3.1: text-text dense, text is a global condition for every image block). */
+typedef struct {
+    int kind;                     /* bsa_static_kind */
+    const uint32_t *bitmap;       /* EXPLICIT: device bitmap, layout as the index bitmap:
+                                     [B*H*nQB][W], or [nQB][W] when broadcast_bh != 0 */
+    int broadcast_bh;             /* EXPLICIT: 1 = one nQB x nKB mask for every (b, h) */
+    int n_text_blocks;            /* MODALITY_BAND, CUBOID: leading text blocks */
+    int band;                     /* MODALITY_BAND: image block rows r, cols c active iff |r-c| <= band */
+    int n_anchors;                /* MODALITY_BAND: number of anchor image blocks (<= 8) */
+    int anchors[BSA_MAX_ANCHORS]; /* MODALITY_BAND: image-block ids dense in both directions */
+    int grid_t, grid_h, grid_w;   /* CUBOID: cuboid grid; image blocks are cuboids in t-major
+                                     raster order, active iff equal or sharing a face */
+} bsa_static_spec;
+
+/*
+ * bsa_build_mask -- build the block mask and emit both index forms.
+ *
+ * Dynamic (spec == NULL): the naive block-sparse selector of [P3] (section on
+ * mean-pooled block scoring): each Q and K block is mean-pooled, every
+ * (Q block i, KV block j) pair is scored by the dot product of the pooled
+ * vectors, and each Q block keeps its k = max(1, floor(density * nKB)) best KV
+ * blocks ([P1] §5.3: a per-Q-block target count). Exact arithmetic, so results
+ * are reproducible bit for bit: pooled sums run over the block's tokens in order
+ * in fp32 round-to-nearest, scaled by 1/block; scores are an fmaf chain over
+ * channels 0..d-1 starting at +0; ranking is by value descending with -0 == +0 and
+ * ties going to the lower block index. A NaN score raises BSA_ERR_NONFINITE on
+ * the device (the emitted index is then unspecified).
+ *
+ * Static (spec != NULL): evaluates the spec's block predicate ([P1] §2.3, §3.1,
+ * §3.2, pre-generated on the GPU as §5.3 recommends) for every (b, h).
+ *
+ *   Q, K            device [B][H][N][d], dtype dt; read only in dynamic mode (may be
+ *                   NULL in static mode)
+ *   density         dynamic mode: in (0, 1]; ignored in static mode
+ *   row_ptr         device int32 [B*H*nQB + 1] (written)
+ *   col_idx         device int32 [col_capacity] (first nnz entries written)
+ *   col_capacity    entries available in col_idx; must be >= nnz. For dynamic,
+ *                   band and cuboid masks nnz is known on the host
+ *                   (bsa_mask_nnz) and a short capacity returns BSA_ERR_CAPACITY
+ *                   without launching; for EXPLICIT masks the device checks and
+ *                   raises BSA_ERR_CAPACITY (writes stay within capacity).
+ *   bitmap          device uint32 [B*H*nQB][W] (written)
+ *   workspace       device, >= bsa_workspace_size(0, ...) bytes, 256-byte aligned
+ */
+bsa_status bsa_build_mask(const void *Q, const void *K, int dt, int B, int H, int N, int d,
+                          int block, float density, const bsa_static_spec *spec,
+                          int32_t *row_ptr, int32_t *col_idx, int64_t col_capacity,
+                          uint32_t *bitmap, void *workspace, size_t workspace_bytes,
+                          void *stream);
+
+/*
+ * bsa_forward -- block-sparse FlashAttention forward ([P1] §4.1 tile loop with the
+ * inner KV loop replaced by the active list, §4.3 skipped blocks count as -inf and
+ * the output is normalised by the true sum over active blocks only).
+ *
+ * For each (b, h) and query row r of Q block i, with A(i) the active KV blocks:
+ *   s_rc = scale * q_r . k_c for keys c in blocks of A(i);
+ *   O_r  = sum_c exp(s_rc) v_c / sum_c exp(s_rc);   LSE_r = ln sum_c exp(s_rc).
+ * A row with no active block gets O_r = 0 and LSE_r = -inf.
+ *
+ *   Q, K, V     device [B][H][N][d], dtype dt
+ *   row_ptr, col_idx   CSR index (read when index_mode == 0)
+ *   bitmap      bitmap index (read when index_mode == 1); unused pointers may be NULL
+ *   index_mode  0: CSR, 1: bitmap + popcount ([P1] §4.1)
+ *   scale       softmax scale; <= 0 selects 1/sqrt(d)
+ *   O           device [B][H][N][d], dtype dt (written)
+ *   LSE         device fp32 [B][H][N] (written)
+ *   workspace   device, >= bsa_workspace_size(1, ...) bytes, 256-byte aligned
+ * The index must be well formed (row_ptr non-decreasing from 0, col_idx strictly
+ * ascending in [0, nKB)); bsa_validate_index checks one on the device.
+ */
+bsa_status bsa_forward(const void *Q, const void *K, const void *V, int dt, int B, int H, int N,
+                       int d, int block, const int32_t *row_ptr, const int32_t *col_idx,
+                       const uint32_t *bitmap, int index_mode, float scale, void *O, float *LSE,
+                       void *workspace, size_t workspace_bytes, void *stream);
+
+/* Host-only: number of active blocks the builder will emit for these arguments.
+ * Dynamic: B*H*nQB*k. MODALITY_BAND / CUBOID: exact count times B*H.
+ * EXPLICIT: the bitmap lives on the device, so the upper bound B*H*nQB*nKB. */
+bsa_status bsa_mask_nnz(int B, int H, int N, int block, float density,
+                        const bsa_static_spec *spec, int64_t *nnz);
+
+/* Host-only: workspace bytes for which = 0 (bsa_build_mask) or 1 (bsa_forward). */
+bsa_status bsa_workspace_size(int which, int B, int H, int N, int d, int block, size_t *bytes);
+
+/* Synchronises `stream`, returns the device-raised status recorded in `workspace`
+ * by earlier calls (BSA_OK if none), and clears it. */
+bsa_status bsa_check_device_error(void *workspace, void *stream);
+
+/* Checks an index on the device: row_ptr[0] == 0 and non-decreasing, col_idx
+ * strictly ascending within each row and < nKB, and (when bitmap != NULL) each
+ * row's bitmap popcount equals its CSR length with the same bits. A violation is
+ * recorded as BSA_ERR_INVALID_ARG in `workspace` (read it with
+ * bsa_check_device_error). */
+bsa_status bsa_validate_index(int B, int H, int N, int block, const int32_t *row_ptr,
+                              const int32_t *col_idx, const uint32_t *bitmap, void *workspace,
+                              size_t workspace_bytes, void *stream);
+
+/* Diagnostics for tests: `flags` bit 0 makes the next bsa_forward launches skip
+ * their loads and MMAs so the softmax warps' first wait runs out (nothing is in
+ * flight); `wait_limit_ns` bounds every device wait (0 restores the default of
+ * 2 s). Host-global; not thread safe. */
+bsa_status bsa_debug_config(uint32_t flags, uint64_t wait_limit_ns);
+
+/* Static string for a status code. */
+const char *bsa_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BSA_H_ */

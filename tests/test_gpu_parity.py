@@ -1,0 +1,248 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle.
+
+Index (bitmap, row_ptr, col_idx) must match bit for bit; O within max-abs 2e-2
+and mean-abs 2e-3, LSE within 1e-3 (bf16 inputs, fp32 accumulation). Small
+cases compare every row; the full-size workloads compare a seeded sample of
+rows plus the whole index.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from block_sparse_attention_mean_gb300 import binding as bb
+from block_sparse_attention_mean_gb300 import build as bbuild
+from block_sparse_attention_mean_gb300 import workloads as wl
+from tests import gpu_util as gu
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    bbuild.build()
+    bb.load()
+    bb.bsa_debug_config(0, 0)
+
+
+def run_workload(w, index_mode=None, rows=None, scale=None):
+    inp = wl.make_inputs(w)
+    q, k, v = (gu.upload(inp, n) for n in ("q", "k", "v"))
+    mask = gu.oracle_mask(w, inp)
+    idx = gu.device_index(w, q, k, mask)
+    gu.assert_index_equal(idx, mask)
+    mode = w.index_mode if index_mode is None else index_mode
+    O, L = bb.forward(q, k, v, idx, index_mode=mode, scale=0.0 if scale is None else scale)
+    torch.cuda.synchronize()
+    return gu.assert_attention_close(O, L, inp, mask, w, rows=rows, scale=scale)
+
+
+# ------------------------------------------------------------ small, all rows
+
+
+def test_tiny_fp32_explicit():
+    run_workload(wl.WORKLOADS["tiny"])
+
+
+def test_tiny_bf16_both_index_modes():
+    w = wl.scaled(wl.WORKLOADS["tiny"], dtype="bf16")
+    run_workload(w, index_mode=0)
+    run_workload(w, index_mode=1)
+
+
+def test_t2i_two_heads_all_rows():
+    run_workload(wl.scaled(wl.WORKLOADS["t2i_static"], B=1, H=2))
+
+
+def test_t2i_ragged_tile_tail_all_rows():
+    # 67 blocks of 64: the last 128-row tile holds a single Q block
+    w = wl.scaled(wl.WORKLOADS["t2i_static"], B=1, H=2, N=64 * 67)
+    run_workload(w)
+
+
+def test_dynamic_topk_small_all_rows():
+    run_workload(wl.scaled(wl.WORKLOADS["dynamic_topk"], H=2, N=2048))
+
+
+def test_long_block128_small_all_rows():
+    run_workload(wl.scaled(wl.WORKLOADS["long_topk"], H=2, N=4096))
+
+
+def test_video_small_grid_all_rows():
+    w = wl.scaled(wl.WORKLOADS["video_cuboid"], H=2, N=256 + 8 * 16 * 16, grid=(2, 4, 4),
+                  video_shape=(8, 16, 16))
+    run_workload(w)
+
+
+@pytest.mark.parametrize("d,block,mode", [(64, 128, 0), (64, 128, 1), (128, 64, 1), (64, 64, 1)])
+def test_shape_combinations(d, block, mode):
+    w = wl.scaled(wl.WORKLOADS["long_topk"], H=3, N=2048, d=d, block=block, density=0.3)
+    run_workload(w, index_mode=mode)
+
+
+def test_custom_scale():
+    w = wl.scaled(wl.WORKLOADS["dynamic_topk"], H=1, N=1024)
+    run_workload(w, scale=0.05)
+
+
+def test_single_block_sequences():
+    for block in (64, 128):
+        w = wl.scaled(wl.WORKLOADS["tiny"], dtype="bf16", N=block, block=block, d=128)
+        run_workload(w)
+    w = wl.scaled(wl.WORKLOADS["tiny"], dtype="bf16", N=128, block=64)
+    run_workload(w)
+
+
+def test_empty_and_full_rows():
+    w = wl.scaled(wl.WORKLOADS["tiny"], dtype="bf16", H=3, N=1024, d=128)
+    inp = wl.make_inputs(w)
+    mask = inp["mask"].copy()
+    mask[0, 0, 3, :] = 0          # one empty Q block (its tile partner is not empty)
+    mask[0, 1, 4:6, :] = 0        # a whole empty 128-row tile
+    mask[0, 2, :, :] = 0          # a head with one full row block and one single-block row
+    mask[0, 2, 0, :] = 1
+    mask[0, 2, 7, 15] = 1
+    inp["mask"] = mask
+    q, k, v = (gu.upload(inp, n) for n in ("q", "k", "v"))
+    for mode in (0, 1):
+        idx = gu.device_index(w, q, k, mask)
+        gu.assert_index_equal(idx, mask)
+        O, L = bb.forward(q, k, v, idx, index_mode=mode)
+        gu.assert_attention_close(O, L, inp, mask, w)
+
+
+def test_fp32_shapes():
+    for d, block in ((128, 128), (128, 64), (64, 128)):
+        w = wl.scaled(wl.WORKLOADS["tiny"], H=1, N=512, d=d, block=block)
+        run_workload(w)
+
+
+def test_random_fuzz():
+    rng = np.random.default_rng(7)
+    for t in range(6):
+        d = int(rng.choice([64, 128]))
+        block = int(rng.choice([64, 128]))
+        nb = int(rng.integers(1, 12))
+        w = wl.scaled(wl.WORKLOADS["tiny"], dtype="bf16", H=int(rng.integers(1, 4)), N=nb * block, d=d,
+                      block=block, mask_seed=100 + t, mask_p=float(rng.uniform(0.05, 0.9)), seed=50 + t)
+        run_workload(w, index_mode=t % 2)
+
+
+# ------------------------------------------------------------ properties
+
+
+def test_csr_and_bitmap_bitwise_identical_and_deterministic():
+    w = wl.scaled(wl.WORKLOADS["dynamic_topk"], H=4, N=4096)
+    inp = wl.make_inputs(w)
+    q, k, v = (gu.upload(inp, n) for n in ("q", "k", "v"))
+    idx = bb.build_mask(q, k, w.block, density=w.density)
+    idx2 = bb.build_mask(q, k, w.block, density=w.density)
+    assert torch.equal(idx.col_idx, idx2.col_idx) and torch.equal(idx.bitmap, idx2.bitmap)
+    O0, L0 = bb.forward(q, k, v, idx, index_mode=0)
+    O1, L1 = bb.forward(q, k, v, idx, index_mode=1)
+    O2, L2 = bb.forward(q, k, v, idx, index_mode=0)
+    assert torch.equal(O0, O1) and torch.equal(L0, L1)
+    assert torch.equal(O0, O2) and torch.equal(L0, L2)
+
+
+def test_validate_index():
+    w = wl.scaled(wl.WORKLOADS["dynamic_topk"], H=2, N=2048)
+    inp = wl.make_inputs(w)
+    q, k = gu.upload(inp, "q"), gu.upload(inp, "k")
+    idx = bb.build_mask(q, k, w.block, density=w.density)
+    ws = bb.workspace(0, w.B, w.H, w.N, w.d, w.block)
+    bb.bsa_validate_index(w.B, w.H, w.N, w.block, idx.row_ptr, idx.col_idx, idx.bitmap, ws, ws.numel())
+    assert bb.bsa_check_device_error(ws) == bb.OK
+    bad = idx.col_idx.clone()
+    bad[5], bad[6] = bad[6].clone(), bad[5].clone()  # breaks ascending order within a row
+    bb.bsa_validate_index(w.B, w.H, w.N, w.block, idx.row_ptr, bad, idx.bitmap, ws, ws.numel())
+    assert bb.bsa_check_device_error(ws) == bb.ERR_INVALID_ARG
+    assert bb.bsa_check_device_error(ws) == bb.OK  # cleared by the read
+
+
+# ------------------------------------------------------------ device-raised errors
+
+
+def test_nan_score_raises_nonfinite():
+    w = wl.scaled(wl.WORKLOADS["dynamic_topk"], H=1, N=1024)
+    inp = wl.make_inputs(w)
+    q, k = gu.upload(inp, "q"), gu.upload(inp, "k")
+    q[0, 0, 5, 3] = float("nan")
+    with pytest.raises(bb.BsaError) as e:
+        bb.build_mask(q, k, w.block, density=w.density)
+    assert e.value.code == bb.ERR_NONFINITE
+
+
+def test_explicit_capacity_overflow_is_reported():
+    w = wl.scaled(wl.WORKLOADS["tiny"], dtype="bf16")
+    inp = wl.make_inputs(w)
+    words = torch.from_numpy(gu.mask_bitmap_words(inp["mask"]).reshape(-1)).cuda()
+    spec = bb.explicit_spec(words)
+    B, H, N, d = w.B, w.H, w.N, w.d
+    nB = N // w.block
+    row_ptr = torch.empty(B * H * nB + 1, dtype=torch.int32, device="cuda")
+    cap = 10
+    col_idx = torch.full((cap + 64,), -7, dtype=torch.int32, device="cuda")
+    bitmap = torch.empty(B * H * nB, dtype=torch.int32, device="cuda")
+    ws = bb.workspace(0, B, H, N, d, w.block)
+    bb.bsa_build_mask(None, None, bb.BF16, B, H, N, d, w.block, 0.0, spec, row_ptr, col_idx, cap, bitmap, ws,
+                      ws.numel())
+    assert bb.bsa_check_device_error(ws) == bb.ERR_CAPACITY
+    assert torch.all(col_idx[cap:] == -7)  # nothing written past the capacity
+
+
+def test_bounded_wait_times_out_and_context_survives():
+    w = wl.scaled(wl.WORKLOADS["dynamic_topk"], H=2, N=1024)
+    inp = wl.make_inputs(w)
+    q, k, v = (gu.upload(inp, n) for n in ("q", "k", "v"))
+    idx = bb.build_mask(q, k, w.block, density=w.density)
+    ws = bb.workspace(1, w.B, w.H, w.N, w.d, w.block)
+    try:
+        # loads and MMAs are skipped, so the softmax warps wait for a score tile nothing produces
+        bb.bsa_debug_config(1, 20_000_000)
+        O = torch.empty_like(q)
+        L = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device="cuda")
+        bb.bsa_forward(q, k, v, bb.BF16, w.B, w.H, w.N, w.d, w.block, idx.row_ptr, idx.col_idx, idx.bitmap,
+                       0, 0.0, O, L, ws, ws.numel())
+        assert bb.bsa_check_device_error(ws) == bb.ERR_TIMEOUT
+    finally:
+        bb.bsa_debug_config(0, 0)
+    mask = gu.oracle_mask(w, inp)
+    O, L = bb.forward(q, k, v, idx)
+    gu.assert_attention_close(O, L, inp, mask, w)
+
+
+# ------------------------------------------------------------ full-size workloads
+
+
+def test_full_t2i_static():
+    w = wl.WORKLOADS["t2i_static"]
+    rng = np.random.default_rng(11)
+    run_workload(w, rows=gu.sample_rows(w, rng, blocks_per_head=8, rows_per_block=8))
+
+
+def test_full_dynamic_topk():
+    w = wl.WORKLOADS["dynamic_topk"]
+    rng = np.random.default_rng(12)
+    run_workload(w, rows=gu.sample_rows(w, rng))
+
+
+def test_full_video_cuboid():
+    w = wl.WORKLOADS["video_cuboid"]
+    rng = np.random.default_rng(13)
+    run_workload(w, rows=gu.sample_rows(w, rng, blocks_per_head=12, rows_per_block=6, text_rows_heads=2))
+
+
+def test_full_long_topk_bitmap():
+    w = wl.WORKLOADS["long_topk"]
+    rng = np.random.default_rng(14)
+    run_workload(w, rows=gu.sample_rows(w, rng, blocks_per_head=10, rows_per_block=4))
+
+
+@pytest.mark.parametrize("name", ["long_sweep_bs64", "long_sweep_bs128"])
+def test_full_block_size_sweep(name):
+    w = wl.WORKLOADS[name]
+    rng = np.random.default_rng(15)
+    run_workload(w, rows=gu.sample_rows(w, rng, blocks_per_head=8, rows_per_block=4))

@@ -1,0 +1,151 @@
+"""C-ABI library checks that need no GPU: it loads, exports every symbol the
+header declares, and rejects bad arguments on the host before any launch."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from block_sparse_attention_mean_gb300 import binding as bb
+from block_sparse_attention_mean_gb300 import build as bbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    bbuild.build()
+    return bb.load()
+
+
+def _header_functions():
+    src = open(os.path.join(ROOT, "include", "bsa.h")).read()
+    return sorted(set(re.findall(r"^(?:bsa_status|const char \*)\s*(bsa_\w+)\s*\(", src, re.M)))
+
+
+def test_header_symbols_exported(lib):
+    names = _header_functions()
+    assert len(names) == 8
+    assert sorted(bb.EXPORTS) == names
+    for n in names:
+        assert getattr(lib, n) is not None  # dlsym succeeds
+
+
+def test_status_strings(lib):
+    assert bb.status_string(0) == "ok"
+    assert "capacity" in bb.status_string(bb.ERR_CAPACITY)
+    assert bb.status_string(99) == "unknown status"
+
+
+def test_workspace_sizes(lib):
+    ws0 = bb.bsa_workspace_size(0, 2, 24, 4224, 64, 64)
+    # header + Qbar + Kbar + row counts
+    assert ws0 == 256 + 2 * (2 * 24 * 66 * 64 * 4) + (2 * 24 * 66 * 4 + 255) // 256 * 256
+    ws1 = bb.bsa_workspace_size(1, 2, 24, 4224, 64, 64)
+    assert ws1 == 256 + (2 * 24 * 33 * 4 + 255) // 256 * 256
+    with pytest.raises(bb.BsaError) as e:
+        bb.bsa_workspace_size(1, 1, 1, 100, 64, 64)
+    assert e.value.code == bb.ERR_SHAPE
+    with pytest.raises(bb.BsaError) as e:
+        bb.bsa_workspace_size(2, 1, 1, 128, 64, 64)
+    assert e.value.code == bb.ERR_INVALID_ARG
+
+
+def test_mask_nnz_counts(lib):
+    # 812 active blocks per (b, h) for the t2i band spec, 3600 for the video cuboids
+    assert bb.bsa_mask_nnz(2, 24, 4224, 64, 0.0, bb.band_spec(2, 2, [0, 32])) == 812 * 48
+    assert bb.bsa_mask_nnz(1, 24, 16640, 64, 0.0, bb.cuboid_spec(4, (4, 8, 8))) == 3600 * 24
+    assert bb.bsa_mask_nnz(1, 24, 8192, 64, 0.15, None) == 24 * 128 * 19
+    assert bb.bsa_mask_nnz(1, 16, 65536, 128, 0.05, None) == 16 * 512 * 25
+    ex = bb.StaticSpec()
+    ex.kind = bb.STATIC_EXPLICIT
+    ex.bitmap = 256
+    assert bb.bsa_mask_nnz(1, 2, 512, 64, 0.0, ex) == 2 * 8 * 8  # upper bound
+    with pytest.raises(bb.BsaError):
+        bb.bsa_mask_nnz(1, 1, 8192, 64, 0.0, None)  # density 0
+    with pytest.raises(bb.BsaError):
+        bb.bsa_mask_nnz(1, 1, 8192, 64, 1.5, None)
+    with pytest.raises(bb.BsaError) as e:
+        bb.bsa_mask_nnz(1, 1, 4224, 64, 0.0, bb.cuboid_spec(4, (4, 8, 8)))  # grid does not match N
+    assert e.value.code == bb.ERR_SHAPE
+
+
+FAKE = 1 << 20  # a 256-aligned non-null address that is never dereferenced on these paths
+
+
+def _build(**kw):
+    args = dict(Q=FAKE, K=FAKE, dt=bb.BF16, B=1, H=2, N=512, d=64, block=64, density=0.5, spec=None,
+                row_ptr=FAKE, col_idx=FAKE, col_capacity=1 << 20, bitmap=FAKE, workspace=FAKE,
+                workspace_bytes=1 << 30)
+    args.update(kw)
+    with pytest.raises(bb.BsaError) as e:
+        bb.bsa_build_mask(**args, stream=0)
+    return e.value.code
+
+
+def _fwd(**kw):
+    args = dict(Q=FAKE, K=FAKE, V=FAKE, dt=bb.BF16, B=1, H=2, N=512, d=64, block=64, row_ptr=FAKE,
+                col_idx=FAKE, bitmap=FAKE, index_mode=0, scale=0.0, O=FAKE, LSE=FAKE, workspace=FAKE,
+                workspace_bytes=1 << 30)
+    args.update(kw)
+    with pytest.raises(bb.BsaError) as e:
+        bb.bsa_forward(**args, stream=0)
+    return e.value.code
+
+
+def test_build_mask_rejects_bad_arguments(lib):
+    assert _build(N=500) == bb.ERR_SHAPE            # N % block
+    assert _build(d=96) == bb.ERR_SHAPE
+    assert _build(block=32) == bb.ERR_SHAPE
+    assert _build(dt=7) == bb.ERR_DTYPE
+    assert _build(Q=None) == bb.ERR_INVALID_ARG
+    assert _build(row_ptr=None) == bb.ERR_INVALID_ARG
+    assert _build(density=0.0) == bb.ERR_INVALID_ARG
+    assert _build(density=float("nan")) == bb.ERR_INVALID_ARG
+    assert _build(workspace=None) == bb.ERR_WORKSPACE
+    assert _build(workspace_bytes=16) == bb.ERR_WORKSPACE
+    assert _build(workspace=FAKE + 16) == bb.ERR_WORKSPACE  # misaligned
+    assert _build(Q=FAKE + 2) == bb.ERR_INVALID_ARG          # TMA-incompatible alignment
+    assert _build(col_capacity=2 * 8 * 4 - 1) == bb.ERR_CAPACITY  # k = 4 per row, 16 rows
+    assert _build(spec=bb.band_spec(2, 2, [0, 99])) == bb.ERR_INVALID_ARG  # anchor out of range
+    assert _build(spec=bb.band_spec(2, 2, [0]), col_capacity=10) == bb.ERR_CAPACITY
+    ex = bb.StaticSpec()
+    ex.kind = bb.STATIC_EXPLICIT
+    assert _build(spec=ex) == bb.ERR_INVALID_ARG  # null bitmap
+    bad = bb.StaticSpec()
+    bad.kind = 9
+    assert _build(spec=bad) == bb.ERR_INVALID_ARG
+
+
+def test_forward_rejects_bad_arguments(lib):
+    assert _fwd(N=500) == bb.ERR_SHAPE
+    assert _fwd(d=32) == bb.ERR_SHAPE
+    assert _fwd(dt=5) == bb.ERR_DTYPE
+    assert _fwd(V=None) == bb.ERR_INVALID_ARG
+    assert _fwd(LSE=None) == bb.ERR_INVALID_ARG
+    assert _fwd(O=FAKE + 8) == bb.ERR_INVALID_ARG
+    assert _fwd(index_mode=2) == bb.ERR_INVALID_ARG
+    assert _fwd(index_mode=0, col_idx=None) == bb.ERR_INVALID_ARG
+    assert _fwd(index_mode=1, bitmap=None) == bb.ERR_INVALID_ARG
+    assert _fwd(scale=float("nan")) == bb.ERR_INVALID_ARG
+    assert _fwd(scale=float("inf")) == bb.ERR_INVALID_ARG
+    assert _fwd(workspace_bytes=100) == bb.ERR_WORKSPACE
+    assert _fwd(B=0) == bb.ERR_SHAPE
+
+
+def test_validate_index_rejects_bad_arguments(lib):
+    with pytest.raises(bb.BsaError) as e:
+        bb.bsa_validate_index(1, 1, 512, 64, None, FAKE, FAKE, FAKE, 1 << 20, stream=0)
+    assert e.value.code == bb.ERR_INVALID_ARG
+    with pytest.raises(bb.BsaError) as e:
+        bb.bsa_validate_index(1, 1, 512, 64, FAKE, FAKE, FAKE, FAKE, 8, stream=0)
+    assert e.value.code == bb.ERR_WORKSPACE
+
+
+def test_debug_config_roundtrip(lib):
+    bb.bsa_debug_config(0, 0)
+
+
+def test_static_spec_layout_matches_header(lib):
+    # int kind; ptr; 4 ints; int[8]; 3 ints  (x86-64 and aarch64 LP64 layout)
+    assert ctypes.sizeof(bb.StaticSpec) == 4 + 4 + 8 + 4 * 4 + 4 * 8 + 4 * 3 + 4
