@@ -55,7 +55,7 @@ struct TcParams {
     uint32_t dbg;
 };
 
-template <int D, int BS, int NS>
+template <int D, int BS, int NS, int NSB>
 struct Cfg {
     static constexpr int kQBytes = kTileM * D * 2;
     static constexpr int kKVBytes = BS * D * 2;
@@ -68,14 +68,14 @@ struct Cfg {
     // barrier indices
     static constexpr int B_QFULL = 0, B_QEMPTY = 1;
     static constexpr int B_KFULL = 2, B_VFULL = 2 + NS, B_KVEMPTY = 2 + 2 * NS;
-    static constexpr int B_SFULL = 2 + 3 * NS, B_PFULL = B_SFULL + 2, B_PVDONE = B_SFULL + 4;
-    static constexpr int B_OEMPTY = B_SFULL + 6, B_TFULL = B_OEMPTY + 1, B_TEMPTY = B_TFULL + 2;
+    static constexpr int B_SFULL = 2 + 3 * NS, B_PFULL = B_SFULL + NSB, B_PVDONE = B_SFULL + 2 * NSB;
+    static constexpr int B_OEMPTY = B_SFULL + 3 * NSB, B_TFULL = B_OEMPTY + 1, B_TEMPTY = B_TFULL + 2;
     static constexpr int B_DRAIN = B_TEMPTY + 2;
     static constexpr int NBAR = B_DRAIN + 1;
     static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
     static constexpr int SMEM = MISC_OFF + 32;
     static constexpr int SMEM_ALLOC = SMEM + 1024;  // manual 1024-byte alignment
-    static constexpr int TCOLS_USED = 2 * BS + D;
+    static constexpr int TCOLS_USED = NSB * BS + D;
     static constexpr int TCOLS = TCOLS_USED <= 256 ? 256 : 512;
     static constexpr uint32_t IDESC_QK = idesc_bf16_f32(kTileM, BS, 0, 0);
     static constexpr uint32_t IDESC_PV = idesc_bf16_f32(kTileM, D, 0, 1);
@@ -89,9 +89,8 @@ struct Ctl {
 
 // Bounded wait on an mbarrier phase. Gives up (and raises the abort flag and
 // BSA_ERR_TIMEOUT) after `limit` ns, or early when another role aborted.
-__device__ __noinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Ctl &c)
+__device__ __noinline__ bool wait_bar_slow(uint32_t bar, uint32_t parity, const Ctl &c)
 {
-    if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t n = 1;; ++n) {
         if (mbar_try_wait(bar, parity)) return true;
@@ -104,6 +103,11 @@ __device__ __noinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Ctl &
             }
         }
     }
+}
+
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Ctl &c)
+{
+    return mbar_try_wait(bar, parity) || wait_bar_slow(bar, parity, c);
 }
 
 // Bounded wait used while draining in-flight async work on the way out; it
@@ -142,12 +146,12 @@ __device__ __forceinline__ void walk_init(TileWalk &w, const TcParams &p, int64_
     }
 }
 
-template <int D, int BS, int NS, int MINB>
+template <int D, int BS, int NS, int NSB, int MINB>
 __global__ void __launch_bounds__(kThreads, MINB)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const TcParams p)
 {
-    using C = Cfg<D, BS, NS>;
+    using C = Cfg<D, BS, NS, NSB>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
@@ -166,10 +170,12 @@ __global__ void __launch_bounds__(kThreads, MINB)
             mbar_init(bar(C::B_VFULL + s), 1);
             mbar_init(bar(C::B_KVEMPTY + s), 1);
         }
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < NSB; ++b) {
             mbar_init(bar(C::B_SFULL + b), 1);
             mbar_init(bar(C::B_PFULL + b), 4);
             mbar_init(bar(C::B_PVDONE + b), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
             mbar_init(bar(C::B_TFULL + b), 1);
             mbar_init(bar(C::B_TEMPTY + b), 5);
         }
@@ -262,13 +268,13 @@ __global__ void __launch_bounds__(kThreads, MINB)
     } else if (warp == 5) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0 && !stall) {
-            const uint32_t tS = tmem;             // two S/P buffers of BS columns
-            const uint32_t tO = tmem + 2 * BS;    // O accumulator, D columns
+            const uint32_t tS = tmem;             // NSB S/P buffers of BS columns
+            const uint32_t tO = tmem + NSB * BS;  // O accumulator, D columns
             int G = 0, e = 0, tcount = 0;
             bool ok = true;
             auto issue_pv = [&](int t, bool first) -> bool {
-                const int b = t & 1, s = t % NS;
-                if (!wait_bar(bar(C::B_PFULL + b), (t >> 1) & 1, ctl)) return false;
+                const int b = t % NSB, s = t % NS;
+                if (!wait_bar(bar(C::B_PFULL + b), (t / NSB) & 1, ctl)) return false;
                 if (!wait_bar(bar(C::B_VFULL + s), (t / NS) & 1, ctl)) return false;
                 if (first && e >= 1 && !wait_bar(bar(C::B_OEMPTY), (e - 1) & 1, ctl)) return false;
                 tc_fence_after();
@@ -301,9 +307,10 @@ __global__ void __launch_bounds__(kThreads, MINB)
                 tc_fence_after();
                 const int G0 = G;
                 do {
-                    const int s = G % NS, b = G & 1;
+                    const int s = G % NS, b = G % NSB;
                     if (!wait_bar(bar(C::B_KFULL + s), (G / NS) & 1, ctl)) { ok = false; break; }
-                    if (G >= 2 && !wait_bar(bar(C::B_PVDONE + b), ((G - 2) >> 1) & 1, ctl)) { ok = false; break; }
+                    // S/P buffer b was last read by PV(G - NSB)
+                    if (G >= NSB && !wait_bar(bar(C::B_PVDONE + b), ((G / NSB) - 1) & 1, ctl)) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t kbase = sbase + C::K_OFF + s * C::kKVBytes;
 #pragma unroll
@@ -330,7 +337,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
         // ------------------------------------------------------------ softmax + epilogue (warps 0-3)
         const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
         const uint32_t tS = tmem + lane_base;
-        const uint32_t tO = tmem + lane_base + 2 * BS;
+        const uint32_t tO = tmem + lane_base + NSB * BS;
         const uint32_t half = BS == 128 ? 0u : static_cast<uint32_t>(warp >> 1);
         int G = 0, e = 0, tcount = 0;
         bool ok = true;
@@ -371,8 +378,8 @@ __global__ void __launch_bounds__(kThreads, MINB)
             // cancels between numerator and denominator)
             float m_run = -CUDART_INF_F, l_run = 0.0f, lp_run = 0.0f;
             do {
-                const int b = G & 1;
-                if (!warp_wait(bar(C::B_SFULL + b), (G >> 1) & 1, ctl, lane)) { ok = false; break; }
+                const int b = G % NSB;
+                if (!warp_wait(bar(C::B_SFULL + b), (G / NSB) & 1, ctl, lane)) { ok = false; break; }
                 tc_fence_after();
                 const bool active = ((m >> half) & 1u) != 0u;
                 bool resc = false;
@@ -384,11 +391,18 @@ __global__ void __launch_bounds__(kThreads, MINB)
                     tmem_wait_ld();
 #pragma unroll
                     for (int c = 0; c < BS / 32; ++c) reg_fence32(sv[c]);
-                    float mx = -CUDART_INF_F;
+                    // row max: four independent three-input max chains
+                    float mx0 = -CUDART_INF_F, mx1 = -CUDART_INF_F, mx2 = -CUDART_INF_F, mx3 = -CUDART_INF_F;
 #pragma unroll
                     for (int c = 0; c < BS / 32; ++c)
 #pragma unroll
-                        for (int t = 0; t < 32; ++t) mx = fmaxf(mx, __uint_as_float(sv[c][t]));
+                        for (int t = 0; t < 32; t += 8) {
+                            mx0 = fmax3(mx0, __uint_as_float(sv[c][t]), __uint_as_float(sv[c][t + 1]));
+                            mx1 = fmax3(mx1, __uint_as_float(sv[c][t + 2]), __uint_as_float(sv[c][t + 3]));
+                            mx2 = fmax3(mx2, __uint_as_float(sv[c][t + 4]), __uint_as_float(sv[c][t + 5]));
+                            mx3 = fmax3(mx3, __uint_as_float(sv[c][t + 6]), __uint_as_float(sv[c][t + 7]));
+                        }
+                    const float mx = fmax3(fmaxf(mx0, mx1), mx2, mx3);
                     const float m_tile = mx * p.scale_log2;
                     if (m_run == -CUDART_INF_F) {
                         m_run = m_tile;
@@ -399,26 +413,36 @@ __global__ void __launch_bounds__(kThreads, MINB)
                         m_run = m_tile;
                         resc = true;
                     }
-                    const float neg_m = -m_run;
-                    float sum = 0.0f, sum_p = 0.0f;
+                    // p = 2^(s * scale * log2 e - m): one packed FFMA per pair, one ex2 each;
+                    // four independent packed accumulators per sum
+                    const uint64_t c2x = f2_pack(p.scale_log2, p.scale_log2);
+                    const uint64_t nm2 = f2_pack(-m_run, -m_run);
+                    uint64_t acc[4], accp[4];
+#pragma unroll
+                    for (int a = 0; a < 4; ++a) acc[a] = accp[a] = 0ull;
 #pragma unroll
                     for (int c2 = 0; c2 < BS / 64; ++c2) {
                         uint32_t pk[32];
 #pragma unroll
                         for (int q = 0; q < 32; ++q) {
                             const int k0 = c2 * 64 + 2 * q;
-                            const float p0 =
-                                ex2_approx(fmaf(__uint_as_float(sv[k0 >> 5][k0 & 31]), p.scale_log2, neg_m));
-                            const float p1 = ex2_approx(
-                                fmaf(__uint_as_float(sv[(k0 + 1) >> 5][(k0 + 1) & 31]), p.scale_log2, neg_m));
-                            sum += p0 + p1;
+                            const uint64_t s2 = f2_pack(__uint_as_float(sv[k0 >> 5][k0 & 31]),
+                                                        __uint_as_float(sv[(k0 + 1) >> 5][(k0 + 1) & 31]));
+                            float x0, x1;
+                            f2_unpack(f2_fma(s2, c2x, nm2), x0, x1);
+                            const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
                             pk[q] = pack_bf16x2(p0, p1);
-                            sum_p += __uint_as_float(pk[q] << 16) + __uint_as_float(pk[q] & 0xFFFF0000u);
+                            acc[q & 3] = f2_add(acc[q & 3], f2_pack(p0, p1));
+                            accp[q & 3] = f2_add(accp[q & 3], f2_pack(__uint_as_float(pk[q] << 16),
+                                                                      __uint_as_float(pk[q] & 0xFFFF0000u)));
                         }
                         tmem_st32(tS + b * BS + c2 * 32, pk);
                     }
-                    l_run += sum;
-                    lp_run += sum_p;
+                    float e0, e1, e2, e3;
+                    f2_unpack(f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3])), e0, e1);
+                    f2_unpack(f2_add(f2_add(accp[0], accp[1]), f2_add(accp[2], accp[3])), e2, e3);
+                    l_run += e0 + e1;
+                    lp_run += e2 + e3;
                 } else {
                     uint32_t z[32];
 #pragma unroll
@@ -429,7 +453,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
                 if (__any_sync(0xffffffffu, resc)) {
                     // O holds the previous blocks' sum: rescale it once the last PV landed
                     const int t = G - 1;
-                    if (!warp_wait(bar(C::B_PVDONE + (t & 1)), (t >> 1) & 1, ctl, lane)) { ok = false; break; }
+                    if (!warp_wait(bar(C::B_PVDONE + t % NSB), (t / NSB) & 1, ctl, lane)) { ok = false; break; }
                     tc_fence_after();
 #pragma unroll
                     for (int c = 0; c < D / 32; ++c) {
@@ -451,7 +475,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
             if (!ok) break;
             // ---------------- epilogue: O / l, LSE = ln2 * (m + log2 l)
             const int t = G - 1;
-            if (!warp_wait(bar(C::B_PVDONE + (t & 1)), (t >> 1) & 1, ctl, lane)) break;
+            if (!warp_wait(bar(C::B_PVDONE + t % NSB), (t / NSB) & 1, ctl, lane)) break;
             tc_fence_after();
             const float inv_l = lp_run > 0.0f ? 1.0f / lp_run : 0.0f;
 #pragma unroll
@@ -591,24 +615,36 @@ bool make_map(CUtensorMap *m, const void *base, uint64_t rows, int d, int box_ro
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D, int BS, int NS, int MINB>
+template <int D, int BS, int NS, int NSB, int MINB>
 bsa_status launch_tc(const FwdArgs &a, cudaStream_t st)
 {
-    using C = Cfg<D, BS, NS>;
+    using C = Cfg<D, BS, NS, NSB>;
     static_assert(C::SMEM_ALLOC <= 227 * 1024, "shared memory budget");
-    auto kern = fwd_tc_kernel<D, BS, NS, MINB>;
+    static_assert(C::TCOLS_USED <= C::TCOLS, "TMEM budget");
+    auto kern = fwd_tc_kernel<D, BS, NS, NSB, MINB>;
     static int grid_cap = 0;
     if (grid_cap == 0) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC) != cudaSuccess)
             return BSA_ERR_CUDA;
-        int dev = 0, sms = 0, occ = 0;
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 cudaSharedmemCarveoutMaxShared) != cudaSuccess)
+            return BSA_ERR_CUDA;
+        int dev = 0, sms = 0, smem_sm = 0, occ = 0;
         if (cudaGetDevice(&dev) != cudaSuccess) return BSA_ERR_CUDA;
         if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return BSA_ERR_CUDA;
+        if (cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess)
+            return BSA_ERR_CUDA;
         if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kThreads, C::SMEM_ALLOC) != cudaSuccess)
             return BSA_ERR_CUDA;
-        if (occ < 1) return BSA_ERR_UNSUPPORTED;
-        const int by_tmem = 512 / C::TCOLS;  // CTAs whose TMEM allocations fit one SM
-        grid_cap = sms * (occ < by_tmem ? occ : by_tmem);
+        // resident CTAs per SM: registers are sized for MINB by the launch bounds,
+        // shared memory (+1 KB reserved per CTA) and TMEM columns bound the rest
+        const int by_smem = smem_sm / (C::SMEM_ALLOC + 1024);
+        const int by_tmem = 512 / C::TCOLS;
+        int per_sm = MINB < by_smem ? MINB : by_smem;
+        if (occ > per_sm) per_sm = occ;
+        if (per_sm > by_tmem) per_sm = by_tmem;
+        if (per_sm < 1) return BSA_ERR_UNSUPPORTED;
+        grid_cap = sms * per_sm;
     }
     const int64_t BH = static_cast<int64_t>(a.B) * a.H;
     const uint64_t rows = static_cast<uint64_t>(BH) * a.N;
@@ -653,10 +689,11 @@ size_t fwd_workspace_bytes(int B, int H, int N, int d, int block)
 
 bsa_status launch_forward_tc(const FwdArgs &a, cudaStream_t st)
 {
-    if (a.d == 64 && a.block == 64) return launch_tc<64, 64, 4, 2>(a, st);
-    if (a.d == 128 && a.block == 64) return launch_tc<128, 64, 2, 2>(a, st);
-    if (a.d == 64 && a.block == 128) return launch_tc<64, 128, 3, 1>(a, st);
-    if (a.d == 128 && a.block == 128) return launch_tc<128, 128, 2, 1>(a, st);
+    // <D, BS, K/V stages, S/P buffers, CTAs per SM>
+    if (a.d == 64 && a.block == 64) return launch_tc<64, 64, 4, 3, 2>(a, st);
+    if (a.d == 128 && a.block == 64) return launch_tc<128, 64, 2, 2, 2>(a, st);
+    if (a.d == 64 && a.block == 128) return launch_tc<64, 128, 3, 3, 1>(a, st);
+    if (a.d == 128 && a.block == 128) return launch_tc<128, 128, 2, 3, 1>(a, st);
     return BSA_ERR_SHAPE;
 }
 
