@@ -11,7 +11,8 @@
 //   * Warp roles: warps 0-3 softmax + epilogue (thread = query row = TMEM lane),
 //     warp 4 TMA producer, warp 5 tcgen05 MMA issuer (one thread).
 //   * Q tile and K/V blocks arrive by TMA (128-byte swizzle), K/V fetched by
-//     block index into an NS-stage shared-memory ring.
+//     block index into separate K and V shared-memory rings (a K slot frees when
+//     its QK^T completes, a V slot when its PV completes).
 //   * S = Q K^T and O += P V run on tcgen05 with fp32 accumulators in TMEM.
 //     S is double-buffered so the QK^T of block n+1 overlaps the softmax of
 //     block n; P (bf16) overwrites S in TMEM and feeds the PV MMA directly.
@@ -34,7 +35,8 @@
 namespace bsa {
 namespace {
 
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;  // warps 0-7 softmax, 8 TMA producer, 9 MMA issuer
+constexpr int kProducerWarp = 8, kMmaWarp = 9;
 constexpr int kTileM = 128;
 constexpr float kRescaleLog2 = 8.0f;
 constexpr uint32_t kDbgStall = 1u;
@@ -55,25 +57,27 @@ struct TcParams {
     uint32_t dbg;
 };
 
-template <int D, int BS, int NS, int NSB>
+template <int D, int BS, int NK, int NV, int NSB, int QS>
 struct Cfg {
     static constexpr int kQBytes = kTileM * D * 2;
     static constexpr int kKVBytes = BS * D * 2;
     static constexpr int kQChunk = kTileM * 128;  // bytes of one 64-column swizzled slab
     static constexpr int kKVChunk = BS * 128;
-    static constexpr int Q_OFF = 0;
-    static constexpr int K_OFF = Q_OFF + kQBytes;
-    static constexpr int V_OFF = K_OFF + NS * kKVBytes;
-    static constexpr int BAR_OFF = V_OFF + NS * kKVBytes;
+    static constexpr int Q_OFF = 0;  // QS Q slots: tile e uses slot e % QS
+    static constexpr int K_OFF = Q_OFF + QS * kQBytes;   // NK-stage K ring
+    static constexpr int V_OFF = K_OFF + NK * kKVBytes;  // NV-stage V ring
+    static constexpr int BAR_OFF = V_OFF + NV * kKVBytes;
     // barrier indices
-    static constexpr int B_QFULL = 0, B_QEMPTY = 1;
-    static constexpr int B_KFULL = 2, B_VFULL = 2 + NS, B_KVEMPTY = 2 + 2 * NS;
-    static constexpr int B_SFULL = 2 + 3 * NS, B_PFULL = B_SFULL + NSB, B_PVDONE = B_SFULL + 2 * NSB;
+    static constexpr int B_QFULL = 0, B_QEMPTY = 2;  // two each
+    static constexpr int B_KFULL = 4, B_KEMPTY = B_KFULL + NK, B_VFULL = B_KEMPTY + NK, B_VEMPTY = B_VFULL + NV;
+    static constexpr int B_SFULL = B_VEMPTY + NV, B_PFULL = B_SFULL + NSB, B_PVDONE = B_SFULL + 2 * NSB;
     static constexpr int B_OEMPTY = B_SFULL + 3 * NSB, B_TFULL = B_OEMPTY + 1, B_TEMPTY = B_TFULL + 2;
     static constexpr int B_DRAIN = B_TEMPTY + 2;
-    static constexpr int NBAR = B_DRAIN + 1;
+    static constexpr int B_XCH = B_DRAIN + 1;  // 4 row quarters x 2 slots: half-row exchange
+    static constexpr int NBAR = B_XCH + 8;
     static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
-    static constexpr int SMEM = MISC_OFF + 32;
+    static constexpr int XCH_OFF = MISC_OFF + 32;  // float2 [2 slots][2 halves][128 rows]
+    static constexpr int SMEM = XCH_OFF + 2 * 2 * kTileM * 8;
     static constexpr int SMEM_ALLOC = SMEM + 1024;  // manual 1024-byte alignment
     static constexpr int TCOLS_USED = NSB * BS + D;
     static constexpr int TCOLS = TCOLS_USED <= 256 ? 256 : 512;
@@ -92,15 +96,14 @@ struct Ctl {
 __device__ __noinline__ bool wait_bar_slow(uint32_t bar, uint32_t parity, const Ctl &c)
 {
     const uint64_t t0 = globaltimer_ns();
-    for (uint32_t n = 1;; ++n) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((n & 15u) == 0u) {
-            if (*c.abort_flag) return false;
-            if (globaltimer_ns() - t0 > c.limit) {
-                *c.abort_flag = 1u;
-                raise_error(c.err, BSA_ERR_TIMEOUT);
-                return false;
-            }
+    for (;;) {
+        // sleeps in hardware until the phase completes or ~50 us pass
+        if (mbar_try_wait_sleep(bar, parity, 50000u)) return true;
+        if (*c.abort_flag) return false;
+        if (globaltimer_ns() - t0 > c.limit) {
+            *c.abort_flag = 1u;
+            raise_error(c.err, BSA_ERR_TIMEOUT);
+            return false;
         }
     }
 }
@@ -115,7 +118,7 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Ct
 __device__ __noinline__ bool wait_bar_drain(uint32_t bar, uint32_t parity, unsigned long long limit)
 {
     const uint64_t t0 = globaltimer_ns();
-    while (!mbar_try_wait(bar, parity))
+    while (!mbar_try_wait_sleep(bar, parity, 50000u))
         if (globaltimer_ns() - t0 > limit) return false;
     return true;
 }
@@ -146,12 +149,12 @@ __device__ __forceinline__ void walk_init(TileWalk &w, const TcParams &p, int64_
     }
 }
 
-template <int D, int BS, int NS, int NSB, int MINB>
+template <int D, int BS, int NK, int NV, int NSB, int QS, int MINB>
 __global__ void __launch_bounds__(kThreads, MINB)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const TcParams p)
 {
-    using C = Cfg<D, BS, NS, NSB>;
+    using C = Cfg<D, BS, NK, NV, NSB, QS>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
@@ -163,32 +166,38 @@ __global__ void __launch_bounds__(kThreads, MINB)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
-        mbar_init(bar(C::B_QFULL), 1);
-        mbar_init(bar(C::B_QEMPTY), 1);
-        for (int s = 0; s < NS; ++s) {
+        for (int q = 0; q < QS; ++q) {
+            mbar_init(bar(C::B_QFULL + q), 1);
+            mbar_init(bar(C::B_QEMPTY + q), 1);
+        }
+        for (int s = 0; s < NK; ++s) {
             mbar_init(bar(C::B_KFULL + s), 1);
+            mbar_init(bar(C::B_KEMPTY + s), 1);
+        }
+        for (int s = 0; s < NV; ++s) {
             mbar_init(bar(C::B_VFULL + s), 1);
-            mbar_init(bar(C::B_KVEMPTY + s), 1);
+            mbar_init(bar(C::B_VEMPTY + s), 1);
         }
         for (int b = 0; b < NSB; ++b) {
             mbar_init(bar(C::B_SFULL + b), 1);
-            mbar_init(bar(C::B_PFULL + b), 4);
+            mbar_init(bar(C::B_PFULL + b), 8);
             mbar_init(bar(C::B_PVDONE + b), 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(bar(C::B_TFULL + b), 1);
-            mbar_init(bar(C::B_TEMPTY + b), 5);
+            mbar_init(bar(C::B_TEMPTY + b), 9);
         }
-        mbar_init(bar(C::B_OEMPTY), 4);
+        mbar_init(bar(C::B_OEMPTY), 8);
         mbar_init(bar(C::B_DRAIN), 1);
+        for (int x = 0; x < 8; ++x) mbar_init(bar(C::B_XCH + x), 2);
         misc[1] = 0u;
         fence_mbar_init();
     }
-    if (warp == 5) {
+    if (warp == kMmaWarp) {
         tmem_alloc(smem_u32(misc), C::TCOLS);
         tmem_relinquish();
     }
-    if (warp == 4 && lane == 0) {
+    if (warp == kProducerWarp && lane == 0) {
         tma_prefetch_map(&tmQ);
         tma_prefetch_map(&tmK);
         tma_prefetch_map(&tmV);
@@ -200,12 +209,11 @@ __global__ void __launch_bounds__(kThreads, MINB)
     const Ctl ctl{reinterpret_cast<volatile uint32_t *>(misc + 1), p.err, p.wait_limit_ns};
     const bool stall = (p.dbg & kDbgStall) != 0u;
 
-    if (warp == 4) {
+    if (warp == kProducerWarp) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
             int G = 0, e = 0, tcount = 0;
-            int last_issue[NS];
-            for (int s = 0; s < NS; ++s) last_issue[s] = -1;
+            int last_issue = -1;  // last iteration whose K and V loads were issued
             int q_issued = -1;
             bool ok = true;
             while (ok) {
@@ -226,46 +234,59 @@ __global__ void __launch_bounds__(kThreads, MINB)
                 int j;
                 uint32_t m;
                 if (!walk.next(j, m)) continue;  // empty tile: nothing to load
-                if (e >= 1 && !wait_bar(bar(C::B_QEMPTY), (e - 1) & 1, ctl)) break;
-                mbar_arrive_expect_tx(bar(C::B_QFULL), C::kQBytes);
+                const int qs = e % QS;  // Q slot; it was last used by tile e - QS
+                if (e >= QS && !wait_bar(bar(C::B_QEMPTY + qs), ((e / QS) - 1) & 1, ctl)) break;
+                mbar_arrive_expect_tx(bar(C::B_QFULL + qs), C::kQBytes);
                 const int qrow = static_cast<int>(bh * p.N) + qt * kTileM;
 #pragma unroll
                 for (int c = 0; c < D / 64; ++c)
-                    tma_load_2d(sbase + C::Q_OFF + c * C::kQChunk, &tmQ, c * 64, qrow, bar(C::B_QFULL));
+                    tma_load_2d(sbase + C::Q_OFF + qs * C::kQBytes + c * C::kQChunk, &tmQ, c * 64, qrow,
+                                bar(C::B_QFULL + qs));
                 q_issued = e;
                 do {
-                    const int s = G % NS;
-                    if (G >= NS && !wait_bar(bar(C::B_KVEMPTY + s), ((G / NS) - 1) & 1, ctl)) {
+                    const int krow = static_cast<int>(bh * p.N) + j * BS;
+                    // K slot: freed when the QK^T that read it completes
+                    const int ks = G % NK;
+                    if (G >= NK && !wait_bar(bar(C::B_KEMPTY + ks), ((G / NK) - 1) & 1, ctl)) {
                         ok = false;
                         break;
                     }
-                    const int krow = static_cast<int>(bh * p.N) + j * BS;
-                    mbar_arrive_expect_tx(bar(C::B_KFULL + s), C::kKVBytes);
+                    mbar_arrive_expect_tx(bar(C::B_KFULL + ks), C::kKVBytes);
 #pragma unroll
                     for (int c = 0; c < D / 64; ++c)
-                        tma_load_2d(sbase + C::K_OFF + s * C::kKVBytes + c * C::kKVChunk, &tmK, c * 64, krow,
-                                    bar(C::B_KFULL + s));
-                    mbar_arrive_expect_tx(bar(C::B_VFULL + s), C::kKVBytes);
+                        tma_load_2d(sbase + C::K_OFF + ks * C::kKVBytes + c * C::kKVChunk, &tmK, c * 64, krow,
+                                    bar(C::B_KFULL + ks));
+                    // V slot: freed when the PV that read it completes
+                    const int vs = G % NV;
+                    if (G >= NV && !wait_bar(bar(C::B_VEMPTY + vs), ((G / NV) - 1) & 1, ctl)) {
+                        // the K load of this iteration is in flight: drain it below
+                        last_issue = G - 1;
+                        ok = false;
+                        wait_bar_drain(bar(C::B_KFULL + ks), (G / NK) & 1, p.wait_limit_ns);
+                        break;
+                    }
+                    mbar_arrive_expect_tx(bar(C::B_VFULL + vs), C::kKVBytes);
 #pragma unroll
                     for (int c = 0; c < D / 64; ++c)
-                        tma_load_2d(sbase + C::V_OFF + s * C::kKVBytes + c * C::kKVChunk, &tmV, c * 64, krow,
-                                    bar(C::B_VFULL + s));
-                    last_issue[s] = G;
+                        tma_load_2d(sbase + C::V_OFF + vs * C::kKVBytes + c * C::kKVChunk, &tmV, c * 64, krow,
+                                    bar(C::B_VFULL + vs));
+                    last_issue = G;
                     ++G;
                 } while (walk.next(j, m));
                 ++e;
             }
             if (*ctl.abort_flag) {
                 // never leave while our copies may still land in shared memory
-                for (int s = 0; s < NS; ++s)
-                    if (last_issue[s] >= 0) {
-                        wait_bar_drain(bar(C::B_KFULL + s), (last_issue[s] / NS) & 1, p.wait_limit_ns);
-                        wait_bar_drain(bar(C::B_VFULL + s), (last_issue[s] / NS) & 1, p.wait_limit_ns);
-                    }
-                if (q_issued >= 0) wait_bar_drain(bar(C::B_QFULL), q_issued & 1, p.wait_limit_ns);
+                for (int g = last_issue - (NK > NV ? NK : NV) + 1; g <= last_issue; ++g) {
+                    if (g < 0) continue;
+                    if (g > last_issue - NK) wait_bar_drain(bar(C::B_KFULL + g % NK), (g / NK) & 1, p.wait_limit_ns);
+                    if (g > last_issue - NV) wait_bar_drain(bar(C::B_VFULL + g % NV), (g / NV) & 1, p.wait_limit_ns);
+                }
+                for (int e2 = q_issued - (QS - 1) < 0 ? 0 : q_issued - (QS - 1); e2 <= q_issued; ++e2)
+                    wait_bar_drain(bar(C::B_QFULL + e2 % QS), (e2 / QS) & 1, p.wait_limit_ns);
             }
         }
-    } else if (warp == 5) {
+    } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0 && !stall) {
             const uint32_t tS = tmem;             // NSB S/P buffers of BS columns
@@ -273,9 +294,9 @@ __global__ void __launch_bounds__(kThreads, MINB)
             int G = 0, e = 0, tcount = 0;
             bool ok = true;
             auto issue_pv = [&](int t, bool first) -> bool {
-                const int b = t % NSB, s = t % NS;
+                const int b = t % NSB, s = t % NV;
                 if (!wait_bar(bar(C::B_PFULL + b), (t / NSB) & 1, ctl)) return false;
-                if (!wait_bar(bar(C::B_VFULL + s), (t / NS) & 1, ctl)) return false;
+                if (!wait_bar(bar(C::B_VFULL + s), (t / NV) & 1, ctl)) return false;
                 if (first && e >= 1 && !wait_bar(bar(C::B_OEMPTY), (e - 1) & 1, ctl)) return false;
                 tc_fence_after();
                 const uint32_t vbase = sbase + C::V_OFF + s * C::kKVBytes;
@@ -285,7 +306,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
                     mma_ts(tO, tS + b * BS + kk * 8, bdesc, C::IDESC_PV, (first && kk == 0) ? 0u : 1u);
                 }
                 tc_commit(bar(C::B_PVDONE + b));
-                tc_commit(bar(C::B_KVEMPTY + s));
+                tc_commit(bar(C::B_VEMPTY + s));
                 return true;
             };
             while (ok) {
@@ -303,12 +324,14 @@ __global__ void __launch_bounds__(kThreads, MINB)
                 int j;
                 uint32_t m;
                 if (!walk.next(j, m)) continue;
-                if (!wait_bar(bar(C::B_QFULL), e & 1, ctl)) break;
+                const int qs = e % QS;
+                if (!wait_bar(bar(C::B_QFULL + qs), (e / QS) & 1, ctl)) break;
                 tc_fence_after();
+                const uint32_t qbase = sbase + C::Q_OFF + qs * C::kQBytes;
                 const int G0 = G;
                 do {
-                    const int s = G % NS, b = G % NSB;
-                    if (!wait_bar(bar(C::B_KFULL + s), (G / NS) & 1, ctl)) { ok = false; break; }
+                    const int s = G % NK, b = G % NSB;
+                    if (!wait_bar(bar(C::B_KFULL + s), (G / NK) & 1, ctl)) { ok = false; break; }
                     // S/P buffer b was last read by PV(G - NSB)
                     if (G >= NSB && !wait_bar(bar(C::B_PVDONE + b), ((G / NSB) - 1) & 1, ctl)) { ok = false; break; }
                     tc_fence_after();
@@ -316,16 +339,17 @@ __global__ void __launch_bounds__(kThreads, MINB)
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk) {
                         const int c = kk >> 2, off = (kk & 3) * 32;
-                        const uint64_t adesc = sdesc_sw128(sbase + C::Q_OFF + c * C::kQChunk + off, 16, 1024);
+                        const uint64_t adesc = sdesc_sw128(qbase + c * C::kQChunk + off, 16, 1024);
                         const uint64_t bdesc = sdesc_sw128(kbase + c * C::kKVChunk + off, 16, 1024);
                         mma_ss(tS + b * BS, adesc, bdesc, C::IDESC_QK, kk > 0 ? 1u : 0u);
                     }
                     tc_commit(bar(C::B_SFULL + b));
+                    tc_commit(bar(C::B_KEMPTY + s));
                     if (G > G0 && !issue_pv(G - 1, G - 1 == G0)) { ok = false; break; }
                     ++G;
                 } while (walk.next(j, m));
                 if (!ok) break;
-                tc_commit(bar(C::B_QEMPTY));
+                tc_commit(bar(C::B_QEMPTY + qs));
                 if (!issue_pv(G - 1, G - 1 == G0)) break;
                 ++e;
             }
@@ -334,11 +358,30 @@ __global__ void __launch_bounds__(kThreads, MINB)
             wait_bar_drain(bar(C::B_DRAIN), 0, p.wait_limit_ns);
         }
     } else {
-        // ------------------------------------------------------------ softmax + epilogue (warps 0-3)
-        const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
-        const uint32_t tS = tmem + lane_base;
-        const uint32_t tO = tmem + lane_base + NSB * BS;
-        const uint32_t half = BS == 128 ? 0u : static_cast<uint32_t>(warp >> 1);
+        // ------------------------------------------------------------ softmax + epilogue (warps 0-7)
+        // Warp w owns TMEM lanes 32*(w%4).. (query rows) and column half h = w/4 of
+        // S, P and O; the two warps of a row quarter exchange their half-row max
+        // (and, at the end, their sums) through shared memory guarded by mbarriers.
+        const int quarter = warp & 3, h = warp >> 2;
+        const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+        const uint32_t tS = tmem + lane_base + h * (BS / 2);        // this thread's S columns
+        const uint32_t tP = tmem + lane_base + h * (BS / 4);        // its P columns (bf16 pairs)
+        const uint32_t tO = tmem + lane_base + NSB * BS + h * (D / 2);
+        const uint32_t qblk = BS == 128 ? 0u : static_cast<uint32_t>(quarter >> 1);
+        const int trow = quarter * 32 + lane;  // row within the tile
+        float2 *xch = reinterpret_cast<float2 *>(smem + C::XCH_OFF);  // [slot][half][row]
+        int X = 0;  // exchanges done (same sequence in both warps of the pair)
+        // exchange one float2 with the partner warp; bounded wait
+        auto exchange = [&](float2 mine, float2 &theirs) -> bool {
+            const int slot = X & 1;
+            xch[(slot * 2 + h) * kTileM + trow] = mine;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(C::B_XCH + quarter * 2 + slot));
+            const bool okx = warp_wait(bar(C::B_XCH + quarter * 2 + slot), (X >> 1) & 1, ctl, lane);
+            theirs = xch[(slot * 2 + (h ^ 1)) * kTileM + trow];
+            ++X;
+            return okx;
+        };
         int G = 0, e = 0, tcount = 0;
         bool ok = true;
         while (ok) {
@@ -355,9 +398,10 @@ __global__ void __launch_bounds__(kThreads, MINB)
             int64_t bh;
             int qt;
             tile_coords(p, tile, bh, qt);
-            const int row = qt * kTileM + warp * 32 + lane;
+            const int row = qt * kTileM + trow;
             const bool row_valid = row < p.N;
             const int64_t grow = bh * p.N + row;
+            __nv_bfloat16 *orow = p.O + grow * D + h * (D / 2);
             TileWalk walk;
             walk_init<BS>(walk, p, bh, qt);
             int j;
@@ -366,35 +410,35 @@ __global__ void __launch_bounds__(kThreads, MINB)
                 // no active block anywhere in the tile: O = 0, LSE = -inf
                 if (row_valid) {
                     uint4 z = make_uint4(0u, 0u, 0u, 0u);
-                    uint4 *dst = reinterpret_cast<uint4 *>(p.O + grow * D);
 #pragma unroll
-                    for (int c = 0; c < D / 8; ++c) dst[c] = z;
-                    p.LSE[grow] = -CUDART_INF_F;
+                    for (int c = 0; c < D / 16; ++c) reinterpret_cast<uint4 *>(orow)[c] = z;
+                    if (h == 0) p.LSE[grow] = -CUDART_INF_F;
                 }
                 continue;
             }
             // l_run: sum of the fp32 probabilities (for LSE); lp_run: sum of the bf16
             // probabilities the PV MMA consumes (normaliser of O, so rounding of P
-            // cancels between numerator and denominator)
+            // cancels between numerator and denominator). Both cover this half row.
             float m_run = -CUDART_INF_F, l_run = 0.0f, lp_run = 0.0f;
             do {
                 const int b = G % NSB;
                 if (!warp_wait(bar(C::B_SFULL + b), (G / NSB) & 1, ctl, lane)) { ok = false; break; }
                 tc_fence_after();
-                const bool active = ((m >> half) & 1u) != 0u;
+                const bool active = ((m >> qblk) & 1u) != 0u;
                 bool resc = false;
                 float alpha = 1.0f;
                 if (active) {
-                    uint32_t sv[BS / 32][32];
+                    constexpr int NC = BS / 64;  // 32-column chunks of this half row
+                    uint32_t sv[NC][32];
 #pragma unroll
-                    for (int c = 0; c < BS / 32; ++c) tmem_ld32(tS + b * BS + c * 32, sv[c]);
+                    for (int c = 0; c < NC; ++c) tmem_ld32(tS + b * BS + c * 32, sv[c]);
                     tmem_wait_ld();
 #pragma unroll
-                    for (int c = 0; c < BS / 32; ++c) reg_fence32(sv[c]);
-                    // row max: four independent three-input max chains
+                    for (int c = 0; c < NC; ++c) reg_fence32(sv[c]);
+                    // half-row max: four independent three-input max chains
                     float mx0 = -CUDART_INF_F, mx1 = -CUDART_INF_F, mx2 = -CUDART_INF_F, mx3 = -CUDART_INF_F;
 #pragma unroll
-                    for (int c = 0; c < BS / 32; ++c)
+                    for (int c = 0; c < NC; ++c)
 #pragma unroll
                         for (int t = 0; t < 32; t += 8) {
                             mx0 = fmax3(mx0, __uint_as_float(sv[c][t]), __uint_as_float(sv[c][t + 1]));
@@ -402,7 +446,9 @@ __global__ void __launch_bounds__(kThreads, MINB)
                             mx2 = fmax3(mx2, __uint_as_float(sv[c][t + 4]), __uint_as_float(sv[c][t + 5]));
                             mx3 = fmax3(mx3, __uint_as_float(sv[c][t + 6]), __uint_as_float(sv[c][t + 7]));
                         }
-                    const float mx = fmax3(fmaxf(mx0, mx1), mx2, mx3);
+                    float2 other;
+                    if (!exchange(make_float2(fmax3(fmaxf(mx0, mx1), mx2, mx3), 0.0f), other)) { ok = false; break; }
+                    const float mx = fmax3(fmaxf(mx0, mx1), mx2, fmaxf(mx3, other.x));
                     const float m_tile = mx * p.scale_log2;
                     if (m_run == -CUDART_INF_F) {
                         m_run = m_tile;
@@ -421,13 +467,12 @@ __global__ void __launch_bounds__(kThreads, MINB)
 #pragma unroll
                     for (int a = 0; a < 4; ++a) acc[a] = accp[a] = 0ull;
 #pragma unroll
-                    for (int c2 = 0; c2 < BS / 64; ++c2) {
-                        uint32_t pk[32];
+                    for (int c = 0; c < NC; ++c) {
+                        uint32_t pk[16];
 #pragma unroll
-                        for (int q = 0; q < 32; ++q) {
-                            const int k0 = c2 * 64 + 2 * q;
-                            const uint64_t s2 = f2_pack(__uint_as_float(sv[k0 >> 5][k0 & 31]),
-                                                        __uint_as_float(sv[(k0 + 1) >> 5][(k0 + 1) & 31]));
+                        for (int q = 0; q < 16; ++q) {
+                            const uint64_t s2 =
+                                f2_pack(__uint_as_float(sv[c][2 * q]), __uint_as_float(sv[c][2 * q + 1]));
                             float x0, x1;
                             f2_unpack(f2_fma(s2, c2x, nm2), x0, x1);
                             const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
@@ -436,7 +481,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
                             accp[q & 3] = f2_add(accp[q & 3], f2_pack(__uint_as_float(pk[q] << 16),
                                                                       __uint_as_float(pk[q] & 0xFFFF0000u)));
                         }
-                        tmem_st32(tS + b * BS + c2 * 32, pk);
+                        tmem_st16(tP + b * BS + c * 16, pk);
                     }
                     float e0, e1, e2, e3;
                     f2_unpack(f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3])), e0, e1);
@@ -444,11 +489,11 @@ __global__ void __launch_bounds__(kThreads, MINB)
                     l_run += e0 + e1;
                     lp_run += e2 + e3;
                 } else {
-                    uint32_t z[32];
+                    uint32_t z[16];
 #pragma unroll
-                    for (int q = 0; q < 32; ++q) z[q] = 0u;
+                    for (int q = 0; q < 16; ++q) z[q] = 0u;
 #pragma unroll
-                    for (int c2 = 0; c2 < BS / 64; ++c2) tmem_st32(tS + b * BS + c2 * 32, z);
+                    for (int c = 0; c < BS / 64; ++c) tmem_st16(tP + b * BS + c * 16, z);
                 }
                 if (__any_sync(0xffffffffu, resc)) {
                     // O holds the previous blocks' sum: rescale it once the last PV landed
@@ -456,7 +501,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
                     if (!warp_wait(bar(C::B_PVDONE + t % NSB), (t / NSB) & 1, ctl, lane)) { ok = false; break; }
                     tc_fence_after();
 #pragma unroll
-                    for (int c = 0; c < D / 32; ++c) {
+                    for (int c = 0; c < D / 64; ++c) {
                         uint32_t ov[32];
                         tmem_ld32(tO + c * 32, ov);
                         tmem_wait_ld();
@@ -473,13 +518,16 @@ __global__ void __launch_bounds__(kThreads, MINB)
                 ++G;
             } while (walk.next(j, m));
             if (!ok) break;
-            // ---------------- epilogue: O / l, LSE = ln2 * (m + log2 l)
+            // ---------------- epilogue: O / l, LSE = ln2 * (m + log2 l) over the whole row
+            float2 other;
+            if (!exchange(make_float2(l_run, lp_run), other)) break;
+            const float l_all = l_run + other.x, lp_all = lp_run + other.y;
             const int t = G - 1;
             if (!warp_wait(bar(C::B_PVDONE + t % NSB), (t / NSB) & 1, ctl, lane)) break;
             tc_fence_after();
-            const float inv_l = lp_run > 0.0f ? 1.0f / lp_run : 0.0f;
+            const float inv_l = lp_all > 0.0f ? 1.0f / lp_all : 0.0f;
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
+            for (int c = 0; c < D / 64; ++c) {
                 uint32_t ov[32];
                 tmem_ld32(tO + c * 32, ov);
                 tmem_wait_ld();
@@ -489,7 +537,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
 #pragma unroll
                     for (int q = 0; q < 16; ++q)
                         pk[q] = pack_bf16x2(__uint_as_float(ov[2 * q]) * inv_l, __uint_as_float(ov[2 * q + 1]) * inv_l);
-                    uint4 *dst = reinterpret_cast<uint4 *>(p.O + grow * D + c * 32);
+                    uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
 #pragma unroll
                     for (int q = 0; q < 4; ++q) dst[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
                 }
@@ -497,15 +545,15 @@ __global__ void __launch_bounds__(kThreads, MINB)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(C::B_OEMPTY));
-            if (row_valid)
-                p.LSE[grow] = l_run > 0.0f ? (m_run + log2f(l_run)) * 0.69314718055994530942f : -CUDART_INF_F;
+            if (row_valid && h == 0)
+                p.LSE[grow] = l_all > 0.0f ? (m_run + log2f(l_all)) * 0.69314718055994530942f : -CUDART_INF_F;
             ++e;
         }
     }
 
     tc_fence_before();
     __syncthreads();
-    if (warp == 5) {
+    if (warp == kMmaWarp) {
         tc_fence_after();
         tmem_dealloc(tmem, C::TCOLS);
     }
@@ -615,13 +663,14 @@ bool make_map(CUtensorMap *m, const void *base, uint64_t rows, int d, int box_ro
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D, int BS, int NS, int NSB, int MINB>
+template <int D, int BS, int NK, int NV, int NSB, int QS, int MINB>
 bsa_status launch_tc(const FwdArgs &a, cudaStream_t st)
 {
-    using C = Cfg<D, BS, NS, NSB>;
+    using C = Cfg<D, BS, NK, NV, NSB, QS>;
+    static_assert(MINB * (C::SMEM_ALLOC + 1024) <= 233472, "shared memory for MINB CTAs per SM");
     static_assert(C::SMEM_ALLOC <= 227 * 1024, "shared memory budget");
     static_assert(C::TCOLS_USED <= C::TCOLS, "TMEM budget");
-    auto kern = fwd_tc_kernel<D, BS, NS, NSB, MINB>;
+    auto kern = fwd_tc_kernel<D, BS, NK, NV, NSB, QS, MINB>;
     static int grid_cap = 0;
     if (grid_cap == 0) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC) != cudaSuccess)
@@ -689,11 +738,11 @@ size_t fwd_workspace_bytes(int B, int H, int N, int d, int block)
 
 bsa_status launch_forward_tc(const FwdArgs &a, cudaStream_t st)
 {
-    // <D, BS, K/V stages, S/P buffers, CTAs per SM>
-    if (a.d == 64 && a.block == 64) return launch_tc<64, 64, 4, 3, 2>(a, st);
-    if (a.d == 128 && a.block == 64) return launch_tc<128, 64, 2, 2, 2>(a, st);
-    if (a.d == 64 && a.block == 128) return launch_tc<64, 128, 3, 3, 1>(a, st);
-    if (a.d == 128 && a.block == 128) return launch_tc<128, 128, 2, 3, 1>(a, st);
+    // <D, BS, K stages, V stages, S/P buffers, Q slots, CTAs per SM>
+    if (a.d == 64 && a.block == 64) return launch_tc<64, 64, 4, 5, 3, 2, 2>(a, st);
+    if (a.d == 128 && a.block == 64) return launch_tc<128, 64, 2, 2, 2, 1, 2>(a, st);
+    if (a.d == 64 && a.block == 128) return launch_tc<64, 128, 5, 6, 3, 2, 1>(a, st);
+    if (a.d == 128 && a.block == 128) return launch_tc<128, 128, 2, 2, 3, 2, 1>(a, st);
     return BSA_ERR_SHAPE;
 }
 
