@@ -35,8 +35,13 @@
 namespace bsa {
 namespace {
 
-constexpr int kThreads = 320;  // warps 0-7 softmax, 8 TMA producer, 9 MMA issuer
-constexpr int kProducerWarp = 8, kMmaWarp = 9;
+// Warp roles: 4 * SPLIT softmax warps, then the TMA producer, then the MMA issuer.
+template <int SPLIT>
+struct Roles {
+    static constexpr int kSoftmaxWarps = 4 * SPLIT;
+    static constexpr int kProducerWarp = kSoftmaxWarps, kMmaWarp = kSoftmaxWarps + 1;
+    static constexpr int kThreads = (kSoftmaxWarps + 2) * 32;
+};
 constexpr int kTileM = 128;
 constexpr float kRescaleLog2 = 8.0f;
 constexpr uint32_t kDbgStall = 1u;
@@ -149,12 +154,14 @@ __device__ __forceinline__ void walk_init(TileWalk &w, const TcParams &p, int64_
     }
 }
 
-template <int D, int BS, int NK, int NV, int NSB, int QS, int MINB>
-__global__ void __launch_bounds__(kThreads, MINB)
+template <int D, int BS, int NK, int NV, int NSB, int QS, int SPLIT, int MINB>
+__global__ void __launch_bounds__((4 * SPLIT + 2) * 32, MINB)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const TcParams p)
 {
     using C = Cfg<D, BS, NK, NV, NSB, QS>;
+    using R = Roles<SPLIT>;
+    constexpr int kProducerWarp = R::kProducerWarp, kMmaWarp = R::kMmaWarp;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
@@ -180,14 +187,14 @@ __global__ void __launch_bounds__(kThreads, MINB)
         }
         for (int b = 0; b < NSB; ++b) {
             mbar_init(bar(C::B_SFULL + b), 1);
-            mbar_init(bar(C::B_PFULL + b), 8);
+            mbar_init(bar(C::B_PFULL + b), R::kSoftmaxWarps);
             mbar_init(bar(C::B_PVDONE + b), 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(bar(C::B_TFULL + b), 1);
-            mbar_init(bar(C::B_TEMPTY + b), 9);
+            mbar_init(bar(C::B_TEMPTY + b), R::kSoftmaxWarps + 1);
         }
-        mbar_init(bar(C::B_OEMPTY), 8);
+        mbar_init(bar(C::B_OEMPTY), R::kSoftmaxWarps);
         mbar_init(bar(C::B_DRAIN), 1);
         for (int x = 0; x < 8; ++x) mbar_init(bar(C::B_XCH + x), 2);
         misc[1] = 0u;
@@ -358,21 +365,27 @@ __global__ void __launch_bounds__(kThreads, MINB)
             wait_bar_drain(bar(C::B_DRAIN), 0, p.wait_limit_ns);
         }
     } else {
-        // ------------------------------------------------------------ softmax + epilogue (warps 0-7)
-        // Warp w owns TMEM lanes 32*(w%4).. (query rows) and column half h = w/4 of
-        // S, P and O; the two warps of a row quarter exchange their half-row max
-        // (and, at the end, their sums) through shared memory guarded by mbarriers.
+        // ------------------------------------------------------------ softmax + epilogue
+        // Warp w owns TMEM lanes 32*(w%4).. (query rows) and column part h = w/4 of
+        // S, P and O (SPLIT parts per row). With SPLIT == 2 the two warps of a row
+        // quarter exchange their partial row max (and, at the end, their sums)
+        // through shared memory guarded by mbarriers.
         const int quarter = warp & 3, h = warp >> 2;
         const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
-        const uint32_t tS = tmem + lane_base + h * (BS / 2);        // this thread's S columns
-        const uint32_t tP = tmem + lane_base + h * (BS / 4);        // its P columns (bf16 pairs)
-        const uint32_t tO = tmem + lane_base + NSB * BS + h * (D / 2);
+        const uint32_t tS = tmem + lane_base + h * (BS / SPLIT);          // this thread's S columns
+        const uint32_t tP = tmem + lane_base + h * (BS / (2 * SPLIT));    // its P columns (bf16 pairs)
+        const uint32_t tO = tmem + lane_base + NSB * BS + h * (D / SPLIT);
         const uint32_t qblk = BS == 128 ? 0u : static_cast<uint32_t>(quarter >> 1);
         const int trow = quarter * 32 + lane;  // row within the tile
         float2 *xch = reinterpret_cast<float2 *>(smem + C::XCH_OFF);  // [slot][half][row]
         int X = 0;  // exchanges done (same sequence in both warps of the pair)
         // exchange one float2 with the partner warp; bounded wait
-        auto exchange = [&](float2 mine, float2 &theirs) -> bool {
+        // with SPLIT == 1 there is no partner: `theirs` is the operation's identity
+        auto exchange = [&](float2 mine, float2 identity, float2 &theirs) -> bool {
+            if (SPLIT == 1) {
+                theirs = identity;
+                return true;
+            }
             const int slot = X & 1;
             xch[(slot * 2 + h) * kTileM + trow] = mine;
             __syncwarp();
@@ -401,7 +414,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
             const int row = qt * kTileM + trow;
             const bool row_valid = row < p.N;
             const int64_t grow = bh * p.N + row;
-            __nv_bfloat16 *orow = p.O + grow * D + h * (D / 2);
+            __nv_bfloat16 *orow = p.O + grow * D + h * (D / SPLIT);
             TileWalk walk;
             walk_init<BS>(walk, p, bh, qt);
             int j;
@@ -411,7 +424,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
                 if (row_valid) {
                     uint4 z = make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
-                    for (int c = 0; c < D / 16; ++c) reinterpret_cast<uint4 *>(orow)[c] = z;
+                    for (int c = 0; c < D / (8 * SPLIT); ++c) reinterpret_cast<uint4 *>(orow)[c] = z;
                     if (h == 0) p.LSE[grow] = -CUDART_INF_F;
                 }
                 continue;
@@ -428,7 +441,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
                 bool resc = false;
                 float alpha = 1.0f;
                 if (active) {
-                    constexpr int NC = BS / 64;  // 32-column chunks of this half row
+                    constexpr int NC = BS / (32 * SPLIT);  // 32-column chunks of this row part
                     uint32_t sv[NC][32];
 #pragma unroll
                     for (int c = 0; c < NC; ++c) tmem_ld32(tS + b * BS + c * 32, sv[c]);
@@ -447,7 +460,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
                             mx3 = fmax3(mx3, __uint_as_float(sv[c][t + 6]), __uint_as_float(sv[c][t + 7]));
                         }
                     float2 other;
-                    if (!exchange(make_float2(fmax3(fmaxf(mx0, mx1), mx2, mx3), 0.0f), other)) { ok = false; break; }
+                    if (!exchange(make_float2(fmax3(fmaxf(mx0, mx1), mx2, mx3), 0.0f), make_float2(-CUDART_INF_F, 0.0f), other)) { ok = false; break; }
                     const float mx = fmax3(fmaxf(mx0, mx1), mx2, fmaxf(mx3, other.x));
                     const float m_tile = mx * p.scale_log2;
                     if (m_run == -CUDART_INF_F) {
@@ -493,7 +506,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
 #pragma unroll
                     for (int q = 0; q < 16; ++q) z[q] = 0u;
 #pragma unroll
-                    for (int c = 0; c < BS / 64; ++c) tmem_st16(tP + b * BS + c * 16, z);
+                    for (int c = 0; c < BS / (32 * SPLIT); ++c) tmem_st16(tP + b * BS + c * 16, z);
                 }
                 if (__any_sync(0xffffffffu, resc)) {
                     // O holds the previous blocks' sum: rescale it once the last PV landed
@@ -501,7 +514,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
                     if (!warp_wait(bar(C::B_PVDONE + t % NSB), (t / NSB) & 1, ctl, lane)) { ok = false; break; }
                     tc_fence_after();
 #pragma unroll
-                    for (int c = 0; c < D / 64; ++c) {
+                    for (int c = 0; c < D / (32 * SPLIT); ++c) {
                         uint32_t ov[32];
                         tmem_ld32(tO + c * 32, ov);
                         tmem_wait_ld();
@@ -520,14 +533,14 @@ __global__ void __launch_bounds__(kThreads, MINB)
             if (!ok) break;
             // ---------------- epilogue: O / l, LSE = ln2 * (m + log2 l) over the whole row
             float2 other;
-            if (!exchange(make_float2(l_run, lp_run), other)) break;
+            if (!exchange(make_float2(l_run, lp_run), make_float2(0.0f, 0.0f), other)) break;
             const float l_all = l_run + other.x, lp_all = lp_run + other.y;
             const int t = G - 1;
             if (!warp_wait(bar(C::B_PVDONE + t % NSB), (t / NSB) & 1, ctl, lane)) break;
             tc_fence_after();
             const float inv_l = lp_all > 0.0f ? 1.0f / lp_all : 0.0f;
 #pragma unroll
-            for (int c = 0; c < D / 64; ++c) {
+            for (int c = 0; c < D / (32 * SPLIT); ++c) {
                 uint32_t ov[32];
                 tmem_ld32(tO + c * 32, ov);
                 tmem_wait_ld();
@@ -663,14 +676,15 @@ bool make_map(CUtensorMap *m, const void *base, uint64_t rows, int d, int box_ro
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D, int BS, int NK, int NV, int NSB, int QS, int MINB>
+template <int D, int BS, int NK, int NV, int NSB, int QS, int SPLIT, int MINB>
 bsa_status launch_tc(const FwdArgs &a, cudaStream_t st)
 {
     using C = Cfg<D, BS, NK, NV, NSB, QS>;
+    constexpr int kThreads = Roles<SPLIT>::kThreads;
     static_assert(MINB * (C::SMEM_ALLOC + 1024) <= 233472, "shared memory for MINB CTAs per SM");
     static_assert(C::SMEM_ALLOC <= 227 * 1024, "shared memory budget");
     static_assert(C::TCOLS_USED <= C::TCOLS, "TMEM budget");
-    auto kern = fwd_tc_kernel<D, BS, NK, NV, NSB, QS, MINB>;
+    auto kern = fwd_tc_kernel<D, BS, NK, NV, NSB, QS, SPLIT, MINB>;
     static int grid_cap = 0;
     if (grid_cap == 0) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC) != cudaSuccess)
@@ -738,11 +752,11 @@ size_t fwd_workspace_bytes(int B, int H, int N, int d, int block)
 
 bsa_status launch_forward_tc(const FwdArgs &a, cudaStream_t st)
 {
-    // <D, BS, K stages, V stages, S/P buffers, Q slots, CTAs per SM>
-    if (a.d == 64 && a.block == 64) return launch_tc<64, 64, 4, 5, 3, 2, 2>(a, st);
-    if (a.d == 128 && a.block == 64) return launch_tc<128, 64, 2, 2, 2, 1, 2>(a, st);
-    if (a.d == 64 && a.block == 128) return launch_tc<64, 128, 5, 6, 3, 2, 1>(a, st);
-    if (a.d == 128 && a.block == 128) return launch_tc<128, 128, 2, 2, 3, 2, 1>(a, st);
+    // <D, BS, K stages, V stages, S/P buffers, Q slots, threads per row, CTAs per SM>
+    if (a.d == 64 && a.block == 64) return launch_tc<64, 64, 4, 5, 3, 2, 1, 2>(a, st);
+    if (a.d == 128 && a.block == 64) return launch_tc<128, 64, 2, 2, 2, 1, 1, 2>(a, st);
+    if (a.d == 64 && a.block == 128) return launch_tc<64, 128, 5, 6, 3, 2, 2, 1>(a, st);
+    if (a.d == 128 && a.block == 128) return launch_tc<128, 128, 2, 2, 3, 2, 2, 1>(a, st);
     return BSA_ERR_SHAPE;
 }
 
