@@ -177,6 +177,11 @@ bsa_status bsa_build_mask(const void *Q, const void *K, int dt, int B, int H, in
     }
     if (nnz > col_capacity) return BSA_ERR_CAPACITY;
     if (R * nB > INT32_MAX && (nnz < 0 || nnz > INT32_MAX)) return BSA_ERR_UNSUPPORTED;  // row_ptr is int32
+    // all argument checks passed: only now touch the device
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&a.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return BSA_ERR_CUDA;
     return bsa::launch_build_mask(a, static_cast<cudaStream_t>(stream));
 }
 

@@ -8,8 +8,11 @@
 // Design (GB300-first, not the pages' Triton/xFormers recipes):
 //   * Persistent CTAs pull 128-row query tiles from a longest-first list with an
 //     atomic counter (balances rows with very different active counts, §5.3).
-//   * Warp roles: warps 0-3 softmax + epilogue (thread = query row = TMEM lane),
-//     warp 4 TMA producer, warp 5 tcgen05 MMA issuer (one thread).
+//   * Warp roles: 4 or 8 softmax + epilogue warps, then one TMA producer warp and
+//     one tcgen05 MMA-issuing warp (one thread each). With 4 softmax warps a
+//     thread owns one query row (32x32b TMEM accesses); with 8, a thread owns two
+//     rows and a quarter of their columns (16x256b / 16x128b accesses) and a row's
+//     max and sums are combined over 4 lanes with shuffles.
 //   * Q tile and K/V blocks arrive by TMA (128-byte swizzle), K/V fetched by
 //     block index into separate K and V shared-memory rings (a K slot frees when
 //     its QK^T completes, a V slot when its PV completes).
@@ -78,11 +81,9 @@ struct Cfg {
     static constexpr int B_SFULL = B_VEMPTY + NV, B_PFULL = B_SFULL + NSB, B_PVDONE = B_SFULL + 2 * NSB;
     static constexpr int B_OEMPTY = B_SFULL + 3 * NSB, B_TFULL = B_OEMPTY + 1, B_TEMPTY = B_TFULL + 2;
     static constexpr int B_DRAIN = B_TEMPTY + 2;
-    static constexpr int B_XCH = B_DRAIN + 1;  // 4 row quarters x 2 slots: half-row exchange
-    static constexpr int NBAR = B_XCH + 8;
+    static constexpr int NBAR = B_DRAIN + 1;
     static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
-    static constexpr int XCH_OFF = MISC_OFF + 32;  // float2 [2 slots][2 halves][128 rows]
-    static constexpr int SMEM = XCH_OFF + 2 * 2 * kTileM * 8;
+    static constexpr int SMEM = MISC_OFF + 32;
     static constexpr int SMEM_ALLOC = SMEM + 1024;  // manual 1024-byte alignment
     static constexpr int TCOLS_USED = NSB * BS + D;
     static constexpr int TCOLS = TCOLS_USED <= 256 ? 256 : 512;
@@ -154,6 +155,379 @@ __device__ __forceinline__ void walk_init(TileWalk &w, const TcParams &p, int64_
     }
 }
 
+// ---------------------------------------------------------------- softmax roles
+//
+// Both variants process, per visited KV block, the S tile of their rows:
+// row max (skipped blocks are never visited, so they contribute nothing),
+// lazy running-max update, p = 2^(s * scale * log2 e - m) (one packed FFMA and
+// one ex2 per score), P packed to bf16 and stored over S in TMEM for the PV MMA,
+// and two running sums: the fp32 one for LSE and the bf16 one that normalises O
+// (P's rounding then cancels between numerator and denominator).
+
+template <class C>
+__device__ __forceinline__ uint32_t barrier_addr(uint32_t sbase, int idx)
+{
+    return sbase + C::BAR_OFF + 8u * idx;
+}
+
+// Fetch the next tile id from the scheduler ring (lane 0 waits, all lanes get it).
+template <class C>
+__device__ __forceinline__ bool fetch_tile(uint32_t sbase, volatile int32_t *tile_ids, const Ctl &ctl, int lane,
+                                           int &tcount, int &tile)
+{
+    const int slot = tcount & 1;
+    if (!warp_wait(barrier_addr<C>(sbase, C::B_TFULL + slot), (tcount >> 1) & 1, ctl, lane)) return false;
+    int t = 0;
+    if (lane == 0) {
+        t = tile_ids[slot];
+        mbar_arrive(barrier_addr<C>(sbase, C::B_TEMPTY + slot));
+    }
+    tile = __shfl_sync(0xffffffffu, t, 0);
+    ++tcount;
+    return true;
+}
+
+// SPLIT == 1: warp w (0-3) owns TMEM lanes 32w..32w+31; thread = one query row,
+// all BS columns of S (32x32b TMEM accesses).
+template <int D, int BS, int NSB, class C>
+__device__ __forceinline__ void softmax_rows(const TcParams &p, uint32_t sbase, uint32_t tmem,
+                                             volatile int32_t *tile_ids, const Ctl &ctl, int warp, int lane)
+{
+    auto bar = [&](int idx) -> uint32_t { return barrier_addr<C>(sbase, idx); };
+    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    const uint32_t tS = tmem + lane_base;
+    const uint32_t tO = tmem + lane_base + NSB * BS;
+    const uint32_t qblk = BS == 128 ? 0u : static_cast<uint32_t>(warp >> 1);
+    const int trow = warp * 32 + lane;
+    int G = 0, tcount = 0;
+    for (;;) {
+        int tile;
+        if (!fetch_tile<C>(sbase, tile_ids, ctl, lane, tcount, tile) || tile < 0) return;
+        int64_t bh;
+        int qt;
+        tile_coords(p, tile, bh, qt);
+        const int row = qt * kTileM + trow;
+        const bool row_valid = row < p.N;
+        const int64_t grow = bh * p.N + row;
+        __nv_bfloat16 *orow = p.O + grow * D;
+        TileWalk walk;
+        walk_init<BS>(walk, p, bh, qt);
+        int j;
+        uint32_t m;
+        if (!walk.next(j, m)) {
+            if (row_valid) {
+                const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+                for (int c = 0; c < D / 8; ++c) reinterpret_cast<uint4 *>(orow)[c] = z;
+                p.LSE[grow] = -CUDART_INF_F;
+            }
+            continue;
+        }
+        float m_run = -CUDART_INF_F, l_run = 0.0f, lp_run = 0.0f;
+        do {
+            const int b = G % NSB;
+            if (!warp_wait(bar(C::B_SFULL + b), (G / NSB) & 1, ctl, lane)) return;
+            tc_fence_after();
+            bool resc = false;
+            float alpha = 1.0f;
+            if ((m >> qblk) & 1u) {
+                constexpr int NC = BS / 32;
+                uint32_t sv[NC][32];
+#pragma unroll
+                for (int c = 0; c < NC; ++c) tmem_ld32(tS + b * BS + c * 32, sv[c]);
+                tmem_wait_ld();
+#pragma unroll
+                for (int c = 0; c < NC; ++c) reg_fence32(sv[c]);
+                float mx0 = -CUDART_INF_F, mx1 = -CUDART_INF_F, mx2 = -CUDART_INF_F, mx3 = -CUDART_INF_F;
+#pragma unroll
+                for (int c = 0; c < NC; ++c)
+#pragma unroll
+                    for (int t = 0; t < 32; t += 8) {
+                        mx0 = fmax3(mx0, __uint_as_float(sv[c][t]), __uint_as_float(sv[c][t + 1]));
+                        mx1 = fmax3(mx1, __uint_as_float(sv[c][t + 2]), __uint_as_float(sv[c][t + 3]));
+                        mx2 = fmax3(mx2, __uint_as_float(sv[c][t + 4]), __uint_as_float(sv[c][t + 5]));
+                        mx3 = fmax3(mx3, __uint_as_float(sv[c][t + 6]), __uint_as_float(sv[c][t + 7]));
+                    }
+                const float m_tile = fmax3(fmaxf(mx0, mx1), mx2, mx3) * p.scale_log2;
+                if (m_run == -CUDART_INF_F) {
+                    m_run = m_tile;
+                } else if (m_tile > m_run + kRescaleLog2) {
+                    alpha = ex2_approx(m_run - m_tile);
+                    l_run *= alpha;
+                    lp_run *= alpha;
+                    m_run = m_tile;
+                    resc = true;
+                }
+                const uint64_t c2x = f2_pack(p.scale_log2, p.scale_log2);
+                const uint64_t nm2 = f2_pack(-m_run, -m_run);
+                uint64_t acc[4], accp[4];
+#pragma unroll
+                for (int a = 0; a < 4; ++a) acc[a] = accp[a] = 0ull;
+#pragma unroll
+                for (int c = 0; c < NC; ++c) {
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int q = 0; q < 16; ++q) {
+                        float x0, x1;
+                        f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[c][2 * q]), __uint_as_float(sv[c][2 * q + 1])),
+                                         c2x, nm2),
+                                  x0, x1);
+                        const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+                        pk[q] = pack_bf16x2(p0, p1);
+                        acc[q & 3] = f2_add(acc[q & 3], f2_pack(p0, p1));
+                        accp[q & 3] = f2_add(accp[q & 3], f2_pack(__uint_as_float(pk[q] << 16),
+                                                                  __uint_as_float(pk[q] & 0xFFFF0000u)));
+                    }
+                    tmem_st16(tS + b * BS + c * 16, pk);
+                }
+                float e0, e1, e2, e3;
+                f2_unpack(f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3])), e0, e1);
+                f2_unpack(f2_add(f2_add(accp[0], accp[1]), f2_add(accp[2], accp[3])), e2, e3);
+                l_run += e0 + e1;
+                lp_run += e2 + e3;
+            } else {
+                uint32_t z[16];
+#pragma unroll
+                for (int q = 0; q < 16; ++q) z[q] = 0u;
+#pragma unroll
+                for (int c = 0; c < BS / 32; ++c) tmem_st16(tS + b * BS + c * 16, z);
+            }
+            if (__any_sync(0xffffffffu, resc)) {
+                // O holds the previous blocks' sum: rescale it once the last PV landed
+                const int t = G - 1;
+                if (!warp_wait(bar(C::B_PVDONE + t % NSB), (t / NSB) & 1, ctl, lane)) return;
+                tc_fence_after();
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t ov[32];
+                    tmem_ld32(tO + c * 32, ov);
+                    tmem_wait_ld();
+                    reg_fence32(ov);
+#pragma unroll
+                    for (int q = 0; q < 32; ++q) ov[q] = __float_as_uint(__uint_as_float(ov[q]) * alpha);
+                    tmem_st32(tO + c * 32, ov);
+                }
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(C::B_PFULL + b));
+            ++G;
+        } while (walk.next(j, m));
+        // epilogue: O / l, LSE = ln2 * (m + log2 l)
+        const int t = G - 1;
+        if (!warp_wait(bar(C::B_PVDONE + t % NSB), (t / NSB) & 1, ctl, lane)) return;
+        tc_fence_after();
+        const float inv_l = lp_run > 0.0f ? 1.0f / lp_run : 0.0f;
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+            uint32_t ov[32];
+            tmem_ld32(tO + c * 32, ov);
+            tmem_wait_ld();
+            reg_fence32(ov);
+            if (row_valid) {
+                uint32_t pk[16];
+#pragma unroll
+                for (int q = 0; q < 16; ++q)
+                    pk[q] = pack_bf16x2(__uint_as_float(ov[2 * q]) * inv_l, __uint_as_float(ov[2 * q + 1]) * inv_l);
+                uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) dst[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+            }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(C::B_OEMPTY));
+        if (row_valid) p.LSE[grow] = l_run > 0.0f ? (m_run + log2f(l_run)) * 0.69314718055994530942f : -CUDART_INF_F;
+    }
+}
+
+// SPLIT == 2: eight warps; warp w owns the 16 TMEM lanes 32*(w%4) + 16*(w/4)..
+// (16x256b / 16x128b accesses). Thread t holds rows t/4 and t/4 + 8 of that
+// group and, in every 8-column group of S and O, columns 2(t%4) and +1; a row's
+// max and sums are reduced over its 4 lanes with two shuffles.
+template <int D, int BS, int NSB, class C>
+__device__ __forceinline__ void softmax_quads(const TcParams &p, uint32_t sbase, uint32_t tmem,
+                                              volatile int32_t *tile_ids, const Ctl &ctl, int warp, int lane)
+{
+    auto bar = [&](int idx) -> uint32_t { return barrier_addr<C>(sbase, idx); };
+    constexpr int RS = BS / 8;  // 8-column groups of S
+    constexpr int RO = D / 8;   // 8-column groups of O
+    const int quarter = warp & 3;
+    const int lane0 = 32 * quarter + 16 * (warp >> 2);  // first tile row of this warp
+    const uint32_t tbase = tmem + (static_cast<uint32_t>(lane0) << 16);
+    const uint32_t tO = tbase + NSB * BS;
+    const int r_lo = lane0 + (lane >> 2);  // this thread's rows r_lo and r_lo + 8
+    const int cpair = 2 * (lane & 3);
+    const uint32_t qblk = BS == 128 ? 0u : static_cast<uint32_t>(quarter >> 1);
+    int G = 0, tcount = 0;
+    for (;;) {
+        int tile;
+        if (!fetch_tile<C>(sbase, tile_ids, ctl, lane, tcount, tile) || tile < 0) return;
+        int64_t bh;
+        int qt;
+        tile_coords(p, tile, bh, qt);
+        const int row_lo = qt * kTileM + r_lo, row_hi = row_lo + 8;
+        const bool lo_valid = row_lo < p.N, hi_valid = row_hi < p.N;
+        const int64_t g_lo = bh * p.N + row_lo, g_hi = g_lo + 8;
+        uint32_t *o_lo = reinterpret_cast<uint32_t *>(p.O + g_lo * D + cpair);
+        uint32_t *o_hi = reinterpret_cast<uint32_t *>(p.O + g_hi * D + cpair);
+        TileWalk walk;
+        walk_init<BS>(walk, p, bh, qt);
+        int j;
+        uint32_t m;
+        if (!walk.next(j, m)) {
+#pragma unroll
+            for (int g = 0; g < RO; ++g) {
+                if (lo_valid) o_lo[4 * g] = 0u;
+                if (hi_valid) o_hi[4 * g] = 0u;
+            }
+            if ((lane & 3) == 0) {
+                if (lo_valid) p.LSE[g_lo] = -CUDART_INF_F;
+                if (hi_valid) p.LSE[g_hi] = -CUDART_INF_F;
+            }
+            continue;
+        }
+        float m_lo = -CUDART_INF_F, m_hi = -CUDART_INF_F;
+        float l_lo = 0.0f, l_hi = 0.0f, lp_lo = 0.0f, lp_hi = 0.0f;  // this thread's columns only
+        do {
+            const int b = G % NSB;
+            if (!warp_wait(bar(C::B_SFULL + b), (G / NSB) & 1, ctl, lane)) return;
+            tc_fence_after();
+            bool resc = false;
+            float a_lo = 1.0f, a_hi = 1.0f;
+            if ((m >> qblk) & 1u) {
+                uint32_t sv[4 * RS];
+                tmem_ld_16x256b<RS>(tbase + b * BS, sv);
+                tmem_wait_ld();
+                reg_fence(sv);
+                float x0 = -CUDART_INF_F, x1 = -CUDART_INF_F, y0 = -CUDART_INF_F, y1 = -CUDART_INF_F;
+#pragma unroll
+                for (int g = 0; g < RS; g += 2) {
+                    x0 = fmax3(x0, __uint_as_float(sv[4 * g]), __uint_as_float(sv[4 * g + 1]));
+                    y0 = fmax3(y0, __uint_as_float(sv[4 * g + 2]), __uint_as_float(sv[4 * g + 3]));
+                    x1 = fmax3(x1, __uint_as_float(sv[4 * g + 4]), __uint_as_float(sv[4 * g + 5]));
+                    y1 = fmax3(y1, __uint_as_float(sv[4 * g + 6]), __uint_as_float(sv[4 * g + 7]));
+                }
+                float mx_lo = fmaxf(x0, x1), mx_hi = fmaxf(y0, y1);
+                mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, 1));
+                mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 1));
+                mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, 2));
+                mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 2));
+                const float t_lo = mx_lo * p.scale_log2, t_hi = mx_hi * p.scale_log2;
+                if (m_lo == -CUDART_INF_F) {
+                    m_lo = t_lo;
+                } else if (t_lo > m_lo + kRescaleLog2) {
+                    a_lo = ex2_approx(m_lo - t_lo);
+                    l_lo *= a_lo;
+                    lp_lo *= a_lo;
+                    m_lo = t_lo;
+                    resc = true;
+                }
+                if (m_hi == -CUDART_INF_F) {
+                    m_hi = t_hi;
+                } else if (t_hi > m_hi + kRescaleLog2) {
+                    a_hi = ex2_approx(m_hi - t_hi);
+                    l_hi *= a_hi;
+                    lp_hi *= a_hi;
+                    m_hi = t_hi;
+                    resc = true;
+                }
+                const uint64_t c2x = f2_pack(p.scale_log2, p.scale_log2);
+                const uint64_t nm_lo = f2_pack(-m_lo, -m_lo), nm_hi = f2_pack(-m_hi, -m_hi);
+                uint64_t acc_lo[2] = {0ull, 0ull}, acc_hi[2] = {0ull, 0ull};
+                uint64_t accp_lo[2] = {0ull, 0ull}, accp_hi[2] = {0ull, 0ull};
+                uint32_t pk[2 * RS];
+#pragma unroll
+                for (int g = 0; g < RS; ++g) {
+                    float x, y;
+                    f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[4 * g]), __uint_as_float(sv[4 * g + 1])), c2x, nm_lo),
+                              x, y);
+                    const float p0 = ex2_approx(x), p1 = ex2_approx(y);
+                    f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[4 * g + 2]), __uint_as_float(sv[4 * g + 3])), c2x,
+                                     nm_hi),
+                              x, y);
+                    const float p2 = ex2_approx(x), p3 = ex2_approx(y);
+                    pk[2 * g] = pack_bf16x2(p0, p1);      // row r_lo, packed column 4g + t%4
+                    pk[2 * g + 1] = pack_bf16x2(p2, p3);  // row r_lo + 8
+                    acc_lo[g & 1] = f2_add(acc_lo[g & 1], f2_pack(p0, p1));
+                    acc_hi[g & 1] = f2_add(acc_hi[g & 1], f2_pack(p2, p3));
+                    accp_lo[g & 1] = f2_add(accp_lo[g & 1], f2_pack(__uint_as_float(pk[2 * g] << 16),
+                                                                    __uint_as_float(pk[2 * g] & 0xFFFF0000u)));
+                    accp_hi[g & 1] = f2_add(accp_hi[g & 1], f2_pack(__uint_as_float(pk[2 * g + 1] << 16),
+                                                                    __uint_as_float(pk[2 * g + 1] & 0xFFFF0000u)));
+                }
+                tmem_st_16x128b<RS>(tbase + b * BS, pk);
+                float u0, u1;
+                f2_unpack(f2_add(acc_lo[0], acc_lo[1]), u0, u1);
+                l_lo += u0 + u1;
+                f2_unpack(f2_add(acc_hi[0], acc_hi[1]), u0, u1);
+                l_hi += u0 + u1;
+                f2_unpack(f2_add(accp_lo[0], accp_lo[1]), u0, u1);
+                lp_lo += u0 + u1;
+                f2_unpack(f2_add(accp_hi[0], accp_hi[1]), u0, u1);
+                lp_hi += u0 + u1;
+            } else {
+                uint32_t z[2 * RS];
+#pragma unroll
+                for (int q = 0; q < 2 * RS; ++q) z[q] = 0u;
+                tmem_st_16x128b<RS>(tbase + b * BS, z);
+            }
+            if (__any_sync(0xffffffffu, resc)) {
+                const int t = G - 1;
+                if (!warp_wait(bar(C::B_PVDONE + t % NSB), (t / NSB) & 1, ctl, lane)) return;
+                tc_fence_after();
+                uint32_t ov[4 * RO];
+                tmem_ld_16x256b<RO>(tO, ov);
+                tmem_wait_ld();
+                reg_fence(ov);
+#pragma unroll
+                for (int g = 0; g < RO; ++g) {
+                    ov[4 * g] = __float_as_uint(__uint_as_float(ov[4 * g]) * a_lo);
+                    ov[4 * g + 1] = __float_as_uint(__uint_as_float(ov[4 * g + 1]) * a_lo);
+                    ov[4 * g + 2] = __float_as_uint(__uint_as_float(ov[4 * g + 2]) * a_hi);
+                    ov[4 * g + 3] = __float_as_uint(__uint_as_float(ov[4 * g + 3]) * a_hi);
+                }
+                tmem_st_16x256b<RO>(tO, ov);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(C::B_PFULL + b));
+            ++G;
+        } while (walk.next(j, m));
+        // epilogue: whole-row sums over the 4 lanes of each row, then O / l and LSE
+#pragma unroll
+        for (int o = 1; o <= 2; o <<= 1) {
+            l_lo += __shfl_xor_sync(0xffffffffu, l_lo, o);
+            l_hi += __shfl_xor_sync(0xffffffffu, l_hi, o);
+            lp_lo += __shfl_xor_sync(0xffffffffu, lp_lo, o);
+            lp_hi += __shfl_xor_sync(0xffffffffu, lp_hi, o);
+        }
+        const int t = G - 1;
+        if (!warp_wait(bar(C::B_PVDONE + t % NSB), (t / NSB) & 1, ctl, lane)) return;
+        tc_fence_after();
+        uint32_t ov[4 * RO];
+        tmem_ld_16x256b<RO>(tO, ov);
+        tmem_wait_ld();
+        reg_fence(ov);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(C::B_OEMPTY));
+        const float i_lo = lp_lo > 0.0f ? 1.0f / lp_lo : 0.0f, i_hi = lp_hi > 0.0f ? 1.0f / lp_hi : 0.0f;
+#pragma unroll
+        for (int g = 0; g < RO; ++g) {
+            if (lo_valid) o_lo[4 * g] = pack_bf16x2(__uint_as_float(ov[4 * g]) * i_lo, __uint_as_float(ov[4 * g + 1]) * i_lo);
+            if (hi_valid)
+                o_hi[4 * g] = pack_bf16x2(__uint_as_float(ov[4 * g + 2]) * i_hi, __uint_as_float(ov[4 * g + 3]) * i_hi);
+        }
+        if ((lane & 3) == 0) {
+            if (lo_valid) p.LSE[g_lo] = l_lo > 0.0f ? (m_lo + log2f(l_lo)) * 0.69314718055994530942f : -CUDART_INF_F;
+            if (hi_valid) p.LSE[g_hi] = l_hi > 0.0f ? (m_hi + log2f(l_hi)) * 0.69314718055994530942f : -CUDART_INF_F;
+        }
+    }
+}
+
 template <int D, int BS, int NK, int NV, int NSB, int QS, int SPLIT, int MINB>
 __global__ void __launch_bounds__((4 * SPLIT + 2) * 32, MINB)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -196,7 +570,6 @@ __global__ void __launch_bounds__((4 * SPLIT + 2) * 32, MINB)
         }
         mbar_init(bar(C::B_OEMPTY), R::kSoftmaxWarps);
         mbar_init(bar(C::B_DRAIN), 1);
-        for (int x = 0; x < 8; ++x) mbar_init(bar(C::B_XCH + x), 2);
         misc[1] = 0u;
         fence_mbar_init();
     }
@@ -337,6 +710,9 @@ __global__ void __launch_bounds__((4 * SPLIT + 2) * 32, MINB)
                 const uint32_t qbase = sbase + C::Q_OFF + qs * C::kQBytes;
                 const int G0 = G;
                 do {
+                    // With a single S/P buffer the previous block's PV must be issued
+                    // before QK^T overwrites the buffer it reads P from.
+                    if (NSB == 1 && G > G0 && !issue_pv(G - 1, G - 1 == G0)) { ok = false; break; }
                     const int s = G % NK, b = G % NSB;
                     if (!wait_bar(bar(C::B_KFULL + s), (G / NK) & 1, ctl)) { ok = false; break; }
                     // S/P buffer b was last read by PV(G - NSB)
@@ -352,7 +728,7 @@ __global__ void __launch_bounds__((4 * SPLIT + 2) * 32, MINB)
                     }
                     tc_commit(bar(C::B_SFULL + b));
                     tc_commit(bar(C::B_KEMPTY + s));
-                    if (G > G0 && !issue_pv(G - 1, G - 1 == G0)) { ok = false; break; }
+                    if (NSB > 1 && G > G0 && !issue_pv(G - 1, G - 1 == G0)) { ok = false; break; }
                     ++G;
                 } while (walk.next(j, m));
                 if (!ok) break;
@@ -366,202 +742,10 @@ __global__ void __launch_bounds__((4 * SPLIT + 2) * 32, MINB)
         }
     } else {
         // ------------------------------------------------------------ softmax + epilogue
-        // Warp w owns TMEM lanes 32*(w%4).. (query rows) and column part h = w/4 of
-        // S, P and O (SPLIT parts per row). With SPLIT == 2 the two warps of a row
-        // quarter exchange their partial row max (and, at the end, their sums)
-        // through shared memory guarded by mbarriers.
-        const int quarter = warp & 3, h = warp >> 2;
-        const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
-        const uint32_t tS = tmem + lane_base + h * (BS / SPLIT);          // this thread's S columns
-        const uint32_t tP = tmem + lane_base + h * (BS / (2 * SPLIT));    // its P columns (bf16 pairs)
-        const uint32_t tO = tmem + lane_base + NSB * BS + h * (D / SPLIT);
-        const uint32_t qblk = BS == 128 ? 0u : static_cast<uint32_t>(quarter >> 1);
-        const int trow = quarter * 32 + lane;  // row within the tile
-        float2 *xch = reinterpret_cast<float2 *>(smem + C::XCH_OFF);  // [slot][half][row]
-        int X = 0;  // exchanges done (same sequence in both warps of the pair)
-        // exchange one float2 with the partner warp; bounded wait
-        // with SPLIT == 1 there is no partner: `theirs` is the operation's identity
-        auto exchange = [&](float2 mine, float2 identity, float2 &theirs) -> bool {
-            if (SPLIT == 1) {
-                theirs = identity;
-                return true;
-            }
-            const int slot = X & 1;
-            xch[(slot * 2 + h) * kTileM + trow] = mine;
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(C::B_XCH + quarter * 2 + slot));
-            const bool okx = warp_wait(bar(C::B_XCH + quarter * 2 + slot), (X >> 1) & 1, ctl, lane);
-            theirs = xch[(slot * 2 + (h ^ 1)) * kTileM + trow];
-            ++X;
-            return okx;
-        };
-        int G = 0, e = 0, tcount = 0;
-        bool ok = true;
-        while (ok) {
-            const int slot = tcount & 1;
-            if (!warp_wait(bar(C::B_TFULL + slot), (tcount >> 1) & 1, ctl, lane)) break;
-            int tile = 0;
-            if (lane == 0) {
-                tile = tile_ids[slot];
-                mbar_arrive(bar(C::B_TEMPTY + slot));
-            }
-            tile = __shfl_sync(0xffffffffu, tile, 0);
-            ++tcount;
-            if (tile < 0) break;
-            int64_t bh;
-            int qt;
-            tile_coords(p, tile, bh, qt);
-            const int row = qt * kTileM + trow;
-            const bool row_valid = row < p.N;
-            const int64_t grow = bh * p.N + row;
-            __nv_bfloat16 *orow = p.O + grow * D + h * (D / SPLIT);
-            TileWalk walk;
-            walk_init<BS>(walk, p, bh, qt);
-            int j;
-            uint32_t m;
-            if (!walk.next(j, m)) {
-                // no active block anywhere in the tile: O = 0, LSE = -inf
-                if (row_valid) {
-                    uint4 z = make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll
-                    for (int c = 0; c < D / (8 * SPLIT); ++c) reinterpret_cast<uint4 *>(orow)[c] = z;
-                    if (h == 0) p.LSE[grow] = -CUDART_INF_F;
-                }
-                continue;
-            }
-            // l_run: sum of the fp32 probabilities (for LSE); lp_run: sum of the bf16
-            // probabilities the PV MMA consumes (normaliser of O, so rounding of P
-            // cancels between numerator and denominator). Both cover this half row.
-            float m_run = -CUDART_INF_F, l_run = 0.0f, lp_run = 0.0f;
-            do {
-                const int b = G % NSB;
-                if (!warp_wait(bar(C::B_SFULL + b), (G / NSB) & 1, ctl, lane)) { ok = false; break; }
-                tc_fence_after();
-                const bool active = ((m >> qblk) & 1u) != 0u;
-                bool resc = false;
-                float alpha = 1.0f;
-                if (active) {
-                    constexpr int NC = BS / (32 * SPLIT);  // 32-column chunks of this row part
-                    uint32_t sv[NC][32];
-#pragma unroll
-                    for (int c = 0; c < NC; ++c) tmem_ld32(tS + b * BS + c * 32, sv[c]);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int c = 0; c < NC; ++c) reg_fence32(sv[c]);
-                    // half-row max: four independent three-input max chains
-                    float mx0 = -CUDART_INF_F, mx1 = -CUDART_INF_F, mx2 = -CUDART_INF_F, mx3 = -CUDART_INF_F;
-#pragma unroll
-                    for (int c = 0; c < NC; ++c)
-#pragma unroll
-                        for (int t = 0; t < 32; t += 8) {
-                            mx0 = fmax3(mx0, __uint_as_float(sv[c][t]), __uint_as_float(sv[c][t + 1]));
-                            mx1 = fmax3(mx1, __uint_as_float(sv[c][t + 2]), __uint_as_float(sv[c][t + 3]));
-                            mx2 = fmax3(mx2, __uint_as_float(sv[c][t + 4]), __uint_as_float(sv[c][t + 5]));
-                            mx3 = fmax3(mx3, __uint_as_float(sv[c][t + 6]), __uint_as_float(sv[c][t + 7]));
-                        }
-                    float2 other;
-                    if (!exchange(make_float2(fmax3(fmaxf(mx0, mx1), mx2, mx3), 0.0f), make_float2(-CUDART_INF_F, 0.0f), other)) { ok = false; break; }
-                    const float mx = fmax3(fmaxf(mx0, mx1), mx2, fmaxf(mx3, other.x));
-                    const float m_tile = mx * p.scale_log2;
-                    if (m_run == -CUDART_INF_F) {
-                        m_run = m_tile;
-                    } else if (m_tile > m_run + kRescaleLog2) {
-                        alpha = ex2_approx(m_run - m_tile);
-                        l_run *= alpha;
-                        lp_run *= alpha;
-                        m_run = m_tile;
-                        resc = true;
-                    }
-                    // p = 2^(s * scale * log2 e - m): one packed FFMA per pair, one ex2 each;
-                    // four independent packed accumulators per sum
-                    const uint64_t c2x = f2_pack(p.scale_log2, p.scale_log2);
-                    const uint64_t nm2 = f2_pack(-m_run, -m_run);
-                    uint64_t acc[4], accp[4];
-#pragma unroll
-                    for (int a = 0; a < 4; ++a) acc[a] = accp[a] = 0ull;
-#pragma unroll
-                    for (int c = 0; c < NC; ++c) {
-                        uint32_t pk[16];
-#pragma unroll
-                        for (int q = 0; q < 16; ++q) {
-                            const uint64_t s2 =
-                                f2_pack(__uint_as_float(sv[c][2 * q]), __uint_as_float(sv[c][2 * q + 1]));
-                            float x0, x1;
-                            f2_unpack(f2_fma(s2, c2x, nm2), x0, x1);
-                            const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
-                            pk[q] = pack_bf16x2(p0, p1);
-                            acc[q & 3] = f2_add(acc[q & 3], f2_pack(p0, p1));
-                            accp[q & 3] = f2_add(accp[q & 3], f2_pack(__uint_as_float(pk[q] << 16),
-                                                                      __uint_as_float(pk[q] & 0xFFFF0000u)));
-                        }
-                        tmem_st16(tP + b * BS + c * 16, pk);
-                    }
-                    float e0, e1, e2, e3;
-                    f2_unpack(f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3])), e0, e1);
-                    f2_unpack(f2_add(f2_add(accp[0], accp[1]), f2_add(accp[2], accp[3])), e2, e3);
-                    l_run += e0 + e1;
-                    lp_run += e2 + e3;
-                } else {
-                    uint32_t z[16];
-#pragma unroll
-                    for (int q = 0; q < 16; ++q) z[q] = 0u;
-#pragma unroll
-                    for (int c = 0; c < BS / (32 * SPLIT); ++c) tmem_st16(tP + b * BS + c * 16, z);
-                }
-                if (__any_sync(0xffffffffu, resc)) {
-                    // O holds the previous blocks' sum: rescale it once the last PV landed
-                    const int t = G - 1;
-                    if (!warp_wait(bar(C::B_PVDONE + t % NSB), (t / NSB) & 1, ctl, lane)) { ok = false; break; }
-                    tc_fence_after();
-#pragma unroll
-                    for (int c = 0; c < D / (32 * SPLIT); ++c) {
-                        uint32_t ov[32];
-                        tmem_ld32(tO + c * 32, ov);
-                        tmem_wait_ld();
-                        reg_fence32(ov);
-#pragma unroll
-                        for (int q = 0; q < 32; ++q) ov[q] = __float_as_uint(__uint_as_float(ov[q]) * alpha);
-                        tmem_st32(tO + c * 32, ov);
-                    }
-                }
-                tmem_wait_st();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar(C::B_PFULL + b));
-                ++G;
-            } while (walk.next(j, m));
-            if (!ok) break;
-            // ---------------- epilogue: O / l, LSE = ln2 * (m + log2 l) over the whole row
-            float2 other;
-            if (!exchange(make_float2(l_run, lp_run), make_float2(0.0f, 0.0f), other)) break;
-            const float l_all = l_run + other.x, lp_all = lp_run + other.y;
-            const int t = G - 1;
-            if (!warp_wait(bar(C::B_PVDONE + t % NSB), (t / NSB) & 1, ctl, lane)) break;
-            tc_fence_after();
-            const float inv_l = lp_all > 0.0f ? 1.0f / lp_all : 0.0f;
-#pragma unroll
-            for (int c = 0; c < D / (32 * SPLIT); ++c) {
-                uint32_t ov[32];
-                tmem_ld32(tO + c * 32, ov);
-                tmem_wait_ld();
-                reg_fence32(ov);
-                if (row_valid) {
-                    uint32_t pk[16];
-#pragma unroll
-                    for (int q = 0; q < 16; ++q)
-                        pk[q] = pack_bf16x2(__uint_as_float(ov[2 * q]) * inv_l, __uint_as_float(ov[2 * q + 1]) * inv_l);
-                    uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) dst[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
-                }
-            }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(C::B_OEMPTY));
-            if (row_valid && h == 0)
-                p.LSE[grow] = l_all > 0.0f ? (m_run + log2f(l_all)) * 0.69314718055994530942f : -CUDART_INF_F;
-            ++e;
-        }
+        if constexpr (SPLIT == 1)
+            softmax_rows<D, BS, NSB, C>(p, sbase, tmem, tile_ids, ctl, warp, lane);
+        else
+            softmax_quads<D, BS, NSB, C>(p, sbase, tmem, tile_ids, ctl, warp, lane);
     }
 
     tc_fence_before();
@@ -596,18 +780,26 @@ __device__ __forceinline__ int tile_length(const TcParams &p, int tile, int BS)
 }
 
 // Longest-first tile list (counting sort by active-block count, clamped) and
-// reset of the scheduler counter. One CTA.
-__global__ void __launch_bounds__(1024) tile_order_kernel(TcParams p, int BS, int32_t *tile_list)
+// reset of the scheduler counter, in one launch: every CTA computes the lengths
+// of its 1024 tiles; the CTA that finishes last sorts them.
+__global__ void __launch_bounds__(1024) tile_order_kernel(TcParams p, int BS, int32_t *tile_list, int32_t *lens,
+                                                          uint32_t *done)
 {
     __shared__ int hist[kBuckets];
     __shared__ int wsum[32];
+    __shared__ bool is_last;
     const int t = threadIdx.x;
+    const int tile0 = blockIdx.x * 1024 + t;
+    if (tile0 < p.n_tiles) lens[tile0] = min(tile_length(p, tile0, BS), kBuckets - 1);
+    __threadfence();
+    __syncthreads();
+    if (t == 0) is_last = atomicAdd(done, 1u) == gridDim.x - 1;
+    __syncthreads();
+    if (!is_last) return;
+    __threadfence();
     for (int b = t; b < kBuckets; b += 1024) hist[b] = 0;
     __syncthreads();
-    for (int tile = t; tile < p.n_tiles; tile += 1024) {
-        const int len = min(tile_length(p, tile, BS), kBuckets - 1);
-        atomicAdd(&hist[kBuckets - 1 - len], 1);
-    }
+    for (int tile = t; tile < p.n_tiles; tile += 1024) atomicAdd(&hist[kBuckets - 1 - __ldcg(lens + tile)], 1);
     __syncthreads();
     // exclusive scan of hist (one bucket per thread)
     const int v = hist[t];
@@ -621,13 +813,13 @@ __global__ void __launch_bounds__(1024) tile_order_kernel(TcParams p, int BS, in
     if (lane == 31) wsum[warp] = x;
     __syncthreads();
     if (warp == 0) {
-        int s = wsum[lane];
+        int s2 = wsum[lane];
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            const int y = __shfl_up_sync(0xffffffffu, s, o);
-            if (lane >= o) s += y;
+            const int y = __shfl_up_sync(0xffffffffu, s2, o);
+            if (lane >= o) s2 += y;
         }
-        wsum[lane] = s;
+        wsum[lane] = s2;
     }
     __syncthreads();
     const int excl = x - v + (warp > 0 ? wsum[warp - 1] : 0);
@@ -635,11 +827,13 @@ __global__ void __launch_bounds__(1024) tile_order_kernel(TcParams p, int BS, in
     hist[t] = excl;
     __syncthreads();
     for (int tile = t; tile < p.n_tiles; tile += 1024) {
-        const int len = min(tile_length(p, tile, BS), kBuckets - 1);
-        const int pos = atomicAdd(&hist[kBuckets - 1 - len], 1);
+        const int pos = atomicAdd(&hist[kBuckets - 1 - __ldcg(lens + tile)], 1);
         tile_list[pos] = tile;
     }
-    if (t == 0) *p.tile_counter = 0u;
+    if (t == 0) {
+        *p.tile_counter = 0u;
+        *done = 0u;
+    }
 }
 
 // ---------------------------------------------------------------- host side
@@ -729,12 +923,14 @@ bsa_status launch_tc(const FwdArgs &a, cudaStream_t st)
     p.scale_log2 = a.scale * 1.4426950408889634f;
     p.O = static_cast<__nv_bfloat16 *>(a.O);
     p.LSE = a.LSE;
-    p.tile_list = reinterpret_cast<const int32_t *>(a.ws + kWsHeader);
+    int32_t *tile_list = reinterpret_cast<int32_t *>(a.ws + kWsHeader);
+    int32_t *lens = tile_list + align_up(static_cast<size_t>(p.n_tiles), 64);
+    p.tile_list = tile_list;
     p.tile_counter = &hdr->tile_counter;
     p.err = &hdr->err;
     p.wait_limit_ns = a.wait_limit_ns;
     p.dbg = a.dbg_flags;
-    tile_order_kernel<<<1, 1024, 0, st>>>(p, BS, reinterpret_cast<int32_t *>(a.ws + kWsHeader));
+    tile_order_kernel<<<(p.n_tiles + 1023) / 1024, 1024, 0, st>>>(p, BS, tile_list, lens, &hdr->order_done);
     const int grid = static_cast<int>(p.n_tiles < grid_cap ? p.n_tiles : grid_cap);
     kern<<<grid, kThreads, C::SMEM_ALLOC, st>>>(mq, mk, mv, p);
     return cudaGetLastError() == cudaSuccess ? BSA_OK : BSA_ERR_CUDA;
@@ -747,7 +943,8 @@ size_t fwd_workspace_bytes(int B, int H, int N, int d, int block)
     (void)d;
     (void)block;
     const size_t tiles = static_cast<size_t>(B) * H * ((N + kTileM - 1) / kTileM);
-    return kWsHeader + align_up(tiles * sizeof(int32_t), 256);
+    // tile list, then per-tile lengths
+    return kWsHeader + align_up(align_up(tiles, 64) * sizeof(int32_t) + tiles * sizeof(int32_t), 256);
 }
 
 bsa_status launch_forward_tc(const FwdArgs &a, cudaStream_t st)
@@ -756,7 +953,7 @@ bsa_status launch_forward_tc(const FwdArgs &a, cudaStream_t st)
     if (a.d == 64 && a.block == 64) return launch_tc<64, 64, 4, 5, 3, 2, 1, 2>(a, st);
     if (a.d == 128 && a.block == 64) return launch_tc<128, 64, 2, 2, 2, 1, 1, 2>(a, st);
     if (a.d == 64 && a.block == 128) return launch_tc<64, 128, 5, 6, 3, 2, 2, 1>(a, st);
-    if (a.d == 128 && a.block == 128) return launch_tc<128, 128, 2, 2, 3, 2, 2, 1>(a, st);
+    if (a.d == 128 && a.block == 128) return launch_tc<128, 128, 3, 2, 3, 1, 2, 1>(a, st);
     return BSA_ERR_SHAPE;
 }
 

@@ -14,12 +14,13 @@ namespace bsa {
 struct WsHeader {
     uint32_t err;          // first device-raised bsa_status (0 = none)
     uint32_t tile_counter; // forward: dynamic tile scheduler counter
-    uint32_t pad[62];
+    uint32_t order_done;   // CTAs of a last-CTA-finishes launch that are done (tile order, static pattern)
+    uint32_t pad[61];
 };
 static_assert(sizeof(WsHeader) == 256, "workspace header is 256 bytes");
 
 constexpr size_t kWsHeader = 256;
-constexpr int kMaxKvBlocks = 4096;     // nKB limit of the selector (scores row in smem)
+constexpr int kMaxKvBlocks = 2048;     // nKB limit of the selector (16 score rows in smem)
 constexpr uint64_t kDefaultWaitNs = 2000000000ull;  // bounded device waits: 2 s
 
 // Records `code` as the workspace's device error unless one is already set.
@@ -41,6 +42,7 @@ struct MaskArgs {
     int64_t col_capacity;
     uint32_t *bitmap;
     char *ws;              // workspace base (device)
+    int sm_count;          // streaming multiprocessors of the current device
 };
 
 size_t mask_workspace_bytes(int B, int H, int N, int d, int block);

@@ -9,8 +9,10 @@
 // Static mode evaluates the block predicates of "多模态DiT中的块稀疏注意力" §3.1-§3.2
 // (text dense + image band + anchors, or video cuboids + faces + text) or copies
 // an explicit bitmap:
-//   static_rows_kernel -> bitmap + per-row counts; scan_kernel -> row_ptr;
-//   emit_kernel -> col_idx ascending (§4.1 index forms).
+//   pattern_kernel + emit_pattern_kernel (one pattern for every head: band, cuboid,
+//   broadcast bitmap): build it once, copy it into every head; per-head bitmaps use
+//   static_rows_kernel -> counts, scan_kernel -> row_ptr, emit_kernel -> col_idx
+//   ascending (§4.1 index forms).
 // Arithmetic of the selector is fixed so results are reproducible bit for bit:
 // pooled sums in token order with round-to-nearest adds, scaled by 1/bs (exact);
 // scores as an fmaf chain over channels from +0; order by value with -0 == +0,
@@ -24,8 +26,6 @@ namespace bsa {
 namespace {
 
 constexpr int kPoolThreads = 128;
-constexpr int kRowsPerCta = 8;   // Q blocks per score/top-k CTA (one warp each)
-constexpr int kKvTile = 32;      // KV blocks staged per step
 
 __device__ __forceinline__ uint32_t lanemask_lt()
 {
@@ -102,50 +102,11 @@ __device__ __forceinline__ uint32_t order_key(float s)
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-__global__ void __launch_bounds__(256) score_topk_kernel(const float *__restrict__ qbar,
-                                                         const float *__restrict__ kbar, int nQB,
-                                                         int nKB, int d, int k, int W,
-                                                         int32_t *__restrict__ row_ptr,
-                                                         int32_t *__restrict__ col_idx,
-                                                         uint32_t *__restrict__ bitmap, uint32_t *err)
+// Exact top-k of one row of order keys held in shared memory (one warp): the k
+// largest (key, -index) pairs, written as a bitmap row and an ascending CSR row.
+__device__ void select_row(const uint32_t *row, int nKB, int k, int W, int64_t r_global,
+                           int32_t *__restrict__ col_idx, uint32_t *__restrict__ bitmap, int lane)
 {
-    extern __shared__ float sm[];
-    float *qs = sm;                                  // [8][d]
-    float *ks = qs + kRowsPerCta * d;                // [32][d + 1]
-    uint32_t *keys = reinterpret_cast<uint32_t *>(ks + kKvTile * (d + 1));  // [8][nKB]
-    const int bh = blockIdx.y;
-    const int i0 = blockIdx.x * kRowsPerCta;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-    for (int e = threadIdx.x; e < kRowsPerCta * d; e += blockDim.x) {
-        const int r = e / d, c = e % d;
-        qs[e] = (i0 + r < nQB) ? qbar[(static_cast<int64_t>(bh) * nQB + i0 + r) * d + c] : 0.0f;
-    }
-    bool nan_seen = false;
-    for (int j0 = 0; j0 < nKB; j0 += kKvTile) {
-        __syncthreads();
-        for (int e = threadIdx.x; e < kKvTile * d; e += blockDim.x) {
-            const int jj = e / d, c = e % d;
-            ks[jj * (d + 1) + c] =
-                (j0 + jj < nKB) ? kbar[(static_cast<int64_t>(bh) * nKB + j0 + jj) * d + c] : 0.0f;
-        }
-        __syncthreads();
-        const int r = warp, j = j0 + lane;
-        if (i0 + r < nQB && j < nKB) {
-            const float *a = qs + r * d;
-            const float *b = ks + lane * (d + 1);
-            float acc = 0.0f;
-            for (int c = 0; c < d; ++c) acc = __fmaf_rn(a[c], b[c], acc);
-            nan_seen |= isnan(acc);
-            keys[r * nKB + j] = order_key(acc);
-        }
-    }
-    if (nan_seen) raise_error(err, BSA_ERR_NONFINITE);
-    __syncthreads();
-
-    const int i = i0 + warp;
-    if (i >= nQB) return;
-    const uint32_t *row = keys + warp * nKB;
     // Largest T with #{key >= T} >= k: the k-th largest key value.
     uint32_t T = 0;
     for (int bit = 31; bit >= 0; --bit) {
@@ -159,7 +120,6 @@ __global__ void __launch_bounds__(256) score_topk_kernel(const float *__restrict
     for (int j = lane; j < nKB; j += 32) gt += row[j] > T;
     gt = __reduce_add_sync(0xffffffffu, gt);
     const int need = k - gt;  // how many of the keys equal to T, lowest index first
-    const int64_t r_global = static_cast<int64_t>(bh) * nQB + i;
     const int64_t out_base = r_global * k;
     int taken = 0, ties = 0;
     for (int w = 0; w < W; ++w) {
@@ -176,10 +136,103 @@ __global__ void __launch_bounds__(256) score_topk_kernel(const float *__restrict
         taken += __popc(sel_mask);
         ties += __popc(eq_mask);
     }
-    if (lane == 0) {
-        row_ptr[r_global] = static_cast<int32_t>(out_base);
-        if (r_global == static_cast<int64_t>(gridDim.y) * nQB - 1)
-            row_ptr[r_global + 1] = static_cast<int32_t>(out_base + k);
+}
+
+// Scores of 16 Q blocks against every KV block of one (b, h), then top-k per row.
+// Thread (warp w, lane l) computes rows 2w, 2w+1 against KV blocks l + 32n of a
+// 128-block tile staged in shared memory, 4 channels per 128-bit load; each
+// score is still one fmaf chain over channels 0..d-1 in order.
+constexpr int kScoreRows = 16;
+constexpr int kScoreTile = 128;
+
+__global__ void __launch_bounds__(256) score_topk_kernel(const float *__restrict__ qbar,
+                                                         const float *__restrict__ kbar, int nQB,
+                                                         int nKB, int d, int k, int W,
+                                                         int32_t *__restrict__ row_ptr,
+                                                         int32_t *__restrict__ col_idx,
+                                                         uint32_t *__restrict__ bitmap, uint32_t *err)
+{
+    extern __shared__ float4 sm4[];
+    const int dp = d + 4;                      // padded row stride (floats): conflict-free 128-bit loads
+    float *qs = reinterpret_cast<float *>(sm4);        // [16][dp]
+    float *ks = qs + kScoreRows * dp;                   // [128][dp]
+    uint32_t *keys = reinterpret_cast<uint32_t *>(ks + kScoreTile * dp);  // [16][nKB]
+    const int bh = blockIdx.y;
+    const int i0 = blockIdx.x * kScoreRows;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int d4 = d / 4;
+
+    for (int e = threadIdx.x; e < kScoreRows * d4; e += blockDim.x) {
+        const int r = e / d4, c4 = e % d4;
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (i0 + r < nQB) v = reinterpret_cast<const float4 *>(qbar + (static_cast<int64_t>(bh) * nQB + i0 + r) * d)[c4];
+        reinterpret_cast<float4 *>(qs + r * dp)[c4] = v;
+    }
+    bool nan_seen = false;
+    const int r0 = 2 * warp;
+    for (int j0 = 0; j0 < nKB; j0 += kScoreTile) {
+        __syncthreads();
+        // stage the tile: all of a thread's 128-bit loads in flight before any store
+        const float4 *src = reinterpret_cast<const float4 *>(kbar + (static_cast<int64_t>(bh) * nKB + j0) * d);
+        const int n4 = min(kScoreTile, nKB - j0) * d4;
+        for (int e0 = 0; e0 < kScoreTile * d4; e0 += 8 * 256) {
+            float4 v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int e = e0 + u * 256 + threadIdx.x;
+                v[u] = e < n4 ? __ldg(src + e) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int e = e0 + u * 256 + threadIdx.x;
+                if (e < kScoreTile * d4) reinterpret_cast<float4 *>(ks + (e / d4) * dp)[e % d4] = v[u];
+            }
+        }
+        __syncthreads();
+        float acc[2][4];
+#pragma unroll
+        for (int a = 0; a < 2; ++a)
+#pragma unroll
+            for (int n = 0; n < 4; ++n) acc[a][n] = 0.0f;
+        for (int c4 = 0; c4 < d4; ++c4) {
+            const float4 qa = reinterpret_cast<const float4 *>(qs + r0 * dp)[c4];
+            const float4 qb = reinterpret_cast<const float4 *>(qs + (r0 + 1) * dp)[c4];
+#pragma unroll
+            for (int n = 0; n < 4; ++n) {
+                const float4 kv = reinterpret_cast<const float4 *>(ks + (lane + 32 * n) * dp)[c4];
+                acc[0][n] = __fmaf_rn(qa.x, kv.x, acc[0][n]);
+                acc[0][n] = __fmaf_rn(qa.y, kv.y, acc[0][n]);
+                acc[0][n] = __fmaf_rn(qa.z, kv.z, acc[0][n]);
+                acc[0][n] = __fmaf_rn(qa.w, kv.w, acc[0][n]);
+                acc[1][n] = __fmaf_rn(qb.x, kv.x, acc[1][n]);
+                acc[1][n] = __fmaf_rn(qb.y, kv.y, acc[1][n]);
+                acc[1][n] = __fmaf_rn(qb.z, kv.z, acc[1][n]);
+                acc[1][n] = __fmaf_rn(qb.w, kv.w, acc[1][n]);
+            }
+        }
+#pragma unroll
+        for (int a = 0; a < 2; ++a)
+#pragma unroll
+            for (int n = 0; n < 4; ++n) {
+                const int j = j0 + lane + 32 * n;
+                if (i0 + r0 + a < nQB && j < nKB) {
+                    nan_seen |= isnan(acc[a][n]);
+                    keys[(r0 + a) * nKB + j] = order_key(acc[a][n]);
+                }
+            }
+    }
+    if (nan_seen) raise_error(err, BSA_ERR_NONFINITE);
+    __syncthreads();
+    for (int a = 0; a < 2; ++a) {
+        const int i = i0 + r0 + a;
+        if (i >= nQB) break;
+        const int64_t r_global = static_cast<int64_t>(bh) * nQB + i;
+        select_row(keys + (r0 + a) * nKB, nKB, k, W, r_global, col_idx, bitmap, lane);
+        if (lane == 0) {
+            row_ptr[r_global] = static_cast<int32_t>(r_global * k);
+            if (r_global == static_cast<int64_t>(gridDim.y) * nQB - 1)
+                row_ptr[r_global + 1] = static_cast<int32_t>((r_global + 1) * k);
+        }
     }
 }
 
@@ -233,6 +286,116 @@ __global__ void __launch_bounds__(256) static_rows_kernel(StaticPred p, int64_t 
         count += __popc(word);
     }
     if (lane == 0) counts[r] = count;
+}
+
+// Masks shared by every (b, h) (band, cuboid, broadcast bitmap). The pattern of
+// one head is built once by pattern_kernel (bitmap words and per-row counts,
+// scanned by the CTA that finishes last), then emit_pattern_kernel writes every
+// head's bitmap, row_ptr and col_idx from it, head bh offset by bh * nnz_per_head.
+__device__ __forceinline__ uint32_t static_word(const StaticPred &p, const uint32_t *src, int i, int w, int nKB,
+                                                int lane)
+{
+    if (p.kind == BSA_STATIC_EXPLICIT) {
+        uint32_t word = src[static_cast<int64_t>(i) * ((nKB + 31) / 32) + w];
+        const int valid = nKB - w * 32;
+        if (valid < 32) word &= (1u << valid) - 1u;
+        return word;
+    }
+    const int j = w * 32 + lane;
+    return __ballot_sync(0xffffffffu, j < nKB && static_active(p, i, j));
+}
+
+// pat_rp: [nQB + 1] row offsets within a head; pat_bm: [nQB][W].
+// One warp per pattern row (bitmap words + count); the CTA that finishes last
+// scans the counts.
+__global__ void __launch_bounds__(256) pattern_kernel(StaticPred p, int nQB, int nKB, int W,
+                                                      const uint32_t *__restrict__ src, int32_t *__restrict__ pat_rp,
+                                                      uint32_t *__restrict__ pat_bm, uint32_t *done)
+{
+    __shared__ int32_t wsum[8];
+    __shared__ bool is_last;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int i = blockIdx.x * 8 + warp;
+    if (i < nQB) {
+        int c = 0;
+        for (int w = 0; w < W; ++w) {
+            const uint32_t word = static_word(p, src, i, w, nKB, lane);
+            if (lane == 0) pat_bm[static_cast<int64_t>(i) * W + w] = word;
+            c += __popc(word);
+        }
+        if (lane == 0) pat_rp[i + 1] = c;
+    }
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) is_last = atomicAdd(done, 1u) == gridDim.x - 1;
+    __syncthreads();
+    if (!is_last) return;
+    __threadfence();
+    // inclusive scan of pat_rp[1..nQB] (each thread scans a contiguous chunk)
+    const int chunk = (nQB + blockDim.x - 1) / blockDim.x;
+    const int b = threadIdx.x * chunk, e = min(nQB, b + chunk);
+    int local = 0;
+    for (int r = b; r < e; ++r) local += __ldcg(pat_rp + r + 1);
+    int x = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) wsum[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        int v = lane < 8 ? wsum[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < 8; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, v, o);
+            if (lane >= o) v += y;
+        }
+        if (lane < 8) wsum[lane] = v;
+    }
+    __syncthreads();
+    int run = x - local + (warp > 0 ? wsum[warp - 1] : 0);
+    for (int r = b; r < e; ++r) {
+        const int c = __ldcg(pat_rp + r + 1);
+        pat_rp[r + 1] = run + c;
+        run += c;
+    }
+    if (threadIdx.x == 0) {
+        pat_rp[0] = 0;
+        *done = 0u;
+    }
+}
+
+// One warp per index row r = bh * nQB + i: copies pattern row i into head bh
+// (bitmap words, row_ptr = bh * nnz_per_head + pattern offset, col_idx).
+__global__ void __launch_bounds__(256) emit_pattern_kernel(int64_t R, int nQB, int W, const int32_t *__restrict__ pat_rp,
+                                                           const uint32_t *__restrict__ pat_bm,
+                                                           uint32_t *__restrict__ bitmap, int32_t *__restrict__ row_ptr,
+                                                           int32_t *__restrict__ col_idx, int64_t capacity, uint32_t *err)
+{
+    const int64_t r = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (r >= R) return;
+    const int i = static_cast<int>(r % nQB);
+    const int64_t bh = r / nQB;
+    const int64_t nnz_head = pat_rp[nQB];
+    int64_t pos = bh * nnz_head + pat_rp[i];
+    if (lane == 0) {
+        row_ptr[r] = static_cast<int32_t>(pos);
+        if (r == R - 1) row_ptr[R] = static_cast<int32_t>((bh + 1) * nnz_head);
+    }
+    bool overflow = false;
+    for (int w = 0; w < W; ++w) {
+        const uint32_t word = pat_bm[static_cast<int64_t>(i) * W + w];
+        if (lane == 0) bitmap[r * W + w] = word;
+        if ((word >> lane) & 1u) {
+            const int64_t q = pos + __popc(word & lanemask_lt());
+            if (q < capacity) col_idx[q] = w * 32 + lane;
+            else overflow = true;
+        }
+        pos += __popc(word);
+    }
+    if (overflow) raise_error(err, BSA_ERR_CAPACITY);
 }
 
 // Exclusive scan of R counts into row_ptr[0..R] (one CTA of 1024 threads).
@@ -331,14 +494,35 @@ __global__ void __launch_bounds__(256) validate_kernel(const int32_t *__restrict
 
 }  // namespace
 
-size_t mask_workspace_bytes(int B, int H, int N, int d, int block)
+// Workspace after the header: the dynamic path uses Qbar and Kbar; the static
+// path uses per-row counts (per-head bitmaps) and one head's pattern
+// (row offsets, bitmap words).
+struct MaskWs {
+    size_t qbar, kbar;                          // dynamic
+    size_t counts, pat_rp, pat_bm;              // static
+    size_t total;
+};
+
+MaskWs mask_ws_layout(int B, int H, int N, int d, int block)
 {
     const size_t BH = static_cast<size_t>(B) * H;
     const size_t nB = static_cast<size_t>(N / block);
-    size_t bytes = kWsHeader;
-    bytes += align_up(BH * nB * d * sizeof(float), 256) * 2;  // Qbar, Kbar
-    bytes += align_up(BH * nB * sizeof(int32_t), 256);        // static row counts
-    return bytes;
+    const size_t W = (nB + 31) / 32;
+    MaskWs l{};
+    l.qbar = kWsHeader;
+    l.kbar = l.qbar + align_up(BH * nB * d * sizeof(float), 256);
+    const size_t dyn_end = l.kbar + align_up(BH * nB * d * sizeof(float), 256);
+    l.counts = kWsHeader;
+    l.pat_rp = l.counts + align_up(BH * nB * sizeof(int32_t), 256);
+    l.pat_bm = l.pat_rp + align_up((nB + 1) * sizeof(int32_t), 256);
+    const size_t static_end = l.pat_bm + align_up(nB * W * sizeof(uint32_t), 256);
+    l.total = dyn_end > static_end ? dyn_end : static_end;
+    return l;
+}
+
+size_t mask_workspace_bytes(int B, int H, int N, int d, int block)
+{
+    return mask_ws_layout(B, H, N, d, block).total;
 }
 
 bsa_status launch_build_mask(const MaskArgs &a, cudaStream_t st)
@@ -346,12 +530,10 @@ bsa_status launch_build_mask(const MaskArgs &a, cudaStream_t st)
     const int64_t BH = static_cast<int64_t>(a.B) * a.H;
     const int64_t R = BH * a.nQB;
     uint32_t *err = reinterpret_cast<uint32_t *>(a.ws);
-    char *p = a.ws + kWsHeader;
-    float *qbar = reinterpret_cast<float *>(p);
-    p += align_up(static_cast<size_t>(BH) * a.nQB * a.d * sizeof(float), 256);
-    float *kbar = reinterpret_cast<float *>(p);
-    p += align_up(static_cast<size_t>(BH) * a.nKB * a.d * sizeof(float), 256);
-    int32_t *counts = reinterpret_cast<int32_t *>(p);
+    const MaskWs l = mask_ws_layout(a.B, a.H, a.N, a.d, a.block);
+    float *qbar = reinterpret_cast<float *>(a.ws + l.qbar);
+    float *kbar = reinterpret_cast<float *>(a.ws + l.kbar);
+    int32_t *counts = reinterpret_cast<int32_t *>(a.ws + l.counts);
 
     if (a.spec == nullptr) {
         const int64_t groups = BH * a.nQB * (a.d / 8);
@@ -364,14 +546,12 @@ bsa_status launch_build_mask(const MaskArgs &a, cudaStream_t st)
             pool_kernel<float><<<pg, kPoolThreads, 0, st>>>(static_cast<const float *>(a.Q),
                                                             static_cast<const float *>(a.K), qbar, kbar,
                                                             groups, a.N, a.d, a.block, a.nQB);
-        const size_t smem = sizeof(float) * (kRowsPerCta * a.d + kKvTile * (a.d + 1)) +
-                            sizeof(uint32_t) * kRowsPerCta * a.nKB;
-        if (smem > 48 * 1024) {
-            cudaError_t e = cudaFuncSetAttribute(score_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 static_cast<int>(smem));
-            if (e != cudaSuccess) return BSA_ERR_CUDA;
-        }
-        dim3 sg((a.nQB + kRowsPerCta - 1) / kRowsPerCta, static_cast<unsigned>(BH));
+        const size_t smem = sizeof(float) * (kScoreRows + kScoreTile) * (a.d + 4) +
+                            sizeof(uint32_t) * kScoreRows * a.nKB;
+        if (cudaFuncSetAttribute(score_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(smem)) != cudaSuccess)
+            return BSA_ERR_CUDA;
+        dim3 sg((a.nQB + kScoreRows - 1) / kScoreRows, static_cast<unsigned>(BH));
         score_topk_kernel<<<sg, 256, smem, st>>>(qbar, kbar, a.nQB, a.nKB, a.d, a.k, a.W, a.row_ptr,
                                                  a.col_idx, a.bitmap, err);
     } else {
@@ -385,10 +565,21 @@ bsa_status launch_build_mask(const MaskArgs &a, cudaStream_t st)
         pr.gh = a.spec->grid_h;
         pr.gw = a.spec->grid_w;
         pr.broadcast = a.spec->broadcast_bh;
-        const unsigned g = static_cast<unsigned>((R + 7) / 8);
-        static_rows_kernel<<<g, 256, 0, st>>>(pr, R, a.nQB, a.nKB, a.W, a.spec->bitmap, a.bitmap, counts);
-        scan_kernel<<<1, 1024, 0, st>>>(counts, R, a.row_ptr);
-        emit_kernel<<<g, 256, 0, st>>>(a.bitmap, a.row_ptr, R, a.W, a.col_idx, a.col_capacity, err);
+        if (pr.kind != BSA_STATIC_EXPLICIT || pr.broadcast) {
+            // one pattern for every (b, h): build it once, then copy it into every head
+            int32_t *pat_rp = reinterpret_cast<int32_t *>(a.ws + l.pat_rp);     // [nQB + 1]
+            uint32_t *pat_bm = reinterpret_cast<uint32_t *>(a.ws + l.pat_bm);   // [nQB][W]
+            WsHeader *hdr = reinterpret_cast<WsHeader *>(a.ws);
+            pattern_kernel<<<(a.nQB + 7) / 8, 256, 0, st>>>(pr, a.nQB, a.nKB, a.W, a.spec->bitmap, pat_rp, pat_bm,
+                                                            &hdr->order_done);
+            emit_pattern_kernel<<<static_cast<unsigned>((R + 7) / 8), 256, 0, st>>>(
+                R, a.nQB, a.W, pat_rp, pat_bm, a.bitmap, a.row_ptr, a.col_idx, a.col_capacity, err);
+        } else {
+            const unsigned g = static_cast<unsigned>((R + 7) / 8);
+            static_rows_kernel<<<g, 256, 0, st>>>(pr, R, a.nQB, a.nKB, a.W, a.spec->bitmap, a.bitmap, counts);
+            scan_kernel<<<1, 1024, 0, st>>>(counts, R, a.row_ptr);
+            emit_kernel<<<g, 256, 0, st>>>(a.bitmap, a.row_ptr, R, a.W, a.col_idx, a.col_capacity, err);
+        }
     }
     return cudaGetLastError() == cudaSuccess ? BSA_OK : BSA_ERR_CUDA;
 }

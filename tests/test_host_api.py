@@ -39,10 +39,15 @@ def test_status_strings(lib):
 
 def test_workspace_sizes(lib):
     ws0 = bb.bsa_workspace_size(0, 2, 24, 4224, 64, 64)
-    # header + Qbar + Kbar + row counts
-    assert ws0 == 256 + 2 * (2 * 24 * 66 * 64 * 4) + (2 * 24 * 66 * 4 + 255) // 256 * 256
+    up = lambda x: (x + 255) // 256 * 256  # noqa: E731
+    BH, nB, d, W = 48, 66, 64, 3
+    dynamic = 256 + 2 * up(BH * nB * d * 4)                                        # Qbar, Kbar
+    static = 256 + up(BH * nB * 4) + up((nB + 1) * 4) + up(nB * W * 4)  # counts, pattern
+    assert ws0 == max(dynamic, static)
     ws1 = bb.bsa_workspace_size(1, 2, 24, 4224, 64, 64)
-    assert ws1 == 256 + (2 * 24 * 33 * 4 + 255) // 256 * 256
+    tiles = 2 * 24 * 33  # 128-row query tiles
+    # header + tile list (padded to 64 entries) + per-tile lengths
+    assert ws1 == 256 + ((tiles + 63) // 64 * 64 * 4 + tiles * 4 + 255) // 256 * 256
     with pytest.raises(bb.BsaError) as e:
         bb.bsa_workspace_size(1, 1, 1, 100, 64, 64)
     assert e.value.code == bb.ERR_SHAPE
