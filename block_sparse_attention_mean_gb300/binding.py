@@ -38,7 +38,8 @@ MAX_ANCHORS = 8
 # every symbol declared in include/bsa.h
 EXPORTS = ("bsa_build_mask", "bsa_forward", "bsa_mask_nnz", "bsa_workspace_size",
            "bsa_check_device_error", "bsa_validate_index", "bsa_debug_config",
-           "bsa_status_string")
+           "bsa_status_string", "bsa_build_mask_noalloc")
+NOALLOC_SCRATCH_BYTES = 16 << 20  # BSA_NOALLOC_SCRATCH_BYTES
 
 
 class StaticSpec(ctypes.Structure):
@@ -71,6 +72,8 @@ def load():
     lib.bsa_build_mask.argtypes = [P, P, I, I, I, I, I, I, F, ctypes.POINTER(StaticSpec), P, P, I64, P, P,
                                    SZ, P]
     lib.bsa_forward.argtypes = [P, P, P, I, I, I, I, I, I, P, P, P, I, F, P, P, P, SZ, P]
+    lib.bsa_build_mask_noalloc.argtypes = [P, P, I, I, I, I, I, I, F, ctypes.POINTER(StaticSpec), P, P, I64, P,
+                                           P, P]
     lib.bsa_mask_nnz.argtypes = [I, I, I, I, F, ctypes.POINTER(StaticSpec), ctypes.POINTER(I64)]
     lib.bsa_workspace_size.argtypes = [I, I, I, I, I, I, ctypes.POINTER(SZ)]
     lib.bsa_check_device_error.argtypes = [P, P]
@@ -129,6 +132,17 @@ def bsa_forward(Q, K, V, dt: int, B: int, H: int, N: int, d: int, block: int, ro
                               _ptr(bitmap), int(index_mode), float(scale), _ptr(O), _ptr(LSE),
                               _ptr(workspace), int(workspace_bytes), _stream(stream))
     _check(code, "bsa_forward")
+
+
+def bsa_build_mask_noalloc(Q, K, dt: int, B: int, H: int, N: int, d: int, block: int, density: float,
+                           spec: Optional[StaticSpec], row_ptr, col_idx, col_capacity: int, bitmap,
+                           device_status=None, stream=None) -> None:
+    """bsa_build_mask without a workspace, for callers that cannot allocate device memory."""
+    code = load().bsa_build_mask_noalloc(_ptr(Q), _ptr(K), dt, B, H, N, d, block, float(density),
+                                         ctypes.byref(spec) if spec is not None else None, _ptr(row_ptr),
+                                         _ptr(col_idx), int(col_capacity), _ptr(bitmap), _ptr(device_status),
+                                         _stream(stream))
+    _check(code, "bsa_build_mask_noalloc")
 
 
 def bsa_mask_nnz(B: int, H: int, N: int, block: int, density: float, spec: Optional[StaticSpec]) -> int:

@@ -144,6 +144,35 @@ bsa_status bsa_forward(const void *Q, const void *K, const void *V, int dt, int 
                        const uint32_t *bitmap, int index_mode, float scale, void *O, float *LSE,
                        void *workspace, size_t workspace_bytes, void *stream);
 
+/*
+ * bsa_build_mask_noalloc -- bsa_build_mask without a caller workspace (the pages
+ * have no counterpart: this is a convenience of this library).
+ *
+ * For callers that cannot allocate device memory: code under a framework that
+ * owns all device memory from start-up on, or a process whose device-memory
+ * budget is frozen once it serves. The scratch comes from a fixed array of
+ * BSA_NOALLOC_SCRATCH_BYTES in the library's device memory; every GPU that loads
+ * the library holds it until the process exits. Arguments and results are those
+ * of bsa_build_mask, minus the workspace; the call allocates and frees nothing.
+ *
+ *   device_status  optional device uint32 (NULL = not wanted): receives, in stream
+ *                  order at the end of the call, the device-raised status of this
+ *                  build (BSA_OK, BSA_ERR_NONFINITE or BSA_ERR_CAPACITY).
+ *
+ * Returns BSA_ERR_WORKSPACE, before any launch, when the problem needs more
+ * scratch than the array holds (bsa_workspace_size(0, ...) larger than
+ * BSA_NOALLOC_SCRATCH_BYTES). The first call on a device looks up the array's
+ * device address (once per device, with that device current): make that first
+ * call before any stream capture. All calls share the one array: calls whose
+ * work overlaps on the GPU (different streams without ordering, or different
+ * host threads) race on it and must be serialised by the caller.
+ */
+#define BSA_NOALLOC_SCRATCH_BYTES (16u << 20)
+bsa_status bsa_build_mask_noalloc(const void *Q, const void *K, int dt, int B, int H, int N, int d,
+                                  int block, float density, const bsa_static_spec *spec,
+                                  int32_t *row_ptr, int32_t *col_idx, int64_t col_capacity,
+                                  uint32_t *bitmap, uint32_t *device_status, void *stream);
+
 /* Host-only: number of active blocks the builder will emit for these arguments.
  * Dynamic: B*H*nQB*k. MODALITY_BAND / CUBOID: exact count times B*H.
  * EXPLICIT: the bitmap lives on the device, so the upper bound B*H*nQB*nKB. */
