@@ -671,6 +671,10 @@ __global__ void __launch_bounds__((4 * SPLIT + 2) * 32, MINB)
         if (lane == 0 && !stall) {
             const uint32_t tS = tmem;             // NSB S/P buffers of BS columns
             const uint32_t tO = tmem + NSB * BS;  // O accumulator, D columns
+            // shared-memory descriptors of K and V slot 0 (slots and steps are added as offsets:
+            // the address field holds addr >> 4 and never carries for these sizes)
+            const uint64_t kdesc0 = sdesc_sw128(sbase + C::K_OFF, 16, 1024);
+            const uint64_t vdesc0 = sdesc_sw128(sbase + C::V_OFF, C::kKVChunk, 1024);
             int G = 0, e = 0, tcount = 0;
             bool ok = true;
             auto issue_pv = [&](int t, bool first) -> bool {
@@ -679,12 +683,13 @@ __global__ void __launch_bounds__((4 * SPLIT + 2) * 32, MINB)
                 if (!wait_bar(bar(C::B_VFULL + s), (t / NV) & 1, ctl)) return false;
                 if (first && e >= 1 && !wait_bar(bar(C::B_OEMPTY), (e - 1) & 1, ctl)) return false;
                 tc_fence_after();
-                const uint32_t vbase = sbase + C::V_OFF + s * C::kKVBytes;
+                // V slot s: descriptor of its first 16-row step; step kk adds kk * 2048 bytes
+                const uint64_t vdesc = vdesc0 + static_cast<uint64_t>(s * (C::kKVBytes >> 4));
+                const uint32_t pa = tS + b * BS;
 #pragma unroll
-                for (int kk = 0; kk < BS / 16; ++kk) {
-                    const uint64_t bdesc = sdesc_sw128(vbase + kk * 16 * 128, C::kKVChunk, 1024);
-                    mma_ts(tO, tS + b * BS + kk * 8, bdesc, C::IDESC_PV, (first && kk == 0) ? 0u : 1u);
-                }
+                for (int kk = 0; kk < BS / 16; ++kk)
+                    mma_ts(tO, pa + kk * 8, vdesc + static_cast<uint64_t>(kk * (16 * 128 >> 4)), C::IDESC_PV,
+                           (first && kk == 0) ? 0u : 1u);
                 tc_commit(bar(C::B_PVDONE + b));
                 tc_commit(bar(C::B_VEMPTY + s));
                 return true;
@@ -707,7 +712,7 @@ __global__ void __launch_bounds__((4 * SPLIT + 2) * 32, MINB)
                 const int qs = e % QS;
                 if (!wait_bar(bar(C::B_QFULL + qs), (e / QS) & 1, ctl)) break;
                 tc_fence_after();
-                const uint32_t qbase = sbase + C::Q_OFF + qs * C::kQBytes;
+                const uint64_t qdesc = sdesc_sw128(sbase + C::Q_OFF + qs * C::kQBytes, 16, 1024);
                 const int G0 = G;
                 do {
                     // With a single S/P buffer the previous block's PV must be issued
@@ -718,13 +723,13 @@ __global__ void __launch_bounds__((4 * SPLIT + 2) * 32, MINB)
                     // S/P buffer b was last read by PV(G - NSB)
                     if (G >= NSB && !wait_bar(bar(C::B_PVDONE + b), ((G / NSB) - 1) & 1, ctl)) { ok = false; break; }
                     tc_fence_after();
-                    const uint32_t kbase = sbase + C::K_OFF + s * C::kKVBytes;
+                    // K-major, 128-byte swizzle: step kk is 32 bytes into 64-column slab kk / 4
+                    const uint64_t kdesc = kdesc0 + static_cast<uint64_t>(s * (C::kKVBytes >> 4));
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk) {
-                        const int c = kk >> 2, off = (kk & 3) * 32;
-                        const uint64_t adesc = sdesc_sw128(qbase + c * C::kQChunk + off, 16, 1024);
-                        const uint64_t bdesc = sdesc_sw128(kbase + c * C::kKVChunk + off, 16, 1024);
-                        mma_ss(tS + b * BS, adesc, bdesc, C::IDESC_QK, kk > 0 ? 1u : 0u);
+                        const uint64_t off_q = static_cast<uint64_t>(((kk >> 2) * C::kQChunk + (kk & 3) * 32) >> 4);
+                        const uint64_t off_k = static_cast<uint64_t>(((kk >> 2) * C::kKVChunk + (kk & 3) * 32) >> 4);
+                        mma_ss(tS + b * BS, qdesc + off_q, kdesc + off_k, C::IDESC_QK, kk > 0 ? 1u : 0u);
                     }
                     tc_commit(bar(C::B_SFULL + b));
                     tc_commit(bar(C::B_KEMPTY + s));
