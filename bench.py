@@ -77,6 +77,24 @@ def effective_flops(w, nnz: int) -> float:
     return float(nnz) * 4.0 * w.block * w.block * w.d
 
 
+def max_over_ranks(x: float, device) -> float:
+    """Largest value of x across the ranks of the default process group (x itself
+    without one). Every rank replicates the workload, so the slowest rank's time
+    is the job's time."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(flops_per_step: float, world: int, steps: int, total_ms: float) -> float:
+    """Whole-job effective TFLOP/s: the work of every rank over the slowest rank's time."""
+    return flops_per_step * world * steps / (total_ms * 1e-3) / 1e12
+
+
 def measured_peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -334,14 +352,10 @@ def run_ours(args, world, rank, local):
     step_ms = [e[0].elapsed_time(e[2]) for e in ev]
     fwd_ms = [e[1].elapsed_time(e[2]) for e in ev]
     build_ms = [e[0].elapsed_time(e[1]) for e in ev]
-    total_ms = sum(step_ms)
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(sum(step_ms), dev)
     flops = effective_flops(w, nnz)
     ms_per_step = total_ms / args.steps
-    value = flops * world * args.steps / (total_ms * 1e-3) / 1e12
+    value = job_throughput(flops, world, args.steps, total_ms)
 
     # end to end through the C ABI from pinned host buffers
     e2e = None
@@ -367,12 +381,8 @@ def run_ours(args, world, rank, local):
                     e2e_ms.append(e0.elapsed_time(e1))
         h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
         d2h = hO.numel() * hO.element_size() + hL.numel() * hL.element_size()
-        e2e_mean = sum(e2e_ms) / len(e2e_ms)
-        if world > 1:
-            t = torch.tensor([e2e_mean], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_mean = float(t.item())
-        e2e = {"value": round(flops * world / (e2e_mean * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
+        e2e_mean = max_over_ranks(sum(e2e_ms) / len(e2e_ms), dev)
+        e2e = {"value": round(job_throughput(flops, world, 1, e2e_mean), 3), "unit": "TFLOP/s",
                "ms_per_step": round(e2e_mean, 4), "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
 
     if rank != 0:

@@ -65,12 +65,16 @@ struct TcParams {
     uint32_t dbg;
 };
 
-template <int D, int BS, int NK, int NV, int NSB, int QS>
+// One KV step = PAIR consecutive KV blocks of the walk (PAIR = 2 at block 64:
+// QK^T then runs as N = 128 MMAs). A K or V ring stage holds one step: per
+// 64-column slab, PAIR * BS rows of 128 bytes, block p of the step at row p * BS.
+template <int D, int BS, int NK, int NV, int NSB, int QS, int PAIR>
 struct Cfg {
+    static constexpr int kStep = PAIR * BS;       // KV rows (S columns) per step
     static constexpr int kQBytes = kTileM * D * 2;
-    static constexpr int kKVBytes = BS * D * 2;
+    static constexpr int kKVBytes = kStep * D * 2;
     static constexpr int kQChunk = kTileM * 128;  // bytes of one 64-column swizzled slab
-    static constexpr int kKVChunk = BS * 128;
+    static constexpr int kKVChunk = kStep * 128;
     static constexpr int Q_OFF = 0;  // QS Q slots: tile e uses slot e % QS
     static constexpr int K_OFF = Q_OFF + QS * kQBytes;   // NK-stage K ring
     static constexpr int V_OFF = K_OFF + NK * kKVBytes;  // NV-stage V ring
@@ -85,9 +89,10 @@ struct Cfg {
     static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
     static constexpr int SMEM = MISC_OFF + 32;
     static constexpr int SMEM_ALLOC = SMEM + 1024;  // manual 1024-byte alignment
-    static constexpr int TCOLS_USED = NSB * BS + D;
+    static constexpr int TCOLS_USED = NSB * kStep + D;
     static constexpr int TCOLS = TCOLS_USED <= 256 ? 256 : 512;
-    static constexpr uint32_t IDESC_QK = idesc_bf16_f32(kTileM, BS, 0, 0);
+    static constexpr uint32_t IDESC_QK = idesc_bf16_f32(kTileM, kStep, 0, 0);
+    static constexpr uint32_t IDESC_QK_HALF = idesc_bf16_f32(kTileM, BS, 0, 0);  // a step with one block
     static constexpr uint32_t IDESC_PV = idesc_bf16_f32(kTileM, D, 0, 1);
 };
 
@@ -188,15 +193,21 @@ __device__ __forceinline__ bool fetch_tile(uint32_t sbase, volatile int32_t *til
 }
 
 // SPLIT == 1: warp w (0-3) owns TMEM lanes 32w..32w+31; thread = one query row,
-// all BS columns of S (32x32b TMEM accesses).
-template <int D, int BS, int NSB, class C>
+// all kStep columns of S (32x32b TMEM accesses). A step holds PAIR KV blocks;
+// block q of the step occupies S columns [q * BS, (q + 1) * BS) and is skipped
+// (P = 0, no effect on the max or the sums) when the step has no block q or the
+// row's Q block does not have it.
+template <int D, int BS, int NSB, int PAIR, class C>
 __device__ __forceinline__ void softmax_rows(const TcParams &p, uint32_t sbase, uint32_t tmem,
                                              volatile int32_t *tile_ids, const Ctl &ctl, int warp, int lane)
 {
     auto bar = [&](int idx) -> uint32_t { return barrier_addr<C>(sbase, idx); };
+    constexpr int kStep = C::kStep;
+    constexpr int NC = kStep / 32;  // 32-column chunks of a step
+    constexpr int CPB = BS / 32;    // chunks per block
     const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
     const uint32_t tS = tmem + lane_base;
-    const uint32_t tO = tmem + lane_base + NSB * BS;
+    const uint32_t tO = tmem + lane_base + NSB * kStep;
     const uint32_t qblk = BS == 128 ? 0u : static_cast<uint32_t>(warp >> 1);
     const int trow = warp * 32 + lane;
     int G = 0, tcount = 0;
@@ -212,9 +223,10 @@ __device__ __forceinline__ void softmax_rows(const TcParams &p, uint32_t sbase, 
         __nv_bfloat16 *orow = p.O + grow * D;
         TileWalk walk;
         walk_init<BS>(walk, p, bh, qt);
-        int j;
-        uint32_t m;
-        if (!walk.next(j, m)) {
+        int js[2];
+        uint32_t ms[2];
+        int cnt = walk.next_step<PAIR>(js, ms);
+        if (cnt == 0) {
             if (row_valid) {
                 const uint4 z = make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
@@ -228,19 +240,27 @@ __device__ __forceinline__ void softmax_rows(const TcParams &p, uint32_t sbase, 
             const int b = G % NSB;
             if (!warp_wait(bar(C::B_SFULL + b), (G / NSB) & 1, ctl, lane)) return;
             tc_fence_after();
+            bool act[PAIR];
+            bool any = false;
+#pragma unroll
+            for (int q = 0; q < PAIR; ++q) {
+                act[q] = q < cnt && ((ms[q] >> qblk) & 1u) != 0u;
+                any |= act[q];
+            }
             bool resc = false;
             float alpha = 1.0f;
-            if ((m >> qblk) & 1u) {
-                constexpr int NC = BS / 32;
+            if (any) {
                 uint32_t sv[NC][32];
 #pragma unroll
-                for (int c = 0; c < NC; ++c) tmem_ld32(tS + b * BS + c * 32, sv[c]);
+                for (int c = 0; c < NC; ++c)
+                    if (act[c / CPB]) tmem_ld32(tS + b * kStep + c * 32, sv[c]);
                 tmem_wait_ld();
 #pragma unroll
                 for (int c = 0; c < NC; ++c) reg_fence32(sv[c]);
                 float mx0 = -CUDART_INF_F, mx1 = -CUDART_INF_F, mx2 = -CUDART_INF_F, mx3 = -CUDART_INF_F;
 #pragma unroll
-                for (int c = 0; c < NC; ++c)
+                for (int c = 0; c < NC; ++c) {
+                    if (!act[c / CPB]) continue;
 #pragma unroll
                     for (int t = 0; t < 32; t += 8) {
                         mx0 = fmax3(mx0, __uint_as_float(sv[c][t]), __uint_as_float(sv[c][t + 1]));
@@ -248,6 +268,7 @@ __device__ __forceinline__ void softmax_rows(const TcParams &p, uint32_t sbase, 
                         mx2 = fmax3(mx2, __uint_as_float(sv[c][t + 4]), __uint_as_float(sv[c][t + 5]));
                         mx3 = fmax3(mx3, __uint_as_float(sv[c][t + 6]), __uint_as_float(sv[c][t + 7]));
                     }
+                }
                 const float m_tile = fmax3(fmaxf(mx0, mx1), mx2, mx3) * p.scale_log2;
                 if (m_run == -CUDART_INF_F) {
                     m_run = m_tile;
@@ -266,19 +287,24 @@ __device__ __forceinline__ void softmax_rows(const TcParams &p, uint32_t sbase, 
 #pragma unroll
                 for (int c = 0; c < NC; ++c) {
                     uint32_t pk[16];
+                    if (act[c / CPB]) {
 #pragma unroll
-                    for (int q = 0; q < 16; ++q) {
-                        float x0, x1;
-                        f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[c][2 * q]), __uint_as_float(sv[c][2 * q + 1])),
-                                         c2x, nm2),
-                                  x0, x1);
-                        const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
-                        pk[q] = pack_bf16x2(p0, p1);
-                        acc[q & 3] = f2_add(acc[q & 3], f2_pack(p0, p1));
-                        accp[q & 3] = f2_add(accp[q & 3], f2_pack(__uint_as_float(pk[q] << 16),
-                                                                  __uint_as_float(pk[q] & 0xFFFF0000u)));
+                        for (int q = 0; q < 16; ++q) {
+                            float x0, x1;
+                            f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[c][2 * q]), __uint_as_float(sv[c][2 * q + 1])),
+                                             c2x, nm2),
+                                      x0, x1);
+                            const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+                            pk[q] = pack_bf16x2(p0, p1);
+                            acc[q & 3] = f2_add(acc[q & 3], f2_pack(p0, p1));
+                            accp[q & 3] = f2_add(accp[q & 3], f2_pack(__uint_as_float(pk[q] << 16),
+                                                                      __uint_as_float(pk[q] & 0xFFFF0000u)));
+                        }
+                    } else {
+#pragma unroll
+                        for (int q = 0; q < 16; ++q) pk[q] = 0u;
                     }
-                    tmem_st16(tS + b * BS + c * 16, pk);
+                    tmem_st16(tS + b * kStep + c * 16, pk);
                 }
                 float e0, e1, e2, e3;
                 f2_unpack(f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3])), e0, e1);
@@ -290,10 +316,10 @@ __device__ __forceinline__ void softmax_rows(const TcParams &p, uint32_t sbase, 
 #pragma unroll
                 for (int q = 0; q < 16; ++q) z[q] = 0u;
 #pragma unroll
-                for (int c = 0; c < BS / 32; ++c) tmem_st16(tS + b * BS + c * 16, z);
+                for (int c = 0; c < NC; ++c) tmem_st16(tS + b * kStep + c * 16, z);
             }
             if (__any_sync(0xffffffffu, resc)) {
-                // O holds the previous blocks' sum: rescale it once the last PV landed
+                // O holds the previous steps' sum: rescale it once the last PV landed
                 const int t = G - 1;
                 if (!warp_wait(bar(C::B_PVDONE + t % NSB), (t / NSB) & 1, ctl, lane)) return;
                 tc_fence_after();
@@ -313,7 +339,7 @@ __device__ __forceinline__ void softmax_rows(const TcParams &p, uint32_t sbase, 
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(C::B_PFULL + b));
             ++G;
-        } while (walk.next(j, m));
+        } while ((cnt = walk.next_step<PAIR>(js, ms)) != 0);
         // epilogue: O / l, LSE = ln2 * (m + log2 l)
         const int t = G - 1;
         if (!warp_wait(bar(C::B_PVDONE + t % NSB), (t / NSB) & 1, ctl, lane)) return;
@@ -528,12 +554,13 @@ __device__ __forceinline__ void softmax_quads(const TcParams &p, uint32_t sbase,
     }
 }
 
-template <int D, int BS, int NK, int NV, int NSB, int QS, int SPLIT, int MINB>
+template <int D, int BS, int NK, int NV, int NSB, int QS, int SPLIT, int PAIR, int MINB>
 __global__ void __launch_bounds__((4 * SPLIT + 2) * 32, MINB)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const TcParams p)
 {
-    using C = Cfg<D, BS, NK, NV, NSB, QS>;
+    static_assert(PAIR == 1 || SPLIT == 1, "two-block steps use one softmax thread per row");
+    using C = Cfg<D, BS, NK, NV, NSB, QS, PAIR>;
     using R = Roles<SPLIT>;
     constexpr int kProducerWarp = R::kProducerWarp, kMmaWarp = R::kMmaWarp;
     extern __shared__ uint8_t smem_raw[];
@@ -611,9 +638,10 @@ __global__ void __launch_bounds__((4 * SPLIT + 2) * 32, MINB)
                 tile_coords(p, tile, bh, qt);
                 TileWalk walk;
                 walk_init<BS>(walk, p, bh, qt);
-                int j;
-                uint32_t m;
-                if (!walk.next(j, m)) continue;  // empty tile: nothing to load
+                int js[2];
+                uint32_t ms[2];
+                int cnt = walk.next_step<PAIR>(js, ms);
+                if (cnt == 0) continue;  // empty tile: nothing to load
                 const int qs = e % QS;  // Q slot; it was last used by tile e - QS
                 if (e >= QS && !wait_bar(bar(C::B_QEMPTY + qs), ((e / QS) - 1) & 1, ctl)) break;
                 mbar_arrive_expect_tx(bar(C::B_QFULL + qs), C::kQBytes);
@@ -624,18 +652,21 @@ __global__ void __launch_bounds__((4 * SPLIT + 2) * 32, MINB)
                                 bar(C::B_QFULL + qs));
                 q_issued = e;
                 do {
-                    const int krow = static_cast<int>(bh * p.N) + j * BS;
+                    const uint32_t step_bytes = static_cast<uint32_t>(cnt * BS * D * 2);
                     // K slot: freed when the QK^T that read it completes
                     const int ks = G % NK;
                     if (G >= NK && !wait_bar(bar(C::B_KEMPTY + ks), ((G / NK) - 1) & 1, ctl)) {
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(bar(C::B_KFULL + ks), C::kKVBytes);
+                    mbar_arrive_expect_tx(bar(C::B_KFULL + ks), step_bytes);
+                    for (int q = 0; q < cnt; ++q) {
+                        const int krow = static_cast<int>(bh * p.N) + js[q] * BS;
 #pragma unroll
-                    for (int c = 0; c < D / 64; ++c)
-                        tma_load_2d(sbase + C::K_OFF + ks * C::kKVBytes + c * C::kKVChunk, &tmK, c * 64, krow,
-                                    bar(C::B_KFULL + ks));
+                        for (int c = 0; c < D / 64; ++c)
+                            tma_load_2d(sbase + C::K_OFF + ks * C::kKVBytes + c * C::kKVChunk + q * BS * 128, &tmK,
+                                        c * 64, krow, bar(C::B_KFULL + ks));
+                    }
                     // V slot: freed when the PV that read it completes
                     const int vs = G % NV;
                     if (G >= NV && !wait_bar(bar(C::B_VEMPTY + vs), ((G / NV) - 1) & 1, ctl)) {
@@ -645,14 +676,17 @@ __global__ void __launch_bounds__((4 * SPLIT + 2) * 32, MINB)
                         wait_bar_drain(bar(C::B_KFULL + ks), (G / NK) & 1, p.wait_limit_ns);
                         break;
                     }
-                    mbar_arrive_expect_tx(bar(C::B_VFULL + vs), C::kKVBytes);
+                    mbar_arrive_expect_tx(bar(C::B_VFULL + vs), step_bytes);
+                    for (int q = 0; q < cnt; ++q) {
+                        const int vrow = static_cast<int>(bh * p.N) + js[q] * BS;
 #pragma unroll
-                    for (int c = 0; c < D / 64; ++c)
-                        tma_load_2d(sbase + C::V_OFF + vs * C::kKVBytes + c * C::kKVChunk, &tmV, c * 64, krow,
-                                    bar(C::B_VFULL + vs));
+                        for (int c = 0; c < D / 64; ++c)
+                            tma_load_2d(sbase + C::V_OFF + vs * C::kKVBytes + c * C::kKVChunk + q * BS * 128, &tmV,
+                                        c * 64, vrow, bar(C::B_VFULL + vs));
+                    }
                     last_issue = G;
                     ++G;
-                } while (walk.next(j, m));
+                } while ((cnt = walk.next_step<PAIR>(js, ms)) != 0);
                 ++e;
             }
             if (*ctl.abort_flag) {
@@ -669,27 +703,31 @@ __global__ void __launch_bounds__((4 * SPLIT + 2) * 32, MINB)
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0 && !stall) {
-            const uint32_t tS = tmem;             // NSB S/P buffers of BS columns
-            const uint32_t tO = tmem + NSB * BS;  // O accumulator, D columns
+            const uint32_t tS = tmem;                   // NSB S/P buffers of kStep columns
+            const uint32_t tO = tmem + NSB * C::kStep;  // O accumulator, D columns
             // shared-memory descriptors of K and V slot 0 (slots and steps are added as offsets:
             // the address field holds addr >> 4 and never carries for these sizes)
             const uint64_t kdesc0 = sdesc_sw128(sbase + C::K_OFF, 16, 1024);
             const uint64_t vdesc0 = sdesc_sw128(sbase + C::V_OFF, C::kKVChunk, 1024);
             int G = 0, e = 0, tcount = 0;
             bool ok = true;
-            auto issue_pv = [&](int t, bool first) -> bool {
+            // PV of step t (tcnt KV blocks); `first` = first step of its tile (overwrites O)
+            auto issue_pv = [&](int t, bool first, int tcnt) -> bool {
                 const int b = t % NSB, s = t % NV;
                 if (!wait_bar(bar(C::B_PFULL + b), (t / NSB) & 1, ctl)) return false;
                 if (!wait_bar(bar(C::B_VFULL + s), (t / NV) & 1, ctl)) return false;
+                // the previous tile's epilogue must have read O before it is overwritten
                 if (first && e >= 1 && !wait_bar(bar(C::B_OEMPTY), (e - 1) & 1, ctl)) return false;
                 tc_fence_after();
                 // V slot s: descriptor of its first 16-row step; step kk adds kk * 2048 bytes
                 const uint64_t vdesc = vdesc0 + static_cast<uint64_t>(s * (C::kKVBytes >> 4));
-                const uint32_t pa = tS + b * BS;
+                const uint32_t pa = tS + b * C::kStep;
+                const int nk = tcnt * (BS / 16);  // 16-row K steps of the blocks this step holds
 #pragma unroll
-                for (int kk = 0; kk < BS / 16; ++kk)
-                    mma_ts(tO, pa + kk * 8, vdesc + static_cast<uint64_t>(kk * (16 * 128 >> 4)), C::IDESC_PV,
-                           (first && kk == 0) ? 0u : 1u);
+                for (int kk = 0; kk < C::kStep / 16; ++kk)
+                    if (kk < nk)
+                        mma_ts(tO, pa + kk * 8, vdesc + static_cast<uint64_t>(kk * (16 * 128 >> 4)), C::IDESC_PV,
+                               (first && kk == 0) ? 0u : 1u);
                 tc_commit(bar(C::B_PVDONE + b));
                 tc_commit(bar(C::B_VEMPTY + s));
                 return true;
@@ -706,18 +744,20 @@ __global__ void __launch_bounds__((4 * SPLIT + 2) * 32, MINB)
                 tile_coords(p, tile, bh, qt);
                 TileWalk walk;
                 walk_init<BS>(walk, p, bh, qt);
-                int j;
-                uint32_t m;
-                if (!walk.next(j, m)) continue;
+                int js[2];
+                uint32_t ms[2];
+                int cnt = walk.next_step<PAIR>(js, ms);
+                if (cnt == 0) continue;
+                int prev_cnt = 0;
                 const int qs = e % QS;
                 if (!wait_bar(bar(C::B_QFULL + qs), (e / QS) & 1, ctl)) break;
                 tc_fence_after();
                 const uint64_t qdesc = sdesc_sw128(sbase + C::Q_OFF + qs * C::kQBytes, 16, 1024);
                 const int G0 = G;
                 do {
-                    // With a single S/P buffer the previous block's PV must be issued
+                    // With a single S/P buffer the previous step's PV must be issued
                     // before QK^T overwrites the buffer it reads P from.
-                    if (NSB == 1 && G > G0 && !issue_pv(G - 1, G - 1 == G0)) { ok = false; break; }
+                    if (NSB == 1 && G > G0 && !issue_pv(G - 1, G - 1 == G0, prev_cnt)) { ok = false; break; }
                     const int s = G % NK, b = G % NSB;
                     if (!wait_bar(bar(C::B_KFULL + s), (G / NK) & 1, ctl)) { ok = false; break; }
                     // S/P buffer b was last read by PV(G - NSB)
@@ -725,20 +765,22 @@ __global__ void __launch_bounds__((4 * SPLIT + 2) * 32, MINB)
                     tc_fence_after();
                     // K-major, 128-byte swizzle: step kk is 32 bytes into 64-column slab kk / 4
                     const uint64_t kdesc = kdesc0 + static_cast<uint64_t>(s * (C::kKVBytes >> 4));
+                    const uint32_t idesc = cnt == PAIR ? C::IDESC_QK : C::IDESC_QK_HALF;
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk) {
                         const uint64_t off_q = static_cast<uint64_t>(((kk >> 2) * C::kQChunk + (kk & 3) * 32) >> 4);
                         const uint64_t off_k = static_cast<uint64_t>(((kk >> 2) * C::kKVChunk + (kk & 3) * 32) >> 4);
-                        mma_ss(tS + b * BS, qdesc + off_q, kdesc + off_k, C::IDESC_QK, kk > 0 ? 1u : 0u);
+                        mma_ss(tS + b * C::kStep, qdesc + off_q, kdesc + off_k, idesc, kk > 0 ? 1u : 0u);
                     }
                     tc_commit(bar(C::B_SFULL + b));
                     tc_commit(bar(C::B_KEMPTY + s));
-                    if (NSB > 1 && G > G0 && !issue_pv(G - 1, G - 1 == G0)) { ok = false; break; }
+                    if (NSB > 1 && G > G0 && !issue_pv(G - 1, G - 1 == G0, prev_cnt)) { ok = false; break; }
+                    prev_cnt = cnt;
                     ++G;
-                } while (walk.next(j, m));
+                } while ((cnt = walk.next_step<PAIR>(js, ms)) != 0);
                 if (!ok) break;
                 tc_commit(bar(C::B_QEMPTY + qs));
-                if (!issue_pv(G - 1, G - 1 == G0)) break;
+                if (!issue_pv(G - 1, G - 1 == G0, prev_cnt)) break;
                 ++e;
             }
             // all MMAs issued by this thread have completed before TMEM is freed
@@ -748,7 +790,7 @@ __global__ void __launch_bounds__((4 * SPLIT + 2) * 32, MINB)
     } else {
         // ------------------------------------------------------------ softmax + epilogue
         if constexpr (SPLIT == 1)
-            softmax_rows<D, BS, NSB, C>(p, sbase, tmem, tile_ids, ctl, warp, lane);
+            softmax_rows<D, BS, NSB, PAIR, C>(p, sbase, tmem, tile_ids, ctl, warp, lane);
         else
             softmax_quads<D, BS, NSB, C>(p, sbase, tmem, tile_ids, ctl, warp, lane);
     }
@@ -875,15 +917,15 @@ bool make_map(CUtensorMap *m, const void *base, uint64_t rows, int d, int box_ro
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D, int BS, int NK, int NV, int NSB, int QS, int SPLIT, int MINB>
+template <int D, int BS, int NK, int NV, int NSB, int QS, int SPLIT, int PAIR, int MINB>
 bsa_status launch_tc(const FwdArgs &a, cudaStream_t st)
 {
-    using C = Cfg<D, BS, NK, NV, NSB, QS>;
+    using C = Cfg<D, BS, NK, NV, NSB, QS, PAIR>;
     constexpr int kThreads = Roles<SPLIT>::kThreads;
     static_assert(MINB * (C::SMEM_ALLOC + 1024) <= 233472, "shared memory for MINB CTAs per SM");
     static_assert(C::SMEM_ALLOC <= 227 * 1024, "shared memory budget");
     static_assert(C::TCOLS_USED <= C::TCOLS, "TMEM budget");
-    auto kern = fwd_tc_kernel<D, BS, NK, NV, NSB, QS, SPLIT, MINB>;
+    auto kern = fwd_tc_kernel<D, BS, NK, NV, NSB, QS, SPLIT, PAIR, MINB>;
     static int grid_cap = 0;
     if (grid_cap == 0) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC) != cudaSuccess)
@@ -954,11 +996,11 @@ size_t fwd_workspace_bytes(int B, int H, int N, int d, int block)
 
 bsa_status launch_forward_tc(const FwdArgs &a, cudaStream_t st)
 {
-    // <D, BS, K stages, V stages, S/P buffers, Q slots, threads per row, CTAs per SM>
-    if (a.d == 64 && a.block == 64) return launch_tc<64, 64, 4, 5, 3, 2, 1, 2>(a, st);
-    if (a.d == 128 && a.block == 64) return launch_tc<128, 64, 2, 2, 2, 1, 1, 2>(a, st);
-    if (a.d == 64 && a.block == 128) return launch_tc<64, 128, 5, 6, 3, 2, 2, 1>(a, st);
-    if (a.d == 128 && a.block == 128) return launch_tc<128, 128, 3, 2, 3, 1, 2, 1>(a, st);
+    // <D, BS, K stages, V stages, S/P buffers, Q slots, threads per row, blocks per step, CTAs per SM>
+    if (a.d == 64 && a.block == 64) return launch_tc<64, 64, 4, 5, 3, 2, 1, 1, 2>(a, st);
+    if (a.d == 128 && a.block == 64) return launch_tc<128, 64, 2, 2, 2, 1, 1, 1, 2>(a, st);
+    if (a.d == 64 && a.block == 128) return launch_tc<64, 128, 5, 6, 3, 2, 2, 1, 1>(a, st);
+    if (a.d == 128 && a.block == 128) return launch_tc<128, 128, 3, 2, 3, 1, 2, 1, 1>(a, st);
     return BSA_ERR_SHAPE;
 }
 

@@ -80,6 +80,16 @@ struct TileWalk {
         m = full ? full : (((b0 >> bit) & 1u) | (((b1 >> bit) & 1u) << 1));
         return true;
     }
+
+    // Up to P consecutive items of the walk (one KV step); returns how many (0 = done).
+    template <int P>
+    __device__ __forceinline__ int next_step(int (&js)[2], uint32_t (&ms)[2])
+    {
+        if (!next(js[0], ms[0])) return 0;
+        if (P == 2 && next(js[1], ms[1])) return 2;
+        ms[1] = 0u;
+        return 1;
+    }
 };
 
 }  // namespace bsa
