@@ -38,12 +38,13 @@
 namespace bsa {
 namespace {
 
-// Warp roles: 4 * SPLIT softmax warps, then the TMA producer, then the MMA issuer.
+// Warp roles: 4 * SPLIT softmax warps, then the TMA producer, the QK^T issuer
+// and the PV issuer (one thread each; TMEM is allocated by the PV issuer's warp).
 template <int SPLIT>
 struct Roles {
     static constexpr int kSoftmaxWarps = 4 * SPLIT;
-    static constexpr int kProducerWarp = kSoftmaxWarps, kMmaWarp = kSoftmaxWarps + 1;
-    static constexpr int kThreads = (kSoftmaxWarps + 2) * 32;
+    static constexpr int kProducerWarp = kSoftmaxWarps, kQkWarp = kSoftmaxWarps + 1, kMmaWarp = kSoftmaxWarps + 2;
+    static constexpr int kThreads = (kSoftmaxWarps + 3) * 32;
 };
 constexpr int kTileM = 128;
 constexpr float kRescaleLog2 = 8.0f;
@@ -84,8 +85,8 @@ struct Cfg {
     static constexpr int B_KFULL = 4, B_KEMPTY = B_KFULL + NK, B_VFULL = B_KEMPTY + NK, B_VEMPTY = B_VFULL + NV;
     static constexpr int B_SFULL = B_VEMPTY + NV, B_PFULL = B_SFULL + NSB, B_PVDONE = B_SFULL + 2 * NSB;
     static constexpr int B_OEMPTY = B_SFULL + 3 * NSB, B_TFULL = B_OEMPTY + 1, B_TEMPTY = B_TFULL + 2;
-    static constexpr int B_DRAIN = B_TEMPTY + 2;
-    static constexpr int NBAR = B_DRAIN + 1;
+    static constexpr int B_DRAIN = B_TEMPTY + 2;  // two: one per MMA-issuing thread
+    static constexpr int NBAR = B_DRAIN + 2;
     static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
     static constexpr int SMEM = MISC_OFF + 32;
     static constexpr int SMEM_ALLOC = SMEM + 1024;  // manual 1024-byte alignment
@@ -555,14 +556,14 @@ __device__ __forceinline__ void softmax_quads(const TcParams &p, uint32_t sbase,
 }
 
 template <int D, int BS, int NK, int NV, int NSB, int QS, int SPLIT, int PAIR, int MINB>
-__global__ void __launch_bounds__((4 * SPLIT + 2) * 32, MINB)
+__global__ void __launch_bounds__((4 * SPLIT + 3) * 32, MINB)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const TcParams p)
 {
     static_assert(PAIR == 1 || SPLIT == 1, "two-block steps use one softmax thread per row");
     using C = Cfg<D, BS, NK, NV, NSB, QS, PAIR>;
     using R = Roles<SPLIT>;
-    constexpr int kProducerWarp = R::kProducerWarp, kMmaWarp = R::kMmaWarp;
+    constexpr int kProducerWarp = R::kProducerWarp, kQkWarp = R::kQkWarp, kMmaWarp = R::kMmaWarp;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
@@ -593,10 +594,11 @@ __global__ void __launch_bounds__((4 * SPLIT + 2) * 32, MINB)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(bar(C::B_TFULL + b), 1);
-            mbar_init(bar(C::B_TEMPTY + b), R::kSoftmaxWarps + 1);
+            mbar_init(bar(C::B_TEMPTY + b), R::kSoftmaxWarps + 2);
         }
         mbar_init(bar(C::B_OEMPTY), R::kSoftmaxWarps);
         mbar_init(bar(C::B_DRAIN), 1);
+        mbar_init(bar(C::B_DRAIN + 1), 1);
         misc[1] = 0u;
         fence_mbar_init();
     }
@@ -700,38 +702,17 @@ __global__ void __launch_bounds__((4 * SPLIT + 2) * 32, MINB)
                     wait_bar_drain(bar(C::B_QFULL + e2 % QS), (e2 / QS) & 1, p.wait_limit_ns);
             }
         }
-    } else if (warp == kMmaWarp) {
-        // ------------------------------------------------------------ MMA issuer
+    } else if (warp == kQkWarp) {
+        // ------------------------------------------------------------ QK^T issuer
+        // Runs ahead of the softmax: QK^T of step G needs only K(G) and S/P buffer
+        // G % NSB, which is free once PV(G - NSB) completed.
         if (lane == 0 && !stall) {
-            const uint32_t tS = tmem;                   // NSB S/P buffers of kStep columns
-            const uint32_t tO = tmem + NSB * C::kStep;  // O accumulator, D columns
-            // shared-memory descriptors of K and V slot 0 (slots and steps are added as offsets:
+            const uint32_t tS = tmem;  // NSB S/P buffers of kStep columns
+            // shared-memory descriptor of K slot 0 (slots and steps are added as offsets:
             // the address field holds addr >> 4 and never carries for these sizes)
             const uint64_t kdesc0 = sdesc_sw128(sbase + C::K_OFF, 16, 1024);
-            const uint64_t vdesc0 = sdesc_sw128(sbase + C::V_OFF, C::kKVChunk, 1024);
             int G = 0, e = 0, tcount = 0;
             bool ok = true;
-            // PV of step t (tcnt KV blocks); `first` = first step of its tile (overwrites O)
-            auto issue_pv = [&](int t, bool first, int tcnt) -> bool {
-                const int b = t % NSB, s = t % NV;
-                if (!wait_bar(bar(C::B_PFULL + b), (t / NSB) & 1, ctl)) return false;
-                if (!wait_bar(bar(C::B_VFULL + s), (t / NV) & 1, ctl)) return false;
-                // the previous tile's epilogue must have read O before it is overwritten
-                if (first && e >= 1 && !wait_bar(bar(C::B_OEMPTY), (e - 1) & 1, ctl)) return false;
-                tc_fence_after();
-                // V slot s: descriptor of its first 16-row step; step kk adds kk * 2048 bytes
-                const uint64_t vdesc = vdesc0 + static_cast<uint64_t>(s * (C::kKVBytes >> 4));
-                const uint32_t pa = tS + b * C::kStep;
-                const int nk = tcnt * (BS / 16);  // 16-row K steps of the blocks this step holds
-#pragma unroll
-                for (int kk = 0; kk < C::kStep / 16; ++kk)
-                    if (kk < nk)
-                        mma_ts(tO, pa + kk * 8, vdesc + static_cast<uint64_t>(kk * (16 * 128 >> 4)), C::IDESC_PV,
-                               (first && kk == 0) ? 0u : 1u);
-                tc_commit(bar(C::B_PVDONE + b));
-                tc_commit(bar(C::B_VEMPTY + s));
-                return true;
-            };
             while (ok) {
                 const int slot = tcount & 1;
                 if (!wait_bar(bar(C::B_TFULL + slot), (tcount >> 1) & 1, ctl)) break;
@@ -748,16 +729,11 @@ __global__ void __launch_bounds__((4 * SPLIT + 2) * 32, MINB)
                 uint32_t ms[2];
                 int cnt = walk.next_step<PAIR>(js, ms);
                 if (cnt == 0) continue;
-                int prev_cnt = 0;
                 const int qs = e % QS;
                 if (!wait_bar(bar(C::B_QFULL + qs), (e / QS) & 1, ctl)) break;
                 tc_fence_after();
                 const uint64_t qdesc = sdesc_sw128(sbase + C::Q_OFF + qs * C::kQBytes, 16, 1024);
-                const int G0 = G;
                 do {
-                    // With a single S/P buffer the previous step's PV must be issued
-                    // before QK^T overwrites the buffer it reads P from.
-                    if (NSB == 1 && G > G0 && !issue_pv(G - 1, G - 1 == G0, prev_cnt)) { ok = false; break; }
                     const int s = G % NK, b = G % NSB;
                     if (!wait_bar(bar(C::B_KFULL + s), (G / NK) & 1, ctl)) { ok = false; break; }
                     // S/P buffer b was last read by PV(G - NSB)
@@ -774,13 +750,64 @@ __global__ void __launch_bounds__((4 * SPLIT + 2) * 32, MINB)
                     }
                     tc_commit(bar(C::B_SFULL + b));
                     tc_commit(bar(C::B_KEMPTY + s));
-                    if (NSB > 1 && G > G0 && !issue_pv(G - 1, G - 1 == G0, prev_cnt)) { ok = false; break; }
-                    prev_cnt = cnt;
                     ++G;
                 } while ((cnt = walk.next_step<PAIR>(js, ms)) != 0);
                 if (!ok) break;
+                // the tile's last QK^T: its Q slot is free once these MMAs complete
                 tc_commit(bar(C::B_QEMPTY + qs));
-                if (!issue_pv(G - 1, G - 1 == G0, prev_cnt)) break;
+                ++e;
+            }
+            // all MMAs issued by this thread have completed before TMEM is freed
+            tc_commit(bar(C::B_DRAIN + 1));
+            wait_bar_drain(bar(C::B_DRAIN + 1), 0, p.wait_limit_ns);
+        }
+    } else if (warp == kMmaWarp) {
+        // ------------------------------------------------------------ PV issuer
+        if (lane == 0 && !stall) {
+            const uint32_t tS = tmem;                   // NSB S/P buffers of kStep columns
+            const uint32_t tO = tmem + NSB * C::kStep;  // O accumulator, D columns
+            const uint64_t vdesc0 = sdesc_sw128(sbase + C::V_OFF, C::kKVChunk, 1024);
+            int G = 0, e = 0, tcount = 0;
+            bool ok = true;
+            while (ok) {
+                const int slot = tcount & 1;
+                if (!wait_bar(bar(C::B_TFULL + slot), (tcount >> 1) & 1, ctl)) break;
+                const int tile = tile_ids[slot];
+                mbar_arrive(bar(C::B_TEMPTY + slot));
+                ++tcount;
+                if (tile < 0) break;
+                int64_t bh;
+                int qt;
+                tile_coords(p, tile, bh, qt);
+                TileWalk walk;
+                walk_init<BS>(walk, p, bh, qt);
+                int js[2];
+                uint32_t ms[2];
+                int cnt = walk.next_step<PAIR>(js, ms);
+                if (cnt == 0) continue;
+                bool first = true;
+                do {
+                    const int b = G % NSB, s = G % NV;
+                    if (!wait_bar(bar(C::B_PFULL + b), (G / NSB) & 1, ctl)) { ok = false; break; }
+                    if (!wait_bar(bar(C::B_VFULL + s), (G / NV) & 1, ctl)) { ok = false; break; }
+                    // the first PV of a tile overwrites O: the previous tile's epilogue must have read it
+                    if (first && e >= 1 && !wait_bar(bar(C::B_OEMPTY), (e - 1) & 1, ctl)) { ok = false; break; }
+                    tc_fence_after();
+                    // V slot s: descriptor of its first 16-row step; step kk adds kk * 2048 bytes
+                    const uint64_t vdesc = vdesc0 + static_cast<uint64_t>(s * (C::kKVBytes >> 4));
+                    const uint32_t pa = tS + b * C::kStep;
+                    const int nk = cnt * (BS / 16);  // 16-row K steps of the blocks this step holds
+#pragma unroll
+                    for (int kk = 0; kk < C::kStep / 16; ++kk)
+                        if (kk < nk)
+                            mma_ts(tO, pa + kk * 8, vdesc + static_cast<uint64_t>(kk * (16 * 128 >> 4)), C::IDESC_PV,
+                                   (first && kk == 0) ? 0u : 1u);
+                    tc_commit(bar(C::B_PVDONE + b));
+                    tc_commit(bar(C::B_VEMPTY + s));
+                    first = false;
+                    ++G;
+                } while ((cnt = walk.next_step<PAIR>(js, ms)) != 0);
+                if (!ok) break;
                 ++e;
             }
             // all MMAs issued by this thread have completed before TMEM is freed
