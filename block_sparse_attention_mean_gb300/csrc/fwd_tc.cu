@@ -1027,7 +1027,7 @@ bsa_status launch_forward_tc(const FwdArgs &a, cudaStream_t st)
     if (a.d == 64 && a.block == 64) return launch_tc<64, 64, 4, 5, 3, 2, 1, 1, 2>(a, st);
     if (a.d == 128 && a.block == 64) return launch_tc<128, 64, 2, 2, 2, 1, 1, 1, 2>(a, st);
     if (a.d == 64 && a.block == 128) return launch_tc<64, 128, 5, 6, 3, 2, 2, 1, 1>(a, st);
-    if (a.d == 128 && a.block == 128) return launch_tc<128, 128, 3, 2, 3, 1, 2, 1, 1>(a, st);
+    if (a.d == 128 && a.block == 128) return launch_tc<128, 128, 2, 4, 3, 1, 2, 1, 1>(a, st);
     return BSA_ERR_SHAPE;
 }
 
