@@ -88,7 +88,8 @@ struct Cfg {
     static constexpr int B_DRAIN = B_TEMPTY + 2;  // two: one per MMA-issuing thread
     static constexpr int NBAR = B_DRAIN + 2;
     static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
-    static constexpr int SMEM = MISC_OFF + 32;
+    static constexpr int MISC_WORDS = 4 + NSB;  // TMEM base, abort flag, 2 tile ids, NSB step descriptors
+    static constexpr int SMEM = MISC_OFF + 4 * ((MISC_WORDS + 7) & ~7);
     static constexpr int SMEM_ALLOC = SMEM + 1024;  // manual 1024-byte alignment
     static constexpr int TCOLS_USED = NSB * kStep + D;
     static constexpr int TCOLS = TCOLS_USED <= 256 ? 256 : 512;
@@ -96,6 +97,23 @@ struct Cfg {
     static constexpr uint32_t IDESC_QK_HALF = idesc_bf16_f32(kTileM, BS, 0, 0);  // a step with one block
     static constexpr uint32_t IDESC_PV = idesc_bf16_f32(kTileM, D, 0, 1);
 };
+
+// The producer marks a tile whose walk is empty in the scheduler ring, so the
+// other roles need not walk the index to find out.
+constexpr int32_t kEmptyTile = 1 << 30;
+
+// Step descriptor the QK^T issuer leaves beside S/P buffer b (it is the only
+// consumer that walks the index): bits 0-1 blocks in the step, bits 2-3 and 4-5
+// which of the tile's Q blocks have block 0 and block 1 of the step, bit 6 set
+// on the tile's last step. The S-full barrier publishes it to the softmax warps
+// and the P-full barrier carries it on to the PV issuer.
+__device__ __forceinline__ uint32_t step_desc(int cnt, const uint32_t (&ms)[2], bool last)
+{
+    return static_cast<uint32_t>(cnt) | (ms[0] << 2) | (ms[1] << 4) | (last ? 64u : 0u);
+}
+__device__ __forceinline__ int desc_count(uint32_t d) { return static_cast<int>(d & 3u); }
+__device__ __forceinline__ uint32_t desc_members(uint32_t d, int q) { return (d >> (2 + 2 * q)) & 3u; }
+__device__ __forceinline__ bool desc_last(uint32_t d) { return (d & 64u) != 0u; }
 
 struct Ctl {
     volatile uint32_t *abort_flag;
@@ -135,12 +153,19 @@ __device__ __noinline__ bool wait_bar_drain(uint32_t bar, uint32_t parity, unsig
     return true;
 }
 
-// Warp-uniform wait: lane 0 waits, the verdict is broadcast.
-__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const Ctl &c, int lane)
+// Every lane waits (and acquires) itself; the verdict is made warp-uniform by a vote.
+// (Cheaper than one lane waiting while the others park on a shuffle.)
+__device__ __forceinline__ bool warp_wait_all(uint32_t bar, uint32_t parity, const Ctl &c)
 {
-    int ok = 0;
-    if (lane == 0) ok = wait_bar(bar, parity, c) ? 1 : 0;
-    return __shfl_sync(0xffffffffu, ok, 0) != 0;
+    return __all_sync(0xffffffffu, wait_bar(bar, parity, c) ? 1 : 0) != 0;
+}
+
+// warp_wait_all for S buffer `b`, then the step descriptor written before it.
+// Returns 0xFFFFFFFF when the wait failed.
+__device__ __forceinline__ uint32_t warp_wait_step(uint32_t bar, uint32_t parity, const Ctl &c,
+                                                   const volatile uint32_t *desc)
+{
+    return warp_wait_all(bar, parity, c) ? *desc : 0xFFFFFFFFu;
 }
 
 __device__ __forceinline__ void tile_coords(const TcParams &p, int tile, int64_t &bh, int &qt)
@@ -182,13 +207,10 @@ __device__ __forceinline__ bool fetch_tile(uint32_t sbase, volatile int32_t *til
                                            int &tcount, int &tile)
 {
     const int slot = tcount & 1;
-    if (!warp_wait(barrier_addr<C>(sbase, C::B_TFULL + slot), (tcount >> 1) & 1, ctl, lane)) return false;
-    int t = 0;
-    if (lane == 0) {
-        t = tile_ids[slot];
-        mbar_arrive(barrier_addr<C>(sbase, C::B_TEMPTY + slot));
-    }
-    tile = __shfl_sync(0xffffffffu, t, 0);
+    if (!warp_wait_all(barrier_addr<C>(sbase, C::B_TFULL + slot), (tcount >> 1) & 1, ctl)) return false;
+    tile = tile_ids[slot];
+    __syncwarp();
+    if (lane == 0) mbar_arrive(barrier_addr<C>(sbase, C::B_TEMPTY + slot));
     ++tcount;
     return true;
 }
@@ -200,7 +222,8 @@ __device__ __forceinline__ bool fetch_tile(uint32_t sbase, volatile int32_t *til
 // row's Q block does not have it.
 template <int D, int BS, int NSB, int PAIR, class C>
 __device__ __forceinline__ void softmax_rows(const TcParams &p, uint32_t sbase, uint32_t tmem,
-                                             volatile int32_t *tile_ids, const Ctl &ctl, int warp, int lane)
+                                             volatile int32_t *tile_ids, const volatile uint32_t *desc,
+                                             const Ctl &ctl, int warp, int lane)
 {
     auto bar = [&](int idx) -> uint32_t { return barrier_addr<C>(sbase, idx); };
     constexpr int kStep = C::kStep;
@@ -215,19 +238,15 @@ __device__ __forceinline__ void softmax_rows(const TcParams &p, uint32_t sbase, 
     for (;;) {
         int tile;
         if (!fetch_tile<C>(sbase, tile_ids, ctl, lane, tcount, tile) || tile < 0) return;
+        const bool empty = (tile & kEmptyTile) != 0;
         int64_t bh;
         int qt;
-        tile_coords(p, tile, bh, qt);
+        tile_coords(p, tile & ~kEmptyTile, bh, qt);
         const int row = qt * kTileM + trow;
         const bool row_valid = row < p.N;
         const int64_t grow = bh * p.N + row;
         __nv_bfloat16 *orow = p.O + grow * D;
-        TileWalk walk;
-        walk_init<BS>(walk, p, bh, qt);
-        int js[2];
-        uint32_t ms[2];
-        int cnt = walk.next_step<PAIR>(js, ms);
-        if (cnt == 0) {
+        if (empty) {
             if (row_valid) {
                 const uint4 z = make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
@@ -237,15 +256,18 @@ __device__ __forceinline__ void softmax_rows(const TcParams &p, uint32_t sbase, 
             continue;
         }
         float m_run = -CUDART_INF_F, l_run = 0.0f, lp_run = 0.0f;
+        bool last;
         do {
             const int b = G % NSB;
-            if (!warp_wait(bar(C::B_SFULL + b), (G / NSB) & 1, ctl, lane)) return;
+            const uint32_t sd = warp_wait_step(bar(C::B_SFULL + b), (G / NSB) & 1, ctl, desc + b);
+            if (sd == 0xFFFFFFFFu) return;
             tc_fence_after();
+            last = desc_last(sd);
             bool act[PAIR];
             bool any = false;
 #pragma unroll
             for (int q = 0; q < PAIR; ++q) {
-                act[q] = q < cnt && ((ms[q] >> qblk) & 1u) != 0u;
+                act[q] = q < desc_count(sd) && ((desc_members(sd, q) >> qblk) & 1u) != 0u;
                 any |= act[q];
             }
             bool resc = false;
@@ -322,7 +344,7 @@ __device__ __forceinline__ void softmax_rows(const TcParams &p, uint32_t sbase, 
             if (__any_sync(0xffffffffu, resc)) {
                 // O holds the previous steps' sum: rescale it once the last PV landed
                 const int t = G - 1;
-                if (!warp_wait(bar(C::B_PVDONE + t % NSB), (t / NSB) & 1, ctl, lane)) return;
+                if (!warp_wait_all(bar(C::B_PVDONE + t % NSB), (t / NSB) & 1, ctl)) return;
                 tc_fence_after();
 #pragma unroll
                 for (int c = 0; c < D / 32; ++c) {
@@ -340,10 +362,10 @@ __device__ __forceinline__ void softmax_rows(const TcParams &p, uint32_t sbase, 
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(C::B_PFULL + b));
             ++G;
-        } while ((cnt = walk.next_step<PAIR>(js, ms)) != 0);
+        } while (!last);
         // epilogue: O / l, LSE = ln2 * (m + log2 l)
         const int t = G - 1;
-        if (!warp_wait(bar(C::B_PVDONE + t % NSB), (t / NSB) & 1, ctl, lane)) return;
+        if (!warp_wait_all(bar(C::B_PVDONE + t % NSB), (t / NSB) & 1, ctl)) return;
         tc_fence_after();
         const float inv_l = lp_run > 0.0f ? 1.0f / lp_run : 0.0f;
 #pragma unroll
@@ -375,7 +397,8 @@ __device__ __forceinline__ void softmax_rows(const TcParams &p, uint32_t sbase, 
 // max and sums are reduced over its 4 lanes with two shuffles.
 template <int D, int BS, int NSB, class C>
 __device__ __forceinline__ void softmax_quads(const TcParams &p, uint32_t sbase, uint32_t tmem,
-                                              volatile int32_t *tile_ids, const Ctl &ctl, int warp, int lane)
+                                              volatile int32_t *tile_ids, const volatile uint32_t *desc,
+                                              const Ctl &ctl, int warp, int lane)
 {
     auto bar = [&](int idx) -> uint32_t { return barrier_addr<C>(sbase, idx); };
     constexpr int RS = BS / 8;  // 8-column groups of S
@@ -391,19 +414,16 @@ __device__ __forceinline__ void softmax_quads(const TcParams &p, uint32_t sbase,
     for (;;) {
         int tile;
         if (!fetch_tile<C>(sbase, tile_ids, ctl, lane, tcount, tile) || tile < 0) return;
+        const bool empty = (tile & kEmptyTile) != 0;
         int64_t bh;
         int qt;
-        tile_coords(p, tile, bh, qt);
+        tile_coords(p, tile & ~kEmptyTile, bh, qt);
         const int row_lo = qt * kTileM + r_lo, row_hi = row_lo + 8;
         const bool lo_valid = row_lo < p.N, hi_valid = row_hi < p.N;
         const int64_t g_lo = bh * p.N + row_lo, g_hi = g_lo + 8;
         uint32_t *o_lo = reinterpret_cast<uint32_t *>(p.O + g_lo * D + cpair);
         uint32_t *o_hi = reinterpret_cast<uint32_t *>(p.O + g_hi * D + cpair);
-        TileWalk walk;
-        walk_init<BS>(walk, p, bh, qt);
-        int j;
-        uint32_t m;
-        if (!walk.next(j, m)) {
+        if (empty) {
 #pragma unroll
             for (int g = 0; g < RO; ++g) {
                 if (lo_valid) o_lo[4 * g] = 0u;
@@ -417,13 +437,16 @@ __device__ __forceinline__ void softmax_quads(const TcParams &p, uint32_t sbase,
         }
         float m_lo = -CUDART_INF_F, m_hi = -CUDART_INF_F;
         float l_lo = 0.0f, l_hi = 0.0f, lp_lo = 0.0f, lp_hi = 0.0f;  // this thread's columns only
+        bool last;
         do {
             const int b = G % NSB;
-            if (!warp_wait(bar(C::B_SFULL + b), (G / NSB) & 1, ctl, lane)) return;
+            const uint32_t sd = warp_wait_step(bar(C::B_SFULL + b), (G / NSB) & 1, ctl, desc + b);
+            if (sd == 0xFFFFFFFFu) return;
             tc_fence_after();
+            last = desc_last(sd);
             bool resc = false;
             float a_lo = 1.0f, a_hi = 1.0f;
-            if ((m >> qblk) & 1u) {
+            if ((desc_members(sd, 0) >> qblk) & 1u) {
                 uint32_t sv[4 * RS];
                 tmem_ld_16x256b<RS>(tbase + b * BS, sv);
                 tmem_wait_ld();
@@ -502,7 +525,7 @@ __device__ __forceinline__ void softmax_quads(const TcParams &p, uint32_t sbase,
             }
             if (__any_sync(0xffffffffu, resc)) {
                 const int t = G - 1;
-                if (!warp_wait(bar(C::B_PVDONE + t % NSB), (t / NSB) & 1, ctl, lane)) return;
+                if (!warp_wait_all(bar(C::B_PVDONE + t % NSB), (t / NSB) & 1, ctl)) return;
                 tc_fence_after();
                 uint32_t ov[4 * RO];
                 tmem_ld_16x256b<RO>(tO, ov);
@@ -522,7 +545,7 @@ __device__ __forceinline__ void softmax_quads(const TcParams &p, uint32_t sbase,
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(C::B_PFULL + b));
             ++G;
-        } while (walk.next(j, m));
+        } while (!last);
         // epilogue: whole-row sums over the 4 lanes of each row, then O / l and LSE
 #pragma unroll
         for (int o = 1; o <= 2; o <<= 1) {
@@ -532,7 +555,7 @@ __device__ __forceinline__ void softmax_quads(const TcParams &p, uint32_t sbase,
             lp_hi += __shfl_xor_sync(0xffffffffu, lp_hi, o);
         }
         const int t = G - 1;
-        if (!warp_wait(bar(C::B_PVDONE + t % NSB), (t / NSB) & 1, ctl, lane)) return;
+        if (!warp_wait_all(bar(C::B_PVDONE + t % NSB), (t / NSB) & 1, ctl)) return;
         tc_fence_after();
         uint32_t ov[4 * RO];
         tmem_ld_16x256b<RO>(tO, ov);
@@ -569,8 +592,10 @@ __global__ void __launch_bounds__((4 * SPLIT + 3) * 32, MINB)
     const uint32_t sbase = smem_u32(smem);
     auto bar = [&](int idx) -> uint32_t { return sbase + C::BAR_OFF + 8u * idx; };
     uint32_t *misc = reinterpret_cast<uint32_t *>(smem + C::MISC_OFF);
-    // misc[0]: TMEM base, misc[1]: abort flag, misc[2..3]: tile ids of the scheduler ring
+    // misc[0]: TMEM base, misc[1]: abort flag, misc[2..3]: tile ids of the scheduler ring,
+    // misc[4..4+NSB): step descriptors of the S/P buffers
     volatile int32_t *tile_ids = reinterpret_cast<volatile int32_t *>(misc + 2);
+    volatile uint32_t *desc = reinterpret_cast<volatile uint32_t *>(misc + 4);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -588,7 +613,7 @@ __global__ void __launch_bounds__((4 * SPLIT + 3) * 32, MINB)
             mbar_init(bar(C::B_VEMPTY + s), 1);
         }
         for (int b = 0; b < NSB; ++b) {
-            mbar_init(bar(C::B_SFULL + b), 1);
+            mbar_init(bar(C::B_SFULL + b), 2);  // the issuer's arrive (descriptor) + the QK^T commit
             mbar_init(bar(C::B_PFULL + b), R::kSoftmaxWarps);
             mbar_init(bar(C::B_PVDONE + b), 1);
         }
@@ -630,20 +655,22 @@ __global__ void __launch_bounds__((4 * SPLIT + 3) * 32, MINB)
                 if (tcount >= 2 && !wait_bar(bar(C::B_TEMPTY + slot), ((tcount >> 1) - 1) & 1, ctl)) break;
                 const uint32_t id = atomicAdd(p.tile_counter, 1u);
                 const int tile = id < static_cast<uint32_t>(p.n_tiles) ? p.tile_list[id] : -1;
-                tile_ids[slot] = tile;
+                int64_t bh = 0;
+                int qt = 0;
+                TileWalk walk;
+                int js[2];
+                uint32_t ms[2];
+                int cnt = 0;
+                if (tile >= 0) {
+                    tile_coords(p, tile, bh, qt);
+                    walk_init<BS>(walk, p, bh, qt);
+                    cnt = walk.next_step<PAIR>(js, ms);
+                }
+                tile_ids[slot] = tile >= 0 && cnt == 0 ? (tile | kEmptyTile) : tile;
                 mbar_arrive(bar(C::B_TFULL + slot));
                 ++tcount;
                 if (tile < 0) break;
-                if (stall) continue;
-                int64_t bh;
-                int qt;
-                tile_coords(p, tile, bh, qt);
-                TileWalk walk;
-                walk_init<BS>(walk, p, bh, qt);
-                int js[2];
-                uint32_t ms[2];
-                int cnt = walk.next_step<PAIR>(js, ms);
-                if (cnt == 0) continue;  // empty tile: nothing to load
+                if (stall || cnt == 0) continue;  // empty tile: nothing to load
                 const int qs = e % QS;  // Q slot; it was last used by tile e - QS
                 if (e >= QS && !wait_bar(bar(C::B_QEMPTY + qs), ((e / QS) - 1) & 1, ctl)) break;
                 mbar_arrive_expect_tx(bar(C::B_QFULL + qs), C::kQBytes);
@@ -705,8 +732,10 @@ __global__ void __launch_bounds__((4 * SPLIT + 3) * 32, MINB)
     } else if (warp == kQkWarp) {
         // ------------------------------------------------------------ QK^T issuer
         // Runs ahead of the softmax: QK^T of step G needs only K(G) and S/P buffer
-        // G % NSB, which is free once PV(G - NSB) completed.
-        if (lane == 0 && !stall) {
+        // G % NSB, which is free once PV(G - NSB) completed. The whole warp runs the
+        // loop (waits and walk are warp-uniform) and one elected lane issues: tcgen05
+        // issue from converged code is several times cheaper than from a lone lane.
+        if (!stall) {
             const uint32_t tS = tmem;  // NSB S/P buffers of kStep columns
             // shared-memory descriptor of K slot 0 (slots and steps are added as offsets:
             // the address field holds addr >> 4 and never carries for these sizes)
@@ -715,55 +744,78 @@ __global__ void __launch_bounds__((4 * SPLIT + 3) * 32, MINB)
             bool ok = true;
             while (ok) {
                 const int slot = tcount & 1;
-                if (!wait_bar(bar(C::B_TFULL + slot), (tcount >> 1) & 1, ctl)) break;
+                if (!warp_wait_all(bar(C::B_TFULL + slot), (tcount >> 1) & 1, ctl)) break;
                 const int tile = tile_ids[slot];
-                mbar_arrive(bar(C::B_TEMPTY + slot));
+                if (lane == 0) mbar_arrive(bar(C::B_TEMPTY + slot));
                 ++tcount;
                 if (tile < 0) break;
+                if (tile & kEmptyTile) continue;
                 int64_t bh;
                 int qt;
                 tile_coords(p, tile, bh, qt);
                 TileWalk walk;
                 walk_init<BS>(walk, p, bh, qt);
-                int js[2];
-                uint32_t ms[2];
+                // one step of lookahead: a step's descriptor says whether it is the tile's last
+                int js[2], jn[2];
+                uint32_t ms[2], mn[2];
                 int cnt = walk.next_step<PAIR>(js, ms);
-                if (cnt == 0) continue;
+                int cnt_n = walk.next_step<PAIR>(jn, mn);
                 const int qs = e % QS;
-                if (!wait_bar(bar(C::B_QFULL + qs), (e / QS) & 1, ctl)) break;
+                if (!warp_wait_all(bar(C::B_QFULL + qs), (e / QS) & 1, ctl)) break;
                 tc_fence_after();
                 const uint64_t qdesc = sdesc_sw128(sbase + C::Q_OFF + qs * C::kQBytes, 16, 1024);
                 do {
                     const int s = G % NK, b = G % NSB;
-                    if (!wait_bar(bar(C::B_KFULL + s), (G / NK) & 1, ctl)) { ok = false; break; }
-                    // S/P buffer b was last read by PV(G - NSB)
-                    if (G >= NSB && !wait_bar(bar(C::B_PVDONE + b), ((G / NSB) - 1) & 1, ctl)) { ok = false; break; }
+                    if (!warp_wait_all(bar(C::B_KFULL + s), (G / NK) & 1, ctl)) { ok = false; break; }
+                    // S/P buffer b (and its descriptor) was last read by PV(G - NSB)
+                    if (G >= NSB && !warp_wait_all(bar(C::B_PVDONE + b), ((G / NSB) - 1) & 1, ctl)) {
+                        ok = false;
+                        break;
+                    }
+                    if (lane == 0) {
+                        desc[b] = step_desc(cnt, ms, cnt_n == 0);
+                        mbar_arrive(bar(C::B_SFULL + b));  // release: the descriptor is visible with the phase
+                    }
                     tc_fence_after();
                     // K-major, 128-byte swizzle: step kk is 32 bytes into 64-column slab kk / 4
                     const uint64_t kdesc = kdesc0 + static_cast<uint64_t>(s * (C::kKVBytes >> 4));
                     const uint32_t idesc = cnt == PAIR ? C::IDESC_QK : C::IDESC_QK_HALF;
+                    __syncwarp();
+                    if (elect_one()) {
 #pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint64_t off_q = static_cast<uint64_t>(((kk >> 2) * C::kQChunk + (kk & 3) * 32) >> 4);
-                        const uint64_t off_k = static_cast<uint64_t>(((kk >> 2) * C::kKVChunk + (kk & 3) * 32) >> 4);
-                        mma_ss(tS + b * C::kStep, qdesc + off_q, kdesc + off_k, idesc, kk > 0 ? 1u : 0u);
+                        for (int kk = 0; kk < D / 16; ++kk) {
+                            const uint64_t off_q = static_cast<uint64_t>(((kk >> 2) * C::kQChunk + (kk & 3) * 32) >> 4);
+                            const uint64_t off_k = static_cast<uint64_t>(((kk >> 2) * C::kKVChunk + (kk & 3) * 32) >> 4);
+                            mma_ss(tS + b * C::kStep, qdesc + off_q, kdesc + off_k, idesc, kk > 0 ? 1u : 0u);
+                        }
+                        tc_commit(bar(C::B_SFULL + b));
+                        tc_commit(bar(C::B_KEMPTY + s));
                     }
-                    tc_commit(bar(C::B_SFULL + b));
-                    tc_commit(bar(C::B_KEMPTY + s));
+                    __syncwarp();
                     ++G;
-                } while ((cnt = walk.next_step<PAIR>(js, ms)) != 0);
+                    cnt = cnt_n;
+                    ms[0] = mn[0];
+                    ms[1] = mn[1];
+                    if (cnt != 0) cnt_n = walk.next_step<PAIR>(jn, mn);
+                } while (cnt != 0);
                 if (!ok) break;
                 // the tile's last QK^T: its Q slot is free once these MMAs complete
-                tc_commit(bar(C::B_QEMPTY + qs));
+                if (elect_one()) tc_commit(bar(C::B_QEMPTY + qs));
+                __syncwarp();
                 ++e;
             }
-            // all MMAs issued by this thread have completed before TMEM is freed
-            tc_commit(bar(C::B_DRAIN + 1));
-            wait_bar_drain(bar(C::B_DRAIN + 1), 0, p.wait_limit_ns);
+            // all MMAs issued by the elected lane have completed before TMEM is freed
+            __syncwarp();
+            if (elect_one()) {
+                tc_commit(bar(C::B_DRAIN + 1));
+                wait_bar_drain(bar(C::B_DRAIN + 1), 0, p.wait_limit_ns);
+            }
+            __syncwarp();
         }
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------ PV issuer
-        if (lane == 0 && !stall) {
+        // Whole-warp loop with one elected issuing lane, like the QK^T issuer.
+        if (!stall) {
             const uint32_t tS = tmem;                   // NSB S/P buffers of kStep columns
             const uint32_t tO = tmem + NSB * C::kStep;  // O accumulator, D columns
             const uint64_t vdesc0 = sdesc_sw128(sbase + C::V_OFF, C::kKVChunk, 1024);
@@ -771,55 +823,59 @@ __global__ void __launch_bounds__((4 * SPLIT + 3) * 32, MINB)
             bool ok = true;
             while (ok) {
                 const int slot = tcount & 1;
-                if (!wait_bar(bar(C::B_TFULL + slot), (tcount >> 1) & 1, ctl)) break;
+                if (!warp_wait_all(bar(C::B_TFULL + slot), (tcount >> 1) & 1, ctl)) break;
                 const int tile = tile_ids[slot];
-                mbar_arrive(bar(C::B_TEMPTY + slot));
+                if (lane == 0) mbar_arrive(bar(C::B_TEMPTY + slot));
                 ++tcount;
                 if (tile < 0) break;
-                int64_t bh;
-                int qt;
-                tile_coords(p, tile, bh, qt);
-                TileWalk walk;
-                walk_init<BS>(walk, p, bh, qt);
-                int js[2];
-                uint32_t ms[2];
-                int cnt = walk.next_step<PAIR>(js, ms);
-                if (cnt == 0) continue;
-                bool first = true;
+                if (tile & kEmptyTile) continue;
+                bool first = true, last;
                 do {
                     const int b = G % NSB, s = G % NV;
-                    if (!wait_bar(bar(C::B_PFULL + b), (G / NSB) & 1, ctl)) { ok = false; break; }
-                    if (!wait_bar(bar(C::B_VFULL + s), (G / NV) & 1, ctl)) { ok = false; break; }
+                    // the descriptor was written by the QK^T issuer before S(G); P-full orders it after that write
+                    if (!warp_wait_all(bar(C::B_PFULL + b), (G / NSB) & 1, ctl)) { ok = false; break; }
+                    const uint32_t sd = desc[b];
+                    const int cnt = desc_count(sd);
+                    last = desc_last(sd);
+                    if (!warp_wait_all(bar(C::B_VFULL + s), (G / NV) & 1, ctl)) { ok = false; break; }
                     // the first PV of a tile overwrites O: the previous tile's epilogue must have read it
-                    if (first && e >= 1 && !wait_bar(bar(C::B_OEMPTY), (e - 1) & 1, ctl)) { ok = false; break; }
+                    if (first && e >= 1 && !warp_wait_all(bar(C::B_OEMPTY), (e - 1) & 1, ctl)) { ok = false; break; }
                     tc_fence_after();
                     // V slot s: descriptor of its first 16-row step; step kk adds kk * 2048 bytes
                     const uint64_t vdesc = vdesc0 + static_cast<uint64_t>(s * (C::kKVBytes >> 4));
                     const uint32_t pa = tS + b * C::kStep;
                     const int nk = cnt * (BS / 16);  // 16-row K steps of the blocks this step holds
+                    __syncwarp();
+                    if (elect_one()) {
 #pragma unroll
-                    for (int kk = 0; kk < C::kStep / 16; ++kk)
-                        if (kk < nk)
-                            mma_ts(tO, pa + kk * 8, vdesc + static_cast<uint64_t>(kk * (16 * 128 >> 4)), C::IDESC_PV,
-                                   (first && kk == 0) ? 0u : 1u);
-                    tc_commit(bar(C::B_PVDONE + b));
-                    tc_commit(bar(C::B_VEMPTY + s));
+                        for (int kk = 0; kk < C::kStep / 16; ++kk)
+                            if (kk < nk)
+                                mma_ts(tO, pa + kk * 8, vdesc + static_cast<uint64_t>(kk * (16 * 128 >> 4)),
+                                       C::IDESC_PV, (first && kk == 0) ? 0u : 1u);
+                        tc_commit(bar(C::B_PVDONE + b));
+                        tc_commit(bar(C::B_VEMPTY + s));
+                    }
+                    __syncwarp();
                     first = false;
                     ++G;
-                } while ((cnt = walk.next_step<PAIR>(js, ms)) != 0);
+                } while (!last);
                 if (!ok) break;
                 ++e;
             }
-            // all MMAs issued by this thread have completed before TMEM is freed
-            tc_commit(bar(C::B_DRAIN));
-            wait_bar_drain(bar(C::B_DRAIN), 0, p.wait_limit_ns);
+            // all MMAs issued by the elected lane have completed before TMEM is freed
+            __syncwarp();
+            if (elect_one()) {
+                tc_commit(bar(C::B_DRAIN));
+                wait_bar_drain(bar(C::B_DRAIN), 0, p.wait_limit_ns);
+            }
+            __syncwarp();
         }
     } else {
         // ------------------------------------------------------------ softmax + epilogue
         if constexpr (SPLIT == 1)
-            softmax_rows<D, BS, NSB, PAIR, C>(p, sbase, tmem, tile_ids, ctl, warp, lane);
+            softmax_rows<D, BS, NSB, PAIR, C>(p, sbase, tmem, tile_ids, desc, ctl, warp, lane);
         else
-            softmax_quads<D, BS, NSB, C>(p, sbase, tmem, tile_ids, ctl, warp, lane);
+            softmax_quads<D, BS, NSB, C>(p, sbase, tmem, tile_ids, desc, ctl, warp, lane);
     }
 
     tc_fence_before();
