@@ -645,16 +645,21 @@ __global__ void __launch_bounds__((4 * SPLIT + 3) * 32, MINB)
 
     if (warp == kProducerWarp) {
         // ------------------------------------------------------------ TMA producer
-        if (lane == 0) {
+        // Whole-warp loop (uniform waits and walk); one elected lane issues the copies.
+        {
             int G = 0, e = 0, tcount = 0;
             int last_issue = -1;  // last iteration whose K and V loads were issued
             int q_issued = -1;
             bool ok = true;
             while (ok) {
                 const int slot = tcount & 1;
-                if (tcount >= 2 && !wait_bar(bar(C::B_TEMPTY + slot), ((tcount >> 1) - 1) & 1, ctl)) break;
-                const uint32_t id = atomicAdd(p.tile_counter, 1u);
-                const int tile = id < static_cast<uint32_t>(p.n_tiles) ? p.tile_list[id] : -1;
+                if (tcount >= 2 && !warp_wait_all(bar(C::B_TEMPTY + slot), ((tcount >> 1) - 1) & 1, ctl)) break;
+                int tile = -1;
+                if (lane == 0) {
+                    const uint32_t id = atomicAdd(p.tile_counter, 1u);
+                    tile = id < static_cast<uint32_t>(p.n_tiles) ? p.tile_list[id] : -1;
+                }
+                tile = __shfl_sync(0xffffffffu, tile, 0);
                 int64_t bh = 0;
                 int qt = 0;
                 TileWalk walk;
@@ -666,59 +671,72 @@ __global__ void __launch_bounds__((4 * SPLIT + 3) * 32, MINB)
                     walk_init<BS>(walk, p, bh, qt);
                     cnt = walk.next_step<PAIR>(js, ms);
                 }
-                tile_ids[slot] = tile >= 0 && cnt == 0 ? (tile | kEmptyTile) : tile;
-                mbar_arrive(bar(C::B_TFULL + slot));
+                if (lane == 0) {
+                    tile_ids[slot] = tile >= 0 && cnt == 0 ? (tile | kEmptyTile) : tile;
+                    mbar_arrive(bar(C::B_TFULL + slot));
+                }
                 ++tcount;
                 if (tile < 0) break;
                 if (stall || cnt == 0) continue;  // empty tile: nothing to load
                 const int qs = e % QS;  // Q slot; it was last used by tile e - QS
-                if (e >= QS && !wait_bar(bar(C::B_QEMPTY + qs), ((e / QS) - 1) & 1, ctl)) break;
-                mbar_arrive_expect_tx(bar(C::B_QFULL + qs), C::kQBytes);
+                if (e >= QS && !warp_wait_all(bar(C::B_QEMPTY + qs), ((e / QS) - 1) & 1, ctl)) break;
                 const int qrow = static_cast<int>(bh * p.N) + qt * kTileM;
+                __syncwarp();
+                if (elect_one()) {
+                    mbar_arrive_expect_tx(bar(C::B_QFULL + qs), C::kQBytes);
 #pragma unroll
-                for (int c = 0; c < D / 64; ++c)
-                    tma_load_2d(sbase + C::Q_OFF + qs * C::kQBytes + c * C::kQChunk, &tmQ, c * 64, qrow,
-                                bar(C::B_QFULL + qs));
+                    for (int c = 0; c < D / 64; ++c)
+                        tma_load_2d(sbase + C::Q_OFF + qs * C::kQBytes + c * C::kQChunk, &tmQ, c * 64, qrow,
+                                    bar(C::B_QFULL + qs));
+                }
+                __syncwarp();
                 q_issued = e;
                 do {
                     const uint32_t step_bytes = static_cast<uint32_t>(cnt * BS * D * 2);
                     // K slot: freed when the QK^T that read it completes
                     const int ks = G % NK;
-                    if (G >= NK && !wait_bar(bar(C::B_KEMPTY + ks), ((G / NK) - 1) & 1, ctl)) {
+                    if (G >= NK && !warp_wait_all(bar(C::B_KEMPTY + ks), ((G / NK) - 1) & 1, ctl)) {
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(bar(C::B_KFULL + ks), step_bytes);
-                    for (int q = 0; q < cnt; ++q) {
-                        const int krow = static_cast<int>(bh * p.N) + js[q] * BS;
+                    if (elect_one()) {
+                        mbar_arrive_expect_tx(bar(C::B_KFULL + ks), step_bytes);
+                        for (int q = 0; q < cnt; ++q) {
+                            const int krow = static_cast<int>(bh * p.N) + js[q] * BS;
 #pragma unroll
-                        for (int c = 0; c < D / 64; ++c)
-                            tma_load_2d(sbase + C::K_OFF + ks * C::kKVBytes + c * C::kKVChunk + q * BS * 128, &tmK,
-                                        c * 64, krow, bar(C::B_KFULL + ks));
+                            for (int c = 0; c < D / 64; ++c)
+                                tma_load_2d(sbase + C::K_OFF + ks * C::kKVBytes + c * C::kKVChunk + q * BS * 128,
+                                            &tmK, c * 64, krow, bar(C::B_KFULL + ks));
+                        }
                     }
+                    __syncwarp();
                     // V slot: freed when the PV that read it completes
                     const int vs = G % NV;
-                    if (G >= NV && !wait_bar(bar(C::B_VEMPTY + vs), ((G / NV) - 1) & 1, ctl)) {
+                    if (G >= NV && !warp_wait_all(bar(C::B_VEMPTY + vs), ((G / NV) - 1) & 1, ctl)) {
                         // the K load of this iteration is in flight: drain it below
                         last_issue = G - 1;
                         ok = false;
-                        wait_bar_drain(bar(C::B_KFULL + ks), (G / NK) & 1, p.wait_limit_ns);
+                        if (lane == 0) wait_bar_drain(bar(C::B_KFULL + ks), (G / NK) & 1, p.wait_limit_ns);
+                        __syncwarp();
                         break;
                     }
-                    mbar_arrive_expect_tx(bar(C::B_VFULL + vs), step_bytes);
-                    for (int q = 0; q < cnt; ++q) {
-                        const int vrow = static_cast<int>(bh * p.N) + js[q] * BS;
+                    if (elect_one()) {
+                        mbar_arrive_expect_tx(bar(C::B_VFULL + vs), step_bytes);
+                        for (int q = 0; q < cnt; ++q) {
+                            const int vrow = static_cast<int>(bh * p.N) + js[q] * BS;
 #pragma unroll
-                        for (int c = 0; c < D / 64; ++c)
-                            tma_load_2d(sbase + C::V_OFF + vs * C::kKVBytes + c * C::kKVChunk + q * BS * 128, &tmV,
-                                        c * 64, vrow, bar(C::B_VFULL + vs));
+                            for (int c = 0; c < D / 64; ++c)
+                                tma_load_2d(sbase + C::V_OFF + vs * C::kKVBytes + c * C::kKVChunk + q * BS * 128,
+                                            &tmV, c * 64, vrow, bar(C::B_VFULL + vs));
+                        }
                     }
+                    __syncwarp();
                     last_issue = G;
                     ++G;
                 } while ((cnt = walk.next_step<PAIR>(js, ms)) != 0);
                 ++e;
             }
-            if (*ctl.abort_flag) {
+            if (lane == 0 && *ctl.abort_flag) {
                 // never leave while our copies may still land in shared memory
                 for (int g = last_issue - (NK > NV ? NK : NV) + 1; g <= last_issue; ++g) {
                     if (g < 0) continue;
@@ -728,6 +746,7 @@ __global__ void __launch_bounds__((4 * SPLIT + 3) * 32, MINB)
                 for (int e2 = q_issued - (QS - 1) < 0 ? 0 : q_issued - (QS - 1); e2 <= q_issued; ++e2)
                     wait_bar_drain(bar(C::B_QFULL + e2 % QS), (e2 / QS) & 1, p.wait_limit_ns);
             }
+            __syncwarp();
         }
     } else if (warp == kQkWarp) {
         // ------------------------------------------------------------ QK^T issuer
