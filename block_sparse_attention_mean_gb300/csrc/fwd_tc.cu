@@ -255,7 +255,12 @@ __device__ __forceinline__ void softmax_rows(const TcParams &p, uint32_t sbase, 
             }
             continue;
         }
-        float m_run = -CUDART_INF_F, l_run = 0.0f, lp_run = 0.0f;
+        // running max; the row sums stay split over partial accumulators (packed fp32
+        // pairs for the fp32 sum, eight floats for the sum of bf16-rounded P) until
+        // the epilogue, and a rescale scales them all
+        float m_run = -CUDART_INF_F;
+        uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
+        float accp[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
         bool last;
         do {
             const int b = G % NSB;
@@ -297,16 +302,16 @@ __device__ __forceinline__ void softmax_rows(const TcParams &p, uint32_t sbase, 
                     m_run = m_tile;
                 } else if (m_tile > m_run + kRescaleLog2) {
                     alpha = ex2_approx(m_run - m_tile);
-                    l_run *= alpha;
-                    lp_run *= alpha;
+                    const uint64_t a2 = f2_pack(alpha, alpha);
+#pragma unroll
+                    for (int a = 0; a < 4; ++a) acc[a] = f2_fma(acc[a], a2, 0ull);
+#pragma unroll
+                    for (int a = 0; a < 8; ++a) accp[a] *= alpha;
                     m_run = m_tile;
                     resc = true;
                 }
                 const uint64_t c2x = f2_pack(p.scale_log2, p.scale_log2);
                 const uint64_t nm2 = f2_pack(-m_run, -m_run);
-                uint64_t acc[4], accp[4];
-#pragma unroll
-                for (int a = 0; a < 4; ++a) acc[a] = accp[a] = 0ull;
 #pragma unroll
                 for (int c = 0; c < NC; ++c) {
                     uint32_t pk[16];
@@ -320,8 +325,7 @@ __device__ __forceinline__ void softmax_rows(const TcParams &p, uint32_t sbase, 
                             const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
                             pk[q] = pack_bf16x2(p0, p1);
                             acc[q & 3] = f2_add(acc[q & 3], f2_pack(p0, p1));
-                            accp[q & 3] = f2_add(accp[q & 3], f2_pack(__uint_as_float(pk[q] << 16),
-                                                                      __uint_as_float(pk[q] & 0xFFFF0000u)));
+                            add_bf16x2_to_f32(accp[2 * (q & 3)], accp[2 * (q & 3) + 1], pk[q]);
                         }
                     } else {
 #pragma unroll
@@ -329,11 +333,6 @@ __device__ __forceinline__ void softmax_rows(const TcParams &p, uint32_t sbase, 
                     }
                     tmem_st16(tS + b * kStep + c * 16, pk);
                 }
-                float e0, e1, e2, e3;
-                f2_unpack(f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3])), e0, e1);
-                f2_unpack(f2_add(f2_add(accp[0], accp[1]), f2_add(accp[2], accp[3])), e2, e3);
-                l_run += e0 + e1;
-                lp_run += e2 + e3;
             } else {
                 uint32_t z[16];
 #pragma unroll
@@ -364,6 +363,10 @@ __device__ __forceinline__ void softmax_rows(const TcParams &p, uint32_t sbase, 
             ++G;
         } while (!last);
         // epilogue: O / l, LSE = ln2 * (m + log2 l)
+        float e0, e1;
+        f2_unpack(f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3])), e0, e1);
+        const float l_run = e0 + e1;
+        const float lp_run = ((accp[0] + accp[1]) + (accp[2] + accp[3])) + ((accp[4] + accp[5]) + (accp[6] + accp[7]));
         const int t = G - 1;
         if (!warp_wait_all(bar(C::B_PVDONE + t % NSB), (t / NSB) & 1, ctl)) return;
         tc_fence_after();
@@ -851,12 +854,14 @@ __global__ void __launch_bounds__((4 * SPLIT + 3) * 32, MINB)
                 bool first = true, last;
                 do {
                     const int b = G % NSB, s = G % NV;
+                    // V(G) normally landed long ago: test it first so that only the P wait
+                    // sits between the softmax's arrival and the MMAs
+                    if (!warp_wait_all(bar(C::B_VFULL + s), (G / NV) & 1, ctl)) { ok = false; break; }
                     // the descriptor was written by the QK^T issuer before S(G); P-full orders it after that write
                     if (!warp_wait_all(bar(C::B_PFULL + b), (G / NSB) & 1, ctl)) { ok = false; break; }
                     const uint32_t sd = desc[b];
                     const int cnt = desc_count(sd);
                     last = desc_last(sd);
-                    if (!warp_wait_all(bar(C::B_VFULL + s), (G / NV) & 1, ctl)) { ok = false; break; }
                     // the first PV of a tile overwrites O: the previous tile's epilogue must have read it
                     if (first && e >= 1 && !warp_wait_all(bar(C::B_OEMPTY), (e - 1) & 1, ctl)) { ok = false; break; }
                     tc_fence_after();

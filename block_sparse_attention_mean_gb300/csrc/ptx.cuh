@@ -339,6 +339,19 @@ __device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b)
 }
 
 // Two floats -> packed bf16x2 (round to nearest even); `lo` in the low half.
+// a0 += lo, a1 += hi for the two bf16 halves of w, in fp32 (the bf16 operand is
+// widened exactly, then added with round-to-nearest: the same result as
+// unpacking the halves and adding them as floats).
+__device__ __forceinline__ void add_bf16x2_to_f32(float &a0, float &a1, uint32_t w)
+{
+    asm("{\n\t.reg .b16 lo, hi;\n\t"
+        "mov.b32 {lo, hi}, %2;\n\t"
+        "add.rn.f32.bf16 %0, lo, %0;\n\t"
+        "add.rn.f32.bf16 %1, hi, %1;\n\t}"
+        : "+f"(a0), "+f"(a1)
+        : "r"(w));
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
 {
     uint32_t r;
