@@ -40,6 +40,10 @@ EXPORTS = ("bsa_build_mask", "bsa_forward", "bsa_mask_nnz", "bsa_workspace_size"
            "bsa_check_device_error", "bsa_validate_index", "bsa_debug_config",
            "bsa_status_string", "bsa_build_mask_noalloc")
 NOALLOC_SCRATCH_BYTES = 16 << 20  # BSA_NOALLOC_SCRATCH_BYTES
+# bsa_debug_config flag bits
+DBG_STALL = 1       # skip loads and MMAs: the first device wait runs out
+DBG_NO_SPLIT = 2    # never split a query tile over several CTAs
+DBG_SPLIT_ALL = 4   # split every tile with two or more steps (within the partial budget)
 
 
 class StaticSpec(ctypes.Structure):

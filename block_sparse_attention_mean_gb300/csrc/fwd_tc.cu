@@ -48,7 +48,20 @@ struct Roles {
 };
 constexpr int kTileM = 128;
 constexpr float kRescaleLog2 = 8.0f;
-constexpr uint32_t kDbgStall = 1u;
+constexpr uint32_t kDbgStall = 1u;     // skip loads and MMAs (the softmax's first wait runs out)
+constexpr uint32_t kDbgNoSplit = 2u;   // never split a query tile
+constexpr uint32_t kDbgSplitAll = 4u;  // split every tile with two or more steps (as the budget allows)
+
+// Work items (load balance, "多模态DiT中的块稀疏注意力" §5.3: rows with very different
+// active counts throttle a uniform launch). A query tile whose KV step count is
+// above the per-CTA share of all steps is split by KV block range into up to
+// kMaxChunks chunks; each chunk is one item and writes an unnormalised partial
+// O with its row max and sums, which the chunk that finishes last merges.
+constexpr int kMaxChunks = 8;
+constexpr int kMinChunkSteps = 4;
+constexpr int kMaxPartials = 640;    // partial-result slots per launch
+constexpr int kItemTileBits = 24;    // item = tile | chunk << 24 | (chunks - 1) << 27
+constexpr int kMergeWarps = 8;       // merge counters per split tile (one per softmax warp)
 
 struct TcParams {
     int N, nQB, nKB, W, tiles_per_bh, n_tiles;
@@ -59,12 +72,49 @@ struct TcParams {
     float scale_log2;
     __nv_bfloat16 *O;
     float *LSE;
-    const int32_t *tile_list;
+    const int32_t *tile_list;  // work items, longest first
+    const uint32_t *n_items;
     uint32_t *tile_counter;
     uint32_t *err;
     unsigned long long wait_limit_ns;
     uint32_t dbg;
+    int split_ok;              // items carry chunk fields (fewer than 2^24 tiles)
+    const int32_t *split_base; // per tile: first partial slot of a split tile, else -1
+    uint32_t *merge_cnt;       // per split tile and softmax warp: chunks finished
+    float *part_o;             // [slot][128][D] unnormalised partial O
+    float4 *part_stats;        // [slot][128] (row max in log2 units, fp32 sum, sum of bf16-rounded P, 0)
 };
+
+struct Item {
+    int tile, chunk, nchunk;
+};
+
+__device__ __forceinline__ Item decode_item(const TcParams &p, int v)
+{
+    Item it;
+    if (p.split_ok) {
+        it.tile = v & ((1 << kItemTileBits) - 1);
+        it.chunk = (v >> kItemTileBits) & 7;
+        it.nchunk = ((v >> (kItemTileBits + 3)) & 7) + 1;
+    } else {
+        it.tile = v;
+        it.chunk = 0;
+        it.nchunk = 1;
+    }
+    return it;
+}
+
+// KV blocks [j_lo, j_hi) of an item (the whole row for an unsplit tile)
+__device__ __forceinline__ void chunk_range(const TcParams &p, const Item &it, int &j_lo, int &j_hi)
+{
+    if (it.nchunk == 1) {
+        j_lo = 0;
+        j_hi = 0x7fffffff;
+        return;
+    }
+    j_lo = static_cast<int>(static_cast<long long>(it.chunk) * p.nKB / it.nchunk);
+    j_hi = static_cast<int>(static_cast<long long>(it.chunk + 1) * p.nKB / it.nchunk);
+}
 
 // One KV step = PAIR consecutive KV blocks of the walk (PAIR = 2 at block 64:
 // QK^T then runs as N = 128 MMAs). A K or V ring stage holds one step: per
@@ -175,14 +225,15 @@ __device__ __forceinline__ void tile_coords(const TcParams &p, int tile, int64_t
 }
 
 template <int BS>
-__device__ __forceinline__ void walk_init(TileWalk &w, const TcParams &p, int64_t bh, int qt)
+__device__ __forceinline__ void walk_init(TileWalk &w, const TcParams &p, int64_t bh, int qt, int j_lo = 0,
+                                          int j_hi = 0x7fffffff)
 {
     if (BS == 128) {
-        w.init(p.index_mode, p.row_ptr, p.col_idx, p.bitmap, p.W, bh * p.nQB + qt, -1, 3u);
+        w.init(p.index_mode, p.row_ptr, p.col_idx, p.bitmap, p.W, bh * p.nQB + qt, -1, 3u, j_lo, j_hi);
     } else {
         const int i0 = 2 * qt, i1 = 2 * qt + 1;
         w.init(p.index_mode, p.row_ptr, p.col_idx, p.bitmap, p.W, bh * p.nQB + i0,
-               i1 < p.nQB ? bh * p.nQB + i1 : -1, 0u);
+               i1 < p.nQB ? bh * p.nQB + i1 : -1, 0u, j_lo, j_hi);
     }
 }
 
@@ -215,6 +266,131 @@ __device__ __forceinline__ bool fetch_tile(uint32_t sbase, volatile int32_t *til
     return true;
 }
 
+// ---------------------------------------------------------------- split tiles
+//
+// The chunks of a split tile hold, per row, an unnormalised partial O_k (P V summed
+// over the chunk's KV blocks, P relative to the chunk's row max m_k) with the sums
+// l_k (fp32 P) and lp_k (bf16-rounded P). The merged row is
+//   O = sum_k w_k O_k / sum_k w_k lp_k,  LSE = ln2 (M + log2 sum_k w_k l_k),
+//   w_k = 2^(m_k - M), M = max_k m_k (m in log2 units),
+// the same quantities the unsplit loop forms, summed in another order. The chunk
+// that finishes last (per softmax warp, by an atomic count) merges; its loads
+// bypass L1 because other SMs wrote the partials.
+
+// Per-chunk weights of one row; returns M, L and LP.
+__device__ __forceinline__ void merge_weights(const TcParams &p, int base, int nchunk, int row, float (&w)[kMaxChunks],
+                                              float &M, float &L, float &LP)
+{
+    M = -CUDART_INF_F;
+#pragma unroll
+    for (int k = 0; k < kMaxChunks; ++k)
+        if (k < nchunk) M = fmaxf(M, __ldcg(&p.part_stats[static_cast<size_t>(base + k) * kTileM + row]).x);
+    L = 0.0f;
+    LP = 0.0f;
+#pragma unroll
+    for (int k = 0; k < kMaxChunks; ++k) {
+        w[k] = 0.0f;
+        if (k < nchunk) {
+            const float4 st = __ldcg(&p.part_stats[static_cast<size_t>(base + k) * kTileM + row]);
+            if (st.x != -CUDART_INF_F) {
+                w[k] = ex2_approx(st.x - M);
+                L += w[k] * st.y;
+                LP += w[k] * st.z;
+            }
+        }
+    }
+}
+
+// One thread merges its whole row (one-thread-per-row softmax). Out of line: it
+// runs once per split tile and warp, and inlined it would crowd the main loop's
+// registers.
+template <int D>
+__device__ __noinline__ void merge_row(const TcParams &p, int base, int nchunk, int trow, __nv_bfloat16 *orow,
+                                          float *lse)
+{
+    float w[kMaxChunks], M, L, LP;
+    merge_weights(p, base, nchunk, trow, w, M, L, LP);
+    const float inv = LP > 0.0f ? 1.0f / LP : 0.0f;
+#pragma unroll 1
+    for (int c = 0; c < D / 16; ++c) {
+        float a[16];
+#pragma unroll
+        for (int q = 0; q < 16; ++q) a[q] = 0.0f;
+#pragma unroll
+        for (int k = 0; k < kMaxChunks; ++k) {
+            if (k >= nchunk || w[k] == 0.0f) continue;
+            const float4 *src =
+                reinterpret_cast<const float4 *>(p.part_o + (static_cast<size_t>(base + k) * kTileM + trow) * D + c * 16);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const float4 v = __ldcg(src + q);
+                a[4 * q] += w[k] * v.x;
+                a[4 * q + 1] += w[k] * v.y;
+                a[4 * q + 2] += w[k] * v.z;
+                a[4 * q + 3] += w[k] * v.w;
+            }
+        }
+        uint32_t pk[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) pk[q] = pack_bf16x2(a[2 * q] * inv, a[2 * q + 1] * inv);
+        uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 16);
+        dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+    }
+    *lse = L > 0.0f ? (M + log2f(L)) * 0.69314718055994530942f : -CUDART_INF_F;
+}
+
+// A thread of the 4-lanes-per-row layout merges rows r and r + 8 at its column
+// pairs 8g + cpair (g < D / 8).
+template <int D>
+__device__ __noinline__ void merge_quad(const TcParams &p, int base, int nchunk, int r, int cpair, int lane,
+                                           bool lo_valid, bool hi_valid, uint32_t *o_lo, uint32_t *o_hi, float *lse_lo,
+                                           float *lse_hi)
+{
+    float wl[kMaxChunks], wh[kMaxChunks], Ml, Ll, LPl, Mh, Lh, LPh;
+    merge_weights(p, base, nchunk, r, wl, Ml, Ll, LPl);
+    merge_weights(p, base, nchunk, r + 8, wh, Mh, Lh, LPh);
+    const float il = LPl > 0.0f ? 1.0f / LPl : 0.0f, ih = LPh > 0.0f ? 1.0f / LPh : 0.0f;
+#pragma unroll 1
+    for (int g = 0; g < D / 8; ++g) {
+        float2 al = make_float2(0.0f, 0.0f), ah = make_float2(0.0f, 0.0f);
+#pragma unroll
+        for (int k = 0; k < kMaxChunks; ++k) {
+            if (k >= nchunk) continue;
+            const float *bk = p.part_o + static_cast<size_t>(base + k) * kTileM * D + 8 * g + cpair;
+            if (wl[k] != 0.0f) {
+                const float2 v = __ldcg(reinterpret_cast<const float2 *>(bk + static_cast<size_t>(r) * D));
+                al.x += wl[k] * v.x;
+                al.y += wl[k] * v.y;
+            }
+            if (wh[k] != 0.0f) {
+                const float2 v = __ldcg(reinterpret_cast<const float2 *>(bk + static_cast<size_t>(r + 8) * D));
+                ah.x += wh[k] * v.x;
+                ah.y += wh[k] * v.y;
+            }
+        }
+        if (lo_valid) o_lo[4 * g] = pack_bf16x2(al.x * il, al.y * il);
+        if (hi_valid) o_hi[4 * g] = pack_bf16x2(ah.x * ih, ah.y * ih);
+    }
+    if ((lane & 3) == 0) {
+        if (lo_valid) *lse_lo = Ll > 0.0f ? (Ml + log2f(Ll)) * 0.69314718055994530942f : -CUDART_INF_F;
+        if (hi_valid) *lse_hi = Lh > 0.0f ? (Mh + log2f(Lh)) * 0.69314718055994530942f : -CUDART_INF_F;
+    }
+}
+
+// Counts this warp's chunk as finished; true for the warp that finished last.
+__device__ __forceinline__ bool last_chunk(const TcParams &p, int base, int nchunk, int warp, int lane)
+{
+    __threadfence();
+    __syncwarp();
+    uint32_t done = 0u;
+    if (lane == 0) done = atomicAdd(p.merge_cnt + static_cast<size_t>(base) * kMergeWarps + warp, 1u);
+    done = __shfl_sync(0xffffffffu, done, 0);
+    const bool last = done == static_cast<uint32_t>(nchunk - 1);
+    if (last) __threadfence();
+    return last;
+}
+
 // SPLIT == 1: warp w (0-3) owns TMEM lanes 32w..32w+31; thread = one query row,
 // all kStep columns of S (32x32b TMEM accesses). A step holds PAIR KV blocks;
 // block q of the step occupies S columns [q * BS, (q + 1) * BS) and is skipped
@@ -241,12 +417,12 @@ __device__ __forceinline__ void softmax_rows(const TcParams &p, uint32_t sbase, 
         const bool empty = (tile & kEmptyTile) != 0;
         int64_t bh;
         int qt;
-        tile_coords(p, tile & ~kEmptyTile, bh, qt);
+        tile_coords(p, decode_item(p, tile & ~kEmptyTile).tile, bh, qt);
         const int row = qt * kTileM + trow;
         const bool row_valid = row < p.N;
         const int64_t grow = bh * p.N + row;
         __nv_bfloat16 *orow = p.O + grow * D;
-        if (empty) {
+        if (empty && decode_item(p, tile & ~kEmptyTile).nchunk == 1) {
             if (row_valid) {
                 const uint4 z = make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
@@ -261,8 +437,8 @@ __device__ __forceinline__ void softmax_rows(const TcParams &p, uint32_t sbase, 
         float m_run = -CUDART_INF_F;
         uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
         float accp[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
-        bool last;
-        do {
+        bool last = empty;  // an empty chunk of a split tile has no step
+        while (!last) {
             const int b = G % NSB;
             const uint32_t sd = warp_wait_step(bar(C::B_SFULL + b), (G / NSB) & 1, ctl, desc + b);
             if (sd == 0xFFFFFFFFu) return;
@@ -361,12 +537,44 @@ __device__ __forceinline__ void softmax_rows(const TcParams &p, uint32_t sbase, 
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(C::B_PFULL + b));
             ++G;
-        } while (!last);
-        // epilogue: O / l, LSE = ln2 * (m + log2 l)
+        }
         float e0, e1;
         f2_unpack(f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3])), e0, e1);
         const float l_run = e0 + e1;
         const float lp_run = ((accp[0] + accp[1]) + (accp[2] + accp[3])) + ((accp[4] + accp[5]) + (accp[6] + accp[7]));
+        const Item it = decode_item(p, tile & ~kEmptyTile);  // decoded again: not live across the loop
+        if (it.nchunk > 1) {
+            // chunk of a split tile: unnormalised partial O and the row's (m, l, lp)
+            const int base = p.split_base[it.tile];
+            const size_t prow = static_cast<size_t>(base + it.chunk) * kTileM + trow;
+            float4 *po = reinterpret_cast<float4 *>(p.part_o + prow * D);
+            if (!empty) {
+                const int t = G - 1;
+                if (!warp_wait_all(bar(C::B_PVDONE + t % NSB), (t / NSB) & 1, ctl)) return;
+                tc_fence_after();
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t ov[32];
+                    tmem_ld32(tO + c * 32, ov);
+                    tmem_wait_ld();
+                    reg_fence32(ov);
+#pragma unroll
+                    for (int q = 0; q < 8; ++q)
+                        po[c * 8 + q] = make_float4(__uint_as_float(ov[4 * q]), __uint_as_float(ov[4 * q + 1]),
+                                                    __uint_as_float(ov[4 * q + 2]), __uint_as_float(ov[4 * q + 3]));
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(C::B_OEMPTY));
+            } else {
+#pragma unroll
+                for (int q = 0; q < D / 4; ++q) po[q] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            }
+            p.part_stats[prow] = make_float4(m_run, l_run, lp_run, 0.0f);
+            if (last_chunk(p, base, it.nchunk, warp, lane) && row_valid) merge_row<D>(p, base, it.nchunk, trow, orow, p.LSE + grow);
+            continue;
+        }
+        // epilogue: O / l, LSE = ln2 * (m + log2 l)
         const int t = G - 1;
         if (!warp_wait_all(bar(C::B_PVDONE + t % NSB), (t / NSB) & 1, ctl)) return;
         tc_fence_after();
@@ -418,15 +626,16 @@ __device__ __forceinline__ void softmax_quads(const TcParams &p, uint32_t sbase,
         int tile;
         if (!fetch_tile<C>(sbase, tile_ids, ctl, lane, tcount, tile) || tile < 0) return;
         const bool empty = (tile & kEmptyTile) != 0;
+        const Item it = decode_item(p, tile & ~kEmptyTile);
         int64_t bh;
         int qt;
-        tile_coords(p, tile & ~kEmptyTile, bh, qt);
+        tile_coords(p, it.tile, bh, qt);
         const int row_lo = qt * kTileM + r_lo, row_hi = row_lo + 8;
         const bool lo_valid = row_lo < p.N, hi_valid = row_hi < p.N;
         const int64_t g_lo = bh * p.N + row_lo, g_hi = g_lo + 8;
         uint32_t *o_lo = reinterpret_cast<uint32_t *>(p.O + g_lo * D + cpair);
         uint32_t *o_hi = reinterpret_cast<uint32_t *>(p.O + g_hi * D + cpair);
-        if (empty) {
+        if (empty && it.nchunk == 1) {
 #pragma unroll
             for (int g = 0; g < RO; ++g) {
                 if (lo_valid) o_lo[4 * g] = 0u;
@@ -440,8 +649,8 @@ __device__ __forceinline__ void softmax_quads(const TcParams &p, uint32_t sbase,
         }
         float m_lo = -CUDART_INF_F, m_hi = -CUDART_INF_F;
         float l_lo = 0.0f, l_hi = 0.0f, lp_lo = 0.0f, lp_hi = 0.0f;  // this thread's columns only
-        bool last;
-        do {
+        bool last = empty;  // an empty chunk of a split tile has no step
+        while (!last) {
             const int b = G % NSB;
             const uint32_t sd = warp_wait_step(bar(C::B_SFULL + b), (G / NSB) & 1, ctl, desc + b);
             if (sd == 0xFFFFFFFFu) return;
@@ -548,7 +757,7 @@ __device__ __forceinline__ void softmax_quads(const TcParams &p, uint32_t sbase,
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(C::B_PFULL + b));
             ++G;
-        } while (!last);
+        }
         // epilogue: whole-row sums over the 4 lanes of each row, then O / l and LSE
 #pragma unroll
         for (int o = 1; o <= 2; o <<= 1) {
@@ -556,6 +765,46 @@ __device__ __forceinline__ void softmax_quads(const TcParams &p, uint32_t sbase,
             l_hi += __shfl_xor_sync(0xffffffffu, l_hi, o);
             lp_lo += __shfl_xor_sync(0xffffffffu, lp_lo, o);
             lp_hi += __shfl_xor_sync(0xffffffffu, lp_hi, o);
+        }
+        if (it.nchunk > 1) {
+            // chunk of a split tile: unnormalised partial O and the rows' (m, l, lp)
+            const int base = p.split_base[it.tile];
+            const size_t srow = static_cast<size_t>(base + it.chunk) * kTileM;
+            float *po_lo = p.part_o + (srow + r_lo) * D + cpair;
+            float *po_hi = p.part_o + (srow + r_lo + 8) * D + cpair;
+            if (!empty) {
+                const int t = G - 1;
+                if (!warp_wait_all(bar(C::B_PVDONE + t % NSB), (t / NSB) & 1, ctl)) return;
+                tc_fence_after();
+                uint32_t ov[4 * RO];
+                tmem_ld_16x256b<RO>(tO, ov);
+                tmem_wait_ld();
+                reg_fence(ov);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(C::B_OEMPTY));
+#pragma unroll
+                for (int g = 0; g < RO; ++g) {
+                    *reinterpret_cast<float2 *>(po_lo + 8 * g) =
+                        make_float2(__uint_as_float(ov[4 * g]), __uint_as_float(ov[4 * g + 1]));
+                    *reinterpret_cast<float2 *>(po_hi + 8 * g) =
+                        make_float2(__uint_as_float(ov[4 * g + 2]), __uint_as_float(ov[4 * g + 3]));
+                }
+            } else {
+#pragma unroll
+                for (int g = 0; g < RO; ++g) {
+                    *reinterpret_cast<float2 *>(po_lo + 8 * g) = make_float2(0.0f, 0.0f);
+                    *reinterpret_cast<float2 *>(po_hi + 8 * g) = make_float2(0.0f, 0.0f);
+                }
+            }
+            if ((lane & 3) == 0) {
+                p.part_stats[srow + r_lo] = make_float4(m_lo, l_lo, lp_lo, 0.0f);
+                p.part_stats[srow + r_lo + 8] = make_float4(m_hi, l_hi, lp_hi, 0.0f);
+            }
+            if (last_chunk(p, base, it.nchunk, warp, lane))
+                merge_quad<D>(p, base, it.nchunk, r_lo, cpair, lane, lo_valid, hi_valid, o_lo, o_hi, p.LSE + g_lo,
+                              p.LSE + g_hi);
+            continue;
         }
         const int t = G - 1;
         if (!warp_wait_all(bar(C::B_PVDONE + t % NSB), (t / NSB) & 1, ctl)) return;
@@ -654,32 +903,36 @@ __global__ void __launch_bounds__((4 * SPLIT + 3) * 32, MINB)
             int last_issue = -1;  // last iteration whose K and V loads were issued
             int q_issued = -1;
             bool ok = true;
+            const uint32_t n_items = *p.n_items;  // written by the tile-order launch before this one
             while (ok) {
                 const int slot = tcount & 1;
                 if (tcount >= 2 && !warp_wait_all(bar(C::B_TEMPTY + slot), ((tcount >> 1) - 1) & 1, ctl)) break;
-                int tile = -1;
+                int item = -1;
                 if (lane == 0) {
                     const uint32_t id = atomicAdd(p.tile_counter, 1u);
-                    tile = id < static_cast<uint32_t>(p.n_tiles) ? p.tile_list[id] : -1;
+                    item = id < n_items ? p.tile_list[id] : -1;
                 }
-                tile = __shfl_sync(0xffffffffu, tile, 0);
+                item = __shfl_sync(0xffffffffu, item, 0);
                 int64_t bh = 0;
                 int qt = 0;
                 TileWalk walk;
                 int js[2];
                 uint32_t ms[2];
                 int cnt = 0;
-                if (tile >= 0) {
-                    tile_coords(p, tile, bh, qt);
-                    walk_init<BS>(walk, p, bh, qt);
+                if (item >= 0) {
+                    const Item it = decode_item(p, item);
+                    int j_lo, j_hi;
+                    chunk_range(p, it, j_lo, j_hi);
+                    tile_coords(p, it.tile, bh, qt);
+                    walk_init<BS>(walk, p, bh, qt, j_lo, j_hi);
                     cnt = walk.next_step<PAIR>(js, ms);
                 }
                 if (lane == 0) {
-                    tile_ids[slot] = tile >= 0 && cnt == 0 ? (tile | kEmptyTile) : tile;
+                    tile_ids[slot] = item >= 0 && cnt == 0 ? (item | kEmptyTile) : item;
                     mbar_arrive(bar(C::B_TFULL + slot));
                 }
                 ++tcount;
-                if (tile < 0) break;
+                if (item < 0) break;
                 if (stall || cnt == 0) continue;  // empty tile: nothing to load
                 const int qs = e % QS;  // Q slot; it was last used by tile e - QS
                 if (e >= QS && !warp_wait_all(bar(C::B_QEMPTY + qs), ((e / QS) - 1) & 1, ctl)) break;
@@ -772,11 +1025,14 @@ __global__ void __launch_bounds__((4 * SPLIT + 3) * 32, MINB)
                 ++tcount;
                 if (tile < 0) break;
                 if (tile & kEmptyTile) continue;
+                const Item it = decode_item(p, tile);
+                int j_lo, j_hi;
+                chunk_range(p, it, j_lo, j_hi);
                 int64_t bh;
                 int qt;
-                tile_coords(p, tile, bh, qt);
+                tile_coords(p, it.tile, bh, qt);
                 TileWalk walk;
-                walk_init<BS>(walk, p, bh, qt);
+                walk_init<BS>(walk, p, bh, qt, j_lo, j_hi);
                 // one step of lookahead: a step's descriptor says whether it is the tile's last
                 int js[2], jn[2];
                 uint32_t ms[2], mn[2];
@@ -914,6 +1170,8 @@ __global__ void __launch_bounds__((4 * SPLIT + 3) * 32, MINB)
 
 constexpr int kBuckets = 1024;
 
+// Length of a tile for ordering and splitting: the sum of its Q blocks' row
+// lengths (an upper bound of the union's step count at block size 64).
 __device__ __forceinline__ int tile_length(const TcParams &p, int tile, int BS)
 {
     const int64_t bh = tile / p.tiles_per_bh;
@@ -933,32 +1191,11 @@ __device__ __forceinline__ int tile_length(const TcParams &p, int tile, int BS)
     return len;
 }
 
-// Longest-first tile list (counting sort by active-block count, clamped) and
-// reset of the scheduler counter, in one launch: every CTA computes the lengths
-// of its 1024 tiles; the CTA that finishes last sorts them.
-__global__ void __launch_bounds__(1024) tile_order_kernel(TcParams p, int BS, int32_t *tile_list, int32_t *lens,
-                                                          uint32_t *done)
+// Exclusive prefix of v over the 1024 threads of the block, and the block total.
+__device__ __forceinline__ int block_scan_excl(int v, int &total, int *wsum)
 {
-    __shared__ int hist[kBuckets];
-    __shared__ int wsum[32];
-    __shared__ bool is_last;
-    const int t = threadIdx.x;
-    const int tile0 = blockIdx.x * 1024 + t;
-    if (tile0 < p.n_tiles) lens[tile0] = min(tile_length(p, tile0, BS), kBuckets - 1);
-    __threadfence();
-    __syncthreads();
-    if (t == 0) is_last = atomicAdd(done, 1u) == gridDim.x - 1;
-    __syncthreads();
-    if (!is_last) return;
-    __threadfence();
-    for (int b = t; b < kBuckets; b += 1024) hist[b] = 0;
-    __syncthreads();
-    for (int tile = t; tile < p.n_tiles; tile += 1024) atomicAdd(&hist[kBuckets - 1 - __ldcg(lens + tile)], 1);
-    __syncthreads();
-    // exclusive scan of hist (one bucket per thread)
-    const int v = hist[t];
+    const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
     int x = v;
-    const int lane = t & 31, warp = t >> 5;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
         const int y = __shfl_up_sync(0xffffffffu, x, o);
@@ -976,17 +1213,251 @@ __global__ void __launch_bounds__(1024) tile_order_kernel(TcParams p, int BS, in
         wsum[lane] = s2;
     }
     __syncthreads();
+    total = wsum[31];
     const int excl = x - v + (warp > 0 ? wsum[warp - 1] : 0);
+    __syncthreads();  // wsum is reused by the next call
+    return excl;
+}
+
+// Chunks of a tile of `len` steps: a tile is split only when it is well above the
+// per-CTA share (a chunk costs a Q load, a partial write and a merge).
+__device__ __forceinline__ bool splits(int len, int share) { return len > share + share / 2; }
+
+__device__ __forceinline__ int n_chunks(int len, int share, uint32_t dbg)
+{
+    if (dbg & kDbgSplitAll) return len >= 2 ? (len < kMaxChunks ? len : kMaxChunks) : 1;
+    if (!splits(len, share)) return 1;
+    const int n = (len + share - 1) / share;
+    return n < kMaxChunks ? n : kMaxChunks;
+}
+
+__device__ __forceinline__ int length_bucket(int len)
+{
+    return kBuckets - 1 - (len < kBuckets - 1 ? len : kBuckets - 1);
+}
+
+// Reserves n consecutive slots of bucket bk (n = 0: none), returning the first.
+// Lanes of a warp whose tile is whole (n == 1) and shares the bucket take their
+// slots with one atomic (top-k masks give every tile the same length: per-lane
+// atomics on one shared address would serialise). Called by all 32 lanes.
+__device__ __forceinline__ int reserve_slots(int *hist, int bk, int n)
+{
+    const int lane = threadIdx.x & 31;
+    const unsigned key = n == 1 ? static_cast<unsigned>(bk) : (n == 0 ? 0xfffffffeu : (0x80000000u | lane));
+    const unsigned grp = __match_any_sync(0xffffffffu, key);
+    const int leader = __ffs(grp) - 1;
+    int base = 0;
+    if (lane == leader && n > 0) base = atomicAdd(&hist[bk], n == 1 ? __popc(grp) : n);
+    base = __shfl_sync(0xffffffffu, base, leader);
+    return base + (n == 1 ? __popc(grp & ((1u << lane) - 1u)) : 0);
+}
+
+struct OrderArgs {
+    int BS, grid, budget;
+    int32_t *items, *lens, *split_base;
+    uint32_t *merge_cnt;
+    WsHeader *hdr;
+};
+
+// Work list for one forward launch, in one launch: every CTA computes the step
+// counts of its 1024 tiles; the CTA that finishes last splits the tiles well above
+// the per-CTA share (partial slots in tile order, within the budget; skipped when
+// even the longest tile is not), then sorts the items longest first (counting sort
+// on item length, clamped) and resets the scheduler counter.
+__global__ void __launch_bounds__(1024) tile_order_kernel(TcParams p, OrderArgs o)
+{
+    __shared__ int hist[kBuckets];
+    __shared__ int wsum[32];
+    __shared__ bool is_last;
+    const int t = threadIdx.x;
+    const int tile0 = blockIdx.x * 1024 + t;
+    int len = 0;
+    if (tile0 < p.n_tiles) {
+        len = tile_length(p, tile0, o.BS);
+        o.lens[tile0] = len;
+    }
+    // block sum and max of the lengths, then one atomic each
+    {
+        const unsigned wsum_l = __reduce_add_sync(0xffffffffu, static_cast<unsigned>(len));
+        const unsigned wmax_l = __reduce_max_sync(0xffffffffu, static_cast<unsigned>(len));
+        if ((t & 31) == 0) {
+            wsum[t >> 5] = static_cast<int>(wsum_l);
+            hist[t >> 5] = static_cast<int>(wmax_l);
+        }
+        __syncthreads();
+        if (t < 32) {
+            const unsigned bs = __reduce_add_sync(0xffffffffu, static_cast<unsigned>(wsum[t]));
+            const unsigned bm = __reduce_max_sync(0xffffffffu, static_cast<unsigned>(hist[t]));
+            if (t == 0) {
+                atomicAdd(&o.hdr->total_steps, static_cast<unsigned long long>(bs));
+                atomicMax(&o.hdr->max_len, bm);
+            }
+        }
+    }
+    __threadfence();
     __syncthreads();
+    if (t == 0) is_last = atomicAdd(&o.hdr->order_done, 1u) == gridDim.x - 1;
+    __syncthreads();
+    if (!is_last) return;
+    __threadfence();
+    const unsigned long long total = atomicAdd(&o.hdr->total_steps, 0ull);
+    unsigned long long share = (total + o.grid - 1) / o.grid;
+    if (share < kMinChunkSteps) share = kMinChunkSteps;
+    if (share > 0x7fffffffull) share = 0x7fffffffull;
+    const int T = static_cast<int>(share);
+    const int max_len = static_cast<int>(atomicMax(&o.hdr->max_len, 0u));
+    const bool can_split = p.split_ok && o.budget > 0 && !(p.dbg & kDbgNoSplit) &&
+                           ((p.dbg & kDbgSplitAll) || splits(max_len, T));
+    // split decisions: partial slots are handed out in tile order while the budget lasts
+    int carry = 0;
+    for (int b0 = 0; can_split && b0 < p.n_tiles; b0 += 1024) {
+        const int tile = b0 + t;
+        const int n0 = can_split && tile < p.n_tiles ? n_chunks(__ldcg(o.lens + tile), T, p.dbg) : 1;
+        const int want = n0 > 1 ? n0 : 0;
+        int step_total;
+        const int excl = carry + block_scan_excl(want, step_total, wsum);
+        if (tile < p.n_tiles) {
+            const bool fits = want > 0 && excl + want <= o.budget;
+            o.split_base[tile] = fits ? excl : -1;
+            if (fits)
+                for (int w = 0; w < kMergeWarps; ++w) o.merge_cnt[static_cast<size_t>(excl) * kMergeWarps + w] = 0u;
+        }
+        carry += step_total;
+    }
+    __syncthreads();
+    // histogram of item lengths, longest first
+    for (int bk = t; bk < kBuckets; bk += 1024) hist[bk] = 0;
+    __syncthreads();
+    for (int b0 = 0; b0 < p.n_tiles; b0 += 1024) {
+        const int tile = b0 + t;
+        int n = 0, bk = 0;
+        if (tile < p.n_tiles) {
+            const int L = __ldcg(o.lens + tile);
+            n = can_split && o.split_base[tile] >= 0 ? n_chunks(L, T, p.dbg) : 1;
+            bk = length_bucket((L + n - 1) / n);
+        }
+        (void)reserve_slots(hist, bk, n);
+    }
+    __syncthreads();
+    int n_items;
+    const int excl = block_scan_excl(hist[t], n_items, wsum);
     hist[t] = excl;
     __syncthreads();
-    for (int tile = t; tile < p.n_tiles; tile += 1024) {
-        const int pos = atomicAdd(&hist[kBuckets - 1 - __ldcg(lens + tile)], 1);
-        tile_list[pos] = tile;
+    for (int b0 = 0; b0 < p.n_tiles; b0 += 1024) {
+        const int tile = b0 + t;
+        int n = 0, bk = 0;
+        if (tile < p.n_tiles) {
+            const int L = __ldcg(o.lens + tile);
+            n = can_split && o.split_base[tile] >= 0 ? n_chunks(L, T, p.dbg) : 1;
+            bk = length_bucket((L + n - 1) / n);
+        }
+        const int pos = reserve_slots(hist, bk, n);
+        for (int c = 0; c < n; ++c) o.items[pos + c] = tile | (c << kItemTileBits) | ((n - 1) << (kItemTileBits + 3));
     }
     if (t == 0) {
+        o.hdr->n_items = static_cast<uint32_t>(n_items);
+        o.hdr->chunk_steps = static_cast<uint32_t>(T);
+        o.hdr->total_steps = 0ull;
+        o.hdr->max_len = 0u;
         *p.tile_counter = 0u;
-        *done = 0u;
+        o.hdr->order_done = 0u;
+    }
+}
+
+// The same work list from one CTA for a CSR index whose tiles fit its registers
+// (up to kOrderPerThread per thread): no length array, no election between CTAs.
+// A tile's Q blocks are consecutive index rows, so its length is one difference
+// of row_ptr; all the loads are issued before any is used.
+constexpr int kOrderPerThread = 8;
+
+__global__ void __launch_bounds__(1024) tile_order_small_kernel(TcParams p, OrderArgs o)
+{
+    __shared__ int hist[kBuckets];
+    __shared__ int wsum[32];
+    __shared__ unsigned red[64];
+    const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+    int L[kOrderPerThread], lo[kOrderPerThread], hi[kOrderPerThread];
+#pragma unroll
+    for (int k = 0; k < kOrderPerThread; ++k) {
+        const int tile = k * 1024 + t;
+        lo[k] = hi[k] = 0;
+        if (tile < p.n_tiles) {
+            const int64_t bh = tile / p.tiles_per_bh;
+            const int qt = tile % p.tiles_per_bh;
+            const int i0 = o.BS == 128 ? qt : 2 * qt;
+            const int nrows = o.BS == 128 || i0 + 1 >= p.nQB ? 1 : 2;
+            lo[k] = __ldg(p.row_ptr + bh * p.nQB + i0);
+            hi[k] = __ldg(p.row_ptr + bh * p.nQB + i0 + nrows);
+        }
+    }
+    unsigned sum = 0u, mx = 0u;
+#pragma unroll
+    for (int k = 0; k < kOrderPerThread; ++k) {
+        L[k] = hi[k] - lo[k];
+        sum += static_cast<unsigned>(L[k]);
+        mx = max(mx, static_cast<unsigned>(L[k]));
+    }
+    sum = __reduce_add_sync(0xffffffffu, sum);
+    mx = __reduce_max_sync(0xffffffffu, mx);
+    if (lane == 0) {
+        red[warp] = sum;
+        red[32 + warp] = mx;
+    }
+    for (int b = t; b < kBuckets; b += 1024) hist[b] = 0;
+    __syncthreads();
+    const unsigned total = __reduce_add_sync(0xffffffffu, red[lane]);
+    const unsigned max_len = __reduce_max_sync(0xffffffffu, red[32 + lane]);
+    unsigned share = (total + o.grid - 1) / o.grid;
+    if (share < kMinChunkSteps) share = kMinChunkSteps;
+    const int T = static_cast<int>(share < 0x7fffffffu ? share : 0x7fffffffu);
+    const bool can_split = p.split_ok && o.budget > 0 && !(p.dbg & kDbgNoSplit) &&
+                           ((p.dbg & kDbgSplitAll) || splits(static_cast<int>(max_len), T));
+    int n[kOrderPerThread];
+#pragma unroll
+    for (int k = 0; k < kOrderPerThread; ++k) n[k] = 1;
+    if (can_split) {
+        int carry = 0;
+#pragma unroll
+        for (int k = 0; k < kOrderPerThread; ++k) {
+            const int tile = k * 1024 + t;
+            const int n0 = tile < p.n_tiles ? n_chunks(L[k], T, p.dbg) : 1;
+            const int want = n0 > 1 ? n0 : 0;
+            int step_total;
+            const int excl = carry + block_scan_excl(want, step_total, wsum);
+            if (tile < p.n_tiles) {
+                const bool fits = want > 0 && excl + want <= o.budget;
+                o.split_base[tile] = fits ? excl : -1;
+                if (fits) {
+                    n[k] = n0;
+                    for (int w = 0; w < kMergeWarps; ++w) o.merge_cnt[static_cast<size_t>(excl) * kMergeWarps + w] = 0u;
+                }
+            }
+            carry += step_total;
+        }
+    }
+#pragma unroll
+    for (int k = 0; k < kOrderPerThread; ++k) {
+        const bool valid = k * 1024 + t < p.n_tiles;
+        (void)reserve_slots(hist, length_bucket((L[k] + n[k] - 1) / n[k]), valid ? n[k] : 0);
+    }
+    __syncthreads();
+    int n_items;
+    const int excl = block_scan_excl(hist[t], n_items, wsum);
+    hist[t] = excl;
+    __syncthreads();
+#pragma unroll
+    for (int k = 0; k < kOrderPerThread; ++k) {
+        const int tile = k * 1024 + t;
+        const bool valid = tile < p.n_tiles;
+        const int pos = reserve_slots(hist, length_bucket((L[k] + n[k] - 1) / n[k]), valid ? n[k] : 0);
+        if (valid)
+            for (int c = 0; c < n[k]; ++c)
+                o.items[pos + c] = tile | (c << kItemTileBits) | ((n[k] - 1) << (kItemTileBits + 3));
+    }
+    if (t == 0) {
+        o.hdr->n_items = static_cast<uint32_t>(n_items);
+        o.hdr->chunk_steps = static_cast<uint32_t>(T);
+        *p.tile_counter = 0u;
     }
 }
 
@@ -1022,6 +1493,37 @@ bool make_map(CUtensorMap *m, const void *base, uint64_t rows, int d, int box_ro
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, es,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Forward workspace: header, item list, per-tile lengths and partial slots, merge
+// counters, then the partial results of split tiles (all 256-byte aligned).
+struct FwdLayout {
+    size_t tiles, budget, items, lens, split_base, merge_cnt, part_stats, part_o, bytes;
+};
+
+FwdLayout fwd_layout(int B, int H, int N, int d)
+{
+    FwdLayout l{};
+    l.tiles = static_cast<size_t>(B) * H * ((N + kTileM - 1) / kTileM);
+    // split tiles need item ids with chunk fields; partial slots: at most 8 per tile
+    l.budget = l.tiles < (size_t(1) << kItemTileBits)
+                   ? (l.tiles * kMaxChunks < size_t(kMaxPartials) ? l.tiles * kMaxChunks : size_t(kMaxPartials))
+                   : 0;
+    size_t off = kWsHeader;
+    l.items = off;
+    off += align_up((l.tiles + l.budget) * sizeof(int32_t), 256);
+    l.lens = off;
+    off += align_up(l.tiles * sizeof(int32_t), 256);
+    l.split_base = off;
+    off += align_up(l.tiles * sizeof(int32_t), 256);
+    l.merge_cnt = off;
+    off += align_up(l.budget * kMergeWarps * sizeof(uint32_t), 256);
+    l.part_stats = off;
+    off += align_up(l.budget * kTileM * sizeof(float4), 256);
+    l.part_o = off;
+    off += align_up(l.budget * kTileM * static_cast<size_t>(d) * sizeof(float), 256);
+    l.bytes = off;
+    return l;
 }
 
 template <int D, int BS, int NK, int NV, int NSB, int QS, int SPLIT, int PAIR, int MINB>
@@ -1077,15 +1579,34 @@ bsa_status launch_tc(const FwdArgs &a, cudaStream_t st)
     p.scale_log2 = a.scale * 1.4426950408889634f;
     p.O = static_cast<__nv_bfloat16 *>(a.O);
     p.LSE = a.LSE;
-    int32_t *tile_list = reinterpret_cast<int32_t *>(a.ws + kWsHeader);
-    int32_t *lens = tile_list + align_up(static_cast<size_t>(p.n_tiles), 64);
-    p.tile_list = tile_list;
+    const FwdLayout lay = fwd_layout(a.B, a.H, a.N, a.d);
+    OrderArgs o{};
+    o.BS = BS;
+    o.budget = static_cast<int>(lay.budget);
+    o.items = reinterpret_cast<int32_t *>(a.ws + lay.items);
+    o.lens = reinterpret_cast<int32_t *>(a.ws + lay.lens);
+    o.split_base = reinterpret_cast<int32_t *>(a.ws + lay.split_base);
+    o.merge_cnt = reinterpret_cast<uint32_t *>(a.ws + lay.merge_cnt);
+    o.hdr = hdr;
+    p.tile_list = o.items;
+    p.n_items = &hdr->n_items;
+    p.split_ok = lay.budget > 0 ? 1 : 0;
+    p.split_base = o.split_base;
+    p.merge_cnt = o.merge_cnt;
+    p.part_stats = reinterpret_cast<float4 *>(a.ws + lay.part_stats);
+    p.part_o = reinterpret_cast<float *>(a.ws + lay.part_o);
     p.tile_counter = &hdr->tile_counter;
     p.err = &hdr->err;
     p.wait_limit_ns = a.wait_limit_ns;
     p.dbg = a.dbg_flags;
-    tile_order_kernel<<<(p.n_tiles + 1023) / 1024, 1024, 0, st>>>(p, BS, tile_list, lens, &hdr->order_done);
-    const int grid = static_cast<int>(p.n_tiles < grid_cap ? p.n_tiles : grid_cap);
+    // persistent CTAs; with splitting on, the item count is only known on the device
+    const int64_t max_items = static_cast<int64_t>(p.n_tiles) + static_cast<int64_t>(lay.budget);
+    const int grid = static_cast<int>(max_items < grid_cap ? max_items : grid_cap);
+    o.grid = grid;
+    if (p.index_mode == 0 && p.n_tiles <= 1024 * kOrderPerThread)
+        tile_order_small_kernel<<<1, 1024, 0, st>>>(p, o);
+    else
+        tile_order_kernel<<<(p.n_tiles + 1023) / 1024, 1024, 0, st>>>(p, o);
     kern<<<grid, kThreads, C::SMEM_ALLOC, st>>>(mq, mk, mv, p);
     return cudaGetLastError() == cudaSuccess ? BSA_OK : BSA_ERR_CUDA;
 }
@@ -1094,11 +1615,8 @@ bsa_status launch_tc(const FwdArgs &a, cudaStream_t st)
 
 size_t fwd_workspace_bytes(int B, int H, int N, int d, int block)
 {
-    (void)d;
     (void)block;
-    const size_t tiles = static_cast<size_t>(B) * H * ((N + kTileM - 1) / kTileM);
-    // tile list, then per-tile lengths
-    return kWsHeader + align_up(align_up(tiles, 64) * sizeof(int32_t) + tiles * sizeof(int32_t), 256);
+    return fwd_layout(B, H, N, d).bytes;
 }
 
 bsa_status launch_forward_tc(const FwdArgs &a, cudaStream_t st)

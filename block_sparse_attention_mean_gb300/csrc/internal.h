@@ -15,8 +15,13 @@ struct WsHeader {
     uint32_t err;          // first device-raised bsa_status (0 = none)
     uint32_t tile_counter; // forward: dynamic tile scheduler counter
     uint32_t order_done;   // CTAs of a last-CTA-finishes launch that are done (tile order, static pattern)
-    uint32_t pad[61];
+    uint32_t n_items;      // forward: work items (query tiles or chunks of them) in the item list
+    unsigned long long total_steps;  // forward: sum of the tiles' KV steps (tile order, then cleared)
+    uint32_t chunk_steps;  // forward: the per-CTA share of steps (chunk length of split tiles)
+    uint32_t max_len;      // forward: longest tile (tile order, then cleared)
+    uint32_t pad[56];
 };
+static_assert(sizeof(WsHeader) == 256, "workspace header size");
 static_assert(sizeof(WsHeader) == 256, "workspace header is 256 bytes");
 
 constexpr size_t kWsHeader = 256;

@@ -197,8 +197,11 @@ bsa_status bsa_validate_index(int B, int H, int N, int block, const int32_t *row
 
 /* Diagnostics for tests: `flags` bit 0 makes the next bsa_forward launches skip
  * their loads and MMAs so the softmax warps' first wait runs out (nothing is in
- * flight); `wait_limit_ns` bounds every device wait (0 restores the default of
- * 2 s). Host-global; not thread safe. */
+ * flight); bit 1 keeps every query tile whole and bit 2 splits every tile with two
+ * or more KV steps over several CTAs (as far as the workspace's partial slots
+ * allow), overriding the load-balance rule that splits only tiles above the
+ * per-CTA share of steps; `wait_limit_ns` bounds every device wait (0 restores
+ * the default of 2 s). Host-global; not thread safe. */
 bsa_status bsa_debug_config(uint32_t flags, uint64_t wait_limit_ns);
 
 /* Static string for a status code. */

@@ -76,6 +76,73 @@ def test_video_small_grid_all_rows():
     run_workload(w)
 
 
+# ------------------------------------------------------------ split query tiles
+#
+# A tile whose step count is well above the per-CTA share is split by KV block
+# range into chunks that separate CTAs run; the last to finish merges the partial
+# (O, max, sums). The debug flags force the split for every tile (with empty
+# chunks, ragged ranges and many merges) or forbid it; both must match the oracle.
+
+SPLIT_CASES = {
+    "t2i": wl.scaled(wl.WORKLOADS["t2i_static"], B=1, H=2),
+    "dynamic": wl.scaled(wl.WORKLOADS["dynamic_topk"], H=2, N=2048),
+    "video": wl.scaled(wl.WORKLOADS["video_cuboid"], H=2, N=256 + 8 * 16 * 16, grid=(2, 4, 4),
+                       video_shape=(8, 16, 16)),
+    # block 128, bitmap index; 16 of 64 blocks per row so that tiles have steps to split
+    "long_bitmap": wl.scaled(wl.WORKLOADS["long_topk"], H=2, N=8192, density=0.25),
+}
+
+
+def _run_with_flags(w, flags):
+    """Forward under debug `flags`; checks the outputs and returns the launch's item count."""
+    bb.bsa_debug_config(flags, 0)
+    try:
+        inp = wl.make_inputs(w)
+        q, k, v = (gu.upload(inp, n) for n in ("q", "k", "v"))
+        mask = gu.oracle_mask(w, inp)
+        idx = gu.device_index(w, q, k, mask)
+        ws = bb.workspace(1, w.B, w.H, w.N, w.d, w.block)
+        O, L = bb.forward(q, k, v, idx, index_mode=w.index_mode, ws=ws)
+        torch.cuda.synchronize()
+        n_items = int(ws[12:16].view(torch.int32).item())  # workspace header: work items of the launch
+        gu.assert_attention_close(O, L, inp, mask, w)
+        return n_items
+    finally:
+        bb.bsa_debug_config(0, 0)
+
+
+@pytest.mark.parametrize("name", sorted(SPLIT_CASES))
+def test_split_tiles_match_oracle(name):
+    w = SPLIT_CASES[name]
+    tiles = w.B * w.H * ((w.N + 127) // 128)
+    assert _run_with_flags(w, bb.DBG_SPLIT_ALL) > tiles
+    assert _run_with_flags(w, bb.DBG_NO_SPLIT) == tiles
+
+
+@pytest.mark.parametrize("flags", [0, bb.DBG_SPLIT_ALL])
+def test_many_tiles_multi_cta_ordering(flags):
+    # more than 8192 query tiles: the work list is built by the multi-CTA ordering
+    # launch (smaller problems use the single-CTA one); sampled rows against the oracle
+    w = wl.scaled(wl.WORKLOADS["t2i_static"], B=1, H=128, N=64 * 130)
+    tiles = w.B * w.H * ((w.N + 127) // 128)
+    assert tiles > 8192
+    bb.bsa_debug_config(flags, 0)
+    try:
+        inp = wl.make_inputs(w)
+        q, k, v = (gu.upload(inp, n) for n in ("q", "k", "v"))
+        mask = gu.oracle_mask(w, inp)
+        idx = gu.device_index(w, q, k, mask)
+        ws = bb.workspace(1, w.B, w.H, w.N, w.d, w.block)
+        O, L = bb.forward(q, k, v, idx, index_mode=w.index_mode, ws=ws)
+        torch.cuda.synchronize()
+        n_items = int(ws[12:16].view(torch.int32).item())
+        assert n_items > tiles if flags else n_items >= tiles
+        rows = gu.sample_rows(w, np.random.default_rng(23), blocks_per_head=2, rows_per_block=4)
+        gu.assert_attention_close(O, L, inp, mask, w, rows=rows)
+    finally:
+        bb.bsa_debug_config(0, 0)
+
+
 @pytest.mark.parametrize("d,block,mode", [(64, 128, 0), (64, 128, 1), (128, 64, 1), (64, 64, 1)])
 def test_shape_combinations(d, block, mode):
     w = wl.scaled(wl.WORKLOADS["long_topk"], H=3, N=2048, d=d, block=block, density=0.3)

@@ -46,8 +46,14 @@ def test_workspace_sizes(lib):
     assert ws0 == max(dynamic, static)
     ws1 = bb.bsa_workspace_size(1, 2, 24, 4224, 64, 64)
     tiles = 2 * 24 * 33  # 128-row query tiles
-    # header + tile list (padded to 64 entries) + per-tile lengths
-    assert ws1 == 256 + ((tiles + 63) // 64 * 64 * 4 + tiles * 4 + 255) // 256 * 256
+    budget = min(640, 8 * tiles)  # partial slots for chunks of split tiles
+    # header, items (tiles + chunks), tile lengths, split bases, merge counters (8 per slot),
+    # partial row stats (16 B per row), partial O (fp32, d per row)
+    assert ws1 == (256 + up((tiles + budget) * 4) + 2 * up(tiles * 4) + up(budget * 8 * 4)
+                   + up(budget * 128 * 16) + up(budget * 128 * d * 4))
+    # a tiny problem gets at most 8 partial slots per tile
+    tiny = bb.bsa_workspace_size(1, 1, 1, 128, 64, 64)
+    assert tiny == 256 + up(9 * 4) + 2 * up(4) + up(8 * 8 * 4) + up(8 * 128 * 16) + up(8 * 128 * 64 * 4)
     with pytest.raises(bb.BsaError) as e:
         bb.bsa_workspace_size(1, 1, 1, 100, 64, 64)
     assert e.value.code == bb.ERR_SHAPE
