@@ -6,19 +6,26 @@
 // visited, and the output is divided by the true sum over the active blocks).
 //
 // Design (GB300-first, not the pages' Triton/xFormers recipes):
-//   * Persistent CTAs pull 128-row query tiles from a longest-first list with an
-//     atomic counter (balances rows with very different active counts, §5.3).
-//   * Warp roles: 4 or 8 softmax + epilogue warps, then one TMA producer warp and
-//     one tcgen05 MMA-issuing warp (one thread each). With 4 softmax warps a
-//     thread owns one query row (32x32b TMEM accesses); with 8, a thread owns two
-//     rows and a quarter of their columns (16x256b / 16x128b accesses) and a row's
-//     max and sums are combined over 4 lanes with shuffles.
+//   * Persistent CTAs pull work items from a longest-first list with an atomic
+//     counter (rows with very different active counts, §5.3). An item is a
+//     128-row query tile, or one KV-range chunk of a tile that is far longer than
+//     the per-CTA share of steps; the last chunk to finish merges the chunks'
+//     partial (O, max, sums).
+//   * Warp roles: 4 or 8 softmax + epilogue warps, a TMA producer warp, a QK^T
+//     issuer warp and a PV issuer warp. The role warps run converged and issue
+//     TMA copies, tcgen05.mma and tcgen05.commit from one elect.sync lane; every
+//     warp waits on mbarriers with all lanes and a vote (a lone lane waiting or
+//     issuing while the others park costs several times more on this GPU).
+//   * With 4 softmax warps a thread owns one query row (32x32b TMEM accesses);
+//     with 8, a thread owns two rows and a quarter of their columns (16x256b /
+//     16x128b accesses) and a row's max and sums are combined over 4 lanes.
 //   * Q tile and K/V blocks arrive by TMA (128-byte swizzle), K/V fetched by
 //     block index into separate K and V shared-memory rings (a K slot frees when
 //     its QK^T completes, a V slot when its PV completes).
-//   * S = Q K^T and O += P V run on tcgen05 with fp32 accumulators in TMEM.
-//     S is double-buffered so the QK^T of block n+1 overlaps the softmax of
-//     block n; P (bf16) overwrites S in TMEM and feeds the PV MMA directly.
+//   * S = Q K^T and O += P V run on tcgen05 with fp32 accumulators in TMEM. The
+//     QK^T issuer, the only consumer that walks the index, runs up to NSB steps
+//     ahead and leaves a step descriptor beside each S buffer; P (bf16)
+//     overwrites S in TMEM and feeds the PV MMA directly.
 //   * Online softmax in the log2 domain with one FFMA + one ex2 per score;
 //     the running max is only raised (and O rescaled in TMEM) when it grows by
 //     more than 2^8, which keeps the result exact while skipping most rescales.
