@@ -1444,6 +1444,7 @@ __global__ void __launch_bounds__(1024) tile_order_small_kernel(TcParams p, Orde
     }
 #pragma unroll
     for (int k = 0; k < kOrderPerThread; ++k) {
+        if (k * 1024 + (t & ~31) >= p.n_tiles) continue;  // no tile in this warp (warp-uniform)
         const bool valid = k * 1024 + t < p.n_tiles;
         (void)reserve_slots(hist, length_bucket((L[k] + n[k] - 1) / n[k]), valid ? n[k] : 0);
     }
@@ -1454,6 +1455,7 @@ __global__ void __launch_bounds__(1024) tile_order_small_kernel(TcParams p, Orde
     __syncthreads();
 #pragma unroll
     for (int k = 0; k < kOrderPerThread; ++k) {
+        if (k * 1024 + (t & ~31) >= p.n_tiles) continue;  // no tile in this warp (warp-uniform)
         const int tile = k * 1024 + t;
         const bool valid = tile < p.n_tiles;
         const int pos = reserve_slots(hist, length_bucket((L[k] + n[k] - 1) / n[k]), valid ? n[k] : 0);
