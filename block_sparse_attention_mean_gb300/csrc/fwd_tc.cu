@@ -612,19 +612,21 @@ __device__ __forceinline__ void softmax_rows(const TcParams &p, uint32_t sbase, 
 // SPLIT == 2: eight warps; warp w owns the 16 TMEM lanes 32*(w%4) + 16*(w/4)..
 // (16x256b / 16x128b accesses). Thread t holds rows t/4 and t/4 + 8 of that
 // group and, in every 8-column group of S and O, columns 2(t%4) and +1; a row's
-// max and sums are reduced over its 4 lanes with two shuffles.
-template <int D, int BS, int NSB, class C>
+// max and sums are reduced over its 4 lanes with two shuffles. A step holds PAIR
+// KV blocks: 8-column group g of the step belongs to block g / (BS / 8).
+template <int D, int BS, int NSB, int PAIR, class C>
 __device__ __forceinline__ void softmax_quads(const TcParams &p, uint32_t sbase, uint32_t tmem,
                                               volatile int32_t *tile_ids, const volatile uint32_t *desc,
                                               const Ctl &ctl, int warp, int lane)
 {
     auto bar = [&](int idx) -> uint32_t { return barrier_addr<C>(sbase, idx); };
-    constexpr int RS = BS / 8;  // 8-column groups of S
+    constexpr int RS = C::kStep / 8;  // 8-column groups of a step's S
+    constexpr int GPB = BS / 8;       // groups per block
     constexpr int RO = D / 8;   // 8-column groups of O
     const int quarter = warp & 3;
     const int lane0 = 32 * quarter + 16 * (warp >> 2);  // first tile row of this warp
     const uint32_t tbase = tmem + (static_cast<uint32_t>(lane0) << 16);
-    const uint32_t tO = tbase + NSB * BS;
+    const uint32_t tO = tbase + NSB * C::kStep;
     const int r_lo = lane0 + (lane >> 2);  // this thread's rows r_lo and r_lo + 8
     const int cpair = 2 * (lane & 3);
     const uint32_t qblk = BS == 128 ? 0u : static_cast<uint32_t>(quarter >> 1);
@@ -654,8 +656,12 @@ __device__ __forceinline__ void softmax_quads(const TcParams &p, uint32_t sbase,
             }
             continue;
         }
+        // running maxima; the sums of this thread's columns stay in partial
+        // accumulators (packed fp32 pairs; floats for the bf16-rounded P) until the
+        // epilogue, and a rescale scales them
         float m_lo = -CUDART_INF_F, m_hi = -CUDART_INF_F;
-        float l_lo = 0.0f, l_hi = 0.0f, lp_lo = 0.0f, lp_hi = 0.0f;  // this thread's columns only
+        uint64_t acc_lo[2] = {0ull, 0ull}, acc_hi[2] = {0ull, 0ull};
+        float ap_lo[4] = {0.0f, 0.0f, 0.0f, 0.0f}, ap_hi[4] = {0.0f, 0.0f, 0.0f, 0.0f};
         bool last = empty;  // an empty chunk of a split tile has no step
         while (!last) {
             const int b = G % NSB;
@@ -665,14 +671,22 @@ __device__ __forceinline__ void softmax_quads(const TcParams &p, uint32_t sbase,
             last = desc_last(sd);
             bool resc = false;
             float a_lo = 1.0f, a_hi = 1.0f;
-            if ((desc_members(sd, 0) >> qblk) & 1u) {
+            bool act[PAIR];
+            bool any = false;
+#pragma unroll
+            for (int q = 0; q < PAIR; ++q) {
+                act[q] = q < desc_count(sd) && ((desc_members(sd, q) >> qblk) & 1u) != 0u;
+                any |= act[q];
+            }
+            if (any) {
                 uint32_t sv[4 * RS];
-                tmem_ld_16x256b<RS>(tbase + b * BS, sv);
+                tmem_ld_16x256b<RS>(tbase + b * C::kStep, sv);
                 tmem_wait_ld();
                 reg_fence(sv);
                 float x0 = -CUDART_INF_F, x1 = -CUDART_INF_F, y0 = -CUDART_INF_F, y1 = -CUDART_INF_F;
 #pragma unroll
                 for (int g = 0; g < RS; g += 2) {
+                    if (!act[g / GPB]) continue;
                     x0 = fmax3(x0, __uint_as_float(sv[4 * g]), __uint_as_float(sv[4 * g + 1]));
                     y0 = fmax3(y0, __uint_as_float(sv[4 * g + 2]), __uint_as_float(sv[4 * g + 3]));
                     x1 = fmax3(x1, __uint_as_float(sv[4 * g + 4]), __uint_as_float(sv[4 * g + 5]));
@@ -688,8 +702,11 @@ __device__ __forceinline__ void softmax_quads(const TcParams &p, uint32_t sbase,
                     m_lo = t_lo;
                 } else if (t_lo > m_lo + kRescaleLog2) {
                     a_lo = ex2_approx(m_lo - t_lo);
-                    l_lo *= a_lo;
-                    lp_lo *= a_lo;
+                    const uint64_t a2 = f2_pack(a_lo, a_lo);
+                    acc_lo[0] = f2_fma(acc_lo[0], a2, 0ull);
+                    acc_lo[1] = f2_fma(acc_lo[1], a2, 0ull);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) ap_lo[k] *= a_lo;
                     m_lo = t_lo;
                     resc = true;
                 }
@@ -697,18 +714,23 @@ __device__ __forceinline__ void softmax_quads(const TcParams &p, uint32_t sbase,
                     m_hi = t_hi;
                 } else if (t_hi > m_hi + kRescaleLog2) {
                     a_hi = ex2_approx(m_hi - t_hi);
-                    l_hi *= a_hi;
-                    lp_hi *= a_hi;
+                    const uint64_t a2 = f2_pack(a_hi, a_hi);
+                    acc_hi[0] = f2_fma(acc_hi[0], a2, 0ull);
+                    acc_hi[1] = f2_fma(acc_hi[1], a2, 0ull);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) ap_hi[k] *= a_hi;
                     m_hi = t_hi;
                     resc = true;
                 }
                 const uint64_t c2x = f2_pack(p.scale_log2, p.scale_log2);
                 const uint64_t nm_lo = f2_pack(-m_lo, -m_lo), nm_hi = f2_pack(-m_hi, -m_hi);
-                uint64_t acc_lo[2] = {0ull, 0ull}, acc_hi[2] = {0ull, 0ull};
-                uint64_t accp_lo[2] = {0ull, 0ull}, accp_hi[2] = {0ull, 0ull};
                 uint32_t pk[2 * RS];
 #pragma unroll
                 for (int g = 0; g < RS; ++g) {
+                    if (!act[g / GPB]) {
+                        pk[2 * g] = pk[2 * g + 1] = 0u;
+                        continue;
+                    }
                     float x, y;
                     f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[4 * g]), __uint_as_float(sv[4 * g + 1])), c2x, nm_lo),
                               x, y);
@@ -721,26 +743,15 @@ __device__ __forceinline__ void softmax_quads(const TcParams &p, uint32_t sbase,
                     pk[2 * g + 1] = pack_bf16x2(p2, p3);  // row r_lo + 8
                     acc_lo[g & 1] = f2_add(acc_lo[g & 1], f2_pack(p0, p1));
                     acc_hi[g & 1] = f2_add(acc_hi[g & 1], f2_pack(p2, p3));
-                    accp_lo[g & 1] = f2_add(accp_lo[g & 1], f2_pack(__uint_as_float(pk[2 * g] << 16),
-                                                                    __uint_as_float(pk[2 * g] & 0xFFFF0000u)));
-                    accp_hi[g & 1] = f2_add(accp_hi[g & 1], f2_pack(__uint_as_float(pk[2 * g + 1] << 16),
-                                                                    __uint_as_float(pk[2 * g + 1] & 0xFFFF0000u)));
+                    add_bf16x2_to_f32(ap_lo[2 * (g & 1)], ap_lo[2 * (g & 1) + 1], pk[2 * g]);
+                    add_bf16x2_to_f32(ap_hi[2 * (g & 1)], ap_hi[2 * (g & 1) + 1], pk[2 * g + 1]);
                 }
-                tmem_st_16x128b<RS>(tbase + b * BS, pk);
-                float u0, u1;
-                f2_unpack(f2_add(acc_lo[0], acc_lo[1]), u0, u1);
-                l_lo += u0 + u1;
-                f2_unpack(f2_add(acc_hi[0], acc_hi[1]), u0, u1);
-                l_hi += u0 + u1;
-                f2_unpack(f2_add(accp_lo[0], accp_lo[1]), u0, u1);
-                lp_lo += u0 + u1;
-                f2_unpack(f2_add(accp_hi[0], accp_hi[1]), u0, u1);
-                lp_hi += u0 + u1;
+                tmem_st_16x128b<RS>(tbase + b * C::kStep, pk);
             } else {
                 uint32_t z[2 * RS];
 #pragma unroll
                 for (int q = 0; q < 2 * RS; ++q) z[q] = 0u;
-                tmem_st_16x128b<RS>(tbase + b * BS, z);
+                tmem_st_16x128b<RS>(tbase + b * C::kStep, z);
             }
             if (__any_sync(0xffffffffu, resc)) {
                 const int t = G - 1;
@@ -766,6 +777,16 @@ __device__ __forceinline__ void softmax_quads(const TcParams &p, uint32_t sbase,
             ++G;
         }
         // epilogue: whole-row sums over the 4 lanes of each row, then O / l and LSE
+        float l_lo, l_hi;
+        {
+            float u0, u1, w0, w1;
+            f2_unpack(f2_add(acc_lo[0], acc_lo[1]), u0, u1);
+            f2_unpack(f2_add(acc_hi[0], acc_hi[1]), w0, w1);
+            l_lo = u0 + u1;
+            l_hi = w0 + w1;
+        }
+        float lp_lo = (ap_lo[0] + ap_lo[1]) + (ap_lo[2] + ap_lo[3]);
+        float lp_hi = (ap_hi[0] + ap_hi[1]) + (ap_hi[2] + ap_hi[3]);
 #pragma unroll
         for (int o = 1; o <= 2; o <<= 1) {
             l_lo += __shfl_xor_sync(0xffffffffu, l_lo, o);
@@ -842,7 +863,6 @@ __global__ void __launch_bounds__((4 * SPLIT + 3) * 32, MINB)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const TcParams p)
 {
-    static_assert(PAIR == 1 || SPLIT == 1, "two-block steps use one softmax thread per row");
     using C = Cfg<D, BS, NK, NV, NSB, QS, PAIR>;
     using R = Roles<SPLIT>;
     constexpr int kProducerWarp = R::kProducerWarp, kQkWarp = R::kQkWarp, kMmaWarp = R::kMmaWarp;
@@ -1162,7 +1182,7 @@ __global__ void __launch_bounds__((4 * SPLIT + 3) * 32, MINB)
         if constexpr (SPLIT == 1)
             softmax_rows<D, BS, NSB, PAIR, C>(p, sbase, tmem, tile_ids, desc, ctl, warp, lane);
         else
-            softmax_quads<D, BS, NSB, C>(p, sbase, tmem, tile_ids, desc, ctl, warp, lane);
+            softmax_quads<D, BS, NSB, PAIR, C>(p, sbase, tmem, tile_ids, desc, ctl, warp, lane);
     }
 
     tc_fence_before();
