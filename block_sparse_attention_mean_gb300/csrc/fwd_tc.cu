@@ -55,6 +55,7 @@ struct Roles {
 };
 constexpr int kTileM = 128;
 constexpr float kRescaleLog2 = 8.0f;
+constexpr float kRescaleSum = 256.0f;  // 2^kRescaleLog2
 constexpr uint32_t kDbgStall = 1u;     // skip loads and MMAs (the softmax's first wait runs out)
 constexpr uint32_t kDbgNoSplit = 2u;   // never split a query tile
 constexpr uint32_t kDbgSplitAll = 4u;  // split every tile with two or more steps (as the budget allows)
@@ -442,8 +443,8 @@ __device__ __forceinline__ void softmax_rows(const TcParams &p, uint32_t sbase, 
         // pairs for the fp32 sum, eight floats for the sum of bf16-rounded P) until
         // the epilogue, and a rescale scales them all
         float m_run = -CUDART_INF_F;
-        uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
-        float accp[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
+        uint64_t acc[2] = {0ull, 0ull};
+        float accp[4] = {0.0f, 0.0f, 0.0f, 0.0f};
         bool last = empty;  // an empty chunk of a split tile has no step
         while (!last) {
             const int b = G % NSB;
@@ -468,54 +469,81 @@ __device__ __forceinline__ void softmax_rows(const TcParams &p, uint32_t sbase, 
                 tmem_wait_ld();
 #pragma unroll
                 for (int c = 0; c < NC; ++c) reg_fence32(sv[c]);
-                float mx0 = -CUDART_INF_F, mx1 = -CUDART_INF_F, mx2 = -CUDART_INF_F, mx3 = -CUDART_INF_F;
+                // row max of the step's active scores, log2 units
+                auto step_max = [&]() -> float {
+                    float mx0 = -CUDART_INF_F, mx1 = -CUDART_INF_F, mx2 = -CUDART_INF_F, mx3 = -CUDART_INF_F;
 #pragma unroll
-                for (int c = 0; c < NC; ++c) {
-                    if (!act[c / CPB]) continue;
+                    for (int c = 0; c < NC; ++c) {
+                        if (!act[c / CPB]) continue;
 #pragma unroll
-                    for (int t = 0; t < 32; t += 8) {
-                        mx0 = fmax3(mx0, __uint_as_float(sv[c][t]), __uint_as_float(sv[c][t + 1]));
-                        mx1 = fmax3(mx1, __uint_as_float(sv[c][t + 2]), __uint_as_float(sv[c][t + 3]));
-                        mx2 = fmax3(mx2, __uint_as_float(sv[c][t + 4]), __uint_as_float(sv[c][t + 5]));
-                        mx3 = fmax3(mx3, __uint_as_float(sv[c][t + 6]), __uint_as_float(sv[c][t + 7]));
+                        for (int t = 0; t < 32; t += 8) {
+                            mx0 = fmax3(mx0, __uint_as_float(sv[c][t]), __uint_as_float(sv[c][t + 1]));
+                            mx1 = fmax3(mx1, __uint_as_float(sv[c][t + 2]), __uint_as_float(sv[c][t + 3]));
+                            mx2 = fmax3(mx2, __uint_as_float(sv[c][t + 4]), __uint_as_float(sv[c][t + 5]));
+                            mx3 = fmax3(mx3, __uint_as_float(sv[c][t + 6]), __uint_as_float(sv[c][t + 7]));
+                        }
                     }
-                }
-                const float m_tile = fmax3(fmaxf(mx0, mx1), mx2, mx3) * p.scale_log2;
-                if (m_run == -CUDART_INF_F) {
-                    m_run = m_tile;
-                } else if (m_tile > m_run + kRescaleLog2) {
-                    alpha = ex2_approx(m_run - m_tile);
-                    const uint64_t a2 = f2_pack(alpha, alpha);
-#pragma unroll
-                    for (int a = 0; a < 4; ++a) acc[a] = f2_fma(acc[a], a2, 0ull);
-#pragma unroll
-                    for (int a = 0; a < 8; ++a) accp[a] *= alpha;
-                    m_run = m_tile;
-                    resc = true;
-                }
+                    return fmax3(fmaxf(mx0, mx1), mx2, mx3) * p.scale_log2;
+                };
+                // p = 2^(s * scale * log2 e - m), P to bf16 and stored over S, and the step's two sums
                 const uint64_t c2x = f2_pack(p.scale_log2, p.scale_log2);
-                const uint64_t nm2 = f2_pack(-m_run, -m_run);
+                uint64_t sacc[2];
+                float sap[4];
+                auto exps = [&](float m) {
+                    const uint64_t nm2 = f2_pack(-m, -m);
+                    sacc[0] = sacc[1] = 0ull;
 #pragma unroll
-                for (int c = 0; c < NC; ++c) {
-                    uint32_t pk[16];
-                    if (act[c / CPB]) {
+                    for (int k = 0; k < 4; ++k) sap[k] = 0.0f;
+#pragma unroll
+                    for (int c = 0; c < NC; ++c) {
+                        uint32_t pk[16];
 #pragma unroll
                         for (int q = 0; q < 16; ++q) {
+                            if (!act[c / CPB]) {
+                                pk[q] = 0u;
+                                continue;
+                            }
                             float x0, x1;
                             f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[c][2 * q]), __uint_as_float(sv[c][2 * q + 1])),
                                              c2x, nm2),
                                       x0, x1);
                             const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
                             pk[q] = pack_bf16x2(p0, p1);
-                            acc[q & 3] = f2_add(acc[q & 3], f2_pack(p0, p1));
-                            add_bf16x2_to_f32(accp[2 * (q & 3)], accp[2 * (q & 3) + 1], pk[q]);
+                            sacc[q & 1] = f2_add(sacc[q & 1], f2_pack(p0, p1));
+                            add_bf16x2_to_f32(sap[2 * (q & 1)], sap[2 * (q & 1) + 1], pk[q]);
                         }
-                    } else {
-#pragma unroll
-                        for (int q = 0; q < 16; ++q) pk[q] = 0u;
+                        tmem_st16(tS + b * kStep + c * 16, pk);
                     }
-                    tmem_st16(tS + b * kStep + c * 16, pk);
+                };
+                if (m_run == -CUDART_INF_F) m_run = step_max();  // a tile's first step
+                exps(m_run);
+                // Lazy rescale without a max pass: a step sum of at most 2^8 bounds every p by 2^8,
+                // the same condition as "no score more than 8 above the running max"; a larger sum
+                // (or inf) raises the running max to the step's and redoes the step.
+                // The decision is per row (register work only); the redo stores P to TMEM, so the
+                // whole warp redoes the step when any row raised its max (tcgen05 accesses are
+                // warp-collective), the other rows recomputing the same values.
+                float s0, s1;
+                f2_unpack(f2_add(sacc[0], sacc[1]), s0, s1);
+                if (!(s0 + s1 <= kRescaleSum)) {
+                    const float m_tile = step_max();
+                    alpha = ex2_approx(m_run - m_tile);
+                    const uint64_t a2 = f2_pack(alpha, alpha);
+#pragma unroll
+                    for (int k = 0; k < 2; ++k) acc[k] = f2_fma(acc[k], a2, 0ull);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) accp[k] *= alpha;
+                    m_run = m_tile;
+                    resc = true;
                 }
+                if (__any_sync(0xffffffffu, resc)) {
+                    tmem_wait_st();  // the first pass's P stores land before they are overwritten
+                    exps(m_run);
+                }
+#pragma unroll
+                for (int k = 0; k < 2; ++k) acc[k] = f2_add(acc[k], sacc[k]);
+#pragma unroll
+                for (int k = 0; k < 4; ++k) accp[k] += sap[k];
             } else {
                 uint32_t z[16];
 #pragma unroll
@@ -546,9 +574,9 @@ __device__ __forceinline__ void softmax_rows(const TcParams &p, uint32_t sbase, 
             ++G;
         }
         float e0, e1;
-        f2_unpack(f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3])), e0, e1);
+        f2_unpack(f2_add(acc[0], acc[1]), e0, e1);
         const float l_run = e0 + e1;
-        const float lp_run = ((accp[0] + accp[1]) + (accp[2] + accp[3])) + ((accp[4] + accp[5]) + (accp[6] + accp[7]));
+        const float lp_run = (accp[0] + accp[1]) + (accp[2] + accp[3]);
         const Item it = decode_item(p, tile & ~kEmptyTile);  // decoded again: not live across the loop
         if (it.nchunk > 1) {
             // chunk of a split tile: unnormalised partial O and the row's (m, l, lp)
