@@ -52,6 +52,8 @@ def parse_args():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--residual", action="store_true",
+                    help="time bsa_forward_residual (residual compensation) with R captured at warm-up")
     return ap.parse_args()
 
 
@@ -275,9 +277,36 @@ def run_ours(args, world, rank, local):
         bb.bsa_build_mask(qk_in[0], qk_in[1], dt, B, H, N, d, bs, w.density, spec, row_ptr, col_idx, cap,
                           bitmap, ws_m, ws_m.numel(), s)
 
-    def fwd_call(s):
+    R = None
+    if args.residual:
+        # anchor step, outside the timed region: dense output (every block active) and sparse
+        # output of this workload, R = O_dense - O_sparse
+        ones = np.ones((B, H, nB, nB), dtype=np.uint8)
+        full_dev = torch.from_numpy(wl.pack_bitmap_words(ones).reshape(-1)).to(dev)
+        full_spec = bb.explicit_spec(full_dev)
+        cap_full = bb.bsa_mask_nnz(B, H, N, bs, 0.0, full_spec)
+        rp_f = torch.empty(B * H * nB + 1, dtype=torch.int32, device=dev)
+        ci_f = torch.empty(cap_full, dtype=torch.int32, device=dev)
+        bm_f = torch.empty(B * H * nB * W, dtype=torch.int32, device=dev)
+        bb.bsa_build_mask(None, None, dt, B, H, N, d, bs, 0.0, full_spec, rp_f, ci_f, cap_full, bm_f, ws_m,
+                          ws_m.numel(), None)
+        O_dense = torch.empty_like(q)
+        bb.bsa_forward(q, k, v, dt, B, H, N, d, bs, rp_f, ci_f, bm_f, 0, 0.0, O_dense, LSE, ws_f, ws_f.numel(), None)
+        bb.bsa_build_mask(qk_in[0], qk_in[1], dt, B, H, N, d, bs, w.density, spec, row_ptr, col_idx, cap,
+                          bitmap, ws_m, ws_m.numel(), None)
         bb.bsa_forward(q, k, v, dt, B, H, N, d, bs, row_ptr, col_idx, bitmap, w.index_mode, 0.0, O, LSE, ws_f,
-                       ws_f.numel(), s)
+                       ws_f.numel(), None)
+        R = bb.residual_capture(O_dense, O)
+        torch.cuda.synchronize()
+        del O_dense, rp_f, ci_f, bm_f, full_dev
+
+    def fwd_call(s):
+        if R is None:
+            bb.bsa_forward(q, k, v, dt, B, H, N, d, bs, row_ptr, col_idx, bitmap, w.index_mode, 0.0, O, LSE, ws_f,
+                           ws_f.numel(), s)
+        else:
+            bb.bsa_forward_residual(q, k, v, dt, B, H, N, d, bs, row_ptr, col_idx, bitmap, w.index_mode, 0.0, R, O,
+                                    LSE, ws_f, ws_f.numel(), s)
 
     launches_per_step = (3 if spec is not None else 2) + (2 if dt == bb.BF16 else 1)
 
@@ -409,12 +438,13 @@ def run_ours(args, world, rank, local):
                    "active_block_pairs": nnz, "block_density": round(nnz / (w.B * w.H * nB * nB), 5),
                    "index_mode": "bitmap" if w.index_mode else "csr",
                    "l2": "flushed (256 MB write) before every timed step", "cuda_graphs": bool(graphs),
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "residual": "O_sparse + R (R captured at warm-up)" if R is not None else None},
         "fwd_ms_per_call": round(fwd_mean, 5), "build_mask_ms": round(sum(build_ms) / len(build_ms), 5),
         "fwd_tflops": round(achieved, 2), "pct_of_bf16_peak": round(100 * achieved / peak, 2),
         "wall_s_timed_loop": round(wall, 4),
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
-                     "frac": round(achieved / peak, 4), "traffic": traffic_from_profile(),
+                     "frac": round(achieved / peak, 4), "traffic": traffic_from_profile() if R is None else None,
                      "kernel": "fwd_tc_kernel (+ tile_order_kernel in the same bracket)",
                      "peak_source": f"{peak_kind} bf16_tflops (burst)"},
         "e2e": e2e, "gpu_launches": launches_per_step * args.steps, "clocks": clocks, "cpu_baseline": cpu,

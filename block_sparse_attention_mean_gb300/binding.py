@@ -38,7 +38,7 @@ MAX_ANCHORS = 8
 # every symbol declared in include/bsa.h
 EXPORTS = ("bsa_build_mask", "bsa_forward", "bsa_mask_nnz", "bsa_workspace_size",
            "bsa_check_device_error", "bsa_validate_index", "bsa_debug_config",
-           "bsa_status_string", "bsa_build_mask_noalloc")
+           "bsa_status_string", "bsa_build_mask_noalloc", "bsa_residual_capture", "bsa_forward_residual")
 NOALLOC_SCRATCH_BYTES = 16 << 20  # BSA_NOALLOC_SCRATCH_BYTES
 # bsa_debug_config flag bits
 DBG_STALL = 1       # skip loads and MMAs: the first device wait runs out
@@ -76,6 +76,8 @@ def load():
     lib.bsa_build_mask.argtypes = [P, P, I, I, I, I, I, I, F, ctypes.POINTER(StaticSpec), P, P, I64, P, P,
                                    SZ, P]
     lib.bsa_forward.argtypes = [P, P, P, I, I, I, I, I, I, P, P, P, I, F, P, P, P, SZ, P]
+    lib.bsa_forward_residual.argtypes = [P, P, P, I, I, I, I, I, I, P, P, P, I, F, P, P, P, P, SZ, P]
+    lib.bsa_residual_capture.argtypes = [P, P, I, I64, P, P]
     lib.bsa_build_mask_noalloc.argtypes = [P, P, I, I, I, I, I, I, F, ctypes.POINTER(StaticSpec), P, P, I64, P,
                                            P, P]
     lib.bsa_mask_nnz.argtypes = [I, I, I, I, F, ctypes.POINTER(StaticSpec), ctypes.POINTER(I64)]
@@ -136,6 +138,20 @@ def bsa_forward(Q, K, V, dt: int, B: int, H: int, N: int, d: int, block: int, ro
                               _ptr(bitmap), int(index_mode), float(scale), _ptr(O), _ptr(LSE),
                               _ptr(workspace), int(workspace_bytes), _stream(stream))
     _check(code, "bsa_forward")
+
+
+def bsa_forward_residual(Q, K, V, dt: int, B: int, H: int, N: int, d: int, block: int, row_ptr, col_idx,
+                         bitmap, index_mode: int, scale: float, R, O, LSE, workspace, workspace_bytes: int,
+                         stream=None) -> None:
+    code = load().bsa_forward_residual(_ptr(Q), _ptr(K), _ptr(V), dt, B, H, N, d, block, _ptr(row_ptr),
+                                       _ptr(col_idx), _ptr(bitmap), int(index_mode), float(scale), _ptr(R),
+                                       _ptr(O), _ptr(LSE), _ptr(workspace), int(workspace_bytes), _stream(stream))
+    _check(code, "bsa_forward_residual")
+
+
+def bsa_residual_capture(O_dense, O_sparse, dt: int, count: int, R, stream=None) -> None:
+    code = load().bsa_residual_capture(_ptr(O_dense), _ptr(O_sparse), dt, int(count), _ptr(R), _stream(stream))
+    _check(code, "bsa_residual_capture")
 
 
 def bsa_build_mask_noalloc(Q, K, dt: int, B: int, H: int, N: int, d: int, block: int, density: float,
@@ -265,8 +281,9 @@ def build_mask(q: Optional[torch.Tensor], k: Optional[torch.Tensor], block: int,
 
 def forward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, index: Index, index_mode: int = 0,
             scale: float = 0.0, ws: Optional[torch.Tensor] = None, out: Optional[torch.Tensor] = None,
-            lse: Optional[torch.Tensor] = None, stream=None, check: bool = True):
-    """Run bsa_forward; returns (O, LSE)."""
+            lse: Optional[torch.Tensor] = None, stream=None, check: bool = True,
+            residual: Optional[torch.Tensor] = None):
+    """Run bsa_forward (or bsa_forward_residual when `residual` is given); returns (O, LSE)."""
     B, H, N, d = q.shape
     if out is None:
         out = torch.empty_like(q)
@@ -274,11 +291,24 @@ def forward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, index: Index, ind
         lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
     if ws is None:
         ws = workspace(1, B, H, N, d, index.block, q.device)
-    bsa_forward(q, k, v, _dtype_code(q), B, H, N, d, index.block, index.row_ptr, index.col_idx, index.bitmap,
-                index_mode, scale, out, lse, ws, ws.numel(), stream)
+    if residual is None:
+        bsa_forward(q, k, v, _dtype_code(q), B, H, N, d, index.block, index.row_ptr, index.col_idx, index.bitmap,
+                    index_mode, scale, out, lse, ws, ws.numel(), stream)
+    else:
+        bsa_forward_residual(q, k, v, _dtype_code(q), B, H, N, d, index.block, index.row_ptr, index.col_idx,
+                             index.bitmap, index_mode, scale, residual, out, lse, ws, ws.numel(), stream)
     if check:
         _check(bsa_check_device_error(ws, stream), "bsa_forward (device)")
     return out, lse
+
+
+def residual_capture(o_dense: torch.Tensor, o_sparse: torch.Tensor, out: Optional[torch.Tensor] = None,
+                     stream=None) -> torch.Tensor:
+    """R = O_dense - O_sparse in fp32 (bsa_residual_capture)."""
+    if out is None:
+        out = torch.empty(o_dense.shape, dtype=torch.float32, device=o_dense.device)
+    bsa_residual_capture(o_dense, o_sparse, _dtype_code(o_dense), o_dense.numel(), out, stream)
+    return out
 
 
 def default_scale(d: int) -> float:

@@ -185,9 +185,10 @@ bsa_status bsa_build_mask(const void *Q, const void *K, int dt, int B, int H, in
     return bsa::launch_build_mask(a, static_cast<cudaStream_t>(stream));
 }
 
-bsa_status bsa_forward(const void *Q, const void *K, const void *V, int dt, int B, int H, int N, int d, int block,
-                       const int32_t *row_ptr, const int32_t *col_idx, const uint32_t *bitmap, int index_mode,
-                       float scale, void *O, float *LSE, void *workspace, size_t workspace_bytes, void *stream)
+static bsa_status forward_impl(const void *Q, const void *K, const void *V, int dt, int B, int H, int N, int d,
+                               int block, const int32_t *row_ptr, const int32_t *col_idx, const uint32_t *bitmap,
+                               int index_mode, float scale, const float *R, void *O, float *LSE, void *workspace,
+                               size_t workspace_bytes, void *stream)
 {
     bsa_status s = check_shape(B, H, N, d, block);
     if (s != BSA_OK) return s;
@@ -225,11 +226,41 @@ bsa_status bsa_forward(const void *Q, const void *K, const void *V, int dt, int 
     a.scale = scale > 0.0f ? scale : static_cast<float>(1.0 / std::sqrt(static_cast<double>(d)));
     a.O = O;
     a.LSE = LSE;
+    a.R = R;
     a.ws = static_cast<char *>(workspace);
     a.dbg_flags = g_dbg_flags;
     a.wait_limit_ns = g_wait_limit_ns;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     return dt == BSA_BF16 ? bsa::launch_forward_tc(a, st) : bsa::launch_forward_simt(a, st);
+}
+
+bsa_status bsa_forward(const void *Q, const void *K, const void *V, int dt, int B, int H, int N, int d, int block,
+                       const int32_t *row_ptr, const int32_t *col_idx, const uint32_t *bitmap, int index_mode,
+                       float scale, void *O, float *LSE, void *workspace, size_t workspace_bytes, void *stream)
+{
+    return forward_impl(Q, K, V, dt, B, H, N, d, block, row_ptr, col_idx, bitmap, index_mode, scale, nullptr, O, LSE,
+                        workspace, workspace_bytes, stream);
+}
+
+bsa_status bsa_forward_residual(const void *Q, const void *K, const void *V, int dt, int B, int H, int N, int d,
+                                int block, const int32_t *row_ptr, const int32_t *col_idx, const uint32_t *bitmap,
+                                int index_mode, float scale, const float *R, void *O, float *LSE, void *workspace,
+                                size_t workspace_bytes, void *stream)
+{
+    if (!R || !aligned(R, 16)) return BSA_ERR_INVALID_ARG;
+    return forward_impl(Q, K, V, dt, B, H, N, d, block, row_ptr, col_idx, bitmap, index_mode, scale, R, O, LSE,
+                        workspace, workspace_bytes, stream);
+}
+
+bsa_status bsa_residual_capture(const void *O_dense, const void *O_sparse, int dt, int64_t count, float *R,
+                                void *stream)
+{
+    if (dt != BSA_BF16 && dt != BSA_FP32) return BSA_ERR_DTYPE;
+    if (count < 0) return BSA_ERR_INVALID_ARG;
+    if (count == 0) return BSA_OK;
+    if (!O_dense || !O_sparse || !R) return BSA_ERR_INVALID_ARG;
+    if (!aligned(O_dense, 16) || !aligned(O_sparse, 16) || !aligned(R, 16)) return BSA_ERR_INVALID_ARG;
+    return bsa::launch_residual_capture(O_dense, O_sparse, dt, count, R, static_cast<cudaStream_t>(stream));
 }
 
 bsa_status bsa_check_device_error(void *workspace, void *stream)

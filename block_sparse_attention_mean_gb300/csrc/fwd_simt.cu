@@ -27,7 +27,7 @@ __global__ void __launch_bounds__(kWarps * 32) fwd_simt_kernel(const float *__re
                                                               const int32_t *__restrict__ col_idx,
                                                               const uint32_t *__restrict__ bitmap, int index_mode,
                                                               float scale, float *__restrict__ O,
-                                                              float *__restrict__ LSE)
+                                                              float *__restrict__ LSE, const float *__restrict__ R)
 {
     constexpr int RPW = BS / kWarps;  // query rows per warp
     constexpr int DPL = D / 32;       // channels per lane
@@ -101,7 +101,8 @@ __global__ void __launch_bounds__(kWarps * 32) fwd_simt_kernel(const float *__re
         const int64_t row = row0 + warp * RPW + r;
         const float inv = l[r] > 0.0f ? 1.0f / l[r] : 0.0f;
 #pragma unroll
-        for (int t = 0; t < DPL; ++t) O[row * D + lane + 32 * t] = o[r][t] * inv;
+        for (int t = 0; t < DPL; ++t)
+            O[row * D + lane + 32 * t] = o[r][t] * inv + (R ? R[row * D + lane + 32 * t] : 0.0f);
         if (lane == 0) LSE[row] = l[r] > 0.0f ? m[r] + logf(l[r]) : -CUDART_INF_F;
     }
 }
@@ -121,7 +122,7 @@ bsa_status launch(const FwdArgs &a, cudaStream_t st)
     fwd_simt_kernel<D, BS><<<grid, kWarps * 32, smem, st>>>(
         static_cast<const float *>(a.Q), static_cast<const float *>(a.K), static_cast<const float *>(a.V), a.N,
         a.nQB, a.nKB, a.W, a.row_ptr, a.col_idx, a.bitmap, a.index_mode, a.scale, static_cast<float *>(a.O),
-        a.LSE);
+        a.LSE, a.R);
     return cudaGetLastError() == cudaSuccess ? BSA_OK : BSA_ERR_CUDA;
 }
 

@@ -90,6 +90,7 @@ struct TcParams {
     const int32_t *split_base; // per tile: first partial slot of a split tile, else -1
     uint32_t *merge_cnt;       // per split tile and softmax warp: chunks finished
     float *part_o;             // [slot][128][D] unnormalised partial O
+    const float *R;            // residual added to O before rounding ([B][H][N][D] fp32), or nullptr
     float4 *part_stats;        // [slot][128] (row max in log2 units, fp32 sum, sum of bf16-rounded P, 0)
 };
 
@@ -314,7 +315,7 @@ __device__ __forceinline__ void merge_weights(const TcParams &p, int base, int n
 // registers.
 template <int D>
 __device__ __noinline__ void merge_row(const TcParams &p, int base, int nchunk, int trow, __nv_bfloat16 *orow,
-                                          float *lse)
+                                          float *lse, const float *rrow)
 {
     float w[kMaxChunks], M, L, LP;
     merge_weights(p, base, nchunk, trow, w, M, L, LP);
@@ -338,9 +339,21 @@ __device__ __noinline__ void merge_row(const TcParams &p, int base, int nchunk, 
                 a[4 * q + 3] += w[k] * v.w;
             }
         }
+#pragma unroll
+        for (int q = 0; q < 16; ++q) a[q] *= inv;
+        if (rrow) {  // residual compensation: O_sparse + R
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const float4 r = __ldg(reinterpret_cast<const float4 *>(rrow + c * 16) + q);
+                a[4 * q] += r.x;
+                a[4 * q + 1] += r.y;
+                a[4 * q + 2] += r.z;
+                a[4 * q + 3] += r.w;
+            }
+        }
         uint32_t pk[8];
 #pragma unroll
-        for (int q = 0; q < 8; ++q) pk[q] = pack_bf16x2(a[2 * q] * inv, a[2 * q + 1] * inv);
+        for (int q = 0; q < 8; ++q) pk[q] = pack_bf16x2(a[2 * q], a[2 * q + 1]);
         uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 16);
         dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
         dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
@@ -353,7 +366,7 @@ __device__ __noinline__ void merge_row(const TcParams &p, int base, int nchunk, 
 template <int D>
 __device__ __noinline__ void merge_quad(const TcParams &p, int base, int nchunk, int r, int cpair, int lane,
                                            bool lo_valid, bool hi_valid, uint32_t *o_lo, uint32_t *o_hi, float *lse_lo,
-                                           float *lse_hi)
+                                           float *lse_hi, const float *r_lo, const float *r_hi)
 {
     float wl[kMaxChunks], wh[kMaxChunks], Ml, Ll, LPl, Mh, Lh, LPh;
     merge_weights(p, base, nchunk, r, wl, Ml, Ll, LPl);
@@ -377,8 +390,13 @@ __device__ __noinline__ void merge_quad(const TcParams &p, int base, int nchunk,
                 ah.y += wh[k] * v.y;
             }
         }
-        if (lo_valid) o_lo[4 * g] = pack_bf16x2(al.x * il, al.y * il);
-        if (hi_valid) o_hi[4 * g] = pack_bf16x2(ah.x * ih, ah.y * ih);
+        float2 rl = make_float2(0.0f, 0.0f), rh = make_float2(0.0f, 0.0f);
+        if (r_lo) {  // residual compensation: O_sparse + R
+            if (lo_valid) rl = __ldg(reinterpret_cast<const float2 *>(r_lo + 8 * g));
+            if (hi_valid) rh = __ldg(reinterpret_cast<const float2 *>(r_hi + 8 * g));
+        }
+        if (lo_valid) o_lo[4 * g] = pack_bf16x2(fmaf(al.x, il, rl.x), fmaf(al.y, il, rl.y));
+        if (hi_valid) o_hi[4 * g] = pack_bf16x2(fmaf(ah.x, ih, rh.x), fmaf(ah.y, ih, rh.y));
     }
     if ((lane & 3) == 0) {
         if (lo_valid) *lse_lo = Ll > 0.0f ? (Ml + log2f(Ll)) * 0.69314718055994530942f : -CUDART_INF_F;
@@ -430,6 +448,10 @@ __device__ __forceinline__ void softmax_rows(const TcParams &p, uint32_t sbase, 
         const bool row_valid = row < p.N;
         const int64_t grow = bh * p.N + row;
         __nv_bfloat16 *orow = p.O + grow * D;
+        if (p.R && row_valid) {  // the epilogue reads this row of the residual: start it towards L2 now
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) prefetch_l2(p.R + grow * D + c * 32);
+        }
         if (empty && decode_item(p, tile & ~kEmptyTile).nchunk == 1) {
             if (row_valid) {
                 const uint4 z = make_uint4(0u, 0u, 0u, 0u);
@@ -606,7 +628,8 @@ __device__ __forceinline__ void softmax_rows(const TcParams &p, uint32_t sbase, 
                 for (int q = 0; q < D / 4; ++q) po[q] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
             }
             p.part_stats[prow] = make_float4(m_run, l_run, lp_run, 0.0f);
-            if (last_chunk(p, base, it.nchunk, warp, lane) && row_valid) merge_row<D>(p, base, it.nchunk, trow, orow, p.LSE + grow);
+            if (last_chunk(p, base, it.nchunk, warp, lane) && row_valid)
+                merge_row<D>(p, base, it.nchunk, trow, orow, p.LSE + grow, p.R ? p.R + grow * D : nullptr);
             continue;
         }
         // epilogue: O / l, LSE = ln2 * (m + log2 l)
@@ -622,9 +645,21 @@ __device__ __forceinline__ void softmax_rows(const TcParams &p, uint32_t sbase, 
             reg_fence32(ov);
             if (row_valid) {
                 uint32_t pk[16];
+                if (p.R) {  // residual compensation: O_sparse + R
+                    const float4 *rs = reinterpret_cast<const float4 *>(p.R + grow * D + c * 32);
 #pragma unroll
-                for (int q = 0; q < 16; ++q)
-                    pk[q] = pack_bf16x2(__uint_as_float(ov[2 * q]) * inv_l, __uint_as_float(ov[2 * q + 1]) * inv_l);
+                    for (int q = 0; q < 8; ++q) {
+                        const float4 r = __ldg(rs + q);
+                        pk[2 * q] = pack_bf16x2(fmaf(__uint_as_float(ov[4 * q]), inv_l, r.x),
+                                                fmaf(__uint_as_float(ov[4 * q + 1]), inv_l, r.y));
+                        pk[2 * q + 1] = pack_bf16x2(fmaf(__uint_as_float(ov[4 * q + 2]), inv_l, r.z),
+                                                    fmaf(__uint_as_float(ov[4 * q + 3]), inv_l, r.w));
+                    }
+                } else {
+#pragma unroll
+                    for (int q = 0; q < 16; ++q)
+                        pk[q] = pack_bf16x2(__uint_as_float(ov[2 * q]) * inv_l, __uint_as_float(ov[2 * q + 1]) * inv_l);
+                }
                 uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
 #pragma unroll
                 for (int q = 0; q < 4; ++q) dst[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
@@ -672,6 +707,10 @@ __device__ __forceinline__ void softmax_quads(const TcParams &p, uint32_t sbase,
         const int64_t g_lo = bh * p.N + row_lo, g_hi = g_lo + 8;
         uint32_t *o_lo = reinterpret_cast<uint32_t *>(p.O + g_lo * D + cpair);
         uint32_t *o_hi = reinterpret_cast<uint32_t *>(p.O + g_hi * D + cpair);
+        if (p.R && (lane & 3) < D / 32) {  // the epilogue reads these residual rows: start them towards L2 now
+            if (lo_valid) prefetch_l2(p.R + g_lo * D + 32 * (lane & 3));
+            if (hi_valid) prefetch_l2(p.R + g_hi * D + 32 * (lane & 3));
+        }
         if (empty && it.nchunk == 1) {
 #pragma unroll
             for (int g = 0; g < RO; ++g) {
@@ -859,7 +898,8 @@ __device__ __forceinline__ void softmax_quads(const TcParams &p, uint32_t sbase,
             }
             if (last_chunk(p, base, it.nchunk, warp, lane))
                 merge_quad<D>(p, base, it.nchunk, r_lo, cpair, lane, lo_valid, hi_valid, o_lo, o_hi, p.LSE + g_lo,
-                              p.LSE + g_hi);
+                              p.LSE + g_hi, p.R ? p.R + g_lo * D + cpair : nullptr,
+                              p.R ? p.R + g_hi * D + cpair : nullptr);
             continue;
         }
         const int t = G - 1;
@@ -875,9 +915,17 @@ __device__ __forceinline__ void softmax_quads(const TcParams &p, uint32_t sbase,
         const float i_lo = lp_lo > 0.0f ? 1.0f / lp_lo : 0.0f, i_hi = lp_hi > 0.0f ? 1.0f / lp_hi : 0.0f;
 #pragma unroll
         for (int g = 0; g < RO; ++g) {
-            if (lo_valid) o_lo[4 * g] = pack_bf16x2(__uint_as_float(ov[4 * g]) * i_lo, __uint_as_float(ov[4 * g + 1]) * i_lo);
+            float2 rl = make_float2(0.0f, 0.0f), rh = make_float2(0.0f, 0.0f);
+            if (p.R) {  // residual compensation: O_sparse + R
+                if (lo_valid) rl = __ldg(reinterpret_cast<const float2 *>(p.R + g_lo * D + cpair + 8 * g));
+                if (hi_valid) rh = __ldg(reinterpret_cast<const float2 *>(p.R + g_hi * D + cpair + 8 * g));
+            }
+            if (lo_valid)
+                o_lo[4 * g] = pack_bf16x2(fmaf(__uint_as_float(ov[4 * g]), i_lo, rl.x),
+                                          fmaf(__uint_as_float(ov[4 * g + 1]), i_lo, rl.y));
             if (hi_valid)
-                o_hi[4 * g] = pack_bf16x2(__uint_as_float(ov[4 * g + 2]) * i_hi, __uint_as_float(ov[4 * g + 3]) * i_hi);
+                o_hi[4 * g] = pack_bf16x2(fmaf(__uint_as_float(ov[4 * g + 2]), i_hi, rh.x),
+                                          fmaf(__uint_as_float(ov[4 * g + 3]), i_hi, rh.y));
         }
         if ((lane & 3) == 0) {
             if (lo_valid) p.LSE[g_lo] = l_lo > 0.0f ? (m_lo + log2f(l_lo)) * 0.69314718055994530942f : -CUDART_INF_F;
@@ -1652,6 +1700,7 @@ bsa_status launch_tc(const FwdArgs &a, cudaStream_t st)
     p.merge_cnt = o.merge_cnt;
     p.part_stats = reinterpret_cast<float4 *>(a.ws + lay.part_stats);
     p.part_o = reinterpret_cast<float *>(a.ws + lay.part_o);
+    p.R = a.R;
     p.tile_counter = &hdr->tile_counter;
     p.err = &hdr->err;
     p.wait_limit_ns = a.wait_limit_ns;

@@ -66,6 +66,7 @@ struct FwdArgs {
     float scale;           // > 0
     void *O;
     float *LSE;
+    const float *R;        // residual added to O before rounding (nullptr: none)
     char *ws;
     uint32_t dbg_flags;
     uint64_t wait_limit_ns;
@@ -74,5 +75,7 @@ struct FwdArgs {
 size_t fwd_workspace_bytes(int B, int H, int N, int d, int block);
 bsa_status launch_forward_tc(const FwdArgs &a, cudaStream_t st);    // bf16, tcgen05
 bsa_status launch_forward_simt(const FwdArgs &a, cudaStream_t st);  // fp32, CUDA cores
+bsa_status launch_residual_capture(const void *dense, const void *sparse, int dt, int64_t count, float *R,
+                                   cudaStream_t st);
 
 }  // namespace bsa

@@ -110,6 +110,12 @@ __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols)
                  : "memory");
 }
 
+// Hint: bring the 128-byte line holding `p` into L2 (p must be a valid global address).
+__device__ __forceinline__ void prefetch_l2(const void *p)
+{
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
 // One lane of a converged warp (the same one every time the whole warp calls it).
 __device__ __forceinline__ bool elect_one()
 {

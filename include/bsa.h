@@ -145,6 +145,37 @@ bsa_status bsa_forward(const void *Q, const void *K, const void *V, int dt, int 
                        void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * Residual compensation ([P3] section "残差补偿找回被丢弃的尾部"; reuse across steps:
+ * section "复用精确选择优于重算均值池化"). The blocks a sparse mask drops carry small
+ * but nonzero attention mass; the dense-minus-sparse residual changes across
+ * denoising steps less than the attention output itself. At an anchor step the
+ * caller runs bsa_forward with a full index (every block active) and with the
+ * sparse index, and captures R = O_dense - O_sparse; later steps call
+ * bsa_forward_residual, which returns O_sparse + R (LSE stays the sparse one).
+ *
+ * bsa_residual_capture: R[i] = float(O_dense[i]) - float(O_sparse[i]) for
+ *   i < count, computed in fp32 (exact widening of bf16, one rounding).
+ *   O_dense, O_sparse  device, dtype dt, >= count elements, 16-byte aligned
+ *   R                  device fp32, >= count elements, 16-byte aligned (written)
+ *   count == 0 enqueues nothing. Errors: BSA_ERR_DTYPE, BSA_ERR_INVALID_ARG (null
+ *   or misaligned pointers, negative count), BSA_ERR_CUDA.
+ */
+bsa_status bsa_residual_capture(const void *O_dense, const void *O_sparse, int dt, int64_t count, float *R,
+                                void *stream);
+
+/*
+ * bsa_forward_residual: bsa_forward whose output is O_sparse + R, with R added in
+ * fp32 before the output is rounded to dt. R: device fp32 [B][H][N][d], 16-byte
+ * aligned, read only. Every other argument, the LSE and the error behaviour are
+ * those of bsa_forward; a null or misaligned R is BSA_ERR_INVALID_ARG.
+ */
+bsa_status bsa_forward_residual(const void *Q, const void *K, const void *V, int dt, int B, int H, int N,
+                                int d, int block, const int32_t *row_ptr, const int32_t *col_idx,
+                                const uint32_t *bitmap, int index_mode, float scale, const float *R,
+                                void *O, float *LSE, void *workspace, size_t workspace_bytes,
+                                void *stream);
+
+/*
  * bsa_build_mask_noalloc -- bsa_build_mask without a caller workspace (the pages
  * have no counterpart: this is a convenience of this library).
  *

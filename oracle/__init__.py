@@ -5,7 +5,9 @@ and by the benchmark's CPU-baseline leg. The product path never imports it.
 
 The arithmetic lives in ``bsa_oracle.c`` (plain C, double precision for the
 attention, the fp32 rules of the selector spelled out there). This module
-compiles it with gcc and wraps it with ctypes and numpy.
+compiles it with gcc and wraps it with ctypes and numpy. The residual
+compensation definitions (``residual``, ``compensate``) are one-line numpy
+expressions in double precision.
 """
 from __future__ import annotations
 
@@ -177,3 +179,18 @@ def select_mask(q: np.ndarray, k: np.ndarray, bs: int, density: float) -> np.nda
     kbar = block_mean(k, bs)
     s = block_scores(qbar, kbar)
     return topk_mask(s, topk_count(density, s.shape[-1]))
+
+
+def residual(o_dense: np.ndarray, o_sparse: np.ndarray) -> np.ndarray:
+    """Residual of sparse attention at an anchor step, in double.
+
+    [P3] "Can sparse attention close the quality gap in diffusion transformers",
+    section "残差补偿找回被丢弃的尾部": the dense-minus-sparse residual R = O_dense - O_sparse
+    is measured at an anchor step and reused at later steps.
+    """
+    return np.asarray(o_dense, dtype=np.float64) - np.asarray(o_sparse, dtype=np.float64)
+
+
+def compensate(o_sparse: np.ndarray, r: np.ndarray) -> np.ndarray:
+    """Residual-compensated output of a later step, O_sparse + R, in double (same section)."""
+    return np.asarray(o_sparse, dtype=np.float64) + np.asarray(r, dtype=np.float64)

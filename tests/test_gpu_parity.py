@@ -143,6 +143,77 @@ def test_many_tiles_multi_cta_ordering(flags):
         bb.bsa_debug_config(0, 0)
 
 
+# ------------------------------------------------------------ residual compensation
+#
+# [P3] section "残差补偿找回被丢弃的尾部": R = O_dense - O_sparse at an anchor step, and
+# later steps output O_sparse + R. The capture must equal the fp32 difference bit
+# for bit; the compensated forward of a later step (other inputs) must match the
+# oracle's sparse attention plus the same R; at the anchor it gives the dense output.
+
+RESIDUAL_CASES = {
+    "t2i": wl.scaled(wl.WORKLOADS["t2i_static"], B=1, H=2),
+    "dynamic": wl.scaled(wl.WORKLOADS["dynamic_topk"], H=2, N=2048),
+    "long_bitmap": wl.scaled(wl.WORKLOADS["long_topk"], H=2, N=8192, density=0.25),
+    "tiny_fp32": wl.WORKLOADS["tiny"],
+}
+
+
+def _step(w, inp):
+    q, k, v = (gu.upload(inp, n) for n in ("q", "k", "v"))
+    mask = gu.oracle_mask(w, inp)
+    return q, k, v, mask, gu.device_index(w, q, k, mask)
+
+
+def _full_index(w):
+    """Every KV block active for every Q block: the dense reference of the anchor step."""
+    ones = np.ones((w.B, w.H, w.nQB, w.nKB), dtype=np.uint8)
+    dev = torch.from_numpy(gu.mask_bitmap_words(ones).reshape(-1)).cuda()
+    return bb.build_mask(None, None, w.block, spec=bb.explicit_spec(dev), shape=(w.B, w.H, w.N, w.d))
+
+
+@pytest.mark.parametrize("flags", [0, bb.DBG_SPLIT_ALL])
+@pytest.mark.parametrize("name", sorted(RESIDUAL_CASES))
+def test_residual_compensation_matches_oracle(name, flags):
+    w = RESIDUAL_CASES[name]
+    bb.bsa_debug_config(flags, 0)
+    try:
+        # anchor step: dense (every block active) and sparse outputs, then R
+        inp0 = wl.make_inputs(w)
+        q0, k0, v0, mask0, idx0 = _step(w, inp0)
+        full = np.ones_like(mask0)
+        idx_full = _full_index(w)
+        gu.assert_index_equal(idx_full, full)
+        O_dense, _ = bb.forward(q0, k0, v0, idx_full, index_mode=w.index_mode)
+        O_sparse, _ = bb.forward(q0, k0, v0, idx0, index_mode=w.index_mode)
+        R = bb.residual_capture(O_dense, O_sparse)
+        torch.cuda.synchronize()
+        expect = (O_dense.float() - O_sparse.float()).cpu().numpy()
+        assert np.array_equal(R.cpu().numpy(), expect)  # fp32 difference, bit for bit
+        R_np = R.cpu().numpy().reshape(-1, w.d).astype(np.float64)
+        # at the anchor, compensation gives the dense output (oracle, full mask)
+        O_a, L_a = bb.forward(q0, k0, v0, idx0, index_mode=w.index_mode, residual=R)
+        torch.cuda.synchronize()
+        Od_ref, _ = oracle.attention(inp0["q"], inp0["k"], inp0["v"], full, w.block)
+        err = np.abs(O_a.float().reshape(-1, w.d).cpu().numpy() - Od_ref)
+        assert err.max() <= gu.O_MAX_ABS and err.mean() <= gu.O_MEAN_ABS
+        # a later step: other inputs, the anchor's R
+        inp1 = wl.make_inputs(wl.scaled(w, seed=w.seed + 1000))
+        q1, k1, v1, mask1, idx1 = _step(w, inp1)
+        O1, L1 = bb.forward(q1, k1, v1, idx1, index_mode=w.index_mode, residual=R)
+        torch.cuda.synchronize()
+        Os_ref, L_ref = oracle.attention(inp1["q"], inp1["k"], inp1["v"], mask1, w.block)
+        O_ref = oracle.compensate(Os_ref, R_np)
+        err = np.abs(O1.float().reshape(-1, w.d).cpu().numpy() - O_ref)
+        assert err.max() <= gu.O_MAX_ABS, f"O max-abs {err.max():.3e}"
+        assert err.mean() <= gu.O_MEAN_ABS, f"O mean-abs {err.mean():.3e}"
+        Lg = L1.reshape(-1).cpu().numpy().astype(np.float64)
+        live = ~np.isneginf(L_ref)
+        assert np.array_equal(np.isneginf(Lg), ~live)
+        assert np.abs(Lg[live] - L_ref[live]).max() <= gu.LSE_MAX_ABS  # the LSE stays the sparse one
+    finally:
+        bb.bsa_debug_config(0, 0)
+
+
 @pytest.mark.parametrize("d,block,mode", [(64, 128, 0), (64, 128, 1), (128, 64, 1), (64, 64, 1)])
 def test_shape_combinations(d, block, mode):
     w = wl.scaled(wl.WORKLOADS["long_topk"], H=3, N=2048, d=d, block=block, density=0.3)

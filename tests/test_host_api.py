@@ -25,7 +25,7 @@ def _header_functions():
 
 def test_header_symbols_exported(lib):
     names = _header_functions()
-    assert len(names) == 9
+    assert len(names) == 11
     assert sorted(bb.EXPORTS) == names
     for n in names:
         assert getattr(lib, n) is not None  # dlsym succeeds
@@ -160,3 +160,31 @@ def test_debug_config_roundtrip(lib):
 def test_static_spec_layout_matches_header(lib):
     # int kind; ptr; 4 ints; int[8]; 3 ints  (x86-64 and aarch64 LP64 layout)
     assert ctypes.sizeof(bb.StaticSpec) == 4 + 4 + 8 + 4 * 4 + 4 * 8 + 4 * 3 + 4
+
+
+def _fwd_res(**kw):
+    args = dict(Q=FAKE, K=FAKE, V=FAKE, dt=bb.BF16, B=1, H=2, N=512, d=64, block=64, row_ptr=FAKE,
+                col_idx=FAKE, bitmap=FAKE, index_mode=0, scale=0.0, R=FAKE, O=FAKE, LSE=FAKE, workspace=FAKE,
+                workspace_bytes=1 << 30)
+    args.update(kw)
+    with pytest.raises(bb.BsaError) as e:
+        bb.bsa_forward_residual(**args, stream=0)
+    return e.value.code
+
+
+def test_residual_entry_points_reject_bad_arguments(lib):
+    # bsa_forward_residual: the residual pointer, then every bsa_forward check
+    assert _fwd_res(R=None) == bb.ERR_INVALID_ARG
+    assert _fwd_res(R=FAKE + 4) == bb.ERR_INVALID_ARG  # fp32 rows read 16 bytes at a time
+    assert _fwd_res(N=500) == bb.ERR_SHAPE
+    assert _fwd_res(dt=5) == bb.ERR_DTYPE
+    assert _fwd_res(workspace=None) == bb.ERR_WORKSPACE
+    # bsa_residual_capture
+    for kw, code in [(dict(dt=9), bb.ERR_DTYPE), (dict(count=-1), bb.ERR_INVALID_ARG),
+                     (dict(R=None), bb.ERR_INVALID_ARG), (dict(O_dense=FAKE + 2), bb.ERR_INVALID_ARG)]:
+        args = dict(O_dense=FAKE, O_sparse=FAKE, dt=bb.BF16, count=1024, R=FAKE)
+        args.update(kw)
+        with pytest.raises(bb.BsaError) as e:
+            bb.bsa_residual_capture(**args, stream=0)
+        assert e.value.code == code
+    bb.bsa_residual_capture(None, None, bb.BF16, 0, None, stream=0)  # nothing to do, nothing enqueued

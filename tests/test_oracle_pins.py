@@ -348,3 +348,29 @@ def test_mask_to_index_brute_force():
             for j in range(nKB):
                 assert ((int(bitmap[r, j // 32]) >> (j % 32)) & 1) == mask[r, j]
             assert sum(bin(int(w)).count("1") for w in bitmap[r]) == len(js)
+
+
+# ------------------------------------------------------------ residual compensation
+
+
+def test_residual_and_compensate_hand_values():
+    # R = dense - sparse (not sparse - dense), and compensation adds it
+    r = oracle.residual(np.array([1.0, 2.0, -4.0]), np.array([0.5, 3.0, -4.0]))
+    assert r.tolist() == [0.5, -1.0, 0.0]
+    assert oracle.compensate(np.array([1.0, 1.0, 2.0]), r).tolist() == [1.5, 0.0, 2.0]
+
+
+def test_compensation_at_the_anchor_gives_the_dense_output():
+    rng = np.random.default_rng(7)
+    N, d, bs = 256, 64, 64
+    q, k, v = (rng.standard_normal((1, 1, N, d)) for _ in range(3))
+    nB = N // bs
+    full = np.ones((1, 1, nB, nB), dtype=np.uint8)
+    sparse = np.eye(nB, dtype=np.uint8)[None, None]
+    o_dense, _ = oracle.attention(q, k, v, full, bs)
+    o_sparse, _ = oracle.attention(q, k, v, sparse, bs)
+    r = oracle.residual(o_dense, o_sparse)
+    assert np.abs(r).max() > 0.01  # the dropped blocks matter here
+    np.testing.assert_allclose(oracle.compensate(o_sparse, r), o_dense, rtol=0, atol=1e-14)
+    # a full mask drops nothing: no residual
+    assert np.array_equal(oracle.residual(o_dense, oracle.attention(q, k, v, full, bs)[0]), np.zeros_like(r))
