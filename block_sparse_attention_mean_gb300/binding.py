@@ -38,7 +38,8 @@ MAX_ANCHORS = 8
 # every symbol declared in include/bsa.h
 EXPORTS = ("bsa_build_mask", "bsa_forward", "bsa_mask_nnz", "bsa_workspace_size",
            "bsa_check_device_error", "bsa_validate_index", "bsa_debug_config",
-           "bsa_status_string", "bsa_build_mask_noalloc", "bsa_residual_capture", "bsa_forward_residual")
+           "bsa_status_string", "bsa_build_mask_noalloc", "bsa_residual_capture", "bsa_forward_residual",
+           "bsa_build_mask_modal", "bsa_mask_nnz_modal")
 NOALLOC_SCRATCH_BYTES = 16 << 20  # BSA_NOALLOC_SCRATCH_BYTES
 # bsa_debug_config flag bits
 DBG_STALL = 1       # skip loads and MMAs: the first device wait runs out
@@ -78,6 +79,8 @@ def load():
     lib.bsa_forward.argtypes = [P, P, P, I, I, I, I, I, I, P, P, P, I, F, P, P, P, SZ, P]
     lib.bsa_forward_residual.argtypes = [P, P, P, I, I, I, I, I, I, P, P, P, I, F, P, P, P, P, SZ, P]
     lib.bsa_residual_capture.argtypes = [P, P, I, I64, P, P]
+    lib.bsa_build_mask_modal.argtypes = [P, P, I, I, I, I, I, I, I, P, P, P, I64, P, P, SZ, P]
+    lib.bsa_mask_nnz_modal.argtypes = [I, I, I, I, I, P, ctypes.POINTER(I64)]
     lib.bsa_build_mask_noalloc.argtypes = [P, P, I, I, I, I, I, I, F, ctypes.POINTER(StaticSpec), P, P, I64, P,
                                            P, P]
     lib.bsa_mask_nnz.argtypes = [I, I, I, I, F, ctypes.POINTER(StaticSpec), ctypes.POINTER(I64)]
@@ -147,6 +150,47 @@ def bsa_forward_residual(Q, K, V, dt: int, B: int, H: int, N: int, d: int, block
                                        _ptr(col_idx), _ptr(bitmap), int(index_mode), float(scale), _ptr(R),
                                        _ptr(O), _ptr(LSE), _ptr(workspace), int(workspace_bytes), _stream(stream))
     _check(code, "bsa_forward_residual")
+
+
+def _densities(density) -> ctypes.Array:
+    d4 = [float(x) for x in density]
+    if len(d4) != 4:
+        raise ValueError("density: four values (text->text, text->image, image->text, image->image)")
+    return (ctypes.c_float * 4)(*d4)
+
+
+def bsa_mask_nnz_modal(B: int, H: int, N: int, block: int, n_text_blocks: int, density) -> int:
+    out = ctypes.c_int64(0)
+    _check(load().bsa_mask_nnz_modal(B, H, N, block, n_text_blocks, _densities(density), ctypes.byref(out)),
+           "bsa_mask_nnz_modal")
+    return int(out.value)
+
+
+def bsa_build_mask_modal(Q, K, dt: int, B: int, H: int, N: int, d: int, block: int, n_text_blocks: int, density,
+                         row_ptr, col_idx, col_capacity: int, bitmap, workspace, workspace_bytes: int,
+                         stream=None) -> None:
+    code = load().bsa_build_mask_modal(_ptr(Q), _ptr(K), dt, B, H, N, d, block, int(n_text_blocks),
+                                       _densities(density), _ptr(row_ptr), _ptr(col_idx), int(col_capacity),
+                                       _ptr(bitmap), _ptr(workspace), int(workspace_bytes), _stream(stream))
+    _check(code, "bsa_build_mask_modal")
+
+
+def build_mask_modal(q: torch.Tensor, k: torch.Tensor, block: int, n_text_blocks: int, density,
+                     ws: Optional[torch.Tensor] = None, stream=None) -> "Index":
+    """Per-modality top-k index (bsa_build_mask_modal) with freshly allocated buffers."""
+    B, H, N, d = q.shape
+    nB = N // block
+    W = (nB + 31) // 32
+    nnz = bsa_mask_nnz_modal(B, H, N, block, n_text_blocks, density)
+    row_ptr = torch.empty(B * H * nB + 1, dtype=torch.int32, device=q.device)
+    col_idx = torch.empty(max(nnz, 1), dtype=torch.int32, device=q.device)
+    bitmap = torch.empty(B * H * nB * W, dtype=torch.int32, device=q.device)
+    if ws is None:
+        ws = workspace(0, B, H, N, d, block, q.device)
+    bsa_build_mask_modal(q, k, _dtype_code(q), B, H, N, d, block, n_text_blocks, density, row_ptr, col_idx,
+                         col_idx.numel(), bitmap, ws, ws.numel(), stream)
+    _check(bsa_check_device_error(ws, stream), "bsa_build_mask_modal (device)")
+    return Index(row_ptr, col_idx, bitmap, nnz, block)
 
 
 def bsa_residual_capture(O_dense, O_sparse, dt: int, count: int, R, stream=None) -> None:

@@ -37,6 +37,34 @@ int topk_keep(float density, int nKB)
 
 bool valid_density(float density) { return std::isfinite(density) && density > 0.0f && density <= 1.0f; }
 
+// Per-modality counts ("多模态DiT中的块稀疏注意力" §3.3): a group of n key blocks with
+// density rho keeps max(1, floor(rho * n)) of them (at most n); rho = 0 switches the
+// group off. density = {text->text, text->image, image->text, image->image}.
+int region_keep(float density, int n)
+{
+    if (n <= 0 || density <= 0.0f) return 0;
+    return topk_keep(density, n);
+}
+
+bool valid_modal(int nB, int n_text, const float *density)
+{
+    if (!density || n_text < 0 || n_text > nB) return false;
+    for (int g = 0; g < 4; ++g)
+        if (!std::isfinite(density[g]) || density[g] < 0.0f || density[g] > 1.0f) return false;
+    return true;
+}
+
+// kq[a][b] and the per-(b, h) count for the modality groups
+int64_t modal_counts(int nB, int n_text, const float *density, int kq[2][2])
+{
+    const int n_img = nB - n_text;
+    kq[0][0] = region_keep(density[0], n_text);
+    kq[0][1] = region_keep(density[1], n_img);
+    kq[1][0] = region_keep(density[2], n_text);
+    kq[1][1] = region_keep(density[3], n_img);
+    return static_cast<int64_t>(n_text) * (kq[0][0] + kq[0][1]) + static_cast<int64_t>(n_img) * (kq[1][0] + kq[1][1]);
+}
+
 // Static spec: structural checks; `count` gets the per-(b, h) active block count
 // (band and cuboid only).
 bsa_status check_spec(const bsa_static_spec *s, int nB, int64_t *count)
@@ -100,6 +128,65 @@ const char *bsa_status_string(int status)
     case BSA_ERR_WORKSPACE: return "workspace missing or too small";
     default: return "unknown status";
     }
+}
+
+bsa_status bsa_mask_nnz_modal(int B, int H, int N, int block, int n_text_blocks, const float *density,
+                              int64_t *nnz)
+{
+    if (!nnz) return BSA_ERR_INVALID_ARG;
+    const bsa_status s = check_shape(B, H, N, 64, block);
+    if (s != BSA_OK) return s;
+    const int nB = N / block;
+    if (!valid_modal(nB, n_text_blocks, density)) return BSA_ERR_INVALID_ARG;
+    int kq[2][2];
+    *nnz = static_cast<int64_t>(B) * H * modal_counts(nB, n_text_blocks, density, kq);
+    return BSA_OK;
+}
+
+bsa_status bsa_build_mask_modal(const void *Q, const void *K, int dt, int B, int H, int N, int d, int block,
+                                int n_text_blocks, const float *density, int32_t *row_ptr, int32_t *col_idx,
+                                int64_t col_capacity, uint32_t *bitmap, void *workspace, size_t workspace_bytes,
+                                void *stream)
+{
+    bsa_status s = check_shape(B, H, N, d, block);
+    if (s != BSA_OK) return s;
+    if (dt != BSA_BF16 && dt != BSA_FP32) return BSA_ERR_DTYPE;
+    if (!Q || !K || !aligned(Q, 16) || !aligned(K, 16)) return BSA_ERR_INVALID_ARG;
+    if (!row_ptr || !col_idx || !bitmap || col_capacity < 0) return BSA_ERR_INVALID_ARG;
+    if (!aligned(row_ptr, 4) || !aligned(col_idx, 4) || !aligned(bitmap, 4)) return BSA_ERR_INVALID_ARG;
+    const int nB = N / block;
+    if (!valid_modal(nB, n_text_blocks, density)) return BSA_ERR_INVALID_ARG;
+    if (!workspace || !aligned(workspace, 256) || workspace_bytes < bsa::mask_workspace_bytes(B, H, N, d, block))
+        return BSA_ERR_WORKSPACE;
+    if (nB > bsa::kMaxKvBlocks) return BSA_ERR_UNSUPPORTED;
+    bsa::MaskArgs a{};
+    a.Q = Q;
+    a.K = K;
+    a.dt = dt;
+    a.B = B;
+    a.H = H;
+    a.N = N;
+    a.d = d;
+    a.block = block;
+    a.nQB = nB;
+    a.nKB = nB;
+    a.W = (nB + 31) / 32;
+    a.spec = nullptr;
+    a.row_ptr = row_ptr;
+    a.col_idx = col_idx;
+    a.col_capacity = col_capacity;
+    a.bitmap = bitmap;
+    a.ws = static_cast<char *>(workspace);
+    a.n_text = n_text_blocks;
+    const int64_t nnz = static_cast<int64_t>(B) * H * modal_counts(nB, n_text_blocks, density, a.kq);
+    a.k = 0;
+    if (nnz > col_capacity) return BSA_ERR_CAPACITY;
+    if (nnz > INT32_MAX) return BSA_ERR_UNSUPPORTED;  // row_ptr is int32
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&a.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return BSA_ERR_CUDA;
+    return bsa::launch_build_mask(a, static_cast<cudaStream_t>(stream));
 }
 
 bsa_status bsa_workspace_size(int which, int B, int H, int N, int d, int block, size_t *bytes)
@@ -168,6 +255,8 @@ bsa_status bsa_build_mask(const void *Q, const void *K, int dt, int B, int H, in
         if (!valid_density(density)) return BSA_ERR_INVALID_ARG;
         if (nB > bsa::kMaxKvBlocks) return BSA_ERR_UNSUPPORTED;
         a.k = topk_keep(density, nB);
+        a.n_text = 0;
+        a.kq[1][1] = a.k;
         nnz = R * a.k;
     } else {
         int64_t c = 0;

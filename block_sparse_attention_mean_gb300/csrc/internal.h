@@ -41,7 +41,9 @@ struct MaskArgs {
     const void *Q, *K;
     int dt, B, H, N, d, block;
     int nQB, nKB, W;       // blocks per row/column, bitmap words per row
-    int k;                 // dynamic: blocks kept per row
+    int k;                 // dynamic: blocks kept per row (plain selector)
+    int n_text;            // dynamic: leading text blocks (0 for the plain selector)
+    int kq[2][2];          // dynamic: blocks kept by a query block of modality a among key modality b
     const bsa_static_spec *spec;  // host copy (NULL -> dynamic)
     int32_t *row_ptr, *col_idx;
     int64_t col_capacity;

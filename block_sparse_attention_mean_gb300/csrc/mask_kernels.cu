@@ -104,38 +104,70 @@ __device__ __forceinline__ uint32_t order_key(float s)
 
 // Exact top-k of one row of order keys held in shared memory (one warp): the k
 // largest (key, -index) pairs, written as a bitmap row and an ascending CSR row.
-__device__ void select_row(const uint32_t *row, int nKB, int k, int W, int64_t r_global,
-                           int32_t *__restrict__ col_idx, uint32_t *__restrict__ bitmap, int lane)
+// The k-th largest key of row[lo..hi) by a bitwise radix select (T), and how many
+// keys equal to T to keep (the lowest indices first). k = 0 keeps nothing.
+__device__ void kth_key(const uint32_t *row, int lo, int hi, int k, int lane, uint32_t &T, int &need)
 {
+    if (k <= 0 || lo >= hi) {
+        T = 0xffffffffu;
+        need = 0;
+        return;
+    }
     // Largest T with #{key >= T} >= k: the k-th largest key value.
-    uint32_t T = 0;
+    T = 0;
     for (int bit = 31; bit >= 0; --bit) {
         const uint32_t cand = T | (1u << bit);
         int cnt = 0;
-        for (int j = lane; j < nKB; j += 32) cnt += row[j] >= cand;
+        for (int j = lo + lane; j < hi; j += 32) cnt += row[j] >= cand;
         cnt = __reduce_add_sync(0xffffffffu, cnt);
         if (cnt >= k) T = cand;
     }
     int gt = 0;
-    for (int j = lane; j < nKB; j += 32) gt += row[j] > T;
+    for (int j = lo + lane; j < hi; j += 32) gt += row[j] > T;
     gt = __reduce_add_sync(0xffffffffu, gt);
-    const int need = k - gt;  // how many of the keys equal to T, lowest index first
-    const int64_t out_base = r_global * k;
-    int taken = 0, ties = 0;
+    need = k - gt;
+}
+
+// Top kA keys among the text columns [0, n_text) and top kB among the image
+// columns [n_text, nKB) of one row (ties: lower index first within each group);
+// writes the row's bitmap words and, in ascending order from out_base, its
+// col_idx entries. With n_text = 0 this is the plain top-kB of the row.
+__device__ void select_row(const uint32_t *row, int nKB, int n_text, int kA, int kB, int W, int64_t r_global,
+                           int64_t out_base, int32_t *__restrict__ col_idx, uint32_t *__restrict__ bitmap, int lane)
+{
+    uint32_t TA, TB;
+    int needA, needB;
+    kth_key(row, 0, n_text, kA, lane, TA, needA);
+    kth_key(row, n_text, nKB, kB, lane, TB, needB);
+    int taken = 0, tiesA = 0, tiesB = 0;
     for (int w = 0; w < W; ++w) {
         const int j = w * 32 + lane;
         const uint32_t key = j < nKB ? row[j] : 0u;
+        const bool inA = j < n_text;
+        const uint32_t T = inA ? TA : TB;
         const bool is_gt = j < nKB && key > T;
         const bool is_eq = j < nKB && key == T;
-        const uint32_t eq_mask = __ballot_sync(0xffffffffu, is_eq);
-        const int eq_rank = ties + __popc(eq_mask & lanemask_lt());
-        const bool sel = is_gt || (is_eq && eq_rank < need);
+        const uint32_t eqA = __ballot_sync(0xffffffffu, is_eq && inA);
+        const uint32_t eqB = __ballot_sync(0xffffffffu, is_eq && !inA);
+        const int eq_rank = inA ? tiesA + __popc(eqA & lanemask_lt()) : tiesB + __popc(eqB & lanemask_lt());
+        const bool sel = is_gt || (is_eq && eq_rank < (inA ? needA : needB));
         const uint32_t sel_mask = __ballot_sync(0xffffffffu, sel);
         if (lane == 0) bitmap[r_global * W + w] = sel_mask;
         if (sel) col_idx[out_base + taken + __popc(sel_mask & lanemask_lt())] = j;
         taken += __popc(sel_mask);
-        ties += __popc(eq_mask);
+        tiesA += __popc(eqA);
+        tiesB += __popc(eqB);
     }
+}
+
+// First col_idx slot of row i of head bh when text rows keep Kt blocks and image
+// rows Ki (rows ordered (b, h, i); the first n_text rows of a head are text).
+__device__ __forceinline__ int64_t row_base(int64_t bh, int i, int nQB, int n_text, int Kt, int Ki)
+{
+    const int64_t per_head = static_cast<int64_t>(n_text) * Kt + static_cast<int64_t>(nQB - n_text) * Ki;
+    const int64_t within = i < n_text ? static_cast<int64_t>(i) * Kt
+                                      : static_cast<int64_t>(n_text) * Kt + static_cast<int64_t>(i - n_text) * Ki;
+    return bh * per_head + within;
 }
 
 // Scores of 16 Q blocks against every KV block of one (b, h), then top-k per row.
@@ -145,9 +177,17 @@ __device__ void select_row(const uint32_t *row, int nKB, int k, int W, int64_t r
 constexpr int kScoreRows = 16;
 constexpr int kScoreTile = 128;
 
+// Per-modality counts ("多模态DiT中的块稀疏注意力" §3.3): k[a][b] blocks kept among the
+// key blocks of modality b (0 text, 1 image) by a query block of modality a; the
+// plain selector is n_text = 0 with k[1][1] = k.
+struct RegionK {
+    int n_text;
+    int k[2][2];
+};
+
 __global__ void __launch_bounds__(256) score_topk_kernel(const float *__restrict__ qbar,
                                                          const float *__restrict__ kbar, int nQB,
-                                                         int nKB, int d, int k, int W,
+                                                         int nKB, int d, RegionK rk, int W,
                                                          int32_t *__restrict__ row_ptr,
                                                          int32_t *__restrict__ col_idx,
                                                          uint32_t *__restrict__ bitmap, uint32_t *err)
@@ -223,15 +263,19 @@ __global__ void __launch_bounds__(256) score_topk_kernel(const float *__restrict
     }
     if (nan_seen) raise_error(err, BSA_ERR_NONFINITE);
     __syncthreads();
+    const int Kt = rk.k[0][0] + rk.k[0][1], Ki = rk.k[1][0] + rk.k[1][1];
     for (int a = 0; a < 2; ++a) {
         const int i = i0 + r0 + a;
         if (i >= nQB) break;
         const int64_t r_global = static_cast<int64_t>(bh) * nQB + i;
-        select_row(keys + (r0 + a) * nKB, nKB, k, W, r_global, col_idx, bitmap, lane);
+        const int qm = i < rk.n_text ? 0 : 1;
+        const int64_t base = row_base(bh, i, nQB, rk.n_text, Kt, Ki);
+        select_row(keys + (r0 + a) * nKB, nKB, rk.n_text, rk.k[qm][0], rk.k[qm][1], W, r_global, base, col_idx,
+                   bitmap, lane);
         if (lane == 0) {
-            row_ptr[r_global] = static_cast<int32_t>(r_global * k);
+            row_ptr[r_global] = static_cast<int32_t>(base);
             if (r_global == static_cast<int64_t>(gridDim.y) * nQB - 1)
-                row_ptr[r_global + 1] = static_cast<int32_t>((r_global + 1) * k);
+                row_ptr[r_global + 1] = static_cast<int32_t>(row_base(bh + 1, 0, nQB, rk.n_text, Kt, Ki));
         }
     }
 }
@@ -552,8 +596,12 @@ bsa_status launch_build_mask(const MaskArgs &a, cudaStream_t st)
                                  static_cast<int>(smem)) != cudaSuccess)
             return BSA_ERR_CUDA;
         dim3 sg((a.nQB + kScoreRows - 1) / kScoreRows, static_cast<unsigned>(BH));
-        score_topk_kernel<<<sg, 256, smem, st>>>(qbar, kbar, a.nQB, a.nKB, a.d, a.k, a.W, a.row_ptr,
-                                                 a.col_idx, a.bitmap, err);
+        RegionK rk{};
+        rk.n_text = a.n_text;
+        for (int x = 0; x < 2; ++x)
+            for (int y = 0; y < 2; ++y) rk.k[x][y] = a.kq[x][y];
+        score_topk_kernel<<<sg, 256, smem, st>>>(qbar, kbar, a.nQB, a.nKB, a.d, rk, a.W, a.row_ptr, a.col_idx,
+                                                 a.bitmap, err);
     } else {
         StaticPred pr{};
         pr.kind = a.spec->kind;

@@ -119,6 +119,34 @@ bsa_status bsa_build_mask(const void *Q, const void *K, int dt, int B, int H, in
                           void *stream);
 
 /*
+ * bsa_build_mask_modal -- the dynamic selector of bsa_build_mask with a density per
+ * modality pair ([P1] §3.3: text tokens are few and image patches many, so one
+ * global sparsity starves the text blocks; set the density per group of the
+ * attention matrix instead, and shift it between groups across denoising steps).
+ * Blocks [0, n_text_blocks) are text, the rest image (the static specs' order).
+ *   density[4]  {text->text, text->image, image->text, image->image}, each in [0, 1]:
+ *               a query block of modality a keeps, among the key blocks of modality
+ *               b (n_b of them), the top max(1, floor(density * n_b)) by the pooled
+ *               score (at most n_b; density 0 keeps none), ties to the lower index,
+ *               the same arithmetic as bsa_build_mask. A row keeps the union of
+ *               its two groups.
+ * Rows of the same modality have equal lengths, so row_ptr is exact and
+ * bsa_mask_nnz_modal gives nnz. Other arguments, outputs, workspace and errors as
+ * bsa_build_mask (dynamic); an invalid density or n_text_blocks outside [0, nB]
+ * is BSA_ERR_INVALID_ARG. With n_text_blocks = 0 and density[3] = rho this is
+ * bsa_build_mask(density = rho) bit for bit.
+ */
+bsa_status bsa_build_mask_modal(const void *Q, const void *K, int dt, int B, int H, int N, int d,
+                                int block, int n_text_blocks, const float *density,
+                                int32_t *row_ptr, int32_t *col_idx, int64_t col_capacity,
+                                uint32_t *bitmap, void *workspace, size_t workspace_bytes,
+                                void *stream);
+
+/* Host-only: exact nnz of bsa_build_mask_modal. */
+bsa_status bsa_mask_nnz_modal(int B, int H, int N, int block, int n_text_blocks,
+                              const float *density, int64_t *nnz);
+
+/*
  * bsa_forward -- block-sparse FlashAttention forward ([P1] §4.1 tile loop with the
  * inner KV loop replaced by the active list, §4.3 skipped blocks count as -inf and
  * the output is normalised by the true sum over active blocks only).

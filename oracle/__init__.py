@@ -181,6 +181,43 @@ def select_mask(q: np.ndarray, k: np.ndarray, bs: int, density: float) -> np.nda
     return topk_mask(s, topk_count(density, s.shape[-1]))
 
 
+def modal_counts(density: Sequence[float], n_text: int, nB: int):
+    """Blocks kept by a query block of modality a among the key blocks of modality b.
+
+    [P1] "多模态DiT中的块稀疏注意力：从原理到工程落地" §3.3: a density per modality group
+    instead of one global rate. Blocks [0, n_text) are text (0), the rest image (1);
+    density = (text->text, text->image, image->text, image->image). A group of n
+    key blocks with density rho keeps the selector's count for n blocks, and none
+    when rho is 0 (or the group is empty).
+    """
+    n = (n_text, nB - n_text)
+    kq = [[0, 0], [0, 0]]
+    for a in (0, 1):
+        for b in (0, 1):
+            rho, nb = float(density[2 * a + b]), n[b]
+            kq[a][b] = 0 if (nb == 0 or rho <= 0.0) else topk_count(rho, nb)
+    return kq
+
+
+def select_mask_modal(q: np.ndarray, k: np.ndarray, bs: int, n_text: int, density: Sequence[float]) -> np.ndarray:
+    """Per-modality selector: pool, score, then the top-k of every (query, key) modality group."""
+    qbar = block_mean(q, bs)
+    kbar = block_mean(k, bs)
+    s = block_scores(qbar, kbar)
+    nB = s.shape[-1]
+    kq = modal_counts(density, n_text, nB)
+    spans = ((0, n_text), (n_text, nB))
+    out = np.zeros(s.shape, np.uint8)
+    for a in (0, 1):
+        r0, r1 = spans[a]
+        for b in (0, 1):
+            c0, c1 = spans[b]
+            if kq[a][b] == 0 or r1 <= r0:
+                continue
+            out[..., r0:r1, c0:c1] = topk_mask(np.ascontiguousarray(s[..., r0:r1, c0:c1]), kq[a][b])
+    return out
+
+
 def residual(o_dense: np.ndarray, o_sparse: np.ndarray) -> np.ndarray:
     """Residual of sparse attention at an anchor step, in double.
 

@@ -214,6 +214,48 @@ def test_residual_compensation_matches_oracle(name, flags):
         bb.bsa_debug_config(0, 0)
 
 
+# ------------------------------------------------------------ per-modality top-k
+#
+# [P1] §3.3: a density per (query modality, key modality) group. The index must equal
+# the oracle's bit for bit, and the forward over it must match the oracle.
+
+MODAL_CASES = {
+    # t2i recipe (rank-8 shared component), 2 text blocks: text rows dense over text, half of the image
+    "t2i_text2": (wl.scaled(wl.WORKLOADS["t2i_static"], B=1, H=2, mask=wl.TOPK, density=0.1), 2,
+                  [1.0, 0.5, 0.5, 0.15]),
+    # clustered recipe at d = 128, 4 "text" blocks, one group switched off
+    "dynamic_text4": (wl.scaled(wl.WORKLOADS["dynamic_topk"], H=2, N=2048), 4, [0.75, 0.0, 0.25, 0.2]),
+    # block 128, bitmap index
+    "long_text2": (wl.scaled(wl.WORKLOADS["long_topk"], H=2, N=4096), 2, [1.0, 0.1, 1.0, 0.05]),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MODAL_CASES))
+def test_modal_index_and_forward_match_oracle(name):
+    w, n_text, dens = MODAL_CASES[name]
+    inp = wl.make_inputs(w)
+    q, k, v = (gu.upload(inp, n) for n in ("q", "k", "v"))
+    mask = oracle.select_mask_modal(inp["q"], inp["k"], w.block, n_text, dens)
+    idx = bb.build_mask_modal(q, k, w.block, n_text, dens)
+    assert idx.nnz == int(mask.sum())
+    gu.assert_index_equal(idx, mask)
+    O, L = bb.forward(q, k, v, idx, index_mode=w.index_mode)
+    torch.cuda.synchronize()
+    gu.assert_attention_close(O, L, inp, mask, w)
+
+
+def test_modal_builder_without_text_is_the_plain_selector():
+    w = wl.scaled(wl.WORKLOADS["dynamic_topk"], H=2, N=4096)
+    inp = wl.make_inputs(w)
+    q, k = gu.upload(inp, "q"), gu.upload(inp, "k")
+    plain = bb.build_mask(q, k, w.block, density=w.density, shape=(w.B, w.H, w.N, w.d))
+    modal = bb.build_mask_modal(q, k, w.block, 0, [0.5, 0.5, 0.5, w.density])
+    torch.cuda.synchronize()
+    assert torch.equal(plain.row_ptr, modal.row_ptr)
+    assert torch.equal(plain.col_idx[:plain.nnz], modal.col_idx[:modal.nnz])
+    assert torch.equal(plain.bitmap, modal.bitmap)
+
+
 @pytest.mark.parametrize("d,block,mode", [(64, 128, 0), (64, 128, 1), (128, 64, 1), (64, 64, 1)])
 def test_shape_combinations(d, block, mode):
     w = wl.scaled(wl.WORKLOADS["long_topk"], H=3, N=2048, d=d, block=block, density=0.3)

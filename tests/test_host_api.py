@@ -25,7 +25,7 @@ def _header_functions():
 
 def test_header_symbols_exported(lib):
     names = _header_functions()
-    assert len(names) == 11
+    assert len(names) == 13
     assert sorted(bb.EXPORTS) == names
     for n in names:
         assert getattr(lib, n) is not None  # dlsym succeeds
@@ -188,3 +188,29 @@ def test_residual_entry_points_reject_bad_arguments(lib):
             bb.bsa_residual_capture(**args, stream=0)
         assert e.value.code == code
     bb.bsa_residual_capture(None, None, bb.BF16, 0, None, stream=0)  # nothing to do, nothing enqueued
+
+
+def test_modal_counts_and_rejects_bad_arguments(lib):
+    # 2 text + 64 image blocks (t2i): text rows keep 2 + 32, image rows 1 + 9
+    dens = [1.0, 0.5, 0.5, 0.15]
+    assert bb.bsa_mask_nnz_modal(2, 24, 4224, 64, 2, dens) == 48 * (2 * (2 + 32) + 64 * (1 + 9))
+    assert bb.bsa_mask_nnz_modal(1, 1, 512, 64, 0, [0.5, 0.5, 0.5, 0.25]) == 8 * 2  # the plain selector
+    assert bb.bsa_mask_nnz_modal(1, 1, 512, 64, 8, [0.0, 0.0, 0.0, 0.0]) == 0
+    for bad in ([1.5, 0, 0, 0], [-0.1, 0, 0, 0], [float("nan"), 0, 0, 0]):
+        with pytest.raises(bb.BsaError) as e:
+            bb.bsa_mask_nnz_modal(1, 1, 512, 64, 2, bad)
+        assert e.value.code == bb.ERR_INVALID_ARG
+    with pytest.raises(bb.BsaError) as e:
+        bb.bsa_mask_nnz_modal(1, 1, 512, 64, 9, dens)  # more text blocks than blocks
+    assert e.value.code == bb.ERR_INVALID_ARG
+    args = dict(Q=FAKE, K=FAKE, dt=bb.BF16, B=1, H=2, N=512, d=64, block=64, n_text_blocks=2, density=dens,
+                row_ptr=FAKE, col_idx=FAKE, col_capacity=1 << 20, bitmap=FAKE, workspace=FAKE,
+                workspace_bytes=1 << 30)
+    for kw, code in [(dict(N=500), bb.ERR_SHAPE), (dict(dt=4), bb.ERR_DTYPE), (dict(Q=None), bb.ERR_INVALID_ARG),
+                     (dict(n_text_blocks=-1), bb.ERR_INVALID_ARG), (dict(density=[2.0, 0, 0, 0]), bb.ERR_INVALID_ARG),
+                     (dict(workspace=None), bb.ERR_WORKSPACE), (dict(col_capacity=3), bb.ERR_CAPACITY)]:
+        a = dict(args)
+        a.update(kw)
+        with pytest.raises(bb.BsaError) as e:
+            bb.bsa_build_mask_modal(**a, stream=0)
+        assert e.value.code == code

@@ -374,3 +374,46 @@ def test_compensation_at_the_anchor_gives_the_dense_output():
     np.testing.assert_allclose(oracle.compensate(o_sparse, r), o_dense, rtol=0, atol=1e-14)
     # a full mask drops nothing: no residual
     assert np.array_equal(oracle.residual(o_dense, oracle.attention(q, k, v, full, bs)[0]), np.zeros_like(r))
+
+
+# ------------------------------------------------------------ per-modality top-k
+
+
+def test_modal_counts_rules():
+    # 2 text + 14 image blocks: groups of 2 and 14 key blocks
+    assert oracle.modal_counts([1.0, 0.5, 0.5, 0.15], 2, 16) == [[2, 7], [1, 2]]
+    assert oracle.modal_counts([0.0, 0.0, 1.0, 0.01], 2, 16) == [[0, 0], [2, 1]]  # rho 0 keeps none; >0 keeps >= 1
+    # no text blocks: no text rows and no text columns (the text-row counts are unused)
+    assert oracle.modal_counts([0.3, 0.3, 0.3, 0.3], 0, 8) == [[0, 2], [0, 2]]
+
+
+def test_modal_selection_brute_force():
+    rng = np.random.default_rng(12)
+    nB, n_text = 13, 3
+    scores = rng.integers(-3, 4, size=(2, nB, nB)).astype(np.float32)  # many ties
+    dens = [0.7, 0.3, 0.4, 0.25]
+    kq = oracle.modal_counts(dens, n_text, nB)
+    spans = ((0, n_text), (n_text, nB))
+    got = np.zeros_like(scores, dtype=np.uint8)
+    for a in (0, 1):
+        for b in (0, 1):
+            (r0, r1), (c0, c1) = spans[a], spans[b]
+            if kq[a][b]:
+                got[:, r0:r1, c0:c1] = oracle.topk_mask(np.ascontiguousarray(scores[:, r0:r1, c0:c1]), kq[a][b])
+    for h in range(2):
+        for i in range(nB):
+            a = 0 if i < n_text else 1
+            want = set()
+            for b in (0, 1):
+                c0, c1 = spans[b]
+                order = sorted(range(c0, c1), key=lambda j: (-scores[h, i, j], j))
+                want |= set(order[:kq[a][b]])
+            assert set(np.flatnonzero(got[h, i]).tolist()) == want
+
+
+def test_modal_selector_reduces_to_plain_without_text():
+    rng = np.random.default_rng(3)
+    q, k = rng.standard_normal((2, 1, 1, 512, 64)).astype(np.float32)
+    plain = oracle.select_mask(q, k, 64, 0.3)
+    modal = oracle.select_mask_modal(q, k, 64, 0, [0.9, 0.9, 0.9, 0.3])
+    assert np.array_equal(plain, modal)
