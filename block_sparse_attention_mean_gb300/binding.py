@@ -11,6 +11,7 @@ import math
 import os
 from typing import Optional, Sequence, Tuple
 
+import numpy as np
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -39,7 +40,7 @@ MAX_ANCHORS = 8
 EXPORTS = ("bsa_build_mask", "bsa_forward", "bsa_mask_nnz", "bsa_workspace_size",
            "bsa_check_device_error", "bsa_validate_index", "bsa_debug_config",
            "bsa_status_string", "bsa_build_mask_noalloc", "bsa_residual_capture", "bsa_forward_residual",
-           "bsa_build_mask_modal", "bsa_mask_nnz_modal")
+           "bsa_build_mask_modal", "bsa_mask_nnz_modal", "bsa_build_mask_exact")
 NOALLOC_SCRATCH_BYTES = 16 << 20  # BSA_NOALLOC_SCRATCH_BYTES
 # bsa_debug_config flag bits
 DBG_STALL = 1       # skip loads and MMAs: the first device wait runs out
@@ -81,6 +82,7 @@ def load():
     lib.bsa_residual_capture.argtypes = [P, P, I, I64, P, P]
     lib.bsa_build_mask_modal.argtypes = [P, P, I, I, I, I, I, I, I, P, P, P, I64, P, P, SZ, P]
     lib.bsa_mask_nnz_modal.argtypes = [I, I, I, I, I, P, ctypes.POINTER(I64)]
+    lib.bsa_build_mask_exact.argtypes = [P, P, I, I, I, I, I, I, F, F, P, P, P, I64, P, P, SZ, P]
     lib.bsa_build_mask_noalloc.argtypes = [P, P, I, I, I, I, I, I, F, ctypes.POINTER(StaticSpec), P, P, I64, P,
                                            P, P]
     lib.bsa_mask_nnz.argtypes = [I, I, I, I, F, ctypes.POINTER(StaticSpec), ctypes.POINTER(I64)]
@@ -191,6 +193,33 @@ def build_mask_modal(q: torch.Tensor, k: torch.Tensor, block: int, n_text_blocks
                          col_idx.numel(), bitmap, ws, ws.numel(), stream)
     _check(bsa_check_device_error(ws, stream), "bsa_build_mask_modal (device)")
     return Index(row_ptr, col_idx, bitmap, nnz, block)
+
+
+def bsa_build_mask_exact(Q, K, dt: int, B: int, H: int, N: int, d: int, block: int, density: float, scale: float,
+                         LSE, row_ptr, col_idx, col_capacity: int, bitmap, workspace, workspace_bytes: int,
+                         stream=None) -> None:
+    code = load().bsa_build_mask_exact(_ptr(Q), _ptr(K), dt, B, H, N, d, block, float(density), float(scale),
+                                       _ptr(LSE), _ptr(row_ptr), _ptr(col_idx), int(col_capacity), _ptr(bitmap),
+                                       _ptr(workspace), int(workspace_bytes), _stream(stream))
+    _check(code, "bsa_build_mask_exact")
+
+
+def build_mask_exact(q: torch.Tensor, k: torch.Tensor, lse_dense: torch.Tensor, block: int, density: float,
+                     scale: float = 0.0, ws: Optional[torch.Tensor] = None, stream=None):
+    """Block-oracle index from the dense LSE (bsa_build_mask_exact); returns (Index, workspace)."""
+    B, H, N, d = q.shape
+    nB = N // block
+    W = (nB + 31) // 32
+    kk = max(1, min(nB, int(math.floor(float(np.float32(density)) * nB))))
+    row_ptr = torch.empty(B * H * nB + 1, dtype=torch.int32, device=q.device)
+    col_idx = torch.empty(B * H * nB * kk, dtype=torch.int32, device=q.device)
+    bitmap = torch.empty(B * H * nB * W, dtype=torch.int32, device=q.device)
+    if ws is None:
+        ws = workspace(2, B, H, N, d, block, q.device)
+    bsa_build_mask_exact(q, k, _dtype_code(q), B, H, N, d, block, density, scale, lse_dense, row_ptr, col_idx,
+                         col_idx.numel(), bitmap, ws, ws.numel(), stream)
+    _check(bsa_check_device_error(ws, stream), "bsa_build_mask_exact (device)")
+    return Index(row_ptr, col_idx, bitmap, col_idx.numel(), block), ws
 
 
 def bsa_residual_capture(O_dense, O_sparse, dt: int, count: int, R, stream=None) -> None:

@@ -189,6 +189,50 @@ bsa_status bsa_build_mask_modal(const void *Q, const void *K, int dt, int B, int
     return bsa::launch_build_mask(a, static_cast<cudaStream_t>(stream));
 }
 
+bsa_status bsa_build_mask_exact(const void *Q, const void *K, int dt, int B, int H, int N, int d, int block,
+                                float density, float scale, const float *LSE, int32_t *row_ptr, int32_t *col_idx,
+                                int64_t col_capacity, uint32_t *bitmap, void *workspace, size_t workspace_bytes,
+                                void *stream)
+{
+    bsa_status s = check_shape(B, H, N, d, block);
+    if (s != BSA_OK) return s;
+    if (dt == BSA_FP32) return BSA_ERR_UNSUPPORTED;  // the mass pass runs on bf16 tensor cores
+    if (dt != BSA_BF16) return BSA_ERR_DTYPE;
+    if (!Q || !K || !LSE || !aligned(Q, 16) || !aligned(K, 16) || !aligned(LSE, 4)) return BSA_ERR_INVALID_ARG;
+    if (!row_ptr || !col_idx || !bitmap || col_capacity < 0) return BSA_ERR_INVALID_ARG;
+    if (!aligned(row_ptr, 4) || !aligned(col_idx, 4) || !aligned(bitmap, 4)) return BSA_ERR_INVALID_ARG;
+    if (!valid_density(density)) return BSA_ERR_INVALID_ARG;
+    if (std::isnan(scale) || std::isinf(scale)) return BSA_ERR_INVALID_ARG;
+    if (!workspace || !aligned(workspace, 256) || workspace_bytes < bsa::exact_workspace_bytes(B, H, N, d, block))
+        return BSA_ERR_WORKSPACE;
+    const int nB = N / block;
+    if (nB > bsa::kMaxKvBlocks) return BSA_ERR_UNSUPPORTED;
+    const int64_t R = static_cast<int64_t>(B) * H * nB;
+    bsa::ExactArgs a{};
+    a.Q = Q;
+    a.K = K;
+    a.B = B;
+    a.H = H;
+    a.N = N;
+    a.d = d;
+    a.block = block;
+    a.nQB = nB;
+    a.nKB = nB;
+    a.W = (nB + 31) / 32;
+    a.k = topk_keep(density, nB);
+    a.scale = scale > 0.0f ? scale : static_cast<float>(1.0 / std::sqrt(static_cast<double>(d)));
+    a.LSE = LSE;
+    a.row_ptr = row_ptr;
+    a.col_idx = col_idx;
+    a.bitmap = bitmap;
+    a.ws = static_cast<char *>(workspace);
+    a.wait_limit_ns = g_wait_limit_ns;
+    const int64_t nnz = R * a.k;
+    if (nnz > col_capacity) return BSA_ERR_CAPACITY;
+    if (nnz > INT32_MAX) return BSA_ERR_UNSUPPORTED;  // row_ptr is int32
+    return bsa::launch_build_mask_exact(a, static_cast<cudaStream_t>(stream));
+}
+
 bsa_status bsa_workspace_size(int which, int B, int H, int N, int d, int block, size_t *bytes)
 {
     if (!bytes) return BSA_ERR_INVALID_ARG;
@@ -196,6 +240,7 @@ bsa_status bsa_workspace_size(int which, int B, int H, int N, int d, int block, 
     if (s != BSA_OK) return s;
     if (which == 0) *bytes = bsa::mask_workspace_bytes(B, H, N, d, block);
     else if (which == 1) *bytes = bsa::fwd_workspace_bytes(B, H, N, d, block);
+    else if (which == 2) *bytes = bsa::exact_workspace_bytes(B, H, N, d, block);
     else return BSA_ERR_INVALID_ARG;
     return BSA_OK;
 }

@@ -40,6 +40,7 @@
 
 #include "internal.h"
 #include "ptx.cuh"
+#include "sync.cuh"
 #include "walk.cuh"
 
 namespace bsa {
@@ -173,51 +174,6 @@ __device__ __forceinline__ uint32_t step_desc(int cnt, const uint32_t (&ms)[2], 
 __device__ __forceinline__ int desc_count(uint32_t d) { return static_cast<int>(d & 3u); }
 __device__ __forceinline__ uint32_t desc_members(uint32_t d, int q) { return (d >> (2 + 2 * q)) & 3u; }
 __device__ __forceinline__ bool desc_last(uint32_t d) { return (d & 64u) != 0u; }
-
-struct Ctl {
-    volatile uint32_t *abort_flag;
-    uint32_t *err;
-    unsigned long long limit;
-};
-
-// Bounded wait on an mbarrier phase. Gives up (and raises the abort flag and
-// BSA_ERR_TIMEOUT) after `limit` ns, or early when another role aborted.
-__device__ __noinline__ bool wait_bar_slow(uint32_t bar, uint32_t parity, const Ctl &c)
-{
-    const uint64_t t0 = globaltimer_ns();
-    for (;;) {
-        // sleeps in hardware until the phase completes or ~50 us pass
-        if (mbar_try_wait_sleep(bar, parity, 50000u)) return true;
-        if (*c.abort_flag) return false;
-        if (globaltimer_ns() - t0 > c.limit) {
-            *c.abort_flag = 1u;
-            raise_error(c.err, BSA_ERR_TIMEOUT);
-            return false;
-        }
-    }
-}
-
-__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Ctl &c)
-{
-    return mbar_try_wait(bar, parity) || wait_bar_slow(bar, parity, c);
-}
-
-// Bounded wait used while draining in-flight async work on the way out; it
-// ignores the abort flag.
-__device__ __noinline__ bool wait_bar_drain(uint32_t bar, uint32_t parity, unsigned long long limit)
-{
-    const uint64_t t0 = globaltimer_ns();
-    while (!mbar_try_wait_sleep(bar, parity, 50000u))
-        if (globaltimer_ns() - t0 > limit) return false;
-    return true;
-}
-
-// Every lane waits (and acquires) itself; the verdict is made warp-uniform by a vote.
-// (Cheaper than one lane waiting while the others park on a shuffle.)
-__device__ __forceinline__ bool warp_wait_all(uint32_t bar, uint32_t parity, const Ctl &c)
-{
-    return __all_sync(0xffffffffu, wait_bar(bar, parity, c) ? 1 : 0) != 0;
-}
 
 // warp_wait_all for S buffer `b`, then the step descriptor written before it.
 // Returns 0xFFFFFFFF when the wait failed.
@@ -1568,38 +1524,6 @@ __global__ void __launch_bounds__(1024) tile_order_small_kernel(TcParams p, Orde
 
 // ---------------------------------------------------------------- host side
 
-typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
-                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn()
-{
-    static EncodeTiledFn fn = nullptr;
-    if (!fn) {
-        void *ptr = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(ptr);
-    }
-    return fn;
-}
-
-// 2-D view [rows][d] of a bf16 tensor, 64-column x box_rows boxes, 128-byte swizzle.
-bool make_map(CUtensorMap *m, const void *base, uint64_t rows, int d, int box_rows)
-{
-    EncodeTiledFn fn = encode_fn();
-    if (!fn) return false;
-    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows)};
-    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(d) * 2};
-    const cuuint32_t box[2] = {64u, static_cast<cuuint32_t>(box_rows)};
-    const cuuint32_t es[2] = {1u, 1u};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, es,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 // Forward workspace: header, item list, per-tile lengths and partial slots, merge
 // counters, then the partial results of split tiles (all 256-byte aligned).
 struct FwdLayout {
@@ -1667,7 +1591,8 @@ bsa_status launch_tc(const FwdArgs &a, cudaStream_t st)
     const int64_t BH = static_cast<int64_t>(a.B) * a.H;
     const uint64_t rows = static_cast<uint64_t>(BH) * a.N;
     CUtensorMap mq, mk, mv;
-    if (!make_map(&mq, a.Q, rows, D, kTileM) || !make_map(&mk, a.K, rows, D, BS) || !make_map(&mv, a.V, rows, D, BS))
+    if (!make_tma_map_bf16(&mq, a.Q, rows, D, kTileM) || !make_tma_map_bf16(&mk, a.K, rows, D, BS) ||
+        !make_tma_map_bf16(&mv, a.V, rows, D, BS))
         return BSA_ERR_CUDA;
     WsHeader *hdr = reinterpret_cast<WsHeader *>(a.ws);
     TcParams p{};
@@ -1733,6 +1658,40 @@ bsa_status launch_forward_tc(const FwdArgs &a, cudaStream_t st)
     if (a.d == 64 && a.block == 128) return launch_tc<64, 128, 5, 6, 3, 2, 2, 1, 1>(a, st);
     if (a.d == 128 && a.block == 128) return launch_tc<128, 128, 2, 4, 3, 1, 2, 1, 1>(a, st);
     return BSA_ERR_SHAPE;
+}
+
+// ---------------------------------------------------------------- TMA descriptors
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn()
+{
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    }
+    return fn;
+}
+
+// 2-D view [rows][d] of a bf16 tensor, 64-column x box_rows boxes, 128-byte swizzle.
+bool make_tma_map_bf16(CUtensorMap *m, const void *base, uint64_t rows, int d, int box_rows)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(d) * 2};
+    const cuuint32_t box[2] = {64u, static_cast<cuuint32_t>(box_rows)};
+    const cuuint32_t es[2] = {1u, 1u};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace bsa

@@ -6,6 +6,8 @@
 #include <cstddef>
 #include <cstdint>
 
+#include <cuda.h>
+
 #include "../../include/bsa.h"
 
 namespace bsa {
@@ -57,6 +59,25 @@ bsa_status launch_build_mask(const MaskArgs &a, cudaStream_t st);
 bsa_status launch_validate_index(int R, int nKB, const int32_t *row_ptr, const int32_t *col_idx,
                                  const uint32_t *bitmap, char *ws, cudaStream_t st);
 
+// ------------------------------------------------------------ exact block-mass selector
+struct ExactArgs {
+    const void *Q, *K;
+    int B, H, N, d, block;
+    int nQB, nKB, W;
+    int k;                 // blocks kept per Q block
+    float scale;           // > 0
+    const float *LSE;      // dense logsumexp per query row (natural log)
+    int32_t *row_ptr, *col_idx;
+    uint32_t *bitmap;
+    char *ws;
+    uint64_t wait_limit_ns;
+};
+
+size_t exact_workspace_bytes(int B, int H, int N, int d, int block);
+bsa_status launch_build_mask_exact(const ExactArgs &a, cudaStream_t st);
+// top-k of the block masses whose partials (4 per 128-row tile, warp order) are at `part`
+bsa_status launch_mass_select(const float *part, const ExactArgs &a, int tiles_per_bh, cudaStream_t st);
+
 // ------------------------------------------------------------ forward
 struct FwdArgs {
     const void *Q, *K, *V;
@@ -75,6 +96,8 @@ struct FwdArgs {
 };
 
 size_t fwd_workspace_bytes(int B, int H, int N, int d, int block);
+// 2-D TMA view [rows][d] of a bf16 tensor with 64-column x box_rows boxes and 128-byte swizzle
+bool make_tma_map_bf16(CUtensorMap *m, const void *base, uint64_t rows, int d, int box_rows);
 bsa_status launch_forward_tc(const FwdArgs &a, cudaStream_t st);    // bf16, tcgen05
 bsa_status launch_forward_simt(const FwdArgs &a, cudaStream_t st);  // fp32, CUDA cores
 bsa_status launch_residual_capture(const void *dense, const void *sparse, int dt, int64_t count, float *R,

@@ -632,6 +632,63 @@ bsa_status launch_build_mask(const MaskArgs &a, cudaStream_t st)
     return cudaGetLastError() == cudaSuccess ? BSA_OK : BSA_ERR_CUDA;
 }
 
+// ------------------------------------------------------------ exact block-mass selection
+//
+// One warp per row (b, h, i): the block masses of the row are the sum of its Q block's
+// partials in a fixed order (warps 2h, 2h + 1 of the tile at block size 64, warps
+// 0..3 at 128), then the same exact top-k as the mean-pooled selector.
+constexpr int kSelWarps = 8;
+
+__global__ void __launch_bounds__(kSelWarps * 32) mass_select_kernel(const float *__restrict__ part, int64_t R,
+                                                                     int nQB, int nKB, int BS, int tiles_per_bh, int k,
+                                                                     int W, int32_t *__restrict__ row_ptr,
+                                                                     int32_t *__restrict__ col_idx,
+                                                                     uint32_t *__restrict__ bitmap, uint32_t *err)
+{
+    extern __shared__ uint32_t sel_keys[];  // [kSelWarps][nKB]
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t r = static_cast<int64_t>(blockIdx.x) * kSelWarps + warp;
+    if (r >= R) return;
+    uint32_t *keys = sel_keys + warp * nKB;
+    const int64_t bh = r / nQB;
+    const int i = static_cast<int>(r % nQB);
+    const int qt = BS == 128 ? i : i / 2;
+    const float *base = part + (bh * tiles_per_bh + qt) * 4 * static_cast<int64_t>(nKB);
+    bool nan_seen = false;
+    for (int j = lane; j < nKB; j += 32) {
+        float m;
+        if (BS == 128) {
+            m = ((base[j] + base[nKB + j]) + base[2 * nKB + j]) + base[3 * nKB + j];
+        } else {
+            const int h = i % 2;
+            m = base[(2 * h) * nKB + j] + base[(2 * h + 1) * nKB + j];
+        }
+        nan_seen |= isnan(m);
+        keys[j] = order_key(m);
+    }
+    if (__any_sync(0xffffffffu, nan_seen) && lane == 0) raise_error(err, BSA_ERR_NONFINITE);
+    __syncwarp();
+    select_row(keys, nKB, 0, 0, k, W, r, r * k, col_idx, bitmap, lane);
+    if (lane == 0) {
+        row_ptr[r] = static_cast<int32_t>(r * k);
+        if (r == R - 1) row_ptr[R] = static_cast<int32_t>(R * k);
+    }
+}
+
+bsa_status launch_mass_select(const float *part, const ExactArgs &a, int tiles_per_bh, cudaStream_t st)
+{
+    const int64_t R = static_cast<int64_t>(a.B) * a.H * a.nQB;
+    const size_t smem = sizeof(uint32_t) * kSelWarps * a.nKB;
+    if (cudaFuncSetAttribute(mass_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem)) != cudaSuccess)
+        return BSA_ERR_CUDA;
+    const unsigned g = static_cast<unsigned>((R + kSelWarps - 1) / kSelWarps);
+    mass_select_kernel<<<g, kSelWarps * 32, smem, st>>>(part, R, a.nQB, a.nKB, a.block, tiles_per_bh, a.k, a.W,
+                                                        a.row_ptr, a.col_idx, a.bitmap,
+                                                        reinterpret_cast<uint32_t *>(a.ws));
+    return cudaGetLastError() == cudaSuccess ? BSA_OK : BSA_ERR_CUDA;
+}
+
 bsa_status launch_validate_index(int R, int nKB, const int32_t *row_ptr, const int32_t *col_idx,
                                  const uint32_t *bitmap, char *ws, cudaStream_t st)
 {

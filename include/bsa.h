@@ -147,6 +147,27 @@ bsa_status bsa_mask_nnz_modal(int B, int H, int N, int block, int n_text_blocks,
                               const float *density, int64_t *nnz);
 
 /*
+ * bsa_build_mask_exact -- the block-oracle selector of [P3] (section "质量差距有三个可
+ * 分离来源": at the same density, keep the blocks that retain the most attention mass
+ * under the exact dense attention). Pass 1 is the caller's: LSE of the dense
+ * attention (bsa_forward with every block active). This call is pass 2 and the
+ * selection: mass_ij = sum over rows r of Q block i and keys c of KV block j of
+ * exp(scale * q_r . k_c - LSE_r) (a dense QK^T on tensor cores, fp32 sums), then the
+ * top k = max(1, floor(density * nKB)) blocks per Q block by mass, ties to the lower
+ * index; CSR and bitmap as bsa_build_mask. Work: 2 * N^2 * d FLOPs per head.
+ *   Q, K        device [B][H][N][d] bf16 (BSA_FP32 is BSA_ERR_UNSUPPORTED), 16-byte aligned
+ *   scale       the attention's softmax scale; <= 0 selects 1/sqrt(d)
+ *   LSE         device fp32 [B][H][N], the dense logsumexp (natural log) of pass 1
+ *   workspace   device, >= bsa_workspace_size(2, ...) bytes, 256-byte aligned
+ * nnz = B*H*nQB*k. Errors as bsa_build_mask; a NaN mass is BSA_ERR_NONFINITE.
+ */
+bsa_status bsa_build_mask_exact(const void *Q, const void *K, int dt, int B, int H, int N, int d,
+                                int block, float density, float scale, const float *LSE,
+                                int32_t *row_ptr, int32_t *col_idx, int64_t col_capacity,
+                                uint32_t *bitmap, void *workspace, size_t workspace_bytes,
+                                void *stream);
+
+/*
  * bsa_forward -- block-sparse FlashAttention forward ([P1] §4.1 tile loop with the
  * inner KV loop replaced by the active list, §4.3 skipped blocks count as -inf and
  * the output is normalised by the true sum over active blocks only).
@@ -238,7 +259,8 @@ bsa_status bsa_build_mask_noalloc(const void *Q, const void *K, int dt, int B, i
 bsa_status bsa_mask_nnz(int B, int H, int N, int block, float density,
                         const bsa_static_spec *spec, int64_t *nnz);
 
-/* Host-only: workspace bytes for which = 0 (bsa_build_mask) or 1 (bsa_forward). */
+/* Host-only: workspace bytes for which = 0 (bsa_build_mask, bsa_build_mask_modal),
+ * 1 (bsa_forward, bsa_forward_residual) or 2 (bsa_build_mask_exact). */
 bsa_status bsa_workspace_size(int which, int B, int H, int N, int d, int block, size_t *bytes);
 
 /* Synchronises `stream`, returns the device-raised status recorded in `workspace`

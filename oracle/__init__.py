@@ -218,6 +218,34 @@ def select_mask_modal(q: np.ndarray, k: np.ndarray, bs: int, n_text: int, densit
     return out
 
 
+def block_mass(q: np.ndarray, k: np.ndarray, lse: np.ndarray, bs: int, scale: Optional[float] = None) -> np.ndarray:
+    """Exact attention mass of every (Q block, KV block) pair, in double.
+
+    [P3] "Can sparse attention close the quality gap in diffusion transformers",
+    section "质量差距有三个可分离来源" (the oracle selectors): with the dense row
+    logsumexp LSE_r, mass_ij = sum over rows r of Q block i and keys c of KV block j
+    of exp(scale * q_r . k_c - LSE_r). Returns [..., nQB, nKB].
+    """
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    *lead, N, d = q.shape
+    sc = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    nB = N // bs
+    out = np.empty((*lead, nB, nB))
+    qf, kf = q.reshape(-1, N, d), k.reshape(-1, N, d)
+    lf = np.asarray(lse, dtype=np.float64).reshape(-1, N)
+    of = out.reshape(-1, nB, nB)
+    for h in range(qf.shape[0]):
+        p = np.exp(sc * (qf[h] @ kf[h].T) - lf[h][:, None])
+        of[h] = p.reshape(nB, bs, nB, bs).sum(axis=(1, 3))
+    return out
+
+
+def select_mask_exact(mass: np.ndarray, density: float) -> np.ndarray:
+    """The block-oracle selector: top-k blocks per Q block by mass (ties -> lower index)."""
+    return topk_mask(np.asarray(mass, dtype=np.float32), topk_count(density, mass.shape[-1]))
+
+
 def residual(o_dense: np.ndarray, o_sparse: np.ndarray) -> np.ndarray:
     """Residual of sparse attention at an anchor step, in double.
 

@@ -256,6 +256,99 @@ def test_modal_builder_without_text_is_the_plain_selector():
     assert torch.equal(plain.bitmap, modal.bitmap)
 
 
+# ------------------------------------------------------------ block-oracle selector
+#
+# [P3] section "质量差距有三个可分离来源": keep the blocks with the most exact attention
+# mass. Pass 1 is the dense LSE; bsa_build_mask_exact is pass 2 and the selection.
+# The masses are floating point, so the selection is checked for validity: every
+# kept block is within the tolerance of the k-th largest mass, and rows whose k-th
+# and (k+1)-th masses are clearly apart select exactly the oracle's blocks.
+
+EXACT_CASES = {
+    "d64_bs64": (wl.scaled(wl.WORKLOADS["t2i_static"], B=1, H=2, N=2048), 0.15),
+    "d128_bs64": (wl.scaled(wl.WORKLOADS["dynamic_topk"], H=2, N=2048), 0.15),
+    "d64_bs128": (wl.scaled(wl.WORKLOADS["t2i_static"], B=1, H=2, N=2048, block=128), 0.25),
+    "d128_bs128": (wl.scaled(wl.WORKLOADS["long_topk"], H=2, N=4096), 0.1),
+}
+MASS_RTOL = 2e-3
+
+
+def _gpu_masses(ws, w):
+    """Block masses from the selector's workspace partials, summed in the kernel's order."""
+    BH, nB, tpb = w.B * w.H, w.nQB, (w.N + 127) // 128
+    part = ws[256:256 + BH * tpb * 4 * nB * 4].view(torch.float32).reshape(BH, tpb, 4, nB).cpu().numpy()
+    out = np.empty((BH, nB, nB), np.float32)
+    for i in range(nB):
+        if w.block == 128:
+            p = part[:, i]
+            out[:, i] = ((p[:, 0] + p[:, 1]) + p[:, 2]) + p[:, 3]
+        else:
+            h = i % 2
+            out[:, i] = part[:, i // 2, 2 * h] + part[:, i // 2, 2 * h + 1]
+    return out
+
+
+def _check_selection(idx, mass_ref, k):
+    """Counts, bitmap/CSR agreement, and the kept set against the exact masses."""
+    R, nB = int(np.prod(mass_ref.shape[:-1])), mass_ref.shape[-1]
+    rp = idx.row_ptr.cpu().numpy()
+    ci = idx.col_idx.cpu().numpy()
+    assert np.array_equal(rp, np.arange(R + 1) * k)
+    m = mass_ref.reshape(R, nB)
+    sel = np.zeros((R, nB), np.uint8)
+    exact_rows = 0
+    for r in range(R):
+        cols = ci[rp[r]:rp[r + 1]]
+        assert np.all(np.diff(cols) > 0)
+        sel[r, cols] = 1
+        order = np.sort(m[r])[::-1]
+        kth = order[k - 1]
+        tol = MASS_RTOL * kth
+        assert np.all(m[r, cols] >= kth - tol), f"row {r} keeps a block below the k-th mass"
+        if k < nB and order[k - 1] - order[k] > 2 * tol:
+            exact_rows += 1
+            assert set(cols.tolist()) == set(np.argsort(-m[r], kind="stable")[:k].tolist())
+    assert np.array_equal(idx.bitmap.cpu().numpy().view(np.uint32),
+                          wl.pack_bitmap_words(sel.reshape(mass_ref.shape)).reshape(-1).view(np.uint32))
+    assert exact_rows > R // 2  # most rows have no near tie at the boundary
+    return sel
+
+
+@pytest.mark.parametrize("name", sorted(EXACT_CASES))
+def test_exact_selector_masses_and_selection(name):
+    w, density = EXACT_CASES[name]
+    inp = wl.make_inputs(w)
+    q, k = gu.upload(inp, "q"), gu.upload(inp, "k")
+    full = np.ones((w.B, w.H, w.nQB, w.nKB), dtype=np.uint8)
+    _, lse = oracle.attention(inp["q"], inp["k"], inp["k"], full, w.block)  # pass 1 in double
+    lse_dev = torch.from_numpy(lse.astype(np.float32)).cuda()
+    idx, ws = bb.build_mask_exact(q, k, lse_dev, w.block, density)
+    torch.cuda.synchronize()
+    mass_ref = oracle.block_mass(inp["q"], inp["k"], lse, w.block)
+    np.testing.assert_allclose(_gpu_masses(ws, w), mass_ref.reshape(-1, w.nQB, w.nKB), rtol=MASS_RTOL,
+                               atol=1e-6 * w.block)
+    _check_selection(idx, mass_ref, oracle.topk_count(density, w.nKB))
+
+
+def test_exact_selector_end_to_end_with_gpu_pass_one():
+    # pass 1 on the GPU (dense forward), pass 2 + selection, then the sparse forward on that index
+    w, density = EXACT_CASES["d128_bs64"]
+    inp = wl.make_inputs(w)
+    q, k, v = (gu.upload(inp, n) for n in ("q", "k", "v"))
+    ones = np.ones((w.B, w.H, w.nQB, w.nKB), dtype=np.uint8)
+    dense_idx = bb.build_mask(None, None, w.block, spec=bb.explicit_spec(
+        torch.from_numpy(gu.mask_bitmap_words(ones).reshape(-1)).cuda()), shape=(w.B, w.H, w.N, w.d))
+    _, lse_dense = bb.forward(q, k, v, dense_idx)
+    idx, _ = bb.build_mask_exact(q, k, lse_dense, w.block, density)
+    torch.cuda.synchronize()
+    _, lse = oracle.attention(inp["q"], inp["k"], inp["k"], ones, w.block)
+    sel = _check_selection(idx, oracle.block_mass(inp["q"], inp["k"], lse, w.block),
+                           oracle.topk_count(density, w.nKB))
+    O, L = bb.forward(q, k, v, idx, index_mode=w.index_mode)
+    torch.cuda.synchronize()
+    gu.assert_attention_close(O, L, inp, sel, w)
+
+
 @pytest.mark.parametrize("d,block,mode", [(64, 128, 0), (64, 128, 1), (128, 64, 1), (64, 64, 1)])
 def test_shape_combinations(d, block, mode):
     w = wl.scaled(wl.WORKLOADS["long_topk"], H=3, N=2048, d=d, block=block, density=0.3)

@@ -25,7 +25,7 @@ def _header_functions():
 
 def test_header_symbols_exported(lib):
     names = _header_functions()
-    assert len(names) == 13
+    assert len(names) == 14
     assert sorted(bb.EXPORTS) == names
     for n in names:
         assert getattr(lib, n) is not None  # dlsym succeeds
@@ -58,7 +58,7 @@ def test_workspace_sizes(lib):
         bb.bsa_workspace_size(1, 1, 1, 100, 64, 64)
     assert e.value.code == bb.ERR_SHAPE
     with pytest.raises(bb.BsaError) as e:
-        bb.bsa_workspace_size(2, 1, 1, 128, 64, 64)
+        bb.bsa_workspace_size(3, 1, 1, 128, 64, 64)  # 0 mask, 1 forward, 2 exact selector
     assert e.value.code == bb.ERR_INVALID_ARG
 
 
@@ -213,4 +213,22 @@ def test_modal_counts_and_rejects_bad_arguments(lib):
         a.update(kw)
         with pytest.raises(bb.BsaError) as e:
             bb.bsa_build_mask_modal(**a, stream=0)
+        assert e.value.code == code
+
+
+def test_exact_selector_workspace_and_bad_arguments(lib):
+    up = lambda x: (x + 255) // 256 * 256  # noqa: E731
+    # partial masses: 4 per 128-row tile and KV block
+    assert bb.bsa_workspace_size(2, 1, 24, 8192, 128, 64) == 256 + up(24 * 64 * 4 * 128 * 4)
+    args = dict(Q=FAKE, K=FAKE, dt=bb.BF16, B=1, H=2, N=512, d=64, block=64, density=0.25, scale=0.0, LSE=FAKE,
+                row_ptr=FAKE, col_idx=FAKE, col_capacity=1 << 20, bitmap=FAKE, workspace=FAKE,
+                workspace_bytes=1 << 30)
+    for kw, code in [(dict(dt=bb.FP32), bb.ERR_UNSUPPORTED), (dict(dt=7), bb.ERR_DTYPE),
+                     (dict(LSE=None), bb.ERR_INVALID_ARG), (dict(density=0.0), bb.ERR_INVALID_ARG),
+                     (dict(scale=float("inf")), bb.ERR_INVALID_ARG), (dict(N=500), bb.ERR_SHAPE),
+                     (dict(workspace_bytes=16), bb.ERR_WORKSPACE), (dict(col_capacity=15), bb.ERR_CAPACITY)]:
+        a = dict(args)
+        a.update(kw)
+        with pytest.raises(bb.BsaError) as e:
+            bb.bsa_build_mask_exact(**a, stream=0)
         assert e.value.code == code

@@ -417,3 +417,44 @@ def test_modal_selector_reduces_to_plain_without_text():
     plain = oracle.select_mask(q, k, 64, 0.3)
     modal = oracle.select_mask_modal(q, k, 64, 0, [0.9, 0.9, 0.9, 0.3])
     assert np.array_equal(plain, modal)
+
+
+# ------------------------------------------------------------ exact block mass (block-oracle selector)
+
+
+def _dense_lse(q, k):
+    nB = q.shape[-2] // 64
+    full = np.ones((*q.shape[:-2], nB, nB), dtype=np.uint8)
+    _, lse = oracle.attention(q, k, k, full, 64)
+    return lse.reshape(q.shape[:-1])
+
+
+def test_block_mass_rows_hold_one_unit_per_query_row():
+    # with the dense LSE every query row's probabilities sum to 1: a Q block's masses sum to bs
+    rng = np.random.default_rng(21)
+    q, k = rng.standard_normal((2, 1, 2, 256, 64)).astype(np.float32)  # the inputs both functions see
+    m = oracle.block_mass(q, k, _dense_lse(q, k), 64)
+    np.testing.assert_allclose(m.sum(axis=-1), 64.0, rtol=1e-12)
+    assert (m > 0).all()
+
+
+def test_block_mass_brute_force_small():
+    rng = np.random.default_rng(22)
+    N, d, bs = 8, 4, 4
+    q, k = rng.standard_normal((2, N, d))
+    lse = rng.standard_normal(N)
+    got = oracle.block_mass(q, k, lse, bs, scale=0.7)
+    for i in range(2):
+        for j in range(2):
+            want = sum(math.exp(0.7 * float(q[r] @ k[c]) - lse[r])
+                       for r in range(i * bs, (i + 1) * bs) for c in range(j * bs, (j + 1) * bs))
+            assert abs(got[i, j] - want) <= 1e-12 * want
+
+
+def test_exact_selector_keeps_the_block_that_holds_the_attention():
+    rng = np.random.default_rng(23)
+    q, k = (rng.standard_normal((2, 1, 1, 512, 64)) * 0.1).astype(np.float32)
+    k[0, 0, 5 * 64 + 7] = 4.0 * q[0, 0, 2 * 64 + 3]  # one key aligned with one query of block 2
+    m = oracle.block_mass(q, k, _dense_lse(q, k), 64)
+    sel = oracle.select_mask_exact(m, 1.0 / 8)  # k = 1
+    assert sel[0, 0, 2].tolist() == [0, 0, 0, 0, 0, 1, 0, 0]
