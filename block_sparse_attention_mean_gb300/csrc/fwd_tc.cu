@@ -11,8 +11,10 @@
 //     128-row query tile, or one KV-range chunk of a tile that is far longer than
 //     the per-CTA share of steps; the last chunk to finish merges the chunks'
 //     partial (O, max, sums).
-//   * Warp roles: 4 or 8 softmax + epilogue warps, a TMA producer warp, a QK^T
-//     issuer warp and a PV issuer warp. The role warps run converged and issue
+//   * Warp roles: 4 or 8 softmax + epilogue warps, a scheduler + Q/K producer
+//     warp, a V producer warp, a QK^T issuer warp and a PV issuer warp. The two
+//     producers walk the index on their own, so a V slot still held by a
+//     lagging PV never holds back a K load. The role warps run converged and issue
 //     TMA copies, tcgen05.mma and tcgen05.commit from one elect.sync lane; every
 //     warp waits on mbarriers with all lanes and a vote (a lone lane waiting or
 //     issuing while the others park costs several times more on this GPU).
@@ -23,9 +25,10 @@
 //     block index into separate K and V shared-memory rings (a K slot frees when
 //     its QK^T completes, a V slot when its PV completes).
 //   * S = Q K^T and O += P V run on tcgen05 with fp32 accumulators in TMEM. The
-//     QK^T issuer, the only consumer that walks the index, runs up to NSB steps
-//     ahead and leaves a step descriptor beside each S buffer; P (bf16)
-//     overwrites S in TMEM and feeds the PV MMA directly.
+//     K producer walks with one step of lookahead and leaves a step descriptor
+//     (blocks, members, last) beside each K slot; the QK^T issuer, which reads no
+//     index, runs up to NSB steps ahead and passes the descriptor on beside each
+//     S buffer. P (bf16) overwrites S in TMEM and feeds the PV MMA directly.
 //   * Online softmax in the log2 domain with one FFMA + one ex2 per score;
 //     the running max is only raised (and O rescaled in TMEM) when it grows by
 //     more than 2^8, which keeps the result exact while skipping most rescales.
@@ -52,7 +55,8 @@ template <int SPLIT>
 struct Roles {
     static constexpr int kSoftmaxWarps = 4 * SPLIT;
     static constexpr int kProducerWarp = kSoftmaxWarps, kQkWarp = kSoftmaxWarps + 1, kMmaWarp = kSoftmaxWarps + 2;
-    static constexpr int kThreads = (kSoftmaxWarps + 3) * 32;
+    static constexpr int kVProducerWarp = kSoftmaxWarps + 3;
+    static constexpr int kThreads = (kSoftmaxWarps + 4) * 32;
 };
 constexpr int kTileM = 128;
 constexpr float kRescaleLog2 = 8.0f;
@@ -148,7 +152,8 @@ struct Cfg {
     static constexpr int B_DRAIN = B_TEMPTY + 2;  // two: one per MMA-issuing thread
     static constexpr int NBAR = B_DRAIN + 2;
     static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
-    static constexpr int MISC_WORDS = 4 + NSB;  // TMEM base, abort flag, 2 tile ids, NSB step descriptors
+    // TMEM base, abort flag, 2 tile ids, NSB step descriptors of the S/P buffers, NK of the K ring
+    static constexpr int MISC_WORDS = 4 + NSB + NK;
     static constexpr int SMEM = MISC_OFF + 4 * ((MISC_WORDS + 7) & ~7);
     static constexpr int SMEM_ALLOC = SMEM + 1024;  // manual 1024-byte alignment
     static constexpr int TCOLS_USED = NSB * kStep + D;
@@ -891,22 +896,24 @@ __device__ __forceinline__ void softmax_quads(const TcParams &p, uint32_t sbase,
 }
 
 template <int D, int BS, int NK, int NV, int NSB, int QS, int SPLIT, int PAIR, int MINB>
-__global__ void __launch_bounds__((4 * SPLIT + 3) * 32, MINB)
+__global__ void __launch_bounds__((4 * SPLIT + 4) * 32, MINB)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const TcParams p)
 {
     using C = Cfg<D, BS, NK, NV, NSB, QS, PAIR>;
     using R = Roles<SPLIT>;
     constexpr int kProducerWarp = R::kProducerWarp, kQkWarp = R::kQkWarp, kMmaWarp = R::kMmaWarp;
+    constexpr int kVProducerWarp = R::kVProducerWarp;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
     auto bar = [&](int idx) -> uint32_t { return sbase + C::BAR_OFF + 8u * idx; };
     uint32_t *misc = reinterpret_cast<uint32_t *>(smem + C::MISC_OFF);
     // misc[0]: TMEM base, misc[1]: abort flag, misc[2..3]: tile ids of the scheduler ring,
-    // misc[4..4+NSB): step descriptors of the S/P buffers
+    // misc[4..4+NSB): step descriptors of the S/P buffers, misc[4+NSB..4+NSB+NK): those of the K ring
     volatile int32_t *tile_ids = reinterpret_cast<volatile int32_t *>(misc + 2);
     volatile uint32_t *desc = reinterpret_cast<volatile uint32_t *>(misc + 4);
+    volatile uint32_t *kdesc = desc + NSB;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -930,7 +937,7 @@ __global__ void __launch_bounds__((4 * SPLIT + 3) * 32, MINB)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(bar(C::B_TFULL + b), 1);
-            mbar_init(bar(C::B_TEMPTY + b), R::kSoftmaxWarps + 2);
+            mbar_init(bar(C::B_TEMPTY + b), R::kSoftmaxWarps + 3);  // softmax, QK^T, PV, V producer
         }
         mbar_init(bar(C::B_OEMPTY), R::kSoftmaxWarps);
         mbar_init(bar(C::B_DRAIN), 1);
@@ -955,11 +962,14 @@ __global__ void __launch_bounds__((4 * SPLIT + 3) * 32, MINB)
     const bool stall = (p.dbg & kDbgStall) != 0u;
 
     if (warp == kProducerWarp) {
-        // ------------------------------------------------------------ TMA producer
+        // ------------------------------------------------------------ tile scheduler, Q and K producer
         // Whole-warp loop (uniform waits and walk); one elected lane issues the copies.
+        // This warp is the walker of the K side: with one step of lookahead it leaves
+        // each step's descriptor (blocks, members, last) beside its K slot, released by
+        // the K-full barrier, so the QK^T issuer has no index reads on its path.
         {
             int G = 0, e = 0, tcount = 0;
-            int last_issue = -1;  // last iteration whose K and V loads were issued
+            int last_issue = -1;  // last step whose K loads were issued
             int q_issued = -1;
             bool ok = true;
             const uint32_t n_items = *p.n_items;  // written by the tile-order launch before this one
@@ -975,8 +985,8 @@ __global__ void __launch_bounds__((4 * SPLIT + 3) * 32, MINB)
                 int64_t bh = 0;
                 int qt = 0;
                 TileWalk walk;
-                int js[2];
-                uint32_t ms[2];
+                int js[2], jn[2];
+                uint32_t ms[2], mn[2];
                 int cnt = 0;
                 if (item >= 0) {
                     const Item it = decode_item(p, item);
@@ -1006,8 +1016,8 @@ __global__ void __launch_bounds__((4 * SPLIT + 3) * 32, MINB)
                 }
                 __syncwarp();
                 q_issued = e;
+                int cnt_n = walk.next_step<PAIR>(jn, mn);
                 do {
-                    const uint32_t step_bytes = static_cast<uint32_t>(cnt * BS * D * 2);
                     // K slot: freed when the QK^T that read it completes
                     const int ks = G % NK;
                     if (G >= NK && !warp_wait_all(bar(C::B_KEMPTY + ks), ((G / NK) - 1) & 1, ctl)) {
@@ -1015,7 +1025,8 @@ __global__ void __launch_bounds__((4 * SPLIT + 3) * 32, MINB)
                         break;
                     }
                     if (elect_one()) {
-                        mbar_arrive_expect_tx(bar(C::B_KFULL + ks), step_bytes);
+                        kdesc[ks] = step_desc(cnt, ms, cnt_n == 0);  // released by the arrive below
+                        mbar_arrive_expect_tx(bar(C::B_KFULL + ks), static_cast<uint32_t>(cnt * BS * D * 2));
                         for (int q = 0; q < cnt; ++q) {
                             const int krow = static_cast<int>(bh * p.N) + js[q] * BS;
 #pragma unroll
@@ -1025,18 +1036,59 @@ __global__ void __launch_bounds__((4 * SPLIT + 3) * 32, MINB)
                         }
                     }
                     __syncwarp();
+                    last_issue = G;
+                    ++G;
+                    cnt = cnt_n;
+                    js[0] = jn[0];
+                    js[1] = jn[1];
+                    ms[0] = mn[0];
+                    ms[1] = mn[1];
+                    if (cnt != 0) cnt_n = walk.next_step<PAIR>(jn, mn);
+                } while (cnt != 0);
+                ++e;
+            }
+            if (lane == 0 && *ctl.abort_flag) {
+                // never leave while our copies may still land in shared memory
+                for (int g = last_issue - NK + 1; g <= last_issue; ++g)
+                    if (g >= 0) wait_bar_drain(bar(C::B_KFULL + g % NK), (g / NK) & 1, p.wait_limit_ns);
+                for (int e2 = q_issued - (QS - 1) < 0 ? 0 : q_issued - (QS - 1); e2 <= q_issued; ++e2)
+                    wait_bar_drain(bar(C::B_QFULL + e2 % QS), (e2 / QS) & 1, p.wait_limit_ns);
+            }
+            __syncwarp();
+        }
+    } else if (warp == kVProducerWarp) {
+        // ------------------------------------------------------------ V producer
+        // Walks each tile on its own, so a V slot still held by a lagging PV never
+        // delays the K loads that QK^T waits for.
+        if (!stall) {
+            int G = 0, tcount = 0;
+            int last_issue = -1;  // last step whose V loads were issued
+            bool ok = true;
+            while (ok) {
+                int tile;
+                if (!fetch_tile<C>(sbase, tile_ids, ctl, lane, tcount, tile)) break;
+                if (tile < 0) break;
+                if (tile & kEmptyTile) continue;
+                const Item it = decode_item(p, tile);
+                int j_lo, j_hi;
+                chunk_range(p, it, j_lo, j_hi);
+                int64_t bh;
+                int qt;
+                tile_coords(p, it.tile, bh, qt);
+                TileWalk walk;
+                walk_init<BS>(walk, p, bh, qt, j_lo, j_hi);
+                int js[2];
+                uint32_t ms[2];
+                int cnt;
+                while ((cnt = walk.next_step<PAIR>(js, ms)) != 0) {
                     // V slot: freed when the PV that read it completes
                     const int vs = G % NV;
                     if (G >= NV && !warp_wait_all(bar(C::B_VEMPTY + vs), ((G / NV) - 1) & 1, ctl)) {
-                        // the K load of this iteration is in flight: drain it below
-                        last_issue = G - 1;
                         ok = false;
-                        if (lane == 0) wait_bar_drain(bar(C::B_KFULL + ks), (G / NK) & 1, p.wait_limit_ns);
-                        __syncwarp();
                         break;
                     }
                     if (elect_one()) {
-                        mbar_arrive_expect_tx(bar(C::B_VFULL + vs), step_bytes);
+                        mbar_arrive_expect_tx(bar(C::B_VFULL + vs), static_cast<uint32_t>(cnt * BS * D * 2));
                         for (int q = 0; q < cnt; ++q) {
                             const int vrow = static_cast<int>(bh * p.N) + js[q] * BS;
 #pragma unroll
@@ -1048,18 +1100,11 @@ __global__ void __launch_bounds__((4 * SPLIT + 3) * 32, MINB)
                     __syncwarp();
                     last_issue = G;
                     ++G;
-                } while ((cnt = walk.next_step<PAIR>(js, ms)) != 0);
-                ++e;
+                }
             }
             if (lane == 0 && *ctl.abort_flag) {
-                // never leave while our copies may still land in shared memory
-                for (int g = last_issue - (NK > NV ? NK : NV) + 1; g <= last_issue; ++g) {
-                    if (g < 0) continue;
-                    if (g > last_issue - NK) wait_bar_drain(bar(C::B_KFULL + g % NK), (g / NK) & 1, p.wait_limit_ns);
-                    if (g > last_issue - NV) wait_bar_drain(bar(C::B_VFULL + g % NV), (g / NV) & 1, p.wait_limit_ns);
-                }
-                for (int e2 = q_issued - (QS - 1) < 0 ? 0 : q_issued - (QS - 1); e2 <= q_issued; ++e2)
-                    wait_bar_drain(bar(C::B_QFULL + e2 % QS), (e2 / QS) & 1, p.wait_limit_ns);
+                for (int g = last_issue - NV + 1; g <= last_issue; ++g)
+                    if (g >= 0) wait_bar_drain(bar(C::B_VFULL + g % NV), (g / NV) & 1, p.wait_limit_ns);
             }
             __syncwarp();
         }
@@ -1067,7 +1112,7 @@ __global__ void __launch_bounds__((4 * SPLIT + 3) * 32, MINB)
         // ------------------------------------------------------------ QK^T issuer
         // Runs ahead of the softmax: QK^T of step G needs only K(G) and S/P buffer
         // G % NSB, which is free once PV(G - NSB) completed. The whole warp runs the
-        // loop (waits and walk are warp-uniform) and one elected lane issues: tcgen05
+        // loop (waits are warp-uniform) and one elected lane issues: tcgen05
         // issue from converged code is several times cheaper than from a lone lane.
         if (!stall) {
             const uint32_t tS = tmem;  // NSB S/P buffers of kStep columns
@@ -1084,57 +1129,44 @@ __global__ void __launch_bounds__((4 * SPLIT + 3) * 32, MINB)
                 ++tcount;
                 if (tile < 0) break;
                 if (tile & kEmptyTile) continue;
-                const Item it = decode_item(p, tile);
-                int j_lo, j_hi;
-                chunk_range(p, it, j_lo, j_hi);
-                int64_t bh;
-                int qt;
-                tile_coords(p, it.tile, bh, qt);
-                TileWalk walk;
-                walk_init<BS>(walk, p, bh, qt, j_lo, j_hi);
-                // one step of lookahead: a step's descriptor says whether it is the tile's last
-                int js[2], jn[2];
-                uint32_t ms[2], mn[2];
-                int cnt = walk.next_step<PAIR>(js, ms);
-                int cnt_n = walk.next_step<PAIR>(jn, mn);
                 const int qs = e % QS;
                 if (!warp_wait_all(bar(C::B_QFULL + qs), (e / QS) & 1, ctl)) break;
                 tc_fence_after();
                 const uint64_t qdesc = sdesc_sw128(sbase + C::Q_OFF + qs * C::kQBytes, 16, 1024);
+                bool last;
                 do {
                     const int s = G % NK, b = G % NSB;
-                    if (!warp_wait_all(bar(C::B_KFULL + s), (G / NK) & 1, ctl)) { ok = false; break; }
+                    // the step's descriptor comes with its K slot (left there by the K producer)
+                    const uint32_t sd = warp_wait_step(bar(C::B_KFULL + s), (G / NK) & 1, ctl, kdesc + s);
+                    if (sd == 0xFFFFFFFFu) { ok = false; break; }
                     // S/P buffer b (and its descriptor) was last read by PV(G - NSB)
                     if (G >= NSB && !warp_wait_all(bar(C::B_PVDONE + b), ((G / NSB) - 1) & 1, ctl)) {
                         ok = false;
                         break;
                     }
                     if (lane == 0) {
-                        desc[b] = step_desc(cnt, ms, cnt_n == 0);
+                        desc[b] = sd;
                         mbar_arrive(bar(C::B_SFULL + b));  // release: the descriptor is visible with the phase
                     }
                     tc_fence_after();
+                    last = desc_last(sd);
                     // K-major, 128-byte swizzle: step kk is 32 bytes into 64-column slab kk / 4
-                    const uint64_t kdesc = kdesc0 + static_cast<uint64_t>(s * (C::kKVBytes >> 4));
-                    const uint32_t idesc = cnt == PAIR ? C::IDESC_QK : C::IDESC_QK_HALF;
+                    const uint64_t kdesc_s = kdesc0 + static_cast<uint64_t>(s * (C::kKVBytes >> 4));
+                    const uint32_t idesc = desc_count(sd) == PAIR ? C::IDESC_QK : C::IDESC_QK_HALF;
                     __syncwarp();
                     if (elect_one()) {
 #pragma unroll
                         for (int kk = 0; kk < D / 16; ++kk) {
                             const uint64_t off_q = static_cast<uint64_t>(((kk >> 2) * C::kQChunk + (kk & 3) * 32) >> 4);
                             const uint64_t off_k = static_cast<uint64_t>(((kk >> 2) * C::kKVChunk + (kk & 3) * 32) >> 4);
-                            mma_ss(tS + b * C::kStep, qdesc + off_q, kdesc + off_k, idesc, kk > 0 ? 1u : 0u);
+                            mma_ss(tS + b * C::kStep, qdesc + off_q, kdesc_s + off_k, idesc, kk > 0 ? 1u : 0u);
                         }
                         tc_commit(bar(C::B_SFULL + b));
                         tc_commit(bar(C::B_KEMPTY + s));
                     }
                     __syncwarp();
                     ++G;
-                    cnt = cnt_n;
-                    ms[0] = mn[0];
-                    ms[1] = mn[1];
-                    if (cnt != 0) cnt_n = walk.next_step<PAIR>(jn, mn);
-                } while (cnt != 0);
+                } while (!last);
                 if (!ok) break;
                 // the tile's last QK^T: its Q slot is free once these MMAs complete
                 if (elect_one()) tc_commit(bar(C::B_QEMPTY + qs));
