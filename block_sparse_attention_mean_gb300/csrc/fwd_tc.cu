@@ -389,6 +389,7 @@ __device__ __forceinline__ void softmax_rows(const TcParams &p, uint32_t sbase, 
                                              const Ctl &ctl, int warp, int lane)
 {
     auto bar = [&](int idx) -> uint32_t { return barrier_addr<C>(sbase, idx); };
+    static_assert(D % 64 == 0, "the epilogue reads O in pairs of 32-column chunks");
     constexpr int kStep = C::kStep;
     constexpr int NC = kStep / 32;  // 32-column chunks of a step
     constexpr int CPB = BS / 32;    // chunks per block
@@ -570,20 +571,29 @@ __device__ __forceinline__ void softmax_rows(const TcParams &p, uint32_t sbase, 
                 const int t = G - 1;
                 if (!warp_wait_all(bar(C::B_PVDONE + t % NSB), (t / NSB) & 1, ctl)) return;
                 tc_fence_after();
+                // O in pairs of 32-column chunks (one load wait per pair); O is released to the
+                // next tile's PV as soon as the last pair is in registers
 #pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
-                    uint32_t ov[32];
-                    tmem_ld32(tO + c * 32, ov);
+                for (int c0 = 0; c0 < D / 32; c0 += 2) {
+                    uint32_t ov[2][32];
+                    tmem_ld32(tO + c0 * 32, ov[0]);
+                    tmem_ld32(tO + (c0 + 1) * 32, ov[1]);
                     tmem_wait_ld();
-                    reg_fence32(ov);
+                    reg_fence32(ov[0]);
+                    reg_fence32(ov[1]);
+                    if (c0 + 2 == D / 32) {
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(bar(C::B_OEMPTY));
+                    }
 #pragma unroll
-                    for (int q = 0; q < 8; ++q)
-                        po[c * 8 + q] = make_float4(__uint_as_float(ov[4 * q]), __uint_as_float(ov[4 * q + 1]),
-                                                    __uint_as_float(ov[4 * q + 2]), __uint_as_float(ov[4 * q + 3]));
+                    for (int h = 0; h < 2; ++h)
+#pragma unroll
+                        for (int q = 0; q < 8; ++q)
+                            po[(c0 + h) * 8 + q] =
+                                make_float4(__uint_as_float(ov[h][4 * q]), __uint_as_float(ov[h][4 * q + 1]),
+                                            __uint_as_float(ov[h][4 * q + 2]), __uint_as_float(ov[h][4 * q + 3]));
                 }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar(C::B_OEMPTY));
             } else {
 #pragma unroll
                 for (int q = 0; q < D / 4; ++q) po[q] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
@@ -598,37 +608,48 @@ __device__ __forceinline__ void softmax_rows(const TcParams &p, uint32_t sbase, 
         if (!warp_wait_all(bar(C::B_PVDONE + t % NSB), (t / NSB) & 1, ctl)) return;
         tc_fence_after();
         const float inv_l = lp_run > 0.0f ? 1.0f / lp_run : 0.0f;
+        // O in pairs of 32-column chunks (one load wait per pair); O is released to the next
+        // tile's PV as soon as the last pair is in registers
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-            uint32_t ov[32];
-            tmem_ld32(tO + c * 32, ov);
+        for (int c0 = 0; c0 < D / 32; c0 += 2) {
+            uint32_t ov[2][32];
+            tmem_ld32(tO + c0 * 32, ov[0]);
+            tmem_ld32(tO + (c0 + 1) * 32, ov[1]);
             tmem_wait_ld();
-            reg_fence32(ov);
+            reg_fence32(ov[0]);
+            reg_fence32(ov[1]);
+            if (c0 + 2 == D / 32) {
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(C::B_OEMPTY));
+            }
             if (row_valid) {
-                uint32_t pk[16];
-                if (p.R) {  // residual compensation: O_sparse + R
-                    const float4 *rs = reinterpret_cast<const float4 *>(p.R + grow * D + c * 32);
 #pragma unroll
-                    for (int q = 0; q < 8; ++q) {
-                        const float4 r = __ldg(rs + q);
-                        pk[2 * q] = pack_bf16x2(fmaf(__uint_as_float(ov[4 * q]), inv_l, r.x),
-                                                fmaf(__uint_as_float(ov[4 * q + 1]), inv_l, r.y));
-                        pk[2 * q + 1] = pack_bf16x2(fmaf(__uint_as_float(ov[4 * q + 2]), inv_l, r.z),
-                                                    fmaf(__uint_as_float(ov[4 * q + 3]), inv_l, r.w));
+                for (int h = 0; h < 2; ++h) {
+                    const int c = c0 + h;
+                    uint32_t pk[16];
+                    if (p.R) {  // residual compensation: O_sparse + R
+                        const float4 *rs = reinterpret_cast<const float4 *>(p.R + grow * D + c * 32);
+#pragma unroll
+                        for (int q = 0; q < 8; ++q) {
+                            const float4 r = __ldg(rs + q);
+                            pk[2 * q] = pack_bf16x2(fmaf(__uint_as_float(ov[h][4 * q]), inv_l, r.x),
+                                                    fmaf(__uint_as_float(ov[h][4 * q + 1]), inv_l, r.y));
+                            pk[2 * q + 1] = pack_bf16x2(fmaf(__uint_as_float(ov[h][4 * q + 2]), inv_l, r.z),
+                                                        fmaf(__uint_as_float(ov[h][4 * q + 3]), inv_l, r.w));
+                        }
+                    } else {
+#pragma unroll
+                        for (int q = 0; q < 16; ++q)
+                            pk[q] = pack_bf16x2(__uint_as_float(ov[h][2 * q]) * inv_l,
+                                                __uint_as_float(ov[h][2 * q + 1]) * inv_l);
                     }
-                } else {
+                    uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
 #pragma unroll
-                    for (int q = 0; q < 16; ++q)
-                        pk[q] = pack_bf16x2(__uint_as_float(ov[2 * q]) * inv_l, __uint_as_float(ov[2 * q + 1]) * inv_l);
+                    for (int q = 0; q < 4; ++q) dst[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
                 }
-                uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
-#pragma unroll
-                for (int q = 0; q < 4; ++q) dst[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
             }
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(C::B_OEMPTY));
         if (row_valid) p.LSE[grow] = l_run > 0.0f ? (m_run + log2f(l_run)) * 0.69314718055994530942f : -CUDART_INF_F;
     }
 }
