@@ -78,11 +78,12 @@ def _check(code: int, what: str):
 
 
 def block_mean(x: np.ndarray, bs: int) -> np.ndarray:
-    """Mean-pooled block representation: x [..., N, d] fp32 -> [..., N/bs, d] fp32."""
+    """Mean-pooled block representation: x [..., N, d] fp32 -> [..., ceil(N/bs), d] fp32
+    (a ragged last block averages the tokens it holds)."""
     x = np.ascontiguousarray(x, dtype=np.float32)
     *lead, N, d = x.shape
     heads = int(np.prod(lead)) if lead else 1
-    out = np.empty((*lead, N // bs, d), np.float32)
+    out = np.empty((*lead, -(-N // bs), d), np.float32)
     _check(_load().bsa_oracle_block_mean(_ptr(x), heads, N, d, bs, _ptr(out)), "block_mean")
     return out
 
@@ -230,14 +231,15 @@ def block_mass(q: np.ndarray, k: np.ndarray, lse: np.ndarray, bs: int, scale: Op
     k = np.asarray(k, dtype=np.float64)
     *lead, N, d = q.shape
     sc = 1.0 / math.sqrt(d) if scale is None else float(scale)
-    nB = N // bs
+    nB = -(-N // bs)  # a ragged last block holds the rows and keys up to N
     out = np.empty((*lead, nB, nB))
     qf, kf = q.reshape(-1, N, d), k.reshape(-1, N, d)
     lf = np.asarray(lse, dtype=np.float64).reshape(-1, N)
     of = out.reshape(-1, nB, nB)
+    pp = np.zeros((nB * bs, nB * bs))
     for h in range(qf.shape[0]):
-        p = np.exp(sc * (qf[h] @ kf[h].T) - lf[h][:, None])
-        of[h] = p.reshape(nB, bs, nB, bs).sum(axis=(1, 3))
+        pp[:N, :N] = np.exp(sc * (qf[h] @ kf[h].T) - lf[h][:, None])
+        of[h] = pp.reshape(nB, bs, nB, bs).sum(axis=(1, 3))
     return out
 
 

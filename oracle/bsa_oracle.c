@@ -49,23 +49,26 @@
 #define ORACLE_ERR_NONFINITE 5
 
 /* ---------------------------------------------------------------------- */
-/* [P3] naive BSA step 1: mean-pooled block representation (reading R1).   */
-/* X: [n_heads][N][d] fp32; out: [n_heads][N/bs][d] fp32.                  */
+/* [P3] naive BSA step 1: mean-pooled block representation (reading R1):  */
+/* the mean of the block's tokens; a ragged last block (N not a multiple   */
+/* of bs, reading R20) averages the tokens it holds.                       */
+/* X: [n_heads][N][d] fp32; out: [n_heads][ceil(N/bs)][d] fp32.            */
 int bsa_oracle_block_mean(const float *X, int64_t n_heads, int64_t N, int d, int bs,
                           float *out)
 {
-    if (!X || !out || n_heads <= 0 || N <= 0 || d <= 0 || bs <= 0 || N % bs != 0)
+    if (!X || !out || n_heads <= 0 || N <= 0 || d <= 0 || bs <= 0)
         return ORACLE_ERR_ARG;
-    const int64_t nB = N / bs;
-    const float inv = 1.0f / (float)bs;
+    const int64_t nB = (N + bs - 1) / bs;
     for (int64_t h = 0; h < n_heads; ++h)
-        for (int64_t i = 0; i < nB; ++i)
+        for (int64_t i = 0; i < nB; ++i) {
+            const int64_t cnt = (N - i * bs) < bs ? (N - i * bs) : bs;
             for (int c = 0; c < d; ++c) {
                 float acc = 0.0f;
-                for (int t = 0; t < bs; ++t)
+                for (int64_t t = 0; t < cnt; ++t)
                     acc = acc + X[(h * N + i * bs + t) * d + c];
-                out[(h * nB + i) * d + c] = acc * inv;
+                out[(h * nB + i) * d + c] = acc / (float)cnt;
             }
+        }
     return ORACLE_OK;
 }
 
@@ -218,11 +221,12 @@ int bsa_oracle_attention(const float *Q, const float *K, const float *V, int64_t
                          const int64_t *rows, int64_t n_rows, double *O, double *LSE)
 {
     if (!Q || !K || !V || !mask || !rows || !O || !LSE || n_heads <= 0 || N <= 0 || d <= 0 ||
-        bs <= 0 || N % bs != 0 || n_rows < 0)
+        bs <= 0 || n_rows < 0)
         return ORACLE_ERR_ARG;
     for (int64_t t = 0; t < n_rows; ++t)
         if (rows[t] < 0 || rows[t] >= n_heads * N) return ORACLE_ERR_ARG;
-    const int64_t nB = N / bs;
+    /* reading R20: a ragged last block holds the keys up to N; nothing past N exists */
+    const int64_t nB = (N + bs - 1) / bs;
     int err = ORACLE_OK;
 #pragma omp parallel
     {

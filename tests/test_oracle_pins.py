@@ -458,3 +458,60 @@ def test_exact_selector_keeps_the_block_that_holds_the_attention():
     m = oracle.block_mass(q, k, _dense_lse(q, k), 64)
     sel = oracle.select_mask_exact(m, 1.0 / 8)  # k = 1
     assert sel[0, 0, 2].tolist() == [0, 0, 0, 0, 0, 1, 0, 0]
+
+
+# ---------------------------------------------------------------- ragged last block (reading R20)
+
+
+def test_ragged_all_ones_mask_equals_dense_attention():
+    # N = 75 at block 16: five blocks, the last holding 11 keys; every key of the row counts once
+    H, N, d, bs = 2, 75, 8, 16
+    q, k, v = _rand(H, N, d), _rand(H, N, d), _rand(H, N, d)
+    nB = -(-N // bs)
+    O, L = oracle.attention(q, k, v, np.ones((H, nB, nB), np.uint8), bs)
+    assert O.shape == (H * N, d)
+    for h in range(H):
+        Od, Ld = _dense_library(q[h], k[h], v[h], 1.0 / math.sqrt(d), np.ones((N, N), bool))
+        np.testing.assert_allclose(O[h * N:(h + 1) * N], Od, rtol=1e-11, atol=1e-12)
+        np.testing.assert_allclose(L[h * N:(h + 1) * N], Ld, rtol=1e-12, atol=1e-12)
+
+
+def test_ragged_block_diagonal_is_independent_block_attention():
+    N, d, bs = 70, 4, 16   # blocks of 16, 16, 16, 16 and 6 tokens
+    q, k, v = _rand(1, N, d), _rand(1, N, d), _rand(1, N, d)
+    nB = -(-N // bs)
+    O, L = oracle.attention(q, k, v, np.eye(nB, dtype=np.uint8)[None], bs, scale=0.5)
+    for i in range(nB):
+        sl = slice(i * bs, min((i + 1) * bs, N))
+        n = sl.stop - sl.start
+        Ob, Lb = _dense_library(q[0, sl], k[0, sl], v[0, sl], 0.5, np.ones((n, n), bool))
+        np.testing.assert_allclose(O[sl], Ob, rtol=1e-11, atol=1e-12)
+        np.testing.assert_allclose(L[sl], Lb, rtol=1e-12)
+
+
+def test_ragged_block_mean_is_the_mean_of_the_tokens_it_holds():
+    # integer tokens: every partial sum is exact in fp32, so the pooled value is the fp32
+    # quotient of the exact sum by the block's token count (3 here, not the block size)
+    N, d, bs = 11, 5, 4
+    x = RNG.integers(-50, 50, size=(2, N, d)).astype(np.float32)
+    m = oracle.block_mean(x, bs)
+    assert m.shape == (2, 3, d)
+    for i, (a, b) in enumerate([(0, 4), (4, 8), (8, 11)]):
+        want = (x[:, a:b].astype(np.float64).sum(axis=1) / (b - a)).astype(np.float32)
+        s = x[:, a:b].sum(axis=1, dtype=np.float64).astype(np.float32)
+        np.testing.assert_array_equal(m[:, i], np.float32(s) / np.float32(b - a))
+        np.testing.assert_allclose(m[:, i], want, rtol=1e-7)
+
+
+def test_ragged_block_mass_rows_hold_one_unit_per_query_row():
+    # with the dense LSE each query row's probabilities sum to 1, so a Q block's masses add up
+    # to its row count: 16 for full blocks, 6 for the ragged last one
+    N, d, bs = 38, 8, 16
+    q, k = _rand(1, N, d), _rand(1, N, d)
+    s = (q[0].astype(np.float64) @ k[0].astype(np.float64).T) / math.sqrt(d)
+    lse = scipy.special.logsumexp(s, axis=-1)
+    mass = oracle.block_mass(q, k, lse[None], bs)
+    assert mass.shape == (1, 3, 3)
+    np.testing.assert_allclose(mass[0].sum(axis=1), [16, 16, 6], rtol=1e-12)
+    # the ragged block's mass against a brute-force sum over its 6 keys
+    np.testing.assert_allclose(mass[0, 0, 2], np.exp(s[:16, 32:] - lse[:16, None]).sum(), rtol=1e-12)
