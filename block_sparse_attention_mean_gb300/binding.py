@@ -181,7 +181,7 @@ def build_mask_modal(q: torch.Tensor, k: torch.Tensor, block: int, n_text_blocks
                      ws: Optional[torch.Tensor] = None, stream=None) -> "Index":
     """Per-modality top-k index (bsa_build_mask_modal) with freshly allocated buffers."""
     B, H, N, d = q.shape
-    nB = N // block
+    nB = -(-N // block)  # a ragged last block counts
     W = (nB + 31) // 32
     nnz = bsa_mask_nnz_modal(B, H, N, block, n_text_blocks, density)
     row_ptr = torch.empty(B * H * nB + 1, dtype=torch.int32, device=q.device)
@@ -208,7 +208,7 @@ def build_mask_exact(q: torch.Tensor, k: torch.Tensor, lse_dense: torch.Tensor, 
                      scale: float = 0.0, ws: Optional[torch.Tensor] = None, stream=None):
     """Block-oracle index from the dense LSE (bsa_build_mask_exact); returns (Index, workspace)."""
     B, H, N, d = q.shape
-    nB = N // block
+    nB = -(-N // block)  # a ragged last block counts
     W = (nB + 31) // 32
     kk = max(1, min(nB, int(math.floor(float(np.float32(density)) * nB))))
     row_ptr = torch.empty(B * H * nB + 1, dtype=torch.int32, device=q.device)
@@ -335,7 +335,7 @@ def build_mask(q: Optional[torch.Tensor], k: Optional[torch.Tensor], block: int,
     else:
         B, H, N, d = shape
         device = torch.device("cuda")
-    nB = N // block
+    nB = -(-N // block)  # a ragged last block counts
     nnz = bsa_mask_nnz(B, H, N, block, density, spec)
     W = (nB + 31) // 32
     row_ptr = torch.empty(B * H * nB + 1, dtype=torch.int32, device=device)

@@ -15,12 +15,15 @@ uint64_t g_wait_limit_ns = bsa::kDefaultWaitNs;
 
 bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+// Blocks per row or column; a sequence that is not a multiple of the block size ends in a
+// ragged block ("多模态DiT中的块稀疏注意力" §4.1: the tile loop masks the padding).
+int n_blocks(int N, int block) { return (N + block - 1) / block; }
+
 bsa_status check_shape(int B, int H, int N, int d, int block)
 {
     if (B <= 0 || H <= 0 || N <= 0) return BSA_ERR_SHAPE;
     if (d != 64 && d != 128) return BSA_ERR_SHAPE;
     if (block != 64 && block != 128) return BSA_ERR_SHAPE;
-    if (N % block != 0) return BSA_ERR_SHAPE;
     const int64_t rows = static_cast<int64_t>(B) * H * N;
     if (rows > INT32_MAX) return BSA_ERR_SHAPE;  // TMA row coordinates are int32
     return BSA_OK;
@@ -136,7 +139,7 @@ bsa_status bsa_mask_nnz_modal(int B, int H, int N, int block, int n_text_blocks,
     if (!nnz) return BSA_ERR_INVALID_ARG;
     const bsa_status s = check_shape(B, H, N, 64, block);
     if (s != BSA_OK) return s;
-    const int nB = N / block;
+    const int nB = n_blocks(N, block);
     if (!valid_modal(nB, n_text_blocks, density)) return BSA_ERR_INVALID_ARG;
     int kq[2][2];
     *nnz = static_cast<int64_t>(B) * H * modal_counts(nB, n_text_blocks, density, kq);
@@ -154,7 +157,7 @@ bsa_status bsa_build_mask_modal(const void *Q, const void *K, int dt, int B, int
     if (!Q || !K || !aligned(Q, 16) || !aligned(K, 16)) return BSA_ERR_INVALID_ARG;
     if (!row_ptr || !col_idx || !bitmap || col_capacity < 0) return BSA_ERR_INVALID_ARG;
     if (!aligned(row_ptr, 4) || !aligned(col_idx, 4) || !aligned(bitmap, 4)) return BSA_ERR_INVALID_ARG;
-    const int nB = N / block;
+    const int nB = n_blocks(N, block);
     if (!valid_modal(nB, n_text_blocks, density)) return BSA_ERR_INVALID_ARG;
     if (!workspace || !aligned(workspace, 256) || workspace_bytes < bsa::mask_workspace_bytes(B, H, N, d, block))
         return BSA_ERR_WORKSPACE;
@@ -205,7 +208,7 @@ bsa_status bsa_build_mask_exact(const void *Q, const void *K, int dt, int B, int
     if (std::isnan(scale) || std::isinf(scale)) return BSA_ERR_INVALID_ARG;
     if (!workspace || !aligned(workspace, 256) || workspace_bytes < bsa::exact_workspace_bytes(B, H, N, d, block))
         return BSA_ERR_WORKSPACE;
-    const int nB = N / block;
+    const int nB = n_blocks(N, block);
     if (nB > bsa::kMaxKvBlocks) return BSA_ERR_UNSUPPORTED;
     const int64_t R = static_cast<int64_t>(B) * H * nB;
     bsa::ExactArgs a{};
@@ -248,8 +251,8 @@ bsa_status bsa_workspace_size(int which, int B, int H, int N, int d, int block, 
 bsa_status bsa_mask_nnz(int B, int H, int N, int block, float density, const bsa_static_spec *spec, int64_t *nnz)
 {
     if (!nnz) return BSA_ERR_INVALID_ARG;
-    if (B <= 0 || H <= 0 || N <= 0 || (block != 64 && block != 128) || N % block != 0) return BSA_ERR_SHAPE;
-    const int nB = N / block;
+    if (B <= 0 || H <= 0 || N <= 0 || (block != 64 && block != 128)) return BSA_ERR_SHAPE;
+    const int nB = n_blocks(N, block);
     const int64_t BH = static_cast<int64_t>(B) * H;
     if (!spec) {
         if (!valid_density(density)) return BSA_ERR_INVALID_ARG;
@@ -274,7 +277,7 @@ bsa_status bsa_build_mask(const void *Q, const void *K, int dt, int B, int H, in
     if (!aligned(row_ptr, 4) || !aligned(col_idx, 4) || !aligned(bitmap, 4)) return BSA_ERR_INVALID_ARG;
     if (!workspace || !aligned(workspace, 256) || workspace_bytes < bsa::mask_workspace_bytes(B, H, N, d, block))
         return BSA_ERR_WORKSPACE;
-    const int nB = N / block;
+    const int nB = n_blocks(N, block);
     const int64_t R = static_cast<int64_t>(B) * H * nB;
     bsa::MaskArgs a{};
     a.Q = Q;
@@ -350,8 +353,8 @@ static bsa_status forward_impl(const void *Q, const void *K, const void *V, int 
     a.N = N;
     a.d = d;
     a.block = block;
-    a.nQB = N / block;
-    a.nKB = N / block;
+    a.nQB = n_blocks(N, block);
+    a.nKB = n_blocks(N, block);
     a.W = (a.nKB + 31) / 32;
     a.row_ptr = row_ptr;
     a.col_idx = col_idx;
@@ -415,12 +418,12 @@ bsa_status bsa_check_device_error(void *workspace, void *stream)
 bsa_status bsa_validate_index(int B, int H, int N, int block, const int32_t *row_ptr, const int32_t *col_idx,
                               const uint32_t *bitmap, void *workspace, size_t workspace_bytes, void *stream)
 {
-    if (B <= 0 || H <= 0 || N <= 0 || (block != 64 && block != 128) || N % block != 0) return BSA_ERR_SHAPE;
+    if (B <= 0 || H <= 0 || N <= 0 || (block != 64 && block != 128)) return BSA_ERR_SHAPE;
     if (!row_ptr || !col_idx) return BSA_ERR_INVALID_ARG;
     if (!workspace || !aligned(workspace, 256) || workspace_bytes < bsa::kWsHeader) return BSA_ERR_WORKSPACE;
-    const int64_t R = static_cast<int64_t>(B) * H * (N / block);
+    const int64_t R = static_cast<int64_t>(B) * H * n_blocks(N, block);
     if (R > INT32_MAX) return BSA_ERR_SHAPE;
-    return bsa::launch_validate_index(static_cast<int>(R), N / block, row_ptr, col_idx, bitmap,
+    return bsa::launch_validate_index(static_cast<int>(R), n_blocks(N, block), row_ptr, col_idx, bitmap,
                                       static_cast<char *>(workspace), static_cast<cudaStream_t>(stream));
 }
 

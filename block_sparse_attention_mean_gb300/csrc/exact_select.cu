@@ -34,6 +34,7 @@ constexpr int kMassWarps = 4, kMassProducer = 4, kMassIssuer = 5, kMassThreads =
 
 struct MassParams {
     int N, nKB, tiles_per_bh, n_tiles;
+    int last_rows;     // keys in the last KV block (fewer than BS for a ragged sequence)
     float scale_log2;
     const float *LSE;  // [B*H*N] dense logsumexp, natural log
     float *part;       // [n_tiles][4][nKB] partial masses (one per mass warp and KV block)
@@ -110,13 +111,13 @@ __global__ void __launch_bounds__(kMassThreads, 2)
             const int qt = tile % p.tiles_per_bh;
             // the single Q slot was last read by the previous tile's QK^T
             if (e >= 1 && !warp_wait_all(bar(C::B_QEMPTY), (e - 1) & 1, ctl)) break;
-            const int qrow = static_cast<int>(bh * p.N) + qt * kMTile;
             __syncwarp();
             if (elect_one()) {
                 mbar_arrive_expect_tx(bar(C::B_QFULL), C::kQBytes);
 #pragma unroll
                 for (int c = 0; c < D / 64; ++c)
-                    tma_load_2d(sbase + C::Q_OFF + c * C::kQChunk, &tmQ, c * 64, qrow, bar(C::B_QFULL));
+                    tma_load_3d(sbase + C::Q_OFF + c * C::kQChunk, &tmQ, c * 64, qt * kMTile, static_cast<int>(bh),
+                                bar(C::B_QFULL));
             }
             __syncwarp();
             q_issued = e;
@@ -127,14 +128,13 @@ __global__ void __launch_bounds__(kMassThreads, 2)
                     ok = false;
                     break;
                 }
-                const int krow = static_cast<int>(bh * p.N) + j * BS;
                 __syncwarp();
                 if (elect_one()) {
                     mbar_arrive_expect_tx(bar(C::B_KFULL + s), C::kKBytes);
 #pragma unroll
                     for (int c = 0; c < D / 64; ++c)
-                        tma_load_2d(sbase + C::K_OFF + s * C::kKBytes + c * C::kKChunk, &tmK, c * 64, krow,
-                                    bar(C::B_KFULL + s));
+                        tma_load_3d(sbase + C::K_OFF + s * C::kKBytes + c * C::kKChunk, &tmK, c * 64, j * BS,
+                                    static_cast<int>(bh), bar(C::B_KFULL + s));
                 }
                 __syncwarp();
                 last_k = G;
@@ -225,6 +225,14 @@ __global__ void __launch_bounds__(kMassThreads, 2)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(C::B_SEMPTY + b));
+                if (j == p.nKB - 1 && p.last_rows < BS) {
+                    // keys past the sequence end (read as zeros) hold no mass
+#pragma unroll
+                    for (int c = 0; c < BS / 32; ++c)
+#pragma unroll
+                        for (int t = 0; t < 32; ++t)
+                            if (c * 32 + t >= p.last_rows) sv[c][t] = 0xFF800000u;
+                }
                 float a0 = 0.0f, a1 = 0.0f, a2 = 0.0f, a3 = 0.0f;
 #pragma unroll
                 for (int c = 0; c < BS / 32; ++c)
@@ -272,13 +280,13 @@ bsa_status launch_mass(const ExactArgs &a, cudaStream_t st)
         grid_cap = 2 * sms;
     }
     const int64_t BH = static_cast<int64_t>(a.B) * a.H;
-    const uint64_t rows = static_cast<uint64_t>(BH) * a.N;
     CUtensorMap mq, mk;
-    if (!make_tma_map_bf16(&mq, a.Q, rows, D, kMTile) || !make_tma_map_bf16(&mk, a.K, rows, D, BS))
+    if (!make_tma_map_bf16(&mq, a.Q, BH, a.N, D, kMTile) || !make_tma_map_bf16(&mk, a.K, BH, a.N, D, BS))
         return BSA_ERR_CUDA;
     MassParams p{};
     p.N = a.N;
     p.nKB = a.nKB;
+    p.last_rows = a.N - (a.nKB - 1) * BS;
     p.tiles_per_bh = (a.N + kMTile - 1) / kMTile;
     p.n_tiles = static_cast<int>(BH * p.tiles_per_bh);
     p.scale_log2 = a.scale * 1.4426950408889634f;
@@ -298,7 +306,7 @@ size_t exact_workspace_bytes(int B, int H, int N, int d, int block)
 {
     (void)d;
     const size_t tiles = static_cast<size_t>(B) * H * ((N + kMTile - 1) / kMTile);
-    const size_t nKB = static_cast<size_t>(N / block);
+    const size_t nKB = static_cast<size_t>((N + block - 1) / block);
     return kWsHeader + align_up(tiles * kMassWarps * nKB * sizeof(float), 256);
 }
 

@@ -41,7 +41,9 @@ __global__ void __launch_bounds__(kWarps * 32) fwd_simt_kernel(const float *__re
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t row0 = bh * N + static_cast<int64_t>(i) * BS;
 
-    for (int e = threadIdx.x; e < BS * D; e += blockDim.x) qs[e] = Q[row0 * D + e];
+    // rows of a ragged last block past the sequence end are zeros (and never written)
+    const int rows = min(BS, N - i * BS);
+    for (int e = threadIdx.x; e < BS * D; e += blockDim.x) qs[e] = e / D < rows ? Q[row0 * D + e] : 0.0f;
 
     float m[RPW], l[RPW], o[RPW][DPL];
 #pragma unroll
@@ -58,13 +60,15 @@ __global__ void __launch_bounds__(kWarps * 32) fwd_simt_kernel(const float *__re
     uint32_t mbits;
     while (walk.next(j, mbits)) {
         if (j < 0 || j >= nKB) continue;  // never read outside the head
-        for (int c0 = 0; c0 < BS; c0 += kChunk) {
+        const int keys = min(BS, N - j * BS);  // a ragged last KV block holds fewer keys
+        for (int c0 = 0; c0 < keys; c0 += kChunk) {
             __syncthreads();
             const int64_t krow = bh * N + static_cast<int64_t>(j) * BS + c0;
             for (int e = threadIdx.x; e < kChunk * D; e += blockDim.x) {
                 const int kk = e / D, c = e % D;
-                ks[kk * (D + 1) + c] = K[(krow + kk) * D + c];
-                vs[e] = V[(krow + kk) * D + c];
+                const bool in = c0 + kk < keys;
+                ks[kk * (D + 1) + c] = in ? K[(krow + kk) * D + c] : 0.0f;
+                vs[e] = in ? V[(krow + kk) * D + c] : 0.0f;
             }
             __syncthreads();
 #pragma unroll
@@ -74,7 +78,7 @@ __global__ void __launch_bounds__(kWarps * 32) fwd_simt_kernel(const float *__re
                 float s = 0.0f;
 #pragma unroll 16
                 for (int c = 0; c < D; ++c) s = fmaf(q[c], k[c], s);
-                s *= scale;
+                s = c0 + lane < keys ? s * scale : -CUDART_INF_F;  // keys past the end do not count
                 float cm = s;
 #pragma unroll
                 for (int off = 16; off > 0; off >>= 1) cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, off));
@@ -98,6 +102,7 @@ __global__ void __launch_bounds__(kWarps * 32) fwd_simt_kernel(const float *__re
     }
 #pragma unroll
     for (int r = 0; r < RPW; ++r) {
+        if (warp * RPW + r >= rows) break;
         const int64_t row = row0 + warp * RPW + r;
         const float inv = l[r] > 0.0f ? 1.0f / l[r] : 0.0f;
 #pragma unroll

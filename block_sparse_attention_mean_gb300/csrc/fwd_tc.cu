@@ -78,6 +78,8 @@ constexpr int kMergeWarps = 8;       // merge counters per split tile (one per s
 
 struct TcParams {
     int N, nQB, nKB, W, tiles_per_bh, n_tiles;
+    int ragged_kb;             // index of the last KV block when it holds fewer than BS keys, else -1
+    int last_rows;             // keys (and query rows) in the last block
     const int32_t *row_ptr;
     const int32_t *col_idx;
     const uint32_t *bitmap;
@@ -167,14 +169,21 @@ struct Cfg {
 // other roles need not walk the index to find out.
 constexpr int32_t kEmptyTile = 1 << 30;
 
-// Step descriptor the QK^T issuer leaves beside S/P buffer b (it is the only
-// consumer that walks the index): bits 0-1 blocks in the step, bits 2-3 and 4-5
-// which of the tile's Q blocks have block 0 and block 1 of the step, bit 6 set
-// on the tile's last step. The S-full barrier publishes it to the softmax warps
-// and the P-full barrier carries it on to the PV issuer.
-__device__ __forceinline__ uint32_t step_desc(int cnt, const uint32_t (&ms)[2], bool last)
+// Step descriptor (written by the K producer, copied beside S/P buffer b by the
+// QK^T issuer): bits 0-1 blocks in the step, bits 2-3 and 4-5 which of the tile's
+// Q blocks have block 0 and block 1 of the step, bit 6 set on the tile's last
+// step, bits 7 and 8 set when block 0 / block 1 of the step is a ragged last KV
+// block (keys past the sequence end must not count). The S-full barrier publishes
+// it to the softmax warps and the P-full barrier carries it on to the PV issuer.
+__device__ __forceinline__ uint32_t step_desc(int cnt, const uint32_t (&ms)[2], bool last, uint32_t ragged)
 {
-    return static_cast<uint32_t>(cnt) | (ms[0] << 2) | (ms[1] << 4) | (last ? 64u : 0u);
+    return static_cast<uint32_t>(cnt) | (ms[0] << 2) | (ms[1] << 4) | (last ? 64u : 0u) | (ragged << 7);
+}
+__device__ __forceinline__ uint32_t desc_ragged(uint32_t d) { return (d >> 7) & 3u; }
+// bit q set when block q of the step is the ragged last KV block
+__device__ __forceinline__ uint32_t ragged_bits(const TcParams &p, const int (&js)[2], int cnt)
+{
+    return (cnt > 0 && js[0] == p.ragged_kb ? 1u : 0u) | (cnt > 1 && js[1] == p.ragged_kb ? 2u : 0u);
 }
 __device__ __forceinline__ int desc_count(uint32_t d) { return static_cast<int>(d & 3u); }
 __device__ __forceinline__ uint32_t desc_members(uint32_t d, int q) { return (d >> (2 + 2 * q)) & 3u; }
@@ -453,6 +462,17 @@ __device__ __forceinline__ void softmax_rows(const TcParams &p, uint32_t sbase, 
                 tmem_wait_ld();
 #pragma unroll
                 for (int c = 0; c < NC; ++c) reg_fence32(sv[c]);
+                if (desc_ragged(sd) != 0u) {
+                    // keys past the sequence end in a ragged last block score -inf (p = 0)
+#pragma unroll
+                    for (int c = 0; c < NC; ++c) {
+                        if (((desc_ragged(sd) >> (c / CPB)) & 1u) == 0u) continue;
+                        const int key0 = (c % CPB) * 32;  // first key of chunk c within its block
+#pragma unroll
+                        for (int t = 0; t < 32; ++t)
+                            if (key0 + t >= p.last_rows) sv[c][t] = 0xFF800000u;
+                    }
+                }
                 // row max of the step's active scores, log2 units
                 auto step_max = [&]() -> float {
                     float mx0 = -CUDART_INF_F, mx1 = -CUDART_INF_F, mx2 = -CUDART_INF_F, mx3 = -CUDART_INF_F;
@@ -732,6 +752,16 @@ __device__ __forceinline__ void softmax_quads(const TcParams &p, uint32_t sbase,
                 tmem_ld_16x256b<RS>(tbase + b * C::kStep, sv);
                 tmem_wait_ld();
                 reg_fence(sv);
+                if (desc_ragged(sd) != 0u) {
+                    // keys past the sequence end in a ragged last block score -inf (p = 0)
+#pragma unroll
+                    for (int g = 0; g < RS; ++g) {
+                        if (((desc_ragged(sd) >> (g / GPB)) & 1u) == 0u) continue;
+                        const int key = (g % GPB) * 8 + cpair;  // this thread's first key of group g
+                        if (key >= p.last_rows) sv[4 * g] = sv[4 * g + 2] = 0xFF800000u;
+                        if (key + 1 >= p.last_rows) sv[4 * g + 1] = sv[4 * g + 3] = 0xFF800000u;
+                    }
+                }
                 float x0 = -CUDART_INF_F, x1 = -CUDART_INF_F, y0 = -CUDART_INF_F, y1 = -CUDART_INF_F;
 #pragma unroll
                 for (int g = 0; g < RS; g += 2) {
@@ -1026,14 +1056,13 @@ __global__ void __launch_bounds__((4 * SPLIT + 4) * 32, MINB)
                 if (stall || cnt == 0) continue;  // empty tile: nothing to load
                 const int qs = e % QS;  // Q slot; it was last used by tile e - QS
                 if (e >= QS && !warp_wait_all(bar(C::B_QEMPTY + qs), ((e / QS) - 1) & 1, ctl)) break;
-                const int qrow = static_cast<int>(bh * p.N) + qt * kTileM;
                 __syncwarp();
                 if (elect_one()) {
                     mbar_arrive_expect_tx(bar(C::B_QFULL + qs), C::kQBytes);
 #pragma unroll
                     for (int c = 0; c < D / 64; ++c)
-                        tma_load_2d(sbase + C::Q_OFF + qs * C::kQBytes + c * C::kQChunk, &tmQ, c * 64, qrow,
-                                    bar(C::B_QFULL + qs));
+                        tma_load_3d(sbase + C::Q_OFF + qs * C::kQBytes + c * C::kQChunk, &tmQ, c * 64, qt * kTileM,
+                                    static_cast<int>(bh), bar(C::B_QFULL + qs));
                 }
                 __syncwarp();
                 q_issued = e;
@@ -1046,14 +1075,14 @@ __global__ void __launch_bounds__((4 * SPLIT + 4) * 32, MINB)
                         break;
                     }
                     if (elect_one()) {
-                        kdesc[ks] = step_desc(cnt, ms, cnt_n == 0);  // released by the arrive below
+                        // released by the arrive below
+                        kdesc[ks] = step_desc(cnt, ms, cnt_n == 0, ragged_bits(p, js, cnt));
                         mbar_arrive_expect_tx(bar(C::B_KFULL + ks), static_cast<uint32_t>(cnt * BS * D * 2));
                         for (int q = 0; q < cnt; ++q) {
-                            const int krow = static_cast<int>(bh * p.N) + js[q] * BS;
 #pragma unroll
                             for (int c = 0; c < D / 64; ++c)
-                                tma_load_2d(sbase + C::K_OFF + ks * C::kKVBytes + c * C::kKVChunk + q * BS * 128,
-                                            &tmK, c * 64, krow, bar(C::B_KFULL + ks));
+                                tma_load_3d(sbase + C::K_OFF + ks * C::kKVBytes + c * C::kKVChunk + q * BS * 128,
+                                            &tmK, c * 64, js[q] * BS, static_cast<int>(bh), bar(C::B_KFULL + ks));
                         }
                     }
                     __syncwarp();
@@ -1111,11 +1140,10 @@ __global__ void __launch_bounds__((4 * SPLIT + 4) * 32, MINB)
                     if (elect_one()) {
                         mbar_arrive_expect_tx(bar(C::B_VFULL + vs), static_cast<uint32_t>(cnt * BS * D * 2));
                         for (int q = 0; q < cnt; ++q) {
-                            const int vrow = static_cast<int>(bh * p.N) + js[q] * BS;
 #pragma unroll
                             for (int c = 0; c < D / 64; ++c)
-                                tma_load_2d(sbase + C::V_OFF + vs * C::kKVBytes + c * C::kKVChunk + q * BS * 128,
-                                            &tmV, c * 64, vrow, bar(C::B_VFULL + vs));
+                                tma_load_3d(sbase + C::V_OFF + vs * C::kKVBytes + c * C::kKVChunk + q * BS * 128,
+                                            &tmV, c * 64, js[q] * BS, static_cast<int>(bh), bar(C::B_VFULL + vs));
                         }
                     }
                     __syncwarp();
@@ -1644,14 +1672,16 @@ bsa_status launch_tc(const FwdArgs &a, cudaStream_t st)
     const int64_t BH = static_cast<int64_t>(a.B) * a.H;
     const uint64_t rows = static_cast<uint64_t>(BH) * a.N;
     CUtensorMap mq, mk, mv;
-    if (!make_tma_map_bf16(&mq, a.Q, rows, D, kTileM) || !make_tma_map_bf16(&mk, a.K, rows, D, BS) ||
-        !make_tma_map_bf16(&mv, a.V, rows, D, BS))
+    if (!make_tma_map_bf16(&mq, a.Q, BH, a.N, D, kTileM) || !make_tma_map_bf16(&mk, a.K, BH, a.N, D, BS) ||
+        !make_tma_map_bf16(&mv, a.V, BH, a.N, D, BS))
         return BSA_ERR_CUDA;
     WsHeader *hdr = reinterpret_cast<WsHeader *>(a.ws);
     TcParams p{};
     p.N = a.N;
     p.nQB = a.nQB;
     p.nKB = a.nKB;
+    p.last_rows = a.N - (a.nKB - 1) * BS;
+    p.ragged_kb = p.last_rows < BS ? a.nKB - 1 : -1;
     p.W = a.W;
     p.tiles_per_bh = (a.N + kTileM - 1) / kTileM;
     p.n_tiles = static_cast<int>(BH * p.tiles_per_bh);
@@ -1734,15 +1764,16 @@ static EncodeTiledFn encode_fn()
 }
 
 // 2-D view [rows][d] of a bf16 tensor, 64-column x box_rows boxes, 128-byte swizzle.
-bool make_tma_map_bf16(CUtensorMap *m, const void *base, uint64_t rows, int d, int box_rows)
+bool make_tma_map_bf16(CUtensorMap *m, const void *base, uint64_t heads, uint64_t n, int d, int box_rows)
 {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
-    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows)};
-    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(d) * 2};
-    const cuuint32_t box[2] = {64u, static_cast<cuuint32_t>(box_rows)};
-    const cuuint32_t es[2] = {1u, 1u};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, es,
+    // {column, row, head}: a box never crosses into the next head; rows >= n read as zeros
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(n), static_cast<cuuint64_t>(heads)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(d) * 2 * n};
+    const cuuint32_t box[3] = {64u, static_cast<cuuint32_t>(box_rows), 1u};
+    const cuuint32_t es[3] = {1u, 1u, 1u};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, es,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }

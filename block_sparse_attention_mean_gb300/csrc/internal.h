@@ -96,8 +96,9 @@ struct FwdArgs {
 };
 
 size_t fwd_workspace_bytes(int B, int H, int N, int d, int block);
-// 2-D TMA view [rows][d] of a bf16 tensor with 64-column x box_rows boxes and 128-byte swizzle
-bool make_tma_map_bf16(CUtensorMap *m, const void *base, uint64_t rows, int d, int box_rows);
+// 3-D TMA view [heads][n][d] of a bf16 tensor with 64-column x box_rows boxes and 128-byte swizzle;
+// rows at or past n (a ragged last block) read as zeros
+bool make_tma_map_bf16(CUtensorMap *m, const void *base, uint64_t heads, uint64_t n, int d, int box_rows);
 bsa_status launch_forward_tc(const FwdArgs &a, cudaStream_t st);    // bf16, tcgen05
 bsa_status launch_forward_simt(const FwdArgs &a, cudaStream_t st);  // fp32, CUDA cores
 bsa_status launch_residual_capture(const void *dense, const void *sparse, int dt, int64_t count, float *R,

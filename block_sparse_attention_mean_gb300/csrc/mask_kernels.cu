@@ -14,7 +14,8 @@
 //   static_rows_kernel -> counts, scan_kernel -> row_ptr, emit_kernel -> col_idx
 //   ascending (§4.1 index forms).
 // Arithmetic of the selector is fixed so results are reproducible bit for bit:
-// pooled sums in token order with round-to-nearest adds, scaled by 1/bs (exact);
+// pooled sums in token order with round-to-nearest adds, divided by the block's
+// token count (round to nearest; a full block's 1/bs scaling is exact);
 // scores as an fmaf chain over channels from +0; order by value with -0 == +0,
 // ties to the lower block index.
 #include <cuda_bf16.h>
@@ -71,22 +72,21 @@ __global__ void __launch_bounds__(kPoolThreads) pool_kernel(const T *__restrict_
     const int i = static_cast<int>(rest % nB);
     const int64_t bh = rest / nB;
     const T *src = X + (bh * N + static_cast<int64_t>(i) * bs) * d + cg * 8;
+    const int cnt = min(bs, N - i * bs);  // a ragged last block holds fewer tokens
     float acc[8];
 #pragma unroll
     for (int e = 0; e < 8; ++e) acc[e] = 0.0f;
 #pragma unroll 8
-    for (int t = 0; t < bs; ++t) {
+    for (int t = 0; t < cnt; ++t) {
         float x[8];
         load8(src + static_cast<int64_t>(t) * d, x);
 #pragma unroll
         for (int e = 0; e < 8; ++e) acc[e] = __fadd_rn(acc[e], x[e]);
     }
-    const float inv = 1.0f / static_cast<float>(bs);  // power of two: exact
+    const float n = static_cast<float>(cnt);
     float *dst = out + (bh * nB + i) * static_cast<int64_t>(d) + cg * 8;
-    float4 lo = make_float4(__fmul_rn(acc[0], inv), __fmul_rn(acc[1], inv), __fmul_rn(acc[2], inv),
-                            __fmul_rn(acc[3], inv));
-    float4 hi = make_float4(__fmul_rn(acc[4], inv), __fmul_rn(acc[5], inv), __fmul_rn(acc[6], inv),
-                            __fmul_rn(acc[7], inv));
+    float4 lo = make_float4(__fdiv_rn(acc[0], n), __fdiv_rn(acc[1], n), __fdiv_rn(acc[2], n), __fdiv_rn(acc[3], n));
+    float4 hi = make_float4(__fdiv_rn(acc[4], n), __fdiv_rn(acc[5], n), __fdiv_rn(acc[6], n), __fdiv_rn(acc[7], n));
     reinterpret_cast<float4 *>(dst)[0] = lo;
     reinterpret_cast<float4 *>(dst)[1] = hi;
 }
@@ -550,7 +550,7 @@ struct MaskWs {
 MaskWs mask_ws_layout(int B, int H, int N, int d, int block)
 {
     const size_t BH = static_cast<size_t>(B) * H;
-    const size_t nB = static_cast<size_t>(N / block);
+    const size_t nB = static_cast<size_t>((N + block - 1) / block);
     const size_t W = (nB + 31) / 32;
     MaskWs l{};
     l.qbar = kWsHeader;

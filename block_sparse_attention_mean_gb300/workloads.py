@@ -70,11 +70,11 @@ class Workload:
 
     @property
     def nQB(self) -> int:
-        return self.N // self.block
+        return -(-self.N // self.block)  # a ragged last block counts
 
     @property
     def nKB(self) -> int:
-        return self.N // self.block
+        return -(-self.N // self.block)  # a ragged last block counts
 
 
 WORKLOADS: Dict[str, Workload] = {

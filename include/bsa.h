@@ -12,7 +12,11 @@
  *   - Q, K, V, O are row-major [B][H][N][d], contiguous, in device memory.
  *     dtype BSA_BF16 (bf16 inputs, bf16 O) or BSA_FP32 (fp32 inputs, fp32 O).
  *     LSE is fp32 [B][H][N], natural logarithm.
- *   - block (bs) in {64, 128}; d in {64, 128}; N % block == 0; nQB = nKB = N / block.
+ *   - block (bs) in {64, 128}; d in {64, 128}; N >= 1; nQB = nKB = ceil(N / block).
+ *     When N is not a multiple of block the last block is ragged: it holds the tokens
+ *     up to N ("多模态DiT中的块稀疏注意力" §4.1, the tile loop's padding mask); keys past N
+ *     do not count, rows past N do not exist, and mean pooling averages the tokens the
+ *     block holds.
  *   - Index: rows r = (b*H + h)*nQB + i.
  *       row_ptr  int32 [B*H*nQB + 1], exclusive prefix sums of row lengths;
  *       col_idx  int32 [nnz], the active KV block ids of each row, strictly ascending;
@@ -46,7 +50,7 @@ extern "C" {
 typedef enum {
     BSA_OK = 0,
     BSA_ERR_INVALID_ARG = 1, /* null pointer, bad enum, density out of (0, 1], misaligned buffer */
-    BSA_ERR_SHAPE = 2,       /* unsupported B, H, N, d or block, or N % block != 0 */
+    BSA_ERR_SHAPE = 2,       /* unsupported B, H, N, d or block */
     BSA_ERR_DTYPE = 3,       /* dtype not supported for this call */
     BSA_ERR_CAPACITY = 4,    /* col_capacity smaller than the mask's nnz */
     BSA_ERR_NONFINITE = 5,   /* a block score was NaN (device-raised) */

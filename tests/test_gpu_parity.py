@@ -76,6 +76,31 @@ def test_video_small_grid_all_rows():
     run_workload(w)
 
 
+# ------------------------------------------------------------ ragged last block
+#
+# N not a multiple of the block size: the last block holds the keys and query rows up to
+# N (the tile loop's padding mask) and pooling averages the tokens it holds. Index bit for
+# bit, then the forward in both index modes and with every tile split.
+
+RAGGED_CASES = {
+    "tiny_fp32": wl.scaled(wl.WORKLOADS["tiny"], N=475),                           # SIMT path
+    "t2i_d64_bs64": wl.scaled(wl.WORKLOADS["t2i_static"], B=1, H=2, N=4224 - 40),  # last block: 24 rows
+    "dynamic_d128_bs64": wl.scaled(wl.WORKLOADS["dynamic_topk"], H=2, N=1000),     # last block: 40 rows
+    "long_d128_bs128": wl.scaled(wl.WORKLOADS["long_sweep_bs128"], H=2, N=1000, density=0.5),
+    "d64_bs128": wl.scaled(wl.WORKLOADS["long_sweep_bs128"], H=2, N=900, d=64, density=0.5),
+}
+
+
+@pytest.mark.parametrize("name", sorted(RAGGED_CASES))
+def test_ragged_sequence_matches_oracle(name):
+    w = RAGGED_CASES[name]
+    assert w.N % w.block != 0
+    run_workload(w)
+    if w.dtype == "bf16":
+        run_workload(w, index_mode=1 - w.index_mode)
+        _run_with_flags(w, bb.DBG_SPLIT_ALL)
+
+
 # ------------------------------------------------------------ split query tiles
 #
 # A tile whose step count is well above the per-CTA share is split by KV block
@@ -269,6 +294,8 @@ EXACT_CASES = {
     "d128_bs64": (wl.scaled(wl.WORKLOADS["dynamic_topk"], H=2, N=2048), 0.15),
     "d64_bs128": (wl.scaled(wl.WORKLOADS["t2i_static"], B=1, H=2, N=2048, block=128), 0.25),
     "d128_bs128": (wl.scaled(wl.WORKLOADS["long_topk"], H=2, N=4096), 0.1),
+    # ragged last block: 32 blocks of 64, the last holding 16 keys (zero-filled loads, masked)
+    "d128_bs64_ragged": (wl.scaled(wl.WORKLOADS["dynamic_topk"], H=2, N=2000), 0.15),
 }
 MASS_RTOL = 2e-3
 

@@ -54,12 +54,22 @@ def test_workspace_sizes(lib):
     # a tiny problem gets at most 8 partial slots per tile
     tiny = bb.bsa_workspace_size(1, 1, 1, 128, 64, 64)
     assert tiny == 256 + up(9 * 4) + 2 * up(4) + up(8 * 8 * 4) + up(8 * 128 * 16) + up(8 * 128 * 64 * 4)
+    # a ragged sequence (N not a multiple of the block) has ceil(N / 128) query tiles
+    assert bb.bsa_workspace_size(1, 1, 1, 100, 64, 64) == tiny
+    assert bb.bsa_workspace_size(0, 1, 1, 100, 64, 64) == bb.bsa_workspace_size(0, 1, 1, 128, 64, 64)
     with pytest.raises(bb.BsaError) as e:
-        bb.bsa_workspace_size(1, 1, 1, 100, 64, 64)
+        bb.bsa_workspace_size(1, 1, 1, 0, 64, 64)
     assert e.value.code == bb.ERR_SHAPE
     with pytest.raises(bb.BsaError) as e:
         bb.bsa_workspace_size(3, 1, 1, 128, 64, 64)  # 0 mask, 1 forward, 2 exact selector
     assert e.value.code == bb.ERR_INVALID_ARG
+
+
+def test_ragged_sequence_block_counts(lib):
+    # N = 500 at block 64: 8 blocks, the last one holding 52 tokens; k = floor(0.5 * 8) = 4
+    assert bb.bsa_mask_nnz(1, 2, 500, 64, 0.5, None) == 2 * 8 * 4
+    assert bb.bsa_mask_nnz(1, 1, 500, 128, 0.25, None) == 4 * 1
+    assert bb.bsa_mask_nnz_modal(1, 1, 500, 64, 2, [1.0, 1.0, 1.0, 0.5]) == 2 * 8 + 6 * (2 + 3)
 
 
 def test_mask_nnz_counts(lib):
@@ -105,7 +115,7 @@ def _fwd(**kw):
 
 
 def test_build_mask_rejects_bad_arguments(lib):
-    assert _build(N=500) == bb.ERR_SHAPE            # N % block
+    assert _build(N=0) == bb.ERR_SHAPE              # empty sequence
     assert _build(d=96) == bb.ERR_SHAPE
     assert _build(block=32) == bb.ERR_SHAPE
     assert _build(dt=7) == bb.ERR_DTYPE
@@ -129,7 +139,7 @@ def test_build_mask_rejects_bad_arguments(lib):
 
 
 def test_forward_rejects_bad_arguments(lib):
-    assert _fwd(N=500) == bb.ERR_SHAPE
+    assert _fwd(N=0) == bb.ERR_SHAPE
     assert _fwd(d=32) == bb.ERR_SHAPE
     assert _fwd(dt=5) == bb.ERR_DTYPE
     assert _fwd(V=None) == bb.ERR_INVALID_ARG
@@ -176,7 +186,7 @@ def test_residual_entry_points_reject_bad_arguments(lib):
     # bsa_forward_residual: the residual pointer, then every bsa_forward check
     assert _fwd_res(R=None) == bb.ERR_INVALID_ARG
     assert _fwd_res(R=FAKE + 4) == bb.ERR_INVALID_ARG  # fp32 rows read 16 bytes at a time
-    assert _fwd_res(N=500) == bb.ERR_SHAPE
+    assert _fwd_res(N=0) == bb.ERR_SHAPE
     assert _fwd_res(dt=5) == bb.ERR_DTYPE
     assert _fwd_res(workspace=None) == bb.ERR_WORKSPACE
     # bsa_residual_capture
@@ -206,7 +216,7 @@ def test_modal_counts_and_rejects_bad_arguments(lib):
     args = dict(Q=FAKE, K=FAKE, dt=bb.BF16, B=1, H=2, N=512, d=64, block=64, n_text_blocks=2, density=dens,
                 row_ptr=FAKE, col_idx=FAKE, col_capacity=1 << 20, bitmap=FAKE, workspace=FAKE,
                 workspace_bytes=1 << 30)
-    for kw, code in [(dict(N=500), bb.ERR_SHAPE), (dict(dt=4), bb.ERR_DTYPE), (dict(Q=None), bb.ERR_INVALID_ARG),
+    for kw, code in [(dict(N=0), bb.ERR_SHAPE), (dict(dt=4), bb.ERR_DTYPE), (dict(Q=None), bb.ERR_INVALID_ARG),
                      (dict(n_text_blocks=-1), bb.ERR_INVALID_ARG), (dict(density=[2.0, 0, 0, 0]), bb.ERR_INVALID_ARG),
                      (dict(workspace=None), bb.ERR_WORKSPACE), (dict(col_capacity=3), bb.ERR_CAPACITY)]:
         a = dict(args)
@@ -225,7 +235,7 @@ def test_exact_selector_workspace_and_bad_arguments(lib):
                 workspace_bytes=1 << 30)
     for kw, code in [(dict(dt=bb.FP32), bb.ERR_UNSUPPORTED), (dict(dt=7), bb.ERR_DTYPE),
                      (dict(LSE=None), bb.ERR_INVALID_ARG), (dict(density=0.0), bb.ERR_INVALID_ARG),
-                     (dict(scale=float("inf")), bb.ERR_INVALID_ARG), (dict(N=500), bb.ERR_SHAPE),
+                     (dict(scale=float("inf")), bb.ERR_INVALID_ARG), (dict(N=0), bb.ERR_SHAPE),
                      (dict(workspace_bytes=16), bb.ERR_WORKSPACE), (dict(col_capacity=15), bb.ERR_CAPACITY)]:
         a = dict(args)
         a.update(kw)
