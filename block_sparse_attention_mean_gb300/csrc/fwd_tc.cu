@@ -1008,6 +1008,8 @@ __global__ void __launch_bounds__((4 * SPLIT + 4) * 32, MINB)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    // the prologue above may overlap the work-list launch; its results are read from here on
+    grid_dependency_wait();
     const uint32_t tmem = misc[0];
     const Ctl ctl{reinterpret_cast<volatile uint32_t *>(misc + 1), p.err, p.wait_limit_ns};
     const bool stall = (p.dbg & kDbgStall) != 0u;
@@ -1406,6 +1408,7 @@ struct OrderArgs {
 // on item length, clamped) and resets the scheduler counter.
 __global__ void __launch_bounds__(1024) tile_order_kernel(TcParams p, OrderArgs o)
 {
+    grid_launch_dependents();  // the forward's prologue may start now (it waits for this grid's results)
     __shared__ int hist[kBuckets];
     __shared__ int wsum[32];
     __shared__ bool is_last;
@@ -1512,6 +1515,7 @@ constexpr int kOrderPerThread = 8;
 
 __global__ void __launch_bounds__(1024) tile_order_small_kernel(TcParams p, OrderArgs o)
 {
+    grid_launch_dependents();  // the forward's prologue may start now (it waits for this grid's results)
     __shared__ int hist[kBuckets];
     __shared__ int wsum[32];
     __shared__ unsigned red[64];
@@ -1721,7 +1725,19 @@ bsa_status launch_tc(const FwdArgs &a, cudaStream_t st)
         tile_order_small_kernel<<<1, 1024, 0, st>>>(p, o);
     else
         tile_order_kernel<<<(p.n_tiles + 1023) / 1024, 1024, 0, st>>>(p, o);
-    kern<<<grid, kThreads, C::SMEM_ALLOC, st>>>(mq, mk, mv, p);
+    // programmatic dependent launch: the forward's CTAs set up barriers and TMEM while the
+    // work-list launch runs, and wait for its results in-kernel
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = C::SMEM_ALLOC;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, kern, mq, mk, mv, p) != cudaSuccess) return BSA_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? BSA_OK : BSA_ERR_CUDA;
 }
 

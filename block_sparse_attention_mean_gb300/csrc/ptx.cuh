@@ -90,6 +90,14 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
         : "memory");
 }
 
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialisation may start while the previous kernel in the stream runs; it must wait
+// here before reading that kernel's results (a no-op without the launch attribute).
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Lets the next kernel in the stream be scheduled before this one finishes (it still
+// waits for this kernel's completion in grid_dependency_wait).
+__device__ __forceinline__ void grid_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" :::); }
+
 // 3-D tiled load: {x, y, z} = {column, row within the head, head}. Rows past the head's
 // last row are outside the tensor and arrive as zeros (they still count as box bytes).
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, int x, int y, int z,
