@@ -475,6 +475,27 @@ def test_nan_score_raises_nonfinite():
     assert e.value.code == bb.ERR_NONFINITE
 
 
+@pytest.mark.parametrize("N", [512, 16384])
+def test_broadcast_explicit_mask(N):
+    # one bitmap for every (b, h), built once and copied into every head: index bit for bit
+    # against the oracle's at two sizes, and the forward on the small one
+    w = wl.scaled(wl.WORKLOADS["tiny"], dtype="bf16", B=2, H=3, N=N)
+    rng = np.random.default_rng(N)
+    one = (rng.random((w.nQB, w.nKB)) < 0.3).astype(np.uint8)
+    one[np.arange(w.nQB), np.arange(w.nKB)] = 1
+    mask = np.broadcast_to(one, (w.B, w.H, w.nQB, w.nKB)).copy()
+    words = torch.from_numpy(gu.mask_bitmap_words(one[None, None]).reshape(-1)).cuda()
+    idx = bb.build_mask(None, None, w.block, spec=bb.explicit_spec(words, broadcast_bh=True),
+                        shape=(w.B, w.H, w.N, w.d))
+    gu.assert_index_equal(idx, mask)
+    if N == 512:
+        inp = wl.make_inputs(w)
+        q, k, v = (gu.upload(inp, n) for n in ("q", "k", "v"))
+        O, L = bb.forward(q, k, v, idx)
+        torch.cuda.synchronize()
+        gu.assert_attention_close(O, L, inp, mask, w)
+
+
 def test_explicit_capacity_overflow_is_reported():
     w = wl.scaled(wl.WORKLOADS["tiny"], dtype="bf16")
     inp = wl.make_inputs(w)
