@@ -261,3 +261,103 @@ def residual(o_dense: np.ndarray, o_sparse: np.ndarray) -> np.ndarray:
 def compensate(o_sparse: np.ndarray, r: np.ndarray) -> np.ndarray:
     """Residual-compensated output of a later step, O_sparse + R, in double (same section)."""
     return np.asarray(o_sparse, dtype=np.float64) + np.asarray(r, dtype=np.float64)
+
+
+# ---------------------------------------------------------------- token-level selection
+#
+# [P3] "Can sparse attention close the quality gap in diffusion transformers", section
+# "token 级选择需要瓦片对齐的查询分组": queries of a head are put in groups of exactly C
+# similar queries (C = the kernel's query tile) by a median split along the principal
+# direction, applied recursively; each group then shares one set of individually
+# selected KV tokens, gathered by index. The exact token selection uses the dense
+# probabilities (the token oracle of section "质量差距有三个可分离来源"): per group and key
+# token, the attention mass the group's queries give it under dense attention.
+
+
+def query_groups(q: np.ndarray, C: int) -> np.ndarray:
+    """Median-split principal-direction grouping of one head's queries (reading R21).
+
+    q: [N, d] (N a multiple of C). A group of m*C rows (m >= 2) is centred, projected on the
+    eigenvector of the largest eigenvalue of its scatter matrix (sign: its entry of largest
+    magnitude positive), its rows ordered by (projection, row index), and cut after the
+    first ceil(m/2)*C rows; the two halves are split again until every group holds C rows.
+    Returns perm [N]: group g is rows perm[g*C:(g+1)*C], groups in depth-first order
+    (first half before second half), rows inside a group in ascending index order.
+    """
+    x = np.asarray(q, dtype=np.float64)
+    N = x.shape[0]
+    if C <= 0 or N % C != 0:
+        raise ValueError("N must be a positive multiple of C")
+    out = []
+
+    def split(rows: np.ndarray):
+        m = rows.size // C
+        if m == 1:
+            out.append(np.sort(rows))
+            return
+        xc = x[rows] - x[rows].mean(axis=0)
+        w, vecs = np.linalg.eigh(xc.T @ xc)
+        u = vecs[:, np.argmax(w)]
+        if u[np.argmax(np.abs(u))] < 0:
+            u = -u
+        proj = xc @ u
+        order = rows[np.lexsort((rows, proj))]
+        cut = -(-m // 2) * C
+        split(order[:cut])
+        split(order[cut:])
+
+    split(np.arange(N))
+    return np.concatenate(out)
+
+
+def token_mass(q: np.ndarray, k: np.ndarray, lse: np.ndarray, perm: np.ndarray, C: int,
+               scale: Optional[float] = None) -> np.ndarray:
+    """Exact attention mass of every (query group, key token) pair of one head, in double:
+    mass[g, t] = sum over rows r of group g of exp(scale * q_r . k_t - LSE_r), with the dense
+    row logsumexp LSE_r. Returns [N/C, N]."""
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    lse = np.asarray(lse, dtype=np.float64)
+    sc = 1.0 / math.sqrt(q.shape[1]) if scale is None else float(scale)
+    G = q.shape[0] // C
+    out = np.empty((G, k.shape[0]))
+    for g in range(G):
+        rows = perm[g * C:(g + 1) * C]
+        out[g] = np.exp(sc * (q[rows] @ k.T) - lse[rows][:, None]).sum(axis=0)
+    return out
+
+
+def select_tokens(mass: np.ndarray, density: float) -> np.ndarray:
+    """The token oracle's selection (reading R22): per group the K = max(1, floor(density * N))
+    tokens of largest mass, ties to the lower index; returns [groups, K], ascending per row."""
+    G, N = mass.shape
+    K = topk_count(density, N)
+    sel = np.empty((G, K), np.int64)
+    for g in range(G):
+        order = np.lexsort((np.arange(N), -mass[g]))  # mass descending, then index ascending
+        sel[g] = np.sort(order[:K])
+    return sel
+
+
+def token_attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, perm: np.ndarray, tokens: np.ndarray,
+                    C: int, scale: Optional[float] = None):
+    """Token-sparse attention of one head in double (reading R23): each row r of group g attends
+    to the keys tokens[g] only, O_r = sum_t softmax_t(scale * q_r . k_t) v_t and
+    LSE_r = ln sum_t exp(scale * q_r . k_t), t over tokens[g]. Returns O [N, d], LSE [N] in row order."""
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    N, d = q.shape
+    sc = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    O = np.empty((N, v.shape[1]))
+    L = np.empty(N)
+    for g in range(N // C):
+        rows = perm[g * C:(g + 1) * C]
+        t = tokens[g]
+        s = sc * (q[rows] @ k[t].T)
+        m = s.max(axis=1, keepdims=True)
+        p = np.exp(s - m)
+        l = p.sum(axis=1, keepdims=True)
+        O[rows] = (p @ v[t]) / l
+        L[rows] = (m + np.log(l))[:, 0]
+    return O, L

@@ -515,3 +515,108 @@ def test_ragged_block_mass_rows_hold_one_unit_per_query_row():
     np.testing.assert_allclose(mass[0].sum(axis=1), [16, 16, 6], rtol=1e-12)
     # the ragged block's mass against a brute-force sum over its 6 keys
     np.testing.assert_allclose(mass[0, 0, 2], np.exp(s[:16, 32:] - lse[:16, None]).sum(), rtol=1e-12)
+
+
+# ---------------------------------------------------------------- token-level selection (readings R21-R23)
+
+
+def test_query_groups_partition_and_sizes():
+    q = _rand(384, 8)
+    perm = oracle.query_groups(q, 128)
+    assert sorted(perm.tolist()) == list(range(384))
+    for g in range(3):
+        grp = perm[g * 128:(g + 1) * 128]
+        assert np.all(np.diff(grp) > 0)  # ascending inside a group
+    with pytest.raises(ValueError):
+        oracle.query_groups(_rand(300, 8), 128)
+
+
+@pytest.mark.parametrize("m", [2, 3, 4, 5])
+def test_query_groups_on_a_line_are_sorted_chunks(m):
+    # points on one line: the principal direction is that line, so every median split keeps
+    # the order along it and the groups are consecutive runs of the sorted coordinate
+    C = 4
+    t = RNG.permutation(m * C).astype(np.float64) * 0.37 + RNG.random(m * C) * 0.01
+    e = np.array([3.0, -4.0, 0.0]) / 5.0
+    q = (t[:, None] * e[None, :]).astype(np.float32)
+    perm = oracle.query_groups(q, C)
+    order = np.argsort(t)
+    got = {frozenset(perm[g * C:(g + 1) * C].tolist()) for g in range(m)}
+    # the direction's sign decides which end comes first; the runs themselves do not change
+    want = {frozenset(order[g * C:(g + 1) * C].tolist()) for g in range(m)}
+    assert got == want
+
+
+def test_query_groups_separate_two_clusters():
+    C = 16
+    a = _rand(C, 6) * 0.1 + np.array([10, 0, 0, 0, 0, 0], np.float32)
+    b = _rand(C, 6) * 0.1 - np.array([10, 0, 0, 0, 0, 0], np.float32)
+    idx = RNG.permutation(2 * C)
+    q = np.concatenate([a, b])[idx]
+    perm = oracle.query_groups(q, C)
+    in_b = set(np.where(idx >= C)[0].tolist())  # rows holding cluster b (the lower projections)
+    assert set(perm[:C].tolist()) == in_b
+
+
+def test_query_groups_follow_a_row_permutation():
+    q = _rand(256, 5)
+    perm = oracle.query_groups(q, 32)
+    shuffle = RNG.permutation(256)
+    perm2 = oracle.query_groups(q[shuffle], 32)
+    for g in range(8):
+        assert set(shuffle[perm2[g * 32:(g + 1) * 32]].tolist()) == set(perm[g * 32:(g + 1) * 32].tolist())
+
+
+def test_token_mass_rows_hold_one_unit_per_query():
+    N, d, C = 64, 8, 16
+    q, k = _rand(N, d), _rand(N, d)
+    s = (q.astype(np.float64) @ k.astype(np.float64).T) / math.sqrt(d)
+    lse = scipy.special.logsumexp(s, axis=-1)
+    perm = oracle.query_groups(q, C)
+    mass = oracle.token_mass(q, k, lse, perm, C)
+    np.testing.assert_allclose(mass.sum(axis=1), C, rtol=1e-12)
+    # brute force of one entry, and the block mass when the groups are the blocks
+    g, t = 2, 37
+    want = sum(math.exp(s[r, t] - lse[r]) for r in perm[g * C:(g + 1) * C])
+    assert math.isclose(mass[g, t], want, rel_tol=1e-12)
+    ident = np.arange(N)
+    mb = oracle.token_mass(q, k, lse, ident, C).reshape(N // C, N // C, C).sum(axis=2)
+    np.testing.assert_allclose(mb, oracle.block_mass(q[None], k[None], lse[None], C)[0], rtol=1e-12)
+
+
+def test_select_tokens_keeps_the_largest_with_low_index_ties():
+    mass = RNG.integers(0, 6, size=(5, 40)).astype(np.float64)
+    sel = oracle.select_tokens(mass, 0.25)
+    K = 10
+    assert sel.shape == (5, K)
+    for g in range(5):
+        chosen = set(sel[g].tolist())
+        assert np.all(np.diff(sel[g]) > 0)
+        rest = [t for t in range(40) if t not in chosen]
+        lo = min(mass[g, t] for t in chosen)
+        assert all(mass[g, t] <= lo for t in rest)
+        # a tie at the boundary goes to the lower indices
+        assert all(t > max(c for c in chosen if mass[g, c] == lo) for t in rest if mass[g, t] == lo)
+
+
+def test_token_attention_all_tokens_is_dense_and_subset_is_masked_dense():
+    N, d, C = 48, 6, 16
+    q, k, v = _rand(N, d), _rand(N, d), _rand(N, d)
+    perm = oracle.query_groups(q, C)
+    full = np.tile(np.arange(N), (N // C, 1))
+    O, L = oracle.token_attention(q, k, v, perm, full, C, scale=0.4)
+    Od, Ld = _dense_library(q, k, v, 0.4, np.ones((N, N), bool))
+    np.testing.assert_allclose(O, Od, rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(L, Ld, rtol=1e-12)
+    tokens = np.stack([np.sort(RNG.choice(N, size=7, replace=False)) for _ in range(N // C)])
+    O, L = oracle.token_attention(q, k, v, perm, tokens, C, scale=0.4)
+    allowed = np.zeros((N, N), bool)
+    for g in range(N // C):
+        allowed[np.ix_(perm[g * C:(g + 1) * C], tokens[g])] = True
+    Od, Ld = _dense_library(q, k, v, 0.4, allowed)
+    np.testing.assert_allclose(O, Od, rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(L, Ld, rtol=1e-12)
+    one = np.full((N // C, 1), 5)
+    O, L = oracle.token_attention(q, k, v, perm, one, C, scale=0.4)
+    np.testing.assert_allclose(O, np.tile(v[5].astype(np.float64), (N, 1)), rtol=1e-12)
+    np.testing.assert_allclose(L, 0.4 * (q.astype(np.float64) @ k[5].astype(np.float64)), rtol=1e-12)
