@@ -51,6 +51,9 @@ def parse_args():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(wl.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--tokens", type=float, default=0.0,
+                    help="time the token-sparse forward (bsa_forward_tokens) at this token density instead: "
+                         "groups of 128 queries and K = floor(density * N) tokens per group, both seeded random")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--residual", action="store_true",
                     help="time bsa_forward_residual (residual compensation) with R captured at warm-up")
@@ -489,11 +492,75 @@ def run_reference(args, world, rank):
     del bb
 
 
+def run_tokens(args):
+    """Token-sparse forward on one GPU: the workload's Q, K, V, seeded random query groups and
+    token sets (the timing does not depend on which tokens are chosen), L2 flushed before every
+    call, CUDA events on the launching stream."""
+    import torch
+
+    from block_sparse_attention_mean_gb300 import binding as bb
+    from block_sparse_attention_mean_gb300 import build as bbuild
+
+    bbuild.build()
+    bb.load()
+    w = wl.WORKLOADS[args.workload]
+    inp = wl.make_inputs(w)
+    dev = torch.device("cuda", 0)
+    up = (lambda n: torch.from_numpy(inp[n + "_bits"].view(np.int16)).to(dev).view(torch.bfloat16)) \
+        if w.dtype == "bf16" else (lambda n: torch.from_numpy(inp[n]).to(dev))
+    q, k, v = up("q"), up("k"), up("v")
+    BH, N, d, C = w.B * w.H, w.N, w.d, 128
+    K = max(1, int(np.floor(args.tokens * N)))
+    rng = np.random.default_rng(w.seed)
+    perm = torch.from_numpy(np.stack([rng.permutation(N) for _ in range(BH)]).astype(np.int32)).to(dev)
+    toks = torch.from_numpy(np.stack([np.sort(rng.choice(N, size=(K,), replace=False))
+                                      for _ in range(BH * (N // C))]).reshape(BH, N // C, K).astype(np.int32)).to(dev)
+    ws = torch.zeros(256, dtype=torch.uint8, device=dev)
+    O = torch.empty_like(q)
+    L = torch.empty((w.B, w.H, N), dtype=torch.float32, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def call():
+        bb.bsa_forward_tokens(q, k, v, bb.BF16 if w.dtype == "bf16" else bb.FP32, w.B, w.H, N, d, perm, toks, K,
+                              0.0, O, L, ws, ws.numel(), stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(args.warmup, 3)):
+            call()
+        code = bb.bsa_check_device_error(ws, stream)
+        if code != 0:
+            raise bb.BsaError(code, "token forward warm-up")
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+        for i in range(args.steps):
+            flush.zero_()
+            ev[i][0].record(stream)
+            call()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+    ms = sum(a.elapsed_time(b) for a, b in ev) / args.steps
+    flops = 4.0 * BH * N * K * d  # every query row against its group's K tokens
+    tflops = flops / (ms * 1e-3) / 1e12
+    peaks, peak_kind = measured_peaks()
+    line = {"metric": "token-sparse attn fwd effective TFLOP/s (4*K*d per query row)", "value": round(tflops, 3),
+            "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
+            "higher_is_better": True, "dtype": "bf16" if w.dtype == "bf16" else "f32",
+            "data": "synthetic (seeded Q, K, V; seeded random groups and token sets)",
+            "config": {"workload": w.name, "B": w.B, "H": w.H, "N": N, "d": d, "group": C, "tokens_per_group": K,
+                       "l2": "flushed (256 MB write) before every timed call"},
+            "roofline": {"bound": "tensor", "achieved": round(tflops, 3), "peak": float(peaks["bf16_tflops"]),
+                         "unit": "TFLOP/s", "frac": round(tflops / float(peaks["bf16_tflops"]), 4),
+                         "kernel": "fwd_tokens_kernel (CUDA cores: first path)", "peak_source": peak_kind}}
+    print(json.dumps(line))
+
+
 def main():
     args = parse_args()
     world, rank, local = dist_env()
     if args.impl == "reference":
         run_reference(args, world, rank)
+    elif args.tokens > 0.0:
+        run_tokens(args)
     else:
         run_ours(args, world, rank, local)
 

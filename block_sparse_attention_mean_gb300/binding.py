@@ -40,7 +40,7 @@ MAX_ANCHORS = 8
 EXPORTS = ("bsa_build_mask", "bsa_forward", "bsa_mask_nnz", "bsa_workspace_size",
            "bsa_check_device_error", "bsa_validate_index", "bsa_debug_config",
            "bsa_status_string", "bsa_build_mask_noalloc", "bsa_residual_capture", "bsa_forward_residual",
-           "bsa_build_mask_modal", "bsa_mask_nnz_modal", "bsa_build_mask_exact")
+           "bsa_build_mask_modal", "bsa_mask_nnz_modal", "bsa_build_mask_exact", "bsa_forward_tokens")
 NOALLOC_SCRATCH_BYTES = 16 << 20  # BSA_NOALLOC_SCRATCH_BYTES
 # bsa_debug_config flag bits
 DBG_STALL = 1       # skip loads and MMAs: the first device wait runs out
@@ -80,6 +80,7 @@ def load():
     lib.bsa_forward.argtypes = [P, P, P, I, I, I, I, I, I, P, P, P, I, F, P, P, P, SZ, P]
     lib.bsa_forward_residual.argtypes = [P, P, P, I, I, I, I, I, I, P, P, P, I, F, P, P, P, P, SZ, P]
     lib.bsa_residual_capture.argtypes = [P, P, I, I64, P, P]
+    lib.bsa_forward_tokens.argtypes = [P, P, P, I, I, I, I, I, P, P, I, F, P, P, P, SZ, P]
     lib.bsa_build_mask_modal.argtypes = [P, P, I, I, I, I, I, I, I, P, P, P, I64, P, P, SZ, P]
     lib.bsa_mask_nnz_modal.argtypes = [I, I, I, I, I, P, ctypes.POINTER(I64)]
     lib.bsa_build_mask_exact.argtypes = [P, P, I, I, I, I, I, I, F, F, P, P, P, I64, P, P, SZ, P]
@@ -220,6 +221,13 @@ def build_mask_exact(q: torch.Tensor, k: torch.Tensor, lse_dense: torch.Tensor, 
                          col_idx.numel(), bitmap, ws, ws.numel(), stream)
     _check(bsa_check_device_error(ws, stream), "bsa_build_mask_exact (device)")
     return Index(row_ptr, col_idx, bitmap, col_idx.numel(), block), ws
+
+
+def bsa_forward_tokens(Q, K, V, dt: int, B: int, H: int, N: int, d: int, perm, tokens, n_tokens: int,
+                       scale: float, O, LSE, ws, ws_bytes: int, stream=None) -> None:
+    _check(load().bsa_forward_tokens(_ptr(Q), _ptr(K), _ptr(V), dt, B, H, N, d, _ptr(perm), _ptr(tokens), n_tokens,
+                                     ctypes.c_float(scale), _ptr(O), _ptr(LSE), _ptr(ws), ctypes.c_size_t(ws_bytes),
+                                     _stream(stream)), "bsa_forward_tokens")
 
 
 def bsa_residual_capture(O_dense, O_sparse, dt: int, count: int, R, stream=None) -> None:
@@ -382,6 +390,25 @@ def residual_capture(o_dense: torch.Tensor, o_sparse: torch.Tensor, out: Optiona
         out = torch.empty(o_dense.shape, dtype=torch.float32, device=o_dense.device)
     bsa_residual_capture(o_dense, o_sparse, _dtype_code(o_dense), o_dense.numel(), out, stream)
     return out
+
+
+def forward_tokens(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, perm: torch.Tensor, tokens: torch.Tensor,
+                   scale: float = 0.0, out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                   ws: Optional[torch.Tensor] = None, stream=None, check: bool = True):
+    """Run bsa_forward_tokens: perm int32 [B*H, N] (groups of 128 rows), tokens int32
+    [B*H, N/128, n_tokens]; returns (O, LSE)."""
+    B, H, N, d = q.shape
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    if ws is None:
+        ws = torch.zeros(256, dtype=torch.uint8, device=q.device)
+    bsa_forward_tokens(q, k, v, _dtype_code(q), B, H, N, d, perm, tokens, int(tokens.shape[-1]), scale, out, lse,
+                       ws, ws.numel(), stream)
+    if check:
+        _check(bsa_check_device_error(ws, stream), "bsa_forward_tokens (device)")
+    return out, lse
 
 
 def default_scale(d: int) -> float:

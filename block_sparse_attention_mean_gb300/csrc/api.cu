@@ -389,6 +389,39 @@ bsa_status bsa_forward_residual(const void *Q, const void *K, const void *V, int
                         workspace, workspace_bytes, stream);
 }
 
+bsa_status bsa_forward_tokens(const void *Q, const void *K, const void *V, int dt, int B, int H, int N, int d,
+                              const int32_t *perm, const int32_t *tokens, int n_tokens, float scale, void *O,
+                              float *LSE, void *workspace, size_t workspace_bytes, void *stream)
+{
+    if (B <= 0 || H <= 0 || N <= 0 || (d != 64 && d != 128) || N % bsa::kTokenGroup != 0) return BSA_ERR_SHAPE;
+    if (static_cast<int64_t>(B) * H * N > INT32_MAX || static_cast<int64_t>(B) * H > 65535) return BSA_ERR_SHAPE;
+    if (dt != BSA_BF16 && dt != BSA_FP32) return BSA_ERR_DTYPE;
+    if (!Q || !K || !V || !O || !LSE || !perm || !tokens) return BSA_ERR_INVALID_ARG;
+    if (!aligned(Q, 16) || !aligned(K, 16) || !aligned(V, 16) || !aligned(O, 16) || !aligned(LSE, 4) ||
+        !aligned(perm, 4) || !aligned(tokens, 4))
+        return BSA_ERR_INVALID_ARG;
+    if (n_tokens < 1 || n_tokens > N) return BSA_ERR_INVALID_ARG;
+    if (std::isnan(scale) || std::isinf(scale)) return BSA_ERR_INVALID_ARG;
+    if (!workspace || !aligned(workspace, 256) || workspace_bytes < bsa::kWsHeader) return BSA_ERR_WORKSPACE;
+    bsa::TokenArgs a{};
+    a.Q = Q;
+    a.K = K;
+    a.V = V;
+    a.dt = dt;
+    a.B = B;
+    a.H = H;
+    a.N = N;
+    a.d = d;
+    a.perm = perm;
+    a.tokens = tokens;
+    a.n_tokens = n_tokens;
+    a.scale = scale > 0.0f ? scale : static_cast<float>(1.0 / std::sqrt(static_cast<double>(d)));
+    a.O = O;
+    a.LSE = LSE;
+    a.ws = static_cast<char *>(workspace);
+    return bsa::launch_forward_tokens(a, static_cast<cudaStream_t>(stream));
+}
+
 bsa_status bsa_residual_capture(const void *O_dense, const void *O_sparse, int dt, int64_t count, float *R,
                                 void *stream)
 {

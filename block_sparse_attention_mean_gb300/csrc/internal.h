@@ -104,4 +104,20 @@ bsa_status launch_forward_simt(const FwdArgs &a, cudaStream_t st);  // fp32, CUD
 bsa_status launch_residual_capture(const void *dense, const void *sparse, int dt, int64_t count, float *R,
                                    cudaStream_t st);
 
+// ------------------------------------------------------------ token-sparse forward
+constexpr int kTokenGroup = 128;  // queries per group (the query tile)
+
+struct TokenArgs {
+    const void *Q, *K, *V;
+    int dt, B, H, N, d;
+    const int32_t *perm;    // [B*H][N]: group g of a head is rows perm[g*128 .. g*128+127]
+    const int32_t *tokens;  // [B*H][N/128][n_tokens]: the keys of each group
+    int n_tokens;
+    float scale;            // > 0
+    void *O;
+    float *LSE;
+    char *ws;               // error word in the first bytes
+};
+bsa_status launch_forward_tokens(const TokenArgs &a, cudaStream_t st);
+
 }  // namespace bsa

@@ -229,6 +229,34 @@ bsa_status bsa_forward_residual(const void *Q, const void *K, const void *V, int
                                 void *stream);
 
 /*
+ * bsa_forward_tokens -- token-sparse attention over tile-aligned query groups
+ * ("Can sparse attention close the quality gap in diffusion transformers", section
+ * "token 级选择需要瓦片对齐的查询分组": groups of 128 similar queries share one set of
+ * individually selected KV tokens, gathered by index).
+ *
+ * For each (b, h), group g = rows perm[g*128 .. g*128+127] of the head, and every row r
+ * of the group:
+ *   O_r = sum_t softmax_t(scale * q_r . k_t) v_t,  LSE_r = ln sum_t exp(scale * q_r . k_t),
+ *   t over tokens[g][0 .. n_tokens-1].
+ *
+ *   Q, K, V     device [B][H][N][d], dtype dt; N a multiple of 128
+ *   perm        device int32 [B*H][N]: per head a permutation of 0..N-1 (the groups)
+ *   tokens      device int32 [B*H][N/128][n_tokens]: each group's key tokens in [0, N)
+ *   n_tokens    keys per group, 1..N
+ *   scale       softmax scale; <= 0 selects 1/sqrt(d)
+ *   O, LSE      as bsa_forward (written for every row that perm names)
+ *   workspace   device, >= 256 bytes, 256-byte aligned (its first bytes hold the
+ *               device error word, read by bsa_check_device_error)
+ * Errors: BSA_ERR_SHAPE (N not a multiple of 128, d, B*H > 65535), BSA_ERR_DTYPE, BSA_ERR_INVALID_ARG
+ * (null or misaligned pointers, n_tokens out of range, non-finite scale),
+ * BSA_ERR_WORKSPACE. An index outside [0, N) in perm or tokens is skipped and raises
+ * BSA_ERR_INVALID_ARG in the workspace. This first path runs on CUDA cores (fp32 math).
+ */
+bsa_status bsa_forward_tokens(const void *Q, const void *K, const void *V, int dt, int B, int H, int N, int d,
+                              const int32_t *perm, const int32_t *tokens, int n_tokens, float scale, void *O,
+                              float *LSE, void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * bsa_build_mask_noalloc -- bsa_build_mask without a caller workspace (the pages
  * have no counterpart: this is a convenience of this library).
  *

@@ -1,0 +1,89 @@
+"""GPU parity of bsa_forward_tokens (token-sparse attention over tile-aligned query groups)
+against the CPU oracle.
+
+The groups (median-split principal-direction grouping) and each group's tokens (the exact
+per-group token mass from the dense LSE, top-K) come from the oracle and are the kernel's
+inputs, as the index is bsa_forward's. O within max-abs 2e-2 and mean-abs 2e-3, LSE within
+1e-3, every row; an out-of-range index raises BSA_ERR_INVALID_ARG without a fault.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from block_sparse_attention_mean_gb300 import binding as bb
+from block_sparse_attention_mean_gb300 import build as bbuild
+from block_sparse_attention_mean_gb300 import workloads as wl
+from tests import gpu_util as gu
+
+pytestmark = pytest.mark.gpu
+C = 128
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    bbuild.build()
+    bb.load()
+    bb.bsa_debug_config(0, 0)
+
+
+def _groups_and_tokens(inp, w, density):
+    BH = w.B * w.H
+    q = inp["q"].reshape(BH, w.N, w.d)
+    k = inp["k"].reshape(BH, w.N, w.d)
+    full = np.ones((BH, w.nQB, w.nKB), np.uint8)
+    _, lse = oracle.attention(q, k, k, full, w.block)  # dense LSE (values unused)
+    lse = lse.reshape(BH, w.N)
+    perms, toks = [], []
+    for h in range(BH):
+        perm = oracle.query_groups(q[h], C)
+        mass = oracle.token_mass(q[h], k[h], lse[h], perm, C)
+        perms.append(perm)
+        toks.append(oracle.select_tokens(mass, density))
+    return np.stack(perms), np.stack(toks)
+
+
+CASES = {
+    "bf16_d128": (wl.scaled(wl.WORKLOADS["dynamic_topk"], H=2, N=1024), 0.1),
+    "bf16_d64": (wl.scaled(wl.WORKLOADS["t2i_static"], B=1, H=2, N=1024), 0.2),
+    "fp32_d64": (wl.scaled(wl.WORKLOADS["tiny"], N=512), 0.25),
+}
+
+
+@pytest.mark.parametrize("name", sorted(CASES))
+def test_token_forward_matches_oracle(name):
+    w, density = CASES[name]
+    inp = wl.make_inputs(w)
+    perm, toks = _groups_and_tokens(inp, w, density)
+    q, k, v = (gu.upload(inp, n) for n in ("q", "k", "v"))
+    perm_d = torch.from_numpy(perm.astype(np.int32)).cuda()
+    toks_d = torch.from_numpy(toks.astype(np.int32)).cuda()
+    O, L = bb.forward_tokens(q, k, v, perm_d, toks_d)
+    torch.cuda.synchronize()
+    BH = w.B * w.H
+    Og = O.float().reshape(BH, w.N, w.d).cpu().numpy().astype(np.float64)
+    Lg = L.reshape(BH, w.N).cpu().numpy().astype(np.float64)
+    qf, kf, vf = (inp[n].reshape(BH, w.N, w.d) for n in ("q", "k", "v"))
+    for h in range(BH):
+        O_ref, L_ref = oracle.token_attention(qf[h], kf[h], vf[h], perm[h], toks[h], C)
+        err = np.abs(Og[h] - O_ref)
+        assert err.max() <= gu.O_MAX_ABS and err.mean() <= gu.O_MEAN_ABS, (h, err.max(), err.mean())
+        assert np.abs(Lg[h] - L_ref).max() <= gu.LSE_MAX_ABS
+
+
+def test_token_forward_out_of_range_index_is_reported():
+    w, density = CASES["bf16_d64"]
+    inp = wl.make_inputs(w)
+    q, k, v = (gu.upload(inp, n) for n in ("q", "k", "v"))
+    BH = w.B * w.H
+    perm = torch.arange(w.N, dtype=torch.int32).repeat(BH, 1).cuda()
+    toks = torch.zeros((BH, w.N // C, 8), dtype=torch.int32).cuda()
+    toks[0, 1, 3] = w.N + 5  # past the sequence: skipped and reported
+    ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
+    bb.forward_tokens(q, k, v, perm, toks, ws=ws, check=False)
+    assert bb.bsa_check_device_error(ws) == bb.ERR_INVALID_ARG
+    O, L = bb.forward_tokens(q, k, v, perm, torch.zeros_like(toks))  # the context is still usable
+    torch.cuda.synchronize()
+    assert torch.isfinite(L).all()

@@ -25,7 +25,7 @@ def _header_functions():
 
 def test_header_symbols_exported(lib):
     names = _header_functions()
-    assert len(names) == 14
+    assert len(names) == 15
     assert sorted(bb.EXPORTS) == names
     for n in names:
         assert getattr(lib, n) is not None  # dlsym succeeds
@@ -180,6 +180,29 @@ def _fwd_res(**kw):
     with pytest.raises(bb.BsaError) as e:
         bb.bsa_forward_residual(**args, stream=0)
     return e.value.code
+
+
+def _fwd_tok(**kw):
+    args = dict(Q=FAKE, K=FAKE, V=FAKE, dt=bb.BF16, B=1, H=2, N=512, d=64, perm=FAKE, tokens=FAKE, n_tokens=32,
+                scale=0.0, O=FAKE, LSE=FAKE, ws=FAKE, ws_bytes=256)
+    args.update(kw)
+    with pytest.raises(bb.BsaError) as e:
+        bb.bsa_forward_tokens(**args, stream=0)
+    return e.value.code
+
+
+def test_token_forward_rejects_bad_arguments(lib):
+    assert _fwd_tok(N=500) == bb.ERR_SHAPE          # groups of 128 queries
+    assert _fwd_tok(d=96) == bb.ERR_SHAPE
+    assert _fwd_tok(B=300, H=300) == bb.ERR_SHAPE   # one grid row per head
+    assert _fwd_tok(dt=7) == bb.ERR_DTYPE
+    assert _fwd_tok(perm=None) == bb.ERR_INVALID_ARG
+    assert _fwd_tok(tokens=FAKE + 2) == bb.ERR_INVALID_ARG
+    assert _fwd_tok(n_tokens=0) == bb.ERR_INVALID_ARG
+    assert _fwd_tok(n_tokens=513) == bb.ERR_INVALID_ARG
+    assert _fwd_tok(scale=float("nan")) == bb.ERR_INVALID_ARG
+    assert _fwd_tok(ws=None) == bb.ERR_WORKSPACE
+    assert _fwd_tok(ws_bytes=255) == bb.ERR_WORKSPACE
 
 
 def test_residual_entry_points_reject_bad_arguments(lib):
