@@ -40,7 +40,8 @@ MAX_ANCHORS = 8
 EXPORTS = ("bsa_build_mask", "bsa_forward", "bsa_mask_nnz", "bsa_workspace_size",
            "bsa_check_device_error", "bsa_validate_index", "bsa_debug_config",
            "bsa_status_string", "bsa_build_mask_noalloc", "bsa_residual_capture", "bsa_forward_residual",
-           "bsa_build_mask_modal", "bsa_mask_nnz_modal", "bsa_build_mask_exact", "bsa_forward_tokens")
+           "bsa_build_mask_modal", "bsa_mask_nnz_modal", "bsa_build_mask_exact", "bsa_forward_tokens",
+           "bsa_select_tokens")
 NOALLOC_SCRATCH_BYTES = 16 << 20  # BSA_NOALLOC_SCRATCH_BYTES
 # bsa_debug_config flag bits
 DBG_STALL = 1       # skip loads and MMAs: the first device wait runs out
@@ -81,6 +82,7 @@ def load():
     lib.bsa_forward_residual.argtypes = [P, P, P, I, I, I, I, I, I, P, P, P, I, F, P, P, P, P, SZ, P]
     lib.bsa_residual_capture.argtypes = [P, P, I, I64, P, P]
     lib.bsa_forward_tokens.argtypes = [P, P, P, I, I, I, I, I, P, P, I, F, P, P, P, SZ, P]
+    lib.bsa_select_tokens.argtypes = [P, P, I, I, I, I, I, P, P, F, F, P, I64, P, SZ, P]
     lib.bsa_build_mask_modal.argtypes = [P, P, I, I, I, I, I, I, I, P, P, P, I64, P, P, SZ, P]
     lib.bsa_mask_nnz_modal.argtypes = [I, I, I, I, I, P, ctypes.POINTER(I64)]
     lib.bsa_build_mask_exact.argtypes = [P, P, I, I, I, I, I, I, F, F, P, P, P, I64, P, P, SZ, P]
@@ -228,6 +230,13 @@ def bsa_forward_tokens(Q, K, V, dt: int, B: int, H: int, N: int, d: int, perm, t
     _check(load().bsa_forward_tokens(_ptr(Q), _ptr(K), _ptr(V), dt, B, H, N, d, _ptr(perm), _ptr(tokens), n_tokens,
                                      ctypes.c_float(scale), _ptr(O), _ptr(LSE), _ptr(ws), ctypes.c_size_t(ws_bytes),
                                      _stream(stream)), "bsa_forward_tokens")
+
+
+def bsa_select_tokens(Q, K, dt: int, B: int, H: int, N: int, d: int, perm, LSE, density: float, scale: float,
+                      tokens, tokens_capacity: int, ws, ws_bytes: int, stream=None) -> None:
+    _check(load().bsa_select_tokens(_ptr(Q), _ptr(K), dt, B, H, N, d, _ptr(perm), _ptr(LSE), ctypes.c_float(density),
+                                    ctypes.c_float(scale), _ptr(tokens), ctypes.c_int64(tokens_capacity), _ptr(ws),
+                                    ctypes.c_size_t(ws_bytes), _stream(stream)), "bsa_select_tokens")
 
 
 def bsa_residual_capture(O_dense, O_sparse, dt: int, count: int, R, stream=None) -> None:
@@ -409,6 +418,26 @@ def forward_tokens(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, perm: torc
     if check:
         _check(bsa_check_device_error(ws, stream), "bsa_forward_tokens (device)")
     return out, lse
+
+
+def tokens_per_group(N: int, density: float) -> int:
+    """K = max(1, floor(density * N)) with density taken as fp32 (the library's rule)."""
+    k = int(math.floor(float(np.float32(density)) * N))
+    return min(max(k, 1), N)
+
+
+def select_tokens(q: torch.Tensor, k: torch.Tensor, perm: torch.Tensor, lse: torch.Tensor, density: float,
+                  scale: float = 0.0, stream=None, check: bool = True):
+    """Run bsa_select_tokens; returns (tokens int32 [B*H, N/128, K], workspace)."""
+    B, H, N, d = q.shape
+    K = tokens_per_group(N, density)
+    tokens = torch.empty((B * H, N // 128, K), dtype=torch.int32, device=q.device)
+    ws = workspace(3, B, H, N, d, 64, q.device)
+    bsa_select_tokens(q, k, _dtype_code(q), B, H, N, d, perm, lse, density, scale, tokens, tokens.numel(), ws,
+                      ws.numel(), stream)
+    if check:
+        _check(bsa_check_device_error(ws, stream), "bsa_select_tokens (device)")
+    return tokens, ws
 
 
 def default_scale(d: int) -> float:

@@ -244,7 +244,10 @@ bsa_status bsa_workspace_size(int which, int B, int H, int N, int d, int block, 
     if (which == 0) *bytes = bsa::mask_workspace_bytes(B, H, N, d, block);
     else if (which == 1) *bytes = bsa::fwd_workspace_bytes(B, H, N, d, block);
     else if (which == 2) *bytes = bsa::exact_workspace_bytes(B, H, N, d, block);
-    else return BSA_ERR_INVALID_ARG;
+    else if (which == 3) {
+        if (N % bsa::kTokenGroup != 0) return BSA_ERR_SHAPE;
+        *bytes = bsa::token_select_ws_layout(B, H, N).total;
+    } else return BSA_ERR_INVALID_ARG;
     return BSA_OK;
 }
 
@@ -420,6 +423,42 @@ bsa_status bsa_forward_tokens(const void *Q, const void *K, const void *V, int d
     a.LSE = LSE;
     a.ws = static_cast<char *>(workspace);
     return bsa::launch_forward_tokens(a, static_cast<cudaStream_t>(stream));
+}
+
+bsa_status bsa_select_tokens(const void *Q, const void *K, int dt, int B, int H, int N, int d, const int32_t *perm,
+                             const float *LSE, float density, float scale, int32_t *tokens, int64_t tokens_capacity,
+                             void *workspace, size_t workspace_bytes, void *stream)
+{
+    if (B <= 0 || H <= 0 || N <= 0 || (d != 64 && d != 128) || N % bsa::kTokenGroup != 0) return BSA_ERR_SHAPE;
+    if (static_cast<int64_t>(B) * H * N > INT32_MAX || static_cast<int64_t>(B) * H > 65535) return BSA_ERR_SHAPE;
+    // shared memory of the first path: the group's rows, a 32-token chunk and one key per token
+    if (sizeof(float) * (bsa::kTokenGroup * d + 32 * (d + 1)) + sizeof(uint32_t) * static_cast<size_t>(N) >
+        232448)
+        return BSA_ERR_SHAPE;
+    if (dt != BSA_BF16 && dt != BSA_FP32) return BSA_ERR_DTYPE;
+    if (!Q || !K || !perm || !LSE || !tokens) return BSA_ERR_INVALID_ARG;
+    if (!aligned(Q, 16) || !aligned(K, 16) || !aligned(perm, 4) || !aligned(LSE, 4) || !aligned(tokens, 4))
+        return BSA_ERR_INVALID_ARG;
+    if (!valid_density(density) || std::isnan(scale) || std::isinf(scale)) return BSA_ERR_INVALID_ARG;
+    const int n_keep = topk_keep(density, N);
+    if (tokens_capacity < static_cast<int64_t>(B) * H * (N / bsa::kTokenGroup) * n_keep) return BSA_ERR_CAPACITY;
+    if (!workspace || !aligned(workspace, 256) || workspace_bytes < bsa::token_select_ws_layout(B, H, N).total)
+        return BSA_ERR_WORKSPACE;
+    bsa::TokenSelectArgs a{};
+    a.Q = Q;
+    a.K = K;
+    a.dt = dt;
+    a.B = B;
+    a.H = H;
+    a.N = N;
+    a.d = d;
+    a.perm = perm;
+    a.LSE = LSE;
+    a.scale = scale > 0.0f ? scale : static_cast<float>(1.0 / std::sqrt(static_cast<double>(d)));
+    a.n_keep = n_keep;
+    a.tokens = tokens;
+    a.ws = static_cast<char *>(workspace);
+    return bsa::launch_select_tokens(a, static_cast<cudaStream_t>(stream));
 }
 
 bsa_status bsa_residual_capture(const void *O_dense, const void *O_sparse, int dt, int64_t count, float *R,

@@ -120,4 +120,22 @@ struct TokenArgs {
 };
 bsa_status launch_forward_tokens(const TokenArgs &a, cudaStream_t st);
 
+// token selection: per group of 128 queries, the n_keep tokens of largest exact mass
+struct TokenSelectArgs {
+    const void *Q, *K;
+    int dt, B, H, N, d;
+    const int32_t *perm;   // [B*H][N] query groups
+    const float *LSE;      // [B*H][N] dense logsumexp (natural log)
+    float scale;           // > 0
+    int n_keep;            // tokens per group
+    int32_t *tokens;       // [B*H][N/128][n_keep] (written, ascending per group)
+    char *ws;
+};
+// workspace: header, masses fp32 [B*H*N/128][N], bitmap words [B*H*N/128][N/32]
+struct TokenSelectWs {
+    size_t mass, bitmap, total;
+};
+TokenSelectWs token_select_ws_layout(int B, int H, int N);
+bsa_status launch_select_tokens(const TokenSelectArgs &a, cudaStream_t st);
+
 }  // namespace bsa

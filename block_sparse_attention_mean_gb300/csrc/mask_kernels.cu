@@ -20,6 +20,7 @@
 // ties to the lower block index.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
+#include <math_constants.h>
 
 #include "internal.h"
 
@@ -687,6 +688,127 @@ bsa_status launch_mass_select(const float *part, const ExactArgs &a, int tiles_p
                                                         a.row_ptr, a.col_idx, a.bitmap,
                                                         reinterpret_cast<uint32_t *>(a.ws));
     return cudaGetLastError() == cudaSuccess ? BSA_OK : BSA_ERR_CUDA;
+}
+
+// ------------------------------------------------------------ token selection
+//
+// "Can sparse attention close the quality gap in diffusion transformers", sections
+// "质量差距有三个可分离来源" (the token oracle) and "token 级选择需要瓦片对齐的查询分组": per group
+// g of 128 queries (rows perm[g*128 ..] of a head) and key token t,
+//   mass[g][t] = sum over rows r of g of exp(scale * q_r . k_t - LSE_r),
+// with the dense row logsumexp, then the n_keep tokens of largest mass (ties to the lower
+// index) in ascending order: the same exact top-k as the block selectors, on a row of N keys.
+//
+// One CTA per (b, h, group), on CUDA cores (first path): the group's rows are gathered
+// into shared memory; per chunk of 32 tokens, lane l of warp w sums exp over the warp's 16
+// rows for token l, the 8 warp sums are added in warp order, and the mass goes to the
+// workspace and, as an order key, to a shared-memory row that warp 0 then selects from.
+template <typename T, int D>
+__global__ void __launch_bounds__(256) token_select_kernel(const T *__restrict__ Q, const T *__restrict__ K, int N,
+                                                           const int32_t *__restrict__ perm,
+                                                           const float *__restrict__ LSE, float scale, int n_keep,
+                                                           float *__restrict__ mass, uint32_t *__restrict__ bitmap,
+                                                           int32_t *__restrict__ tokens, uint32_t *err)
+{
+    constexpr int C = kTokenGroup, RPW = C / 8;
+    extern __shared__ float tsm[];
+    float *qs = tsm;                                                // [C][D]
+    float *ks = qs + C * D;                                         // [32][D + 1]
+    uint32_t *keys = reinterpret_cast<uint32_t *>(ks + 32 * (D + 1));  // [N]
+    __shared__ int32_t rows[C];
+    __shared__ float lse[C];
+    __shared__ float colsum[8][32];
+    const int g = blockIdx.x;
+    const int64_t bh = blockIdx.y;
+    const int G = N / C;
+    const int64_t rg = bh * G + g;  // selection row
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int r = threadIdx.x; r < C; r += blockDim.x) {
+        int row = perm[bh * N + static_cast<int64_t>(g) * C + r];
+        if (row < 0 || row >= N) {
+            raise_error(err, BSA_ERR_INVALID_ARG);
+            row = -1;
+        }
+        rows[r] = row;
+        lse[r] = row >= 0 ? LSE[bh * N + row] : CUDART_INF_F;  // a skipped row adds nothing
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < C * D; e += blockDim.x) {
+        const int r = e / D, c = e % D;
+        qs[e] = rows[r] >= 0 ? static_cast<float>(Q[(bh * N + rows[r]) * D + c]) : 0.0f;
+    }
+    bool nan_seen = false;
+    for (int c0 = 0; c0 < N; c0 += 32) {
+        __syncthreads();
+        for (int e = threadIdx.x; e < 32 * D; e += blockDim.x) {
+            const int kk = e / D, c = e % D;
+            ks[kk * (D + 1) + c] = static_cast<float>(K[(bh * N + c0 + kk) * D + c]);
+        }
+        __syncthreads();
+        const float *k = ks + lane * (D + 1);
+        float acc = 0.0f;
+        for (int r = 0; r < RPW; ++r) {
+            const int rr = warp * RPW + r;
+            const float *q = qs + rr * D;
+            float s = 0.0f;
+#pragma unroll 16
+            for (int c = 0; c < D; ++c) s = fmaf(q[c], k[c], s);
+            acc += expf(s * scale - lse[rr]);
+        }
+        colsum[warp][lane] = acc;
+        __syncthreads();
+        if (warp == 0) {
+            float m = colsum[0][lane];
+#pragma unroll
+            for (int w = 1; w < 8; ++w) m += colsum[w][lane];
+            nan_seen |= isnan(m);
+            mass[rg * N + c0 + lane] = m;
+            keys[c0 + lane] = order_key(m);
+        }
+    }
+    __syncthreads();
+    if (warp == 0) {
+        if (__any_sync(0xffffffffu, nan_seen) && lane == 0) raise_error(err, BSA_ERR_NONFINITE);
+        select_row(keys, N, 0, 0, n_keep, N / 32, rg, rg * n_keep, tokens, bitmap, lane);
+    }
+}
+
+template <typename T, int D>
+static bsa_status launch_token_select(const TokenSelectArgs &a, cudaStream_t st)
+{
+    const TokenSelectWs l = token_select_ws_layout(a.B, a.H, a.N);
+    const size_t smem = sizeof(float) * (kTokenGroup * D + 32 * (D + 1)) + sizeof(uint32_t) * a.N;
+    if (cudaFuncSetAttribute(token_select_kernel<T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem)) != cudaSuccess)
+        return BSA_ERR_CUDA;
+    dim3 grid(a.N / kTokenGroup, a.B * a.H);
+    token_select_kernel<T, D><<<grid, 256, smem, st>>>(
+        static_cast<const T *>(a.Q), static_cast<const T *>(a.K), a.N, a.perm, a.LSE, a.scale, a.n_keep,
+        reinterpret_cast<float *>(a.ws + l.mass), reinterpret_cast<uint32_t *>(a.ws + l.bitmap), a.tokens,
+        reinterpret_cast<uint32_t *>(a.ws));
+    return cudaGetLastError() == cudaSuccess ? BSA_OK : BSA_ERR_CUDA;
+}
+
+TokenSelectWs token_select_ws_layout(int B, int H, int N)
+{
+    const size_t rows = static_cast<size_t>(B) * H * (N / kTokenGroup);
+    TokenSelectWs l{};
+    l.mass = kWsHeader;
+    l.bitmap = l.mass + align_up(rows * N * sizeof(float), 256);
+    l.total = l.bitmap + align_up(rows * (N / 32) * sizeof(uint32_t), 256);
+    return l;
+}
+
+bsa_status launch_select_tokens(const TokenSelectArgs &a, cudaStream_t st)
+{
+    if (a.dt == BSA_BF16) {
+        if (a.d == 64) return launch_token_select<__nv_bfloat16, 64>(a, st);
+        if (a.d == 128) return launch_token_select<__nv_bfloat16, 128>(a, st);
+    } else {
+        if (a.d == 64) return launch_token_select<float, 64>(a, st);
+        if (a.d == 128) return launch_token_select<float, 128>(a, st);
+    }
+    return BSA_ERR_SHAPE;
 }
 
 bsa_status launch_validate_index(int R, int nKB, const int32_t *row_ptr, const int32_t *col_idx,

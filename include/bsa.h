@@ -229,6 +229,33 @@ bsa_status bsa_forward_residual(const void *Q, const void *K, const void *V, int
                                 void *stream);
 
 /*
+ * bsa_select_tokens -- the token oracle's selection for token-sparse attention ("Can
+ * sparse attention close the quality gap in diffusion transformers", sections
+ * "质量差距有三个可分离来源" and "token 级选择需要瓦片对齐的查询分组").
+ *
+ * For each (b, h) and group g = rows perm[g*128 .. g*128+127]:
+ *   mass[g][t] = sum over rows r of g of exp(scale * q_r . k_t - LSE_r),  t = 0..N-1,
+ * and the group keeps the K = max(1, floor(density * N)) tokens of largest mass (ties to
+ * the lower index), written ascending to tokens[(b*H+h)*(N/128) + g][0..K-1].
+ *
+ *   Q, K        device [B][H][N][d], dtype dt; N a multiple of 128
+ *   perm        device int32 [B*H][N]: per head a permutation of 0..N-1 (the groups)
+ *   LSE         device fp32 [B][H][N]: the dense logsumexp (natural log), e.g. bsa_forward
+ *               over a full index
+ *   density     in (0, 1]; scale <= 0 selects 1/sqrt(d)
+ *   tokens      device int32, capacity >= B*H*(N/128)*K entries
+ *   workspace   device, >= bsa_workspace_size(3, ...) bytes, 256-byte aligned; after the call
+ *               it holds the masses fp32 [B*H*N/128][N] at byte offset 256
+ * Errors: BSA_ERR_SHAPE (N not a multiple of 128, d, B*H > 65535, N too large for the
+ * shared-memory row of this first path), BSA_ERR_DTYPE, BSA_ERR_INVALID_ARG, BSA_ERR_CAPACITY,
+ * BSA_ERR_WORKSPACE; device-raised: BSA_ERR_INVALID_ARG (perm index outside [0, N), skipped),
+ * BSA_ERR_NONFINITE (a NaN mass). Runs on CUDA cores (first path).
+ */
+bsa_status bsa_select_tokens(const void *Q, const void *K, int dt, int B, int H, int N, int d, const int32_t *perm,
+                             const float *LSE, float density, float scale, int32_t *tokens, int64_t tokens_capacity,
+                             void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * bsa_forward_tokens -- token-sparse attention over tile-aligned query groups
  * ("Can sparse attention close the quality gap in diffusion transformers", section
  * "token 级选择需要瓦片对齐的查询分组": groups of 128 similar queries share one set of
@@ -292,7 +319,8 @@ bsa_status bsa_mask_nnz(int B, int H, int N, int block, float density,
                         const bsa_static_spec *spec, int64_t *nnz);
 
 /* Host-only: workspace bytes for which = 0 (bsa_build_mask, bsa_build_mask_modal),
- * 1 (bsa_forward, bsa_forward_residual) or 2 (bsa_build_mask_exact). */
+ * 1 (bsa_forward, bsa_forward_residual), 2 (bsa_build_mask_exact) or 3 (bsa_select_tokens;
+ * N a multiple of 128, block any valid value). */
 bsa_status bsa_workspace_size(int which, int B, int H, int N, int d, int block, size_t *bytes);
 
 /* Synchronises `stream`, returns the device-raised status recorded in `workspace`

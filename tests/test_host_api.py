@@ -25,7 +25,7 @@ def _header_functions():
 
 def test_header_symbols_exported(lib):
     names = _header_functions()
-    assert len(names) == 15
+    assert len(names) == 16
     assert sorted(bb.EXPORTS) == names
     for n in names:
         assert getattr(lib, n) is not None  # dlsym succeeds
@@ -61,7 +61,7 @@ def test_workspace_sizes(lib):
         bb.bsa_workspace_size(1, 1, 1, 0, 64, 64)
     assert e.value.code == bb.ERR_SHAPE
     with pytest.raises(bb.BsaError) as e:
-        bb.bsa_workspace_size(3, 1, 1, 128, 64, 64)  # 0 mask, 1 forward, 2 exact selector
+        bb.bsa_workspace_size(4, 1, 1, 128, 64, 64)  # 0 mask, 1 forward, 2 exact, 3 token selection
     assert e.value.code == bb.ERR_INVALID_ARG
 
 
@@ -189,6 +189,32 @@ def _fwd_tok(**kw):
     with pytest.raises(bb.BsaError) as e:
         bb.bsa_forward_tokens(**args, stream=0)
     return e.value.code
+
+
+def test_token_selection_workspace_and_arguments(lib):
+    up = lambda x: (x + 255) // 256 * 256  # noqa: E731
+    rows = 2 * 3 * (1024 // 128)
+    assert bb.bsa_workspace_size(3, 2, 3, 1024, 128, 64) == 256 + up(rows * 1024 * 4) + up(rows * 32 * 4)
+    with pytest.raises(bb.BsaError) as e:
+        bb.bsa_workspace_size(3, 1, 1, 1000, 64, 64)
+    assert e.value.code == bb.ERR_SHAPE
+    assert bb.tokens_per_group(1024, 0.1) == 102 and bb.tokens_per_group(1024, 1e-6) == 1
+
+    def sel(**kw):
+        args = dict(Q=FAKE, K=FAKE, dt=bb.BF16, B=1, H=2, N=512, d=64, perm=FAKE, LSE=FAKE, density=0.25,
+                    scale=0.0, tokens=FAKE, tokens_capacity=2 * 4 * 128, ws=FAKE, ws_bytes=1 << 30)
+        args.update(kw)
+        with pytest.raises(bb.BsaError) as e:
+            bb.bsa_select_tokens(**args, stream=0)
+        return e.value.code
+
+    assert sel(N=500) == bb.ERR_SHAPE
+    assert sel(N=1 << 16, d=128) == bb.ERR_SHAPE  # one shared-memory key per token
+    assert sel(dt=3) == bb.ERR_DTYPE
+    assert sel(LSE=None) == bb.ERR_INVALID_ARG
+    assert sel(density=0.0) == bb.ERR_INVALID_ARG
+    assert sel(tokens_capacity=2 * 4 * 128 - 1) == bb.ERR_CAPACITY
+    assert sel(ws_bytes=256) == bb.ERR_WORKSPACE
 
 
 def test_token_forward_rejects_bad_arguments(lib):
