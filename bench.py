@@ -540,6 +540,28 @@ def run_tokens(args):
         torch.cuda.synchronize()
     ms = sum(a.elapsed_time(b) for a, b in ev) / args.steps
     flops = 4.0 * BH * N * K * d  # every query row against its group's K tokens
+
+    # the anchor-step stages of the token path, once each after a warm-up: the query groups
+    # and the exact token selection (with the dense LSE of a full-index forward)
+    def timed(fn):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            fn()
+            torch.cuda.synchronize()
+            flush.zero_()
+            e0.record(stream)
+            out = fn()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        return out, e0.elapsed_time(e1)
+
+    gperm, group_ms = timed(lambda: bb.query_groups(q, stream=stream))
+    ones = np.ones((w.B, w.H, w.nQB, w.nKB), dtype=np.uint8)
+    full = bb.build_mask(None, None, w.block, spec=bb.explicit_spec(
+        torch.from_numpy(wl.pack_bitmap_words(ones).reshape(-1)).to(dev)), shape=(w.B, w.H, N, d))
+    _, lse = bb.forward(q, k, v, full)
+    del full
+    _, select_ms = timed(lambda: bb.select_tokens(q, k, gperm, lse, args.tokens, stream=stream))
     tflops = flops / (ms * 1e-3) / 1e12
     peaks, peak_kind = measured_peaks()
     line = {"metric": "token-sparse attn fwd effective TFLOP/s (4*K*d per query row)", "value": round(tflops, 3),
@@ -548,6 +570,7 @@ def run_tokens(args):
             "data": "synthetic (seeded Q, K, V; seeded random groups and token sets)",
             "config": {"workload": w.name, "B": w.B, "H": w.H, "N": N, "d": d, "group": C, "tokens_per_group": K,
                        "l2": "flushed (256 MB write) before every timed call"},
+            "anchor_step_ms": {"query_groups": round(group_ms, 3), "select_tokens": round(select_ms, 3)},
             "roofline": {"bound": "tensor", "achieved": round(tflops, 3), "peak": float(peaks["bf16_tflops"]),
                          "unit": "TFLOP/s", "frac": round(tflops / float(peaks["bf16_tflops"]), 4),
                          "kernel": "fwd_tokens_kernel (CUDA cores: first path)", "peak_source": peak_kind}}

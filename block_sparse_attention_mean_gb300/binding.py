@@ -41,7 +41,7 @@ EXPORTS = ("bsa_build_mask", "bsa_forward", "bsa_mask_nnz", "bsa_workspace_size"
            "bsa_check_device_error", "bsa_validate_index", "bsa_debug_config",
            "bsa_status_string", "bsa_build_mask_noalloc", "bsa_residual_capture", "bsa_forward_residual",
            "bsa_build_mask_modal", "bsa_mask_nnz_modal", "bsa_build_mask_exact", "bsa_forward_tokens",
-           "bsa_select_tokens")
+           "bsa_select_tokens", "bsa_query_groups")
 NOALLOC_SCRATCH_BYTES = 16 << 20  # BSA_NOALLOC_SCRATCH_BYTES
 # bsa_debug_config flag bits
 DBG_STALL = 1       # skip loads and MMAs: the first device wait runs out
@@ -83,6 +83,7 @@ def load():
     lib.bsa_residual_capture.argtypes = [P, P, I, I64, P, P]
     lib.bsa_forward_tokens.argtypes = [P, P, P, I, I, I, I, I, P, P, I, F, P, P, P, SZ, P]
     lib.bsa_select_tokens.argtypes = [P, P, I, I, I, I, I, P, P, F, F, P, I64, P, SZ, P]
+    lib.bsa_query_groups.argtypes = [P, I, I, I, I, I, P, P, SZ, P]
     lib.bsa_build_mask_modal.argtypes = [P, P, I, I, I, I, I, I, I, P, P, P, I64, P, P, SZ, P]
     lib.bsa_mask_nnz_modal.argtypes = [I, I, I, I, I, P, ctypes.POINTER(I64)]
     lib.bsa_build_mask_exact.argtypes = [P, P, I, I, I, I, I, I, F, F, P, P, P, I64, P, P, SZ, P]
@@ -230,6 +231,11 @@ def bsa_forward_tokens(Q, K, V, dt: int, B: int, H: int, N: int, d: int, perm, t
     _check(load().bsa_forward_tokens(_ptr(Q), _ptr(K), _ptr(V), dt, B, H, N, d, _ptr(perm), _ptr(tokens), n_tokens,
                                      ctypes.c_float(scale), _ptr(O), _ptr(LSE), _ptr(ws), ctypes.c_size_t(ws_bytes),
                                      _stream(stream)), "bsa_forward_tokens")
+
+
+def bsa_query_groups(Q, dt: int, B: int, H: int, N: int, d: int, perm, ws, ws_bytes: int, stream=None) -> None:
+    _check(load().bsa_query_groups(_ptr(Q), dt, B, H, N, d, _ptr(perm), _ptr(ws), ctypes.c_size_t(ws_bytes),
+                                   _stream(stream)), "bsa_query_groups")
 
 
 def bsa_select_tokens(Q, K, dt: int, B: int, H: int, N: int, d: int, perm, LSE, density: float, scale: float,
@@ -424,6 +430,15 @@ def tokens_per_group(N: int, density: float) -> int:
     """K = max(1, floor(density * N)) with density taken as fp32 (the library's rule)."""
     k = int(math.floor(float(np.float32(density)) * N))
     return min(max(k, 1), N)
+
+
+def query_groups(q: torch.Tensor, stream=None) -> torch.Tensor:
+    """Run bsa_query_groups; returns perm int32 [B*H, N] (groups of 128 rows)."""
+    B, H, N, d = q.shape
+    perm = torch.empty((B * H, N), dtype=torch.int32, device=q.device)
+    ws = workspace(4, B, H, N, d, 64, q.device)
+    bsa_query_groups(q, _dtype_code(q), B, H, N, d, perm, ws, ws.numel(), stream)
+    return perm
 
 
 def select_tokens(q: torch.Tensor, k: torch.Tensor, perm: torch.Tensor, lse: torch.Tensor, density: float,

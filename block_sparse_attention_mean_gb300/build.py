@@ -15,7 +15,7 @@ CSRC = os.path.join(HERE, "csrc")
 LIB = os.path.join(HERE, "libbsa.so")
 BUILD_DIR = os.path.join(HERE, "_build")
 SOURCES = ["api.cu", "mask_kernels.cu", "fwd_tc.cu", "fwd_simt.cu", "noalloc.cu", "residual.cu",
-           "exact_select.cu", "fwd_tokens.cu"]
+           "exact_select.cu", "fwd_tokens.cu", "query_groups.cu"]
 HEADERS = ["internal.h", "ptx.cuh", "walk.cuh", "sync.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")

@@ -247,6 +247,9 @@ bsa_status bsa_workspace_size(int which, int B, int H, int N, int d, int block, 
     else if (which == 3) {
         if (N % bsa::kTokenGroup != 0) return BSA_ERR_SHAPE;
         *bytes = bsa::token_select_ws_layout(B, H, N).total;
+    } else if (which == 4) {
+        if (N % bsa::kTokenGroup != 0) return BSA_ERR_SHAPE;
+        *bytes = bsa::query_groups_ws_layout(B, H, N).total;
     } else return BSA_ERR_INVALID_ARG;
     return BSA_OK;
 }
@@ -423,6 +426,28 @@ bsa_status bsa_forward_tokens(const void *Q, const void *K, const void *V, int d
     a.LSE = LSE;
     a.ws = static_cast<char *>(workspace);
     return bsa::launch_forward_tokens(a, static_cast<cudaStream_t>(stream));
+}
+
+bsa_status bsa_query_groups(const void *Q, int dt, int B, int H, int N, int d, int32_t *perm, void *workspace,
+                            size_t workspace_bytes, void *stream)
+{
+    if (B <= 0 || H <= 0 || N <= 0 || (d != 64 && d != 128) || N % bsa::kTokenGroup != 0) return BSA_ERR_SHAPE;
+    if (N / bsa::kTokenGroup > bsa::kMaxQueryGroups || static_cast<int64_t>(B) * H * N > INT32_MAX)
+        return BSA_ERR_SHAPE;
+    if (dt != BSA_BF16 && dt != BSA_FP32) return BSA_ERR_DTYPE;
+    if (!Q || !perm || !aligned(Q, 16) || !aligned(perm, 4)) return BSA_ERR_INVALID_ARG;
+    if (!workspace || !aligned(workspace, 256) || workspace_bytes < bsa::query_groups_ws_layout(B, H, N).total)
+        return BSA_ERR_WORKSPACE;
+    bsa::GroupArgs a{};
+    a.Q = Q;
+    a.dt = dt;
+    a.B = B;
+    a.H = H;
+    a.N = N;
+    a.d = d;
+    a.perm = perm;
+    a.ws = static_cast<char *>(workspace);
+    return bsa::launch_query_groups(a, static_cast<cudaStream_t>(stream));
 }
 
 bsa_status bsa_select_tokens(const void *Q, const void *K, int dt, int B, int H, int N, int d, const int32_t *perm,

@@ -138,4 +138,19 @@ struct TokenSelectWs {
 TokenSelectWs token_select_ws_layout(int B, int H, int N);
 bsa_status launch_select_tokens(const TokenSelectArgs &a, cudaStream_t st);
 
+// query groups: per head, the median-split principal-direction partition into groups of 128
+constexpr int kMaxQueryGroups = 512;  // groups per head (N <= 65536)
+struct GroupArgs {
+    const void *Q;
+    int dt, B, H, N, d;
+    int32_t *perm;  // [B*H][N] (written)
+    char *ws;
+};
+// workspace: header, working permutation, projection keys and a scratch copy, [B*H][N] each
+struct QueryGroupWs {
+    size_t work, keys, scratch, total;
+};
+QueryGroupWs query_groups_ws_layout(int B, int H, int N);
+bsa_status launch_query_groups(const GroupArgs &a, cudaStream_t st);
+
 }  // namespace bsa

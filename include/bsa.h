@@ -229,6 +229,27 @@ bsa_status bsa_forward_residual(const void *Q, const void *K, const void *V, int
                                 void *stream);
 
 /*
+ * bsa_query_groups -- tile-aligned query groups for token-level selection ("Can sparse
+ * attention close the quality gap in diffusion transformers", section "token 级选择需要瓦片
+ * 对齐的查询分组"): the queries of each head are split recursively at the median of their
+ * projection on the group's principal direction until every group holds 128 queries. A
+ * group of m*128 rows keeps its first ceil(m/2)*128 rows in (projection, row index) order
+ * as its first half. perm receives per head the groups in depth-first order, each group's
+ * rows ascending: group g = perm[(b*H+h)*N + g*128 .. +127] (the layout of
+ * bsa_select_tokens and bsa_forward_tokens).
+ *
+ *   Q           device [B][H][N][d], dtype dt; N a multiple of 128, N/128 <= 512
+ *   perm        device int32 [B*H][N] (written)
+ *   workspace   device, >= bsa_workspace_size(4, ...) bytes, 256-byte aligned
+ * The principal direction comes from fp32 power iteration (32 steps from a fixed start),
+ * so a row lying within rounding of a median may land on the other side than an exact
+ * eigendecomposition would put it. Errors: BSA_ERR_SHAPE, BSA_ERR_DTYPE,
+ * BSA_ERR_INVALID_ARG, BSA_ERR_WORKSPACE. Runs on CUDA cores, one CTA per (b, h).
+ */
+bsa_status bsa_query_groups(const void *Q, int dt, int B, int H, int N, int d, int32_t *perm, void *workspace,
+                            size_t workspace_bytes, void *stream);
+
+/*
  * bsa_select_tokens -- the token oracle's selection for token-sparse attention ("Can
  * sparse attention close the quality gap in diffusion transformers", sections
  * "质量差距有三个可分离来源" and "token 级选择需要瓦片对齐的查询分组").
@@ -319,8 +340,8 @@ bsa_status bsa_mask_nnz(int B, int H, int N, int block, float density,
                         const bsa_static_spec *spec, int64_t *nnz);
 
 /* Host-only: workspace bytes for which = 0 (bsa_build_mask, bsa_build_mask_modal),
- * 1 (bsa_forward, bsa_forward_residual), 2 (bsa_build_mask_exact) or 3 (bsa_select_tokens;
- * N a multiple of 128, block any valid value). */
+ * 1 (bsa_forward, bsa_forward_residual), 2 (bsa_build_mask_exact), 3 (bsa_select_tokens) or
+ * 4 (bsa_query_groups); for 3 and 4 N is a multiple of 128 and block any valid value. */
 bsa_status bsa_workspace_size(int which, int B, int H, int N, int d, int block, size_t *bytes);
 
 /* Synchronises `stream`, returns the device-raised status recorded in `workspace`

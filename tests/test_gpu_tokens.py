@@ -130,3 +130,69 @@ def test_token_selection_matches_oracle(name):
         err = np.abs(Og[h] - O_ref)
         assert err.max() <= gu.O_MAX_ABS and err.mean() <= gu.O_MEAN_ABS
         assert np.abs(Lg[h] - L_ref).max() <= gu.LSE_MAX_ABS
+
+
+def _sse(x, perm):
+    """Within-group sum of squared distances to the group mean (double)."""
+    g = x[perm].reshape(-1, C, x.shape[1]).astype(np.float64)
+    return float(((g - g.mean(axis=1, keepdims=True)) ** 2).sum())
+
+
+def test_query_groups_on_a_line_match_the_oracle():
+    # points on one line: every median split is an exact cut of the sorted coordinate, so
+    # the GPU's groups are the oracle's, bit for bit (4 and 5 groups: even and odd splits)
+    for m in (4, 5):
+        N, d = m * C, 64
+        rng = np.random.default_rng(m)
+        t = rng.permutation(N).astype(np.float64) * 0.5 + rng.random(N) * 0.1
+        e = rng.standard_normal(d)
+        e /= np.linalg.norm(e)
+        q = (t[:, None] * e[None, :]).astype(np.float32)
+        perm = bb.query_groups(torch.from_numpy(q).reshape(1, 1, N, d).cuda())
+        torch.cuda.synchronize()
+        assert np.array_equal(perm.cpu().numpy()[0], oracle.query_groups(q, C))
+
+
+@pytest.mark.parametrize("name", sorted(CASES))
+def test_query_groups_partition_and_quality(name):
+    # a valid partition into ascending groups of 128, as tight as the oracle's (its direction
+    # is an fp32 power iteration, so a row within rounding of a median may change sides)
+    w, _ = CASES[name]
+    inp = wl.make_inputs(w)
+    BH = w.B * w.H
+    q = gu.upload(inp, "q")
+    perm = bb.query_groups(q)
+    torch.cuda.synchronize()
+    got = perm.cpu().numpy()
+    qf = inp["q"].reshape(BH, w.N, w.d)
+    for h in range(BH):
+        assert sorted(got[h].tolist()) == list(range(w.N))
+        assert np.all(np.diff(got[h].reshape(-1, C), axis=1) > 0)
+        ref = oracle.query_groups(qf[h], C)
+        assert _sse(qf[h], got[h]) <= 1.01 * _sse(qf[h], ref)
+
+
+def test_token_path_end_to_end_on_the_gpu():
+    # groups, dense LSE, selection and the token forward all on the GPU; the forward checked
+    # against the oracle's token attention over the GPU's own groups and tokens
+    w, density = CASES["bf16_d128"]
+    inp = wl.make_inputs(w)
+    BH = w.B * w.H
+    q, k, v = (gu.upload(inp, n) for n in ("q", "k", "v"))
+    perm = bb.query_groups(q)
+    ones = np.ones((w.B, w.H, w.nQB, w.nKB), dtype=np.uint8)
+    full = bb.build_mask(None, None, w.block, spec=bb.explicit_spec(
+        torch.from_numpy(gu.mask_bitmap_words(ones).reshape(-1)).cuda()), shape=(w.B, w.H, w.N, w.d))
+    _, lse = bb.forward(q, k, v, full)
+    toks, _ = bb.select_tokens(q, k, perm, lse, density)
+    O, L = bb.forward_tokens(q, k, v, perm, toks)
+    torch.cuda.synchronize()
+    pg, tg = perm.cpu().numpy(), toks.cpu().numpy()
+    Og = O.float().reshape(BH, w.N, w.d).cpu().numpy().astype(np.float64)
+    Lg = L.reshape(BH, w.N).cpu().numpy().astype(np.float64)
+    qf, kf, vf = (inp[n].reshape(BH, w.N, w.d) for n in ("q", "k", "v"))
+    for h in range(BH):
+        O_ref, L_ref = oracle.token_attention(qf[h], kf[h], vf[h], pg[h], tg[h], C)
+        err = np.abs(Og[h] - O_ref)
+        assert err.max() <= gu.O_MAX_ABS and err.mean() <= gu.O_MEAN_ABS
+        assert np.abs(Lg[h] - L_ref).max() <= gu.LSE_MAX_ABS

@@ -25,7 +25,7 @@ def _header_functions():
 
 def test_header_symbols_exported(lib):
     names = _header_functions()
-    assert len(names) == 16
+    assert len(names) == 17
     assert sorted(bb.EXPORTS) == names
     for n in names:
         assert getattr(lib, n) is not None  # dlsym succeeds
@@ -61,7 +61,7 @@ def test_workspace_sizes(lib):
         bb.bsa_workspace_size(1, 1, 1, 0, 64, 64)
     assert e.value.code == bb.ERR_SHAPE
     with pytest.raises(bb.BsaError) as e:
-        bb.bsa_workspace_size(4, 1, 1, 128, 64, 64)  # 0 mask, 1 forward, 2 exact, 3 token selection
+        bb.bsa_workspace_size(5, 1, 1, 128, 64, 64)  # 0 mask, 1 forward, 2 exact, 3 tokens, 4 groups
     assert e.value.code == bb.ERR_INVALID_ARG
 
 
@@ -215,6 +215,26 @@ def test_token_selection_workspace_and_arguments(lib):
     assert sel(density=0.0) == bb.ERR_INVALID_ARG
     assert sel(tokens_capacity=2 * 4 * 128 - 1) == bb.ERR_CAPACITY
     assert sel(ws_bytes=256) == bb.ERR_WORKSPACE
+
+
+def test_query_groups_workspace_and_arguments(lib):
+    up = lambda x: (x + 255) // 256 * 256  # noqa: E731
+    n = 2 * 3 * 1024
+    assert bb.bsa_workspace_size(4, 2, 3, 1024, 64, 64) == 256 + 3 * up(n * 4)
+
+    def grp(**kw):
+        args = dict(Q=FAKE, dt=bb.BF16, B=1, H=2, N=512, d=64, perm=FAKE, ws=FAKE, ws_bytes=1 << 30)
+        args.update(kw)
+        with pytest.raises(bb.BsaError) as e:
+            bb.bsa_query_groups(**args, stream=0)
+        return e.value.code
+
+    assert grp(N=500) == bb.ERR_SHAPE
+    assert grp(N=128 * 513) == bb.ERR_SHAPE  # at most 512 groups per head
+    assert grp(d=32) == bb.ERR_SHAPE
+    assert grp(dt=2) == bb.ERR_DTYPE
+    assert grp(perm=None) == bb.ERR_INVALID_ARG
+    assert grp(ws_bytes=1024) == bb.ERR_WORKSPACE
 
 
 def test_token_forward_rejects_bad_arguments(lib):
