@@ -39,6 +39,7 @@ from block_sparse_attention_mean_gb300 import workloads as wl  # noqa: E402
 
 DEFAULT_WORKLOAD = "t2i_static"
 FLUSH_BYTES = 256 << 20
+FP32_FMA_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12  # CUDA-core fp32 peak of the GB300 (nominal clock)
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "fwd_tc_traffic.txt")
 FWD_SOURCE = os.path.join(ROOT, "block_sparse_attention_mean_gb300", "csrc", "fwd_tc.cu")
 
@@ -571,9 +572,12 @@ def run_tokens(args):
             "config": {"workload": w.name, "B": w.B, "H": w.H, "N": N, "d": d, "group": C, "tokens_per_group": K,
                        "l2": "flushed (256 MB write) before every timed call"},
             "anchor_step_ms": {"query_groups": round(group_ms, 3), "select_tokens": round(select_ms, 3)},
-            "roofline": {"bound": "tensor", "achieved": round(tflops, 3), "peak": float(peaks["bf16_tflops"]),
-                         "unit": "TFLOP/s", "frac": round(tflops / float(peaks["bf16_tflops"]), 4),
-                         "kernel": "fwd_tokens_kernel (CUDA cores: first path)", "peak_source": peak_kind}}
+            # a CUDA-core kernel: bounded by the fp32 FMA pipe, not the tensor cores
+            "roofline": {"bound": "alu", "achieved": round(tflops, 3), "peak": FP32_FMA_TFLOPS,
+                         "unit": "TFLOP/s", "frac": round(tflops / FP32_FMA_TFLOPS, 4),
+                         "kernel": "fwd_tokens_kernel (CUDA cores: first path)",
+                         "peak_source": "derived: 152 SMs x 128 fp32 FMA lanes x 2 FLOP x 2.07 GHz",
+                         "bf16_tensor_frac": round(tflops / float(peaks["bf16_tflops"]), 4)}}
     print(json.dumps(line))
 
 
