@@ -31,6 +31,19 @@ def test_header_symbols_exported(lib):
         assert getattr(lib, n) is not None  # dlsym succeeds
 
 
+def test_header_is_plain_c_and_cpp():
+    # the boundary is a C ABI: the header must compile as C99 and as C++17 with no other include
+    import shutil
+    import subprocess
+    header = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "bsa.h")
+    for cc, std, lang in (("gcc", "-std=c99", "c"), ("g++", "-std=c++17", "c++")):
+        if shutil.which(cc) is None:
+            pytest.skip(f"{cc} not available")
+        r = subprocess.run([cc, std, "-Wall", "-Wextra", "-Werror", "-fsyntax-only", "-x", lang, header],
+                           capture_output=True, text=True)
+        assert r.returncode == 0, r.stderr
+
+
 def test_status_strings(lib):
     assert bb.status_string(0) == "ok"
     assert "capacity" in bb.status_string(bb.ERR_CAPACITY)
