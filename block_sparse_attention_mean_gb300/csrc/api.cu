@@ -114,6 +114,68 @@ bsa_status check_spec(const bsa_static_spec *s, int nB, int64_t *count)
 
 }  // namespace
 
+namespace bsa {
+
+bsa_status current_sm_count(int *sm_count)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return BSA_ERR_CUDA;
+    return BSA_OK;
+}
+
+bsa_status prepare_build_mask(const void *Q, const void *K, int dt, int B, int H, int N, int d, int block,
+                              float density, const bsa_static_spec *spec, int32_t *row_ptr, int32_t *col_idx,
+                              int64_t col_capacity, uint32_t *bitmap, MaskArgs *out)
+{
+    bsa_status s = check_shape(B, H, N, d, block);
+    if (s != BSA_OK) return s;
+    if (dt != BSA_BF16 && dt != BSA_FP32) return BSA_ERR_DTYPE;
+    if (!row_ptr || !col_idx || !bitmap || col_capacity < 0) return BSA_ERR_INVALID_ARG;
+    if (!aligned(row_ptr, 4) || !aligned(col_idx, 4) || !aligned(bitmap, 4)) return BSA_ERR_INVALID_ARG;
+    const int nB = n_blocks(N, block);
+    const int64_t R = static_cast<int64_t>(B) * H * nB;
+    MaskArgs a{};
+    a.Q = Q;
+    a.K = K;
+    a.dt = dt;
+    a.B = B;
+    a.H = H;
+    a.N = N;
+    a.d = d;
+    a.block = block;
+    a.nQB = nB;
+    a.nKB = nB;
+    a.W = (nB + 31) / 32;
+    a.spec = spec;
+    a.row_ptr = row_ptr;
+    a.col_idx = col_idx;
+    a.col_capacity = col_capacity;
+    a.bitmap = bitmap;
+    int64_t nnz;
+    if (!spec) {
+        if (!Q || !K || !aligned(Q, 16) || !aligned(K, 16)) return BSA_ERR_INVALID_ARG;
+        if (!valid_density(density)) return BSA_ERR_INVALID_ARG;
+        if (nB > kMaxKvBlocks) return BSA_ERR_UNSUPPORTED;
+        a.k = topk_keep(density, nB);
+        a.n_text = 0;
+        a.kq[1][1] = a.k;
+        nnz = R * a.k;
+    } else {
+        int64_t c = 0;
+        s = check_spec(spec, nB, &c);
+        if (s != BSA_OK) return s;
+        nnz = spec->kind == BSA_STATIC_EXPLICIT ? -1 : R / nB * c;
+    }
+    if (nnz > col_capacity) return BSA_ERR_CAPACITY;
+    if (R * nB > INT32_MAX && (nnz < 0 || nnz > INT32_MAX)) return BSA_ERR_UNSUPPORTED;  // row_ptr is int32
+    *out = a;
+    return BSA_OK;
+}
+
+}  // namespace bsa
+
 extern "C" {
 
 const char *bsa_status_string(int status)
@@ -276,55 +338,16 @@ bsa_status bsa_build_mask(const void *Q, const void *K, int dt, int B, int H, in
                           const bsa_static_spec *spec, int32_t *row_ptr, int32_t *col_idx, int64_t col_capacity,
                           uint32_t *bitmap, void *workspace, size_t workspace_bytes, void *stream)
 {
-    bsa_status s = check_shape(B, H, N, d, block);
+    bsa::MaskArgs a{};
+    bsa_status s = bsa::prepare_build_mask(Q, K, dt, B, H, N, d, block, density, spec, row_ptr, col_idx,
+                                           col_capacity, bitmap, &a);
     if (s != BSA_OK) return s;
-    if (dt != BSA_BF16 && dt != BSA_FP32) return BSA_ERR_DTYPE;
-    if (!row_ptr || !col_idx || !bitmap || col_capacity < 0) return BSA_ERR_INVALID_ARG;
-    if (!aligned(row_ptr, 4) || !aligned(col_idx, 4) || !aligned(bitmap, 4)) return BSA_ERR_INVALID_ARG;
     if (!workspace || !aligned(workspace, 256) || workspace_bytes < bsa::mask_workspace_bytes(B, H, N, d, block))
         return BSA_ERR_WORKSPACE;
-    const int nB = n_blocks(N, block);
-    const int64_t R = static_cast<int64_t>(B) * H * nB;
-    bsa::MaskArgs a{};
-    a.Q = Q;
-    a.K = K;
-    a.dt = dt;
-    a.B = B;
-    a.H = H;
-    a.N = N;
-    a.d = d;
-    a.block = block;
-    a.nQB = nB;
-    a.nKB = nB;
-    a.W = (nB + 31) / 32;
-    a.spec = spec;
-    a.row_ptr = row_ptr;
-    a.col_idx = col_idx;
-    a.col_capacity = col_capacity;
-    a.bitmap = bitmap;
     a.ws = static_cast<char *>(workspace);
-    int64_t nnz;
-    if (!spec) {
-        if (!Q || !K || !aligned(Q, 16) || !aligned(K, 16)) return BSA_ERR_INVALID_ARG;
-        if (!valid_density(density)) return BSA_ERR_INVALID_ARG;
-        if (nB > bsa::kMaxKvBlocks) return BSA_ERR_UNSUPPORTED;
-        a.k = topk_keep(density, nB);
-        a.n_text = 0;
-        a.kq[1][1] = a.k;
-        nnz = R * a.k;
-    } else {
-        int64_t c = 0;
-        s = check_spec(spec, nB, &c);
-        if (s != BSA_OK) return s;
-        nnz = spec->kind == BSA_STATIC_EXPLICIT ? -1 : R / nB * c;
-    }
-    if (nnz > col_capacity) return BSA_ERR_CAPACITY;
-    if (R * nB > INT32_MAX && (nnz < 0 || nnz > INT32_MAX)) return BSA_ERR_UNSUPPORTED;  // row_ptr is int32
     // all argument checks passed: only now touch the device
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&a.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-        return BSA_ERR_CUDA;
+    s = bsa::current_sm_count(&a.sm_count);
+    if (s != BSA_OK) return s;
     return bsa::launch_build_mask(a, static_cast<cudaStream_t>(stream));
 }
 
@@ -484,6 +507,15 @@ bsa_status bsa_select_tokens(const void *Q, const void *K, int dt, int B, int H,
     a.tokens = tokens;
     a.ws = static_cast<char *>(workspace);
     return bsa::launch_select_tokens(a, static_cast<cudaStream_t>(stream));
+}
+
+bsa_status bsa_tokens_per_group(int N, float density, int *n_tokens)
+{
+    if (!n_tokens) return BSA_ERR_INVALID_ARG;
+    if (N <= 0) return BSA_ERR_SHAPE;
+    if (!valid_density(density)) return BSA_ERR_INVALID_ARG;
+    *n_tokens = topk_keep(density, N);
+    return BSA_OK;
 }
 
 bsa_status bsa_residual_capture(const void *O_dense, const void *O_sparse, int dt, int64_t count, float *R,

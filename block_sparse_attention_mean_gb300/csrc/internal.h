@@ -55,6 +55,16 @@ struct MaskArgs {
 };
 
 size_t mask_workspace_bytes(int B, int H, int N, int d, int block);
+// bytes of the workspace that one build reads or writes: the dynamic (pooled
+// blocks) or the static (counts, one head's pattern) part of the layout
+size_t mask_workspace_need(int B, int H, int N, int d, int block, bool dynamic);
+// Every host-side check of bsa_build_mask except the workspace's: fills `a`
+// (all but `ws`) and touches no device state, so a failing call enqueues nothing.
+bsa_status prepare_build_mask(const void *Q, const void *K, int dt, int B, int H, int N, int d, int block,
+                              float density, const bsa_static_spec *spec, int32_t *row_ptr, int32_t *col_idx,
+                              int64_t col_capacity, uint32_t *bitmap, MaskArgs *a);
+// streaming multiprocessors of the current device (a host query; enqueues nothing)
+bsa_status current_sm_count(int *sm_count);
 bsa_status launch_build_mask(const MaskArgs &a, cudaStream_t st);
 bsa_status launch_validate_index(int R, int nKB, const int32_t *row_ptr, const int32_t *col_idx,
                                  const uint32_t *bitmap, char *ws, cudaStream_t st);

@@ -545,6 +545,7 @@ __global__ void __launch_bounds__(256) validate_kernel(const int32_t *__restrict
 struct MaskWs {
     size_t qbar, kbar;                          // dynamic
     size_t counts, pat_rp, pat_bm;              // static
+    size_t dyn_end, static_end;                 // bytes a dynamic / static build touches
     size_t total;
 };
 
@@ -562,12 +563,20 @@ MaskWs mask_ws_layout(int B, int H, int N, int d, int block)
     l.pat_bm = l.pat_rp + align_up((nB + 1) * sizeof(int32_t), 256);
     const size_t static_end = l.pat_bm + align_up(nB * W * sizeof(uint32_t), 256);
     l.total = dyn_end > static_end ? dyn_end : static_end;
+    l.dyn_end = dyn_end;
+    l.static_end = static_end;
     return l;
 }
 
 size_t mask_workspace_bytes(int B, int H, int N, int d, int block)
 {
     return mask_ws_layout(B, H, N, d, block).total;
+}
+
+size_t mask_workspace_need(int B, int H, int N, int d, int block, bool dynamic)
+{
+    const MaskWs l = mask_ws_layout(B, H, N, d, block);
+    return dynamic ? l.dyn_end : l.static_end;
 }
 
 bsa_status launch_build_mask(const MaskArgs &a, cudaStream_t st)

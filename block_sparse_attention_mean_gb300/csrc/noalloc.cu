@@ -9,6 +9,7 @@
 // holds the array until the process exits.
 #include <cuda_runtime.h>
 
+#include <cstdint>
 #include <mutex>
 
 #include "internal.h"
@@ -47,20 +48,30 @@ extern "C" bsa_status bsa_build_mask_noalloc(const void *Q, const void *K, int d
                                              int32_t *row_ptr, int32_t *col_idx, int64_t col_capacity,
                                              uint32_t *bitmap, uint32_t *device_status, void *stream)
 {
-    size_t need = 0;
-    bsa_status s = bsa_workspace_size(0, B, H, N, d, block, &need);
+    // Every argument check runs first: a call that fails here has enqueued nothing,
+    // so it neither clears the status word of an earlier call still in flight nor
+    // leaves a stray node in a stream capture.
+    bsa::MaskArgs a{};
+    bsa_status s = bsa::prepare_build_mask(Q, K, dt, B, H, N, d, block, density, spec, row_ptr, col_idx,
+                                           col_capacity, bitmap, &a);
     if (s != BSA_OK) return s;
-    if (need > BSA_NOALLOC_SCRATCH_BYTES) return BSA_ERR_WORKSPACE;  // problem larger than the fixed scratch
+    if (device_status != nullptr && reinterpret_cast<uintptr_t>(device_status) % 4 != 0) return BSA_ERR_INVALID_ARG;
+    // A dynamic build pools Q and K into the scratch; a static one keeps only per-row
+    // counts and one head's pattern there.
+    if (bsa::mask_workspace_need(B, H, N, d, block, spec == nullptr) > BSA_NOALLOC_SCRATCH_BYTES)
+        return BSA_ERR_WORKSPACE;  // problem larger than the fixed scratch
+    s = bsa::current_sm_count(&a.sm_count);
+    if (s != BSA_OK) return s;
     void *scratch = nullptr;
     s = scratch_for_current_device(&scratch);
     if (s != BSA_OK) return s;
+    a.ws = static_cast<char *>(scratch);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     // The array keeps the previous call's contents: the header (device status
     // word and the counters of last-CTA launches) must start at zero. Every other
     // byte the build reads is written by the same build first.
     if (cudaMemsetAsync(scratch, 0, bsa::kWsHeader, st) != cudaSuccess) return BSA_ERR_CUDA;
-    s = bsa_build_mask(Q, K, dt, B, H, N, d, block, density, spec, row_ptr, col_idx, col_capacity, bitmap, scratch,
-                       BSA_NOALLOC_SCRATCH_BYTES, stream);
+    s = bsa::launch_build_mask(a, st);
     if (s != BSA_OK) return s;
     if (device_status != nullptr &&
         cudaMemcpyAsync(device_status, scratch, sizeof(uint32_t), cudaMemcpyDeviceToDevice, st) != cudaSuccess)

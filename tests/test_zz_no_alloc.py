@@ -7,6 +7,8 @@ This file is collected last on purpose: a run that stops at the first failure ha
 already run every other test. It must pass alone in a fresh process and after the
 other tests, which both exercise the per-device set-up and the reuse of the array.
 """
+import warnings
+
 import numpy as np
 import pytest
 import torch
@@ -93,3 +95,71 @@ def test_noalloc_rejects_problems_larger_than_its_scratch():
         bb.bsa_build_mask_noalloc(1 << 20, 1 << 20, bb.BF16, B, H, N, d, block, 0.1, None, 1 << 20, 1 << 20,
                                   1 << 30, 1 << 20)
     assert e.value.code == bb.ERR_WORKSPACE
+
+
+def _captures_nothing(fn) -> bool:
+    """Capture fn(stream) into a CUDA graph; True when the graph came out empty (torch
+    warns about an empty capture)."""
+    g = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    with warnings.catch_warnings(record=True) as rec:
+        warnings.simplefilter("always")
+        with torch.cuda.graph(g, stream=side):
+            fn(side)
+    torch.cuda.synchronize()
+    return any("graph is empty" in str(r.message).lower() for r in rec)
+
+
+def test_noalloc_failed_call_enqueues_nothing():
+    """A call rejected by an argument check enqueues no work: captured into a CUDA graph
+    on its own, it leaves the graph empty (no clearing of the array's header, no copy of a
+    status word, no kernel). A valid call, captured the same way, does not."""
+    w = wl.scaled(wl.WORKLOADS["dynamic_topk"], H=1, N=1024)
+    inp = wl.make_inputs(w)
+    q, k = _upload(inp, "q"), _upload(inp, "k")
+    cap = bb.bsa_mask_nnz(w.B, w.H, w.N, w.block, w.density, None)
+    row_ptr, col_idx, bitmap = _index_buffers(w, cap)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+
+    def call(stream, density=w.density, rp=row_ptr, capacity=cap):
+        bb.bsa_build_mask_noalloc(q, k, bb.BF16, w.B, w.H, w.N, w.d, w.block, density, None, rp, col_idx,
+                                  capacity, bitmap, device_status=status, stream=stream)
+
+    call(None)  # the per-device set-up happens outside any capture
+    torch.cuda.synchronize()
+    assert not _captures_nothing(call)  # control: a valid call is captured
+    codes = []
+
+    def failing(stream):
+        for kw in (dict(density=float("nan")), dict(density=1.5), dict(capacity=cap - 1), dict(rp=0)):
+            try:
+                call(stream, **kw)
+                codes.append(bb.OK)
+            except bb.BsaError as e:
+                codes.append(e.code)
+
+    assert _captures_nothing(failing)
+    assert codes == [bb.ERR_INVALID_ARG, bb.ERR_INVALID_ARG, bb.ERR_CAPACITY, bb.ERR_INVALID_ARG]
+
+
+def test_noalloc_static_spec_sized_by_the_static_path():
+    """A static build needs only per-row counts and one head's pattern, so a band
+    mask whose dynamic build would not fit the array is accepted."""
+    w = wl.scaled(wl.WORKLOADS["t2i_static"], B=1, H=64)
+    spec = bb.band_spec(w.n_text_blocks, w.band, list(w.anchors))
+    B, H, N, d, block = 1, 64, 65536 + w.n_text_blocks * 64, 128, 64
+    assert bb.bsa_workspace_size(0, B, H, N, d, block) > bb.NOALLOC_SCRATCH_BYTES
+    nB = N // block
+    cap = bb.bsa_mask_nnz(B, H, N, block, 0.0, spec)
+    row_ptr = torch.empty(B * H * nB + 1, dtype=torch.int32, device="cuda")
+    col_idx = torch.empty(cap, dtype=torch.int32, device="cuda")
+    bitmap = torch.empty(B * H * nB * ((nB + 31) // 32), dtype=torch.int32, device="cuda")
+    status = torch.full((1,), 12345, dtype=torch.int32, device="cuda")
+    bb.bsa_build_mask_noalloc(None, None, bb.BF16, B, H, N, d, block, 0.0, spec, row_ptr, col_idx, cap, bitmap,
+                              device_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == bb.OK
+    ref = bb.build_mask(None, None, block, spec=spec, shape=(B, H, N, d))
+    assert torch.equal(row_ptr, ref.row_ptr)
+    assert torch.equal(col_idx, ref.col_idx[:cap])
+    assert torch.equal(bitmap, ref.bitmap)
