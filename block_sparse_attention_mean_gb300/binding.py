@@ -41,7 +41,7 @@ EXPORTS = ("bsa_build_mask", "bsa_forward", "bsa_mask_nnz", "bsa_workspace_size"
            "bsa_check_device_error", "bsa_validate_index", "bsa_debug_config",
            "bsa_status_string", "bsa_build_mask_noalloc", "bsa_residual_capture", "bsa_forward_residual",
            "bsa_build_mask_modal", "bsa_mask_nnz_modal", "bsa_build_mask_exact", "bsa_forward_tokens",
-           "bsa_select_tokens", "bsa_query_groups")
+           "bsa_select_tokens", "bsa_query_groups", "bsa_tokens_per_group")
 NOALLOC_SCRATCH_BYTES = 16 << 20  # BSA_NOALLOC_SCRATCH_BYTES
 # bsa_debug_config flag bits
 DBG_STALL = 1       # skip loads and MMAs: the first device wait runs out
@@ -84,6 +84,7 @@ def load():
     lib.bsa_forward_tokens.argtypes = [P, P, P, I, I, I, I, I, P, P, I, F, P, P, P, SZ, P]
     lib.bsa_select_tokens.argtypes = [P, P, I, I, I, I, I, P, P, F, F, P, I64, P, SZ, P]
     lib.bsa_query_groups.argtypes = [P, I, I, I, I, I, P, P, SZ, P]
+    lib.bsa_tokens_per_group.argtypes = [I, F, ctypes.POINTER(I)]
     lib.bsa_build_mask_modal.argtypes = [P, P, I, I, I, I, I, I, I, P, P, P, I64, P, P, SZ, P]
     lib.bsa_mask_nnz_modal.argtypes = [I, I, I, I, I, P, ctypes.POINTER(I64)]
     lib.bsa_build_mask_exact.argtypes = [P, P, I, I, I, I, I, I, F, F, P, P, P, I64, P, P, SZ, P]
@@ -214,9 +215,9 @@ def build_mask_exact(q: torch.Tensor, k: torch.Tensor, lse_dense: torch.Tensor, 
     B, H, N, d = q.shape
     nB = -(-N // block)  # a ragged last block counts
     W = (nB + 31) // 32
-    kk = max(1, min(nB, int(math.floor(float(np.float32(density)) * nB))))
+    nnz = bsa_mask_nnz(B, H, N, block, density, None)  # the same count rule as the pooled selector
     row_ptr = torch.empty(B * H * nB + 1, dtype=torch.int32, device=q.device)
-    col_idx = torch.empty(B * H * nB * kk, dtype=torch.int32, device=q.device)
+    col_idx = torch.empty(nnz, dtype=torch.int32, device=q.device)
     bitmap = torch.empty(B * H * nB * W, dtype=torch.int32, device=q.device)
     if ws is None:
         ws = workspace(2, B, H, N, d, block, q.device)
@@ -426,10 +427,15 @@ def forward_tokens(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, perm: torc
     return out, lse
 
 
+def bsa_tokens_per_group(N: int, density: float) -> int:
+    out = ctypes.c_int(0)
+    _check(load().bsa_tokens_per_group(int(N), float(density), ctypes.byref(out)), "bsa_tokens_per_group")
+    return int(out.value)
+
+
 def tokens_per_group(N: int, density: float) -> int:
-    """K = max(1, floor(density * N)) with density taken as fp32 (the library's rule)."""
-    k = int(math.floor(float(np.float32(density)) * N))
-    return min(max(k, 1), N)
+    """Tokens each query group keeps (the library's host count, bsa_tokens_per_group)."""
+    return bsa_tokens_per_group(N, density)
 
 
 def query_groups(q: torch.Tensor, stream=None) -> torch.Tensor:

@@ -276,6 +276,14 @@ bsa_status bsa_select_tokens(const void *Q, const void *K, int dt, int B, int H,
                              const float *LSE, float density, float scale, int32_t *tokens, int64_t tokens_capacity,
                              void *workspace, size_t workspace_bytes, void *stream);
 
+/* Host-only: the tokens each query group keeps in bsa_select_tokens ("Can sparse attention
+ * close the quality gap in diffusion transformers", section "质量差距有三个可分离来源": the
+ * token oracle keeps a fixed share of the keys), K = max(1, floor(density * N)) with density
+ * as given (fp32) and the product in double, at most N. Sizes the tokens buffer
+ * (B*H*(N/128)*K entries). Errors: BSA_ERR_INVALID_ARG (null out, density outside (0, 1]),
+ * BSA_ERR_SHAPE (N <= 0). */
+bsa_status bsa_tokens_per_group(int N, float density, int *n_tokens);
+
 /*
  * bsa_forward_tokens -- token-sparse attention over tile-aligned query groups
  * ("Can sparse attention close the quality gap in diffusion transformers", section
@@ -319,9 +327,12 @@ bsa_status bsa_forward_tokens(const void *Q, const void *K, const void *V, int d
  *                  order at the end of the call, the device-raised status of this
  *                  build (BSA_OK, BSA_ERR_NONFINITE or BSA_ERR_CAPACITY).
  *
- * Returns BSA_ERR_WORKSPACE, before any launch, when the problem needs more
- * scratch than the array holds (bsa_workspace_size(0, ...) larger than
- * BSA_NOALLOC_SCRATCH_BYTES). The first call on a device looks up the array's
+ * Every argument check of bsa_build_mask runs before anything is enqueued: a
+ * call that returns an error has enqueued no work. Returns BSA_ERR_WORKSPACE,
+ * before any launch, when the problem needs more scratch than the array holds:
+ * a dynamic build needs the pooled blocks (about 2 * B*H*nB*d*4 bytes), a static
+ * one only per-row counts and one head's pattern (about B*H*nB*4 + nB*(nB/8)
+ * bytes). The first call on a device looks up the array's
  * device address (once per device, with that device current): make that first
  * call before any stream capture. All calls share the one array: calls whose
  * work overlaps on the GPU (different streams without ordering, or different

@@ -25,7 +25,7 @@ def _header_functions():
 
 def test_header_symbols_exported(lib):
     names = _header_functions()
-    assert len(names) == 17
+    assert len(names) == 18
     assert sorted(bb.EXPORTS) == names
     for n in names:
         assert getattr(lib, n) is not None  # dlsym succeeds
@@ -324,3 +324,20 @@ def test_exact_selector_workspace_and_bad_arguments(lib):
         with pytest.raises(bb.BsaError) as e:
             bb.bsa_build_mask_exact(**a, stream=0)
         assert e.value.code == code
+
+
+def test_tokens_per_group_count(lib):
+    # K = max(1, floor(density * N)), density as fp32, at most N
+    assert bb.bsa_tokens_per_group(8192, 0.15) == 1228
+    assert bb.bsa_tokens_per_group(1024, 0.1) == 102
+    assert bb.bsa_tokens_per_group(128, 1e-6) == 1
+    assert bb.bsa_tokens_per_group(128, 1.0) == 128
+    # 0.3 in fp32 is 0.30000001192..., so 10 * it floors to 3, not 2
+    assert bb.bsa_tokens_per_group(10, 0.3) == 3
+    for bad in (0.0, -0.1, 1.5, float("nan")):
+        with pytest.raises(bb.BsaError) as e:
+            bb.bsa_tokens_per_group(1024, bad)
+        assert e.value.code == bb.ERR_INVALID_ARG
+    with pytest.raises(bb.BsaError) as e:
+        bb.bsa_tokens_per_group(0, 0.5)
+    assert e.value.code == bb.ERR_SHAPE
