@@ -274,7 +274,7 @@ def compensate(o_sparse: np.ndarray, r: np.ndarray) -> np.ndarray:
 # token, the attention mass the group's queries give it under dense attention.
 
 
-def query_groups(q: np.ndarray, C: int) -> np.ndarray:
+def query_groups(q: np.ndarray, C: int, splits: Optional[list] = None) -> np.ndarray:
     """Median-split principal-direction grouping of one head's queries (reading R21).
 
     q: [N, d] (N a multiple of C). A group of m*C rows (m >= 2) is centred, projected on the
@@ -283,6 +283,9 @@ def query_groups(q: np.ndarray, C: int) -> np.ndarray:
     first ceil(m/2)*C rows; the two halves are split again until every group holds C rows.
     Returns perm [N]: group g is rows perm[g*C:(g+1)*C], groups in depth-first order
     (first half before second half), rows inside a group in ascending index order.
+    If `splits` is a list, one record per split is appended to it (for tests that bound how
+    far an inexact computation may be from this one): the two largest eigenvalues, the gap
+    between the projections on either side of the cut, and the largest centred row norm.
     """
     x = np.asarray(q, dtype=np.float64)
     N = x.shape[0]
@@ -303,6 +306,10 @@ def query_groups(q: np.ndarray, C: int) -> np.ndarray:
         proj = xc @ u
         order = rows[np.lexsort((rows, proj))]
         cut = -(-m // 2) * C
+        if splits is not None:
+            p = np.sort(proj)
+            splits.append({"lam1": float(w[-1]), "lam2": float(w[-2]), "gap": float(p[cut] - p[cut - 1]),
+                           "rmax": float(np.sqrt((xc * xc).sum(axis=1)).max())})
         split(order[:cut])
         split(order[cut:])
 

@@ -153,6 +153,37 @@ def test_query_groups_on_a_line_match_the_oracle():
         assert np.array_equal(perm.cpu().numpy()[0], oracle.query_groups(q, C))
 
 
+def anisotropic_queries(N, d, seed):
+    """Gaussian queries with distinct leading variances (scales 81, 27, 9, 3, 1.5, then 1) in a
+    seeded random orientation: every split of the grouping has a clear principal direction."""
+    rng = np.random.default_rng(seed)
+    sc = np.ones(d)
+    sc[:5] = [81, 27, 9, 3, 1.5]
+    rot, _ = np.linalg.qr(rng.standard_normal((d, d)))
+    return ((rng.standard_normal((N, d)) * sc) @ rot.T / 8).astype(np.float32)
+
+
+@pytest.mark.parametrize("d,seed", [(128, 1), (64, 2)])
+def test_query_groups_anisotropic_match_the_oracle_exactly(d, seed):
+    # The GPU takes each principal direction by 32 fp32 power-iteration steps. Against the
+    # exact eigenvector its direction errs by at most ~ T * rho^32 (rho = lam2/lam1, T the
+    # tangent of the start vector's angle, <= 10 here) plus fp32 rounding ~ 4*d*2^-24, so a
+    # difference of two projections errs by at most eps = 2 * rmax * (10 * rho^32 + 4*d*2^-24)
+    # (rmax: largest centred row norm). When every cut's gap exceeds its eps, no row can change
+    # sides and the groups must equal the oracle's bit for bit.
+    N = 1024
+    x = anisotropic_queries(N, d, seed)
+    splits = []
+    ref = oracle.query_groups(x, C, splits=splits)
+    for sp in splits:
+        rho = sp["lam2"] / sp["lam1"]
+        eps = 2.0 * sp["rmax"] * (10.0 * rho ** 32 + 4.0 * d * 2.0 ** -24)
+        assert sp["gap"] > eps, (sp, eps)  # the data leave no row within eps of a cut
+    perm = bb.query_groups(torch.from_numpy(x).reshape(1, 1, N, d).cuda())
+    torch.cuda.synchronize()
+    assert np.array_equal(perm.cpu().numpy()[0], ref)
+
+
 @pytest.mark.parametrize("name", sorted(CASES))
 def test_query_groups_partition_and_quality(name):
     # a valid partition into ascending groups of 128, as tight as the oracle's (its direction
