@@ -24,3 +24,15 @@ def test_reference_arm_prints_the_contract_line():
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"] and cb["sample"]
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
     assert d["e2e"]["value"] == d["value"] and d["e2e"]["unit"] == d["unit"]
+
+
+def test_reference_arm_loads_no_product_library():
+    """The reference arm counts its FLOPs on the oracle's own masks: it neither imports the
+    binding nor maps libbsa.so."""
+    code = ("import sys; sys.argv = ['bench.py', '--impl', 'reference', '--workload', 'tiny', '--steps', '1', "
+            "'--warmup', '0']; import bench; bench.main(); "
+            "assert 'block_sparse_attention_mean_gb300.binding' not in sys.modules; "
+            "maps = open('/proc/self/maps').read(); assert 'libbsa' not in maps; print('clean')")
+    r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    assert r.stdout.strip().endswith("clean")
