@@ -1327,7 +1327,8 @@ __device__ __forceinline__ int tile_length(const TcParams &p, int tile, int BS)
         if (p.index_mode == 0) {
             len += p.row_ptr[r + 1] - p.row_ptr[r];
         } else {
-            for (int w = 0; w < p.W; ++w) len += __popc(p.bitmap[r * p.W + w]);
+#pragma unroll 4
+            for (int w = 0; w < p.W; ++w) len += __popc(__ldg(p.bitmap + r * p.W + w));
         }
     }
     return len;
@@ -1394,6 +1395,85 @@ __device__ __forceinline__ int reserve_slots(int *hist, int bk, int n)
     return base + (n == 1 ? __popc(grp & ((1u << lane) - 1u)) : 0);
 }
 
+// Stable placement of one 1024-tile chunk (one tile per thread, in tile order):
+// a tile's n items go to bucket bk after every item of the same bucket from
+// earlier chunks and from lower threads of this chunk, so items of equal length
+// keep tile order. Persistent CTAs then take neighbouring tiles of one head
+// together and its K and V stay in L2 (an order that interleaves heads re-reads
+// them from DRAM). hist[bk] holds the bucket's next free position and is advanced.
+// cnt is a [kBuckets][32] table of per-warp item counts in dynamic shared memory,
+// zero on entry and on return (each entry is written and cleared by the one lane
+// that leads its warp's group of the bucket). Called by all threads of the block; n = 0 places
+// nothing.
+constexpr size_t kOrderTableBytes = sizeof(uint16_t) * kBuckets * 32;
+
+__device__ __forceinline__ int place_ordered(int *hist, int bk, int n, uint16_t *cnt)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int key = n > 0 ? bk : -1;
+    // lanes with the same bucket (one group when the warp agrees: no match needed)
+    const unsigned grp = __all_sync(0xffffffffu, key == __shfl_sync(0xffffffffu, key, 0))
+                             ? 0xffffffffu
+                             : __match_any_sync(0xffffffffu, key);
+    const unsigned lower = (1u << lane) - 1u;
+    // rank among earlier lanes of the same bucket, weighted by items, and the group total
+    int rank, total;
+    if (!__any_sync(0xffffffffu, n > 1)) {
+        rank = __popc(grp & lower);
+        total = __popc(grp);
+    } else {  // a split tile in this warp: items per lane differ
+        rank = total = 0;
+#pragma unroll 8
+        for (int l = 0; l < 32; ++l) {
+            const int nl = __shfl_sync(0xffffffffu, n, l);
+            if ((grp >> l) & 1u) {
+                total += nl;
+                if (l < lane) rank += nl;
+            }
+        }
+    }
+    const bool leader = key >= 0 && lane == __ffs(grp) - 1;
+    if (leader) cnt[bk * 32 + warp] = static_cast<uint16_t>(total);
+    __syncthreads();
+    int pos = 0;
+    if (key >= 0) {
+        // items of this bucket from lower warps of the chunk: the row's first `warp` counts
+        const uint4 *row = reinterpret_cast<const uint4 *>(cnt + bk * 32);
+        int pref = 0;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const uint4 v = row[q];
+            const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+                const int w0 = 8 * q + 2 * h;  // warps of the two halves of this word
+                if (w0 < warp) pref += static_cast<int>(w4[h] & 0xffffu);
+                if (w0 + 1 < warp) pref += static_cast<int>(w4[h] >> 16);
+            }
+        }
+        pos = hist[bk] + pref + rank;
+    }
+    __syncthreads();  // every thread has read hist and the table
+    // each (warp, bucket) leader advances its bucket and clears its own entry, which
+    // leaves the table zero for the next chunk
+    if (leader) {
+        atomicAdd(&hist[bk], total);
+        cnt[bk * 32 + warp] = 0;
+    }
+    __syncthreads();
+    return pos;
+}
+
+// zero the count table once per launch
+__device__ __forceinline__ void clear_order_table(uint16_t *cnt)
+{
+    uint4 *p = reinterpret_cast<uint4 *>(cnt);
+    for (int i = threadIdx.x; i < static_cast<int>(kOrderTableBytes / 16); i += blockDim.x)
+        p[i] = make_uint4(0u, 0u, 0u, 0u);
+}
+
+constexpr int kOrderPerThread = 8;  // 1024-tile chunks handled per batch (tiles per thread)
+
 struct OrderArgs {
     int BS, grid, budget;
     int32_t *items, *lens, *split_base;
@@ -1410,30 +1490,77 @@ __global__ void __launch_bounds__(1024) tile_order_kernel(TcParams p, OrderArgs 
 {
     grid_launch_dependents();  // the forward's prologue may start now (it waits for this grid's results)
     __shared__ int hist[kBuckets];
+    extern __shared__ uint4 order_dyn[];
+    uint16_t *ocnt = reinterpret_cast<uint16_t *>(order_dyn);
     __shared__ int wsum[32];
     __shared__ bool is_last;
     const int t = threadIdx.x;
     const int tile0 = blockIdx.x * 1024 + t;
     int len = 0;
-    if (tile0 < p.n_tiles) {
-        len = tile_length(p, tile0, o.BS);
-        o.lens[tile0] = len;
+    if (p.index_mode == 0) {
+        if (tile0 < p.n_tiles) len = tile_length(p, tile0, o.BS);
+    } else {
+        // Bitmap lengths, coalesced: the index rows of consecutive tiles are consecutive,
+        // so a warp reads the words of its 32 tiles as one contiguous run (lane-strided)
+        // and adds each word's popcount to its tile's count in shared memory. (One tile
+        // per thread would read words 4*W bytes apart: 32 sectors per load instruction.)
+        int *tl = hist;  // the bucket histogram is not in use yet
+        tl[t] = 0;
+        __syncthreads();
+        const int lane = t & 31;
+        const int first = blockIdx.x * 1024 + (t & ~31);  // this warp's first tile
+        const int last = min(first + 32, p.n_tiles);      // one past its last tile
+        if (first < last) {
+            const int per = o.BS == 128 ? 1 : 2;  // Q blocks per tile
+            // rows of the warp's tiles, relative to the first tile's head: tile index
+            // arithmetic stays in 32 bits (64-bit divisions are emulated and slow)
+            const int bh0 = first / p.tiles_per_bh;
+            const int qt0 = first - bh0 * p.tiles_per_bh;
+            const int64_t row0 = static_cast<int64_t>(bh0) * p.nQB + qt0 * per;  // first row of `first`
+            const int bhl = (last - 1) / p.tiles_per_bh;
+            const int qtl = (last - 1) - bhl * p.tiles_per_bh;
+            const int rows = static_cast<int>(static_cast<int64_t>(bhl) * p.nQB + min(qtl * per + per, p.nQB) - row0);
+            const uint32_t *words = p.bitmap + row0 * p.W;
+            const int n_words = rows * p.W;
+            for (int e0 = lane; e0 < n_words; e0 += 32 * 8) {
+                uint32_t v[8];  // eight loads in flight before any is used
+#pragma unroll
+                for (int u = 0; u < 8; ++u) v[u] = e0 + 32 * u < n_words ? __ldg(words + e0 + 32 * u) : 0u;
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int e = e0 + 32 * u;
+                    if (e >= n_words) break;
+                    const int lr = qt0 * per + e / p.W;  // row within head bh0 (may run into later heads)
+                    const int dh = lr / p.nQB;
+                    const int tile = first - qt0 + dh * p.tiles_per_bh + (lr - dh * p.nQB) / per;
+                    atomicAdd(&tl[tile - blockIdx.x * 1024], __popc(v[u]));
+                }
+            }
+        }
+        __syncthreads();
+        len = tile0 < p.n_tiles ? tl[t] : 0;
+        __syncthreads();
     }
-    // block sum and max of the lengths, then one atomic each
+    if (tile0 < p.n_tiles) o.lens[tile0] = len;
+    // block sum, max and min of the lengths, then one atomic each
     {
         const unsigned wsum_l = __reduce_add_sync(0xffffffffu, static_cast<unsigned>(len));
         const unsigned wmax_l = __reduce_max_sync(0xffffffffu, static_cast<unsigned>(len));
+        const unsigned wmin_c = __reduce_max_sync(0xffffffffu, tile0 < p.n_tiles ? ~static_cast<unsigned>(len) : 0u);
         if ((t & 31) == 0) {
             wsum[t >> 5] = static_cast<int>(wsum_l);
             hist[t >> 5] = static_cast<int>(wmax_l);
+            hist[32 + (t >> 5)] = static_cast<int>(wmin_c);
         }
         __syncthreads();
         if (t < 32) {
             const unsigned bs = __reduce_add_sync(0xffffffffu, static_cast<unsigned>(wsum[t]));
             const unsigned bm = __reduce_max_sync(0xffffffffu, static_cast<unsigned>(hist[t]));
+            const unsigned bmc = __reduce_max_sync(0xffffffffu, static_cast<unsigned>(hist[32 + t]));
             if (t == 0) {
                 atomicAdd(&o.hdr->total_steps, static_cast<unsigned long long>(bs));
                 atomicMax(&o.hdr->max_len, bm);
+                atomicMax(&o.hdr->min_len_c, bmc);
             }
         }
     }
@@ -1443,65 +1570,108 @@ __global__ void __launch_bounds__(1024) tile_order_kernel(TcParams p, OrderArgs 
     __syncthreads();
     if (!is_last) return;
     __threadfence();
-    const unsigned long long total = atomicAdd(&o.hdr->total_steps, 0ull);
+    // every CTA's atomics precede its count, so plain L2 loads see the final values
+    const unsigned long long total = __ldcg(&o.hdr->total_steps);
     unsigned long long share = (total + o.grid - 1) / o.grid;
     if (share < kMinChunkSteps) share = kMinChunkSteps;
     if (share > 0x7fffffffull) share = 0x7fffffffull;
     const int T = static_cast<int>(share);
-    const int max_len = static_cast<int>(atomicMax(&o.hdr->max_len, 0u));
+    const int max_len = static_cast<int>(__ldcg(&o.hdr->max_len));
+    const int min_len = static_cast<int>(~__ldcg(&o.hdr->min_len_c));
     const bool can_split = p.split_ok && o.budget > 0 && !(p.dbg & kDbgNoSplit) &&
                            ((p.dbg & kDbgSplitAll) || splits(max_len, T));
+    int n_items;
+    if (!can_split && min_len == max_len) {
+        // every tile has the same length (any top-k mask): the stable longest-first
+        // order is tile order
+        for (int i = t; i < p.n_tiles; i += 1024) o.items[i] = i;
+        n_items = p.n_tiles;
+    } else {
+    // The passes below walk the tiles in batches of kOrderPerThread 1024-tile chunks
+    // whose lengths (and split slots) are loaded together: one round trip per batch.
+    constexpr int KB = kOrderPerThread;
     // split decisions: partial slots are handed out in tile order while the budget lasts
     int carry = 0;
-    for (int b0 = 0; can_split && b0 < p.n_tiles; b0 += 1024) {
-        const int tile = b0 + t;
-        const int n0 = can_split && tile < p.n_tiles ? n_chunks(__ldcg(o.lens + tile), T, p.dbg) : 1;
-        const int want = n0 > 1 ? n0 : 0;
-        int step_total;
-        const int excl = carry + block_scan_excl(want, step_total, wsum);
-        if (tile < p.n_tiles) {
-            const bool fits = want > 0 && excl + want <= o.budget;
-            o.split_base[tile] = fits ? excl : -1;
-            if (fits)
-                for (int w = 0; w < kMergeWarps; ++w) o.merge_cnt[static_cast<size_t>(excl) * kMergeWarps + w] = 0u;
+    for (int s0 = 0; can_split && s0 < p.n_tiles; s0 += 1024 * KB) {
+        int Lb[KB];
+#pragma unroll
+        for (int k = 0; k < KB; ++k) {
+            const int tile = s0 + k * 1024 + t;
+            Lb[k] = tile < p.n_tiles ? __ldcg(o.lens + tile) : 0;
         }
-        carry += step_total;
+#pragma unroll
+        for (int k = 0; k < KB; ++k) {
+            if (s0 + k * 1024 >= p.n_tiles) break;  // block-uniform
+            const int tile = s0 + k * 1024 + t;
+            const int n0 = tile < p.n_tiles ? n_chunks(Lb[k], T, p.dbg) : 1;
+            const int want = n0 > 1 ? n0 : 0;
+            int step_total;
+            const int excl = carry + block_scan_excl(want, step_total, wsum);
+            if (tile < p.n_tiles) {
+                const bool fits = want > 0 && excl + want <= o.budget;
+                o.split_base[tile] = fits ? excl : -1;
+                if (fits)
+                    for (int w = 0; w < kMergeWarps; ++w)
+                        o.merge_cnt[static_cast<size_t>(excl) * kMergeWarps + w] = 0u;
+            }
+            carry += step_total;
+        }
     }
     __syncthreads();
+    // items and length bucket of the tiles of one batch
+    auto batch = [&](int s0, int (&nb)[KB], int (&bkb)[KB]) {
+        int Lb[KB], sb[KB];
+#pragma unroll
+        for (int k = 0; k < KB; ++k) {
+            const int tile = s0 + k * 1024 + t;
+            const bool valid = tile < p.n_tiles;
+            Lb[k] = valid ? __ldcg(o.lens + tile) : 0;
+            sb[k] = valid && can_split ? o.split_base[tile] : -1;
+        }
+#pragma unroll
+        for (int k = 0; k < KB; ++k) {
+            const bool valid = s0 + k * 1024 + t < p.n_tiles;
+            nb[k] = !valid ? 0 : (sb[k] >= 0 ? n_chunks(Lb[k], T, p.dbg) : 1);
+            bkb[k] = length_bucket(nb[k] > 0 ? (Lb[k] + nb[k] - 1) / nb[k] : 0);
+        }
+    };
     // histogram of item lengths, longest first
     for (int bk = t; bk < kBuckets; bk += 1024) hist[bk] = 0;
     __syncthreads();
-    for (int b0 = 0; b0 < p.n_tiles; b0 += 1024) {
-        const int tile = b0 + t;
-        int n = 0, bk = 0;
-        if (tile < p.n_tiles) {
-            const int L = __ldcg(o.lens + tile);
-            n = can_split && o.split_base[tile] >= 0 ? n_chunks(L, T, p.dbg) : 1;
-            bk = length_bucket((L + n - 1) / n);
+    for (int s0 = 0; s0 < p.n_tiles; s0 += 1024 * KB) {
+        int nb[KB], bkb[KB];
+        batch(s0, nb, bkb);
+#pragma unroll
+        for (int k = 0; k < KB; ++k) {
+            if (s0 + k * 1024 + (t & ~31) >= p.n_tiles) continue;  // no tile in this warp (warp-uniform)
+            (void)reserve_slots(hist, bkb[k], nb[k]);
         }
-        (void)reserve_slots(hist, bk, n);
     }
+    clear_order_table(ocnt);
     __syncthreads();
-    int n_items;
     const int excl = block_scan_excl(hist[t], n_items, wsum);
     hist[t] = excl;
     __syncthreads();
-    for (int b0 = 0; b0 < p.n_tiles; b0 += 1024) {
-        const int tile = b0 + t;
-        int n = 0, bk = 0;
-        if (tile < p.n_tiles) {
-            const int L = __ldcg(o.lens + tile);
-            n = can_split && o.split_base[tile] >= 0 ? n_chunks(L, T, p.dbg) : 1;
-            bk = length_bucket((L + n - 1) / n);
+    for (int s0 = 0; s0 < p.n_tiles; s0 += 1024 * KB) {
+        int nb[KB], bkb[KB];
+        batch(s0, nb, bkb);
+#pragma unroll
+        for (int k = 0; k < KB; ++k) {
+            if (s0 + k * 1024 >= p.n_tiles) break;  // block-uniform
+            const int tile = s0 + k * 1024 + t;
+            const int n = nb[k];
+            const int pos = place_ordered(hist, bkb[k], n, ocnt);
+            for (int c = 0; c < n; ++c)
+                o.items[pos + c] = tile | (c << kItemTileBits) | ((n - 1) << (kItemTileBits + 3));
         }
-        const int pos = reserve_slots(hist, bk, n);
-        for (int c = 0; c < n; ++c) o.items[pos + c] = tile | (c << kItemTileBits) | ((n - 1) << (kItemTileBits + 3));
     }
+    }  // lengths differ or tiles split
     if (t == 0) {
         o.hdr->n_items = static_cast<uint32_t>(n_items);
         o.hdr->chunk_steps = static_cast<uint32_t>(T);
         o.hdr->total_steps = 0ull;
         o.hdr->max_len = 0u;
+        o.hdr->min_len_c = 0u;
         *p.tile_counter = 0u;
         o.hdr->order_done = 0u;
     }
@@ -1510,52 +1680,78 @@ __global__ void __launch_bounds__(1024) tile_order_kernel(TcParams p, OrderArgs 
 // The same work list from one CTA for a CSR index whose tiles fit its registers
 // (up to kOrderPerThread per thread): no length array, no election between CTAs.
 // A tile's Q blocks are consecutive index rows, so its length is one difference
-// of row_ptr; all the loads are issued before any is used.
-constexpr int kOrderPerThread = 8;
-
+// of row_ptr; all the loads are issued before any is used. (Bitmap lengths are
+// popcounts of rows strided across the threads: one SM would pull them too
+// slowly, so bitmap indexes take the multi-CTA launch.)
 __global__ void __launch_bounds__(1024) tile_order_small_kernel(TcParams p, OrderArgs o)
 {
     grid_launch_dependents();  // the forward's prologue may start now (it waits for this grid's results)
     __shared__ int hist[kBuckets];
+    extern __shared__ uint4 order_dyn[];
+    uint16_t *ocnt = reinterpret_cast<uint16_t *>(order_dyn);
     __shared__ int wsum[32];
-    __shared__ unsigned red[64];
+    __shared__ unsigned red[96];
     const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
-    int L[kOrderPerThread], lo[kOrderPerThread], hi[kOrderPerThread];
+    int L[kOrderPerThread];
+    // first index row of each of this thread's tiles and how many rows it holds
+    int64_t r0[kOrderPerThread];
+    int nr[kOrderPerThread];
 #pragma unroll
     for (int k = 0; k < kOrderPerThread; ++k) {
         const int tile = k * 1024 + t;
-        lo[k] = hi[k] = 0;
+        r0[k] = 0;
+        nr[k] = 0;
         if (tile < p.n_tiles) {
             const int64_t bh = tile / p.tiles_per_bh;
             const int qt = tile % p.tiles_per_bh;
             const int i0 = o.BS == 128 ? qt : 2 * qt;
-            const int nrows = o.BS == 128 || i0 + 1 >= p.nQB ? 1 : 2;
-            lo[k] = __ldg(p.row_ptr + bh * p.nQB + i0);
-            hi[k] = __ldg(p.row_ptr + bh * p.nQB + i0 + nrows);
+            r0[k] = bh * p.nQB + i0;
+            nr[k] = o.BS == 128 || i0 + 1 >= p.nQB ? 1 : 2;
         }
     }
-    unsigned sum = 0u, mx = 0u;
+    {
+        // a tile's Q blocks are consecutive index rows: its length is one row_ptr difference
+        int lo[kOrderPerThread], hi[kOrderPerThread];
+#pragma unroll
+        for (int k = 0; k < kOrderPerThread; ++k) {
+            lo[k] = nr[k] ? __ldg(p.row_ptr + r0[k]) : 0;
+            hi[k] = nr[k] ? __ldg(p.row_ptr + r0[k] + nr[k]) : 0;
+        }
+#pragma unroll
+        for (int k = 0; k < kOrderPerThread; ++k) L[k] = hi[k] - lo[k];
+    }
+    unsigned sum = 0u, mx = 0u, mnc = 0u;  // mnc: ~(shortest length)
 #pragma unroll
     for (int k = 0; k < kOrderPerThread; ++k) {
-        L[k] = hi[k] - lo[k];
         sum += static_cast<unsigned>(L[k]);
         mx = max(mx, static_cast<unsigned>(L[k]));
+        if (nr[k]) mnc = max(mnc, ~static_cast<unsigned>(L[k]));
     }
     sum = __reduce_add_sync(0xffffffffu, sum);
     mx = __reduce_max_sync(0xffffffffu, mx);
+    mnc = __reduce_max_sync(0xffffffffu, mnc);
     if (lane == 0) {
         red[warp] = sum;
         red[32 + warp] = mx;
+        red[64 + warp] = mnc;
     }
     for (int b = t; b < kBuckets; b += 1024) hist[b] = 0;
     __syncthreads();
     const unsigned total = __reduce_add_sync(0xffffffffu, red[lane]);
     const unsigned max_len = __reduce_max_sync(0xffffffffu, red[32 + lane]);
+    const unsigned min_len = ~__reduce_max_sync(0xffffffffu, red[64 + lane]);
     unsigned share = (total + o.grid - 1) / o.grid;
     if (share < kMinChunkSteps) share = kMinChunkSteps;
     const int T = static_cast<int>(share < 0x7fffffffu ? share : 0x7fffffffu);
     const bool can_split = p.split_ok && o.budget > 0 && !(p.dbg & kDbgNoSplit) &&
                            ((p.dbg & kDbgSplitAll) || splits(static_cast<int>(max_len), T));
+    int n_items;
+    if (!can_split && min_len == max_len) {
+        // every tile has the same length (any top-k mask): the stable longest-first
+        // order is tile order
+        for (int i = t; i < p.n_tiles; i += 1024) o.items[i] = i;
+        n_items = p.n_tiles;
+    } else {
     int n[kOrderPerThread];
 #pragma unroll
     for (int k = 0; k < kOrderPerThread; ++k) n[k] = 1;
@@ -1585,21 +1781,22 @@ __global__ void __launch_bounds__(1024) tile_order_small_kernel(TcParams p, Orde
         const bool valid = k * 1024 + t < p.n_tiles;
         (void)reserve_slots(hist, length_bucket((L[k] + n[k] - 1) / n[k]), valid ? n[k] : 0);
     }
+    clear_order_table(ocnt);
     __syncthreads();
-    int n_items;
     const int excl = block_scan_excl(hist[t], n_items, wsum);
     hist[t] = excl;
     __syncthreads();
 #pragma unroll
     for (int k = 0; k < kOrderPerThread; ++k) {
-        if (k * 1024 + (t & ~31) >= p.n_tiles) continue;  // no tile in this warp (warp-uniform)
+        if (k * 1024 >= p.n_tiles) break;  // no tile in this chunk (block-uniform)
         const int tile = k * 1024 + t;
         const bool valid = tile < p.n_tiles;
-        const int pos = reserve_slots(hist, length_bucket((L[k] + n[k] - 1) / n[k]), valid ? n[k] : 0);
+        const int pos = place_ordered(hist, length_bucket((L[k] + n[k] - 1) / n[k]), valid ? n[k] : 0, ocnt);
         if (valid)
             for (int c = 0; c < n[k]; ++c)
                 o.items[pos + c] = tile | (c << kItemTileBits) | ((n[k] - 1) << (kItemTileBits + 3));
     }
+    }  // lengths differ or tiles split
     if (t == 0) {
         o.hdr->n_items = static_cast<uint32_t>(n_items);
         o.hdr->chunk_steps = static_cast<uint32_t>(T);
@@ -1721,10 +1918,19 @@ bsa_status launch_tc(const FwdArgs &a, cudaStream_t st)
     const int64_t max_items = static_cast<int64_t>(p.n_tiles) + static_cast<int64_t>(lay.budget);
     const int grid = static_cast<int>(max_items < grid_cap ? max_items : grid_cap);
     o.grid = grid;
+    static bool order_smem_set = false;
+    if (!order_smem_set) {
+        if (cudaFuncSetAttribute(tile_order_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(kOrderTableBytes)) != cudaSuccess ||
+            cudaFuncSetAttribute(tile_order_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(kOrderTableBytes)) != cudaSuccess)
+            return BSA_ERR_CUDA;
+        order_smem_set = true;
+    }
     if (p.index_mode == 0 && p.n_tiles <= 1024 * kOrderPerThread)
-        tile_order_small_kernel<<<1, 1024, 0, st>>>(p, o);
+        tile_order_small_kernel<<<1, 1024, kOrderTableBytes, st>>>(p, o);
     else
-        tile_order_kernel<<<(p.n_tiles + 1023) / 1024, 1024, 0, st>>>(p, o);
+        tile_order_kernel<<<(p.n_tiles + 1023) / 1024, 1024, kOrderTableBytes, st>>>(p, o);
     // programmatic dependent launch: the forward's CTAs set up barriers and TMEM while the
     // work-list launch runs, and wait for its results in-kernel
     cudaLaunchConfig_t cfg{};

@@ -21,7 +21,8 @@ struct WsHeader {
     unsigned long long total_steps;  // forward: sum of the tiles' KV steps (tile order, then cleared)
     uint32_t chunk_steps;  // forward: the per-CTA share of steps (chunk length of split tiles)
     uint32_t max_len;      // forward: longest tile (tile order, then cleared)
-    uint32_t pad[56];
+    uint32_t min_len_c;    // forward: ~(shortest tile) (tile order, then cleared)
+    uint32_t pad[55];
 };
 static_assert(sizeof(WsHeader) == 256, "workspace header size");
 static_assert(sizeof(WsHeader) == 256, "workspace header is 256 bytes");

@@ -3,9 +3,11 @@
 // Dynamic mode is the naive block-sparse selector of "Can sparse attention close
 // the quality gap in diffusion transformers" (mean-pooled block scoring):
 //   pool_kernel        Q, K [BH][N][d] -> Qbar, Kbar fp32 [BH][nB][d]   (HBM-bound)
-//   score_topk_kernel  per Q block: nKB scores (fmaf chains), exact top-k by a
-//                      bitwise radix select on order-preserving keys, emits the
-//                      bitmap row and the CSR row (row_ptr = r * k, no scan).
+//   score_kernel       every (Q block, KV block) score (fmaf chains, outer-product
+//                      tiling) as an order-preserving key in the workspace
+//   select_kernel      per Q block: exact top-k by a bitwise radix select on the
+//                      keys held in registers, emits the bitmap row and the CSR
+//                      row (row_ptr = r * k, no scan).
 // Static mode evaluates the block predicates of "多模态DiT中的块稀疏注意力" §3.1-§3.2
 // (text dense + image band + anchors, or video cuboids + faces + text) or copies
 // an explicit bitmap:
@@ -171,12 +173,22 @@ __device__ __forceinline__ int64_t row_base(int64_t bh, int i, int nQB, int n_te
     return bh * per_head + within;
 }
 
-// Scores of 16 Q blocks against every KV block of one (b, h), then top-k per row.
-// Thread (warp w, lane l) computes rows 2w, 2w+1 against KV blocks l + 32n of a
-// 128-block tile staged in shared memory, 4 channels per 128-bit load; each
-// score is still one fmaf chain over channels 0..d-1 in order.
-constexpr int kScoreRows = 16;
-constexpr int kScoreTile = 128;
+// Scores of every (Q block, KV block) pair of a head, then top-k per Q block, in two
+// launches:
+//   score_kernel   an outer-product tiling over channels (the SGEMM pattern): a CTA
+//                  stages a 64-row Qbar tile and a 128-row Kbar tile transposed in
+//                  shared memory ([channel][block]) and each thread accumulates a
+//                  4 x 8 block of scores, so every staged value feeds 8 or 4 FMAs and
+//                  a head's Kbar is read nQB/64 times, not once per Q block. Each score
+//                  is still one fmaf chain over channels 0..d-1 in order from +0. The
+//                  scores go to the workspace as order-preserving keys [BH][nQB][nKB].
+//   select_kernel  one warp per Q block: the row's keys in registers (key j in lane
+//                  j%32, slot j/32), an exact bitwise radix select of the k-th largest
+//                  key, and the bitmap and ascending CSR row.
+constexpr int kScoreTileQ = 64;
+constexpr int kScoreTileK = 128;
+constexpr int kScoreThreads = 256;
+constexpr int kSelectWarps = 8;
 
 // Per-modality counts ("多模态DiT中的块稀疏注意力" §3.3): k[a][b] blocks kept among the
 // key blocks of modality b (0 text, 1 image) by a query block of modality a; the
@@ -186,99 +198,302 @@ struct RegionK {
     int k[2][2];
 };
 
-__global__ void __launch_bounds__(256) score_topk_kernel(const float *__restrict__ qbar,
-                                                         const float *__restrict__ kbar, int nQB,
-                                                         int nKB, int d, RegionK rk, int W,
-                                                         int32_t *__restrict__ row_ptr,
-                                                         int32_t *__restrict__ col_idx,
-                                                         uint32_t *__restrict__ bitmap, uint32_t *err)
+// Keys of a row outside columns [lo, hi) replaced by 0, which is below every radix
+// candidate (a valid key is never 0: that would be the NaN 0xffffffff).
+template <int R, int KPL>
+__device__ __forceinline__ void keys_in_range(const uint32_t (&kv)[R][KPL], int lo, int hi, int lane,
+                                              uint32_t (&x)[R][KPL])
+{
+#pragma unroll
+    for (int q = 0; q < R; ++q)
+#pragma unroll
+        for (int m = 0; m < KPL; ++m) {
+            const int j = 32 * m + lane;
+            x[q][m] = j >= lo && j < hi ? kv[q][m] : 0u;
+        }
+}
+
+// The k-th largest key of R rows at once (the radix searches are independent, so
+// their instructions interleave), and how many keys equal to it each row keeps (the
+// lowest columns first). Slots outside the group hold 0. k <= 0 keeps nothing.
+template <int R, int KPL>
+__device__ __forceinline__ void kth_rows(const uint32_t (&x)[R][KPL], const int (&k)[R], uint32_t (&T)[R],
+                                         int (&need)[R])
+{
+#pragma unroll
+    for (int q = 0; q < R; ++q) T[q] = 0;
+    for (int bit = 31; bit >= 0; --bit) {
+        int n[R];
+#pragma unroll
+        for (int q = 0; q < R; ++q) {
+            const uint32_t c = T[q] | (1u << bit);
+            n[q] = 0;
+#pragma unroll
+            for (int m = 0; m < KPL; ++m) n[q] += x[q][m] >= c ? 1 : 0;
+        }
+#pragma unroll
+        for (int q = 0; q < R; ++q)
+            if (static_cast<int>(__reduce_add_sync(0xffffffffu, n[q])) >= k[q]) T[q] |= 1u << bit;
+    }
+#pragma unroll
+    for (int q = 0; q < R; ++q) {
+        int g = 0;
+#pragma unroll
+        for (int m = 0; m < KPL; ++m) g += x[q][m] > T[q] ? 1 : 0;
+        need[q] = k[q] - static_cast<int>(__reduce_add_sync(0xffffffffu, g));
+        if (k[q] <= 0) {
+            T[q] = 0xffffffffu;
+            need[q] = 0;
+        }
+    }
+}
+
+// The k-th largest key of one row (slots outside the group hold 0) by the same
+// bitwise search, narrowed as it goes: it keeps the bounds T (at least k keys are
+// >= T) and U (fewer than k keys are >= U); once at most 32 keys lie in [T, U) they
+// are gathered into one register per lane (through buf, 32 words of this warp's
+// shared memory) and the remaining bits test that register only. Returns T and how
+// many keys equal to it to keep (the lowest columns first). k <= 0 keeps nothing.
+template <int KPL>
+__device__ __forceinline__ void kth_narrowing(const uint32_t (&x)[KPL], int k, int lane, uint32_t *buf,
+                                              uint32_t &T, int &need)
+{
+    if (k <= 0) {
+        T = 0xffffffffu;
+        need = 0;
+        return;
+    }
+    T = 0;
+    uint64_t U = 1ull << 32;  // exclusive upper bound
+    int cT = 32 * KPL, cU = 0;  // keys >= T (all slots, zeros included), keys >= U
+    int bit = 31;
+    for (; bit >= 0; --bit) {
+        if (cT - cU <= 32) break;
+        const uint32_t c = T | (1u << bit);
+        int n = 0;
+#pragma unroll
+        for (int m = 0; m < KPL; ++m) n += x[m] >= c ? 1 : 0;
+        n = static_cast<int>(__reduce_add_sync(0xffffffffu, n));
+        if (n >= k) {
+            T = c;
+            cT = n;
+        } else {
+            U = c;
+            cU = n;
+        }
+    }
+    if (bit < 0) {  // every bit decided on the full row
+        int g = 0;
+#pragma unroll
+        for (int m = 0; m < KPL; ++m) g += x[m] > T ? 1 : 0;
+        need = k - static_cast<int>(__reduce_add_sync(0xffffffffu, g));
+        return;
+    }
+    // gather the keys of [T, U) (at most 32) into buf, one per lane
+    int off = 0;
+#pragma unroll
+    for (int m = 0; m < KPL; ++m) {
+        const bool in = x[m] >= T && static_cast<uint64_t>(x[m]) < U;
+        const uint32_t b = __ballot_sync(0xffffffffu, in);
+        if (in) buf[off + __popc(b & lanemask_lt())] = x[m];
+        off += __popc(b);
+    }
+    __syncwarp();
+    const uint32_t y = lane < off ? buf[lane] : 0u;  // 0 is below every remaining candidate
+    __syncwarp();
+    for (; bit >= 0; --bit) {
+        const uint32_t c = T | (1u << bit);
+        // keys >= c: the cU keys at or above U plus the gathered ones
+        const int n = cU + static_cast<int>(__reduce_add_sync(0xffffffffu, y >= c ? 1u : 0u));
+        if (n >= k) T = c;
+    }
+    need = k - cU - static_cast<int>(__reduce_add_sync(0xffffffffu, y > T ? 1u : 0u));
+}
+
+// Bitmap words and ascending col_idx of one row from its thresholds: text columns
+// [0, n_text) keep keys above TA plus the first needA equal to it, image columns keep
+// keys above TB plus the first needB equal to it (ties: lower column first).
+template <int KPL>
+__device__ __forceinline__ void emit_row_regs(const uint32_t (&kv)[KPL], int nKB, int n_text, uint32_t TA, int needA,
+                                              uint32_t TB, int needB, int W, int64_t r_global, int64_t out_base,
+                                              int32_t *__restrict__ col_idx, uint32_t *__restrict__ bitmap, int lane)
+{
+    int taken = 0, tiesA = 0, tiesB = 0;
+#pragma unroll
+    for (int m = 0; m < KPL; ++m) {
+        if (m >= W) break;
+        const int j = 32 * m + lane;
+        const bool valid = j < nKB;
+        const bool inA = j < n_text;
+        const uint32_t T = inA ? TA : TB;
+        const bool is_gt = valid && kv[m] > T;
+        const bool is_eq = valid && kv[m] == T;
+        const uint32_t eqA = __ballot_sync(0xffffffffu, is_eq && inA);
+        const uint32_t eqB = __ballot_sync(0xffffffffu, is_eq && !inA);
+        const int eq_rank = inA ? tiesA + __popc(eqA & lanemask_lt()) : tiesB + __popc(eqB & lanemask_lt());
+        const bool sel = is_gt || (is_eq && eq_rank < (inA ? needA : needB));
+        const uint32_t sel_mask = __ballot_sync(0xffffffffu, sel);
+        if (lane == 0) bitmap[r_global * W + m] = sel_mask;
+        if (sel) col_idx[out_base + taken + __popc(sel_mask & lanemask_lt())] = j;
+        taken += __popc(sel_mask);
+        tiesA += __popc(eqA);
+        tiesB += __popc(eqB);
+    }
+}
+
+// Shared memory of score_kernel: one 32-channel chunk of Qbar^T [32][64] and of
+// Kbar^T [32][128] (24 KB, so several CTAs share an SM and hide each other's staging).
+constexpr int kScoreChunk = 32;
+size_t score_smem(int) { return sizeof(float) * static_cast<size_t>(kScoreChunk) * (kScoreTileQ + kScoreTileK); }
+
+// Stages channels [c0, c0 + 32) of rows [row0, row0 + ROWS) of one head's pooled
+// blocks transposed into dst[32][ROWS] (absent rows past n as zeros). Consecutive
+// threads take consecutive rows of one channel quad, so a warp's shared-memory stores
+// are contiguous.
+template <int ROWS>
+__device__ __forceinline__ void stage_chunk(const float *__restrict__ src, int row0, int n, int d, int c0,
+                                            float *__restrict__ dst)
+{
+    constexpr int Q4 = kScoreChunk / 4;  // channel quads per chunk
+    constexpr int PER = ROWS * Q4 / kScoreThreads;
+    static_assert(ROWS * Q4 % kScoreThreads == 0, "whole loads per thread");
+    const int d4 = d / 4;
+    const float4 *s4 = reinterpret_cast<const float4 *>(src);
+    float4 v[PER];
+#pragma unroll
+    for (int u = 0; u < PER; ++u) {
+        const int e = u * kScoreThreads + threadIdx.x;
+        const int r = e % ROWS, q = e / ROWS;
+        v[u] = row0 + r < n ? __ldg(s4 + static_cast<int64_t>(row0 + r) * d4 + c0 / 4 + q)
+                            : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int u = 0; u < PER; ++u) {
+        const int e = u * kScoreThreads + threadIdx.x;
+        const int r = e % ROWS, q = e / ROWS;
+        dst[(4 * q + 0) * ROWS + r] = v[u].x;
+        dst[(4 * q + 1) * ROWS + r] = v[u].y;
+        dst[(4 * q + 2) * ROWS + r] = v[u].z;
+        dst[(4 * q + 3) * ROWS + r] = v[u].w;
+    }
+}
+
+// grid (BH, nQB tiles, nKB tiles). Thread (warp w, lane l): rows 4(4(w%4) + l%4) .. +3
+// of the Q tile, columns 8(8(w/4) + l/4) .. +7 of the K tile; per channel a warp reads
+// 64 bytes of Qbar and 256 of Kbar (three shared-memory wavefronts) for 32 FMAs per
+// thread. Channels arrive 32 at a time; the accumulators carry each score's fmaf chain
+// on from chunk to chunk, so the order over channels is unchanged.
+__global__ void __launch_bounds__(kScoreThreads) score_kernel(const float *__restrict__ qbar,
+                                                             const float *__restrict__ kbar, int nQB, int nKB,
+                                                             int d, uint32_t *__restrict__ keys, uint32_t *err)
 {
     extern __shared__ float4 sm4[];
-    const int dp = d + 4;                      // padded row stride (floats): conflict-free 128-bit loads
-    float *qs = reinterpret_cast<float *>(sm4);        // [16][dp]
-    float *ks = qs + kScoreRows * dp;                   // [128][dp]
-    uint32_t *keys = reinterpret_cast<uint32_t *>(ks + kScoreTile * dp);  // [16][nKB]
-    const int bh = blockIdx.y;
-    const int i0 = blockIdx.x * kScoreRows;
+    float *qT = reinterpret_cast<float *>(sm4);          // [32][64]
+    float *kT = qT + kScoreChunk * kScoreTileQ;          // [32][128]
+    const int64_t bh = blockIdx.x;
+    const int i0 = blockIdx.y * kScoreTileQ, j0 = blockIdx.z * kScoreTileK;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int d4 = d / 4;
-
-    for (int e = threadIdx.x; e < kScoreRows * d4; e += blockDim.x) {
-        const int r = e / d4, c4 = e % d4;
-        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (i0 + r < nQB) v = reinterpret_cast<const float4 *>(qbar + (static_cast<int64_t>(bh) * nQB + i0 + r) * d)[c4];
-        reinterpret_cast<float4 *>(qs + r * dp)[c4] = v;
+    const float *qsrc = qbar + bh * nQB * static_cast<int64_t>(d);
+    const float *ksrc = kbar + bh * nKB * static_cast<int64_t>(d);
+    const int rg = 4 * (warp & 3) + (lane & 3);    // rows 4rg .. 4rg + 3
+    const int cg = 8 * (warp >> 2) + (lane >> 2);  // columns 8cg .. 8cg + 7 (cg < 16)
+    float acc[4][8];
+#pragma unroll
+    for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int n = 0; n < 8; ++n) acc[a][n] = 0.0f;
+    for (int c0 = 0; c0 < d; c0 += kScoreChunk) {
+        if (c0 > 0) __syncthreads();  // the previous chunk is consumed
+        stage_chunk<kScoreTileQ>(qsrc, i0, nQB, d, c0, qT);
+        stage_chunk<kScoreTileK>(ksrc, j0, nKB, d, c0, kT);
+        __syncthreads();
+#pragma unroll 4
+        for (int c = 0; c < kScoreChunk; ++c) {
+            const float4 q = *reinterpret_cast<const float4 *>(qT + c * kScoreTileQ + 4 * rg);
+            const float4 k0 = *reinterpret_cast<const float4 *>(kT + c * kScoreTileK + 8 * cg);
+            const float4 k1 = *reinterpret_cast<const float4 *>(kT + c * kScoreTileK + 8 * cg + 4);
+            const float qa[4] = {q.x, q.y, q.z, q.w};
+            const float ka[8] = {k0.x, k0.y, k0.z, k0.w, k1.x, k1.y, k1.z, k1.w};
+#pragma unroll
+            for (int a = 0; a < 4; ++a)
+#pragma unroll
+                for (int n = 0; n < 8; ++n) acc[a][n] = __fmaf_rn(qa[a], ka[n], acc[a][n]);
+        }
     }
     bool nan_seen = false;
-    const int r0 = 2 * warp;
-    for (int j0 = 0; j0 < nKB; j0 += kScoreTile) {
-        __syncthreads();
-        // stage the tile: all of a thread's 128-bit loads in flight before any store
-        const float4 *src = reinterpret_cast<const float4 *>(kbar + (static_cast<int64_t>(bh) * nKB + j0) * d);
-        const int n4 = min(kScoreTile, nKB - j0) * d4;
-        for (int e0 = 0; e0 < kScoreTile * d4; e0 += 8 * 256) {
-            float4 v[8];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const int e = e0 + u * 256 + threadIdx.x;
-                v[u] = e < n4 ? __ldg(src + e) : make_float4(0.f, 0.f, 0.f, 0.f);
-            }
+    for (int a = 0; a < 4; ++a) {
+        const int i = i0 + 4 * rg + a;
+        if (i >= nQB) continue;
+        const int j = j0 + 8 * cg;
+        uint32_t kk[8];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const int e = e0 + u * 256 + threadIdx.x;
-                if (e < kScoreTile * d4) reinterpret_cast<float4 *>(ks + (e / d4) * dp)[e % d4] = v[u];
-            }
+        for (int n = 0; n < 8; ++n) {
+            nan_seen |= j + n < nKB && isnan(acc[a][n]);
+            kk[n] = order_key(acc[a][n]);
         }
-        __syncthreads();
-        float acc[2][4];
+        uint32_t *row = keys + (bh * nQB + i) * static_cast<int64_t>(nKB);
+        if (j + 7 < nKB && (nKB & 3) == 0) {
+            reinterpret_cast<uint4 *>(row + j)[0] = make_uint4(kk[0], kk[1], kk[2], kk[3]);
+            reinterpret_cast<uint4 *>(row + j)[1] = make_uint4(kk[4], kk[5], kk[6], kk[7]);
+        } else {
 #pragma unroll
-        for (int a = 0; a < 2; ++a)
-#pragma unroll
-            for (int n = 0; n < 4; ++n) acc[a][n] = 0.0f;
-        for (int c4 = 0; c4 < d4; ++c4) {
-            const float4 qa = reinterpret_cast<const float4 *>(qs + r0 * dp)[c4];
-            const float4 qb = reinterpret_cast<const float4 *>(qs + (r0 + 1) * dp)[c4];
-#pragma unroll
-            for (int n = 0; n < 4; ++n) {
-                const float4 kv = reinterpret_cast<const float4 *>(ks + (lane + 32 * n) * dp)[c4];
-                acc[0][n] = __fmaf_rn(qa.x, kv.x, acc[0][n]);
-                acc[0][n] = __fmaf_rn(qa.y, kv.y, acc[0][n]);
-                acc[0][n] = __fmaf_rn(qa.z, kv.z, acc[0][n]);
-                acc[0][n] = __fmaf_rn(qa.w, kv.w, acc[0][n]);
-                acc[1][n] = __fmaf_rn(qb.x, kv.x, acc[1][n]);
-                acc[1][n] = __fmaf_rn(qb.y, kv.y, acc[1][n]);
-                acc[1][n] = __fmaf_rn(qb.z, kv.z, acc[1][n]);
-                acc[1][n] = __fmaf_rn(qb.w, kv.w, acc[1][n]);
-            }
+            for (int n = 0; n < 8; ++n)
+                if (j + n < nKB) row[j + n] = kk[n];
         }
-#pragma unroll
-        for (int a = 0; a < 2; ++a)
-#pragma unroll
-            for (int n = 0; n < 4; ++n) {
-                const int j = j0 + lane + 32 * n;
-                if (i0 + r0 + a < nQB && j < nKB) {
-                    nan_seen |= isnan(acc[a][n]);
-                    keys[(r0 + a) * nKB + j] = order_key(acc[a][n]);
-                }
-            }
     }
     if (nan_seen) raise_error(err, BSA_ERR_NONFINITE);
-    __syncthreads();
-    const int Kt = rk.k[0][0] + rk.k[0][1], Ki = rk.k[1][0] + rk.k[1][1];
-    for (int a = 0; a < 2; ++a) {
-        const int i = i0 + r0 + a;
-        if (i >= nQB) break;
-        const int64_t r_global = static_cast<int64_t>(bh) * nQB + i;
-        const int qm = i < rk.n_text ? 0 : 1;
-        const int64_t base = row_base(bh, i, nQB, rk.n_text, Kt, Ki);
-        select_row(keys + (r0 + a) * nKB, nKB, rk.n_text, rk.k[qm][0], rk.k[qm][1], W, r_global, base, col_idx,
-                   bitmap, lane);
-        if (lane == 0) {
-            row_ptr[r_global] = static_cast<int32_t>(base);
-            if (r_global == static_cast<int64_t>(gridDim.y) * nQB - 1)
-                row_ptr[r_global + 1] = static_cast<int32_t>(row_base(bh + 1, 0, nQB, rk.n_text, Kt, Ki));
-        }
+}
+
+// One warp per Q block row r (of BH * nQB): top-k of the row's keys, bitmap and CSR.
+template <int KPL>
+__global__ void __launch_bounds__(32 * kSelectWarps) select_kernel(const uint32_t *__restrict__ keys, int64_t R,
+                                                                   int nQB, int nKB, RegionK rk, int W,
+                                                                   int32_t *__restrict__ row_ptr,
+                                                                   int32_t *__restrict__ col_idx,
+                                                                   uint32_t *__restrict__ bitmap)
+{
+    const int lane = threadIdx.x & 31;
+    const int64_t r = static_cast<int64_t>(blockIdx.x) * kSelectWarps + (threadIdx.x >> 5);
+    if (r >= R) return;
+    const int64_t bh = r / nQB;
+    const int i = static_cast<int>(r % nQB);
+    const uint32_t *row = keys + r * nKB;
+    uint32_t kv[1][KPL];
+#pragma unroll
+    for (int m = 0; m < KPL; ++m) {
+        const int j = 32 * m + lane;
+        kv[0][m] = j < nKB ? __ldg(row + j) : 0u;
     }
+    __shared__ uint32_t gather[kSelectWarps][32];
+    uint32_t *buf = gather[threadIdx.x >> 5];
+    const int qm = i < rk.n_text ? 0 : 1;
+    uint32_t TA = 0xffffffffu, TB;
+    int nA = 0, nB;
+    if (rk.n_text == 0) {  // the plain selector: every column is in the image group
+        kth_narrowing<KPL>(kv[0], rk.k[qm][1], lane, buf, TB, nB);
+    } else {
+        uint32_t x[1][KPL];
+        keys_in_range<1, KPL>(kv, 0, rk.n_text, lane, x);
+        kth_narrowing<KPL>(x[0], rk.k[qm][0], lane, buf, TA, nA);
+        keys_in_range<1, KPL>(kv, rk.n_text, nKB, lane, x);
+        kth_narrowing<KPL>(x[0], rk.k[qm][1], lane, buf, TB, nB);
+    }
+    const int Kt = rk.k[0][0] + rk.k[0][1], Ki = rk.k[1][0] + rk.k[1][1];
+    const int64_t base = row_base(bh, i, nQB, rk.n_text, Kt, Ki);
+    emit_row_regs<KPL>(kv[0], nKB, rk.n_text, TA, nA, TB, nB, W, r, base, col_idx, bitmap, lane);
+    if (lane == 0) {
+        row_ptr[r] = static_cast<int32_t>(base);
+        if (r == R - 1) row_ptr[R] = static_cast<int32_t>(row_base(bh + 1, 0, nQB, rk.n_text, Kt, Ki));
+    }
+}
+
+template <int KPL>
+bsa_status launch_select(const uint32_t *keys, const MaskArgs &a, const RegionK &rk, int64_t R, cudaStream_t st)
+{
+    select_kernel<KPL><<<static_cast<unsigned>((R + kSelectWarps - 1) / kSelectWarps), 32 * kSelectWarps, 0, st>>>(
+        keys, R, a.nQB, a.nKB, rk, a.W, a.row_ptr, a.col_idx, a.bitmap);
+    return BSA_OK;
 }
 
 // ------------------------------------------------------------ static masks
@@ -543,7 +758,7 @@ __global__ void __launch_bounds__(256) validate_kernel(const int32_t *__restrict
 // path uses per-row counts (per-head bitmaps) and one head's pattern
 // (row offsets, bitmap words).
 struct MaskWs {
-    size_t qbar, kbar;                          // dynamic
+    size_t qbar, kbar, keys;                    // dynamic
     size_t counts, pat_rp, pat_bm;              // static
     size_t dyn_end, static_end;                 // bytes a dynamic / static build touches
     size_t total;
@@ -557,7 +772,8 @@ MaskWs mask_ws_layout(int B, int H, int N, int d, int block)
     MaskWs l{};
     l.qbar = kWsHeader;
     l.kbar = l.qbar + align_up(BH * nB * d * sizeof(float), 256);
-    const size_t dyn_end = l.kbar + align_up(BH * nB * d * sizeof(float), 256);
+    l.keys = l.kbar + align_up(BH * nB * d * sizeof(float), 256);
+    const size_t dyn_end = l.keys + align_up(BH * nB * nB * sizeof(uint32_t), 256);
     l.counts = kWsHeader;
     l.pat_rp = l.counts + align_up(BH * nB * sizeof(int32_t), 256);
     l.pat_bm = l.pat_rp + align_up((nB + 1) * sizeof(int32_t), 256);
@@ -600,18 +816,23 @@ bsa_status launch_build_mask(const MaskArgs &a, cudaStream_t st)
             pool_kernel<float><<<pg, kPoolThreads, 0, st>>>(static_cast<const float *>(a.Q),
                                                             static_cast<const float *>(a.K), qbar, kbar,
                                                             groups, a.N, a.d, a.block, a.nQB);
-        const size_t smem = sizeof(float) * (kScoreRows + kScoreTile) * (a.d + 4) +
-                            sizeof(uint32_t) * kScoreRows * a.nKB;
-        if (cudaFuncSetAttribute(score_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(smem)) != cudaSuccess)
-            return BSA_ERR_CUDA;
-        dim3 sg((a.nQB + kScoreRows - 1) / kScoreRows, static_cast<unsigned>(BH));
         RegionK rk{};
         rk.n_text = a.n_text;
         for (int x = 0; x < 2; ++x)
             for (int y = 0; y < 2; ++y) rk.k[x][y] = a.kq[x][y];
-        score_topk_kernel<<<sg, 256, smem, st>>>(qbar, kbar, a.nQB, a.nKB, a.d, rk, a.W, a.row_ptr, a.col_idx,
-                                                 a.bitmap, err);
+        uint32_t *keys = reinterpret_cast<uint32_t *>(a.ws + l.keys);
+        const size_t smem = score_smem(a.d);
+        if (cudaFuncSetAttribute(score_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
+            cudaSuccess)
+            return BSA_ERR_CUDA;
+        dim3 sg(static_cast<unsigned>(BH), (a.nQB + kScoreTileQ - 1) / kScoreTileQ,
+                (a.nKB + kScoreTileK - 1) / kScoreTileK);
+        score_kernel<<<sg, kScoreThreads, smem, st>>>(qbar, kbar, a.nQB, a.nKB, a.d, keys, err);
+        // keys per lane of the register-held rows: nKB <= 32 * KPL
+        const bsa_status s = a.nKB <= 128   ? launch_select<4>(keys, a, rk, R, st)
+                             : a.nKB <= 512 ? launch_select<16>(keys, a, rk, R, st)
+                                            : launch_select<64>(keys, a, rk, R, st);
+        if (s != BSA_OK) return s;
     } else {
         StaticPred pr{};
         pr.kind = a.spec->kind;

@@ -66,6 +66,18 @@ def test_dynamic_topk_small_all_rows():
     run_workload(wl.scaled(wl.WORKLOADS["dynamic_topk"], H=2, N=2048))
 
 
+@pytest.mark.parametrize("nB", [128, 130, 200, 257])
+def test_selector_score_tiles_all_columns(nB):
+    # the scorer works on 64 x 128 tiles of (Q block, KV block) pairs: every column of a
+    # full tile, a ragged second tile of Q rows and of KV columns, and a row that is not
+    # a multiple of 4 keys (scalar score stores)
+    w = wl.scaled(wl.WORKLOADS["dynamic_topk"], H=1, N=64 * nB, density=0.2)
+    inp = wl.make_inputs(w)
+    q, k = gu.upload(inp, "q"), gu.upload(inp, "k")
+    mask = gu.oracle_mask(w, inp)
+    gu.assert_index_equal(gu.device_index(w, q, k, mask), mask)
+
+
 def test_long_block128_small_all_rows():
     run_workload(wl.scaled(wl.WORKLOADS["long_topk"], H=2, N=4096))
 
@@ -166,6 +178,52 @@ def test_many_tiles_multi_cta_ordering(flags):
         gu.assert_attention_close(O, L, inp, mask, w, rows=rows)
     finally:
         bb.bsa_debug_config(0, 0)
+
+
+def _expected_work_list(w, mask):
+    """Items (unsplit tiles) longest first, equal lengths in tile order; a tile's length is
+    the sum of its Q blocks' active counts, clamped like the kernel's 1024 length buckets."""
+    counts = mask.reshape(w.B * w.H, w.nQB, w.nKB).sum(axis=2)
+    per = 2 if w.block == 64 else 1
+    tiles_per_bh = (w.N + 127) // 128
+    lens = []
+    for bh in range(w.B * w.H):
+        for qt in range(tiles_per_bh):
+            lens.append(int(counts[bh, per * qt:per * qt + per].sum()))
+    lens = np.minimum(np.array(lens), 1023)
+    return np.lexsort((np.arange(lens.size), -lens)).astype(np.int32)
+
+
+ORDER_CASES = {
+    "t2i_csr": wl.scaled(wl.WORKLOADS["t2i_static"], B=1, H=4),
+    "video_csr": wl.scaled(wl.WORKLOADS["video_cuboid"], H=2),
+    "long_bitmap": wl.scaled(wl.WORKLOADS["long_topk"], H=16, N=8192),
+    "t2i_csr_multi_cta": wl.scaled(wl.WORKLOADS["t2i_static"], B=1, H=128, N=64 * 130),
+}
+
+
+@pytest.mark.parametrize("name", sorted(ORDER_CASES))
+def test_work_list_is_longest_first_then_tile_order(name):
+    # row a6: the work list is a stable counting sort (length descending, ties in tile
+    # order), which keeps a head's tiles together; single-CTA (CSR) and multi-CTA
+    # (bitmap, or more than 8192 tiles) ordering launches, no splitting
+    w = ORDER_CASES[name]
+    inp = wl.make_inputs(w)
+    q, k, v = (gu.upload(inp, n) for n in ("q", "k", "v"))
+    mask = gu.oracle_mask(w, inp)
+    idx = gu.device_index(w, q, k, mask)
+    ws = bb.workspace(1, w.B, w.H, w.N, w.d, w.block)
+    bb.bsa_debug_config(bb.DBG_NO_SPLIT, 0)
+    try:
+        bb.forward(q, k, v, idx, index_mode=w.index_mode, ws=ws)
+        torch.cuda.synchronize()
+    finally:
+        bb.bsa_debug_config(0, 0)
+    expect = _expected_work_list(w, mask)
+    n_items = int(ws[12:16].view(torch.int32).item())
+    assert n_items == expect.size
+    items = ws[256:256 + 4 * n_items].view(torch.int32).cpu().numpy()
+    assert np.array_equal(items, expect)
 
 
 # ------------------------------------------------------------ residual compensation

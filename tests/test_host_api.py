@@ -54,7 +54,7 @@ def test_workspace_sizes(lib):
     ws0 = bb.bsa_workspace_size(0, 2, 24, 4224, 64, 64)
     up = lambda x: (x + 255) // 256 * 256  # noqa: E731
     BH, nB, d, W = 48, 66, 64, 3
-    dynamic = 256 + 2 * up(BH * nB * d * 4)                                        # Qbar, Kbar
+    dynamic = 256 + 2 * up(BH * nB * d * 4) + up(BH * nB * nB * 4)                # Qbar, Kbar, score keys
     static = 256 + up(BH * nB * 4) + up((nB + 1) * 4) + up(nB * W * 4)  # counts, pattern
     assert ws0 == max(dynamic, static)
     ws1 = bb.bsa_workspace_size(1, 2, 24, 4224, 64, 64)
