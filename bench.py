@@ -574,12 +574,15 @@ def run_tokens(args):
             "config": {"workload": w.name, "B": w.B, "H": w.H, "N": N, "d": d, "group": C, "tokens_per_group": K,
                        "l2": "flushed (256 MB write) before every timed call"},
             "anchor_step_ms": {"query_groups": round(group_ms, 3), "select_tokens": round(select_ms, 3)},
-            # a CUDA-core kernel: bounded by the fp32 FMA pipe, not the tensor cores
-            "roofline": {"bound": "alu", "achieved": round(tflops, 3), "peak": FP32_FMA_TFLOPS,
-                         "unit": "TFLOP/s", "frac": round(tflops / FP32_FMA_TFLOPS, 4),
-                         "kernel": "fwd_tokens_kernel (CUDA cores: first path)",
-                         "peak_source": "derived: 152 SMs x 128 fp32 FMA lanes x 2 FLOP x 2.07 GHz",
-                         "bf16_tensor_frac": round(tflops / float(peaks["bf16_tflops"]), 4)}}
+            "roofline": ({"bound": "tensor", "achieved": round(tflops, 3), "peak": float(peaks["bf16_tflops"]),
+                          "unit": "TFLOP/s", "frac": round(tflops / float(peaks["bf16_tflops"]), 4),
+                          "kernel": "fwd_tc_kernel in token mode (rows gathered by index)",
+                          "peak_source": f"{peak_kind} bf16_tflops (burst)"} if w.dtype == "bf16" else
+                         # fp32 inputs run on CUDA cores: bounded by the fp32 FMA pipe
+                         {"bound": "alu", "achieved": round(tflops, 3), "peak": FP32_FMA_TFLOPS,
+                          "unit": "TFLOP/s", "frac": round(tflops / FP32_FMA_TFLOPS, 4),
+                          "kernel": "fwd_tokens_kernel (CUDA cores)",
+                          "peak_source": "derived: 152 SMs x 128 fp32 FMA lanes x 2 FLOP x 2.07 GHz"})}
     print(json.dumps(line))
 
 

@@ -448,7 +448,10 @@ bsa_status bsa_forward_tokens(const void *Q, const void *K, const void *V, int d
     a.O = O;
     a.LSE = LSE;
     a.ws = static_cast<char *>(workspace);
-    return bsa::launch_forward_tokens(a, static_cast<cudaStream_t>(stream));
+    a.wait_limit_ns = g_wait_limit_ns;
+    // bf16 on the tensor cores (rows gathered by index); fp32 on CUDA cores
+    return dt == BSA_BF16 ? bsa::launch_forward_tokens_tc(a, static_cast<cudaStream_t>(stream))
+                          : bsa::launch_forward_tokens(a, static_cast<cudaStream_t>(stream));
 }
 
 bsa_status bsa_query_groups(const void *Q, int dt, int B, int H, int N, int d, int32_t *perm, void *workspace,
@@ -479,11 +482,11 @@ bsa_status bsa_select_tokens(const void *Q, const void *K, int dt, int B, int H,
 {
     if (B <= 0 || H <= 0 || N <= 0 || (d != 64 && d != 128) || N % bsa::kTokenGroup != 0) return BSA_ERR_SHAPE;
     if (static_cast<int64_t>(B) * H * N > INT32_MAX || static_cast<int64_t>(B) * H > 65535) return BSA_ERR_SHAPE;
-    // shared memory of the first path: the group's rows, a 32-token chunk and one key per token
-    if (sizeof(float) * (bsa::kTokenGroup * d + 32 * (d + 1)) + sizeof(uint32_t) * static_cast<size_t>(N) >
-        232448)
-        return BSA_ERR_SHAPE;
     if (dt != BSA_BF16 && dt != BSA_FP32) return BSA_ERR_DTYPE;
+    // fp32 runs on CUDA cores with a shared-memory row of N keys per group
+    if (dt == BSA_FP32 &&
+        sizeof(float) * (bsa::kTokenGroup * d + 32 * (d + 1)) + sizeof(uint32_t) * static_cast<size_t>(N) > 232448)
+        return BSA_ERR_SHAPE;
     if (!Q || !K || !perm || !LSE || !tokens) return BSA_ERR_INVALID_ARG;
     if (!aligned(Q, 16) || !aligned(K, 16) || !aligned(perm, 4) || !aligned(LSE, 4) || !aligned(tokens, 4))
         return BSA_ERR_INVALID_ARG;
@@ -506,6 +509,7 @@ bsa_status bsa_select_tokens(const void *Q, const void *K, int dt, int B, int H,
     a.n_keep = n_keep;
     a.tokens = tokens;
     a.ws = static_cast<char *>(workspace);
+    a.wait_limit_ns = g_wait_limit_ns;
     return bsa::launch_select_tokens(a, static_cast<cudaStream_t>(stream));
 }
 

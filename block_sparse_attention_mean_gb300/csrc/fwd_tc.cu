@@ -99,6 +99,11 @@ struct TcParams {
     float *part_o;             // [slot][128][D] unnormalised partial O
     const float *R;            // residual added to O before rounding ([B][H][N][D] fp32), or nullptr
     float4 *part_stats;        // [slot][128] (row max in log2 units, fp32 sum, sum of bf16-rounded P, 0)
+    // token mode (tile = (b, h, query group); steps are 128-token chunks of the group's keys)
+    const int32_t *perm;       // [B*H][N]: group g of a head is rows perm[g*128 .. g*128+127]
+    const int32_t *tokens;     // [B*H][N/128][n_tok]: each group's keys
+    int n_tok;                 // keys per group
+    int groups;                // query groups per head (N / 128)
 };
 
 struct Item {
@@ -201,6 +206,59 @@ __device__ __forceinline__ void tile_coords(const TcParams &p, int tile, int64_t
 {
     bh = tile / p.tiles_per_bh;
     qt = tile % p.tiles_per_bh;
+}
+
+// Global output row (b*H + h)*N + row of tile row `trow`, and whether it exists: the
+// tile's rows in order, or in token mode the group's rows as the permutation lists them
+// (an index outside [0, N) was reported by the Q producer and is not written).
+template <bool TOK>
+__device__ __forceinline__ int64_t out_row(const TcParams &p, int tile, int trow, bool &valid)
+{
+    if constexpr (TOK) {
+        const int64_t bh = tile / p.groups;
+        const int r = __ldg(p.perm + static_cast<int64_t>(tile) * kTileM + trow);
+        valid = r >= 0 && r < p.N;
+        return bh * p.N + (valid ? r : 0);
+    } else {
+        int64_t bh;
+        int qt;
+        tile_coords(p, tile, bh, qt);
+        const int row = qt * kTileM + trow;
+        valid = row < p.N;
+        return bh * p.N + row;
+    }
+}
+
+// Token mode: the global row ((b*H + h)*N + token) of each of this lane's four rows
+// (4*lane .. 4*lane + 3) of a 128-row gather, from idx[0 .. n) (rows past n repeat
+// idx[n - 1]: a valid key whose score the softmax masks). An index outside [0, N) is
+// reported and replaced by 0.
+__device__ __forceinline__ void gather_idx(const int32_t *idx, int n, int lane, int (&v)[4])
+{
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int k = 4 * lane + i;
+        v[i] = __ldg(idx + (k < n ? k : n - 1));
+    }
+}
+__device__ __forceinline__ void gather_rows_of(const TcParams &p, const int (&v)[4], int64_t bh, int (&rows)[4])
+{
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        int x = v[i];
+        if (x < 0 || x >= p.N) {
+            raise_error(p.err, BSA_ERR_INVALID_ARG);
+            x = 0;
+        }
+        rows[i] = static_cast<int>(bh * p.N + x);
+    }
+}
+__device__ __forceinline__ void gather_rows(const TcParams &p, const int32_t *idx, int n, int64_t bh, int lane,
+                                            int (&rows)[4])
+{
+    int v[4];
+    gather_idx(idx, n, lane, v);
+    gather_rows_of(p, v, bh, rows);
 }
 
 template <int BS>
@@ -392,7 +450,7 @@ __device__ __forceinline__ bool last_chunk(const TcParams &p, int base, int nchu
 // block q of the step occupies S columns [q * BS, (q + 1) * BS) and is skipped
 // (P = 0, no effect on the max or the sums) when the step has no block q or the
 // row's Q block does not have it.
-template <int D, int BS, int NSB, int PAIR, class C>
+template <int D, int BS, int NSB, int PAIR, class C, bool TOK>
 __device__ __forceinline__ void softmax_rows(const TcParams &p, uint32_t sbase, uint32_t tmem,
                                              volatile int32_t *tile_ids, const volatile uint32_t *desc,
                                              const Ctl &ctl, int warp, int lane)
@@ -412,12 +470,8 @@ __device__ __forceinline__ void softmax_rows(const TcParams &p, uint32_t sbase, 
         int tile;
         if (!fetch_tile<C>(sbase, tile_ids, ctl, lane, tcount, tile) || tile < 0) return;
         const bool empty = (tile & kEmptyTile) != 0;
-        int64_t bh;
-        int qt;
-        tile_coords(p, decode_item(p, tile & ~kEmptyTile).tile, bh, qt);
-        const int row = qt * kTileM + trow;
-        const bool row_valid = row < p.N;
-        const int64_t grow = bh * p.N + row;
+        bool row_valid;
+        const int64_t grow = out_row<TOK>(p, decode_item(p, tile & ~kEmptyTile).tile, trow, row_valid);
         __nv_bfloat16 *orow = p.O + grow * D;
         if (p.R && row_valid) {  // the epilogue reads this row of the residual: start it towards L2 now
 #pragma unroll
@@ -679,7 +733,7 @@ __device__ __forceinline__ void softmax_rows(const TcParams &p, uint32_t sbase, 
 // group and, in every 8-column group of S and O, columns 2(t%4) and +1; a row's
 // max and sums are reduced over its 4 lanes with two shuffles. A step holds PAIR
 // KV blocks: 8-column group g of the step belongs to block g / (BS / 8).
-template <int D, int BS, int NSB, int PAIR, class C>
+template <int D, int BS, int NSB, int PAIR, class C, bool TOK>
 __device__ __forceinline__ void softmax_quads(const TcParams &p, uint32_t sbase, uint32_t tmem,
                                               volatile int32_t *tile_ids, const volatile uint32_t *desc,
                                               const Ctl &ctl, int warp, int lane)
@@ -701,12 +755,9 @@ __device__ __forceinline__ void softmax_quads(const TcParams &p, uint32_t sbase,
         if (!fetch_tile<C>(sbase, tile_ids, ctl, lane, tcount, tile) || tile < 0) return;
         const bool empty = (tile & kEmptyTile) != 0;
         const Item it = decode_item(p, tile & ~kEmptyTile);
-        int64_t bh;
-        int qt;
-        tile_coords(p, it.tile, bh, qt);
-        const int row_lo = qt * kTileM + r_lo, row_hi = row_lo + 8;
-        const bool lo_valid = row_lo < p.N, hi_valid = row_hi < p.N;
-        const int64_t g_lo = bh * p.N + row_lo, g_hi = g_lo + 8;
+        bool lo_valid, hi_valid;
+        const int64_t g_lo = out_row<TOK>(p, it.tile, r_lo, lo_valid);
+        const int64_t g_hi = out_row<TOK>(p, it.tile, r_lo + 8, hi_valid);
         uint32_t *o_lo = reinterpret_cast<uint32_t *>(p.O + g_lo * D + cpair);
         uint32_t *o_hi = reinterpret_cast<uint32_t *>(p.O + g_hi * D + cpair);
         if (p.R && (lane & 3) < D / 32) {  // the epilogue reads these residual rows: start them towards L2 now
@@ -946,11 +997,12 @@ __device__ __forceinline__ void softmax_quads(const TcParams &p, uint32_t sbase,
     }
 }
 
-template <int D, int BS, int NK, int NV, int NSB, int QS, int SPLIT, int PAIR, int MINB>
+template <int D, int BS, int NK, int NV, int NSB, int QS, int SPLIT, int PAIR, int MINB, bool TOK = false>
 __global__ void __launch_bounds__((4 * SPLIT + 4) * 32, MINB)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const TcParams p)
 {
+    static_assert(!TOK || (BS == kTileM && PAIR == 1), "token mode: 128-key steps");
     using C = Cfg<D, BS, NK, NV, NSB, QS, PAIR>;
     using R = Roles<SPLIT>;
     constexpr int kProducerWarp = R::kProducerWarp, kQkWarp = R::kQkWarp, kMmaWarp = R::kMmaWarp;
@@ -1014,7 +1066,126 @@ __global__ void __launch_bounds__((4 * SPLIT + 4) * 32, MINB)
     const Ctl ctl{reinterpret_cast<volatile uint32_t *>(misc + 1), p.err, p.wait_limit_ns};
     const bool stall = (p.dbg & kDbgStall) != 0u;
 
-    if (warp == kProducerWarp) {
+    if (TOK && warp == kProducerWarp) {
+        // ------------------------------------------------------------ token mode: tiles, Q and K by gather
+        // Every tile (one query group) has the same steps, so CTA b takes tiles b, b + grid,
+        // ... in order. Q rows come through the permutation, K rows through the group's
+        // token list, four rows per gather and every lane issuing its own rows.
+        if constexpr (TOK) {
+            const int steps = (p.n_tok + kTileM - 1) / kTileM;
+            const bool ragged = p.n_tok % kTileM != 0;
+            int G = 0, e = 0, tcount = 0;
+            int last_issue = -1, q_issued = -1;
+            bool ok = true;
+            while (ok) {
+                const int slot = tcount & 1;
+                if (tcount >= 2 && !warp_wait_all(bar(C::B_TEMPTY + slot), ((tcount >> 1) - 1) & 1, ctl)) break;
+                const int id = blockIdx.x + tcount * static_cast<int>(gridDim.x);
+                const int item = id < p.n_tiles ? id : -1;
+                if (lane == 0) {
+                    tile_ids[slot] = item;
+                    mbar_arrive(bar(C::B_TFULL + slot));
+                }
+                ++tcount;
+                if (item < 0) break;
+                if (stall) continue;
+                const int64_t bh = item / p.groups;
+                const int qs = e % QS;
+                if (e >= QS && !warp_wait_all(bar(C::B_QEMPTY + qs), ((e / QS) - 1) & 1, ctl)) break;
+                const int32_t *toks = p.tokens + static_cast<int64_t>(item) * p.n_tok;
+                // the first K step's indices load with the Q rows'; later ones one step ahead
+                int nxt[4];
+                gather_idx(toks, min(kTileM, p.n_tok), lane, nxt);
+                int rows[4];
+                gather_rows(p, p.perm + static_cast<int64_t>(item) * kTileM, kTileM, bh, lane, rows);
+                if (lane == 0) mbar_arrive_expect_tx(bar(C::B_QFULL + qs), C::kQBytes);
+                __syncwarp();
+#pragma unroll
+                for (int c = 0; c < D / 64; ++c)
+                    tma_gather4(sbase + C::Q_OFF + qs * C::kQBytes + c * C::kQChunk + lane * 512, &tmQ, c * 64,
+                                rows[0], rows[1], rows[2], rows[3], bar(C::B_QFULL + qs));
+                __syncwarp();
+                q_issued = e;
+                for (int st = 0; st < steps; ++st) {
+                    const int ks = G % NK;
+                    gather_rows_of(p, nxt, bh, rows);
+                    if (st + 1 < steps)
+                        gather_idx(toks + (st + 1) * kTileM, min(kTileM, p.n_tok - (st + 1) * kTileM), lane, nxt);
+                    if (G >= NK && !warp_wait_all(bar(C::B_KEMPTY + ks), ((G / NK) - 1) & 1, ctl)) {
+                        ok = false;
+                        break;
+                    }
+                    if (lane == 0) {
+                        const uint32_t ms[2] = {3u, 0u};
+                        kdesc[ks] = step_desc(1, ms, st == steps - 1, ragged && st == steps - 1 ? 1u : 0u);
+                        mbar_arrive_expect_tx(bar(C::B_KFULL + ks), static_cast<uint32_t>(kTileM * D * 2));
+                    }
+                    __syncwarp();
+#pragma unroll
+                    for (int c = 0; c < D / 64; ++c)
+                        tma_gather4(sbase + C::K_OFF + ks * C::kKVBytes + c * C::kKVChunk + lane * 512, &tmK,
+                                    c * 64, rows[0], rows[1], rows[2], rows[3], bar(C::B_KFULL + ks));
+                    __syncwarp();
+                    last_issue = G;
+                    ++G;
+                }
+                ++e;
+            }
+            if (lane == 0 && *ctl.abort_flag) {
+                // never leave while our gathers may still land in shared memory
+                for (int g = last_issue - NK + 1; g <= last_issue; ++g)
+                    if (g >= 0) wait_bar_drain(bar(C::B_KFULL + g % NK), (g / NK) & 1, p.wait_limit_ns);
+                for (int e2 = q_issued - (QS - 1) < 0 ? 0 : q_issued - (QS - 1); e2 <= q_issued; ++e2)
+                    wait_bar_drain(bar(C::B_QFULL + e2 % QS), (e2 / QS) & 1, p.wait_limit_ns);
+            }
+            __syncwarp();
+        }
+    } else if (TOK && warp == kVProducerWarp) {
+        // ------------------------------------------------------------ token mode: V by gather
+        if constexpr (TOK) {
+            if (!stall) {
+                const int steps = (p.n_tok + kTileM - 1) / kTileM;
+                int G = 0, tcount = 0;
+                int last_issue = -1;
+                bool ok = true;
+                while (ok) {
+                    int tile;
+                    if (!fetch_tile<C>(sbase, tile_ids, ctl, lane, tcount, tile)) break;
+                    if (tile < 0) break;
+                    const int64_t bh = tile / p.groups;
+                    const int32_t *toks = p.tokens + static_cast<int64_t>(tile) * p.n_tok;
+                    int nxt[4];  // the next step's indices, loaded one step ahead
+                    gather_idx(toks, min(kTileM, p.n_tok), lane, nxt);
+                    for (int st = 0; st < steps; ++st) {
+                        const int vs = G % NV;
+                        int rows[4];
+                        gather_rows_of(p, nxt, bh, rows);
+                        if (st + 1 < steps)
+                            gather_idx(toks + (st + 1) * kTileM, min(kTileM, p.n_tok - (st + 1) * kTileM), lane, nxt);
+                        if (G >= NV && !warp_wait_all(bar(C::B_VEMPTY + vs), ((G / NV) - 1) & 1, ctl)) {
+                            ok = false;
+                            break;
+                        }
+                        if (lane == 0)
+                            mbar_arrive_expect_tx(bar(C::B_VFULL + vs), static_cast<uint32_t>(kTileM * D * 2));
+                        __syncwarp();
+#pragma unroll
+                        for (int c = 0; c < D / 64; ++c)
+                            tma_gather4(sbase + C::V_OFF + vs * C::kKVBytes + c * C::kKVChunk + lane * 512, &tmV,
+                                        c * 64, rows[0], rows[1], rows[2], rows[3], bar(C::B_VFULL + vs));
+                        __syncwarp();
+                        last_issue = G;
+                        ++G;
+                    }
+                }
+                if (lane == 0 && *ctl.abort_flag) {
+                    for (int g = last_issue - NV + 1; g <= last_issue; ++g)
+                        if (g >= 0) wait_bar_drain(bar(C::B_VFULL + g % NV), (g / NV) & 1, p.wait_limit_ns);
+                }
+                __syncwarp();
+            }
+        }
+    } else if (warp == kProducerWarp) {
         // ------------------------------------------------------------ tile scheduler, Q and K producer
         // Whole-warp loop (uniform waits and walk); one elected lane issues the copies.
         // This warp is the walker of the K side: with one step of lookahead it leaves
@@ -1295,9 +1466,9 @@ __global__ void __launch_bounds__((4 * SPLIT + 4) * 32, MINB)
     } else {
         // ------------------------------------------------------------ softmax + epilogue
         if constexpr (SPLIT == 1)
-            softmax_rows<D, BS, NSB, PAIR, C>(p, sbase, tmem, tile_ids, desc, ctl, warp, lane);
+            softmax_rows<D, BS, NSB, PAIR, C, TOK>(p, sbase, tmem, tile_ids, desc, ctl, warp, lane);
         else
-            softmax_quads<D, BS, NSB, PAIR, C>(p, sbase, tmem, tile_ids, desc, ctl, warp, lane);
+            softmax_quads<D, BS, NSB, PAIR, C, TOK>(p, sbase, tmem, tile_ids, desc, ctl, warp, lane);
     }
 
     tc_fence_before();
@@ -1837,15 +2008,17 @@ FwdLayout fwd_layout(int B, int H, int N, int d)
     return l;
 }
 
-template <int D, int BS, int NK, int NV, int NSB, int QS, int SPLIT, int PAIR, int MINB>
-bsa_status launch_tc(const FwdArgs &a, cudaStream_t st)
+// Resident CTAs of a forward instance over the whole GPU (set-up once per instance:
+// shared-memory attributes, then registers, shared memory and TMEM per SM).
+template <int D, int BS, int NK, int NV, int NSB, int QS, int SPLIT, int PAIR, int MINB, bool TOK>
+bsa_status forward_grid_cap(int &cap)
 {
     using C = Cfg<D, BS, NK, NV, NSB, QS, PAIR>;
     constexpr int kThreads = Roles<SPLIT>::kThreads;
     static_assert(MINB * (C::SMEM_ALLOC + 1024) <= 233472, "shared memory for MINB CTAs per SM");
     static_assert(C::SMEM_ALLOC <= 227 * 1024, "shared memory budget");
     static_assert(C::TCOLS_USED <= C::TCOLS, "TMEM budget");
-    auto kern = fwd_tc_kernel<D, BS, NK, NV, NSB, QS, SPLIT, PAIR, MINB>;
+    auto kern = fwd_tc_kernel<D, BS, NK, NV, NSB, QS, SPLIT, PAIR, MINB, TOK>;
     static int grid_cap = 0;
     if (grid_cap == 0) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC) != cudaSuccess)
@@ -1870,8 +2043,22 @@ bsa_status launch_tc(const FwdArgs &a, cudaStream_t st)
         if (per_sm < 1) return BSA_ERR_UNSUPPORTED;
         grid_cap = sms * per_sm;
     }
+    cap = grid_cap;
+    return BSA_OK;
+}
+
+template <int D, int BS, int NK, int NV, int NSB, int QS, int SPLIT, int PAIR, int MINB>
+bsa_status launch_tc(const FwdArgs &a, cudaStream_t st)
+{
+    using C = Cfg<D, BS, NK, NV, NSB, QS, PAIR>;
+    constexpr int kThreads = Roles<SPLIT>::kThreads;
+    auto kern = fwd_tc_kernel<D, BS, NK, NV, NSB, QS, SPLIT, PAIR, MINB, false>;
+    int grid_cap = 0;
+    {
+        const bsa_status s = forward_grid_cap<D, BS, NK, NV, NSB, QS, SPLIT, PAIR, MINB, false>(grid_cap);
+        if (s != BSA_OK) return s;
+    }
     const int64_t BH = static_cast<int64_t>(a.B) * a.H;
-    const uint64_t rows = static_cast<uint64_t>(BH) * a.N;
     CUtensorMap mq, mk, mv;
     if (!make_tma_map_bf16(&mq, a.Q, BH, a.N, D, kTileM) || !make_tma_map_bf16(&mk, a.K, BH, a.N, D, BS) ||
         !make_tma_map_bf16(&mv, a.V, BH, a.N, D, BS))
@@ -1947,7 +2134,57 @@ bsa_status launch_tc(const FwdArgs &a, cudaStream_t st)
     return cudaGetLastError() == cudaSuccess ? BSA_OK : BSA_ERR_CUDA;
 }
 
+// Token-sparse forward ("Can sparse attention close the quality gap in diffusion
+// transformers", section "token 级选择需要瓦片对齐的查询分组"): the block-128 kernel in
+// token mode. A tile is one query group of 128 rows gathered through the permutation;
+// its steps are 128-key chunks of the group's token list, gathered by index (the last
+// chunk's missing keys are masked); outputs go back to the rows the permutation names.
+template <int D, int NK, int NV, int NSB, int QS, int SPLIT, int MINB>
+bsa_status launch_tc_tokens(const TokenArgs &a, cudaStream_t st)
+{
+    using C = Cfg<D, kTileM, NK, NV, NSB, QS, 1>;
+    constexpr int kThreads = Roles<SPLIT>::kThreads;
+    auto kern = fwd_tc_kernel<D, kTileM, NK, NV, NSB, QS, SPLIT, 1, MINB, true>;
+    int grid_cap = 0;
+    {
+        const bsa_status s = forward_grid_cap<D, kTileM, NK, NV, NSB, QS, SPLIT, 1, MINB, true>(grid_cap);
+        if (s != BSA_OK) return s;
+    }
+    const int64_t BH = static_cast<int64_t>(a.B) * a.H;
+    const uint64_t rows = static_cast<uint64_t>(BH) * a.N;
+    CUtensorMap mq, mk, mv;
+    if (!make_tma_map_bf16_rows(&mq, a.Q, rows, D) || !make_tma_map_bf16_rows(&mk, a.K, rows, D) ||
+        !make_tma_map_bf16_rows(&mv, a.V, rows, D))
+        return BSA_ERR_CUDA;
+    TcParams p{};
+    p.N = a.N;
+    p.groups = a.N / kTileM;
+    p.n_tiles = static_cast<int>(BH * p.groups);
+    p.n_tok = a.n_tokens;
+    p.last_rows = a.n_tokens - (a.n_tokens - 1) / kTileM * kTileM;  // keys in the last 128-key step
+    p.ragged_kb = -1;
+    p.perm = a.perm;
+    p.tokens = a.tokens;
+    p.scale_log2 = a.scale * 1.4426950408889634f;
+    p.O = static_cast<__nv_bfloat16 *>(a.O);
+    p.LSE = a.LSE;
+    p.split_ok = 0;
+    p.err = &reinterpret_cast<WsHeader *>(a.ws)->err;
+    p.wait_limit_ns = a.wait_limit_ns;
+    const int grid = p.n_tiles < grid_cap ? p.n_tiles : grid_cap;
+    kern<<<grid, kThreads, C::SMEM_ALLOC, st>>>(mq, mk, mv, p);
+    return cudaGetLastError() == cudaSuccess ? BSA_OK : BSA_ERR_CUDA;
+}
+
 }  // namespace
+
+bsa_status launch_forward_tokens_tc(const TokenArgs &a, cudaStream_t st)
+{
+    // the block-128 instances' stages and layouts: <D, K stages, V stages, S/P buffers, Q slots, threads per row, CTAs per SM>
+    if (a.d == 64) return launch_tc_tokens<64, 5, 6, 3, 2, 2, 1>(a, st);
+    if (a.d == 128) return launch_tc_tokens<128, 2, 4, 3, 1, 2, 1>(a, st);
+    return BSA_ERR_SHAPE;
+}
 
 size_t fwd_workspace_bytes(int B, int H, int N, int d, int block)
 {
@@ -1985,7 +2222,22 @@ static EncodeTiledFn encode_fn()
     return fn;
 }
 
-// 2-D view [rows][d] of a bf16 tensor, 64-column x box_rows boxes, 128-byte swizzle.
+// 2-D view [rows][d] of a bf16 tensor with 64-column x 1-row boxes and 128-byte swizzle:
+// the map of tile::gather4 loads (four rows by index per copy).
+bool make_tma_map_bf16_rows(CUtensorMap *m, const void *base, uint64_t rows, int d)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(d) * 2};
+    const cuuint32_t box[2] = {64u, 1u};
+    const cuuint32_t es[2] = {1u, 1u};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 3-D view [heads][n][d] of a bf16 tensor, 64-column x box_rows boxes, 128-byte swizzle.
 bool make_tma_map_bf16(CUtensorMap *m, const void *base, uint64_t heads, uint64_t n, int d, int box_rows)
 {
     EncodeTiledFn fn = encode_fn();

@@ -128,8 +128,11 @@ struct TokenArgs {
     void *O;
     float *LSE;
     char *ws;               // error word in the first bytes
+    uint64_t wait_limit_ns; // bounded device waits (tensor-core path)
 };
-bsa_status launch_forward_tokens(const TokenArgs &a, cudaStream_t st);
+bsa_status launch_forward_tokens(const TokenArgs &a, cudaStream_t st);     // CUDA cores (fp32 and bf16)
+bsa_status launch_forward_tokens_tc(const TokenArgs &a, cudaStream_t st);  // bf16, tcgen05 with row gathers
+bool make_tma_map_bf16_rows(CUtensorMap *m, const void *base, uint64_t rows, int d);
 
 // token selection: per group of 128 queries, the n_keep tokens of largest exact mass
 struct TokenSelectArgs {
@@ -141,6 +144,7 @@ struct TokenSelectArgs {
     int n_keep;            // tokens per group
     int32_t *tokens;       // [B*H][N/128][n_keep] (written, ascending per group)
     char *ws;
+    uint64_t wait_limit_ns;  // bounded device waits (tensor-core path)
 };
 // workspace: header, masses fp32 [B*H*N/128][N], bitmap words [B*H*N/128][N/32]
 struct TokenSelectWs {
@@ -148,6 +152,8 @@ struct TokenSelectWs {
 };
 TokenSelectWs token_select_ws_layout(int B, int H, int N);
 bsa_status launch_select_tokens(const TokenSelectArgs &a, cudaStream_t st);
+// bf16: the masses of every (group, key) on tcgen05 into mass [B*H*N/128][N]
+bsa_status launch_token_mass_tc(const TokenSelectArgs &a, float *mass, cudaStream_t st);
 
 // query groups: per head, the median-split principal-direction partition into groups of 128
 constexpr int kMaxQueryGroups = 512;  // groups per head (N <= 65536)

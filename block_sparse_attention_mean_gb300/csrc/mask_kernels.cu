@@ -1019,6 +1019,117 @@ static bsa_status launch_token_select(const TokenSelectArgs &a, cudaStream_t st)
     return cudaGetLastError() == cudaSuccess ? BSA_OK : BSA_ERR_CUDA;
 }
 
+// The n_keep tokens of largest mass of one selection row (one group of one head), from
+// the masses in global memory, for any N: an exact radix select with 8-bit digits (four
+// passes, each a shared-memory histogram of the keys that match the digits found so far),
+// then the bitmap words and the ascending token list (keys above the threshold, and the
+// lowest-indexed keys equal to it). Ties go to the lower index, as in select_row.
+constexpr int kTopkThreads = 256;
+constexpr int kTopkWarps = kTopkThreads / 32;
+
+__global__ void __launch_bounds__(kTopkThreads) token_topk_kernel(const float *__restrict__ mass, int N, int n_keep,
+                                                                  uint32_t *__restrict__ bitmap,
+                                                                  int32_t *__restrict__ tokens, uint32_t *err)
+{
+    __shared__ int hist[kTopkWarps][256];
+    __shared__ int total[256];
+    __shared__ int s_digit, s_krem;
+    __shared__ int w_gt[kTopkWarps], w_eq[kTopkWarps];
+    const int64_t rg = blockIdx.x;
+    const float *row = mass + rg * N;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    uint32_t prefix = 0u, pmask = 0u;
+    int krem = n_keep;
+    bool nan_seen = false;
+    for (int pass = 0; pass < 4; ++pass) {
+        const int shift = 24 - 8 * pass;
+        for (int i = threadIdx.x; i < kTopkWarps * 256; i += kTopkThreads) (&hist[0][0])[i] = 0;
+        __syncthreads();
+        for (int t = threadIdx.x; t < N; t += kTopkThreads) {
+            const float m = __ldg(row + t);
+            if (pass == 0) nan_seen |= isnan(m);
+            const uint32_t key = order_key(m);
+            if ((key & pmask) == prefix) atomicAdd(&hist[warp][(key >> shift) & 255u], 1);
+        }
+        __syncthreads();
+        for (int dg = threadIdx.x; dg < 256; dg += kTopkThreads) {
+            int c = 0;
+#pragma unroll
+            for (int w = 0; w < kTopkWarps; ++w) c += hist[w][dg];
+            total[dg] = c;
+        }
+        __syncthreads();
+        if (warp == 0) {
+            // lane l covers digits 255 - 8l down to 248 - 8l: counts above each lane by a scan
+            int cnt[8], sum = 0;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                cnt[i] = total[255 - 8 * lane - i];
+                sum += cnt[i];
+            }
+            int incl = sum;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += y;
+            }
+            const int excl = incl - sum;  // matching keys with a larger digit than this lane's
+            const unsigned who = __ballot_sync(0xffffffffu, excl < krem && krem <= incl);
+            if (lane == __ffs(who) - 1) {
+                int above = excl;
+                for (int i = 0; i < 8; ++i) {
+                    if (above + cnt[i] >= krem) {
+                        s_digit = 255 - 8 * lane - i;
+                        s_krem = krem - above;
+                        break;
+                    }
+                    above += cnt[i];
+                }
+            }
+        }
+        __syncthreads();
+        prefix |= static_cast<uint32_t>(s_digit) << shift;
+        pmask |= 0xFFu << shift;
+        krem = s_krem;
+        __syncthreads();  // every thread has read s_digit / s_krem
+    }
+    if (__syncthreads_or(nan_seen) && threadIdx.x == 0) raise_error(err, BSA_ERR_NONFINITE);
+    // keys above T = prefix, plus the first `krem` keys equal to it; each warp takes a
+    // contiguous range of 32-key words, counted first so that its output offset is known
+    const uint32_t T = prefix;
+    const int need = krem, W = N / 32;
+    const int per = (W + kTopkWarps - 1) / kTopkWarps;
+    const int w0 = warp * per, w1 = min(W, w0 + per);
+    int cgt = 0, ceq = 0;
+    for (int w = w0; w < w1; ++w) {
+        const uint32_t key = order_key(__ldg(row + 32 * w + lane));
+        cgt += __popc(__ballot_sync(0xffffffffu, key > T));
+        ceq += __popc(__ballot_sync(0xffffffffu, key == T));
+    }
+    if (lane == 0) {
+        w_gt[warp] = cgt;
+        w_eq[warp] = ceq;
+    }
+    __syncthreads();
+    int eq_before = 0, out = 0;
+    for (int w = 0; w < warp; ++w) {
+        out += w_gt[w] + max(0, min(w_eq[w], need - eq_before));
+        eq_before += w_eq[w];
+    }
+    const int64_t base = rg * n_keep;
+    for (int w = w0; w < w1; ++w) {
+        const int j = 32 * w + lane;
+        const uint32_t key = order_key(__ldg(row + j));
+        const uint32_t eq = __ballot_sync(0xffffffffu, key == T);
+        const bool sel = key > T || (key == T && eq_before + __popc(eq & lanemask_lt()) < need);
+        const uint32_t sm = __ballot_sync(0xffffffffu, sel);
+        if (lane == 0) bitmap[rg * W + w] = sm;
+        if (sel) tokens[base + out + __popc(sm & lanemask_lt())] = j;
+        out += __popc(sm);
+        eq_before += __popc(eq);
+    }
+}
+
 TokenSelectWs token_select_ws_layout(int B, int H, int N)
 {
     const size_t rows = static_cast<size_t>(B) * H * (N / kTokenGroup);
@@ -1032,8 +1143,16 @@ TokenSelectWs token_select_ws_layout(int B, int H, int N)
 bsa_status launch_select_tokens(const TokenSelectArgs &a, cudaStream_t st)
 {
     if (a.dt == BSA_BF16) {
-        if (a.d == 64) return launch_token_select<__nv_bfloat16, 64>(a, st);
-        if (a.d == 128) return launch_token_select<__nv_bfloat16, 128>(a, st);
+        // masses on tcgen05 into the workspace, then the radix top-k of every group's row
+        const TokenSelectWs l = token_select_ws_layout(a.B, a.H, a.N);
+        float *mass = reinterpret_cast<float *>(a.ws + l.mass);
+        const bsa_status s = launch_token_mass_tc(a, mass, st);
+        if (s != BSA_OK) return s;
+        const int64_t rows = static_cast<int64_t>(a.B) * a.H * (a.N / kTokenGroup);
+        token_topk_kernel<<<static_cast<unsigned>(rows), kTopkThreads, 0, st>>>(
+            mass, a.N, a.n_keep, reinterpret_cast<uint32_t *>(a.ws + l.bitmap), a.tokens,
+            reinterpret_cast<uint32_t *>(a.ws));
+        return cudaGetLastError() == cudaSuccess ? BSA_OK : BSA_ERR_CUDA;
     } else {
         if (a.d == 64) return launch_token_select<float, 64>(a, st);
         if (a.d == 128) return launch_token_select<float, 128>(a, st);

@@ -90,6 +90,20 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
         : "memory");
 }
 
+// 2-D gather of four rows (tile::gather4): rows y0..y3 of the columns [x, x + box
+// width) land one after another at dst (the tensor map's box is one row high). With
+// the 128-byte swizzle each row is swizzled by its position in shared memory, so four
+// gathers of four rows fill an 8-row atom exactly as one tiled load would.
+__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap *map, int x, int y0, int y1, int y2,
+                                            int y3, uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3), "r"(bar)
+        : "memory");
+}
+
 // Programmatic dependent launch: a kernel launched with programmatic stream
 // serialisation may start while the previous kernel in the stream runs; it must wait
 // here before reading that kernel's results (a no-op without the launch attribute).

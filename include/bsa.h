@@ -267,10 +267,13 @@ bsa_status bsa_query_groups(const void *Q, int dt, int B, int H, int N, int d, i
  *   tokens      device int32, capacity >= B*H*(N/128)*K entries
  *   workspace   device, >= bsa_workspace_size(3, ...) bytes, 256-byte aligned; after the call
  *               it holds the masses fp32 [B*H*N/128][N] at byte offset 256
- * Errors: BSA_ERR_SHAPE (N not a multiple of 128, d, B*H > 65535, N too large for the
- * shared-memory row of this first path), BSA_ERR_DTYPE, BSA_ERR_INVALID_ARG, BSA_ERR_CAPACITY,
- * BSA_ERR_WORKSPACE; device-raised: BSA_ERR_INVALID_ARG (perm index outside [0, N), skipped),
- * BSA_ERR_NONFINITE (a NaN mass). Runs on CUDA cores (first path).
+ * Errors: BSA_ERR_SHAPE (N not a multiple of 128, d, B*H > 65535; for fp32 also N too
+ * large for its shared-memory row of N keys), BSA_ERR_DTYPE, BSA_ERR_INVALID_ARG,
+ * BSA_ERR_CAPACITY, BSA_ERR_WORKSPACE; device-raised: BSA_ERR_INVALID_ARG (perm index
+ * outside [0, N), skipped), BSA_ERR_NONFINITE (a NaN mass).
+ * bf16: the masses run on tcgen05 as K_chunk Q_g^T (one thread per key sums its mass over
+ * the group's 128 queries), then an exact 8-bit radix top-K per group reads them from the
+ * workspace (any N). fp32: CUDA cores.
  */
 bsa_status bsa_select_tokens(const void *Q, const void *K, int dt, int B, int H, int N, int d, const int32_t *perm,
                              const float *LSE, float density, float scale, int32_t *tokens, int64_t tokens_capacity,
@@ -305,8 +308,10 @@ bsa_status bsa_tokens_per_group(int N, float density, int *n_tokens);
  *               device error word, read by bsa_check_device_error)
  * Errors: BSA_ERR_SHAPE (N not a multiple of 128, d, B*H > 65535), BSA_ERR_DTYPE, BSA_ERR_INVALID_ARG
  * (null or misaligned pointers, n_tokens out of range, non-finite scale),
- * BSA_ERR_WORKSPACE. An index outside [0, N) in perm or tokens is skipped and raises
- * BSA_ERR_INVALID_ARG in the workspace. This first path runs on CUDA cores (fp32 math).
+ * BSA_ERR_WORKSPACE. An index outside [0, N) in perm or tokens raises BSA_ERR_INVALID_ARG in
+ * the workspace (the row or key is then not computed as asked: the results are undefined).
+ * bf16 runs on tcgen05: a 128-query group is one tile, its keys arrive 128 per step with rows
+ * gathered by index (TMA tile::gather4), the last step masked. fp32 runs on CUDA cores.
  */
 bsa_status bsa_forward_tokens(const void *Q, const void *K, const void *V, int dt, int B, int H, int N, int d,
                               const int32_t *perm, const int32_t *tokens, int n_tokens, float scale, void *O,

@@ -73,6 +73,37 @@ def test_token_forward_matches_oracle(name):
         assert np.abs(Lg[h] - L_ref).max() <= gu.LSE_MAX_ABS
 
 
+@pytest.mark.parametrize("d,density", [(128, 0.15), (64, 0.1)])
+def test_token_forward_working_size_sampled_groups(d, density):
+    # the dynamic_topk shape (N = 8192, 64 groups of 128 per head) at 15% / 10% of the keys:
+    # 1228 / 819 tokens per group, so the last 128-key step is ragged. Groups from the
+    # oracle, token sets seeded (the forward must hold for any ascending set); every row
+    # of a seeded sample of groups against the oracle's token attention.
+    w = wl.scaled(wl.WORKLOADS["dynamic_topk"], H=2, d=d)
+    inp = wl.make_inputs(w)
+    BH, G = w.B * w.H, w.N // C
+    K = bb.tokens_per_group(w.N, density)
+    assert K % C != 0
+    qf, kf, vf = (inp[n].reshape(BH, w.N, w.d) for n in ("q", "k", "v"))
+    perm = np.stack([oracle.query_groups(qf[h], C) for h in range(BH)])
+    rng = np.random.default_rng(d)
+    toks = np.stack([[np.sort(rng.choice(w.N, size=K, replace=False)) for _ in range(G)] for _ in range(BH)])
+    q, k, v = (gu.upload(inp, n) for n in ("q", "k", "v"))
+    O, L = bb.forward_tokens(q, k, v, torch.from_numpy(perm.astype(np.int32)).cuda(),
+                             torch.from_numpy(toks.astype(np.int32)).cuda())
+    torch.cuda.synchronize()
+    Og = O.float().reshape(BH, w.N, w.d).cpu().numpy().astype(np.float64)
+    Lg = L.reshape(BH, w.N).cpu().numpy().astype(np.float64)
+    for h in range(BH):
+        for g in sorted({0, G - 1} | set(rng.choice(G, size=6, replace=False).tolist())):
+            rows = perm[h, g * C:(g + 1) * C]
+            sub = np.arange(C)  # the group alone: its own permutation is 0..127
+            O_ref, L_ref = oracle.token_attention(qf[h][rows], kf[h], vf[h], sub, toks[h, g][None], C)
+            err = np.abs(Og[h][rows] - O_ref)
+            assert err.max() <= gu.O_MAX_ABS and err.mean() <= gu.O_MEAN_ABS, (h, g, err.max(), err.mean())
+            assert np.abs(Lg[h][rows] - L_ref).max() <= gu.LSE_MAX_ABS
+
+
 def test_token_forward_out_of_range_index_is_reported():
     w, density = CASES["bf16_d64"]
     inp = wl.make_inputs(w)
@@ -130,6 +161,41 @@ def test_token_selection_matches_oracle(name):
         err = np.abs(Og[h] - O_ref)
         assert err.max() <= gu.O_MAX_ABS and err.mean() <= gu.O_MEAN_ABS
         assert np.abs(Lg[h] - L_ref).max() <= gu.LSE_MAX_ABS
+
+
+@pytest.mark.parametrize("N,density", [(8192, 0.15), (40960, 0.05)])
+def test_token_selection_working_sizes(N, density):
+    # the selection at the dynamic_topk size and above the former shared-memory limit of
+    # about 37k keys: the dense LSE from the GPU's full-index forward (pass 1), groups from
+    # a seeded permutation; masses of sampled groups against the oracle's (double, same
+    # LSE), and every group's kept tokens bit for bit against the oracle's rule on the
+    # kernel's own fp32 masses
+    w = wl.scaled(wl.WORKLOADS["dynamic_topk"], H=1, N=N)
+    inp = wl.make_inputs(w)
+    BH, G = w.B * w.H, N // C
+    q, k, v = (gu.upload(inp, n) for n in ("q", "k", "v"))
+    ones = np.ones((w.B, w.H, w.nQB, w.nKB), dtype=np.uint8)
+    full = bb.build_mask(None, None, w.block, spec=bb.explicit_spec(
+        torch.from_numpy(gu.mask_bitmap_words(ones).reshape(-1)).cuda()), shape=(w.B, w.H, N, w.d))
+    _, lse = bb.forward(q, k, v, full)
+    del full
+    rng = np.random.default_rng(N)
+    perm = np.stack([rng.permutation(N) for _ in range(BH)]).astype(np.int32)
+    perm_d = torch.from_numpy(perm).cuda()
+    toks, ws = bb.select_tokens(q, k, perm_d, lse, density)
+    torch.cuda.synchronize()
+    K = bb.tokens_per_group(N, density)
+    got = ws[256:256 + BH * G * N * 4].view(torch.float32).reshape(BH, G, N).cpu().numpy()
+    sel = toks.cpu().numpy()
+    lse_h = lse.reshape(BH, N).cpu().numpy().astype(np.float64)
+    qf, kf = (inp[n].reshape(BH, N, w.d) for n in ("q", "k"))
+    for h in range(BH):
+        for g in sorted({0, G - 1} | set(rng.choice(G, size=4, replace=False).tolist())):
+            rows = perm[h, g * C:(g + 1) * C]
+            ref = oracle.token_mass(qf[h][rows], kf[h], lse_h[h][rows], np.arange(C), C)[0]
+            np.testing.assert_allclose(got[h, g], ref, rtol=MASS_RTOL, atol=1e-6 * C)
+        np.testing.assert_array_equal(sel[h], oracle.select_tokens(got[h].astype(np.float64), density))
+        assert sel.shape[-1] == K
 
 
 def _sse(x, perm):

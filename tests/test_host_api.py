@@ -222,7 +222,10 @@ def test_token_selection_workspace_and_arguments(lib):
         return e.value.code
 
     assert sel(N=500) == bb.ERR_SHAPE
-    assert sel(N=1 << 16, d=128) == bb.ERR_SHAPE  # one shared-memory key per token
+    # fp32 runs on CUDA cores with one shared-memory key per token; bf16 (tcgen05 masses in the
+    # workspace, radix top-k) has no such limit and reaches the capacity check instead
+    assert sel(N=1 << 16, d=128, dt=bb.FP32) == bb.ERR_SHAPE
+    assert sel(N=1 << 16, d=128) == bb.ERR_CAPACITY
     assert sel(dt=3) == bb.ERR_DTYPE
     assert sel(LSE=None) == bb.ERR_INVALID_ARG
     assert sel(density=0.0) == bb.ERR_INVALID_ARG
