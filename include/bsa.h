@@ -241,10 +241,11 @@ bsa_status bsa_forward_residual(const void *Q, const void *K, const void *V, int
  *   Q           device [B][H][N][d], dtype dt; N a multiple of 128, N/128 <= 512
  *   perm        device int32 [B*H][N] (written)
  *   workspace   device, >= bsa_workspace_size(4, ...) bytes, 256-byte aligned
- * The principal direction comes from fp32 power iteration (32 steps from a fixed start),
- * so a row lying within rounding of a median may land on the other side than an exact
- * eigendecomposition would put it. Errors: BSA_ERR_SHAPE, BSA_ERR_DTYPE,
- * BSA_ERR_INVALID_ARG, BSA_ERR_WORKSPACE. Runs on CUDA cores, one CTA per (b, h).
+ * The principal direction comes from fp32 power iteration (32 steps from a fixed start) on
+ * the segment's centred scatter matrix, so a row lying within rounding of a median may land
+ * on the other side than an exact eigendecomposition would put it. Errors: BSA_ERR_SHAPE,
+ * BSA_ERR_DTYPE, BSA_ERR_INVALID_ARG, BSA_ERR_WORKSPACE. Runs on CUDA cores: one launch per
+ * level of the split tree, one CTA per (b, h, segment).
  */
 bsa_status bsa_query_groups(const void *Q, int dt, int B, int H, int N, int d, int32_t *perm, void *workspace,
                             size_t workspace_bytes, void *stream);

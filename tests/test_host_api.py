@@ -236,7 +236,8 @@ def test_token_selection_workspace_and_arguments(lib):
 def test_query_groups_workspace_and_arguments(lib):
     up = lambda x: (x + 255) // 256 * 256  # noqa: E731
     n = 2 * 3 * 1024
-    assert bb.bsa_workspace_size(4, 2, 3, 1024, 64, 64) == 256 + 3 * up(n * 4)
+    # working permutation, 64-bit (projection, row) keys, scratch copy
+    assert bb.bsa_workspace_size(4, 2, 3, 1024, 64, 64) == 256 + up(n * 4) + up(n * 8) + up(n * 4)
 
     def grp(**kw):
         args = dict(Q=FAKE, dt=bb.BF16, B=1, H=2, N=512, d=64, perm=FAKE, ws=FAKE, ws_bytes=1 << 30)
