@@ -311,7 +311,7 @@ bsa_status bsa_workspace_size(int which, int B, int H, int N, int d, int block, 
         *bytes = bsa::token_select_ws_layout(B, H, N).total;
     } else if (which == 4) {
         if (N % bsa::kTokenGroup != 0) return BSA_ERR_SHAPE;
-        *bytes = bsa::query_groups_ws_layout(B, H, N).total;
+        *bytes = bsa::query_groups_ws_layout(B, H, N, d).total;
     } else return BSA_ERR_INVALID_ARG;
     return BSA_OK;
 }
@@ -458,11 +458,12 @@ bsa_status bsa_query_groups(const void *Q, int dt, int B, int H, int N, int d, i
                             size_t workspace_bytes, void *stream)
 {
     if (B <= 0 || H <= 0 || N <= 0 || (d != 64 && d != 128) || N % bsa::kTokenGroup != 0) return BSA_ERR_SHAPE;
-    if (N / bsa::kTokenGroup > bsa::kMaxQueryGroups || static_cast<int64_t>(B) * H * N > INT32_MAX)
+    if (N / bsa::kTokenGroup > bsa::kMaxQueryGroups || static_cast<int64_t>(B) * H * N > INT32_MAX ||
+        static_cast<int64_t>(B) * H > 65535)
         return BSA_ERR_SHAPE;
     if (dt != BSA_BF16 && dt != BSA_FP32) return BSA_ERR_DTYPE;
     if (!Q || !perm || !aligned(Q, 16) || !aligned(perm, 4)) return BSA_ERR_INVALID_ARG;
-    if (!workspace || !aligned(workspace, 256) || workspace_bytes < bsa::query_groups_ws_layout(B, H, N).total)
+    if (!workspace || !aligned(workspace, 256) || workspace_bytes < bsa::query_groups_ws_layout(B, H, N, d).total)
         return BSA_ERR_WORKSPACE;
     bsa::GroupArgs a{};
     a.Q = Q;

@@ -163,11 +163,13 @@ struct GroupArgs {
     int32_t *perm;  // [B*H][N] (written)
     char *ws;
 };
-// workspace: header, working permutation, projection keys and a scratch copy, [B*H][N] each
+// workspace: header; working permutation, projection keys and a scratch copy, [B*H][N]
+// each; per head N/128 slots of a slice's row sum [d], a slice's scatter blocks
+// [d*d/256 * 136] and a segment's (mean, direction) [2][d]
 struct QueryGroupWs {
-    size_t work, keys, scratch, total;
+    size_t work, keys, scratch, psum, pscatter, dir, total;
 };
-QueryGroupWs query_groups_ws_layout(int B, int H, int N);
+QueryGroupWs query_groups_ws_layout(int B, int H, int N, int d);
 bsa_status launch_query_groups(const GroupArgs &a, cudaStream_t st);
 
 }  // namespace bsa

@@ -7,25 +7,35 @@
 // by (projection, row index), as the first half; groups come out in depth-first order,
 // rows ascending inside a group (the layout bsa_select_tokens and bsa_forward_tokens take).
 //
-// The split tree depends on N only, so the splits run level by level: one launch per
-// level, one CTA per (b, h, segment of that level), every segment of every head at once.
-// A CTA, in place in the working permutation of its head:
-//   mean of the segment's rows (fp32; warps over rows, then the warps in order),
-//   the centred scatter matrix S = sum (x - mu)(x - mu)^T in one pass (each thread owns a
-//   block of entries and adds the rows in order),
-//   the principal direction by kPowerIters steps of power iteration on S from a fixed start
-//   (sign: its largest-magnitude entry positive),
-//   64-bit keys (projection as an order-preserving key, row index) in the workspace,
-//   the cut: the cut-th smallest key by an exact radix select (8-bit digits), and a
-//   stable partition (first half: keys up to the cut) through a scratch copy.
-// A final launch sorts each group's rows ascending. fp32 and an iterative eigenvector:
-// near the median a row may fall on the other side than in an exact eigendecomposition,
-// so results are judged by the partition they form, and bit for bit where no row lies
-// within the rounding bound of a cut.
+// The split tree depends on N only, so the splits run level by level, every segment of
+// every head at once, in place in the working permutation of each head. Each segment of a
+// level is cut into P slices of at most kSliceRows rows (P the same for the whole level), and
+// a level is five launches:
+//   slice_sum_kernel      per slice: the sum of its rows (fp32; each warp adds its rows in
+//                         order, then the warps in order);
+//   slice_scatter_kernel  per slice: the segment's mean (the slice sums in slice order, over
+//                         the length), then sum (x - mu)(x - mu)^T over the slice's rows, the
+//                         blocks on or above the diagonal (a thread owns a block and adds the
+//                         rows in order);
+//   direction_kernel      per segment: the centred scatter matrix S = the slices' blocks
+//                         added in slice order, and the principal direction by kPowerIters
+//                         steps of power iteration on S from a fixed start (sign: its
+//                         largest-magnitude entry positive);
+//   slice_keys_kernel     per slice: 64-bit keys (projection as an order-preserving key, row
+//                         index);
+//   cut_kernel            per segment: the cut-th smallest key by an exact radix select
+//                         (8-bit digits), and a stable partition (first half: keys up to the
+//                         cut) through a scratch copy.
+// Every sum runs in a fixed order, so the groups do not change from run to run. A final
+// launch sorts each group's rows ascending. fp32 and an iterative eigenvector: near the
+// median a row may fall on the other side than in an exact eigendecomposition, so results
+// are judged by the partition they form, and bit for bit where no row lies within the
+// rounding bound of a cut.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace bsa {
 namespace {
@@ -33,10 +43,10 @@ namespace {
 constexpr int kGrpThreads = 256;
 constexpr int kGrpWarps = kGrpThreads / 32;
 constexpr int kPowerIters = 32;
-constexpr int kStageRows = 32;  // rows staged per step of the scatter-matrix pass
-
-__device__ __forceinline__ float ld(const float *p) { return *p; }
-__device__ __forceinline__ float ld(const __nv_bfloat16 *p) { return __bfloat162float(*p); }
+constexpr int kStageRows = 32;                 // rows staged per step of the scatter pass
+constexpr int kSliceRows = 4 * kTokenGroup;    // rows per slice at most
+constexpr int kTriBlocks = 136;                // blocks of a 16 x 16 grid on or above the diagonal
+constexpr int kScatThreads = 160;              // kTriBlocks computing threads, 5 warps staging rows
 
 __device__ __forceinline__ uint32_t order_key_asc(float s)
 {
@@ -66,116 +76,215 @@ __device__ __forceinline__ bool segment_of(int N, int level, int seg, int &s, in
     return len > C;
 }
 
-// Sum over the CTA, the warps in order (fixed order).
-__device__ __forceinline__ float block_sum(float v, float *red)
+// Slices: a segment of `len` rows at a level with P slices per segment is cut into P runs
+// of ceil(len / P) rows (the last may be shorter or empty). False when the segment is final.
+__device__ __forceinline__ bool slice_of(int N, int level, int P, int slot, int &seg, int &s, int &len, int &r0,
+                                         int &r1)
 {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    __syncthreads();
-    if (lane == 0) red[warp] = v;
-    __syncthreads();
-    float t = 0.0f;
-    for (int w = 0; w < kGrpWarps; ++w) t += red[w];
-    return t;
+    seg = slot / P;
+    const int p = slot - seg * P;
+    if (!segment_of(N, level, seg, s, len)) return false;
+    const int chunk = (len + P - 1) / P;
+    r0 = min(len, p * chunk);
+    r1 = min(len, r0 + chunk);
+    return true;
 }
 
-// One split of every segment of one level. grid (2^level, B*H).
-template <typename T, int D>
-__global__ void __launch_bounds__(kGrpThreads) split_level_kernel(const T *__restrict__ X, int N, int level,
-                                                                  int32_t *__restrict__ work,
-                                                                  unsigned long long *__restrict__ keys,
-                                                                  int32_t *__restrict__ scratch)
+// VEC consecutive elements of a row as fp32 (8- or 16-byte loads).
+template <int VEC>
+__device__ __forceinline__ void ldvec(const float *p, float (&o)[VEC])
 {
-    constexpr int C = kTokenGroup;
-    constexpr int DPL = D / 32;             // dimensions per lane (row-wise passes)
-    constexpr int BLK = D / 16;             // scatter-matrix block per thread: BLK x BLK entries
-    __shared__ float red[kGrpWarps];
-    __shared__ int redi[kGrpWarps];
+    static_assert(VEC == 2 || VEC == 4, "8- or 16-byte loads");
+    if constexpr (VEC == 4) {
+        const float4 f = *reinterpret_cast<const float4 *>(p);
+        o[0] = f.x, o[1] = f.y, o[2] = f.z, o[3] = f.w;
+    } else {
+        const float2 f = *reinterpret_cast<const float2 *>(p);
+        o[0] = f.x, o[1] = f.y;
+    }
+}
+template <int VEC>
+__device__ __forceinline__ void ldvec(const __nv_bfloat16 *p, float (&o)[VEC])
+{
+    static_assert(VEC == 2 || VEC == 4 || VEC == 8, "4-, 8- or 16-byte loads");
+    if constexpr (VEC == 8) {
+        const uint4 u = *reinterpret_cast<const uint4 *>(p);
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) o[2 * k] = __uint_as_float(w[k] << 16), o[2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
+    } else if constexpr (VEC == 4) {
+        const uint2 u = *reinterpret_cast<const uint2 *>(p);
+        o[0] = __uint_as_float(u.x << 16), o[1] = __uint_as_float(u.x & 0xFFFF0000u);
+        o[2] = __uint_as_float(u.y << 16), o[3] = __uint_as_float(u.y & 0xFFFF0000u);
+    } else {
+        const uint32_t u = *reinterpret_cast<const uint32_t *>(p);
+        o[0] = __uint_as_float(u << 16), o[1] = __uint_as_float(u & 0xFFFF0000u);
+    }
+}
+
+// Row passes with 16-byte loads: a lane holds E elements of a row, LPR lanes one row,
+// a warp RPI rows per load and kInFlight loads in flight.
+template <typename T, int D>
+struct RowPass {
+    static constexpr int E = 16 / static_cast<int>(sizeof(T));
+    static constexpr int LPR = D / E;
+    static constexpr int RPI = 32 / LPR;
+    static constexpr int ROWS = RPI * 4;  // rows per warp per step
+};
+
+// Block (bi, bj), bi <= bj, of the 16 x 16 grid of the scatter matrix owned by thread t of
+// kTriBlocks: row blocks p and 15 - p share 17 consecutive threads (16 - p + p + 1 blocks).
+__device__ __forceinline__ void tri_block(int t, int &bi, int &bj)
+{
+    const int pr = t / 17, k = t - 17 * (t / 17);
+    if (k < 16 - pr) {
+        bi = pr;
+        bj = pr + k;
+    } else {
+        bi = 15 - pr;
+        bj = bi + k - (16 - pr);
+    }
+}
+
+// Column c of a staged row in the scatter pass (4 padding floats after every 32).
+__device__ __forceinline__ int pad(int c) { return c + 4 * (c >> 5); }
+
+// The segment's mean: its slices' sums added in slice order, over len.
+template <int D>
+__device__ __forceinline__ void segment_mean(const float *__restrict__ psum, int64_t slot0, int P, int len, float *mu)
+{
+    for (int c = threadIdx.x; c < D; c += blockDim.x) {
+        float m = 0.0f;
+        for (int q = 0; q < P; ++q) m += psum[(slot0 + q) * D + c];
+        mu[c] = m / static_cast<float>(len);
+    }
+}
+
+// Per slice: the sum of its rows. grid (2^level * P, B*H).
+template <typename T, int D>
+__global__ void __launch_bounds__(kGrpThreads) slice_sum_kernel(const T *__restrict__ X, int N, int level, int P,
+                                                                int G, const int32_t *__restrict__ work,
+                                                                float *__restrict__ psum)
+{
+    using RP = RowPass<T, D>;
+    constexpr int E = RP::E;
     __shared__ float part[kGrpWarps][D];
-    __shared__ __align__(16) float mu[D];
-    __shared__ float v[D], w[D];
-    __shared__ int hist[256];
-    // dynamic: the scatter matrix S [D][D + 1] (padded rows) and the staged centred rows [32][D]
-    extern __shared__ float4 grp_dyn[];
-    float (*S)[D + 1] = reinterpret_cast<float (*)[D + 1]>(grp_dyn);
-    float (*xs)[D] = reinterpret_cast<float (*)[D]>(reinterpret_cast<float *>(grp_dyn) + D * (D + 1));
-    __shared__ int s_digit, s_krem;
-    int s, len;
-    if (!segment_of(N, level, blockIdx.x, s, len)) return;  // block-uniform
+    grid_dependency_wait();
+    int seg, s, len, r0, r1;
+    if (!slice_of(N, level, P, blockIdx.x, seg, s, len, r0, r1)) return;  // block-uniform
+    const int64_t bh = blockIdx.y;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int rs = lane / RP::LPR, cp = lane % RP::LPR;  // row of the load, columns cp*E ..
+    const T *x = X + bh * static_cast<int64_t>(N) * D + cp * E;
+    const int32_t *idx = work + bh * N + s;
+    float acc[E];
+#pragma unroll
+    for (int t = 0; t < E; ++t) acc[t] = 0.0f;
+    // each lane adds the rows of its load slot in order
+    for (int i0 = r0 + warp * RP::ROWS; i0 < r1; i0 += kGrpWarps * RP::ROWS) {
+        float vals[4][E];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int i = i0 + u * RP::RPI + rs;
+            if (i < r1) {
+                ldvec<E>(x + static_cast<int64_t>(idx[i]) * D, vals[u]);
+            } else {
+#pragma unroll
+                for (int t = 0; t < E; ++t) vals[u][t] = 0.0f;
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+#pragma unroll
+            for (int t = 0; t < E; ++t) acc[t] += vals[u][t];
+    }
+    // the warp's load slots (xor butterfly: every lane of a column part ends with one sum)
+#pragma unroll
+    for (int o = RP::LPR; o < 32; o <<= 1)
+#pragma unroll
+        for (int t = 0; t < E; ++t) acc[t] += __shfl_xor_sync(0xffffffffu, acc[t], o);
+    if (rs == 0) {
+#pragma unroll
+        for (int t = 0; t < E; ++t) part[warp][cp * E + t] = acc[t];
+    }
+    __syncthreads();
+    for (int c = threadIdx.x; c < D; c += kGrpThreads) {
+        float m = 0.0f;
+        for (int w = 0; w < kGrpWarps; ++w) m += part[w][c];
+        psum[(bh * G + blockIdx.x) * D + c] = m;
+    }
+}
+
+// Per slice: sum over its rows of (x - mu)(x - mu)^T, the blocks on or above the diagonal.
+// Thread t < kTriBlocks owns one BLK x BLK block and adds the rows in order; entry e of
+// block t goes to pS[slot][e][t]. grid (2^level * P, B*H).
+template <typename T, int D>
+__global__ void __launch_bounds__(kScatThreads, 3)
+    slice_scatter_kernel(const T *__restrict__ X, int N, int level, int P, int G, const int32_t *__restrict__ work,
+                         const float *__restrict__ psum, float *__restrict__ pS)
+{
+    constexpr int VEC = D / 32;
+    constexpr int BLK = D / 16;
+    constexpr int NW = kScatThreads / 32;
+    constexpr int RPW = (kStageRows + NW - 1) / NW;  // staged rows per warp
+    constexpr int XW = D + D / 8;  // staged row: 4 padding floats after every 32 (float4 reads of 8-float blocks hit distinct banks)
+    __shared__ __align__(16) float xs[kStageRows][XW];
+    __shared__ float mu[D];
+    grid_dependency_wait();
+    int seg, s, len, r0, r1;
+    if (!slice_of(N, level, P, blockIdx.x, seg, s, len, r0, r1)) return;  // block-uniform
     const int64_t bh = blockIdx.y;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const T *x = X + bh * static_cast<int64_t>(N) * D;
-    int32_t *idx = work + bh * N + s;
-    unsigned long long *key = keys + bh * N + s;
-    int32_t *tmp = scratch + bh * N + s;
-
-    // mean
-    {
-        float acc[DPL];
+    const int32_t *idx = work + bh * N + s;
+    segment_mean<D>(psum, bh * G + static_cast<int64_t>(seg) * P, P, len, mu);
+    const bool comp = threadIdx.x < kTriBlocks;
+    int bi = 0, bj = 0;
+    tri_block(comp ? threadIdx.x : 0, bi, bj);
+    float acc[BLK][BLK];
 #pragma unroll
-        for (int t = 0; t < DPL; ++t) acc[t] = 0.0f;
-        // four rows per warp in flight; each warp still adds its rows in order
-        for (int i0 = warp * 4; i0 < len; i0 += kGrpWarps * 4) {
-            float vals[4][DPL];
+    for (int a = 0; a < BLK; ++a)
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int i = i0 + u;
-                const T *row = x + static_cast<int64_t>(i < len ? idx[i] : idx[0]) * D;
+        for (int b = 0; b < BLK; ++b) acc[a][b] = 0.0f;
+    // the next stage of rows is loaded into registers while this one is used
+    float nxt[RPW][VEC];
+    auto fetch = [&](int a0) {
 #pragma unroll
-                for (int t = 0; t < DPL; ++t) vals[u][t] = i < len ? ld(row + lane + 32 * t) : 0.0f;
+        for (int u = 0; u < RPW; ++u) {
+            const int r = warp + NW * u;
+            if (r < kStageRows && a0 + r < r1) {
+                ldvec<VEC>(x + static_cast<int64_t>(idx[a0 + r]) * D + lane * VEC, nxt[u]);
+            } else {
+#pragma unroll
+                for (int t = 0; t < VEC; ++t) nxt[u][t] = 0.0f;
             }
-#pragma unroll
-            for (int u = 0; u < 4; ++u)
-#pragma unroll
-                for (int t = 0; t < DPL; ++t) acc[t] += vals[u][t];
         }
+    };
+    fetch(r0);
+    __syncthreads();  // mu
+    for (int a0 = r0; a0 < r1; a0 += kStageRows) {
+        if (a0 != r0) __syncthreads();
 #pragma unroll
-        for (int t = 0; t < DPL; ++t) part[warp][lane + 32 * t] = acc[t];
-        __syncthreads();
-        if (threadIdx.x < D) {
-            float m = 0.0f;
-            for (int ww = 0; ww < kGrpWarps; ++ww) m += part[ww][threadIdx.x];
-            mu[threadIdx.x] = m / static_cast<float>(len);
+        for (int u = 0; u < RPW; ++u) {
+            const int r = warp + NW * u;
+            if (r < kStageRows) {
+#pragma unroll
+                for (int t = 0; t < VEC; ++t)
+                    xs[r][pad(lane * VEC + t)] = a0 + r < r1 ? nxt[u][t] - mu[lane * VEC + t] : 0.0f;
+            }
         }
         __syncthreads();
-    }
-    // centred scatter matrix: thread (ti, tj) owns rows BLK*ti.. and columns BLK*tj..
-    {
-        const int ti = threadIdx.x / 16, tj = threadIdx.x % 16;
-        float acc[BLK][BLK];
-#pragma unroll
-        for (int a = 0; a < BLK; ++a)
-#pragma unroll
-            for (int b = 0; b < BLK; ++b) acc[a][b] = 0.0f;
-        // the next batch of rows is loaded into registers while this one is used
-        constexpr int PER = kStageRows * D / kGrpThreads;
-        float nxt[PER];
-        auto fetch = [&](int r0) {
-#pragma unroll
-            for (int q = 0; q < PER; ++q) {
-                const int e = q * kGrpThreads + threadIdx.x;
-                const int r = e / D, c = e % D;
-                nxt[q] = r0 + r < len ? ld(x + static_cast<int64_t>(idx[r0 + r]) * D + c) : 0.0f;
-            }
-        };
-        fetch(0);
-        for (int r0 = 0; r0 < len; r0 += kStageRows) {
-            __syncthreads();
-#pragma unroll
-            for (int q = 0; q < PER; ++q) {
-                const int e = q * kGrpThreads + threadIdx.x;
-                const int r = e / D, c = e % D;
-                xs[r][c] = r0 + r < len ? nxt[q] - mu[c] : 0.0f;
-            }
-            __syncthreads();
-            if (r0 + kStageRows < len) fetch(r0 + kStageRows);
-            for (int r = 0; r < kStageRows; ++r) {
+        if (a0 + kStageRows < r1) fetch(a0 + kStageRows);
+        const int nr = min(kStageRows, r1 - a0);
+        if (comp) {
+            for (int r = 0; r < nr; ++r) {
                 float a_[BLK], b_[BLK];
 #pragma unroll
-                for (int a = 0; a < BLK; ++a) {
-                    a_[a] = xs[r][BLK * ti + a];
-                    b_[a] = xs[r][BLK * tj + a];
+                for (int q = 0; q < BLK / 4; ++q) {
+                    const float4 fa = *reinterpret_cast<const float4 *>(&xs[r][pad(BLK * bi + 4 * q)]);
+                    const float4 fb = *reinterpret_cast<const float4 *>(&xs[r][pad(BLK * bj + 4 * q)]);
+                    a_[4 * q] = fa.x, a_[4 * q + 1] = fa.y, a_[4 * q + 2] = fa.z, a_[4 * q + 3] = fa.w;
+                    b_[4 * q] = fb.x, b_[4 * q + 1] = fb.y, b_[4 * q + 2] = fb.z, b_[4 * q + 3] = fb.w;
                 }
 #pragma unroll
                 for (int a = 0; a < BLK; ++a)
@@ -183,22 +292,110 @@ __global__ void __launch_bounds__(kGrpThreads) split_level_kernel(const T *__res
                     for (int b = 0; b < BLK; ++b) acc[a][b] = fmaf(a_[a], b_[b], acc[a][b]);
             }
         }
+    }
+    if (comp) {
+        float *out = pS + (bh * G + blockIdx.x) * static_cast<int64_t>(BLK * BLK * kTriBlocks) + threadIdx.x;
 #pragma unroll
         for (int a = 0; a < BLK; ++a)
 #pragma unroll
-            for (int b = 0; b < BLK; ++b) S[BLK * ti + a][BLK * tj + b] = acc[a][b];
-        if (threadIdx.x < D) v[threadIdx.x] = (1.0f + 0.01f * threadIdx.x) * rsqrtf(static_cast<float>(D));
-        __syncthreads();
+            for (int b = 0; b < BLK; ++b) out[(a * BLK + b) * kTriBlocks] = acc[a][b];
     }
-    // power iteration on S
-    for (int it = 0; it < kPowerIters; ++it) {
-        float wi = 0.0f;
-        if (threadIdx.x < D) {
-            for (int j = 0; j < D; ++j) wi = fmaf(S[threadIdx.x][j], v[j], wi);
-            w[threadIdx.x] = wi;
+}
+
+// Per segment: S = its slices' scatter blocks added in slice order (mirrored below the
+// diagonal), then the principal direction by kPowerIters steps of power iteration from a
+// fixed start; writes dir[seg] = (mu, v). grid (2^level, B*H).
+template <int D>
+__global__ void __launch_bounds__(kGrpThreads) direction_kernel(int N, int level, int P, int G,
+                                                                const float *__restrict__ psum,
+                                                                const float *__restrict__ pS,
+                                                                float *__restrict__ dir)
+{
+    constexpr int BLK = D / 16;
+    constexpr int PER = BLK * BLK * kTriBlocks;
+    constexpr int SW = D + 8;  // row stride of S: 16-byte rows, 8 rows x 2 halves on distinct banks
+    constexpr int EB = 4;      // entries per thread per batch
+    constexpr int QB = 4;      // slices per batch
+    static_assert(2 * D <= kGrpThreads, "two threads per row of S");
+    extern __shared__ float4 grp_dyn[];
+    float *S = reinterpret_cast<float *>(grp_dyn);
+    __shared__ __align__(16) float v[D];
+    __shared__ float mu[D], red[kGrpWarps];
+    grid_dependency_wait();
+    int s, len;
+    if (!segment_of(N, level, blockIdx.x, s, len)) return;  // block-uniform
+    const int64_t bh = blockIdx.y;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int64_t slot0 = bh * G + static_cast<int64_t>(blockIdx.x) * P;
+    segment_mean<D>(psum, slot0, P, len, mu);
+    // each entry: its slices added in order; EB entries x QB slices of loads in flight
+    const float *src = pS + slot0 * PER;
+    for (int e0 = threadIdx.x; e0 < PER; e0 += EB * kGrpThreads) {
+        float m[EB];
+#pragma unroll
+        for (int k = 0; k < EB; ++k) m[k] = 0.0f;
+        for (int q0 = 0; q0 < P; q0 += QB) {
+            float val[QB][EB];
+#pragma unroll
+            for (int q = 0; q < QB; ++q)
+#pragma unroll
+                for (int k = 0; k < EB; ++k) {
+                    const int e = e0 + k * kGrpThreads;
+                    val[q][k] = q0 + q < P && e < PER ? src[static_cast<int64_t>(q0 + q) * PER + e] : 0.0f;
+                }
+#pragma unroll
+            for (int q = 0; q < QB; ++q)
+#pragma unroll
+                for (int k = 0; k < EB; ++k)
+                    if (q0 + q < P) m[k] += val[q][k];
         }
-        const float nrm2 = block_sum(threadIdx.x < D ? wi * wi : 0.0f, red);
-        if (threadIdx.x < D && nrm2 > 0.0f) v[threadIdx.x] = wi * rsqrtf(nrm2);
+#pragma unroll
+        for (int k = 0; k < EB; ++k) {
+            const int e = e0 + k * kGrpThreads;
+            if (e < PER) {
+                const int t = e % kTriBlocks, ent = e / kTriBlocks;
+                int bi, bj;
+                tri_block(t, bi, bj);
+                const int i = BLK * bi + ent / BLK, j = BLK * bj + ent % BLK;
+                S[i * SW + j] = m[k];
+                if (bi != bj) S[j * SW + i] = m[k];  // a diagonal block holds (i, j) and (j, i) itself
+            }
+        }
+    }
+    if (threadIdx.x < D) v[threadIdx.x] = (1.0f + 0.01f * threadIdx.x) * rsqrtf(static_cast<float>(D));
+    __syncthreads();
+    // w = S v: two threads per row, each over alternate 4-column chunks of the row (held in
+    // registers) with 4 accumulators
+    const bool act = threadIdx.x < 2 * D;
+    const int row = threadIdx.x >> 1, half = threadIdx.x & 1;
+    float sreg[D / 2];
+#pragma unroll
+    for (int m = 0; m < D / 8; ++m) {
+        float4 sv = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        if (act) sv = *reinterpret_cast<const float4 *>(S + row * SW + 8 * m + 4 * half);
+        sreg[4 * m] = sv.x, sreg[4 * m + 1] = sv.y, sreg[4 * m + 2] = sv.z, sreg[4 * m + 3] = sv.w;
+    }
+    for (int it = 0; it < kPowerIters; ++it) {
+        float a4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+        for (int m = 0; m < D / 8; ++m) {
+            const float4 vv = *reinterpret_cast<const float4 *>(v + 8 * m + 4 * half);
+            a4[0] = fmaf(sreg[4 * m], vv.x, a4[0]);
+            a4[1] = fmaf(sreg[4 * m + 1], vv.y, a4[1]);
+            a4[2] = fmaf(sreg[4 * m + 2], vv.z, a4[2]);
+            a4[3] = fmaf(sreg[4 * m + 3], vv.w, a4[3]);
+        }
+        float w = (a4[0] + a4[1]) + (a4[2] + a4[3]);
+        w += __shfl_xor_sync(0xffffffffu, w, 1);  // both threads of a row hold the same sum
+        float sq = act && half == 0 ? w * w : 0.0f;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
+        if (lane == 0) red[warp] = sq;
+        __syncthreads();
+        float nrm2 = 0.0f;
+#pragma unroll
+        for (int ww = 0; ww < kGrpWarps; ++ww) nrm2 += red[ww];
+        if (act && half == 0 && nrm2 > 0.0f) v[row] = w * rsqrtf(nrm2);
         __syncthreads();
     }
     // sign: the entry of largest magnitude (lowest index on ties) is positive
@@ -222,35 +419,90 @@ __global__ void __launch_bounds__(kGrpThreads) split_level_kernel(const T *__res
             }
         }
         const float sgn = v[bj] < 0.0f ? -1.0f : 1.0f;
-        __syncwarp();
-        for (int j = lane; j < D; j += 32) v[j] *= sgn;
+        float *o = dir + (bh * G + blockIdx.x) * 2 * D;
+        for (int j = lane; j < D; j += 32) {
+            o[j] = mu[j];
+            o[D + j] = v[j] * sgn;
+        }
+    }
+}
+
+// Per slice: the keys (projection on the segment's direction as an ascending key, row
+// index) of its rows. grid (2^level * P, B*H).
+template <typename T, int D>
+__global__ void __launch_bounds__(kGrpThreads) slice_keys_kernel(const T *__restrict__ X, int N, int level, int P,
+                                                                 int G, const int32_t *__restrict__ work,
+                                                                 const float *__restrict__ dir,
+                                                                 unsigned long long *__restrict__ keys)
+{
+    using RP = RowPass<T, D>;
+    constexpr int E = RP::E;
+    __shared__ float mu[D], v[D];
+    grid_dependency_wait();
+    int seg, s, len, r0, r1;
+    if (!slice_of(N, level, P, blockIdx.x, seg, s, len, r0, r1)) return;  // block-uniform
+    const int64_t bh = blockIdx.y;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int rs = lane / RP::LPR, cp = lane % RP::LPR;
+    const T *x = X + bh * static_cast<int64_t>(N) * D + cp * E;
+    const int32_t *idx = work + bh * N + s;
+    unsigned long long *key = keys + bh * N + s;
+    const float *dv = dir + (bh * G + seg) * 2 * D;
+    for (int c = threadIdx.x; c < D; c += kGrpThreads) {
+        mu[c] = dv[c];
+        v[c] = dv[D + c];
     }
     __syncthreads();
-    // keys: (projection as an ascending key, row index)
-    for (int i0 = warp * 4; i0 < len; i0 += kGrpWarps * 4) {
-        float vals[4][DPL];
+    float mu_[E], v_[E];
+#pragma unroll
+    for (int t = 0; t < E; ++t) {
+        mu_[t] = mu[cp * E + t];
+        v_[t] = v[cp * E + t];
+    }
+    for (int i0 = r0 + warp * RP::ROWS; i0 < r1; i0 += kGrpWarps * RP::ROWS) {
+        float vals[4][E];
         int rr[4];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {  // four rows per warp in flight
-            const int i = i0 + u;
-            rr[u] = i < len ? idx[i] : idx[0];
-            const T *row = x + static_cast<int64_t>(rr[u]) * D;
-#pragma unroll
-            for (int t = 0; t < DPL; ++t) vals[u][t] = ld(row + lane + 32 * t);
+        for (int u = 0; u < 4; ++u) {
+            const int i = i0 + u * RP::RPI + rs;
+            rr[u] = idx[i < r1 ? i : r0];
+            ldvec<E>(x + static_cast<int64_t>(rr[u]) * D, vals[u]);
         }
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
             float dot = 0.0f;
 #pragma unroll
-            for (int t = 0; t < DPL; ++t) dot = fmaf(vals[u][t] - mu[lane + 32 * t], v[lane + 32 * t], dot);
+            for (int t = 0; t < E; ++t) dot = fmaf(vals[u][t] - mu_[t], v_[t], dot);
+            // over the row's LPR lanes (xor butterfly: every lane of the row ends with one sum)
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
-            if (lane == 0 && i0 + u < len)
-                key[i0 + u] = (static_cast<unsigned long long>(order_key_asc(dot)) << 32) | static_cast<uint32_t>(rr[u]);
+            for (int o = RP::LPR / 2; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
+            const int i = i0 + u * RP::RPI + rs;
+            if (cp == 0 && i < r1)
+                key[i] = (static_cast<unsigned long long>(order_key_asc(dot)) << 32) | static_cast<uint32_t>(rr[u]);
         }
     }
-    __syncthreads();
-    // the cut-th smallest key (keys are unique: the row index breaks ties), digit by digit
+}
+
+// Per segment: the cut-th smallest key (keys are unique: the row index breaks ties) by an
+// exact radix select, 8-bit digits, then a stable partition (first half: the keys up to it)
+// through the scratch copy. grid (2^level, B*H).
+__global__ void __launch_bounds__(kGrpThreads) cut_kernel(int N, int level, int32_t *__restrict__ work,
+                                                          const unsigned long long *__restrict__ keys,
+                                                          int32_t *__restrict__ scratch)
+{
+    constexpr int C = kTokenGroup;
+    __shared__ int hist[256];
+    __shared__ int redi[kGrpWarps];
+    __shared__ int s_digit, s_krem;
+    __shared__ bool s_one;
+    grid_dependency_wait();
+    int s, len;
+    if (!segment_of(N, level, blockIdx.x, s, len)) return;  // block-uniform
+    const int64_t bh = blockIdx.y;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int32_t *idx = work + bh * N + s;
+    const unsigned long long *key = keys + bh * N + s;
+    int32_t *tmp = scratch + bh * N + s;
     const int cut = ((len / C + 1) / 2) * C;
     unsigned long long prefix = 0ull, pmask = 0ull;
     int krem = cut;
@@ -285,6 +537,7 @@ __global__ void __launch_bounds__(kGrpThreads) split_level_kernel(const T *__res
                     if (below + cnt[q] >= krem) {
                         s_digit = 8 * lane + q;
                         s_krem = krem - below;
+                        s_one = cnt[q] == 1;
                         break;
                     }
                     below += cnt[q];
@@ -295,30 +548,38 @@ __global__ void __launch_bounds__(kGrpThreads) split_level_kernel(const T *__res
         prefix |= static_cast<unsigned long long>(s_digit) << shift;
         pmask |= 0xFFull << shift;
         krem = s_krem;
+        const bool one = s_one;
         __syncthreads();
+        // a lone key under this prefix is the cut-th smallest: no other key shares the prefix
+        if (one) {
+            prefix |= ~pmask;
+            break;
+        }
     }
-    const unsigned long long Tk = prefix;  // the cut-th smallest: keys <= Tk form the first half
-    // stable partition through the scratch copy (contiguous chunks per thread)
-    const int per = (len + kGrpThreads - 1) / kGrpThreads;
-    const int b0 = min(len, threadIdx.x * per), b1 = min(len, b0 + per);
+    const unsigned long long Tk = prefix;  // the cut-th smallest key, or a bound no other key reaches: keys <= Tk form the first half
+    // stable partition through the scratch copy: warp w takes the w-th run of whole 32-row
+    // chunks; ballots give each row its place
+    const int nch = (len + 31) / 32;
+    const int c0 = warp * nch / kGrpWarps, c1 = (warp + 1) * nch / kGrpWarps;
+    const unsigned below = (1u << lane) - 1u;
     int mine = 0;
-    for (int i = b0; i < b1; ++i) mine += key[i] <= Tk ? 1 : 0;
-    int xsum = mine;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, xsum, o);
-        if (lane >= o) xsum += y;
+    for (int c = c0; c < c1; ++c) {
+        const int i = 32 * c + lane;
+        mine += __popc(__ballot_sync(0xffffffffu, i < len && key[i] <= Tk));
     }
+    if (lane == 0) redi[warp] = mine;
     __syncthreads();
-    if (lane == 31) redi[warp] = xsum;
-    __syncthreads();
-    int wbase = 0;
-    for (int ww = 0; ww < warp; ++ww) wbase += redi[ww];
-    int pos_first = wbase + xsum - mine;
-    int pos_second = cut + (b0 - pos_first);  // elements before this chunk that go second
-    for (int i = b0; i < b1; ++i) {
-        if (key[i] <= Tk) tmp[pos_first++] = idx[i];
-        else tmp[pos_second++] = idx[i];
+    int first = 0;
+    for (int w = 0; w < warp; ++w) first += redi[w];
+    int second = cut + 32 * c0 - first;  // rows before this run that go second
+    for (int c = c0; c < c1; ++c) {
+        const int i = 32 * c + lane;
+        const bool valid = i < len;
+        const bool f = valid && key[i] <= Tk;
+        const unsigned bf = __ballot_sync(0xffffffffu, f), bs = __ballot_sync(0xffffffffu, valid && !f);
+        if (valid) tmp[f ? first + __popc(bf & below) : second + __popc(bs & below)] = idx[i];
+        first += __popc(bf);
+        second += __popc(bs);
     }
     __syncthreads();
     for (int i = threadIdx.x; i < len; i += kGrpThreads) idx[i] = tmp[i];
@@ -344,26 +605,68 @@ __global__ void init_work_kernel(int32_t *__restrict__ work, int N, int64_t tota
     if (i < total) work[i] = static_cast<int32_t>(i % N);
 }
 
+template <typename... KArgs, typename... Args>
+bool pdl_launch(void (*kern)(KArgs...), dim3 grid, int threads, size_t smem, cudaStream_t st, Args... args)
+{
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(static_cast<unsigned>(threads));
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...) == cudaSuccess;
+}
+
+// Largest segment at `level`, in rows: repeated ceil/floor halving of G groups leaves
+// ceil(G / 2^level) groups at most.
+int max_segment_rows(int G, int level) { return ((G + (1 << level) - 1) >> level) * kTokenGroup; }
+
 template <typename T, int D>
 bsa_status launch(const GroupArgs &a, cudaStream_t st)
 {
-    const QueryGroupWs l = query_groups_ws_layout(a.B, a.H, a.N);
+    const QueryGroupWs l = query_groups_ws_layout(a.B, a.H, a.N, a.d);
     int32_t *work = reinterpret_cast<int32_t *>(a.ws + l.work);
     auto *keys = reinterpret_cast<unsigned long long *>(a.ws + l.keys);
     int32_t *scratch = reinterpret_cast<int32_t *>(a.ws + l.scratch);
+    float *psum = reinterpret_cast<float *>(a.ws + l.psum);
+    float *pS = reinterpret_cast<float *>(a.ws + l.pscatter);
+    float *dir = reinterpret_cast<float *>(a.ws + l.dir);
     const int BH = a.B * a.H;
     const int64_t total = static_cast<int64_t>(BH) * a.N;
     init_work_kernel<<<static_cast<unsigned>((total + 255) / 256), 256, 0, st>>>(work, a.N, total);
     const int G = a.N / kTokenGroup;
     int depth = 0;
     while ((1 << depth) < G) ++depth;  // levels until every segment is one group
-    const size_t smem = sizeof(float) * (D * (D + 1) + kStageRows * D);
-    if (cudaFuncSetAttribute(split_level_kernel<T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    const size_t smem = sizeof(float) * D * (D + 8);
+    if (cudaFuncSetAttribute(direction_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem)) != cudaSuccess)
         return BSA_ERR_CUDA;
-    for (int level = 0; level < depth; ++level)
-        split_level_kernel<T, D><<<dim3(1u << level, static_cast<unsigned>(BH)), kGrpThreads, smem, st>>>(
-            static_cast<const T *>(a.Q), a.N, level, work, keys, scratch);
+    const T *X = static_cast<const T *>(a.Q);
+    for (int level = 0; level < depth; ++level) {
+        const int P = (max_segment_rows(G, level) + kSliceRows - 1) / kSliceRows;
+        const int slots = (1 << level) * P;  // <= G with slices of 4 groups: the workspace holds G per head
+        if (slots > G) return BSA_ERR_INVALID_ARG;
+        const dim3 sl(static_cast<unsigned>(slots), static_cast<unsigned>(BH));
+        const dim3 sg(1u << level, static_cast<unsigned>(BH));
+        // programmatic dependent launches (no early trigger: CTAs waiting at
+        // griddepcontrol.wait slow the kernel they wait for): a launch is set up while the
+        // previous kernel runs and its CTAs start as that kernel's complete
+        bool ok = pdl_launch(slice_sum_kernel<T, D>, sl, kGrpThreads, 0, st, X, a.N, level, P, G,
+                             static_cast<const int32_t *>(work), psum);
+        ok = ok && pdl_launch(slice_scatter_kernel<T, D>, sl, kScatThreads, 0, st, X, a.N, level, P, G,
+                              static_cast<const int32_t *>(work), static_cast<const float *>(psum), pS);
+        ok = ok && pdl_launch(direction_kernel<D>, sg, kGrpThreads, smem, st, a.N, level, P, G,
+                              static_cast<const float *>(psum), static_cast<const float *>(pS), dir);
+        ok = ok && pdl_launch(slice_keys_kernel<T, D>, sl, kGrpThreads, 0, st, X, a.N, level, P, G,
+                              static_cast<const int32_t *>(work), static_cast<const float *>(dir), keys);
+        ok = ok && pdl_launch(cut_kernel, sg, kGrpThreads, 0, st, a.N, level, work,
+                              static_cast<const unsigned long long *>(keys), scratch);
+        if (!ok) return BSA_ERR_CUDA;
+    }
     sort_groups_kernel<<<dim3(static_cast<unsigned>(G), static_cast<unsigned>(BH)), kTokenGroup, 0, st>>>(
         work, a.N, a.perm);
     return cudaGetLastError() == cudaSuccess ? BSA_OK : BSA_ERR_CUDA;
@@ -371,14 +674,18 @@ bsa_status launch(const GroupArgs &a, cudaStream_t st)
 
 }  // namespace
 
-QueryGroupWs query_groups_ws_layout(int B, int H, int N)
+QueryGroupWs query_groups_ws_layout(int B, int H, int N, int d)
 {
     const size_t n = static_cast<size_t>(B) * H * N;
+    const size_t slots = static_cast<size_t>(B) * H * (N / kTokenGroup);  // one per group of each head
     QueryGroupWs l{};
     l.work = kWsHeader;
     l.keys = l.work + align_up(n * sizeof(int32_t), 256);
     l.scratch = l.keys + align_up(n * sizeof(unsigned long long), 256);
-    l.total = l.scratch + align_up(n * sizeof(int32_t), 256);
+    l.psum = l.scratch + align_up(n * sizeof(int32_t), 256);
+    l.pscatter = l.psum + align_up(slots * d * sizeof(float), 256);
+    l.dir = l.pscatter + align_up(slots * (static_cast<size_t>(d) * d / 256 * kTriBlocks) * sizeof(float), 256);
+    l.total = l.dir + align_up(slots * 2 * d * sizeof(float), 256);
     return l;
 }
 

@@ -238,14 +238,16 @@ bsa_status bsa_forward_residual(const void *Q, const void *K, const void *V, int
  * rows ascending: group g = perm[(b*H+h)*N + g*128 .. +127] (the layout of
  * bsa_select_tokens and bsa_forward_tokens).
  *
- *   Q           device [B][H][N][d], dtype dt; N a multiple of 128, N/128 <= 512
+ *   Q           device [B][H][N][d], dtype dt; N a multiple of 128, N/128 <= 512, B*H <= 65535
  *   perm        device int32 [B*H][N] (written)
- *   workspace   device, >= bsa_workspace_size(4, ...) bytes, 256-byte aligned
+ *   workspace   device, >= bsa_workspace_size(4, ...) bytes (it depends on d), 256-byte aligned
  * The principal direction comes from fp32 power iteration (32 steps from a fixed start) on
  * the segment's centred scatter matrix, so a row lying within rounding of a median may land
- * on the other side than an exact eigendecomposition would put it. Errors: BSA_ERR_SHAPE,
- * BSA_ERR_DTYPE, BSA_ERR_INVALID_ARG, BSA_ERR_WORKSPACE. Runs on CUDA cores: one launch per
- * level of the split tree, one CTA per (b, h, segment).
+ * on the other side than an exact eigendecomposition would put it. Every sum runs in a
+ * fixed order: the same Q gives the same groups. Errors: BSA_ERR_SHAPE, BSA_ERR_DTYPE,
+ * BSA_ERR_INVALID_ARG, BSA_ERR_WORKSPACE. Runs on CUDA cores, the split tree level by level:
+ * the row sums, scatter matrices and projections over slices of at most 512 rows of each
+ * segment, the power iteration and the cut over one CTA per segment.
  */
 bsa_status bsa_query_groups(const void *Q, int dt, int B, int H, int N, int d, int32_t *perm, void *workspace,
                             size_t workspace_bytes, void *stream);

@@ -235,9 +235,14 @@ def test_token_selection_workspace_and_arguments(lib):
 
 def test_query_groups_workspace_and_arguments(lib):
     up = lambda x: (x + 255) // 256 * 256  # noqa: E731
-    n = 2 * 3 * 1024
-    # working permutation, 64-bit (projection, row) keys, scratch copy
-    assert bb.bsa_workspace_size(4, 2, 3, 1024, 64, 64) == 256 + up(n * 4) + up(n * 8) + up(n * 4)
+    for d in (64, 128):
+        n = 2 * 3 * 1024
+        slots = 2 * 3 * (1024 // 128)  # one per group of each head
+        # working permutation, 64-bit (projection, row) keys, scratch copy; per slot a slice's
+        # row sum, its scatter blocks (136 of (d/16)^2 entries), a segment's mean and direction
+        want = (256 + up(n * 4) + up(n * 8) + up(n * 4) + up(slots * d * 4)
+                + up(slots * (d * d // 256 * 136) * 4) + up(slots * 2 * d * 4))
+        assert bb.bsa_workspace_size(4, 2, 3, 1024, d, 64) == want
 
     def grp(**kw):
         args = dict(Q=FAKE, dt=bb.BF16, B=1, H=2, N=512, d=64, perm=FAKE, ws=FAKE, ws_bytes=1 << 30)
@@ -249,6 +254,7 @@ def test_query_groups_workspace_and_arguments(lib):
     assert grp(N=500) == bb.ERR_SHAPE
     assert grp(N=128 * 513) == bb.ERR_SHAPE  # at most 512 groups per head
     assert grp(d=32) == bb.ERR_SHAPE
+    assert grp(B=300, H=300) == bb.ERR_SHAPE  # one grid row per head
     assert grp(dt=2) == bb.ERR_DTYPE
     assert grp(perm=None) == bb.ERR_INVALID_ARG
     assert grp(ws_bytes=1024) == bb.ERR_WORKSPACE
