@@ -41,12 +41,13 @@ EXPORTS = ("bsa_build_mask", "bsa_forward", "bsa_mask_nnz", "bsa_workspace_size"
            "bsa_check_device_error", "bsa_validate_index", "bsa_debug_config",
            "bsa_status_string", "bsa_build_mask_noalloc", "bsa_residual_capture", "bsa_forward_residual",
            "bsa_build_mask_modal", "bsa_mask_nnz_modal", "bsa_build_mask_exact", "bsa_forward_tokens",
-           "bsa_select_tokens", "bsa_query_groups", "bsa_tokens_per_group")
+           "bsa_select_tokens", "bsa_query_groups", "bsa_tokens_per_group", "bsa_forward_plan")
 NOALLOC_SCRATCH_BYTES = 16 << 20  # BSA_NOALLOC_SCRATCH_BYTES
 # bsa_debug_config flag bits
 DBG_STALL = 1       # skip loads and MMAs: the first device wait runs out
 DBG_NO_SPLIT = 2    # never split a query tile over several CTAs
 DBG_SPLIT_ALL = 4   # split every tile with two or more steps (within the partial budget)
+INDEX_PLANNED = 0x100  # BSA_INDEX_PLANNED: index_mode flag, reuse the work list of bsa_forward_plan
 
 
 class StaticSpec(ctypes.Structure):
@@ -80,6 +81,7 @@ def load():
                                    SZ, P]
     lib.bsa_forward.argtypes = [P, P, P, I, I, I, I, I, I, P, P, P, I, F, P, P, P, SZ, P]
     lib.bsa_forward_residual.argtypes = [P, P, P, I, I, I, I, I, I, P, P, P, I, F, P, P, P, P, SZ, P]
+    lib.bsa_forward_plan.argtypes = [I, I, I, I, I, I, P, P, P, I, P, SZ, P]
     lib.bsa_residual_capture.argtypes = [P, P, I, I64, P, P]
     lib.bsa_forward_tokens.argtypes = [P, P, P, I, I, I, I, I, P, P, I, F, P, P, P, SZ, P]
     lib.bsa_select_tokens.argtypes = [P, P, I, I, I, I, I, P, P, F, F, P, I64, P, SZ, P]
@@ -148,6 +150,13 @@ def bsa_forward(Q, K, V, dt: int, B: int, H: int, N: int, d: int, block: int, ro
                               _ptr(bitmap), int(index_mode), float(scale), _ptr(O), _ptr(LSE),
                               _ptr(workspace), int(workspace_bytes), _stream(stream))
     _check(code, "bsa_forward")
+
+
+def bsa_forward_plan(dt: int, B: int, H: int, N: int, d: int, block: int, row_ptr, col_idx, bitmap,
+                     index_mode: int, workspace, workspace_bytes: int, stream=None) -> None:
+    code = load().bsa_forward_plan(dt, B, H, N, d, block, _ptr(row_ptr), _ptr(col_idx), _ptr(bitmap),
+                                   int(index_mode), _ptr(workspace), int(workspace_bytes), _stream(stream))
+    _check(code, "bsa_forward_plan")
 
 
 def bsa_forward_residual(Q, K, V, dt: int, B: int, H: int, N: int, d: int, block: int, row_ptr, col_idx,
@@ -397,6 +406,18 @@ def forward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, index: Index, ind
     if check:
         _check(bsa_check_device_error(ws, stream), "bsa_forward (device)")
     return out, lse
+
+
+def forward_plan(q: torch.Tensor, index: Index, index_mode: int = 0, ws: Optional[torch.Tensor] = None,
+                 stream=None) -> torch.Tensor:
+    """Run bsa_forward_plan into `ws` (allocated when None); returns the workspace to pass to
+    forward(..., index_mode=index_mode | INDEX_PLANNED, ws=ws)."""
+    B, H, N, d = q.shape
+    if ws is None:
+        ws = workspace(1, B, H, N, d, index.block, q.device)
+    bsa_forward_plan(_dtype_code(q), B, H, N, d, index.block, index.row_ptr, index.col_idx, index.bitmap,
+                     index_mode, ws, ws.numel(), stream)
+    return ws
 
 
 def residual_capture(o_dense: torch.Tensor, o_sparse: torch.Tensor, out: Optional[torch.Tensor] = None,

@@ -15,6 +15,14 @@ uint64_t g_wait_limit_ns = bsa::kDefaultWaitNs;
 
 bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+// index_mode 0 reads the CSR arrays, 1 the bitmap
+bool index_args_ok(const int32_t *row_ptr, const int32_t *col_idx, const uint32_t *bitmap, int index_mode)
+{
+    if (index_mode == 0) return row_ptr && col_idx;
+    if (index_mode == 1) return bitmap != nullptr;
+    return false;
+}
+
 // Blocks per row or column; a sequence that is not a multiple of the block size ends in a
 // ragged block ("多模态DiT中的块稀疏注意力" §4.1: the tile loop masks the padding).
 int n_blocks(int N, int block) { return (N + block - 1) / block; }
@@ -362,13 +370,9 @@ static bsa_status forward_impl(const void *Q, const void *K, const void *V, int 
     if (!Q || !K || !V || !O || !LSE) return BSA_ERR_INVALID_ARG;
     if (!aligned(Q, 16) || !aligned(K, 16) || !aligned(V, 16) || !aligned(O, 16) || !aligned(LSE, 4))
         return BSA_ERR_INVALID_ARG;
-    if (index_mode == 0) {
-        if (!row_ptr || !col_idx) return BSA_ERR_INVALID_ARG;
-    } else if (index_mode == 1) {
-        if (!bitmap) return BSA_ERR_INVALID_ARG;
-    } else {
-        return BSA_ERR_INVALID_ARG;
-    }
+    const bool planned = (index_mode & BSA_INDEX_PLANNED) != 0;
+    index_mode &= ~BSA_INDEX_PLANNED;
+    if (!index_args_ok(row_ptr, col_idx, bitmap, index_mode)) return BSA_ERR_INVALID_ARG;
     if (std::isnan(scale) || std::isinf(scale)) return BSA_ERR_INVALID_ARG;
     if (!workspace || !aligned(workspace, 256) || workspace_bytes < bsa::fwd_workspace_bytes(B, H, N, d, block))
         return BSA_ERR_WORKSPACE;
@@ -396,8 +400,40 @@ static bsa_status forward_impl(const void *Q, const void *K, const void *V, int 
     a.ws = static_cast<char *>(workspace);
     a.dbg_flags = g_dbg_flags;
     a.wait_limit_ns = g_wait_limit_ns;
+    a.planned = planned ? 1 : 0;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     return dt == BSA_BF16 ? bsa::launch_forward_tc(a, st) : bsa::launch_forward_simt(a, st);
+}
+
+bsa_status bsa_forward_plan(int dt, int B, int H, int N, int d, int block, const int32_t *row_ptr,
+                            const int32_t *col_idx, const uint32_t *bitmap, int index_mode, void *workspace,
+                            size_t workspace_bytes, void *stream)
+{
+    bsa_status s = check_shape(B, H, N, d, block);
+    if (s != BSA_OK) return s;
+    if (dt != BSA_BF16 && dt != BSA_FP32) return BSA_ERR_DTYPE;
+    if (!index_args_ok(row_ptr, col_idx, bitmap, index_mode)) return BSA_ERR_INVALID_ARG;
+    if (!workspace || !aligned(workspace, 256) || workspace_bytes < bsa::fwd_workspace_bytes(B, H, N, d, block))
+        return BSA_ERR_WORKSPACE;
+    if (dt == BSA_FP32) return BSA_OK;  // the CUDA-core forward keeps no work list
+    bsa::FwdArgs a{};
+    a.dt = dt;
+    a.B = B;
+    a.H = H;
+    a.N = N;
+    a.d = d;
+    a.block = block;
+    a.nQB = n_blocks(N, block);
+    a.nKB = n_blocks(N, block);
+    a.W = (a.nKB + 31) / 32;
+    a.row_ptr = row_ptr;
+    a.col_idx = col_idx;
+    a.bitmap = bitmap;
+    a.index_mode = index_mode;
+    a.ws = static_cast<char *>(workspace);
+    a.dbg_flags = g_dbg_flags;
+    a.wait_limit_ns = g_wait_limit_ns;
+    return bsa::launch_forward_plan_tc(a, static_cast<cudaStream_t>(stream));
 }
 
 bsa_status bsa_forward(const void *Q, const void *K, const void *V, int dt, int B, int H, int N, int d, int block,

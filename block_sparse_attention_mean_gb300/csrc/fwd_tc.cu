@@ -1196,7 +1196,8 @@ __global__ void __launch_bounds__((4 * SPLIT + 4) * 32, MINB)
             int last_issue = -1;  // last step whose K loads were issued
             int q_issued = -1;
             bool ok = true;
-            const uint32_t n_items = *p.n_items;  // written by the tile-order launch before this one
+            // written by the tile-order launch before this one (or the plan gate of a planned call)
+            const uint32_t n_items = *p.n_items;
             while (ok) {
                 const int slot = tcount & 1;
                 if (tcount >= 2 && !warp_wait_all(bar(C::B_TEMPTY + slot), ((tcount >> 1) - 1) & 1, ctl)) break;
@@ -1650,6 +1651,7 @@ struct OrderArgs {
     int32_t *items, *lens, *split_base;
     uint32_t *merge_cnt;
     WsHeader *hdr;
+    uint32_t plan_sig;      // signature of the configuration (stamped into the header)
 };
 
 // Work list for one forward launch, in one launch: every CTA computes the step
@@ -1844,6 +1846,8 @@ __global__ void __launch_bounds__(1024) tile_order_kernel(TcParams p, OrderArgs 
         o.hdr->max_len = 0u;
         o.hdr->min_len_c = 0u;
         *p.tile_counter = 0u;
+        o.hdr->run_items = static_cast<uint32_t>(n_items);
+        o.hdr->plan_sig = o.plan_sig;
         o.hdr->order_done = 0u;
     }
 }
@@ -1972,6 +1976,23 @@ __global__ void __launch_bounds__(1024) tile_order_small_kernel(TcParams p, Orde
         o.hdr->n_items = static_cast<uint32_t>(n_items);
         o.hdr->chunk_steps = static_cast<uint32_t>(T);
         *p.tile_counter = 0u;
+        o.hdr->run_items = static_cast<uint32_t>(n_items);
+        o.hdr->plan_sig = o.plan_sig;
+    }
+}
+
+// Before a forward on a work list made by an earlier launch: the list runs only if it was
+// made for this configuration (else BSA_ERR_INVALID_ARG and nothing runs), and the
+// scheduler and merge counters start from zero again.
+__global__ void __launch_bounds__(256) plan_gate_kernel(WsHeader *hdr, uint32_t sig, uint32_t *merge_cnt, int n_merge)
+{
+    grid_launch_dependents();  // the forward's prologue may start now (it waits for this grid's results)
+    for (int i = threadIdx.x; i < n_merge; i += blockDim.x) merge_cnt[i] = 0u;
+    if (threadIdx.x == 0) {
+        const bool ok = hdr->plan_sig == sig;
+        hdr->run_items = ok ? hdr->n_items : 0u;
+        hdr->tile_counter = 0u;
+        if (!ok) raise_error(&hdr->err, BSA_ERR_INVALID_ARG);
     }
 }
 
@@ -2047,8 +2068,25 @@ bsa_status forward_grid_cap(int &cap)
     return BSA_OK;
 }
 
+// Signature of the configuration a work list is made for: the launch shape and every input
+// of the ordering except the index contents (never 0, so a zeroed header matches nothing).
+uint32_t plan_signature(int n_tiles, int grid, int index_mode, int D, int BS, int budget, uint32_t dbg, int N, int BH)
+{
+    uint32_t h = 0x811C9DC5u;
+    const uint32_t v[8] = {static_cast<uint32_t>(n_tiles), static_cast<uint32_t>(grid),
+                           static_cast<uint32_t>(index_mode), static_cast<uint32_t>(D | (BS << 8)),
+                           static_cast<uint32_t>(budget), dbg & (kDbgNoSplit | kDbgSplitAll),
+                           static_cast<uint32_t>(N), static_cast<uint32_t>(BH)};
+    for (uint32_t x : v)
+        for (int b = 0; b < 4; ++b) h = (h ^ ((x >> (8 * b)) & 0xFFu)) * 0x01000193u;
+    return h | 1u;
+}
+
+// mode: kRunOrderAndForward, kRunForward (a plan is in the workspace), kRunOrder (make the plan)
+enum { kRunOrderAndForward = 0, kRunForward = 1, kRunOrder = 2 };
+
 template <int D, int BS, int NK, int NV, int NSB, int QS, int SPLIT, int PAIR, int MINB>
-bsa_status launch_tc(const FwdArgs &a, cudaStream_t st)
+bsa_status launch_tc(const FwdArgs &a, cudaStream_t st, int mode)
 {
     using C = Cfg<D, BS, NK, NV, NSB, QS, PAIR>;
     constexpr int kThreads = Roles<SPLIT>::kThreads;
@@ -2090,7 +2128,7 @@ bsa_status launch_tc(const FwdArgs &a, cudaStream_t st)
     o.merge_cnt = reinterpret_cast<uint32_t *>(a.ws + lay.merge_cnt);
     o.hdr = hdr;
     p.tile_list = o.items;
-    p.n_items = &hdr->n_items;
+    p.n_items = &hdr->run_items;  // the items this launch runs (the order kernel or the plan gate sets it)
     p.split_ok = lay.budget > 0 ? 1 : 0;
     p.split_base = o.split_base;
     p.merge_cnt = o.merge_cnt;
@@ -2105,6 +2143,8 @@ bsa_status launch_tc(const FwdArgs &a, cudaStream_t st)
     const int64_t max_items = static_cast<int64_t>(p.n_tiles) + static_cast<int64_t>(lay.budget);
     const int grid = static_cast<int>(max_items < grid_cap ? max_items : grid_cap);
     o.grid = grid;
+    o.plan_sig = plan_signature(p.n_tiles, grid, p.index_mode, D, BS, static_cast<int>(lay.budget), p.dbg, a.N,
+                                static_cast<int>(BH));
     static bool order_smem_set = false;
     if (!order_smem_set) {
         if (cudaFuncSetAttribute(tile_order_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -2114,10 +2154,16 @@ bsa_status launch_tc(const FwdArgs &a, cudaStream_t st)
             return BSA_ERR_CUDA;
         order_smem_set = true;
     }
-    if (p.index_mode == 0 && p.n_tiles <= 1024 * kOrderPerThread)
-        tile_order_small_kernel<<<1, 1024, kOrderTableBytes, st>>>(p, o);
-    else
-        tile_order_kernel<<<(p.n_tiles + 1023) / 1024, 1024, kOrderTableBytes, st>>>(p, o);
+    if (mode != kRunForward) {
+        if (p.index_mode == 0 && p.n_tiles <= 1024 * kOrderPerThread)
+            tile_order_small_kernel<<<1, 1024, kOrderTableBytes, st>>>(p, o);
+        else
+            tile_order_kernel<<<(p.n_tiles + 1023) / 1024, 1024, kOrderTableBytes, st>>>(p, o);
+    } else {
+        plan_gate_kernel<<<1, 256, 0, st>>>(hdr, o.plan_sig, o.merge_cnt,
+                                            static_cast<int>(lay.budget) * kMergeWarps);
+    }
+    if (mode == kRunOrder) return cudaGetLastError() == cudaSuccess ? BSA_OK : BSA_ERR_CUDA;
     // programmatic dependent launch: the forward's CTAs set up barriers and TMEM while the
     // work-list launch runs, and wait for its results in-kernel
     cudaLaunchConfig_t cfg{};
@@ -2192,14 +2238,24 @@ size_t fwd_workspace_bytes(int B, int H, int N, int d, int block)
     return fwd_layout(B, H, N, d).bytes;
 }
 
-bsa_status launch_forward_tc(const FwdArgs &a, cudaStream_t st)
+static bsa_status launch_forward_mode(const FwdArgs &a, cudaStream_t st, int mode)
 {
     // <D, BS, K stages, V stages, S/P buffers, Q slots, threads per row, blocks per step, CTAs per SM>
-    if (a.d == 64 && a.block == 64) return launch_tc<64, 64, 4, 5, 3, 2, 1, 1, 2>(a, st);
-    if (a.d == 128 && a.block == 64) return launch_tc<128, 64, 2, 2, 2, 1, 1, 1, 2>(a, st);
-    if (a.d == 64 && a.block == 128) return launch_tc<64, 128, 5, 6, 3, 2, 2, 1, 1>(a, st);
-    if (a.d == 128 && a.block == 128) return launch_tc<128, 128, 2, 4, 3, 1, 2, 1, 1>(a, st);
+    if (a.d == 64 && a.block == 64) return launch_tc<64, 64, 4, 5, 3, 2, 1, 1, 2>(a, st, mode);
+    if (a.d == 128 && a.block == 64) return launch_tc<128, 64, 2, 2, 2, 1, 1, 1, 2>(a, st, mode);
+    if (a.d == 64 && a.block == 128) return launch_tc<64, 128, 5, 6, 3, 2, 2, 1, 1>(a, st, mode);
+    if (a.d == 128 && a.block == 128) return launch_tc<128, 128, 2, 4, 3, 1, 2, 1, 1>(a, st, mode);
     return BSA_ERR_SHAPE;
+}
+
+bsa_status launch_forward_tc(const FwdArgs &a, cudaStream_t st)
+{
+    return launch_forward_mode(a, st, a.planned ? kRunForward : kRunOrderAndForward);
+}
+
+bsa_status launch_forward_plan_tc(const FwdArgs &a, cudaStream_t st)
+{
+    return launch_forward_mode(a, st, kRunOrder);
 }
 
 // ---------------------------------------------------------------- TMA descriptors

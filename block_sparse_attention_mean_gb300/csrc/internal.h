@@ -22,7 +22,9 @@ struct WsHeader {
     uint32_t chunk_steps;  // forward: the per-CTA share of steps (chunk length of split tiles)
     uint32_t max_len;      // forward: longest tile (tile order, then cleared)
     uint32_t min_len_c;    // forward: ~(shortest tile) (tile order, then cleared)
-    uint32_t pad[55];
+    uint32_t plan_sig;     // forward: signature of the configuration the work list was made for
+    uint32_t run_items;    // forward: items the next forward launch runs (n_items, or 0 for a bad plan)
+    uint32_t pad[53];
 };
 static_assert(sizeof(WsHeader) == 256, "workspace header size");
 static_assert(sizeof(WsHeader) == 256, "workspace header is 256 bytes");
@@ -104,6 +106,7 @@ struct FwdArgs {
     char *ws;
     uint32_t dbg_flags;
     uint64_t wait_limit_ns;
+    int planned;           // the work list is already in the workspace (bsa_forward_plan)
 };
 
 size_t fwd_workspace_bytes(int B, int H, int N, int d, int block);
@@ -111,6 +114,7 @@ size_t fwd_workspace_bytes(int B, int H, int N, int d, int block);
 // rows at or past n (a ragged last block) read as zeros
 bool make_tma_map_bf16(CUtensorMap *m, const void *base, uint64_t heads, uint64_t n, int d, int box_rows);
 bsa_status launch_forward_tc(const FwdArgs &a, cudaStream_t st);    // bf16, tcgen05
+bsa_status launch_forward_plan_tc(const FwdArgs &a, cudaStream_t st);  // bf16: the work list only
 bsa_status launch_forward_simt(const FwdArgs &a, cudaStream_t st);  // fp32, CUDA cores
 bsa_status launch_residual_capture(const void *dense, const void *sparse, int dt, int64_t count, float *R,
                                    cudaStream_t st);

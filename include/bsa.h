@@ -171,6 +171,10 @@ bsa_status bsa_build_mask_exact(const void *Q, const void *K, int dt, int B, int
                                 uint32_t *bitmap, void *workspace, size_t workspace_bytes,
                                 void *stream);
 
+/* index_mode flag of bsa_forward / bsa_forward_residual: reuse the work list already in
+ * the workspace (bsa_forward_plan) instead of building it in the call. */
+#define BSA_INDEX_PLANNED 0x100
+
 /*
  * bsa_forward -- block-sparse FlashAttention forward ([P1] §4.1 tile loop with the
  * inner KV loop replaced by the active list, §4.3 skipped blocks count as -inf and
@@ -184,18 +188,44 @@ bsa_status bsa_build_mask_exact(const void *Q, const void *K, int dt, int B, int
  *   Q, K, V     device [B][H][N][d], dtype dt
  *   row_ptr, col_idx   CSR index (read when index_mode == 0)
  *   bitmap      bitmap index (read when index_mode == 1); unused pointers may be NULL
- *   index_mode  0: CSR, 1: bitmap + popcount ([P1] §4.1)
+ *   index_mode  0: CSR, 1: bitmap + popcount ([P1] §4.1); either may carry
+ *               BSA_INDEX_PLANNED (see bsa_forward_plan)
  *   scale       softmax scale; <= 0 selects 1/sqrt(d)
  *   O           device [B][H][N][d], dtype dt (written)
  *   LSE         device fp32 [B][H][N] (written)
  *   workspace   device, >= bsa_workspace_size(1, ...) bytes, 256-byte aligned
  * The index must be well formed (row_ptr non-decreasing from 0, col_idx strictly
  * ascending in [0, nKB)); bsa_validate_index checks one on the device.
+ * bf16 runs as two launches on `stream`: the work list (query tiles longest first,
+ * long tiles split by KV range, [P1] §5.3) into the workspace, then the tcgen05
+ * kernel. With BSA_INDEX_PLANNED the first is replaced by a one-CTA launch that checks
+ * the work list an earlier bsa_forward_plan (or bsa_forward) left in the workspace
+ * against this call and resets the scheduler's counters.
  */
 bsa_status bsa_forward(const void *Q, const void *K, const void *V, int dt, int B, int H, int N,
                        int d, int block, const int32_t *row_ptr, const int32_t *col_idx,
                        const uint32_t *bitmap, int index_mode, float scale, void *O, float *LSE,
                        void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * bsa_forward_plan -- the forward's work list for one index, made once into the forward
+ * workspace, for a mask used by many calls ([P1] §5.3: static masks are pre-generated
+ * once). The list depends on the index's row lengths and the launch shape, not on Q, K,
+ * V: it stays valid for bsa_forward / bsa_forward_residual calls with index_mode |
+ * BSA_INDEX_PLANNED, the same dt, B, H, N, d, block, index_mode and workspace, while
+ * every query tile's row lengths are those of the planned index (a static mask rebuilt
+ * into the same buffers, or any plain top-k mask of the same shape and density). A
+ * planned call whose workspace holds no plan for its shape raises BSA_ERR_INVALID_ARG
+ * on the device and writes nothing. Each planned call resets the counters it uses, so
+ * one plan serves any number of calls in stream order.
+ *   row_ptr, col_idx, bitmap, index_mode   as bsa_forward (index_mode 0 or 1)
+ *   workspace   device, >= bsa_workspace_size(1, ...) bytes, 256-byte aligned
+ * One launch (none for BSA_FP32, whose CUDA-core forward keeps no work list).
+ * Errors: BSA_ERR_SHAPE, BSA_ERR_DTYPE, BSA_ERR_INVALID_ARG, BSA_ERR_WORKSPACE.
+ */
+bsa_status bsa_forward_plan(int dt, int B, int H, int N, int d, int block, const int32_t *row_ptr,
+                            const int32_t *col_idx, const uint32_t *bitmap, int index_mode,
+                            void *workspace, size_t workspace_bytes, void *stream);
 
 /*
  * Residual compensation ([P3] section "残差补偿找回被丢弃的尾部"; reuse across steps:

@@ -339,6 +339,83 @@ def test_modal_builder_without_text_is_the_plain_selector():
     assert torch.equal(plain.bitmap, modal.bitmap)
 
 
+# ------------------------------------------------------------ planned work list
+#
+# bsa_forward_plan makes the forward's work list once; bsa_forward with BSA_INDEX_PLANNED
+# reuses it. Planned calls must equal the unplanned call bit for bit, call after call (the
+# forward resets its scheduler and merge counters itself), with and without split tiles.
+
+PLAN_CASES = {
+    "t2i_csr": (wl.scaled(wl.WORKLOADS["t2i_static"], B=1, H=4), 0),
+    "video_bitmap": (wl.scaled(wl.WORKLOADS["video_cuboid"], H=2), 1),
+    "dynamic_csr": (wl.scaled(wl.WORKLOADS["dynamic_topk"], H=3, N=4096), 0),
+    "long_bitmap": (wl.scaled(wl.WORKLOADS["long_topk"], H=2, N=8192), 1),
+}
+
+
+@pytest.mark.parametrize("flags", [0, bb.DBG_SPLIT_ALL])
+@pytest.mark.parametrize("name", sorted(PLAN_CASES))
+def test_planned_forward_equals_unplanned(name, flags):
+    w, mode = PLAN_CASES[name]
+    inp = wl.make_inputs(w)
+    q, k, v = (gu.upload(inp, n) for n in ("q", "k", "v"))
+    mask = gu.oracle_mask(w, inp)
+    idx = gu.device_index(w, q, k, mask)
+    bb.bsa_debug_config(flags, 0)
+    try:
+        O0, L0 = bb.forward(q, k, v, idx, index_mode=mode)
+        ws = bb.forward_plan(q, idx, index_mode=mode)
+        outs = [bb.forward(q, k, v, idx, index_mode=mode | bb.INDEX_PLANNED, ws=ws) for _ in range(3)]
+        split_items = int(ws[12:16].view(torch.int32).item())  # n_items in the header
+    finally:
+        bb.bsa_debug_config(0, 0)
+    torch.cuda.synchronize()
+    if flags:
+        assert split_items > w.B * w.H * (-(-w.N // 128))  # the plan holds chunks of split tiles
+    for O, L in outs:
+        assert torch.equal(O, O0)
+        assert torch.equal(L, L0)
+    gu.assert_attention_close(O0, L0, inp, mask, w)
+
+
+def test_planned_residual_forward_equals_unplanned():
+    w = wl.scaled(wl.WORKLOADS["t2i_static"], B=1, H=2)
+    inp = wl.make_inputs(w)
+    q, k, v = (gu.upload(inp, n) for n in ("q", "k", "v"))
+    idx = gu.device_index(w, q, k, gu.oracle_mask(w, inp))
+    R = torch.randn(q.shape, dtype=torch.float32, device="cuda") * 0.01
+    O0, L0 = bb.forward(q, k, v, idx, residual=R)
+    ws = bb.forward_plan(q, idx)
+    for _ in range(2):
+        O, L = bb.forward(q, k, v, idx, index_mode=bb.INDEX_PLANNED, ws=ws, residual=R)
+        torch.cuda.synchronize()
+        assert torch.equal(O, O0)
+        assert torch.equal(L, L0)
+
+
+def test_planned_forward_needs_its_own_plan():
+    w = wl.scaled(wl.WORKLOADS["dynamic_topk"], H=2, N=2048)
+    inp = wl.make_inputs(w)
+    q, k, v = (gu.upload(inp, n) for n in ("q", "k", "v"))
+    mask = gu.oracle_mask(w, inp)
+    idx = gu.device_index(w, q, k, mask)
+    ws = bb.workspace(1, w.B, w.H, w.N, w.d, w.block)
+    # no plan in a fresh workspace: an argument error raised on the device, nothing run
+    bb.forward(q, k, v, idx, index_mode=bb.INDEX_PLANNED, ws=ws, check=False)
+    assert bb.bsa_check_device_error(ws) == bb.ERR_INVALID_ARG
+    # a plan for the bitmap index is not a plan for the CSR one
+    bb.forward_plan(q, idx, index_mode=1, ws=ws)
+    bb.forward(q, k, v, idx, index_mode=0 | bb.INDEX_PLANNED, ws=ws, check=False)
+    assert bb.bsa_check_device_error(ws) == bb.ERR_INVALID_ARG
+    # the matching plan runs, and an unplanned call leaves a usable plan too
+    bb.forward_plan(q, idx, index_mode=0, ws=ws)
+    O, L = bb.forward(q, k, v, idx, index_mode=bb.INDEX_PLANNED, ws=ws)
+    gu.assert_attention_close(O, L, inp, mask, w)
+    bb.forward(q, k, v, idx, index_mode=1, ws=ws)
+    O, L = bb.forward(q, k, v, idx, index_mode=1 | bb.INDEX_PLANNED, ws=ws)
+    gu.assert_attention_close(O, L, inp, mask, w)
+
+
 # ------------------------------------------------------------ block-oracle selector
 #
 # [P3] section "质量差距有三个可分离来源": keep the blocks with the most exact attention

@@ -25,7 +25,7 @@ def _header_functions():
 
 def test_header_symbols_exported(lib):
     names = _header_functions()
-    assert len(names) == 18
+    assert len(names) == 19
     assert sorted(bb.EXPORTS) == names
     for n in names:
         assert getattr(lib, n) is not None  # dlsym succeeds
@@ -165,6 +165,35 @@ def test_forward_rejects_bad_arguments(lib):
     assert _fwd(scale=float("inf")) == bb.ERR_INVALID_ARG
     assert _fwd(workspace_bytes=100) == bb.ERR_WORKSPACE
     assert _fwd(B=0) == bb.ERR_SHAPE
+    # the planned flag rides on either index mode and is checked with it
+    assert _fwd(index_mode=2 | bb.INDEX_PLANNED) == bb.ERR_INVALID_ARG
+    assert _fwd(index_mode=1 | bb.INDEX_PLANNED, bitmap=None) == bb.ERR_INVALID_ARG
+    assert _fwd(index_mode=0 | bb.INDEX_PLANNED, row_ptr=None) == bb.ERR_INVALID_ARG
+
+
+def _plan(**kw):
+    args = dict(dt=bb.BF16, B=1, H=2, N=512, d=64, block=64, row_ptr=FAKE, col_idx=FAKE, bitmap=FAKE,
+                index_mode=0, workspace=FAKE, workspace_bytes=1 << 30)
+    args.update(kw)
+    with pytest.raises(bb.BsaError) as e:
+        bb.bsa_forward_plan(**args, stream=0)
+    return e.value.code
+
+
+def test_forward_plan_rejects_bad_arguments(lib):
+    assert _plan(N=0) == bb.ERR_SHAPE
+    assert _plan(d=96) == bb.ERR_SHAPE
+    assert _plan(block=32) == bb.ERR_SHAPE
+    assert _plan(dt=3) == bb.ERR_DTYPE
+    assert _plan(index_mode=2) == bb.ERR_INVALID_ARG
+    assert _plan(index_mode=bb.INDEX_PLANNED) == bb.ERR_INVALID_ARG  # a plan takes a plain index mode
+    assert _plan(index_mode=0, col_idx=None) == bb.ERR_INVALID_ARG
+    assert _plan(index_mode=1, bitmap=None) == bb.ERR_INVALID_ARG
+    assert _plan(workspace=None) == bb.ERR_WORKSPACE
+    assert _plan(workspace=FAKE + 16) == bb.ERR_WORKSPACE
+    assert _plan(workspace_bytes=100) == bb.ERR_WORKSPACE
+    # fp32 keeps no work list: a valid call launches nothing and succeeds without a device
+    bb.bsa_forward_plan(bb.FP32, 1, 2, 512, 64, 64, FAKE, FAKE, FAKE, 0, FAKE, 1 << 30, stream=0)
 
 
 def test_validate_index_rejects_bad_arguments(lib):
