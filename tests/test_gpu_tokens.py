@@ -269,6 +269,17 @@ def test_query_groups_partition_and_quality(name):
         assert _sse(qf[h], got[h]) <= 1.01 * _sse(qf[h], ref)
 
 
+def test_query_groups_repeat_run_to_run():
+    # every sum of the grouping runs in a fixed order (slices in order, blocks in order), so
+    # the same queries give the same groups on every call, at a size with several slices
+    # per segment on the top levels
+    w = wl.scaled(wl.WORKLOADS["dynamic_topk"], H=4)
+    q = gu.upload(wl.make_inputs(w), "q")
+    first = bb.query_groups(q)
+    for _ in range(2):
+        assert torch.equal(bb.query_groups(q), first)
+
+
 def test_token_path_end_to_end_on_the_gpu():
     # groups, dense LSE, selection and the token forward all on the GPU; the forward checked
     # against the oracle's token attention over the GPU's own groups and tokens
