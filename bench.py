@@ -16,6 +16,8 @@ its fraction of the measured dense bf16 tensor peak.
 Timing: W warm-up steps, a short clock-settling phase, then exactly K timed
 steps, each replayed from CUDA graphs and bracketed by CUDA events on the
 launching stream; L2 is flushed (256 MB write) before every timed step.
+The end-to-end figure copies each step's inputs in from pinned host memory and its
+outputs out inside the timed region, overlapped by chunks of heads on three streams.
 --impl reference times the CPU oracle (test infrastructure, double precision)
 on a bounded sample of the same workload.
 """
@@ -55,6 +57,9 @@ def parse_args():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(wl.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--e2e-chunks", type=int, default=0,
+                    help="end-to-end: heads in this many chunks, copy-in / compute / copy-out overlapped "
+                         "(0: about 128 MB of copies per chunk)")
     ap.add_argument("--tokens", type=float, default=0.0,
                     help="time the token-sparse forward (bsa_forward_tokens) at this token density instead: "
                          "groups of 128 queries and K = floor(density * N) tokens per group, both seeded random")
@@ -404,33 +409,87 @@ def run_ours(args, world, rank, local):
     ms_per_step = total_ms / args.steps
     value = job_throughput(flops, world, args.steps, total_ms)
 
-    # end to end through the C ABI from pinned host buffers
+    # end to end through the C ABI from pinned host buffers. Heads are independent, so the step
+    # runs in chunks of heads on three streams: chunk c + 1 is copied in while chunk c is
+    # computed (mask build + forward, the same calls on the chunk's heads) and chunk c - 1 is
+    # copied out. Copies in and out share the host link (about 210 GB/s each way on this machine).
     e2e = None
     if args.e2e_steps > 0:
+        BHt = B * H
+        moved = sum(t.numel() * t.element_size() for t in (q, k, v, O, LSE))
+        C = args.e2e_chunks if args.e2e_chunks > 0 else max(1, moved // (128 << 20))
+        while C > 1 and BHt % C != 0:
+            C -= 1  # whole heads per chunk
+        if spec is not None and spec.kind == bb.STATIC_EXPLICIT:
+            C = 1  # a per-head explicit bitmap is not split by head here
+        hc = BHt // C
         hq, hk, hv = (t.cpu().pin_memory() for t in (q, k, v))
         hO = torch.empty(O.shape, dtype=O.dtype).pin_memory()
         hL = torch.empty(LSE.shape, dtype=LSE.dtype).pin_memory()
+        flat = lambda t: t.reshape(BHt, N, -1) if t.dim() == 4 else t.reshape(BHt, N)  # noqa: E731
+        dq, dk, dv, dO, dL = flat(q), flat(k), flat(v), flat(O), flat(LSE)
+        sq, sk, sv, sO, sL = flat(hq), flat(hk), flat(hv), flat(hO), flat(hL)
+        cap_c = bb.bsa_mask_nnz(1, hc, N, bs, w.density, spec)
+        rp_c = torch.empty(hc * nB + 1, dtype=torch.int32, device=dev)
+        ci_c = torch.empty(max(cap_c, 1), dtype=torch.int32, device=dev)
+        bm_c = torch.empty(hc * nB * W, dtype=torch.int32, device=dev)
+        wsm_c = bb.workspace(0, 1, hc, N, d, bs, dev)
+        wsf_c = bb.workspace(1, 1, hc, N, d, bs, dev)
+        s_in, s_cmp, s_out = (torch.cuda.Stream(device=dev) for _ in range(3))
+        mode_c = w.index_mode
+        if planned:  # a static mask is the same for every head: one plan serves every chunk
+            bb.bsa_build_mask(None, None, dt, 1, hc, N, d, bs, w.density, spec, rp_c, ci_c, cap_c, bm_c, wsm_c,
+                              wsm_c.numel(), s_cmp)
+            bb.bsa_forward_plan(dt, 1, hc, N, d, bs, rp_c, ci_c, bm_c, w.index_mode, wsf_c, wsf_c.numel(), s_cmp)
+            mode_c |= bb.INDEX_PLANNED
+
+        def chunk_compute(c, st):
+            sl = slice(c * hc, (c + 1) * hc)
+            qc, kc, vc = dq[sl], dk[sl], dv[sl]
+            bb.bsa_build_mask(None if spec is not None else qc, None if spec is not None else kc, dt, 1, hc, N, d,
+                              bs, w.density, spec, rp_c, ci_c, cap_c, bm_c, wsm_c, wsm_c.numel(), st)
+            if R is None:
+                bb.bsa_forward(qc, kc, vc, dt, 1, hc, N, d, bs, rp_c, ci_c, bm_c, mode_c, 0.0, dO[sl], dL[sl],
+                               wsf_c, wsf_c.numel(), st)
+            else:
+                bb.bsa_forward_residual(qc, kc, vc, dt, 1, hc, N, d, bs, rp_c, ci_c, bm_c, mode_c, 0.0,
+                                        R.reshape(BHt, N, d)[sl], dO[sl], dL[sl], wsf_c, wsf_c.numel(), st)
+
         e2e_ms = []
-        with torch.cuda.stream(stream):
-            for i in range(args.e2e_steps + 2):
-                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                e0.record(stream)
-                q.copy_(hq, non_blocking=True)
-                k.copy_(hk, non_blocking=True)
-                v.copy_(hv, non_blocking=True)
-                build_call(stream)
-                fwd_call(stream)
-                hO.copy_(O, non_blocking=True)
-                hL.copy_(LSE, non_blocking=True)
-                e1.record(stream)
-                e1.synchronize()
-                if i >= 2:
-                    e2e_ms.append(e0.elapsed_time(e1))
+        for i in range(args.e2e_steps + 2):
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(s_in)
+            for c in range(C):
+                sl = slice(c * hc, (c + 1) * hc)
+                with torch.cuda.stream(s_in):
+                    dq[sl].copy_(sq[sl], non_blocking=True)
+                    dk[sl].copy_(sk[sl], non_blocking=True)
+                    dv[sl].copy_(sv[sl], non_blocking=True)
+                    ev_in = torch.cuda.Event()
+                    ev_in.record(s_in)
+                s_cmp.wait_event(ev_in)
+                chunk_compute(c, s_cmp)
+                ev_c = torch.cuda.Event()
+                ev_c.record(s_cmp)
+                s_out.wait_event(ev_c)
+                with torch.cuda.stream(s_out):
+                    sO[sl].copy_(dO[sl], non_blocking=True)
+                    sL[sl].copy_(dL[sl], non_blocking=True)
+            e1.record(s_out)
+            e1.synchronize()
+            if i >= 2:
+                e2e_ms.append(e0.elapsed_time(e1))
+        for ws in (wsm_c, wsf_c):
+            code = bb.bsa_check_device_error(ws, s_cmp)
+            if code != 0:
+                raise bb.BsaError(code, "end-to-end steps")
         h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
         d2h = hO.numel() * hO.element_size() + hL.numel() * hL.element_size()
         e2e_mean = max_over_ranks(sum(e2e_ms) / len(e2e_ms), dev)
         e2e = {"value": round(job_throughput(flops, world, 1, e2e_mean), 3), "unit": "TFLOP/s",
-               "ms_per_step": round(e2e_mean, 4), "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+               "ms_per_step": round(e2e_mean, 4), "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "pipeline": f"{C} chunks of {hc} heads: copy-in, mask build + forward, copy-out on three streams"}
 
     if rank != 0:
         if world > 1:
