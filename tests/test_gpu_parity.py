@@ -697,6 +697,15 @@ def test_full_long_topk_bitmap():
     run_workload(w, rows=gu.sample_rows(w, rng, blocks_per_head=10, rows_per_block=4))
 
 
+@pytest.mark.parametrize("N", [65536, 131072])
+def test_selector_at_the_largest_key_block_counts(N):
+    # 1024 and 2048 key blocks per row (the selector's widest register path, 64 keys per lane;
+    # 2048 is the limit): the index bit for bit and sampled rows of the forward over it
+    w = wl.scaled(wl.WORKLOADS["long_sweep_bs64"], H=1, N=N)
+    rng = np.random.default_rng(N)
+    run_workload(w, rows=gu.sample_rows(w, rng, blocks_per_head=8, rows_per_block=4))
+
+
 @pytest.mark.parametrize("name", ["long_sweep_bs64", "long_sweep_bs128"])
 def test_full_block_size_sweep(name):
     w = wl.WORKLOADS[name]
