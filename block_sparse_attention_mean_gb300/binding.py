@@ -459,12 +459,14 @@ def tokens_per_group(N: int, density: float) -> int:
     return bsa_tokens_per_group(N, density)
 
 
-def query_groups(q: torch.Tensor, stream=None) -> torch.Tensor:
+def query_groups(q: torch.Tensor, stream=None, check: bool = True) -> torch.Tensor:
     """Run bsa_query_groups; returns perm int32 [B*H, N] (groups of 128 rows)."""
     B, H, N, d = q.shape
     perm = torch.empty((B * H, N), dtype=torch.int32, device=q.device)
     ws = workspace(4, B, H, N, d, 64, q.device)
     bsa_query_groups(q, _dtype_code(q), B, H, N, d, perm, ws, ws.numel(), stream)
+    if check:
+        _check(bsa_check_device_error(ws, stream), "bsa_query_groups (device)")
     return perm
 
 

@@ -510,6 +510,7 @@ bsa_status bsa_query_groups(const void *Q, int dt, int B, int H, int N, int d, i
     a.d = d;
     a.perm = perm;
     a.ws = static_cast<char *>(workspace);
+    a.wait_limit_ns = g_wait_limit_ns;
     return bsa::launch_query_groups(a, static_cast<cudaStream_t>(stream));
 }
 

@@ -166,6 +166,7 @@ struct GroupArgs {
     int dt, B, H, N, d;
     int32_t *perm;  // [B*H][N] (written)
     char *ws;
+    uint64_t wait_limit_ns;  // bounded device waits (the tcgen05 scatter pass)
 };
 // workspace: header; working permutation, projection keys and a scratch copy, [B*H][N]
 // each; per head N/128 slots of a slice's row sum [d], a slice's scatter blocks

@@ -31,11 +31,14 @@
 // median a row may fall on the other side than in an exact eigendecomposition, so results
 // are judged by the partition they form, and bit for bit where no row lies within the
 // rounding bound of a cut.
+#include <type_traits>
+
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include "internal.h"
 #include "ptx.cuh"
+#include "sync.cuh"
 
 namespace bsa {
 namespace {
@@ -47,6 +50,8 @@ constexpr int kStageRows = 32;                 // rows staged per step of the sc
 constexpr int kSliceRows = 4 * kTokenGroup;    // rows per slice at most
 constexpr int kTriBlocks = 136;                // blocks of a 16 x 16 grid on or above the diagonal
 constexpr int kScatThreads = 160;              // kTriBlocks computing threads, 5 warps staging rows
+constexpr int kGramRows = 64;                  // rows per tcgen05 chunk of the bf16 scatter pass
+constexpr int kGramStages = 4;                 // gather ring stages of that pass
 
 __device__ __forceinline__ uint32_t order_key_asc(float s)
 {
@@ -77,14 +82,16 @@ __device__ __forceinline__ bool segment_of(int N, int level, int seg, int &s, in
 }
 
 // Slices: a segment of `len` rows at a level with P slices per segment is cut into P runs
-// of ceil(len / P) rows (the last may be shorter or empty). False when the segment is final.
+// of ceil(len / P) rows rounded up to whole 64-row chunks (len is a multiple of 128, so
+// every run is whole chunks; the last may be shorter or empty). False when the segment
+// is final.
 __device__ __forceinline__ bool slice_of(int N, int level, int P, int slot, int &seg, int &s, int &len, int &r0,
                                          int &r1)
 {
     seg = slot / P;
     const int p = slot - seg * P;
     if (!segment_of(N, level, seg, s, len)) return false;
-    const int chunk = (len + P - 1) / P;
+    const int chunk = ((len + P - 1) / P + kGramRows - 1) / kGramRows * kGramRows;
     r0 = min(len, p * chunk);
     r1 = min(len, r0 + chunk);
     return true;
@@ -302,10 +309,155 @@ __global__ void __launch_bounds__(kScatThreads, 3)
     }
 }
 
+// Index within the kTriBlocks blocks of block (bi, bj), bi <= bj (the inverse of tri_block).
+__device__ __forceinline__ int tri_index(int bi, int bj) { return bi <= 7 ? 17 * bi + (bj - bi) : 17 * (15 - bi) + 1 + bj; }
+
+// bf16, d = 128: per slice, G = sum over its rows of x x^T (raw, not centred) on tcgen05;
+// the segment's rank-one mean term comes off in direction_kernel. The rows arrive through
+// the permutation by TMA tile::gather4 (64 rows per chunk, both 64-column slabs, into a
+// 128-byte-swizzled ring) and one chunk is both MMA operands: A = X^T and B = X, both
+// MN-major (the tile is [rows][d] with d contiguous), M = N = 128, K = 16 rows per MMA,
+// accumulated in TMEM in fp32 (bf16 products are exact). Warp 0 gathers, warp 1 issues
+// (and owns TMEM), then all four warps write the blocks on or above the diagonal in the
+// same [slot][entry][block] layout as slice_scatter_kernel. grid (2^level * P, B*H).
+struct GramCfg {
+    static constexpr int kSlab = kGramRows * 128;     // one 64-column slab of a chunk, 8 KB
+    static constexpr int kStage = 2 * kSlab;          // d = 128: two slabs
+    static constexpr int BAR_OFF = kGramStages * kStage;
+    static constexpr int B_FULL = 0, B_EMPTY = kGramStages, B_DONE = 2 * kGramStages, B_DRAIN = B_DONE + 1;
+    static constexpr int NBAR = B_DRAIN + 1;
+    static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;  // [0] TMEM base, [1] abort flag
+    static constexpr int SMEM = MISC_OFF + 16;
+    static constexpr int SMEM_ALLOC = SMEM + 1024;       // manual 1024-byte alignment
+    static constexpr int TCOLS = 128;
+    static constexpr uint32_t IDESC = idesc_bf16_f32(128, 128, 1, 1);
+};
+
+__global__ void __launch_bounds__(128) slice_gram_tc_kernel(const __grid_constant__ CUtensorMap tmX, int N, int level,
+                                                            int P, int G, const int32_t *__restrict__ work,
+                                                            float *__restrict__ pS, uint32_t *err,
+                                                            unsigned long long wait_limit_ns)
+{
+    using C = GramCfg;
+    constexpr int D = 128, BLK = D / 16, PER = BLK * BLK * kTriBlocks;
+    extern __shared__ uint8_t gram_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(gram_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = smem_u32(smem);
+    auto bar = [&](int idx) -> uint32_t { return sbase + C::BAR_OFF + 8u * idx; };
+    uint32_t *misc = reinterpret_cast<uint32_t *>(smem + C::MISC_OFF);
+    grid_dependency_wait();
+    int seg, s, len, r0, r1;
+    if (!slice_of(N, level, P, blockIdx.x, seg, s, len, r0, r1)) return;  // block-uniform
+    const int64_t bh = blockIdx.y;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nch = (r1 - r0) / kGramRows;  // whole chunks (slice_of)
+    float *out = pS + (bh * G + blockIdx.x) * static_cast<int64_t>(PER);
+    if (nch == 0) {  // an empty slice adds nothing
+        for (int e = threadIdx.x; e < PER; e += blockDim.x) out[e] = 0.0f;
+        return;
+    }
+    if (threadIdx.x == 0) {
+        for (int st = 0; st < kGramStages; ++st) {
+            mbar_init(bar(C::B_FULL + st), 1);
+            mbar_init(bar(C::B_EMPTY + st), 1);
+        }
+        mbar_init(bar(C::B_DONE), 1);
+        mbar_init(bar(C::B_DRAIN), 1);
+        misc[1] = 0u;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(misc), C::TCOLS);
+        tmem_relinquish();
+    }
+    if (warp == 0 && lane == 0) tma_prefetch_map(&tmX);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = misc[0];
+    const Ctl ctl{reinterpret_cast<volatile uint32_t *>(misc + 1), err, wait_limit_ns};
+    const int32_t *idx = work + bh * N + s;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ gather producer
+        // lane l gathers rows 4(l % 16) .. +3 of the chunk into slab l / 16
+        int last = -1;
+        for (int c = 0; c < nch; ++c) {
+            const int st = c % kGramStages;
+            if (c >= kGramStages && !warp_wait_all(bar(C::B_EMPTY + st), ((c / kGramStages) - 1) & 1, ctl)) break;
+            const int slab = lane >> 4, q0 = 4 * (lane & 15);
+            int y[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) y[q] = static_cast<int>(bh * N + idx[r0 + c * kGramRows + q0 + q]);
+            if (lane == 0) mbar_arrive_expect_tx(bar(C::B_FULL + st), C::kStage);
+            __syncwarp();
+            tma_gather4(sbase + st * C::kStage + slab * C::kSlab + q0 * 128, &tmX, slab * 64, y[0], y[1], y[2], y[3],
+                        bar(C::B_FULL + st));
+            __syncwarp();
+            last = c;
+        }
+        if (lane == 0 && *ctl.abort_flag) {
+            // never leave while our copies may still land in shared memory
+            for (int c = last - kGramStages + 1; c <= last; ++c)
+                if (c >= 0) wait_bar_drain(bar(C::B_FULL + c % kGramStages), (c / kGramStages) & 1, wait_limit_ns);
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        const uint64_t desc0 = sdesc_sw128(sbase, C::kSlab, 1024);
+        for (int c = 0; c < nch; ++c) {
+            const int st = c % kGramStages;
+            if (!warp_wait_all(bar(C::B_FULL + st), (c / kGramStages) & 1, ctl)) break;
+            tc_fence_after();
+            const uint64_t desc = desc0 + static_cast<uint64_t>(st * (C::kStage >> 4));
+            __syncwarp();
+            if (elect_one()) {
+#pragma unroll
+                for (int kk = 0; kk < kGramRows / 16; ++kk) {
+                    const uint64_t d = desc + static_cast<uint64_t>(kk * (16 * 128 >> 4));
+                    mma_ss(tmem, d, d, C::IDESC, (c > 0 || kk > 0) ? 1u : 0u);
+                }
+                tc_commit(bar(C::B_EMPTY + st));
+                if (c == nch - 1) tc_commit(bar(C::B_DONE));
+            }
+            __syncwarp();
+        }
+        __syncwarp();
+        if (elect_one()) {
+            tc_commit(bar(C::B_DRAIN));
+            wait_bar_drain(bar(C::B_DRAIN), 0, wait_limit_ns);
+        }
+        __syncwarp();
+    }
+    // ------------------------------------------------------------ epilogue: thread = row i of G
+    if (warp_wait_all(bar(C::B_DONE), 0, ctl)) {
+        tc_fence_after();
+        const int i = warp * 32 + lane, bi = i / BLK, a = i % BLK;
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+            uint32_t v[32];
+            tmem_ld32(tmem + (static_cast<uint32_t>(warp * 32) << 16) + c * 32, v);
+            tmem_wait_ld();
+            reg_fence32(v);
+#pragma unroll
+            for (int q = 0; q < 32; ++q) {
+                const int j = c * 32 + q, bj = j / BLK;
+                if (bj >= bi) out[(a * BLK + j % BLK) * kTriBlocks + tri_index(bi, bj)] = __uint_as_float(v[q]);
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, C::TCOLS);
+    }
+}
+
 // Per segment: S = its slices' scatter blocks added in slice order (mirrored below the
 // diagonal), then the principal direction by kPowerIters steps of power iteration from a
 // fixed start; writes dir[seg] = (mu, v). grid (2^level, B*H).
-template <int D>
+template <int D, bool RAW>
 __global__ void __launch_bounds__(kGrpThreads) direction_kernel(int N, int level, int P, int G,
                                                                 const float *__restrict__ psum,
                                                                 const float *__restrict__ pS,
@@ -328,7 +480,11 @@ __global__ void __launch_bounds__(kGrpThreads) direction_kernel(int N, int level
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int64_t slot0 = bh * G + static_cast<int64_t>(blockIdx.x) * P;
     segment_mean<D>(psum, slot0, P, len, mu);
+    __syncthreads();  // mu
+    const float rlen = sqrtf(static_cast<float>(len));
     // each entry: its slices added in order; EB entries x QB slices of loads in flight
+    // (RAW: uncentred sums, less len * mu_i * mu_j taken as (sqrt(len) mu_i)(sqrt(len) mu_j),
+    // the same value for (i, j) and (j, i))
     const float *src = pS + slot0 * PER;
     for (int e0 = threadIdx.x; e0 < PER; e0 += EB * kGrpThreads) {
         float m[EB];
@@ -356,9 +512,13 @@ __global__ void __launch_bounds__(kGrpThreads) direction_kernel(int N, int level
                 const int t = e % kTriBlocks, ent = e / kTriBlocks;
                 int bi, bj;
                 tri_block(t, bi, bj);
-                const int i = BLK * bi + ent / BLK, j = BLK * bj + ent % BLK;
-                S[i * SW + j] = m[k];
-                if (bi != bj) S[j * SW + i] = m[k];  // a diagonal block holds (i, j) and (j, i) itself
+                const int a = ent / BLK, b = ent % BLK;
+                const int i = BLK * bi + a, j = BLK * bj + b;
+                if (bi == bj && a > b) continue;  // a diagonal block: its upper half, mirrored
+                float v = m[k];
+                if (RAW) v = fmaf(-(rlen * mu[i]), rlen * mu[j], v);
+                S[i * SW + j] = v;
+                S[j * SW + i] = v;
             }
         }
     }
@@ -641,10 +801,21 @@ bsa_status launch(const GroupArgs &a, cudaStream_t st)
     const int G = a.N / kTokenGroup;
     int depth = 0;
     while ((1 << depth) < G) ++depth;  // levels until every segment is one group
+    // bf16 at d = 128: the scatter blocks on tcgen05 (raw sums; the mean term comes off per
+    // segment); otherwise on CUDA cores, centred per slice
+    constexpr bool kTc = std::is_same<T, __nv_bfloat16>::value && D == 128;
     const size_t smem = sizeof(float) * D * (D + 8);
-    if (cudaFuncSetAttribute(direction_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(direction_kernel<D, kTc>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem)) != cudaSuccess)
         return BSA_ERR_CUDA;
+    CUtensorMap mx;
+    if (kTc) {
+        if (!make_tma_map_bf16_rows(&mx, a.Q, static_cast<uint64_t>(BH) * a.N, D)) return BSA_ERR_CUDA;
+        if (cudaFuncSetAttribute(slice_gram_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 GramCfg::SMEM_ALLOC) != cudaSuccess)
+            return BSA_ERR_CUDA;
+    }
+    uint32_t *err = reinterpret_cast<uint32_t *>(a.ws);
     const T *X = static_cast<const T *>(a.Q);
     for (int level = 0; level < depth; ++level) {
         const int P = (max_segment_rows(G, level) + kSliceRows - 1) / kSliceRows;
@@ -657,9 +828,13 @@ bsa_status launch(const GroupArgs &a, cudaStream_t st)
         // previous kernel runs and its CTAs start as that kernel's complete
         bool ok = pdl_launch(slice_sum_kernel<T, D>, sl, kGrpThreads, 0, st, X, a.N, level, P, G,
                              static_cast<const int32_t *>(work), psum);
-        ok = ok && pdl_launch(slice_scatter_kernel<T, D>, sl, kScatThreads, 0, st, X, a.N, level, P, G,
-                              static_cast<const int32_t *>(work), static_cast<const float *>(psum), pS);
-        ok = ok && pdl_launch(direction_kernel<D>, sg, kGrpThreads, smem, st, a.N, level, P, G,
+        if (kTc)
+            ok = ok && pdl_launch(slice_gram_tc_kernel, sl, 128, static_cast<size_t>(GramCfg::SMEM_ALLOC), st, mx,
+                                  a.N, level, P, G, static_cast<const int32_t *>(work), pS, err, a.wait_limit_ns);
+        else
+            ok = ok && pdl_launch(slice_scatter_kernel<T, D>, sl, kScatThreads, 0, st, X, a.N, level, P, G,
+                                  static_cast<const int32_t *>(work), static_cast<const float *>(psum), pS);
+        ok = ok && pdl_launch(direction_kernel<D, kTc>, sg, kGrpThreads, smem, st, a.N, level, P, G,
                               static_cast<const float *>(psum), static_cast<const float *>(pS), dir);
         ok = ok && pdl_launch(slice_keys_kernel<T, D>, sl, kGrpThreads, 0, st, X, a.N, level, P, G,
                               static_cast<const int32_t *>(work), static_cast<const float *>(dir), keys);

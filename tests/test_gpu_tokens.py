@@ -229,23 +229,29 @@ def anisotropic_queries(N, d, seed):
     return ((rng.standard_normal((N, d)) * sc) @ rot.T / 8).astype(np.float32)
 
 
-@pytest.mark.parametrize("d,seed", [(128, 1), (64, 2)])
-def test_query_groups_anisotropic_match_the_oracle_exactly(d, seed):
+@pytest.mark.parametrize("d,seed,dtype", [(128, 1, "fp32"), (64, 2, "fp32"), (128, 3, "bf16"), (64, 4, "bf16")])
+def test_query_groups_anisotropic_match_the_oracle_exactly(d, seed, dtype):
     # The GPU takes each principal direction by 32 fp32 power-iteration steps. Against the
     # exact eigenvector its direction errs by at most ~ T * rho^32 (rho = lam2/lam1, T the
     # tangent of the start vector's angle, <= 10 here) plus fp32 rounding ~ 4*d*2^-24, so a
     # difference of two projections errs by at most eps = 2 * rmax * (10 * rho^32 + 4*d*2^-24)
     # (rmax: largest centred row norm). When every cut's gap exceeds its eps, no row can change
     # sides and the groups must equal the oracle's bit for bit.
+    # bf16 at d = 128 takes the tcgen05 scatter pass (raw sums of exact products in fp32, the
+    # segment's mean term taken off afterwards); the oracle sees the same bf16-rounded values.
     N = 1024
     x = anisotropic_queries(N, d, seed)
+    if dtype == "bf16":
+        xt = torch.from_numpy(x).to(torch.bfloat16)
+        x = xt.float().numpy()
     splits = []
     ref = oracle.query_groups(x, C, splits=splits)
     for sp in splits:
         rho = sp["lam2"] / sp["lam1"]
         eps = 2.0 * sp["rmax"] * (10.0 * rho ** 32 + 4.0 * d * 2.0 ** -24)
         assert sp["gap"] > eps, (sp, eps)  # the data leave no row within eps of a cut
-    perm = bb.query_groups(torch.from_numpy(x).reshape(1, 1, N, d).cuda())
+    qdev = (xt if dtype == "bf16" else torch.from_numpy(x)).reshape(1, 1, N, d).cuda()
+    perm = bb.query_groups(qdev)
     torch.cuda.synchronize()
     assert np.array_equal(perm.cpu().numpy()[0], ref)
 
