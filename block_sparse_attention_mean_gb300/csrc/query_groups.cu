@@ -1,4 +1,4 @@
-// query_groups.cu -- tile-aligned query groups for token-level selection (CUDA cores).
+// query_groups.cu -- tile-aligned query groups for token-level selection.
 //
 // "Can sparse attention close the quality gap in diffusion transformers", section
 // "token 级选择需要瓦片对齐的查询分组": the queries of a head are split recursively at the
@@ -9,18 +9,20 @@
 //
 // The split tree depends on N only, so the splits run level by level, every segment of
 // every head at once, in place in the working permutation of each head. Each segment of a
-// level is cut into P slices of at most kSliceRows rows (P the same for the whole level), and
-// a level is five launches:
+// level is cut into P slices of at most kSliceRows rows in whole 64-row chunks (P the same
+// for the whole level), and a level is five launches:
 //   slice_sum_kernel      per slice: the sum of its rows (fp32; each warp adds its rows in
 //                         order, then the warps in order);
-//   slice_scatter_kernel  per slice: the segment's mean (the slice sums in slice order, over
-//                         the length), then sum (x - mu)(x - mu)^T over the slice's rows, the
-//                         blocks on or above the diagonal (a thread owns a block and adds the
-//                         rows in order);
-//   direction_kernel      per segment: the centred scatter matrix S = the slices' blocks
-//                         added in slice order, and the principal direction by kPowerIters
-//                         steps of power iteration on S from a fixed start (sign: its
-//                         largest-magnitude entry positive);
+//   slice_gram_tc_kernel  (bf16, d = 128) per slice on tcgen05: sum x x^T over the slice's
+//                         rows, uncentred (bf16 products are exact, the sums fp32); or
+//   slice_scatter_kernel  (otherwise) per slice on CUDA cores: the segment's mean (the slice
+//                         sums in slice order, over the length), then sum (x - mu)(x - mu)^T
+//                         over the slice's rows (a thread owns a block and adds the rows in
+//                         order); either way only the blocks on or above the diagonal;
+//   direction_kernel      per segment: S = the slices' blocks added in slice order (less the
+//                         rank-one mean term after the tensor-core pass), and the principal
+//                         direction by kPowerIters steps of power iteration on S from a fixed
+//                         start (sign: its largest-magnitude entry positive);
 //   slice_keys_kernel     per slice: 64-bit keys (projection as an order-preserving key, row
 //                         index);
 //   cut_kernel            per segment: the cut-th smallest key by an exact radix select

@@ -378,6 +378,23 @@ def test_planned_forward_equals_unplanned(name, flags):
     gu.assert_attention_close(O0, L0, inp, mask, w)
 
 
+def test_planned_fp32_forward_is_the_plain_forward():
+    # the CUDA-core fp32 forward keeps no work list: planning is a no-op and the planned flag
+    # changes nothing
+    w = wl.WORKLOADS["tiny"]
+    inp = wl.make_inputs(w)
+    q, k, v = (gu.upload(inp, n) for n in ("q", "k", "v"))
+    mask = gu.oracle_mask(w, inp)
+    idx = gu.device_index(w, q, k, mask)
+    O0, L0 = bb.forward(q, k, v, idx)
+    ws = bb.forward_plan(q, idx)
+    O, L = bb.forward(q, k, v, idx, index_mode=bb.INDEX_PLANNED, ws=ws)
+    torch.cuda.synchronize()
+    assert torch.equal(O, O0)
+    assert torch.equal(L, L0)
+    gu.assert_attention_close(O, L, inp, mask, w)
+
+
 def test_planned_residual_forward_equals_unplanned():
     w = wl.scaled(wl.WORKLOADS["t2i_static"], B=1, H=2)
     inp = wl.make_inputs(w)
