@@ -275,9 +275,13 @@ bsa_status bsa_forward_residual(const void *Q, const void *K, const void *V, int
  * the segment's centred scatter matrix, so a row lying within rounding of a median may land
  * on the other side than an exact eigendecomposition would put it. Every sum runs in a
  * fixed order: the same Q gives the same groups. Errors: BSA_ERR_SHAPE, BSA_ERR_DTYPE,
- * BSA_ERR_INVALID_ARG, BSA_ERR_WORKSPACE. Runs on CUDA cores, the split tree level by level:
- * the row sums, scatter matrices and projections over slices of at most 512 rows of each
- * segment, the power iteration and the cut over one CTA per segment.
+ * BSA_ERR_INVALID_ARG, BSA_ERR_WORKSPACE; device-raised BSA_ERR_TIMEOUT (a bounded wait of the
+ * tensor-core pass gave up). The split tree runs level by level: the row sums, scatter
+ * matrices and projections over slices of at most 512 rows of each segment, the power
+ * iteration and the cut over one CTA per segment. The scatter matrices of bf16 queries at
+ * d = 128 run on tcgen05 as uncentred sums (the mean term taken off per segment, which loses
+ * accuracy when a segment's mean is large against its spread); fp32 and d = 64 run centred
+ * on CUDA cores.
  */
 bsa_status bsa_query_groups(const void *Q, int dt, int B, int H, int N, int d, int32_t *perm, void *workspace,
                             size_t workspace_bytes, void *stream);
