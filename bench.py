@@ -484,6 +484,13 @@ def run_ours(args, world, rank, local):
             code = bb.bsa_check_device_error(ws, s_cmp)
             if code != 0:
                 raise bb.BsaError(code, "end-to-end steps")
+        # heads are independent: the chunked calls must give the unchunked step's outputs exactly
+        torch.cuda.synchronize()
+        build_call(stream)
+        fwd_call(stream)
+        torch.cuda.synchronize()
+        if not (torch.equal(hO, O.cpu()) and torch.equal(hL, LSE.cpu())):
+            raise RuntimeError("end-to-end outputs differ from the unchunked step's")
         h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
         d2h = hO.numel() * hO.element_size() + hL.numel() * hL.element_size()
         e2e_mean = max_over_ranks(sum(e2e_ms) / len(e2e_ms), dev)

@@ -382,19 +382,26 @@ __global__ void __launch_bounds__(128) slice_gram_tc_kernel(const __grid_constan
 
     if (warp == 0) {
         // ------------------------------------------------------------ gather producer
-        // lane l gathers rows 4(l % 16) .. +3 of the chunk into slab l / 16
+        // lane l gathers rows 4(l % 16) .. +3 of each chunk into slab l / 16; the slice's row
+        // indices (at most kMaxChunks chunks) are all loaded first, so no gather waits on one
+        constexpr int kMaxChunks = kSliceRows / kGramRows;
+        const int slab = lane >> 4, q0 = 4 * (lane & 15);
+        int y[kMaxChunks][4];
+#pragma unroll
+        for (int c = 0; c < kMaxChunks; ++c)
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                y[c][q] = c < nch ? static_cast<int>(bh * N + idx[r0 + c * kGramRows + q0 + q]) : 0;
         int last = -1;
-        for (int c = 0; c < nch; ++c) {
+#pragma unroll
+        for (int c = 0; c < kMaxChunks; ++c) {
+            if (c >= nch) break;
             const int st = c % kGramStages;
             if (c >= kGramStages && !warp_wait_all(bar(C::B_EMPTY + st), ((c / kGramStages) - 1) & 1, ctl)) break;
-            const int slab = lane >> 4, q0 = 4 * (lane & 15);
-            int y[4];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) y[q] = static_cast<int>(bh * N + idx[r0 + c * kGramRows + q0 + q]);
             if (lane == 0) mbar_arrive_expect_tx(bar(C::B_FULL + st), C::kStage);
             __syncwarp();
-            tma_gather4(sbase + st * C::kStage + slab * C::kSlab + q0 * 128, &tmX, slab * 64, y[0], y[1], y[2], y[3],
-                        bar(C::B_FULL + st));
+            tma_gather4(sbase + st * C::kStage + slab * C::kSlab + q0 * 128, &tmX, slab * 64, y[c][0], y[c][1],
+                        y[c][2], y[c][3], bar(C::B_FULL + st));
             __syncwarp();
             last = c;
         }
