@@ -41,7 +41,8 @@ EXPORTS = ("bsa_build_mask", "bsa_forward", "bsa_mask_nnz", "bsa_workspace_size"
            "bsa_check_device_error", "bsa_validate_index", "bsa_debug_config",
            "bsa_status_string", "bsa_build_mask_noalloc", "bsa_residual_capture", "bsa_forward_residual",
            "bsa_build_mask_modal", "bsa_mask_nnz_modal", "bsa_build_mask_exact", "bsa_forward_tokens",
-           "bsa_select_tokens", "bsa_query_groups", "bsa_tokens_per_group", "bsa_forward_plan")
+           "bsa_select_tokens", "bsa_query_groups", "bsa_tokens_per_group", "bsa_forward_plan",
+           "bsa_forward_lse")
 NOALLOC_SCRATCH_BYTES = 16 << 20  # BSA_NOALLOC_SCRATCH_BYTES
 # bsa_debug_config flag bits
 DBG_STALL = 1       # skip loads and MMAs: the first device wait runs out
@@ -82,6 +83,7 @@ def load():
     lib.bsa_forward.argtypes = [P, P, P, I, I, I, I, I, I, P, P, P, I, F, P, P, P, SZ, P]
     lib.bsa_forward_residual.argtypes = [P, P, P, I, I, I, I, I, I, P, P, P, I, F, P, P, P, P, SZ, P]
     lib.bsa_forward_plan.argtypes = [I, I, I, I, I, I, P, P, P, I, P, SZ, P]
+    lib.bsa_forward_lse.argtypes = [P, P, I, I, I, I, I, I, P, P, P, I, F, P, P, SZ, P]
     lib.bsa_residual_capture.argtypes = [P, P, I, I64, P, P]
     lib.bsa_forward_tokens.argtypes = [P, P, P, I, I, I, I, I, P, P, I, F, P, P, P, SZ, P]
     lib.bsa_select_tokens.argtypes = [P, P, I, I, I, I, I, P, P, F, F, P, I64, P, SZ, P]
@@ -150,6 +152,14 @@ def bsa_forward(Q, K, V, dt: int, B: int, H: int, N: int, d: int, block: int, ro
                               _ptr(bitmap), int(index_mode), float(scale), _ptr(O), _ptr(LSE),
                               _ptr(workspace), int(workspace_bytes), _stream(stream))
     _check(code, "bsa_forward")
+
+
+def bsa_forward_lse(Q, K, dt: int, B: int, H: int, N: int, d: int, block: int, row_ptr, col_idx, bitmap,
+                    index_mode: int, scale: float, LSE, workspace, workspace_bytes: int, stream=None) -> None:
+    code = load().bsa_forward_lse(_ptr(Q), _ptr(K), dt, B, H, N, d, block, _ptr(row_ptr), _ptr(col_idx),
+                                  _ptr(bitmap), int(index_mode), float(scale), _ptr(LSE), _ptr(workspace),
+                                  int(workspace_bytes), _stream(stream))
+    _check(code, "bsa_forward_lse")
 
 
 def bsa_forward_plan(dt: int, B: int, H: int, N: int, d: int, block: int, row_ptr, col_idx, bitmap,
@@ -406,6 +416,22 @@ def forward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, index: Index, ind
     if check:
         _check(bsa_check_device_error(ws, stream), "bsa_forward (device)")
     return out, lse
+
+
+def forward_lse(q: torch.Tensor, k: torch.Tensor, index: Index, index_mode: int = 0, scale: float = 0.0,
+                ws: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None, stream=None,
+                check: bool = True) -> torch.Tensor:
+    """Run bsa_forward_lse; returns LSE fp32 [B, H, N]."""
+    B, H, N, d = q.shape
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    if ws is None:
+        ws = workspace(1, B, H, N, d, index.block, q.device)
+    bsa_forward_lse(q, k, _dtype_code(q), B, H, N, d, index.block, index.row_ptr, index.col_idx, index.bitmap,
+                    index_mode, scale, lse, ws, ws.numel(), stream)
+    if check:
+        _check(bsa_check_device_error(ws, stream), "bsa_forward_lse (device)")
+    return lse
 
 
 def forward_plan(q: torch.Tensor, index: Index, index_mode: int = 0, ws: Optional[torch.Tensor] = None,

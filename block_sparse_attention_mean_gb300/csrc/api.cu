@@ -405,6 +405,44 @@ static bsa_status forward_impl(const void *Q, const void *K, const void *V, int 
     return dt == BSA_BF16 ? bsa::launch_forward_tc(a, st) : bsa::launch_forward_simt(a, st);
 }
 
+bsa_status bsa_forward_lse(const void *Q, const void *K, int dt, int B, int H, int N, int d, int block,
+                           const int32_t *row_ptr, const int32_t *col_idx, const uint32_t *bitmap, int index_mode,
+                           float scale, float *LSE, void *workspace, size_t workspace_bytes, void *stream)
+{
+    bsa_status s = check_shape(B, H, N, d, block);
+    if (s != BSA_OK) return s;
+    if (dt != BSA_BF16 && dt != BSA_FP32) return BSA_ERR_DTYPE;
+    if (!Q || !K || !LSE || !aligned(Q, 16) || !aligned(K, 16) || !aligned(LSE, 4)) return BSA_ERR_INVALID_ARG;
+    if (!index_args_ok(row_ptr, col_idx, bitmap, index_mode)) return BSA_ERR_INVALID_ARG;
+    if (std::isnan(scale) || std::isinf(scale)) return BSA_ERR_INVALID_ARG;
+    if (!workspace || !aligned(workspace, 256) || workspace_bytes < bsa::fwd_workspace_bytes(B, H, N, d, block))
+        return BSA_ERR_WORKSPACE;
+    bsa::FwdArgs a{};
+    a.Q = Q;
+    a.K = K;
+    a.dt = dt;
+    a.B = B;
+    a.H = H;
+    a.N = N;
+    a.d = d;
+    a.block = block;
+    a.nQB = n_blocks(N, block);
+    a.nKB = n_blocks(N, block);
+    a.W = (a.nKB + 31) / 32;
+    a.row_ptr = row_ptr;
+    a.col_idx = col_idx;
+    a.bitmap = bitmap;
+    a.index_mode = index_mode;
+    a.scale = scale > 0.0f ? scale : static_cast<float>(1.0 / std::sqrt(static_cast<double>(d)));
+    a.LSE = LSE;
+    a.ws = static_cast<char *>(workspace);
+    a.dbg_flags = g_dbg_flags;
+    a.wait_limit_ns = g_wait_limit_ns;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    // V and O stay null: the kernels read no V and write no O
+    return dt == BSA_BF16 ? bsa::launch_forward_lse_tc(a, st) : bsa::launch_forward_simt(a, st);
+}
+
 bsa_status bsa_forward_plan(int dt, int B, int H, int N, int d, int block, const int32_t *row_ptr,
                             const int32_t *col_idx, const uint32_t *bitmap, int index_mode, void *workspace,
                             size_t workspace_bytes, void *stream)

@@ -68,7 +68,7 @@ __global__ void __launch_bounds__(kWarps * 32) fwd_simt_kernel(const float *__re
                 const int kk = e / D, c = e % D;
                 const bool in = c0 + kk < keys;
                 ks[kk * (D + 1) + c] = in ? K[(krow + kk) * D + c] : 0.0f;
-                vs[e] = in ? V[(krow + kk) * D + c] : 0.0f;
+                if (V) vs[e] = in ? V[(krow + kk) * D + c] : 0.0f;  // no V: the LSE only
             }
             __syncthreads();
 #pragma unroll
@@ -92,6 +92,7 @@ __global__ void __launch_bounds__(kWarps * 32) fwd_simt_kernel(const float *__re
                 m[r] = mn;
 #pragma unroll
                 for (int t = 0; t < DPL; ++t) o[r][t] *= alpha;
+                if (!V) continue;
                 for (int kk = 0; kk < kChunk; ++kk) {
                     const float pk = __shfl_sync(0xffffffffu, p, kk);
 #pragma unroll
@@ -105,9 +106,11 @@ __global__ void __launch_bounds__(kWarps * 32) fwd_simt_kernel(const float *__re
         if (warp * RPW + r >= rows) break;
         const int64_t row = row0 + warp * RPW + r;
         const float inv = l[r] > 0.0f ? 1.0f / l[r] : 0.0f;
+        if (O) {
 #pragma unroll
-        for (int t = 0; t < DPL; ++t)
-            O[row * D + lane + 32 * t] = o[r][t] * inv + (R ? R[row * D + lane + 32 * t] : 0.0f);
+            for (int t = 0; t < DPL; ++t)
+                O[row * D + lane + 32 * t] = o[r][t] * inv + (R ? R[row * D + lane + 32 * t] : 0.0f);
+        }
         if (lane == 0) LSE[row] = l[r] > 0.0f ? m[r] + logf(l[r]) : -CUDART_INF_F;
     }
 }

@@ -450,7 +450,7 @@ __device__ __forceinline__ bool last_chunk(const TcParams &p, int base, int nchu
 // block q of the step occupies S columns [q * BS, (q + 1) * BS) and is skipped
 // (P = 0, no effect on the max or the sums) when the step has no block q or the
 // row's Q block does not have it.
-template <int D, int BS, int NSB, int PAIR, class C, bool TOK>
+template <int D, int BS, int NSB, int PAIR, class C, bool TOK, bool LSE>
 __device__ __forceinline__ void softmax_rows(const TcParams &p, uint32_t sbase, uint32_t tmem,
                                              volatile int32_t *tile_ids, const volatile uint32_t *desc,
                                              const Ctl &ctl, int warp, int lane)
@@ -479,9 +479,11 @@ __device__ __forceinline__ void softmax_rows(const TcParams &p, uint32_t sbase, 
         }
         if (empty && decode_item(p, tile & ~kEmptyTile).nchunk == 1) {
             if (row_valid) {
-                const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+                if constexpr (!LSE) {
+                    const uint4 z = make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
-                for (int c = 0; c < D / 8; ++c) reinterpret_cast<uint4 *>(orow)[c] = z;
+                    for (int c = 0; c < D / 8; ++c) reinterpret_cast<uint4 *>(orow)[c] = z;
+                }
                 p.LSE[grow] = -CUDART_INF_F;
             }
             continue;
@@ -566,11 +568,13 @@ __device__ __forceinline__ void softmax_rows(const TcParams &p, uint32_t sbase, 
                                              c2x, nm2),
                                       x0, x1);
                             const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
-                            pk[q] = pack_bf16x2(p0, p1);
                             sacc[q & 1] = f2_add(sacc[q & 1], f2_pack(p0, p1));
-                            add_bf16x2_to_f32(sap[2 * (q & 1)], sap[2 * (q & 1) + 1], pk[q]);
+                            if constexpr (!LSE) {  // P for the PV MMA and its bf16-rounded sum
+                                pk[q] = pack_bf16x2(p0, p1);
+                                add_bf16x2_to_f32(sap[2 * (q & 1)], sap[2 * (q & 1) + 1], pk[q]);
+                            }
                         }
-                        tmem_st16(tS + b * kStep + c * 16, pk);
+                        if constexpr (!LSE) tmem_st16(tS + b * kStep + c * 16, pk);
                     }
                 };
                 if (m_run == -CUDART_INF_F) m_run = step_max();  // a tile's first step
@@ -602,14 +606,14 @@ __device__ __forceinline__ void softmax_rows(const TcParams &p, uint32_t sbase, 
                 for (int k = 0; k < 2; ++k) acc[k] = f2_add(acc[k], sacc[k]);
 #pragma unroll
                 for (int k = 0; k < 4; ++k) accp[k] += sap[k];
-            } else {
+            } else if constexpr (!LSE) {
                 uint32_t z[16];
 #pragma unroll
                 for (int q = 0; q < 16; ++q) z[q] = 0u;
 #pragma unroll
                 for (int c = 0; c < NC; ++c) tmem_st16(tS + b * kStep + c * 16, z);
             }
-            if (__any_sync(0xffffffffu, resc)) {
+            if (!LSE && __any_sync(0xffffffffu, resc)) {
                 // O holds the previous steps' sum: rescale it once the last PV landed
                 const int t = G - 1;
                 if (!warp_wait_all(bar(C::B_PVDONE + t % NSB), (t / NSB) & 1, ctl)) return;
@@ -636,6 +640,10 @@ __device__ __forceinline__ void softmax_rows(const TcParams &p, uint32_t sbase, 
         const float l_run = e0 + e1;
         const float lp_run = (accp[0] + accp[1]) + (accp[2] + accp[3]);
         const Item it = decode_item(p, tile & ~kEmptyTile);  // decoded again: not live across the loop
+        if constexpr (LSE) {  // no O: the row's LSE only (tiles are never split in this mode)
+            if (row_valid) p.LSE[grow] = l_run > 0.0f ? (m_run + log2f(l_run)) * 0.69314718055994530942f : -CUDART_INF_F;
+            continue;
+        }
         if (it.nchunk > 1) {
             // chunk of a split tile: unnormalised partial O and the row's (m, l, lp)
             const int base = p.split_base[it.tile];
@@ -733,7 +741,7 @@ __device__ __forceinline__ void softmax_rows(const TcParams &p, uint32_t sbase, 
 // group and, in every 8-column group of S and O, columns 2(t%4) and +1; a row's
 // max and sums are reduced over its 4 lanes with two shuffles. A step holds PAIR
 // KV blocks: 8-column group g of the step belongs to block g / (BS / 8).
-template <int D, int BS, int NSB, int PAIR, class C, bool TOK>
+template <int D, int BS, int NSB, int PAIR, class C, bool TOK, bool LSE>
 __device__ __forceinline__ void softmax_quads(const TcParams &p, uint32_t sbase, uint32_t tmem,
                                               volatile int32_t *tile_ids, const volatile uint32_t *desc,
                                               const Ctl &ctl, int warp, int lane)
@@ -765,10 +773,12 @@ __device__ __forceinline__ void softmax_quads(const TcParams &p, uint32_t sbase,
             if (hi_valid) prefetch_l2(p.R + g_hi * D + 32 * (lane & 3));
         }
         if (empty && it.nchunk == 1) {
+            if constexpr (!LSE) {
 #pragma unroll
-            for (int g = 0; g < RO; ++g) {
-                if (lo_valid) o_lo[4 * g] = 0u;
-                if (hi_valid) o_hi[4 * g] = 0u;
+                for (int g = 0; g < RO; ++g) {
+                    if (lo_valid) o_lo[4 * g] = 0u;
+                    if (hi_valid) o_hi[4 * g] = 0u;
+                }
             }
             if ((lane & 3) == 0) {
                 if (lo_valid) p.LSE[g_lo] = -CUDART_INF_F;
@@ -869,21 +879,23 @@ __device__ __forceinline__ void softmax_quads(const TcParams &p, uint32_t sbase,
                                      nm_hi),
                               x, y);
                     const float p2 = ex2_approx(x), p3 = ex2_approx(y);
-                    pk[2 * g] = pack_bf16x2(p0, p1);      // row r_lo, packed column 4g + t%4
-                    pk[2 * g + 1] = pack_bf16x2(p2, p3);  // row r_lo + 8
                     acc_lo[g & 1] = f2_add(acc_lo[g & 1], f2_pack(p0, p1));
                     acc_hi[g & 1] = f2_add(acc_hi[g & 1], f2_pack(p2, p3));
-                    add_bf16x2_to_f32(ap_lo[2 * (g & 1)], ap_lo[2 * (g & 1) + 1], pk[2 * g]);
-                    add_bf16x2_to_f32(ap_hi[2 * (g & 1)], ap_hi[2 * (g & 1) + 1], pk[2 * g + 1]);
+                    if constexpr (!LSE) {  // P for the PV MMA and its bf16-rounded sums
+                        pk[2 * g] = pack_bf16x2(p0, p1);      // row r_lo, packed column 4g + t%4
+                        pk[2 * g + 1] = pack_bf16x2(p2, p3);  // row r_lo + 8
+                        add_bf16x2_to_f32(ap_lo[2 * (g & 1)], ap_lo[2 * (g & 1) + 1], pk[2 * g]);
+                        add_bf16x2_to_f32(ap_hi[2 * (g & 1)], ap_hi[2 * (g & 1) + 1], pk[2 * g + 1]);
+                    }
                 }
-                tmem_st_16x128b<RS>(tbase + b * C::kStep, pk);
-            } else {
+                if constexpr (!LSE) tmem_st_16x128b<RS>(tbase + b * C::kStep, pk);
+            } else if constexpr (!LSE) {
                 uint32_t z[2 * RS];
 #pragma unroll
                 for (int q = 0; q < 2 * RS; ++q) z[q] = 0u;
                 tmem_st_16x128b<RS>(tbase + b * C::kStep, z);
             }
-            if (__any_sync(0xffffffffu, resc)) {
+            if (!LSE && __any_sync(0xffffffffu, resc)) {
                 const int t = G - 1;
                 if (!warp_wait_all(bar(C::B_PVDONE + t % NSB), (t / NSB) & 1, ctl)) return;
                 tc_fence_after();
@@ -923,6 +935,13 @@ __device__ __forceinline__ void softmax_quads(const TcParams &p, uint32_t sbase,
             l_hi += __shfl_xor_sync(0xffffffffu, l_hi, o);
             lp_lo += __shfl_xor_sync(0xffffffffu, lp_lo, o);
             lp_hi += __shfl_xor_sync(0xffffffffu, lp_hi, o);
+        }
+        if constexpr (LSE) {  // no O: the rows' LSE only (tiles are never split in this mode)
+            if ((lane & 3) == 0) {
+                if (lo_valid) p.LSE[g_lo] = l_lo > 0.0f ? (m_lo + log2f(l_lo)) * 0.69314718055994530942f : -CUDART_INF_F;
+                if (hi_valid) p.LSE[g_hi] = l_hi > 0.0f ? (m_hi + log2f(l_hi)) * 0.69314718055994530942f : -CUDART_INF_F;
+            }
+            continue;
         }
         if (it.nchunk > 1) {
             // chunk of a split tile: unnormalised partial O and the rows' (m, l, lp)
@@ -997,12 +1016,14 @@ __device__ __forceinline__ void softmax_quads(const TcParams &p, uint32_t sbase,
     }
 }
 
-template <int D, int BS, int NK, int NV, int NSB, int QS, int SPLIT, int PAIR, int MINB, bool TOK = false>
+template <int D, int BS, int NK, int NV, int NSB, int QS, int SPLIT, int PAIR, int MINB, bool TOK = false,
+          bool LSE = false>
 __global__ void __launch_bounds__((4 * SPLIT + 4) * 32, MINB)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const TcParams p)
 {
     static_assert(!TOK || (BS == kTileM && PAIR == 1), "token mode: 128-key steps");
+    static_assert(!(TOK && LSE), "the LSE-only mode runs over a block index");
     using C = Cfg<D, BS, NK, NV, NSB, QS, PAIR>;
     using R = Roles<SPLIT>;
     constexpr int kProducerWarp = R::kProducerWarp, kQkWarp = R::kQkWarp, kMmaWarp = R::kMmaWarp;
@@ -1280,6 +1301,13 @@ __global__ void __launch_bounds__((4 * SPLIT + 4) * 32, MINB)
             }
             __syncwarp();
         }
+    } else if (LSE && warp == kVProducerWarp) {
+        // ------------------------------------------------------------ LSE only: no V to load
+        int tcount = 0;
+        for (;;) {
+            int tile;
+            if (!fetch_tile<C>(sbase, tile_ids, ctl, lane, tcount, tile) || tile < 0) break;
+        }
     } else if (warp == kVProducerWarp) {
         // ------------------------------------------------------------ V producer
         // Walks each tile on its own, so a V slot still held by a lagging PV never
@@ -1404,6 +1432,31 @@ __global__ void __launch_bounds__((4 * SPLIT + 4) * 32, MINB)
             }
             __syncwarp();
         }
+    } else if (LSE && warp == kMmaWarp) {
+        // ------------------------------------------------------------ LSE only: no PV
+        // A buffer is free again as soon as every softmax warp has loaded its S.
+        if (!stall) {
+            int G = 0, tcount = 0;
+            bool ok = true;
+            while (ok) {
+                const int slot = tcount & 1;
+                if (!warp_wait_all(bar(C::B_TFULL + slot), (tcount >> 1) & 1, ctl)) break;
+                const int tile = tile_ids[slot];
+                if (lane == 0) mbar_arrive(bar(C::B_TEMPTY + slot));
+                ++tcount;
+                if (tile < 0) break;
+                if (tile & kEmptyTile) continue;
+                bool last;
+                do {
+                    const int b = G % NSB;
+                    if (!warp_wait_all(bar(C::B_PFULL + b), (G / NSB) & 1, ctl)) { ok = false; break; }
+                    last = desc_last(desc[b]);
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar(C::B_PVDONE + b));
+                    ++G;
+                } while (!last);
+            }
+        }
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------ PV issuer
         // Whole-warp loop with one elected issuing lane, like the QK^T issuer.
@@ -1467,9 +1520,9 @@ __global__ void __launch_bounds__((4 * SPLIT + 4) * 32, MINB)
     } else {
         // ------------------------------------------------------------ softmax + epilogue
         if constexpr (SPLIT == 1)
-            softmax_rows<D, BS, NSB, PAIR, C, TOK>(p, sbase, tmem, tile_ids, desc, ctl, warp, lane);
+            softmax_rows<D, BS, NSB, PAIR, C, TOK, LSE>(p, sbase, tmem, tile_ids, desc, ctl, warp, lane);
         else
-            softmax_quads<D, BS, NSB, PAIR, C, TOK>(p, sbase, tmem, tile_ids, desc, ctl, warp, lane);
+            softmax_quads<D, BS, NSB, PAIR, C, TOK, LSE>(p, sbase, tmem, tile_ids, desc, ctl, warp, lane);
     }
 
     tc_fence_before();
@@ -2031,7 +2084,7 @@ FwdLayout fwd_layout(int B, int H, int N, int d)
 
 // Resident CTAs of a forward instance over the whole GPU (set-up once per instance:
 // shared-memory attributes, then registers, shared memory and TMEM per SM).
-template <int D, int BS, int NK, int NV, int NSB, int QS, int SPLIT, int PAIR, int MINB, bool TOK>
+template <int D, int BS, int NK, int NV, int NSB, int QS, int SPLIT, int PAIR, int MINB, bool TOK, bool LSE = false>
 bsa_status forward_grid_cap(int &cap)
 {
     using C = Cfg<D, BS, NK, NV, NSB, QS, PAIR>;
@@ -2039,7 +2092,7 @@ bsa_status forward_grid_cap(int &cap)
     static_assert(MINB * (C::SMEM_ALLOC + 1024) <= 233472, "shared memory for MINB CTAs per SM");
     static_assert(C::SMEM_ALLOC <= 227 * 1024, "shared memory budget");
     static_assert(C::TCOLS_USED <= C::TCOLS, "TMEM budget");
-    auto kern = fwd_tc_kernel<D, BS, NK, NV, NSB, QS, SPLIT, PAIR, MINB, TOK>;
+    auto kern = fwd_tc_kernel<D, BS, NK, NV, NSB, QS, SPLIT, PAIR, MINB, TOK, LSE>;
     static int grid_cap = 0;
     if (grid_cap == 0) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC) != cudaSuccess)
@@ -2085,21 +2138,22 @@ uint32_t plan_signature(int n_tiles, int grid, int index_mode, int D, int BS, in
 // mode: kRunOrderAndForward, kRunForward (a plan is in the workspace), kRunOrder (make the plan)
 enum { kRunOrderAndForward = 0, kRunForward = 1, kRunOrder = 2 };
 
-template <int D, int BS, int NK, int NV, int NSB, int QS, int SPLIT, int PAIR, int MINB>
+// LSE: the LSE-only kernel (no V, no O; tiles never split)
+template <int D, int BS, int NK, int NV, int NSB, int QS, int SPLIT, int PAIR, int MINB, bool LSE = false>
 bsa_status launch_tc(const FwdArgs &a, cudaStream_t st, int mode)
 {
     using C = Cfg<D, BS, NK, NV, NSB, QS, PAIR>;
     constexpr int kThreads = Roles<SPLIT>::kThreads;
-    auto kern = fwd_tc_kernel<D, BS, NK, NV, NSB, QS, SPLIT, PAIR, MINB, false>;
+    auto kern = fwd_tc_kernel<D, BS, NK, NV, NSB, QS, SPLIT, PAIR, MINB, false, LSE>;
     int grid_cap = 0;
     {
-        const bsa_status s = forward_grid_cap<D, BS, NK, NV, NSB, QS, SPLIT, PAIR, MINB, false>(grid_cap);
+        const bsa_status s = forward_grid_cap<D, BS, NK, NV, NSB, QS, SPLIT, PAIR, MINB, false, LSE>(grid_cap);
         if (s != BSA_OK) return s;
     }
     const int64_t BH = static_cast<int64_t>(a.B) * a.H;
     CUtensorMap mq, mk, mv;
     if (!make_tma_map_bf16(&mq, a.Q, BH, a.N, D, kTileM) || !make_tma_map_bf16(&mk, a.K, BH, a.N, D, BS) ||
-        !make_tma_map_bf16(&mv, a.V, BH, a.N, D, BS))
+        !make_tma_map_bf16(&mv, LSE ? a.K : a.V, BH, a.N, D, BS))  // the LSE-only kernel reads no V
         return BSA_ERR_CUDA;
     WsHeader *hdr = reinterpret_cast<WsHeader *>(a.ws);
     TcParams p{};
@@ -2139,6 +2193,7 @@ bsa_status launch_tc(const FwdArgs &a, cudaStream_t st, int mode)
     p.err = &hdr->err;
     p.wait_limit_ns = a.wait_limit_ns;
     p.dbg = a.dbg_flags;
+    if (LSE) p.dbg = (p.dbg & ~kDbgSplitAll) | kDbgNoSplit;  // a chunk's partial O has nowhere to go
     // persistent CTAs; with splitting on, the item count is only known on the device
     const int64_t max_items = static_cast<int64_t>(p.n_tiles) + static_cast<int64_t>(lay.budget);
     const int grid = static_cast<int>(max_items < grid_cap ? max_items : grid_cap);
@@ -2256,6 +2311,16 @@ bsa_status launch_forward_tc(const FwdArgs &a, cudaStream_t st)
 bsa_status launch_forward_plan_tc(const FwdArgs &a, cudaStream_t st)
 {
     return launch_forward_mode(a, st, kRunOrder);
+}
+
+bsa_status launch_forward_lse_tc(const FwdArgs &a, cudaStream_t st)
+{
+    // the forward's instances, LSE only
+    if (a.d == 64 && a.block == 64) return launch_tc<64, 64, 4, 5, 3, 2, 1, 1, 2, true>(a, st, kRunOrderAndForward);
+    if (a.d == 128 && a.block == 64) return launch_tc<128, 64, 2, 2, 2, 1, 1, 1, 2, true>(a, st, kRunOrderAndForward);
+    if (a.d == 64 && a.block == 128) return launch_tc<64, 128, 5, 6, 3, 2, 2, 1, 1, true>(a, st, kRunOrderAndForward);
+    if (a.d == 128 && a.block == 128) return launch_tc<128, 128, 2, 4, 3, 1, 2, 1, 1, true>(a, st, kRunOrderAndForward);
+    return BSA_ERR_SHAPE;
 }
 
 // ---------------------------------------------------------------- TMA descriptors

@@ -115,6 +115,7 @@ size_t fwd_workspace_bytes(int B, int H, int N, int d, int block);
 bool make_tma_map_bf16(CUtensorMap *m, const void *base, uint64_t heads, uint64_t n, int d, int box_rows);
 bsa_status launch_forward_tc(const FwdArgs &a, cudaStream_t st);    // bf16, tcgen05
 bsa_status launch_forward_plan_tc(const FwdArgs &a, cudaStream_t st);  // bf16: the work list only
+bsa_status launch_forward_lse_tc(const FwdArgs &a, cudaStream_t st);   // bf16: LSE only (no V, no O)
 bsa_status launch_forward_simt(const FwdArgs &a, cudaStream_t st);  // fp32, CUDA cores
 bsa_status launch_residual_capture(const void *dense, const void *sparse, int dt, int64_t count, float *R,
                                    cudaStream_t st);

@@ -208,6 +208,27 @@ bsa_status bsa_forward(const void *Q, const void *K, const void *V, int dt, int 
                        void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * bsa_forward_lse -- the LSE alone of bsa_forward over the same index: LSE_r = ln sum over
+ * the keys c of the row's active blocks of exp(scale * q_r . k_c), -inf for a row with no
+ * active block. With every block active it is pass 1 (the dense logsumexp) of the exact
+ * selectors ("Can sparse attention close the quality gap in diffusion transformers",
+ * section "质量差距有三个可分离来源": bsa_build_mask_exact and bsa_select_tokens take it).
+ * No V is read and no O is written: QK^T and the softmax sums only, so about half the
+ * forward's MMA work and no PV chain. The values are those bsa_forward writes for LSE, bit
+ * for bit, as long as bsa_forward splits no tile (this call never splits one).
+ *   Q, K        device [B][H][N][d], dtype dt
+ *   row_ptr, col_idx, bitmap, index_mode   as bsa_forward (index_mode 0 or 1, not planned)
+ *   scale       softmax scale; <= 0 selects 1/sqrt(d)
+ *   LSE         device fp32 [B][H][N] (written)
+ *   workspace   device, >= bsa_workspace_size(1, ...) bytes, 256-byte aligned
+ * Errors: as bsa_forward.
+ */
+bsa_status bsa_forward_lse(const void *Q, const void *K, int dt, int B, int H, int N, int d, int block,
+                           const int32_t *row_ptr, const int32_t *col_idx, const uint32_t *bitmap,
+                           int index_mode, float scale, float *LSE, void *workspace,
+                           size_t workspace_bytes, void *stream);
+
+/*
  * bsa_forward_plan -- the forward's work list for one index, made once into the forward
  * workspace, for a mask used by many calls ([P1] §5.3: static masks are pre-generated
  * once). The list depends on the index's row lengths and the launch shape, not on Q, K,

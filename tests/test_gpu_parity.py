@@ -433,6 +433,58 @@ def test_planned_forward_needs_its_own_plan():
     gu.assert_attention_close(O, L, inp, mask, w)
 
 
+# ------------------------------------------------------------ LSE only
+#
+# bsa_forward_lse runs the forward's QK^T and softmax sums only. Its LSE must be the full
+# forward's bit for bit (the full forward without split tiles: a split tile's LSE is merged in
+# another order) and match the oracle.
+
+LSE_CASES = {
+    "dynamic_csr": (wl.scaled(wl.WORKLOADS["dynamic_topk"], H=3, N=4096), 0),        # d128 bs64, one thread per row
+    "long_bitmap": (wl.scaled(wl.WORKLOADS["long_topk"], H=2, N=8192), 1),           # d128 bs128, four lanes per row
+    "t2i_csr": (wl.scaled(wl.WORKLOADS["t2i_static"], B=1, H=4), 0),                 # d64 bs64
+    "d64_bs128": (wl.scaled(wl.WORKLOADS["t2i_static"], B=1, H=2, N=2048, block=128, mask=wl.TOPK,
+                            density=0.25), 1),
+    "ragged": (wl.scaled(wl.WORKLOADS["dynamic_topk"], H=2, N=2000), 0),
+    "fp32_tiny": (wl.WORKLOADS["tiny"], 0),
+}
+
+
+@pytest.mark.parametrize("name", sorted(LSE_CASES))
+def test_forward_lse_is_the_forward_lse(name):
+    w, mode = LSE_CASES[name]
+    inp = wl.make_inputs(w)
+    q, k, v = (gu.upload(inp, n) for n in ("q", "k", "v"))
+    mask = gu.oracle_mask(w, inp)
+    idx = gu.device_index(w, q, k, mask)
+    bb.bsa_debug_config(bb.DBG_NO_SPLIT, 0)
+    try:
+        _, L0 = bb.forward(q, k, v, idx, index_mode=mode)
+    finally:
+        bb.bsa_debug_config(0, 0)
+    L = bb.forward_lse(q, k, idx, index_mode=mode)
+    torch.cuda.synchronize()
+    assert torch.equal(L, L0)
+    _, L_ref = oracle.attention(inp["q"], inp["k"], inp["v"], mask, w.block, rows=None)
+    assert np.abs(L.reshape(-1).cpu().numpy().astype(np.float64) - L_ref).max() <= gu.LSE_MAX_ABS
+
+
+def test_forward_lse_dense_and_empty_rows():
+    # every block active (the exact selectors' pass 1) and rows with no active block (-inf)
+    w = wl.scaled(wl.WORKLOADS["dynamic_topk"], H=2, N=2048)
+    inp = wl.make_inputs(w)
+    q, k = gu.upload(inp, "q"), gu.upload(inp, "k")
+    full = np.ones((w.B, w.H, w.nQB, w.nKB), dtype=np.uint8)
+    full[0, 1, 3:5, :] = 0  # two Q blocks of head 1 attend to nothing
+    idx = bb.build_mask(None, None, w.block, spec=bb.explicit_spec(
+        torch.from_numpy(gu.mask_bitmap_words(full).reshape(-1)).cuda()), shape=(w.B, w.H, w.N, w.d))
+    L = bb.forward_lse(q, k, idx).reshape(-1).cpu().numpy().astype(np.float64)
+    _, L_ref = oracle.attention(inp["q"], inp["k"], inp["v"], full, w.block, rows=None)
+    empty = np.isneginf(L_ref)
+    assert empty.sum() == 2 * w.block and np.all(np.isneginf(L[empty]))
+    assert np.abs(L[~empty] - L_ref[~empty]).max() <= gu.LSE_MAX_ABS
+
+
 # ------------------------------------------------------------ block-oracle selector
 #
 # [P3] section "质量差距有三个可分离来源": keep the blocks with the most exact attention

@@ -25,7 +25,7 @@ def _header_functions():
 
 def test_header_symbols_exported(lib):
     names = _header_functions()
-    assert len(names) == 19
+    assert len(names) == 20
     assert sorted(bb.EXPORTS) == names
     for n in names:
         assert getattr(lib, n) is not None  # dlsym succeeds
@@ -169,6 +169,29 @@ def test_forward_rejects_bad_arguments(lib):
     assert _fwd(index_mode=2 | bb.INDEX_PLANNED) == bb.ERR_INVALID_ARG
     assert _fwd(index_mode=1 | bb.INDEX_PLANNED, bitmap=None) == bb.ERR_INVALID_ARG
     assert _fwd(index_mode=0 | bb.INDEX_PLANNED, row_ptr=None) == bb.ERR_INVALID_ARG
+
+
+def _lse(**kw):
+    args = dict(Q=FAKE, K=FAKE, dt=bb.BF16, B=1, H=2, N=512, d=64, block=64, row_ptr=FAKE, col_idx=FAKE,
+                bitmap=FAKE, index_mode=0, scale=0.0, LSE=FAKE, workspace=FAKE, workspace_bytes=1 << 30)
+    args.update(kw)
+    with pytest.raises(bb.BsaError) as e:
+        bb.bsa_forward_lse(**args, stream=0)
+    return e.value.code
+
+
+def test_forward_lse_rejects_bad_arguments(lib):
+    assert _lse(N=0) == bb.ERR_SHAPE
+    assert _lse(d=32) == bb.ERR_SHAPE
+    assert _lse(dt=5) == bb.ERR_DTYPE
+    assert _lse(K=None) == bb.ERR_INVALID_ARG
+    assert _lse(LSE=None) == bb.ERR_INVALID_ARG
+    assert _lse(Q=FAKE + 8) == bb.ERR_INVALID_ARG
+    assert _lse(index_mode=2) == bb.ERR_INVALID_ARG
+    assert _lse(index_mode=bb.INDEX_PLANNED) == bb.ERR_INVALID_ARG  # no planned LSE-only call
+    assert _lse(index_mode=1, bitmap=None) == bb.ERR_INVALID_ARG
+    assert _lse(scale=float("nan")) == bb.ERR_INVALID_ARG
+    assert _lse(workspace_bytes=100) == bb.ERR_WORKSPACE
 
 
 def _plan(**kw):
