@@ -12,6 +12,25 @@
 
 namespace bsa {
 
+// Launch with programmatic stream serialisation: the grid may be scheduled while the
+// previous kernel on the stream drains; it waits for that kernel's results with
+// griddepcontrol.wait before reading them.
+template <typename... KArgs, typename... Args>
+inline bool pdl_launch(void (*kern)(KArgs...), dim3 grid, int threads, size_t smem, cudaStream_t st, Args... args)
+{
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(static_cast<unsigned>(threads));
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...) == cudaSuccess;
+}
+
 // Workspace header (first 256 bytes of every workspace).
 struct WsHeader {
     uint32_t err;          // first device-raised bsa_status (0 = none)

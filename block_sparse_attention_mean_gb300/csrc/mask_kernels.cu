@@ -24,12 +24,12 @@
 #include <cuda_runtime.h>
 #include <math_constants.h>
 
+
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace bsa {
 namespace {
-
-constexpr int kPoolThreads = 128;
 
 __device__ __forceinline__ uint32_t lanemask_lt()
 {
@@ -37,6 +37,8 @@ __device__ __forceinline__ uint32_t lanemask_lt()
     asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
     return m;
 }
+
+constexpr int kPoolThreads = 128;
 
 // ------------------------------------------------------------------ pooling
 
@@ -185,10 +187,11 @@ __device__ __forceinline__ int64_t row_base(int64_t bh, int i, int nQB, int n_te
 //   select_kernel  one warp per Q block: the row's keys in registers (key j in lane
 //                  j%32, slot j/32), an exact bitwise radix select of the k-th largest
 //                  key, and the bitmap and ascending CSR row.
-constexpr int kScoreTileQ = 64;
-constexpr int kScoreTileK = 128;
-constexpr int kScoreThreads = 256;
+constexpr int kScoreTile = 64;     // Q blocks and KV blocks of a score tile
+constexpr int kScoreThreads = 128;
+constexpr int kScoreChunk = 32;    // channels per staged chunk
 constexpr int kSelectWarps = 8;
+constexpr int kSelectCand = 128;   // candidate keys the prefiltered search holds (4 per lane)
 
 // Per-modality counts ("多模态DiT中的块稀疏注意力" §3.3): k[a][b] blocks kept among the
 // key blocks of modality b (0 text, 1 image) by a query block of modality a; the
@@ -310,6 +313,121 @@ __device__ __forceinline__ void kth_narrowing(const uint32_t (&x)[KPL], int k, i
     need = k - cU - static_cast<int>(__reduce_add_sync(0xffffffffu, y > T ? 1u : 0u));
 }
 
+// The k-th largest key among candidate keys gathered in buf[0, C) (NR words per lane,
+// slots past C read as 0, below every candidate), all of them in [L, M] with M the largest:
+// the bits above the highest bit in which L and M differ are M's, and the search decides
+// the rest. Also returns how many keys equal to it to keep, and how many candidates equal it.
+template <int NR>
+__device__ __forceinline__ void kth_of_candidates(const uint32_t *buf, int C, int k, uint32_t L, uint32_t M,
+                                                  int lane, uint32_t &T, int &need, int &n_eq)
+{
+    uint32_t y[NR];
+#pragma unroll
+    for (int r = 0; r < NR; ++r) y[r] = 32 * r + lane < C ? buf[32 * r + lane] : 0u;
+    const uint32_t D = L ^ M;
+    const int hb = D ? 31 - __clz(D) : -1;
+    T = D ? M & ~((2u << hb) - 1u) : M;
+    for (int bit = hb; bit >= 0; --bit) {
+        const uint32_t c = T | (1u << bit);
+        int n = 0;
+#pragma unroll
+        for (int r = 0; r < NR; ++r) n += __popc(__ballot_sync(0xffffffffu, y[r] >= c));
+        if (n >= k) T = c;
+    }
+    int g = 0, e = 0;
+#pragma unroll
+    for (int r = 0; r < NR; ++r) {
+        g += __popc(__ballot_sync(0xffffffffu, y[r] > T));
+        e += __popc(__ballot_sync(0xffffffffu, y[r] == T));
+    }
+    need = k - g;
+    n_eq = e;
+}
+
+// The k-th largest key of one row for 1 <= k <= 32 (slots outside the row hold 0). The k
+// lanes with the largest maxima each hold a key >= the k-th largest lane maximum, so that
+// maximum, and anything below it, is a lower bound on the k-th largest key; L is the k-th
+// largest lane maximum with its low 16 bits cleared (found on the top 16 bits only, which
+// is cheaper and still a lower bound). The k largest keys are all >= L; those keys (a few
+// dozen on typical rows) are gathered into buf (kSelectCand words of this warp's shared
+// memory) and searched bit by bit. Returns false, deciding nothing, when more than
+// kSelectCand keys are >= L.
+template <int KPL>
+__device__ __forceinline__ bool kth_prefiltered(const uint32_t (&x)[KPL], int k, int lane, uint32_t *buf,
+                                                uint32_t &T, int &need, int &n_eq)
+{
+    uint32_t mx = x[0];
+#pragma unroll
+    for (int m = 1; m < KPL; ++m) mx = max(mx, x[m]);
+    const uint32_t M = __reduce_max_sync(0xffffffffu, mx);
+    const uint32_t mn = __reduce_min_sync(0xffffffffu, mx);
+    // the k-th largest lane maximum lies in [mn, M]: search below their common top bits
+    const uint32_t D = (mn ^ M) & 0xFFFF0000u;
+    uint32_t L = M & 0xFFFF0000u;
+    if (D) {
+        const int hb = 31 - __clz(D);
+        L = M & ~((2u << hb) - 1u);
+        for (int bit = hb; bit >= 16; --bit) {
+            const uint32_t c = L | (1u << bit);
+            if (__popc(__ballot_sync(0xffffffffu, mx >= c)) >= k) L = c;
+        }
+    }
+    int C = 0;
+#pragma unroll
+    for (int m = 0; m < KPL; ++m) {
+        const bool in = x[m] >= L;
+        const uint32_t b = __ballot_sync(0xffffffffu, in);
+        const int at = C + __popc(b & lanemask_lt());
+        if (in && at < kSelectCand) buf[at] = x[m];
+        C += __popc(b);
+    }
+    __syncwarp();
+    if (C > kSelectCand) return false;
+    if (C <= 32)
+        kth_of_candidates<1>(buf, C, k, L, M, lane, T, need, n_eq);
+    else if (C <= 64)
+        kth_of_candidates<2>(buf, C, k, L, M, lane, T, need, n_eq);
+    else
+        kth_of_candidates<kSelectCand / 32>(buf, C, k, L, M, lane, T, need, n_eq);
+    return true;
+}
+
+// Bitmap words and ascending col_idx of one row of the plain selector: keys above T plus
+// the first `need` keys equal to T (ties: lower column first; all_ties: need is the number
+// of keys equal to T, so every key >= T is kept). Lane l stores the bitmap
+// words 32c + l.
+template <int KPL>
+__device__ __forceinline__ void emit_row_plain(const uint32_t (&kv)[KPL], int nKB, uint32_t T, int need,
+                                               bool all_ties, int W,
+                                               int64_t r_global, int64_t out_base, int32_t *__restrict__ col_idx,
+                                               uint32_t *__restrict__ bitmap, int lane)
+{
+    int taken = 0, ties = 0;
+    uint32_t word = 0;
+#pragma unroll
+    for (int m = 0; m < KPL; ++m) {
+        if (m >= W) break;
+        const int j = 32 * m + lane;
+        const bool valid = j < nKB;
+        bool sel;
+        if (all_ties) {  // every key equal to T is kept
+            sel = valid && kv[m] >= T;
+        } else {
+            const bool is_eq = valid && kv[m] == T;
+            const uint32_t eq = __ballot_sync(0xffffffffu, is_eq);
+            sel = (valid && kv[m] > T) || (is_eq && ties + __popc(eq & lanemask_lt()) < need);
+            ties += __popc(eq);
+        }
+        const uint32_t sel_mask = __ballot_sync(0xffffffffu, sel);
+        if (lane == (m & 31)) word = sel_mask;
+        if (sel) col_idx[out_base + taken + __popc(sel_mask & lanemask_lt())] = j;
+        taken += __popc(sel_mask);
+        if ((m & 31) == 31 || m == W - 1) {  // words m & ~31 .. m are complete
+            if ((m & ~31) + lane <= m) bitmap[r_global * W + (m & ~31) + lane] = word;
+        }
+    }
+}
+
 // Bitmap words and ascending col_idx of one row from its thresholds: text columns
 // [0, n_text) keep keys above TA plus the first needA equal to it, image columns keep
 // keys above TB plus the first needB equal to it (ties: lower column first).
@@ -341,105 +459,112 @@ __device__ __forceinline__ void emit_row_regs(const uint32_t (&kv)[KPL], int nKB
     }
 }
 
-// Shared memory of score_kernel: one 32-channel chunk of Qbar^T [32][64] and of
-// Kbar^T [32][128] (24 KB, so several CTAs share an SM and hide each other's staging).
-constexpr int kScoreChunk = 32;
-size_t score_smem(int) { return sizeof(float) * static_cast<size_t>(kScoreChunk) * (kScoreTileQ + kScoreTileK); }
+// Shared memory of score_kernel: two stages, each a 32-channel chunk of 64 Qbar rows and of
+// 64 Kbar rows, row-major with rows padded to 36 floats: the four consecutive Q rows and the
+// eight consecutive K rows a warp reads per channel quad start 16 bytes apart in the bank
+// space, so neither read conflicts, and every read is at a constant offset from the
+// thread's row base. 36 KB: six CTAs share an SM.
+constexpr int kScorePitch = kScoreChunk + 4;
+constexpr int kScoreStageFloats = 2 * kScoreTile * kScorePitch;
+size_t score_smem(int) { return sizeof(float) * 2 * static_cast<size_t>(kScoreStageFloats); }
 
-// Stages channels [c0, c0 + 32) of rows [row0, row0 + ROWS) of one head's pooled
-// blocks transposed into dst[32][ROWS] (absent rows past n as zeros). Consecutive
-// threads take consecutive rows of one channel quad, so a warp's shared-memory stores
-// are contiguous.
-template <int ROWS>
-__device__ __forceinline__ void stage_chunk(const float *__restrict__ src, int row0, int n, int d, int c0,
-                                            float *__restrict__ dst)
+__device__ __forceinline__ void cp_async16(float *dst, const float *src, bool valid)
 {
-    constexpr int Q4 = kScoreChunk / 4;  // channel quads per chunk
-    constexpr int PER = ROWS * Q4 / kScoreThreads;
-    static_assert(ROWS * Q4 % kScoreThreads == 0, "whole loads per thread");
-    const int d4 = d / 4;
-    const float4 *s4 = reinterpret_cast<const float4 *>(src);
-    float4 v[PER];
+    const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(dst));
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(d), "l"(src), "r"(valid ? 16 : 0)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+
+// Starts the copy of channels [c0, c0 + 32) of rows [row0, row0 + 64) of one head's
+// pooled blocks into dst (rows at or past n are zero-filled). Eight consecutive threads
+// copy one row's 128 bytes.
+__device__ __forceinline__ void stage_rows(const float *__restrict__ src, int row0, int n, int d, int c0,
+                                           float *__restrict__ dst)
+{
 #pragma unroll
-    for (int u = 0; u < PER; ++u) {
-        const int e = u * kScoreThreads + threadIdx.x;
-        const int r = e % ROWS, q = e / ROWS;
-        v[u] = row0 + r < n ? __ldg(s4 + static_cast<int64_t>(row0 + r) * d4 + c0 / 4 + q)
-                            : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-#pragma unroll
-    for (int u = 0; u < PER; ++u) {
-        const int e = u * kScoreThreads + threadIdx.x;
-        const int r = e % ROWS, q = e / ROWS;
-        dst[(4 * q + 0) * ROWS + r] = v[u].x;
-        dst[(4 * q + 1) * ROWS + r] = v[u].y;
-        dst[(4 * q + 2) * ROWS + r] = v[u].z;
-        dst[(4 * q + 3) * ROWS + r] = v[u].w;
+    for (int u = 0; u < kScoreTile * 8 / kScoreThreads; ++u) {
+        const int e = u * kScoreThreads + static_cast<int>(threadIdx.x);
+        const int r = e >> 3, q4 = e & 7;
+        const bool ok = row0 + r < n;
+        cp_async16(dst + r * kScorePitch + 4 * q4, ok ? src + static_cast<int64_t>(row0 + r) * d + c0 + 4 * q4 : src,
+                   ok);
     }
 }
 
-// grid (BH, nQB tiles, nKB tiles). Thread (warp w, lane l): rows 4(4(w%4) + l%4) .. +3
-// of the Q tile, columns 8(8(w/4) + l/4) .. +7 of the K tile; per channel a warp reads
-// 64 bytes of Qbar and 256 of Kbar (three shared-memory wavefronts) for 32 FMAs per
-// thread. Channels arrive 32 at a time; the accumulators carry each score's fmaf chain
-// on from chunk to chunk, so the order over channels is unchanged.
-__global__ void __launch_bounds__(kScoreThreads) score_kernel(const float *__restrict__ qbar,
+// grid (BH, nQB tiles, nKB tiles), 64 x 64 scores per CTA. Thread (warp w, lane l): rows
+// rg + 16a (rg = 4w + l%4, a < 4) and columns cg + 8n (cg = l/4, n < 8) of the tile. Per
+// 4-channel quad a thread loads 4 Q and 8 K quads (16 bytes each) for 128 FMAs. The chunk
+// after the current one is copied (cp.async) while the current one is consumed; the
+// accumulators carry each score's fmaf chain on from quad to quad and chunk to chunk, so
+// every score is one chain over channels 0..d-1 in order.
+__global__ void __launch_bounds__(kScoreThreads, 6) score_kernel(const float *__restrict__ qbar,
                                                              const float *__restrict__ kbar, int nQB, int nKB,
                                                              int d, uint32_t *__restrict__ keys, uint32_t *err)
 {
     extern __shared__ float4 sm4[];
-    float *qT = reinterpret_cast<float *>(sm4);          // [32][64]
-    float *kT = qT + kScoreChunk * kScoreTileQ;          // [32][128]
+    float *sm = reinterpret_cast<float *>(sm4);
     const int64_t bh = blockIdx.x;
-    const int i0 = blockIdx.y * kScoreTileQ, j0 = blockIdx.z * kScoreTileK;
+    const int i0 = blockIdx.y * kScoreTile, j0 = blockIdx.z * kScoreTile;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int rg = 4 * warp + (lane & 3);
+    const int cg = lane >> 2;
     const float *qsrc = qbar + bh * nQB * static_cast<int64_t>(d);
     const float *ksrc = kbar + bh * nKB * static_cast<int64_t>(d);
-    const int rg = 4 * (warp & 3) + (lane & 3);    // rows 4rg .. 4rg + 3
-    const int cg = 8 * (warp >> 2) + (lane >> 2);  // columns 8cg .. 8cg + 7 (cg < 16)
     float acc[4][8];
 #pragma unroll
     for (int a = 0; a < 4; ++a)
 #pragma unroll
         for (int n = 0; n < 8; ++n) acc[a][n] = 0.0f;
-    for (int c0 = 0; c0 < d; c0 += kScoreChunk) {
-        if (c0 > 0) __syncthreads();  // the previous chunk is consumed
-        stage_chunk<kScoreTileQ>(qsrc, i0, nQB, d, c0, qT);
-        stage_chunk<kScoreTileK>(ksrc, j0, nKB, d, c0, kT);
-        __syncthreads();
+    grid_dependency_wait();  // the pooled blocks come from the previous launch
+    const int nch = d / kScoreChunk;
+    stage_rows(qsrc, i0, nQB, d, 0, sm);
+    stage_rows(ksrc, j0, nKB, d, 0, sm + kScoreTile * kScorePitch);
+    cp_async_commit();
+    for (int ch = 0; ch < nch; ++ch) {
+        cp_async_wait_all();
+        __syncthreads();  // chunk ch is visible to every thread; the other stage is consumed
+        if (ch + 1 < nch) {
+            float *nx = sm + ((ch + 1) & 1) * kScoreStageFloats;
+            stage_rows(qsrc, i0, nQB, d, (ch + 1) * kScoreChunk, nx);
+            stage_rows(ksrc, j0, nKB, d, (ch + 1) * kScoreChunk, nx + kScoreTile * kScorePitch);
+        }
+        cp_async_commit();
+        const float *qs = sm + (ch & 1) * kScoreStageFloats + rg * kScorePitch;
+        const float *ks = sm + (ch & 1) * kScoreStageFloats + (kScoreTile + cg) * kScorePitch;
 #pragma unroll 4
-        for (int c = 0; c < kScoreChunk; ++c) {
-            const float4 q = *reinterpret_cast<const float4 *>(qT + c * kScoreTileQ + 4 * rg);
-            const float4 k0 = *reinterpret_cast<const float4 *>(kT + c * kScoreTileK + 8 * cg);
-            const float4 k1 = *reinterpret_cast<const float4 *>(kT + c * kScoreTileK + 8 * cg + 4);
-            const float qa[4] = {q.x, q.y, q.z, q.w};
-            const float ka[8] = {k0.x, k0.y, k0.z, k0.w, k1.x, k1.y, k1.z, k1.w};
+        for (int q4 = 0; q4 < kScoreChunk / 4; ++q4) {
+            float4 qv[4];
 #pragma unroll
             for (int a = 0; a < 4; ++a)
+                qv[a] = *reinterpret_cast<const float4 *>(qs + 16 * a * kScorePitch + 4 * q4);
 #pragma unroll
-                for (int n = 0; n < 8; ++n) acc[a][n] = __fmaf_rn(qa[a], ka[n], acc[a][n]);
+            for (int n = 0; n < 8; ++n) {
+                const float4 kv = *reinterpret_cast<const float4 *>(ks + 8 * n * kScorePitch + 4 * q4);
+#pragma unroll
+                for (int a = 0; a < 4; ++a) {
+                    acc[a][n] = __fmaf_rn(qv[a].x, kv.x, acc[a][n]);
+                    acc[a][n] = __fmaf_rn(qv[a].y, kv.y, acc[a][n]);
+                    acc[a][n] = __fmaf_rn(qv[a].z, kv.z, acc[a][n]);
+                    acc[a][n] = __fmaf_rn(qv[a].w, kv.w, acc[a][n]);
+                }
+            }
         }
     }
     bool nan_seen = false;
 #pragma unroll
     for (int a = 0; a < 4; ++a) {
-        const int i = i0 + 4 * rg + a;
+        const int i = i0 + rg + 16 * a;
         if (i >= nQB) continue;
-        const int j = j0 + 8 * cg;
-        uint32_t kk[8];
+        uint32_t *row = keys + (bh * nQB + i) * static_cast<int64_t>(nKB);
 #pragma unroll
         for (int n = 0; n < 8; ++n) {
-            nan_seen |= j + n < nKB && isnan(acc[a][n]);
-            kk[n] = order_key(acc[a][n]);
-        }
-        uint32_t *row = keys + (bh * nQB + i) * static_cast<int64_t>(nKB);
-        if (j + 7 < nKB && (nKB & 3) == 0) {
-            reinterpret_cast<uint4 *>(row + j)[0] = make_uint4(kk[0], kk[1], kk[2], kk[3]);
-            reinterpret_cast<uint4 *>(row + j)[1] = make_uint4(kk[4], kk[5], kk[6], kk[7]);
-        } else {
-#pragma unroll
-            for (int n = 0; n < 8; ++n)
-                if (j + n < nKB) row[j + n] = kk[n];
+            const int j = j0 + cg + 8 * n;
+            if (j < nKB) {
+                nan_seen |= isnan(acc[a][n]);
+                row[j] = order_key(acc[a][n]);
+            }
         }
     }
     if (nan_seen) raise_error(err, BSA_ERR_NONFINITE);
@@ -447,11 +572,9 @@ __global__ void __launch_bounds__(kScoreThreads) score_kernel(const float *__res
 
 // One warp per Q block row r (of BH * nQB): top-k of the row's keys, bitmap and CSR.
 template <int KPL>
-__global__ void __launch_bounds__(32 * kSelectWarps) select_kernel(const uint32_t *__restrict__ keys, int64_t R,
-                                                                   int nQB, int nKB, RegionK rk, int W,
-                                                                   int32_t *__restrict__ row_ptr,
-                                                                   int32_t *__restrict__ col_idx,
-                                                                   uint32_t *__restrict__ bitmap)
+__global__ void __launch_bounds__(32 * kSelectWarps, KPL <= 16 ? 4 : 1)
+    select_kernel(const uint32_t *__restrict__ keys, int64_t R, int nQB, int nKB, RegionK rk, int W,
+                  int32_t *__restrict__ row_ptr, int32_t *__restrict__ col_idx, uint32_t *__restrict__ bitmap)
 {
     const int lane = threadIdx.x & 31;
     const int64_t r = static_cast<int64_t>(blockIdx.x) * kSelectWarps + (threadIdx.x >> 5);
@@ -459,19 +582,31 @@ __global__ void __launch_bounds__(32 * kSelectWarps) select_kernel(const uint32_
     const int64_t bh = r / nQB;
     const int i = static_cast<int>(r % nQB);
     const uint32_t *row = keys + r * nKB;
+    grid_dependency_wait();  // the keys come from the previous launch
     uint32_t kv[1][KPL];
 #pragma unroll
     for (int m = 0; m < KPL; ++m) {
         const int j = 32 * m + lane;
         kv[0][m] = j < nKB ? __ldg(row + j) : 0u;
     }
-    __shared__ uint32_t gather[kSelectWarps][32];
+    __shared__ uint32_t gather[kSelectWarps][kSelectCand];
     uint32_t *buf = gather[threadIdx.x >> 5];
     const int qm = i < rk.n_text ? 0 : 1;
     uint32_t TA = 0xffffffffu, TB;
     int nA = 0, nB;
     if (rk.n_text == 0) {  // the plain selector: every column is in the image group
-        kth_narrowing<KPL>(kv[0], rk.k[qm][1], lane, buf, TB, nB);
+        const int k = rk.k[qm][1];
+        const int Ki = rk.k[1][0] + rk.k[1][1];
+        const int64_t base = static_cast<int64_t>(r) * Ki;
+        int n_eq = -1;
+        if (k < 1 || k > 32 || !kth_prefiltered<KPL>(kv[0], k, lane, buf, TB, nB, n_eq))
+            kth_narrowing<KPL>(kv[0], k, lane, buf, TB, nB);
+        emit_row_plain<KPL>(kv[0], nKB, TB, nB, n_eq == nB, W, r, base, col_idx, bitmap, lane);
+        if (lane == 0) {
+            row_ptr[r] = static_cast<int32_t>(base);
+            if (r == R - 1) row_ptr[R] = static_cast<int32_t>(base + Ki);
+        }
+        return;
     } else {
         uint32_t x[1][KPL];
         keys_in_range<1, KPL>(kv, 0, rk.n_text, lane, x);
@@ -491,9 +626,11 @@ __global__ void __launch_bounds__(32 * kSelectWarps) select_kernel(const uint32_
 template <int KPL>
 bsa_status launch_select(const uint32_t *keys, const MaskArgs &a, const RegionK &rk, int64_t R, cudaStream_t st)
 {
-    select_kernel<KPL><<<static_cast<unsigned>((R + kSelectWarps - 1) / kSelectWarps), 32 * kSelectWarps, 0, st>>>(
-        keys, R, a.nQB, a.nKB, rk, a.W, a.row_ptr, a.col_idx, a.bitmap);
-    return BSA_OK;
+    const dim3 g(static_cast<unsigned>((R + kSelectWarps - 1) / kSelectWarps));
+    return pdl_launch(select_kernel<KPL>, g, 32 * kSelectWarps, 0, st, keys, R, a.nQB, a.nKB, rk, a.W, a.row_ptr,
+                      a.col_idx, a.bitmap)
+               ? BSA_OK
+               : BSA_ERR_CUDA;
 }
 
 // ------------------------------------------------------------ static masks
@@ -806,16 +943,6 @@ bsa_status launch_build_mask(const MaskArgs &a, cudaStream_t st)
     int32_t *counts = reinterpret_cast<int32_t *>(a.ws + l.counts);
 
     if (a.spec == nullptr) {
-        const int64_t groups = BH * a.nQB * (a.d / 8);
-        dim3 pg(static_cast<unsigned>((groups + kPoolThreads - 1) / kPoolThreads), 2);
-        if (a.dt == BSA_BF16)
-            pool_kernel<__nv_bfloat16><<<pg, kPoolThreads, 0, st>>>(
-                static_cast<const __nv_bfloat16 *>(a.Q), static_cast<const __nv_bfloat16 *>(a.K), qbar,
-                kbar, groups, a.N, a.d, a.block, a.nQB);
-        else
-            pool_kernel<float><<<pg, kPoolThreads, 0, st>>>(static_cast<const float *>(a.Q),
-                                                            static_cast<const float *>(a.K), qbar, kbar,
-                                                            groups, a.N, a.d, a.block, a.nQB);
         RegionK rk{};
         rk.n_text = a.n_text;
         for (int x = 0; x < 2; ++x)
@@ -823,11 +950,27 @@ bsa_status launch_build_mask(const MaskArgs &a, cudaStream_t st)
         uint32_t *keys = reinterpret_cast<uint32_t *>(a.ws + l.keys);
         const size_t smem = score_smem(a.d);
         if (cudaFuncSetAttribute(score_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
-            cudaSuccess)
+                cudaSuccess ||
+            cudaFuncSetAttribute(score_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 cudaSharedmemCarveoutMaxShared) != cudaSuccess)
             return BSA_ERR_CUDA;
-        dim3 sg(static_cast<unsigned>(BH), (a.nQB + kScoreTileQ - 1) / kScoreTileQ,
-                (a.nKB + kScoreTileK - 1) / kScoreTileK);
-        score_kernel<<<sg, kScoreThreads, smem, st>>>(qbar, kbar, a.nQB, a.nKB, a.d, keys, err);
+        const int64_t groups = BH * a.nQB * (a.d / 8);
+        const dim3 pg(static_cast<unsigned>((groups + kPoolThreads - 1) / kPoolThreads), 2);
+        if (a.dt == BSA_BF16)
+            pool_kernel<__nv_bfloat16><<<pg, kPoolThreads, 0, st>>>(
+                static_cast<const __nv_bfloat16 *>(a.Q), static_cast<const __nv_bfloat16 *>(a.K), qbar, kbar,
+                groups, a.N, a.d, a.block, a.nQB);
+        else
+            pool_kernel<float><<<pg, kPoolThreads, 0, st>>>(static_cast<const float *>(a.Q),
+                                                            static_cast<const float *>(a.K), qbar, kbar, groups,
+                                                            a.N, a.d, a.block, a.nQB);
+        // the scoring and the selection wait for their inputs with griddepcontrol.wait, so each
+        // is set up while the launch before it drains
+        const dim3 sg(static_cast<unsigned>(BH), (a.nQB + kScoreTile - 1) / kScoreTile,
+                      (a.nKB + kScoreTile - 1) / kScoreTile);
+        if (!pdl_launch(score_kernel, sg, kScoreThreads, smem, st, static_cast<const float *>(qbar),
+                        static_cast<const float *>(kbar), a.nQB, a.nKB, a.d, keys, err))
+            return BSA_ERR_CUDA;
         // keys per lane of the register-held rows: nKB <= 32 * KPL
         const bsa_status s = a.nKB <= 128   ? launch_select<4>(keys, a, rk, R, st)
                              : a.nKB <= 512 ? launch_select<16>(keys, a, rk, R, st)

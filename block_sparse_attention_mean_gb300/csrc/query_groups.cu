@@ -774,22 +774,6 @@ __global__ void init_work_kernel(int32_t *__restrict__ work, int N, int64_t tota
     if (i < total) work[i] = static_cast<int32_t>(i % N);
 }
 
-template <typename... KArgs, typename... Args>
-bool pdl_launch(void (*kern)(KArgs...), dim3 grid, int threads, size_t smem, cudaStream_t st, Args... args)
-{
-    cudaLaunchConfig_t cfg{};
-    cfg.gridDim = grid;
-    cfg.blockDim = dim3(static_cast<unsigned>(threads));
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...) == cudaSuccess;
-}
-
 // Largest segment at `level`, in rows: repeated ceil/floor halving of G groups leaves
 // ceil(G / 2^level) groups at most.
 int max_segment_rows(int G, int level) { return ((G + (1 << level) - 1) >> level) * kTokenGroup; }

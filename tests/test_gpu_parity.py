@@ -651,6 +651,35 @@ def test_csr_and_bitmap_bitwise_identical_and_deterministic():
     assert torch.equal(O0, O2) and torch.equal(L0, L2)
 
 
+@pytest.mark.parametrize("H", [13])
+def test_build_eager_and_graph_replayed(H):
+    # the builder's launches (the scoring and the selection with programmatic dependent
+    # launch) captured in a CUDA graph: the eager build and two replays of the captured one
+    # all give the oracle's index
+    w = wl.scaled(wl.WORKLOADS["long_sweep_bs64"], H=H)
+    inp = wl.make_inputs(w)
+    q, k = gu.upload(inp, "q"), gu.upload(inp, "k")
+    mask = gu.oracle_mask(w, inp)
+    gu.assert_index_equal(gu.device_index(w, q, k), mask)
+    nB, W = w.nQB, (w.nQB + 31) // 32
+    cap = bb.bsa_mask_nnz(w.B, w.H, w.N, w.block, w.density, None)
+    rp = torch.empty(w.B * w.H * nB + 1, dtype=torch.int32, device="cuda")
+    ci = torch.empty(cap, dtype=torch.int32, device="cuda")
+    bm = torch.empty(w.B * w.H * nB * W, dtype=torch.int32, device="cuda")
+    ws = bb.workspace(0, w.B, w.H, w.N, w.d, w.block, q.device)
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        bb.bsa_build_mask(q, k, bb.BF16, w.B, w.H, w.N, w.d, w.block, w.density, None, rp, ci, cap, bm, ws,
+                          ws.numel(), torch.cuda.current_stream())
+    for _ in range(2):
+        rp.fill_(-1), ci.fill_(-1), bm.fill_(-1)
+        g.replay()
+        torch.cuda.synchronize()
+        assert bb.bsa_check_device_error(ws, s) == 0
+        gu.assert_index_equal(bb.Index(rp, ci, bm, cap, w.block), mask)
+
+
 def test_validate_index():
     w = wl.scaled(wl.WORKLOADS["dynamic_topk"], H=2, N=2048)
     inp = wl.make_inputs(w)
