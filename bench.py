@@ -660,7 +660,7 @@ def run_tokens(args):
                                "select_tokens": round(select_ms, 3)},
             "roofline": ({"bound": "tensor", "achieved": round(tflops, 3), "peak": float(peaks["bf16_tflops"]),
                           "unit": "TFLOP/s", "frac": round(tflops / float(peaks["bf16_tflops"]), 4),
-                          "kernel": "fwd_tc_kernel in token mode (rows gathered by index)",
+                          "kernel": "fwd_tc_kernel in token mode (Q rows by TMA gather, K and V rows by cp.async)",
                           "peak_source": f"{peak_kind} bf16_tflops (burst)"} if w.dtype == "bf16" else
                          # fp32 inputs run on CUDA cores: bounded by the fp32 FMA pipe
                          {"bound": "alu", "achieved": round(tflops, 3), "peak": FP32_FMA_TFLOPS,

@@ -104,6 +104,7 @@ struct TcParams {
     const int32_t *tokens;     // [B*H][N/128][n_tok]: each group's keys
     int n_tok;                 // keys per group
     int groups;                // query groups per head (N / 128)
+    const __nv_bfloat16 *Kg, *Vg; // K and V rows [B*H*N][D], copied by cp.async in token mode
 };
 
 struct Item {
@@ -259,6 +260,32 @@ __device__ __forceinline__ void gather_rows(const TcParams &p, const int32_t *id
     int v[4];
     gather_idx(idx, n, lane, v);
     gather_rows_of(p, v, bh, rows);
+}
+
+// Token mode: the 128 rows of a step (lane l holds the global rows of 4l .. 4l + 3, as
+// gather_rows_of gives them) copied into a K or V stage by 16-byte cp.async, in the
+// layout the TMA loads write: D/64 slabs of 128-byte rows, 16-byte chunk c of slab row r
+// at c ^ (r & 7) (the 128-byte swizzle; slabs are 1024-byte aligned). A warp instruction
+// covers 256 / D whole rows, so each copies whole 128-byte lines.
+template <int D>
+__device__ __forceinline__ void copy_rows_async(uint32_t dst, uint32_t slab_bytes, const __nv_bfloat16 *src, const int (&rows)[4], int lane)
+{
+    constexpr int CPR = D / 8, RPI = 32 / CPR;
+    const int rr = lane / CPR, cj = lane % CPR, sc = cj >> 3, ch = cj & 7;
+    const uint32_t slab = dst + sc * slab_bytes;
+#pragma unroll 4
+    for (int m = 0; m < 32; ++m) {
+        int r4[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) r4[i] = __shfl_sync(0xffffffffu, rows[i], m);
+#pragma unroll
+        for (int h = 0; h < 4 / RPI; ++h) {
+            const int k = RPI * h + rr;
+            const int grow = k == 0 ? r4[0] : k == 1 ? r4[1] : k == 2 ? r4[2] : r4[3];
+            const int r = 4 * m + k;
+            cp_async16(slab + r * 128 + ((ch ^ (r & 7)) << 4), src + static_cast<int64_t>(grow) * D + sc * 64 + ch * 8);
+        }
+    }
 }
 
 template <int BS>
@@ -1088,15 +1115,21 @@ __global__ void __launch_bounds__((4 * SPLIT + 4) * 32, MINB)
     const bool stall = (p.dbg & kDbgStall) != 0u;
 
     if (TOK && warp == kProducerWarp) {
-        // ------------------------------------------------------------ token mode: tiles, Q and K by gather
+        // ------------------------------------------------------------ token mode: tiles, Q and K
         // Every tile (one query group) has the same steps, so CTA b takes tiles b, b + grid,
-        // ... in order. Q rows come through the permutation, K rows through the group's
-        // token list, four rows per gather and every lane issuing its own rows.
+        // ... in order. Q rows come through the permutation by TMA gathers (four rows per
+        // gather, every lane issuing its own rows). K rows come through the group's token
+        // list by cp.async: the TMA engine's gathers of scattered rows ran at about 3 TB/s
+        // and set the pace of a step, the load/store path moves them faster. A step is
+        // published one step late: once its copies have landed (wait_group 1 while the next
+        // step's are in flight) and been fenced for the tensor-core reads, one lane arrives on
+        // its K-full barrier with the step descriptor; a tile's last step is published before
+        // the next tile's Q slot is awaited.
         if constexpr (TOK) {
             const int steps = (p.n_tok + kTileM - 1) / kTileM;
             const bool ragged = p.n_tok % kTileM != 0;
-            int G = 0, e = 0, tcount = 0;
-            int last_issue = -1, q_issued = -1;
+            int G = 0, e = 0, tcount = 0, kpend = -1;  // kpend: the step copied but not yet published
+            int q_issued = -1;
             bool ok = true;
             while (ok) {
                 const int slot = tcount & 1;
@@ -1139,35 +1172,42 @@ __global__ void __launch_bounds__((4 * SPLIT + 4) * 32, MINB)
                     if (lane == 0) {
                         const uint32_t ms[2] = {3u, 0u};
                         kdesc[ks] = step_desc(1, ms, st == steps - 1, ragged && st == steps - 1 ? 1u : 0u);
-                        mbar_arrive_expect_tx(bar(C::B_KFULL + ks), static_cast<uint32_t>(kTileM * D * 2));
                     }
-                    __syncwarp();
-#pragma unroll
-                    for (int c = 0; c < D / 64; ++c)
-                        tma_gather4(sbase + C::K_OFF + ks * C::kKVBytes + c * C::kKVChunk + lane * 512, &tmK,
-                                    c * 64, rows[0], rows[1], rows[2], rows[3], bar(C::B_KFULL + ks));
-                    __syncwarp();
-                    last_issue = G;
+                    copy_rows_async<D>(sbase + C::K_OFF + ks * C::kKVBytes, C::kKVChunk, p.Kg, rows, lane);
+                    cp_async_commit();
+                    if (kpend >= 0) {
+                        cp_async_wait_group<1>();
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(bar(C::B_KFULL + kpend % NK));
+                    }
+                    kpend = G;
                     ++G;
+                }
+                if (kpend >= 0) {
+                    cp_async_wait_group<0>();
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar(C::B_KFULL + kpend % NK));
+                    kpend = -1;
                 }
                 ++e;
             }
+            // never leave while our copies or gathers may still land in shared memory
+            cp_async_wait_group<0>();
             if (lane == 0 && *ctl.abort_flag) {
-                // never leave while our gathers may still land in shared memory
-                for (int g = last_issue - NK + 1; g <= last_issue; ++g)
-                    if (g >= 0) wait_bar_drain(bar(C::B_KFULL + g % NK), (g / NK) & 1, p.wait_limit_ns);
                 for (int e2 = q_issued - (QS - 1) < 0 ? 0 : q_issued - (QS - 1); e2 <= q_issued; ++e2)
                     wait_bar_drain(bar(C::B_QFULL + e2 % QS), (e2 / QS) & 1, p.wait_limit_ns);
             }
             __syncwarp();
         }
     } else if (TOK && warp == kVProducerWarp) {
-        // ------------------------------------------------------------ token mode: V by gather
+        // ------------------------------------------------------------ token mode: V by cp.async
+        // Like K: the step's rows copied by cp.async, published one step late on V-full.
         if constexpr (TOK) {
             if (!stall) {
                 const int steps = (p.n_tok + kTileM - 1) / kTileM;
-                int G = 0, tcount = 0;
-                int last_issue = -1;
+                int G = 0, tcount = 0, vpend = -1;  // vpend: the step copied but not yet published
                 bool ok = true;
                 while (ok) {
                     int tile;
@@ -1187,22 +1227,26 @@ __global__ void __launch_bounds__((4 * SPLIT + 4) * 32, MINB)
                             ok = false;
                             break;
                         }
-                        if (lane == 0)
-                            mbar_arrive_expect_tx(bar(C::B_VFULL + vs), static_cast<uint32_t>(kTileM * D * 2));
-                        __syncwarp();
-#pragma unroll
-                        for (int c = 0; c < D / 64; ++c)
-                            tma_gather4(sbase + C::V_OFF + vs * C::kKVBytes + c * C::kKVChunk + lane * 512, &tmV,
-                                        c * 64, rows[0], rows[1], rows[2], rows[3], bar(C::B_VFULL + vs));
-                        __syncwarp();
-                        last_issue = G;
+                        copy_rows_async<D>(sbase + C::V_OFF + vs * C::kKVBytes, C::kKVChunk, p.Vg, rows, lane);
+                        cp_async_commit();
+                        if (vpend >= 0) {
+                            cp_async_wait_group<1>();
+                            fence_proxy_async_smem();
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(bar(C::B_VFULL + vpend % NV));
+                        }
+                        vpend = G;
                         ++G;
                     }
+                    if (vpend >= 0) {
+                        cp_async_wait_group<0>();
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(bar(C::B_VFULL + vpend % NV));
+                        vpend = -1;
+                    }
                 }
-                if (lane == 0 && *ctl.abort_flag) {
-                    for (int g = last_issue - NV + 1; g <= last_issue; ++g)
-                        if (g >= 0) wait_bar_drain(bar(C::B_VFULL + g % NV), (g / NV) & 1, p.wait_limit_ns);
-                }
+                cp_async_wait_group<0>();  // never leave while copies may still land in shared memory
                 __syncwarp();
             }
         }
@@ -2266,6 +2310,8 @@ bsa_status launch_tc_tokens(const TokenArgs &a, cudaStream_t st)
     p.ragged_kb = -1;
     p.perm = a.perm;
     p.tokens = a.tokens;
+    p.Kg = static_cast<const __nv_bfloat16 *>(a.K);
+    p.Vg = static_cast<const __nv_bfloat16 *>(a.V);
     p.scale_log2 = a.scale * 1.4426950408889634f;
     p.O = static_cast<__nv_bfloat16 *>(a.O);
     p.LSE = a.LSE;
@@ -2283,7 +2329,7 @@ bsa_status launch_forward_tokens_tc(const TokenArgs &a, cudaStream_t st)
 {
     // the block-128 instances' stages and layouts: <D, K stages, V stages, S/P buffers, Q slots, threads per row, CTAs per SM>
     if (a.d == 64) return launch_tc_tokens<64, 5, 6, 3, 2, 2, 1>(a, st);
-    if (a.d == 128) return launch_tc_tokens<128, 2, 4, 3, 1, 2, 1>(a, st);
+    if (a.d == 128) return launch_tc_tokens<128, 3, 3, 3, 1, 2, 1>(a, st);  // 3 + 3 stages: measured best
     return BSA_ERR_SHAPE;
 }
 

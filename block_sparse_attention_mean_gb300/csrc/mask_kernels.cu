@@ -468,28 +468,19 @@ constexpr int kScorePitch = kScoreChunk + 4;
 constexpr int kScoreStageFloats = 2 * kScoreTile * kScorePitch;
 size_t score_smem(int) { return sizeof(float) * 2 * static_cast<size_t>(kScoreStageFloats); }
 
-__device__ __forceinline__ void cp_async16(float *dst, const float *src, bool valid)
-{
-    const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(dst));
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(d), "l"(src), "r"(valid ? 16 : 0)
-                 : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
-
 // Starts the copy of channels [c0, c0 + 32) of rows [row0, row0 + 64) of one head's
 // pooled blocks into dst (rows at or past n are zero-filled). Eight consecutive threads
 // copy one row's 128 bytes.
 __device__ __forceinline__ void stage_rows(const float *__restrict__ src, int row0, int n, int d, int c0,
-                                           float *__restrict__ dst)
+                                           uint32_t dst)
 {
 #pragma unroll
     for (int u = 0; u < kScoreTile * 8 / kScoreThreads; ++u) {
         const int e = u * kScoreThreads + static_cast<int>(threadIdx.x);
         const int r = e >> 3, q4 = e & 7;
         const bool ok = row0 + r < n;
-        cp_async16(dst + r * kScorePitch + 4 * q4, ok ? src + static_cast<int64_t>(row0 + r) * d + c0 + 4 * q4 : src,
-                   ok);
+        cp_async16(dst + 4u * static_cast<uint32_t>(r * kScorePitch + 4 * q4),
+                   ok ? src + static_cast<int64_t>(row0 + r) * d + c0 + 4 * q4 : src, ok ? 16u : 0u);
     }
 }
 
@@ -519,16 +510,17 @@ __global__ void __launch_bounds__(kScoreThreads, 6) score_kernel(const float *__
         for (int n = 0; n < 8; ++n) acc[a][n] = 0.0f;
     grid_dependency_wait();  // the pooled blocks come from the previous launch
     const int nch = d / kScoreChunk;
-    stage_rows(qsrc, i0, nQB, d, 0, sm);
-    stage_rows(ksrc, j0, nKB, d, 0, sm + kScoreTile * kScorePitch);
+    const uint32_t sm_u = smem_u32(sm);
+    stage_rows(qsrc, i0, nQB, d, 0, sm_u);
+    stage_rows(ksrc, j0, nKB, d, 0, sm_u + 4u * kScoreTile * kScorePitch);
     cp_async_commit();
     for (int ch = 0; ch < nch; ++ch) {
-        cp_async_wait_all();
+        cp_async_wait_group<0>();
         __syncthreads();  // chunk ch is visible to every thread; the other stage is consumed
         if (ch + 1 < nch) {
-            float *nx = sm + ((ch + 1) & 1) * kScoreStageFloats;
+            const uint32_t nx = sm_u + 4u * ((ch + 1) & 1) * kScoreStageFloats;
             stage_rows(qsrc, i0, nQB, d, (ch + 1) * kScoreChunk, nx);
-            stage_rows(ksrc, j0, nKB, d, (ch + 1) * kScoreChunk, nx + kScoreTile * kScorePitch);
+            stage_rows(ksrc, j0, nKB, d, (ch + 1) * kScoreChunk, nx + 4u * kScoreTile * kScorePitch);
         }
         cp_async_commit();
         const float *qs = sm + (ch & 1) * kScoreStageFloats + rg * kScorePitch;
