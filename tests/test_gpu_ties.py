@@ -7,8 +7,11 @@ small palette, so many block scores are exactly equal: small-integer dot product
 all-zero key blocks, -0 from one tiny product that underflows in the last channel, and +inf /
 -inf from one product that overflows. The selection must equal the oracle's bit for bit
 (value descending with -0 equal to +0, ties to the lower block index) in CSR and bitmap, at
-both block sizes, with 72 key blocks so that tie groups straddle the 32-bit words of the
-bitmap. The data are checked to contain each kind of tie at the k-th position.
+both block sizes, with 72 or 300 key blocks so that tie groups straddle the 32-bit words of the
+bitmap. The data are checked to contain each kind of tie at the k-th position. The three
+densities take the selector's three searches: k = 36 of 72 the full-row search (k > 32); k = 18
+of 72 the search over the keys above the lane-maximum bound (at most 72 of them); k = 30 of 300
+both, about half the rows holding more than 128 keys above the bound and falling back.
 """
 import numpy as np
 import pytest
@@ -87,9 +90,10 @@ def tie_coverage(q, k, bs, kk):
 
 
 @pytest.mark.gpu
+@pytest.mark.parametrize("nB,density", [(72, 0.5), (72, 0.25), (300, 0.1)])
 @pytest.mark.parametrize("block,d", [(64, 128), (128, 128), (64, 64)])
-def test_selection_on_exact_ties_matches_oracle(block, d):
-    H, nB, density = 4, 72, 0.5
+def test_selection_on_exact_ties_matches_oracle(block, d, nB, density):
+    H = 4
     q, k = tie_inputs(H, nB, block, d, seed=block + d)
     N = nB * block
     kk = oracle.topk_count(density, nB)
