@@ -4,10 +4,12 @@
 // the quality gap in diffusion transformers" (mean-pooled block scoring):
 //   pool_kernel        Q, K [BH][N][d] -> Qbar, Kbar fp32 [BH][nB][d]   (HBM-bound)
 //   score_kernel       every (Q block, KV block) score (fmaf chains, outer-product
-//                      tiling) as an order-preserving key in the workspace
+//                      tiling, cp.async-staged chunks) as an order-preserving key in
+//                      the workspace
 //   select_kernel      per Q block: exact top-k by a bitwise radix select on the
-//                      keys held in registers, emits the bitmap row and the CSR
-//                      row (row_ptr = r * k, no scan).
+//                      keys held in registers (over the few keys above a lane-maximum
+//                      bound where k <= 32), emits the bitmap row and the CSR row
+//                      (row_ptr = r * k, no scan).
 // Static mode evaluates the block predicates of "多模态DiT中的块稀疏注意力" §3.1-§3.2
 // (text dense + image band + anchors, or video cuboids + faces + text) or copies
 // an explicit bitmap:
@@ -178,12 +180,12 @@ __device__ __forceinline__ int64_t row_base(int64_t bh, int i, int nQB, int n_te
 // Scores of every (Q block, KV block) pair of a head, then top-k per Q block, in two
 // launches:
 //   score_kernel   an outer-product tiling over channels (the SGEMM pattern): a CTA
-//                  stages a 64-row Qbar tile and a 128-row Kbar tile transposed in
-//                  shared memory ([channel][block]) and each thread accumulates a
-//                  4 x 8 block of scores, so every staged value feeds 8 or 4 FMAs and
-//                  a head's Kbar is read nQB/64 times, not once per Q block. Each score
-//                  is still one fmaf chain over channels 0..d-1 in order from +0. The
-//                  scores go to the workspace as order-preserving keys [BH][nQB][nKB].
+//                  stages 32-channel chunks of a 64-row Qbar tile and a 64-row Kbar
+//                  tile in shared memory and each thread accumulates a 4 x 8 block of
+//                  scores, so every staged value feeds 8 or 4 FMAs and a head's Kbar is
+//                  read nQB/64 times, not once per Q block. Each score is still one fmaf
+//                  chain over channels 0..d-1 in order from +0. The scores go to the
+//                  workspace as order-preserving keys [BH][nQB][nKB].
 //   select_kernel  one warp per Q block: the row's keys in registers (key j in lane
 //                  j%32, slot j/32), an exact bitwise radix select of the k-th largest
 //                  key, and the bitmap and ascending CSR row.

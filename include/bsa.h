@@ -368,8 +368,9 @@ bsa_status bsa_tokens_per_group(int N, float density, int *n_tokens);
  * (null or misaligned pointers, n_tokens out of range, non-finite scale),
  * BSA_ERR_WORKSPACE. An index outside [0, N) in perm or tokens raises BSA_ERR_INVALID_ARG in
  * the workspace (the row or key is then not computed as asked: the results are undefined).
- * bf16 runs on tcgen05: a 128-query group is one tile, its keys arrive 128 per step with rows
- * gathered by index (TMA tile::gather4), the last step masked. fp32 runs on CUDA cores.
+ * bf16 runs on tcgen05: a 128-query group is one tile (its query rows gathered by TMA
+ * tile::gather4), its keys arrive 128 per step with the K and V rows copied by index
+ * (cp.async), the last step masked. fp32 runs on CUDA cores.
  */
 bsa_status bsa_forward_tokens(const void *Q, const void *K, const void *V, int dt, int B, int H, int N, int d,
                               const int32_t *perm, const int32_t *tokens, int n_tokens, float scale, void *O,
