@@ -68,9 +68,8 @@ def test_dynamic_topk_small_all_rows():
 
 @pytest.mark.parametrize("nB", [128, 130, 200, 257])
 def test_selector_score_tiles_all_columns(nB):
-    # the scorer works on 64 x 128 tiles of (Q block, KV block) pairs: every column of a
-    # full tile, a ragged second tile of Q rows and of KV columns, and a row that is not
-    # a multiple of 4 keys (scalar score stores)
+    # the scorer works on 64 x 64 tiles of (Q block, KV block) pairs: full tiles (128), and
+    # ragged last tiles of Q rows and of KV columns holding 2, 8 and 1 blocks (130, 200, 257)
     w = wl.scaled(wl.WORKLOADS["dynamic_topk"], H=1, N=64 * nB, density=0.2)
     inp = wl.make_inputs(w)
     q, k = gu.upload(inp, "q"), gu.upload(inp, "k")
@@ -378,6 +377,25 @@ def test_planned_forward_equals_unplanned(name, flags):
     gu.assert_attention_close(O0, L0, inp, mask, w)
 
 
+@pytest.mark.parametrize("name", ["t2i_static", "video_cuboid"])
+def test_planned_forward_full_size_static_masks(name):
+    # the configurations the bench plans once: at full size, three planned calls equal the
+    # unplanned call bit for bit, and sampled rows match the oracle
+    w = wl.WORKLOADS[name]
+    inp = wl.make_inputs(w)
+    q, k, v = (gu.upload(inp, n) for n in ("q", "k", "v"))
+    mask = gu.oracle_mask(w, inp)
+    idx = gu.device_index(w, q, k, mask)
+    O0, L0 = bb.forward(q, k, v, idx, index_mode=w.index_mode)
+    ws = bb.forward_plan(q, idx, index_mode=w.index_mode)
+    for _ in range(3):
+        O, L = bb.forward(q, k, v, idx, index_mode=w.index_mode | bb.INDEX_PLANNED, ws=ws)
+        torch.cuda.synchronize()
+        assert torch.equal(O, O0) and torch.equal(L, L0)
+    rng = np.random.default_rng(21)
+    gu.assert_attention_close(O0, L0, inp, mask, w, rows=gu.sample_rows(w, rng, blocks_per_head=4, rows_per_block=4))
+
+
 def test_planned_fp32_forward_is_the_plain_forward():
     # the CUDA-core fp32 forward keeps no work list: planning is a no-op and the planned flag
     # changes nothing
@@ -483,6 +501,31 @@ def test_forward_lse_dense_and_empty_rows():
     empty = np.isneginf(L_ref)
     assert empty.sum() == 2 * w.block and np.all(np.isneginf(L[empty]))
     assert np.abs(L[~empty] - L_ref[~empty]).max() <= gu.LSE_MAX_ABS
+
+
+def test_forward_lse_full_size_dense_anchor_pass():
+    # the token path's anchor pass at its working shape (B1 H24 N8192 d128): the LSE-only
+    # forward over an all-active block-128 index equals the full forward's LSE bit for bit and
+    # the oracle's dense LSE on sampled rows
+    w = wl.scaled(wl.WORKLOADS["dynamic_topk"], block=128)
+    inp = wl.make_inputs(w)
+    q, k, v = (gu.upload(inp, n) for n in ("q", "k", "v"))
+    nb = w.N // 128
+    full = np.ones((w.B, w.H, nb, nb), dtype=np.uint8)
+    idx = bb.build_mask(None, None, 128, spec=bb.explicit_spec(
+        torch.from_numpy(gu.mask_bitmap_words(full).reshape(-1)).cuda()), shape=(w.B, w.H, w.N, w.d))
+    L = bb.forward_lse(q, k, idx)
+    bb.bsa_debug_config(bb.DBG_NO_SPLIT, 0)
+    try:
+        _, L0 = bb.forward(q, k, v, idx)
+    finally:
+        bb.bsa_debug_config(0, 0)
+    torch.cuda.synchronize()
+    assert torch.equal(L, L0)
+    rng = np.random.default_rng(22)
+    rows = gu.sample_rows(w, rng, blocks_per_head=4, rows_per_block=4)
+    _, L_ref = oracle.attention(inp["q"], inp["k"], inp["v"], full, 128, rows=rows)
+    assert np.abs(L.reshape(-1).cpu().numpy().astype(np.float64)[rows] - L_ref).max() <= gu.LSE_MAX_ABS
 
 
 # ------------------------------------------------------------ block-oracle selector
