@@ -417,12 +417,19 @@ def run_ours(args, world, rank, local):
     if args.e2e_steps > 0:
         BHt = B * H
         moved = sum(t.numel() * t.element_size() for t in (q, k, v, O, LSE))
+        # about 128 MB per chunk (more chunks cost more than they overlap on small steps: dynamic_topk
+        # in 4 chunks took 1.39 ms against 1.20 ms in one)
         C = args.e2e_chunks if args.e2e_chunks > 0 else max(1, moved // (128 << 20))
         while C > 1 and BHt % C != 0:
             C -= 1  # whole heads per chunk
         if spec is not None and spec.kind == bb.STATIC_EXPLICIT:
             C = 1  # a per-head explicit bitmap is not split by head here
         hc = BHt // C
+        # chunks of hc heads; without a shared plan the last chunk is split into single heads, so
+        # that the compute and copy-out left after the last copy-in are one head's
+        spans = [(c * hc, (c + 1) * hc) for c in range(C)]
+        if not planned and C > 1 and hc > 1:
+            spans = spans[:-1] + [(h, h + 1) for h in range((C - 1) * hc, C * hc)]
         hq, hk, hv = (t.cpu().pin_memory() for t in (q, k, v))
         hO = torch.empty(O.shape, dtype=O.dtype).pin_memory()
         hL = torch.empty(LSE.shape, dtype=LSE.dtype).pin_memory()
@@ -443,16 +450,16 @@ def run_ours(args, world, rank, local):
             bb.bsa_forward_plan(dt, 1, hc, N, d, bs, rp_c, ci_c, bm_c, w.index_mode, wsf_c, wsf_c.numel(), s_cmp)
             mode_c |= bb.INDEX_PLANNED
 
-        def chunk_compute(c, st):
-            sl = slice(c * hc, (c + 1) * hc)
+        def chunk_compute(h0, h1, st):
+            sl, nh = slice(h0, h1), h1 - h0
             qc, kc, vc = dq[sl], dk[sl], dv[sl]
-            bb.bsa_build_mask(None if spec is not None else qc, None if spec is not None else kc, dt, 1, hc, N, d,
+            bb.bsa_build_mask(None if spec is not None else qc, None if spec is not None else kc, dt, 1, nh, N, d,
                               bs, w.density, spec, rp_c, ci_c, cap_c, bm_c, wsm_c, wsm_c.numel(), st)
             if R is None:
-                bb.bsa_forward(qc, kc, vc, dt, 1, hc, N, d, bs, rp_c, ci_c, bm_c, mode_c, 0.0, dO[sl], dL[sl],
+                bb.bsa_forward(qc, kc, vc, dt, 1, nh, N, d, bs, rp_c, ci_c, bm_c, mode_c, 0.0, dO[sl], dL[sl],
                                wsf_c, wsf_c.numel(), st)
             else:
-                bb.bsa_forward_residual(qc, kc, vc, dt, 1, hc, N, d, bs, rp_c, ci_c, bm_c, mode_c, 0.0,
+                bb.bsa_forward_residual(qc, kc, vc, dt, 1, nh, N, d, bs, rp_c, ci_c, bm_c, mode_c, 0.0,
                                         R.reshape(BHt, N, d)[sl], dO[sl], dL[sl], wsf_c, wsf_c.numel(), st)
 
         e2e_ms = []
@@ -460,8 +467,8 @@ def run_ours(args, world, rank, local):
             torch.cuda.synchronize()
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(s_in)
-            for c in range(C):
-                sl = slice(c * hc, (c + 1) * hc)
+            for h0, h1 in spans:
+                sl = slice(h0, h1)
                 with torch.cuda.stream(s_in):
                     dq[sl].copy_(sq[sl], non_blocking=True)
                     dk[sl].copy_(sk[sl], non_blocking=True)
@@ -469,7 +476,7 @@ def run_ours(args, world, rank, local):
                     ev_in = torch.cuda.Event()
                     ev_in.record(s_in)
                 s_cmp.wait_event(ev_in)
-                chunk_compute(c, s_cmp)
+                chunk_compute(h0, h1, s_cmp)
                 ev_c = torch.cuda.Event()
                 ev_c.record(s_cmp)
                 s_out.wait_event(ev_c)
@@ -484,19 +491,29 @@ def run_ours(args, world, rank, local):
             code = bb.bsa_check_device_error(ws, s_cmp)
             if code != 0:
                 raise bb.BsaError(code, "end-to-end steps")
-        # heads are independent: the chunked calls must give the unchunked step's outputs exactly
+        # heads are independent, so the chunked calls give the unchunked step's outputs: bit for bit
+        # when no query tile is split, else to rounding (a chunk of fewer heads can split its longest
+        # tiles differently, and split tiles merge their partial sums in another order)
         torch.cuda.synchronize()
         build_call(stream)
         fwd_call(stream)
         torch.cuda.synchronize()
-        if not (torch.equal(hO, O.cpu()) and torch.equal(hL, LSE.cpu())):
-            raise RuntimeError("end-to-end outputs differ from the unchunked step's")
+        O_ref, L_ref = O.cpu(), LSE.cpu()
+        e2e_exact = torch.equal(hO, O_ref) and torch.equal(hL, L_ref)
+        if not e2e_exact:
+            o_err = (hO.float() - O_ref.float()).abs().max().item()
+            fin = torch.isfinite(L_ref)
+            l_err = (hL[fin] - L_ref[fin]).abs().max().item() if fin.any() else 0.0
+            if not (o_err <= 2e-2 and l_err <= 1e-3 and torch.equal(torch.isfinite(hL), fin)):
+                raise RuntimeError(f"end-to-end outputs differ from the unchunked step's (O {o_err}, LSE {l_err})")
         h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
         d2h = hO.numel() * hO.element_size() + hL.numel() * hL.element_size()
         e2e_mean = max_over_ranks(sum(e2e_ms) / len(e2e_ms), dev)
         e2e = {"value": round(job_throughput(flops, world, 1, e2e_mean), 3), "unit": "TFLOP/s",
                "ms_per_step": round(e2e_mean, 4), "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-               "pipeline": f"{C} chunks of {hc} heads: copy-in, mask build + forward, copy-out on three streams"}
+               "pipeline": f"{len(spans)} chunks of {'/'.join(str(b - a) for a, b in spans)} heads: copy-in, mask build + "
+                           "forward, copy-out on three streams",
+               "outputs": "equal to the unchunked step's" if e2e_exact else "within rounding of the unchunked step's"}
 
     if rank != 0:
         if world > 1:
