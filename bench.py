@@ -326,7 +326,16 @@ def run_ours(args, world, rank, local):
             bb.bsa_forward_residual(q, k, v, dt, B, H, N, d, bs, row_ptr, col_idx, bitmap, fwd_mode[0], 0.0, R, O,
                                     LSE, ws_f, ws_f.numel(), s)
 
-    launches_per_step = (3 if spec is not None else 2) + (1 if dt == bb.FP32 or planned else 2)
+    # kernels of one step: the build (pooling, scoring, selection for a dynamic mask; pattern and
+    # copy for a shared static pattern; rows, scan and emit for a per-head bitmap), then the
+    # forward (work list or plan gate, and the forward kernel; one CUDA-core kernel for fp32)
+    if spec is None:
+        build_launches = 3
+    elif spec.kind != bb.STATIC_EXPLICIT or spec.broadcast_bh:
+        build_launches = 2
+    else:
+        build_launches = 3
+    launches_per_step = build_launches + (1 if dt == bb.FP32 else 2)
 
     with torch.cuda.stream(stream):
         for _ in range(max(args.warmup, 3)):
