@@ -847,6 +847,18 @@ def test_selector_at_the_largest_key_block_counts(N):
     run_workload(w, rows=gu.sample_rows(w, rng, blocks_per_head=8, rows_per_block=4))
 
 
+@pytest.mark.parametrize("nB,density", [(1500, 0.01), (2048, 0.015)])
+def test_selector_widest_rows_small_k(nB, density):
+    # 64 keys per lane with k = 14 / 30 <= 32: the search over the keys above the lane-maximum
+    # bound on the widest register rows (a ragged last word at 1500); the index bit for bit
+    w = wl.scaled(wl.WORKLOADS["long_sweep_bs64"], H=2, N=64 * nB, density=density)
+    assert 1 <= oracle.topk_count(density, nB) <= 32
+    inp = wl.make_inputs(w)
+    q, k = gu.upload(inp, "q"), gu.upload(inp, "k")
+    mask = gu.oracle_mask(w, inp)
+    gu.assert_index_equal(gu.device_index(w, q, k, mask), mask)
+
+
 @pytest.mark.parametrize("name", ["long_sweep_bs64", "long_sweep_bs128"])
 def test_full_block_size_sweep(name):
     w = wl.WORKLOADS[name]
