@@ -6,8 +6,10 @@
 // visited, and the output is divided by the true sum over the active blocks).
 //
 // Design (GB300-first, not the pages' Triton/xFormers recipes):
-//   * Persistent CTAs pull work items from a longest-first list with an atomic
-//     counter (rows with very different active counts, §5.3). An item is a
+//   * Persistent CTAs pull work items from a list with an atomic counter: items of
+//     at least an eighth of the per-CTA share of steps longest first (rows with very
+//     different active counts, §5.3), the rest in tile order (a head's tiles together,
+//     its K and V in L2). An item is a
 //     128-row query tile, or one KV-range chunk of a tile that is far longer than
 //     the per-CTA share of steps; the last chunk to finish merges the chunks'
 //     partial (O, max, sums).
@@ -87,7 +89,7 @@ struct TcParams {
     float scale_log2;
     __nv_bfloat16 *O;
     float *LSE;
-    const int32_t *tile_list;  // work items, longest first
+    const int32_t *tile_list;  // work items: long ones longest first, the rest in tile order
     const uint32_t *n_items;
     uint32_t *tile_counter;
     uint32_t *err;
@@ -1643,10 +1645,16 @@ __device__ __forceinline__ int n_chunks(int len, int share, uint32_t dbg)
     return n < kMaxChunks ? n : kMaxChunks;
 }
 
-__device__ __forceinline__ int length_bucket(int len)
+// Counting-sort bucket of an item of `len` steps: items of at least long_min steps longest first,
+// the rest after them in one bucket, so that (the sort being stable) they keep tile order and
+// each head's tiles run together while its K and V stay in L2. long_min = share / 8: items that
+// matter for the balance of the launch's last round go first.
+__device__ __forceinline__ int length_bucket(int len, int long_min)
 {
-    return kBuckets - 1 - (len < kBuckets - 1 ? len : kBuckets - 1);
+    if (len < long_min) return kBuckets - 1;
+    return kBuckets - 2 - (len < kBuckets - 2 ? len : kBuckets - 2);
 }
+__device__ __forceinline__ int long_item_min(int share) { return share / 8 > 1 ? share / 8 : 1; }
 
 // Reserves n consecutive slots of bucket bk (n = 0: none), returning the first.
 // Lanes of a warp whose tile is whole (n == 1) and shares the bucket take their
@@ -1754,8 +1762,9 @@ struct OrderArgs {
 // Work list for one forward launch, in one launch: every CTA computes the step
 // counts of its 1024 tiles; the CTA that finishes last splits the tiles well above
 // the per-CTA share (partial slots in tile order, within the budget; skipped when
-// even the longest tile is not), then sorts the items longest first (counting sort
-// on item length, clamped) and resets the scheduler counter.
+// even the longest tile is not), then sorts the items (counting sort on item length,
+// clamped: items of at least share / 8 steps longest first, the rest in tile order)
+// and resets the scheduler counter.
 __global__ void __launch_bounds__(1024) tile_order_kernel(TcParams p, OrderArgs o)
 {
     grid_launch_dependents();  // the forward's prologue may start now (it waits for this grid's results)
@@ -1902,7 +1911,7 @@ __global__ void __launch_bounds__(1024) tile_order_kernel(TcParams p, OrderArgs 
         for (int k = 0; k < KB; ++k) {
             const bool valid = s0 + k * 1024 + t < p.n_tiles;
             nb[k] = !valid ? 0 : (sb[k] >= 0 ? n_chunks(Lb[k], T, p.dbg) : 1);
-            bkb[k] = length_bucket(nb[k] > 0 ? (Lb[k] + nb[k] - 1) / nb[k] : 0);
+            bkb[k] = length_bucket(nb[k] > 0 ? (Lb[k] + nb[k] - 1) / nb[k] : 0, long_item_min(T));
         }
     };
     // histogram of item lengths, longest first
@@ -2051,7 +2060,7 @@ __global__ void __launch_bounds__(1024) tile_order_small_kernel(TcParams p, Orde
     for (int k = 0; k < kOrderPerThread; ++k) {
         if (k * 1024 + (t & ~31) >= p.n_tiles) continue;  // no tile in this warp (warp-uniform)
         const bool valid = k * 1024 + t < p.n_tiles;
-        (void)reserve_slots(hist, length_bucket((L[k] + n[k] - 1) / n[k]), valid ? n[k] : 0);
+        (void)reserve_slots(hist, length_bucket((L[k] + n[k] - 1) / n[k], long_item_min(T)), valid ? n[k] : 0);
     }
     clear_order_table(ocnt);
     __syncthreads();
@@ -2063,7 +2072,8 @@ __global__ void __launch_bounds__(1024) tile_order_small_kernel(TcParams p, Orde
         if (k * 1024 >= p.n_tiles) break;  // no tile in this chunk (block-uniform)
         const int tile = k * 1024 + t;
         const bool valid = tile < p.n_tiles;
-        const int pos = place_ordered(hist, length_bucket((L[k] + n[k] - 1) / n[k]), valid ? n[k] : 0, ocnt);
+        const int pos =
+            place_ordered(hist, length_bucket((L[k] + n[k] - 1) / n[k], long_item_min(T)), valid ? n[k] : 0, ocnt);
         if (valid)
             for (int c = 0; c < n[k]; ++c)
                 o.items[pos + c] = tile | (c << kItemTileBits) | ((n[k] - 1) << (kItemTileBits + 3));

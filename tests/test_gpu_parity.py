@@ -180,8 +180,11 @@ def test_many_tiles_multi_cta_ordering(flags):
 
 
 def _expected_work_list(w, mask):
-    """Items (unsplit tiles) longest first, equal lengths in tile order; a tile's length is
-    the sum of its Q blocks' active counts, clamped like the kernel's 1024 length buckets."""
+    """Unsplit tiles in the kernel's order: tiles of at least share / 8 steps longest first
+    (ties in tile order), then the rest in tile order. A tile's length is the sum of its Q
+    blocks' active counts (clamped like the kernel's 1024 length buckets); the share is the
+    total over the resident CTAs of the launch (SMs x CTAs per SM, at most the tiles plus the
+    partial slots), at least 4."""
     counts = mask.reshape(w.B * w.H, w.nQB, w.nKB).sum(axis=2)
     per = 2 if w.block == 64 else 1
     tiles_per_bh = (w.N + 127) // 128
@@ -189,8 +192,17 @@ def _expected_work_list(w, mask):
     for bh in range(w.B * w.H):
         for qt in range(tiles_per_bh):
             lens.append(int(counts[bh, per * qt:per * qt + per].sum()))
-    lens = np.minimum(np.array(lens), 1023)
-    return np.lexsort((np.arange(lens.size), -lens)).astype(np.int32)
+    lens = np.array(lens)
+    n_tiles = lens.size
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    grid = min(n_tiles + min(8 * n_tiles, 640), sms * (2 if w.block == 64 else 1))
+    share = max(-(-int(lens.sum()) // grid), 4)
+    long_min = max(share // 8, 1)
+    tiles = np.arange(n_tiles)
+    is_long = lens >= long_min
+    clamped = np.minimum(lens, 1022)
+    head = tiles[is_long][np.lexsort((tiles[is_long], -clamped[is_long]))]
+    return np.concatenate([head, tiles[~is_long]]).astype(np.int32)
 
 
 ORDER_CASES = {
@@ -203,9 +215,10 @@ ORDER_CASES = {
 
 @pytest.mark.parametrize("name", sorted(ORDER_CASES))
 def test_work_list_is_longest_first_then_tile_order(name):
-    # row a6: the work list is a stable counting sort (length descending, ties in tile
-    # order), which keeps a head's tiles together; single-CTA (CSR) and multi-CTA
-    # (bitmap, or more than 8192 tiles) ordering launches, no splitting
+    # row a6: the work list is a stable counting sort (long tiles by length descending, ties
+    # in tile order, then the rest in tile order), which keeps a head's tiles together;
+    # single-CTA (CSR) and multi-CTA (bitmap, or more than 8192 tiles) ordering launches, no
+    # splitting
     w = ORDER_CASES[name]
     inp = wl.make_inputs(w)
     q, k, v = (gu.upload(inp, n) for n in ("q", "k", "v"))
