@@ -218,43 +218,8 @@ __device__ __forceinline__ void keys_in_range(const uint32_t (&kv)[R][KPL], int 
         }
 }
 
-// The k-th largest key of R rows at once (the radix searches are independent, so
-// their instructions interleave), and how many keys equal to it each row keeps (the
-// lowest columns first). Slots outside the group hold 0. k <= 0 keeps nothing.
-template <int R, int KPL>
-__device__ __forceinline__ void kth_rows(const uint32_t (&x)[R][KPL], const int (&k)[R], uint32_t (&T)[R],
-                                         int (&need)[R])
-{
-#pragma unroll
-    for (int q = 0; q < R; ++q) T[q] = 0;
-    for (int bit = 31; bit >= 0; --bit) {
-        int n[R];
-#pragma unroll
-        for (int q = 0; q < R; ++q) {
-            const uint32_t c = T[q] | (1u << bit);
-            n[q] = 0;
-#pragma unroll
-            for (int m = 0; m < KPL; ++m) n[q] += x[q][m] >= c ? 1 : 0;
-        }
-#pragma unroll
-        for (int q = 0; q < R; ++q)
-            if (static_cast<int>(__reduce_add_sync(0xffffffffu, n[q])) >= k[q]) T[q] |= 1u << bit;
-    }
-#pragma unroll
-    for (int q = 0; q < R; ++q) {
-        int g = 0;
-#pragma unroll
-        for (int m = 0; m < KPL; ++m) g += x[q][m] > T[q] ? 1 : 0;
-        need[q] = k[q] - static_cast<int>(__reduce_add_sync(0xffffffffu, g));
-        if (k[q] <= 0) {
-            T[q] = 0xffffffffu;
-            need[q] = 0;
-        }
-    }
-}
-
-// The k-th largest key of one row (slots outside the group hold 0) by the same
-// bitwise search, narrowed as it goes: it keeps the bounds T (at least k keys are
+// The k-th largest key of one row (slots outside the group hold 0) by a bitwise
+// radix search, narrowed as it goes: it keeps the bounds T (at least k keys are
 // >= T) and U (fewer than k keys are >= U); once at most 32 keys lie in [T, U) they
 // are gathered into one register per lane (through buf, 32 words of this warp's
 // shared memory) and the remaining bits test that register only. Returns T and how
