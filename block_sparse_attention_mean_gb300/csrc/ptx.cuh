@@ -97,18 +97,6 @@ __device__ __forceinline__ void tma_prefetch_map(const CUtensorMap *map)
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
-// 2-D tiled load of one box into shared memory; completion is signalled as
-// transaction bytes on `bar`. x is the innermost (element) coordinate.
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y,
-                                            uint32_t bar)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
-        : "memory");
-}
-
 // 2-D gather of four rows (tile::gather4): rows y0..y3 of the columns [x, x + box
 // width) land one after another at dst (the tensor map's box is one row high). With
 // the 128-byte swizzle each row is swizzled by its position in shared memory, so four
