@@ -11,7 +11,6 @@ import math
 import os
 from typing import Optional, Sequence, Tuple
 
-import numpy as np
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
