@@ -95,7 +95,8 @@ typedef struct {
  * vectors, and each Q block keeps its k = max(1, floor(density * nKB)) best KV
  * blocks ([P1] §5.3: a per-Q-block target count). Exact arithmetic, so results
  * are reproducible bit for bit: pooled sums run over the block's tokens in order
- * in fp32 round-to-nearest, scaled by 1/block; scores are an fmaf chain over
+ * in fp32 round-to-nearest, divided by the block's token count (round to nearest;
+ * a ragged last block holds fewer than `block` tokens); scores are an fmaf chain over
  * channels 0..d-1 starting at +0; ranking is by value descending with -0 == +0 and
  * ties going to the lower block index. A NaN score raises BSA_ERR_NONFINITE on
  * the device (the emitted index is then unspecified).
