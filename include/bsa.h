@@ -197,9 +197,10 @@ bsa_status bsa_build_mask_exact(const void *Q, const void *K, int dt, int B, int
  *   workspace   device, >= bsa_workspace_size(1, ...) bytes, 256-byte aligned
  * The index must be well formed (row_ptr non-decreasing from 0, col_idx strictly
  * ascending in [0, nKB)); bsa_validate_index checks one on the device.
- * bf16 runs as two launches on `stream`: the work list (query tiles longest first,
- * long tiles split by KV range, [P1] §5.3) into the workspace, then the tcgen05
- * kernel. With BSA_INDEX_PLANNED the first is replaced by a one-CTA launch that checks
+ * bf16 runs as two launches on `stream`: the work list (long tiles split by KV range,
+ * [P1] §5.3; items of at least an eighth of the per-CTA share longest first, the rest
+ * in tile order so that a head's tiles run together) into the workspace, then the
+ * tcgen05 kernel. With BSA_INDEX_PLANNED the first is replaced by a one-CTA launch that checks
  * the work list an earlier bsa_forward_plan (or bsa_forward) left in the workspace
  * against this call and resets the scheduler's counters.
  */
