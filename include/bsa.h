@@ -33,7 +33,11 @@
  *     that gave up) are recorded in the first bytes of the call's workspace and are
  *     returned by bsa_check_device_error on that workspace.
  *   - Workspaces are caller-provided device buffers of at least the size
- *     bsa_workspace_size reports; they must be 256-byte aligned.
+ *     bsa_workspace_size reports; they must be 256-byte aligned. A new workspace
+ *     must be zero-filled once before its first call (e.g. cudaMemset): its first
+ *     bytes hold the device status word and the counters of the launches whose
+ *     last CTA finishes the work (the forward's work list, a static pattern), and
+ *     every call leaves them ready for the next one.
  *   - Calls that share a workspace, or write the same outputs, must not overlap
  *     on the GPU (put them on one stream or order them with events).
  */
